@@ -13,7 +13,9 @@ the readings taken here:
 * group e occupies [offsets[e], offsets[e] + counts[e]) and is padded with
   filler rows up to a multiple of ``align``:
   offsets[e+1] = offsets[e] + roundup(counts[e], align);
-* filler rows have src_row = -1.
+* the inverse map src_row holds, for each permuted row, the flattened
+  (token, slot) entry t*k + j it came from (so that both the token and its
+  routing probability can be found from the row); filler rows have -1.
 """
 from __future__ import annotations
 
@@ -43,7 +45,7 @@ def permute_indices(topk_idx, E, align):
         dest[ent] = offsets[e] + np.arange(ent.size)
     row_id_map = dest.reshape(T, k)
     src_row = np.full(int(offsets[-1]), -1, dtype=np.int64)
-    src_row[dest] = np.repeat(np.arange(T), k)
+    src_row[dest] = np.arange(T * k)
     return (row_id_map.astype(np.int32), src_row.astype(np.int32),
             offsets.astype(np.int32), counts.astype(np.int32))
 
@@ -71,7 +73,7 @@ def permute_indices_bruteforce(topk_idx, E, align):
     src_row = [-1] * offsets[-1]
     for t in range(T):
         for j in range(k):
-            src_row[row_id_map[t][j]] = t
+            src_row[row_id_map[t][j]] = t * k + j
     return row_id_map, src_row, offsets, counts
 
 
