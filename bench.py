@@ -1,0 +1,482 @@
+"""Benchmark of the low-precision MoE expert layer (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the whole hot path over one batch: quantisation of the
+grouped weights, the forward (permute + quantise, gate/up grouped GEMM,
+SwiGLU + quantise, down grouped GEMM, unpermute) and, for the training
+workload, the backward (unpermute backward + quantise, dgrad and wgrad of both
+GEMMs, dSwiGLU + quantise, permute backward) and the delayed-scaling update.
+The default workload is the Mixtral-8x7B-shaped layer, forward + backward
+(8 experts, top-2, 16384 tokens, hidden 4096, ffn 14336, hybrid e4m3/e5m2,
+delayed scaling with a 1024-long amax history).
+
+metric: grouped-GEMM TFLOP/s of the step (algorithmic GEMM FLOPs of the
+unpadded rows / step time). The GEMM kernel's own roofline fraction, the
+memory-bound kernels' GB/s, an end-to-end figure through host buffers and the
+CPU oracle on a bounded sample are reported beside it.
+
+--impl reference times the CPU oracle (the only reference implementation of
+this method) on the host cores, on a bounded sample of the same workload.
+Multi-GPU (torchrun): every rank runs its own replica of the layer (the path
+has no exchange step on one node); value = work of all ranks / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+# Fallback peaks of this GPU pool (earlier GB300 measurement) when the measured
+# file is absent; FP8 dense = bf16 x 2 (nominal 4.5 / 2.25 PFLOP/s).
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_OVER_BF16 = 2.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        src = "measured"
+        out = {}
+        for key in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+            v = d.get(key)
+            if isinstance(v, dict):
+                v = v.get("value")
+            out[key] = float(v) if v else FALLBACK[key]
+        return out, src
+    return dict(FALLBACK), "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = f"/tmp/mgq_clocks_{os.getpid()}.csv"
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- the layer step
+
+class Step:
+    """Inputs resident on the device + the layer; one call = one step."""
+
+    def __init__(self, w, dev, time_kernels=False):
+        from fp8_grouped_gemm_gb300 import layer as L
+        from fp8_grouped_gemm_gb300 import workloads as W
+        self.w = w
+        self.dev = dev
+        self.lay = L.ExpertLayer(w, dev)
+        self.train = self.lay.train
+        x = W.make_activations(w)
+        idx, probs = W.make_routing(w)
+        self.x = x.to(dev)
+        self.idx = torch.from_numpy(idx).to(dev)
+        self.probs = torch.from_numpy(probs).to(dev)
+        # weights drawn on the device (same distribution, seeded) to keep start-up short
+        g = torch.Generator(device=dev)
+        g.manual_seed(w.seed * 1000 + 4)
+        self.w1 = (torch.randn(w.E, 2 * w.F, w.H, generator=g, device=dev, dtype=torch.float32) * 0.02).to(
+            torch.bfloat16)
+        self.w2 = (torch.randn(w.E, w.H, w.F, generator=g, device=dev, dtype=torch.float32) * 0.02).to(
+            torch.bfloat16)
+        self.dout = W.make_dout(w).to(dev) if self.train else None
+        self.time_kernels = time_kernels
+        self.events = []
+
+    def _gemm_timed(self, fn):
+        if not self.time_kernels:
+            return fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        self.events.append((a, b))
+
+    def __call__(self):
+        lay = self.lay
+        if not self.time_kernels:
+            lay.quantize_weights(self.w1, self.w2)
+            lay.forward(self.x, self.idx, self.probs)
+            if self.train:
+                lay.backward(self.dout, self.probs)
+                lay.update_scaling()
+            return
+        # same sequence, with events around every launch group
+        ev = {}
+
+        def rec(name, fn):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            ev.setdefault(name, []).append((a, b))
+        from fp8_grouped_gemm_gb300 import mgq
+        w, E, H, F, R = self.w, self.w.E, self.w.H, self.w.F, lay.R_cap
+        mx = lay.scaling == mgq.MX32_E8M0
+        rec("weight_quant", lambda: lay.quantize_weights(self.w1, self.w2))
+        if mx:
+            qx = mgq.qdesc(mgq.E4M3, lay.scaling, lay.xq, lay.xs)
+        else:
+            qx = mgq.qdesc(mgq.E4M3, lay.scaling, lay.xq, None, lay.xcol, None, lay._fs(0), lay._fa(0))
+        rec("permute_quant", lambda: mgq.moe_permute(self.x, self.idx, E, 128, qx, R, lay.row_id_map, lay.src_row,
+                                                     lay.offsets, lay.counts, lay.ws, None))
+        sa = lay.xs if mx else lay._fs(0)
+        sw1 = lay.w1s if mx else lay._fs(2, E)
+        A1 = mgq.operand(lay.xq, sa, H, mgq.E4M3)
+        B1 = mgq.operand(lay.w1q, sw1, H, mgq.E4M3)
+        rec("gemm", lambda: mgq.grouped_gemm_fwd(A1, B1, lay.scaling, lay.offsets, E, R, 2 * F, H, lay.gu))
+        if mx:
+            qh = mgq.qdesc(mgq.E4M3, lay.scaling, lay.hq, lay.hs)
+        else:
+            qh = mgq.qdesc(mgq.E4M3, lay.scaling, lay.hq, None, lay.hcol, None, lay._fs(1), lay._fa(1))
+        rec("swiglu_quant", lambda: mgq.swiglu_quantize(lay.gu, R, F, lay.offsets, E, qh, None))
+        sh = lay.hs if mx else lay._fs(1)
+        sw2 = lay.w2s if mx else lay._fs(2 + E, E)
+        A2 = mgq.operand(lay.hq, sh, F, mgq.E4M3)
+        B2 = mgq.operand(lay.w2q, sw2, F, mgq.E4M3)
+        rec("gemm", lambda: mgq.grouped_gemm_fwd(A2, B2, lay.scaling, lay.offsets, E, R, H, F, lay.y))
+        rec("unpermute", lambda: mgq.moe_unpermute(lay.y, lay.row_id_map, self.probs, lay.out))
+        if self.train:
+            sdy2, sdy1 = lay.bwd_scale[0:1], lay.bwd_scale[1:2]
+            q2 = mgq.qdesc(mgq.E5M2, mgq.TENSOR_F32, lay.dy2q, None, lay.dy2col, None, sdy2, lay.bwd_amax[0:1])
+            rec("unpermute_bwd_quant", lambda: mgq.moe_unpermute_bwd(self.dout, lay.y, lay.row_id_map, lay.src_row,
+                                                                     self.probs, R, lay.offsets, E, q2, lay.dprobs))
+            o = [mgq.operand(lay.dy2q, sdy2, H, mgq.E5M2), mgq.operand(lay.w2col, lay._fs(2 + E, E), H, mgq.E4M3),
+                 mgq.operand(lay.dy2col, sdy2, R, mgq.E5M2), mgq.operand(lay.hcol, lay._fs(1), R, mgq.E4M3)]
+            rec("gemm", lambda: mgq.grouped_gemm_dgrad(o[0], o[1], mgq.TENSOR_F32, lay.offsets, E, R, H, F, lay.dh))
+            rec("gemm", lambda: mgq.grouped_gemm_wgrad(o[2], o[3], mgq.TENSOR_F32, lay.offsets, E, R, H, F, lay.dw2))
+            q1 = mgq.qdesc(mgq.E5M2, mgq.TENSOR_F32, lay.dy1q, None, lay.dy1col, None, sdy1, lay.bwd_amax[1:2])
+            rec("dswiglu_quant", lambda: mgq.dswiglu_quantize(lay.dh, lay.gu, R, F, lay.offsets, E, q1, None))
+            p = [mgq.operand(lay.dy1q, sdy1, 2 * F, mgq.E5M2), mgq.operand(lay.w1col, lay._fs(2, E), 2 * F, mgq.E4M3),
+                 mgq.operand(lay.dy1col, sdy1, R, mgq.E5M2), mgq.operand(lay.xcol, lay._fs(0), R, mgq.E4M3)]
+            rec("gemm", lambda: mgq.grouped_gemm_dgrad(p[0], p[1], mgq.TENSOR_F32, lay.offsets, E, R, 2 * F, H,
+                                                       lay.dxp))
+            rec("gemm", lambda: mgq.grouped_gemm_wgrad(p[2], p[3], mgq.TENSOR_F32, lay.offsets, E, R, 2 * F, H,
+                                                       lay.dw1))
+            rec("permute_bwd", lambda: mgq.moe_permute_bwd(lay.dxp, lay.row_id_map, lay.dx))
+            rec("scaling_update", lambda: lay.update_scaling())
+        self.events.append(ev)
+
+
+def algorithmic_bytes(w, R_pad):
+    """Compulsory HBM bytes of the memory-bound steps (each input read once,
+    each output written once; a row quantised once per token is written k
+    times)."""
+    T, k, H, F, E = w.T, w.k, w.H, w.F, w.E
+    R = T * k
+    b = {}
+    b["permute_quant"] = T * H * 2 + R * H * 1 + (R * H * 1 if w.backward else 0)   # + col copy (transpose)
+    b["swiglu_quant"] = R * 2 * F * 2 + R * F * 1 + (2 * R * F if w.backward else 0)
+    b["unpermute"] = R * H * 2 + T * H * 2
+    b["weight_quant"] = E * 3 * F * H * (2 + 1) + (E * 3 * F * H * 2 if w.backward else 0)
+    if w.backward:
+        b["unpermute_bwd_quant"] = T * H * 2 + R * H * 2 + R * H * 1 + 2 * R * H
+        b["dswiglu_quant"] = R * F * 2 + R * 2 * F * 2 + R * 2 * F * 1 + 2 * R * 2 * F
+        b["permute_bwd"] = R * H * 2 + T * H * 2
+    return b
+
+
+# ----------------------------------------------------------------------------- CPU oracle sample
+
+def oracle_sample(w, rows=512, f_slice=1024):
+    """Times the CPU oracle on a bounded sample of the workload: one expert,
+    `rows` routed rows, the full hidden size, an `f_slice`-wide slice of the
+    FFN; the same chain of steps as the GPU step. Returns (seconds, GEMM FLOPs
+    of the sample)."""
+    from oracle import gemm as OG
+    from oracle import layer as OL
+    from oracle import quant as OQ
+    from oracle import routing as OR
+    rng = np.random.default_rng(w.seed)
+    H, Fs = w.H, f_slice
+    x = rng.standard_normal((rows, H))
+    if w.outlier_frac:
+        x[:, :max(1, int(round(w.outlier_frac * H)))] *= w.outlier_mult
+    from oracle.formats import round_to_bf16
+    x = round_to_bf16(x)
+    w1 = round_to_bf16(rng.standard_normal((1, 2 * Fs, H)) * 0.02)
+    w2 = round_to_bf16(rng.standard_normal((1, H, Fs)) * 0.02)
+    dout = round_to_bf16(rng.standard_normal((rows, H)) * w.dout_std)
+    off = np.array([0, rows])
+    idx = np.zeros((rows, 1), dtype=np.int32)
+    probs = np.ones((rows, 1), dtype=np.float32)
+    t0 = time.perf_counter()
+    rim, src, o2, cnt = OR.permute_indices(idx, 1, 128)
+    if w.recipe == "mxfp8":
+        cx, sx = OQ.quantize_mx(x)
+        c1, s1 = OQ.quantize_mx(w1[0])
+        c2, s2 = OQ.quantize_mx(w2[0])
+        gu = OG.grouped_gemm_fwd(OQ.dequantize_mx(cx, sx), OQ.dequantize_mx(c1, s1)[None], off)
+        h = round_to_bf16(OL.swiglu(round_to_bf16(gu), Fs))
+        ch, sh = OQ.quantize_mx(h)
+        y = OG.grouped_gemm_fwd(OQ.dequantize_mx(ch, sh), OQ.dequantize_mx(c2, s2)[None], off)
+        OR.unpermute(round_to_bf16(y), rim, probs)
+        flops = 2.0 * rows * H * 2 * Fs + 2.0 * rows * Fs * H
+    else:
+        s = np.float32(1.0)
+        cx, _ = OQ.quantize_tensor(x, s)
+        c1, _ = OQ.quantize_tensor(w1[0], s)
+        c2, _ = OQ.quantize_tensor(w2[0], s)
+        xd, w1d, w2d = OQ.dequantize_tensor(cx, s), OQ.dequantize_tensor(c1, s)[None], OQ.dequantize_tensor(c2, s)[None]
+        gu = round_to_bf16(OG.grouped_gemm_fwd(xd, w1d, off))
+        h = round_to_bf16(OL.swiglu(gu, Fs))
+        ch, _ = OQ.quantize_tensor(h, s)
+        hd = OQ.dequantize_tensor(ch, s)
+        y = round_to_bf16(OG.grouped_gemm_fwd(hd, w2d, off))
+        OR.unpermute(y, rim, probs)
+        dy32, _ = OR.unpermute_bwd(dout, y, rim, probs, rows)
+        cdy, _ = OQ.quantize_tensor(dy32.astype(np.float64), s, "e5m2")
+        dyd = OQ.dequantize_tensor(cdy, s, "e5m2")
+        dh = round_to_bf16(OG.grouped_gemm_dgrad(dyd, w2d, off))
+        OG.grouped_gemm_wgrad(dyd, hd, off, 1)
+        dgu = round_to_bf16(OL.dswiglu(dh, gu, Fs))
+        cd1, _ = OQ.quantize_tensor(dgu, s, "e5m2")
+        d1 = OQ.dequantize_tensor(cd1, s, "e5m2")
+        dxp = round_to_bf16(OG.grouped_gemm_dgrad(d1, w1d, off))
+        OG.grouped_gemm_wgrad(d1, xd, off, 1)
+        OR.permute_bwd(dxp, rim)
+        flops = 3 * (2.0 * rows * H * 2 * Fs + 2.0 * rows * Fs * H)
+    return time.perf_counter() - t0, flops
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------- main
+
+def run_reference(args, w, rank, world):
+    """The CPU oracle, timed on the host cores, one bounded sample per step."""
+    if rank != 0:
+        return
+    ncores = cpu_threads()
+    for _ in range(args.warmup):
+        oracle_sample(w, rows=128, f_slice=256)
+    times, flops = [], 0.0
+    for _ in range(args.steps):
+        dt, flops = oracle_sample(w)
+        times.append(dt)
+    tot = sum(times)
+    value = flops * args.steps / tot / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE[w.recipe],
+        "data": "synthetic", "config": config_of(w, args),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": ncores, "kind": "oracle",
+                         "sample": SAMPLE_DESC},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+METRIC = "grouped FP8 GEMM fwd+bwd TFLOP/s (Mixtral-shaped expert layer step)"
+DTYPE = {"mxfp8": "e4m3 (MXFP8, f32 accumulate)", "delayed": "e4m3/e5m2 (per-tensor delayed, f32 accumulate)"}
+SAMPLE_DESC = ("CPU oracle (numpy, float64 GEMMs) on one expert, 512 routed rows, full hidden size, "
+               "a 1024-wide FFN slice; same step chain; TFLOP/s = sample GEMM FLOPs / wall time")
+
+
+def config_of(w, args):
+    return {"workload": f"{w.name}: E={w.E} top-{w.k} T={w.T} H={w.H} F={w.F} SwiGLU, recipe={w.recipe}"
+                        + (", fwd+bwd" if w.backward else ", fwd"),
+            "experts": w.E, "topk": w.k, "tokens": w.T, "hidden": w.H, "ffn": w.F,
+            "parallelism": f"replicas x{args.gpus}",
+            "l2": "inputs larger than L2 (bf16 weights 2.8 GB resident, re-quantised every step)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="mixtral_fwdbwd")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    from fp8_grouped_gemm_gb300.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+    import torch.distributed as dist
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    from fp8_grouped_gemm_gb300 import mgq
+    mgq.load()
+    step = Step(w, dev)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    barrier()
+    clocks.start()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        step()
+    t1.record()
+    barrier()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    ms_step = ms / args.steps
+    flops = w.gemm_flops()
+    value = flops * world / (ms_step * 1e-3) / 1e12
+    launches = step.lay.gpu_launches_per_step() * args.steps
+
+    # per-kernel timing: the same steps with events around every launch
+    kstep = Step.__new__(Step)
+    kstep.__dict__.update(step.__dict__)
+    kstep.time_kernels = True
+    kstep.events = []
+    for _ in range(args.steps):
+        kstep()
+    torch.cuda.synchronize()
+    per = {}
+    for ev in kstep.events:
+        for name, pairs in ev.items():
+            per.setdefault(name, 0.0)
+            per[name] += sum(a.elapsed_time(b) for a, b in pairs)
+    per = {k: v / args.steps for k, v in per.items()}          # ms per step
+    pk, pk_src = peaks()
+    gemm_ms = per.get("gemm", float("nan"))
+    achieved = flops / (gemm_ms * 1e-3) / 1e12
+    peak_fp8 = pk["bf16_tflops_sustained"] * FP8_OVER_BF16
+    R_pad = int(step.lay.offsets[-1].item())
+    ab = algorithmic_bytes(w, R_pad)
+    hbm = {k: {"ms": per[k], "GB/s": ab[k] / (per[k] * 1e-3) / 1e9,
+               "frac": ab[k] / (per[k] * 1e-3) / 1e9 / pk["hbm_gbs"]} for k in ab if k in per}
+    roofline = {"bound": "tensor", "kernel": "grouped_gemm_kernel (all grouped GEMM launches of the step)",
+                "achieved": achieved, "peak": peak_fp8, "unit": "TFLOP/s", "frac": achieved / peak_fp8,
+                "traffic": None,
+                "peak_source": f"{pk_src}: bf16 sustained {pk['bf16_tflops_sustained']} TFLOP/s x 2 (fp8/bf16 nominal)",
+                "gemm_ms_per_step": gemm_ms}
+
+    # end to end through host buffers: H2D of the step's inputs, D2H of dX (or the output)
+    e2e = None
+    if not args.no_e2e:
+        lay = step.lay
+        hx = step.x.cpu().pin_memory()
+        hidx = step.idx.cpu().pin_memory()
+        hp = step.probs.cpu().pin_memory()
+        hd = step.dout.cpu().pin_memory() if step.train else None
+        res_dev = lay.dx if step.train else lay.out
+        hres = torch.empty(res_dev.shape, dtype=res_dev.dtype, pin_memory=True)
+        h2d = hx.numel() * 2 + hidx.numel() * 4 + hp.numel() * 4 + (hd.numel() * 2 if hd is not None else 0)
+        d2h = hres.numel() * 2
+
+        def e2e_step():
+            step.x.copy_(hx, non_blocking=True)
+            step.idx.copy_(hidx, non_blocking=True)
+            step.probs.copy_(hp, non_blocking=True)
+            if hd is not None:
+                step.dout.copy_(hd, non_blocking=True)
+            step()
+            hres.copy_(res_dev, non_blocking=True)
+        e2e_step()
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            e2e_step()
+        b.record()
+        barrier()
+        ems = a.elapsed_time(b) / args.steps
+        e2e = {"value": flops * world / (ems * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ems}
+    assert mgq.get_error() == mgq.OK
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        dt, f = oracle_sample(w)
+        cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+               "sample": SAMPLE_DESC, "seconds": dt}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": DTYPE[w.recipe], "data": "synthetic (seeded; shapes of the workload)",
+            "config": config_of(w, args), "roofline": roofline, "hbm_kernels": hbm,
+            "kernel_ms_per_step": per, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

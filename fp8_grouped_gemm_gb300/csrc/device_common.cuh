@@ -1,0 +1,132 @@
+// Device-side helpers shared by the kernels of libmgq: bf16 access, the
+// saturating round-to-nearest casts to the 8- and 4-bit formats, the E8M0
+// block-scale exponent, and the device error word.
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "mgq.h"
+
+namespace mgq {
+
+// ---------------------------------------------------------------------------
+// error word (one per device, see abi.cu); kernels receive its address.
+
+__device__ __forceinline__ void report(int* err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+// ---------------------------------------------------------------------------
+// bf16
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);   // .x = lo, .y = hi
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float round_bf16(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// ---------------------------------------------------------------------------
+// Saturating round-to-nearest-even casts (PTX cvt .rn.satfinite). The first
+// source operand of the x2 forms lands in the upper half of the result.
+
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t cvt_e5m2x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// four values -> four codes in one word, element 0 in the low byte
+template <int DT>
+__device__ __forceinline__ uint32_t cvt_fp8x4(float a, float b, float c, float d) {
+  if (DT == MGQ_E4M3) return cvt_e4m3x2(a, b) | (cvt_e4m3x2(c, d) << 16);
+  return cvt_e5m2x2(a, b) | (cvt_e5m2x2(c, d) << 16);
+}
+// eight e2m1 values -> one word, element 2i in the low nibble of byte i
+__device__ __forceinline__ uint32_t cvt_e2m1x8(const float* v) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return r;
+}
+// one non-negative value -> ue4m3 code (e4m3 with the sign bit clear)
+__device__ __forceinline__ uint32_t cvt_ue4m3(float x) { return cvt_e4m3x2(x, 0.0f) & 0xFFu; }
+__device__ __forceinline__ float ue4m3_value(uint32_t code) {
+  // exact decode: exponent field e (bias 7), mantissa m (3 bits)
+  uint32_t e = (code >> 3) & 0xF, m = code & 7;
+  if (e == 0) return (float)m * 0.001953125f;             // m * 2^-9
+  return __uint_as_float(((e + 120u) << 23) | (m << 20));  // 2^(e-7) * (1 + m/8)
+}
+
+template <int DT> struct FmtInfo;
+template <> struct FmtInfo<MGQ_E4M3> { static constexpr float fmax = 448.0f;   static constexpr int emax = 8; };
+template <> struct FmtInfo<MGQ_E5M2> { static constexpr float fmax = 57344.0f; static constexpr int emax = 15; };
+
+// ---------------------------------------------------------------------------
+// E8M0 block-scale exponent from the float32 bits of a non-negative amax.
+// rceil: smallest e with amax <= fmax * 2^e (fmax = 1.75 * 2^emax), i.e.
+// floor(log2 amax) - emax, plus one when the significand exceeds 1.75.
+// floor: floor(log2 amax) - emax. amax == 0 -> -127. Clamped to [-127, 127].
+// Returns 128 for a NaN / infinite amax (scale code 0xFF).
+__device__ __forceinline__ int mx_exponent(uint32_t amax_bits, int emax, bool rceil) {
+  if (amax_bits >= 0x7F800000u) return 128;
+  if (amax_bits == 0) return -127;
+  int eb = (int)(amax_bits >> 23);
+  uint32_t m = amax_bits & 0x7FFFFFu;
+  int p;
+  if (eb == 0) {                       // subnormal amax: normalise
+    int lz = __clz(m) - 8;
+    m = (m << lz) & 0x7FFFFFu;
+    p = -126 - lz;
+  } else {
+    p = eb - 127;
+  }
+  int e = p - emax + ((rceil && m > 0x600000u) ? 1 : 0);
+  return max(-127, min(127, e));
+}
+// 2^-e as a float32 multiplier (NaN for the NaN/inf marker)
+__device__ __forceinline__ float mx_multiplier(int e) {
+  if (e == 128) return __uint_as_float(0x7FC00000u);
+  int b = 127 - e;                     // e in [-127, 126] -> normal float
+  if (b >= 1) return __uint_as_float((uint32_t)b << 23);
+  return 0x1p-127f;                    // e == 127 (unreachable for finite fp8 inputs)
+}
+__device__ __forceinline__ uint32_t mx_scale_code(int e) { return e == 128 ? 255u : (uint32_t)(e + 127); }
+
+// Byte offset of the block scale of (row r, block b) in the 128x4-tiled
+// layout, for a matrix whose row pitch holds `kblocks4` groups of 4 blocks.
+__device__ __forceinline__ int64_t tiled_scale_offset(int64_t r, int64_t b, int64_t kblocks4) {
+  return ((r >> 7) * kblocks4 + (b >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (b & 3);
+}
+
+// |x| maximum of packed bf16 pairs as integers: NaN > inf > finite values
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t acc, uint32_t w) {
+  return __vmaxu2(acc, w & 0x7FFF7FFFu);
+}
+__device__ __forceinline__ uint32_t fold_bf16x2(uint32_t w) {   // max of the halves, as float bits
+  uint32_t a = w & 0xFFFFu, b = w >> 16;
+  return (a > b ? a : b) << 16;
+}
+
+__device__ __forceinline__ void atomic_max_nonneg(float* p, float v) {
+  // valid for non-negative floats (and +NaN, which then sticks)
+  atomicMax(reinterpret_cast<unsigned int*>(p), __float_as_uint(v));
+}
+
+}  // namespace mgq

@@ -1,0 +1,479 @@
+// HBM-bound steps of the routed-expert layer, each fused with the
+// quantisation of its output: SwiGLU (+ its derivative), unpermute / combine
+// and its backward, permute backward, block quantisation of grouped weights,
+// and the delayed-scaling amax history.
+//
+// Sources: the SwiGLU experts of the Mixtral / Llama4 layers ("[BUG] Loss
+// difference when training with FP8 vs. BF16 MoE", Megatron-LM issue #1152;
+// "float8 moe training conversion API prototype", pytorch/ao PR #2275, testing:
+// outputs, input gradients and parameter gradients); row-wise and column-wise
+// copies with their own scales ("Numerical fix for moe single grouped weight
+// with fp8 fp4 primary weight and grad norm spikes", Megatron-LM PR #5487;
+// "FP8BlockQuantizer not work on TE", TransformerEngine issue #2393, transpose
+// identity); delayed scaling with a 1024-long history and max (issue #1152,
+// repro steps).
+#include "mgq_internal.h"
+#include "rowquant.cuh"
+
+namespace mgq {
+namespace {
+
+constexpr int kWarps = 8;
+
+// ---- SwiGLU + quantise: warp per row ----------------------------------------
+struct SwigluArgs {
+  const uint16_t* gu;   // [R_cap, 2F]
+  const int32_t* rows_used;
+  int64_t R_cap;
+  int F;
+  uint8_t* codes;       // [R_cap, F]
+  uint8_t* scales;
+  uint16_t* h_out;      // [R_cap, F] or null
+  const float* tensor_scale;
+  float* amax_out;
+  int rceil;
+};
+
+__device__ __forceinline__ float silu_f(float g) { return __fdiv_rn(g, 1.0f + expf(-g)); }
+
+template <int SC, int DT>
+__global__ void __launch_bounds__(256) swiglu_quant_kernel(SwigluArgs a) {
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * kWarps + warp;
+  if (r >= *a.rows_used) return;
+  const int F = a.F;
+  const float ts = (SC == MGQ_TENSOR_F32) ? a.tensor_scale[0] : 1.0f;
+  uint32_t tam = 0;
+  for (int c0 = 0; c0 < F; c0 += 1024) {
+    const int c = c0 + 32 * lane;
+    const bool act = c < F;
+    float h[32];
+    if (act) {
+      float g[32], u[32];
+      load_bf16x32(a.gu + r * 2 * F + c, g);
+      load_bf16x32(a.gu + r * 2 * F + F + c, u);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) h[i] = round_bf16(__fmul_rn(silu_f(g[i]), u[i]));
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) h[i] = 0.0f;
+    }
+    const uint32_t am = absmax_bits_f32(h, 32);
+    tam = max(tam, am);
+    Block32 o;
+    quantize32<SC, DT>(h, am, ts, a.rceil != 0, o);
+    if (act) {
+      store32<SC>(o, a.codes, a.scales, r, c, F, a.R_cap, lane);
+      if (a.h_out) store_bf16x32(a.h_out + r * F + c, h);
+    }
+  }
+  if (SC == MGQ_TENSOR_F32 && a.amax_out) {
+    tam = warp_max_u32(tam);
+    if (lane == 0) atomic_max_nonneg(a.amax_out, __uint_as_float(tam));
+  }
+}
+
+// ---- dSwiGLU + quantise: warp per row ---------------------------------------
+struct DswigluArgs {
+  const uint16_t* dh;   // [R_cap, F]
+  const uint16_t* gu;   // [R_cap, 2F]
+  const int32_t* rows_used;
+  int64_t R_cap;
+  int F;
+  uint8_t* codes;       // [R_cap, 2F]
+  uint8_t* scales;
+  uint16_t* dgu_out;    // [R_cap, 2F] or null
+  const float* tensor_scale;
+  float* amax_out;
+  int rceil;
+};
+
+template <int SC, int DT>
+__global__ void __launch_bounds__(256) dswiglu_quant_kernel(DswigluArgs a) {
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * kWarps + warp;
+  if (r >= *a.rows_used) return;
+  const int F = a.F;
+  const float ts = (SC == MGQ_TENSOR_F32) ? a.tensor_scale[0] : 1.0f;
+  uint32_t tam = 0;
+  for (int c0 = 0; c0 < F; c0 += 1024) {
+    const int c = c0 + 32 * lane;
+    const bool act = c < F;
+    float dg[32], du[32];
+    if (act) {
+      float d[32], g[32], u[32];
+      load_bf16x32(a.dh + r * F + c, d);
+      load_bf16x32(a.gu + r * 2 * F + c, g);
+      load_bf16x32(a.gu + r * 2 * F + F + c, u);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float s = __fdiv_rn(1.0f, 1.0f + expf(-g[i]));
+        dg[i] = round_bf16(d[i] * u[i] * s * (1.0f + g[i] * (1.0f - s)));
+        du[i] = round_bf16(d[i] * g[i] * s);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) dg[i] = du[i] = 0.0f;
+    }
+    const uint32_t amg = absmax_bits_f32(dg, 32), amu = absmax_bits_f32(du, 32);
+    tam = max(tam, max(amg, amu));
+    Block32 og, ou;
+    quantize32<SC, DT>(dg, amg, ts, a.rceil != 0, og);
+    quantize32<SC, DT>(du, amu, ts, a.rceil != 0, ou);
+    if (act) {
+      store32<SC>(og, a.codes, a.scales, r, c, 2 * F, a.R_cap, lane);
+      store32<SC>(ou, a.codes, a.scales, r, F + c, 2 * F, a.R_cap, lane);
+      if (a.dgu_out) {
+        store_bf16x32(a.dgu_out + r * 2 * F + c, dg);
+        store_bf16x32(a.dgu_out + r * 2 * F + F + c, du);
+      }
+    }
+  }
+  if (SC == MGQ_TENSOR_F32 && a.amax_out) {
+    tam = warp_max_u32(tam);
+    if (lane == 0) atomic_max_nonneg(a.amax_out, __uint_as_float(tam));
+  }
+}
+
+// ---- combine: out[t] = sum_j w_j * y[row(t, j)] (w = probs, or 1) -----------
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ rim,
+                                                      const float* __restrict__ probs, int T, int k, int H,
+                                                      uint16_t* __restrict__ out) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarps + warp;
+  if (t >= T) return;
+  int rows[8];
+  float w[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    rows[j] = j < k ? rim[(int64_t)t * k + j] : -1;
+    w[j] = (j < k && probs) ? probs[(int64_t)t * k + j] : 1.0f;
+  }
+  for (int c = lane * 8; c < H; c += 256) {
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j >= k) break;
+      if (rows[j] < 0) continue;
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(y + (int64_t)rows[j] * H + c));
+      acc[0] = fmaf(w[j], bf16_lo(v.x), acc[0]); acc[1] = fmaf(w[j], bf16_hi(v.x), acc[1]);
+      acc[2] = fmaf(w[j], bf16_lo(v.y), acc[2]); acc[3] = fmaf(w[j], bf16_hi(v.y), acc[3]);
+      acc[4] = fmaf(w[j], bf16_lo(v.z), acc[4]); acc[5] = fmaf(w[j], bf16_hi(v.z), acc[5]);
+      acc[6] = fmaf(w[j], bf16_lo(v.w), acc[6]); acc[7] = fmaf(w[j], bf16_hi(v.w), acc[7]);
+    }
+    *reinterpret_cast<uint4*>(out + (int64_t)t * H + c) =
+        make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                   pack_bf16x2(acc[6], acc[7]));
+  }
+}
+
+// ---- unpermute backward + quantise of dY, and dprobs ------------------------
+struct UnpermBwdArgs {
+  const uint16_t* dout;  // [T, H]
+  const uint16_t* y;     // [R_cap, H]
+  const int32_t* rim;
+  const int32_t* src_row;
+  const float* probs;
+  const int32_t* offsets;
+  int T, k, H, E;
+  int64_t R_cap;
+  uint8_t* codes;        // [R_cap, H]
+  uint8_t* scales;
+  const float* tensor_scale;
+  float* amax_out;
+  float* dprobs;
+  int rceil;
+  int token_blocks;
+};
+
+template <int SC, int DT>
+__global__ void __launch_bounds__(256) unpermute_bwd_kernel(UnpermBwdArgs a) {
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31;
+  const int H = a.H;
+  if ((int)blockIdx.x >= a.token_blocks) {
+    // filler rows of expert e: zero codes and scales
+    const int e = blockIdx.x - a.token_blocks;
+    if (e >= a.E) return;
+    for (int64_t r = a.offsets[e] + warp; r < a.offsets[e + 1]; r += kWarps) {
+      if (a.src_row[r] >= 0) continue;
+      for (int c = lane * 16; c < H; c += 512) *reinterpret_cast<uint4*>(a.codes + r * H + c) = make_uint4(0, 0, 0, 0);
+      if (SC == MGQ_MX32_E8M0)
+        for (int b4 = lane; b4 < H / 128; b4 += 32)
+          *reinterpret_cast<uint32_t*>(a.scales + tiled_scale_offset(r, (int64_t)b4 * 4, H / 128)) = 0u;
+    }
+    return;
+  }
+  const int t = blockIdx.x * kWarps + warp;
+  if (t >= a.T) return;
+  const float ts = (SC == MGQ_TENSOR_F32) ? a.tensor_scale[0] : 1.0f;
+  int rows[8];
+  float pr[8], dp[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    rows[j] = j < a.k ? a.rim[(int64_t)t * a.k + j] : -1;
+    pr[j] = j < a.k ? a.probs[(int64_t)t * a.k + j] : 0.0f;
+    dp[j] = 0.0f;
+  }
+  uint32_t tam = 0;
+  for (int c0 = 0; c0 < H; c0 += 1024) {
+    const int c = c0 + 32 * lane;
+    const bool act = c < H;
+    float d[32];
+    if (act) {
+      load_bf16x32(a.dout + (int64_t)t * H + c, d);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) d[i] = 0.0f;
+    }
+#pragma unroll 1
+    for (int j = 0; j < a.k; ++j) {
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(pr[j], d[i]);
+      const uint32_t am = absmax_bits_f32(v, 32);
+      tam = max(tam, am);
+      Block32 o;
+      quantize32<SC, DT>(v, am, ts, a.rceil != 0, o);
+      if (act && rows[j] >= 0) {
+        store32<SC>(o, a.codes, a.scales, rows[j], c, H, a.R_cap, lane);
+        float yv[32];
+        load_bf16x32(a.y + (int64_t)rows[j] * H + c, yv);
+        float s = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s = fmaf(d[i], yv[i], s);
+        dp[j] += s;
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j >= a.k) break;
+    float s = dp[j];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+    if (lane == 0) a.dprobs[(int64_t)t * a.k + j] = s;
+  }
+  if (SC == MGQ_TENSOR_F32 && a.amax_out) {
+    tam = warp_max_u32(tam);
+    if (lane == 0) atomic_max_nonneg(a.amax_out, __uint_as_float(tam));
+  }
+}
+
+// ---- row-wise quantisation of [G*M, K] (grouped weights) ---------------------
+struct QuantRowsArgs {
+  const uint16_t* x;
+  int64_t rows, M, K;
+  uint8_t* codes;
+  uint8_t* scales;
+  const float* tensor_scale;   // per group
+  float* amax_out;             // per group
+  int rceil;
+};
+
+template <int SC, int DT>
+__global__ void __launch_bounds__(256) quant_rows_kernel(QuantRowsArgs a) {
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * kWarps + warp;
+  if (r >= a.rows) return;
+  const int64_t g = r / a.M;
+  const float ts = (SC == MGQ_TENSOR_F32) ? a.tensor_scale[g] : 1.0f;
+  uint32_t tam = 0;
+  for (int64_t c0 = 0; c0 < a.K; c0 += 1024) {
+    const int64_t c = c0 + 32 * lane;
+    const bool act = c < a.K;
+    float v[32];
+    if (act) {
+      load_bf16x32(a.x + r * a.K + c, v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+    }
+    const uint32_t am = absmax_bits_f32(v, 32);
+    tam = max(tam, am);
+    Block32 o;
+    quantize32<SC, DT>(v, am, ts, a.rceil != 0, o);
+    if (act) store32<SC>(o, a.codes, a.scales, r, c, a.K, a.rows, lane);
+  }
+  if (SC == MGQ_TENSOR_F32 && a.amax_out) {
+    tam = warp_max_u32(tam);
+    if (lane == 0) atomic_max_nonneg(a.amax_out + g, __uint_as_float(tam));
+  }
+}
+
+// ---- delayed scaling ------------------------------------------------------------
+__global__ void amax_history_kernel(float* hist, int32_t* head, float* amax, float* scale, int n, int L, float fmax) {
+  const int h = *head;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    float* ring = hist + (int64_t)i * L;
+    ring[h] = amax[i];
+    float m = 0.0f;
+    for (int j = 0; j < L; ++j) m = fmaxf(m, ring[j]);
+    if (m > 0.0f && isfinite(m)) scale[i] = __fdiv_rn(fmax, m);
+    amax[i] = 0.0f;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) *head = (h + 1) % L;
+}
+
+bool dtype_ok(int dt) { return dt == MGQ_E4M3 || dt == MGQ_E5M2; }
+
+int check_q(const mgq_qdesc* q) {
+  if (!q || !q->row.data || !aligned16(q->row.data)) return MGQ_ERR_INVALID_ARG;
+  if (!dtype_ok(q->dtype)) return MGQ_ERR_UNSUPPORTED;
+  if (q->scaling == MGQ_MX32_E8M0 || q->scaling == MGQ_BLK_1x128_F32) {
+    if (!q->row.scale || !aligned16(q->row.scale)) return MGQ_ERR_INVALID_ARG;
+  } else if (q->scaling == MGQ_TENSOR_F32) {
+    if (!q->tensor_scale) return MGQ_ERR_INVALID_ARG;
+  } else {
+    return MGQ_ERR_UNSUPPORTED;
+  }
+  if (q->col.data && (q->scaling != MGQ_TENSOR_F32 || !aligned16(q->col.data))) return MGQ_ERR_UNSUPPORTED;
+  return MGQ_OK;
+}
+
+}  // namespace
+}  // namespace mgq
+
+using namespace mgq;
+
+#define MGQ_DISPATCH_Q(q, KERNEL, GRID, ARGS)                                                         \
+  do {                                                                                               \
+    const int sc_ = (q)->scaling, dt_ = (q)->dtype;                                                  \
+    if (sc_ == MGQ_MX32_E8M0 && dt_ == MGQ_E4M3) KERNEL<MGQ_MX32_E8M0, MGQ_E4M3><<<GRID, 256, 0, s>>>(ARGS); \
+    else if (sc_ == MGQ_MX32_E8M0 && dt_ == MGQ_E5M2) KERNEL<MGQ_MX32_E8M0, MGQ_E5M2><<<GRID, 256, 0, s>>>(ARGS); \
+    else if (sc_ == MGQ_BLK_1x128_F32 && dt_ == MGQ_E4M3) KERNEL<MGQ_BLK_1x128_F32, MGQ_E4M3><<<GRID, 256, 0, s>>>(ARGS); \
+    else if (sc_ == MGQ_BLK_1x128_F32 && dt_ == MGQ_E5M2) KERNEL<MGQ_BLK_1x128_F32, MGQ_E5M2><<<GRID, 256, 0, s>>>(ARGS); \
+    else if (sc_ == MGQ_TENSOR_F32 && dt_ == MGQ_E4M3) KERNEL<MGQ_TENSOR_F32, MGQ_E4M3><<<GRID, 256, 0, s>>>(ARGS); \
+    else if (sc_ == MGQ_TENSOR_F32 && dt_ == MGQ_E5M2) KERNEL<MGQ_TENSOR_F32, MGQ_E5M2><<<GRID, 256, 0, s>>>(ARGS); \
+    else return MGQ_ERR_UNSUPPORTED;                                                                  \
+    MGQ_LAUNCH_CHECK();                                                                              \
+  } while (0)
+
+extern "C" {
+
+int mgq_swiglu_quantize(const void* gu_bf16, int64_t R_cap, int F, const int32_t* offsets, int E,
+                        const mgq_qdesc* q, void* h_bf16, void* stream) {
+  int rc = check_q(q);
+  if (rc != MGQ_OK) return rc;
+  MGQ_CHECK_ARG(gu_bf16 && aligned16(gu_bf16) && aligned16(h_bf16) && offsets && E >= 1);
+  MGQ_CHECK_ARG(F > 0 && F % 128 == 0 && R_cap > 0 && R_cap % 128 == 0);
+  cudaStream_t s = as_stream(stream);
+  SwigluArgs a{static_cast<const uint16_t*>(gu_bf16), offsets + E, R_cap, F,
+               static_cast<uint8_t*>(q->row.data), static_cast<uint8_t*>(q->row.scale),
+               static_cast<uint16_t*>(h_bf16), q->tensor_scale, q->amax_out, q->e8m0_mode == MGQ_E8M0_RCEIL};
+  const unsigned grid = (unsigned)((R_cap + kWarps - 1) / kWarps);
+  MGQ_DISPATCH_Q(q, swiglu_quant_kernel, grid, a);
+  if (q->col.data)
+    return launch_transpose_u8(static_cast<const uint8_t*>(q->row.data), F, static_cast<uint8_t*>(q->col.data),
+                               R_cap, offsets + E, R_cap, F, s);
+  return MGQ_OK;
+}
+
+int mgq_dswiglu_quantize(const void* dh_bf16, const void* gu_bf16, int64_t R_cap, int F, const int32_t* offsets,
+                         int E, const mgq_qdesc* q, void* dgu_bf16, void* stream) {
+  int rc = check_q(q);
+  if (rc != MGQ_OK) return rc;
+  MGQ_CHECK_ARG(dh_bf16 && gu_bf16 && aligned16(dh_bf16) && aligned16(gu_bf16) && aligned16(dgu_bf16));
+  MGQ_CHECK_ARG(offsets && E >= 1 && F > 0 && F % 128 == 0 && R_cap > 0 && R_cap % 128 == 0);
+  cudaStream_t s = as_stream(stream);
+  DswigluArgs a{static_cast<const uint16_t*>(dh_bf16), static_cast<const uint16_t*>(gu_bf16), offsets + E, R_cap, F,
+                static_cast<uint8_t*>(q->row.data), static_cast<uint8_t*>(q->row.scale),
+                static_cast<uint16_t*>(dgu_bf16), q->tensor_scale, q->amax_out, q->e8m0_mode == MGQ_E8M0_RCEIL};
+  const unsigned grid = (unsigned)((R_cap + kWarps - 1) / kWarps);
+  MGQ_DISPATCH_Q(q, dswiglu_quant_kernel, grid, a);
+  if (q->col.data)
+    return launch_transpose_u8(static_cast<const uint8_t*>(q->row.data), 2 * (int64_t)F,
+                               static_cast<uint8_t*>(q->col.data), R_cap, offsets + E, R_cap, 2 * (int64_t)F, s);
+  return MGQ_OK;
+}
+
+int mgq_moe_unpermute(const void* y_bf16, const int32_t* row_id_map, const float* probs, int T, int k, int H,
+                      void* out_bf16, void* stream) {
+  MGQ_CHECK_ARG(T >= 0 && k >= 1 && k <= 8 && H > 0 && H % 8 == 0);
+  MGQ_CHECK_ARG(T == 0 || (y_bf16 && row_id_map && probs && out_bf16));
+  MGQ_CHECK_ARG(aligned16(y_bf16) && aligned16(out_bf16));
+  if (T == 0) return MGQ_OK;
+  combine_kernel<<<(T + kWarps - 1) / kWarps, 256, 0, as_stream(stream)>>>(
+      static_cast<const uint16_t*>(y_bf16), row_id_map, probs, T, k, H, static_cast<uint16_t*>(out_bf16));
+  MGQ_LAUNCH_CHECK();
+  return MGQ_OK;
+}
+
+int mgq_moe_permute_bwd(const void* da_bf16, const int32_t* row_id_map, int T, int k, int H, void* dx_bf16,
+                        void* stream) {
+  MGQ_CHECK_ARG(T >= 0 && k >= 1 && k <= 8 && H > 0 && H % 8 == 0);
+  MGQ_CHECK_ARG(T == 0 || (da_bf16 && row_id_map && dx_bf16));
+  MGQ_CHECK_ARG(aligned16(da_bf16) && aligned16(dx_bf16));
+  if (T == 0) return MGQ_OK;
+  combine_kernel<<<(T + kWarps - 1) / kWarps, 256, 0, as_stream(stream)>>>(
+      static_cast<const uint16_t*>(da_bf16), row_id_map, nullptr, T, k, H, static_cast<uint16_t*>(dx_bf16));
+  MGQ_LAUNCH_CHECK();
+  return MGQ_OK;
+}
+
+int mgq_moe_unpermute_bwd(const void* dout_bf16, const void* y_bf16, const int32_t* row_id_map,
+                          const int32_t* src_row, const float* probs, int T, int k, int H, int64_t R_cap,
+                          const int32_t* offsets, int E, const mgq_qdesc* q, float* dprobs, void* stream) {
+  int rc = check_q(q);
+  if (rc != MGQ_OK) return rc;
+  MGQ_CHECK_ARG(T >= 0 && k >= 1 && k <= 8 && H > 0 && H % 128 == 0 && E >= 1 && offsets && dprobs && src_row);
+  MGQ_CHECK_ARG(T == 0 || (dout_bf16 && y_bf16 && row_id_map && probs));
+  MGQ_CHECK_ARG(aligned16(dout_bf16) && aligned16(y_bf16) && R_cap > 0 && R_cap % 128 == 0);
+  cudaStream_t s = as_stream(stream);
+  UnpermBwdArgs a;
+  a.dout = static_cast<const uint16_t*>(dout_bf16);
+  a.y = static_cast<const uint16_t*>(y_bf16);
+  a.rim = row_id_map;
+  a.src_row = src_row;
+  a.probs = probs;
+  a.offsets = offsets;
+  a.T = T; a.k = k; a.H = H; a.E = E;
+  a.R_cap = R_cap;
+  a.codes = static_cast<uint8_t*>(q->row.data);
+  a.scales = static_cast<uint8_t*>(q->row.scale);
+  a.tensor_scale = q->tensor_scale;
+  a.amax_out = q->amax_out;
+  a.dprobs = dprobs;
+  a.rceil = q->e8m0_mode == MGQ_E8M0_RCEIL;
+  a.token_blocks = (T + kWarps - 1) / kWarps;
+  const unsigned grid = (unsigned)(a.token_blocks + E);
+  MGQ_DISPATCH_Q(q, unpermute_bwd_kernel, grid, a);
+  if (q->col.data)
+    return launch_transpose_u8(static_cast<const uint8_t*>(q->row.data), H, static_cast<uint8_t*>(q->col.data),
+                               R_cap, offsets + E, R_cap, H, s);
+  return MGQ_OK;
+}
+
+int mgq_block_quantize(const void* x_bf16, int64_t G, int64_t M, int64_t K, const mgq_qdesc* q, void* stream) {
+  int rc = check_q(q);
+  if (rc != MGQ_OK) return rc;
+  MGQ_CHECK_ARG(x_bf16 && aligned16(x_bf16) && G >= 1 && M > 0 && K > 0 && M % 128 == 0 && K % 128 == 0);
+  cudaStream_t s = as_stream(stream);
+  QuantRowsArgs a{static_cast<const uint16_t*>(x_bf16), G * M, M, K, static_cast<uint8_t*>(q->row.data),
+                  static_cast<uint8_t*>(q->row.scale), q->tensor_scale, q->amax_out,
+                  q->e8m0_mode == MGQ_E8M0_RCEIL};
+  const unsigned grid = (unsigned)((G * M + kWarps - 1) / kWarps);
+  MGQ_DISPATCH_Q(q, quant_rows_kernel, grid, a);
+  if (q->col.data) {
+    for (int64_t g = 0; g < G; ++g) {
+      rc = launch_transpose_u8(static_cast<const uint8_t*>(q->row.data) + g * M * K, K,
+                               static_cast<uint8_t*>(q->col.data) + g * M * K, M, nullptr, M, K, s);
+      if (rc != MGQ_OK) return rc;
+    }
+  }
+  return MGQ_OK;
+}
+
+int mgq_amax_history_update(float* history, int32_t* head, float* amax, float* scale, int n, int L, float fmax,
+                            void* stream) {
+  MGQ_CHECK_ARG(history && head && amax && scale && n >= 1 && L >= 1 && fmax > 0.0f);
+  amax_history_kernel<<<1, 256, 0, as_stream(stream)>>>(history, head, amax, scale, n, L, fmax);
+  MGQ_LAUNCH_CHECK();
+  return MGQ_OK;
+}
+
+}  // extern "C"

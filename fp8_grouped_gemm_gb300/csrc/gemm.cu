@@ -1,0 +1,436 @@
+// Grouped FP8 GEMM on the Blackwell tensor cores (tcgen05), one launch for
+// all experts over variable per-expert row counts.
+//
+// The grouped GEMM of the routed-expert layer ("--moe-grouped-gemm",
+// TEGroupedMLP: "[BUG] Loss difference when training with FP8 vs. BF16 MoE",
+// Megatron-LM issue #1152), fed by dynamic quantisation ("float8 moe training
+// conversion API prototype", pytorch/ao PR #2275), with MXFP8 block scales or
+// per-tensor scales ("Numerical fix for moe single grouped weight with fp8 fp4
+// primary weight and grad norm spikes", Megatron-LM PR #5487, coverage
+// matrix), and the backward GEMMs on the column-wise copies ("FP8BlockQuantizer
+// not work on TE", TransformerEngine issue #2393, 128x1 blocks for backward).
+//
+// Design (one CTA per SM, persistent):
+//   warp 0     TMA producer: 128x128 A tile + 256x128 B tile per stage (128-byte
+//              swizzle), plus the 512-byte E8M0 scale chunks (bulk copies)
+//   warp 1     allocates tensor memory; lane 0 issues tcgen05.cp (scales to
+//              tensor memory) and tcgen05.mma (M=128, N=256, K=32 each)
+//   warps 2-5  epilogue: tcgen05.ld of the f32 accumulator, scale, convert, store
+// The tile scheduler walks the expert offset array; every role derives the
+// same tile sequence from it. Every mbarrier wait is bounded: on a timeout the
+// kernel records MGQ_ERR_TIMEOUT, all roles leave their loops, tensor memory is
+// freed and the kernel returns.
+#include "device_common.cuh"
+#include "mgq_internal.h"
+#include "ptx_sm100.cuh"
+
+namespace mgq {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 128;     // BK: bytes = fp8 elements
+constexpr int STAGES = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfaCol = 256, kSfbCol = 256 + 4 * STAGES;
+constexpr uint64_t kWaitNs = 2000000000ull;     // 2 s: far beyond any tile
+constexpr int kMaxE = 1024;
+
+constexpr uint32_t kABytes = BM * BK, kBBytes = BN * BK;
+constexpr uint32_t kSfaBytes = 512, kSfbBytes = 1024;
+constexpr size_t kSmemStage = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+constexpr size_t kSmemBytes = 1024 /*align slack*/ + STAGES * kSmemStage + 256 /*barriers*/ + (kMaxE + 8) * 4;
+
+enum { kModeRows = 0, kModeContract = 1 };
+
+struct GemmParams {
+  const int32_t* offsets;
+  int E;
+  int64_t N;          // rows: output columns; contract: output rows
+  int64_t K;          // rows: contraction length; contract: output columns
+  int64_t R_cap;
+  const uint8_t* sfa;
+  int64_t sfa_kb4;    // 512-byte scale chunks per 128-row tile of A
+  const uint8_t* sfb;
+  int64_t sfb_kb4;
+  const float* sa;
+  const float* sb;
+  void* out;
+  int64_t ldo;
+  int out_f32;
+  float beta;
+  uint32_t idesc;
+  int* err;
+};
+
+struct Tile {
+  int e;
+  int nst;            // contraction stages (128 each)
+  int64_t row_a, row_b, kx0, out_row, out_col;
+};
+
+// Tile t of the sequence. kModeRows: tiles ordered expert, N tile, M tile
+// (M fastest, so a wave shares the B tiles of one expert); kModeContract
+// (wgrad): expert, output-row tile, output-column tile (columns fastest).
+template <int MODE>
+__device__ __forceinline__ bool get_tile(const int32_t* s_off, int E, const GemmParams& p, int64_t t, int& ecur,
+                                         Tile& tl) {
+  if (MODE == kModeRows) {
+    const int64_t nN = p.N / BN;
+    const int64_t total = (int64_t)(s_off[E] / BM) * nN;
+    if (t >= total) return false;
+    while (ecur < E - 1 && (int64_t)(s_off[ecur + 1] / BM) * nN <= t) ++ecur;
+    const int e = ecur;
+    const int64_t mt = (s_off[e + 1] - s_off[e]) / BM;
+    const int64_t local = t - (int64_t)(s_off[e] / BM) * nN;
+    const int64_t n = local / mt, m = local % mt;
+    tl.e = e;
+    tl.nst = (int)(p.K / BK);
+    tl.row_a = s_off[e] + BM * m;
+    tl.row_b = (int64_t)e * p.N + BN * n;
+    tl.kx0 = 0;
+    tl.out_row = tl.row_a;
+    tl.out_col = BN * n;
+  } else {
+    const int64_t mN = p.N / BM, nK = p.K / BN;
+    const int64_t tpe = mN * nK;
+    if (t >= tpe * E) return false;
+    const int e = (int)(t / tpe);
+    const int64_t local = t % tpe;
+    const int64_t m = local / nK, n = local % nK;
+    tl.e = e;
+    tl.nst = (s_off[e + 1] - s_off[e]) / BK;
+    tl.row_a = BM * m;
+    tl.row_b = BN * n;
+    tl.kx0 = s_off[e];
+    tl.out_row = (int64_t)e * p.N + BM * m;
+    tl.out_col = BN * n;
+  }
+  return true;
+}
+
+template <int MODE, bool MX>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + STAGES * kABytes;
+  uint8_t* sSFA = sB + STAGES * kBBytes;
+  uint8_t* sSFB = sSFA + STAGES * kSfaBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sSFB + STAGES * kSfbBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tmem_full = bars + 2 * STAGES;
+  uint64_t* tmem_empty = bars + 2 * STAGES + 1;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  int* s_bad = reinterpret_cast<int*>(s_tmem + 2);
+  int32_t* s_off = reinterpret_cast<int32_t*>(bars + 32);
+
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31;
+  const int E = p.E;
+
+  for (int i = threadIdx.x; i <= E; i += kThreads) s_off[i] = p.offsets[i];
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    ptx::mbar_init(tmem_full, 1);
+    ptx::mbar_init(tmem_empty, 4 * 32);
+    *s_abort = 0;
+    *s_bad = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(s_tmem, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (threadIdx.x == 0) {
+    // the group layout must be 128-row aligned and inside the buffers
+    bool bad = s_off[0] != 0;
+    for (int e = 0; e < E; ++e) bad |= (s_off[e + 1] < s_off[e]) || (s_off[e + 1] % BM) != 0;
+    bad |= (int64_t)s_off[E] > p.R_cap;
+    if (bad) {
+      *s_bad = 1;
+      report(p.err, MGQ_ERR_INVALID_ARG);
+    }
+  }
+  __syncthreads();
+  const uint32_t tmem = *s_tmem;
+  const bool run = (*s_bad == 0);
+
+  if (run && warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    int ecur = 0;
+    uint32_t it = 0;
+    Tile tl;
+    for (int64_t t = blockIdx.x; get_tile<MODE>(s_off, E, p, t, ecur, tl); t += gridDim.x) {
+      for (int s = 0; s < tl.nst; ++s, ++it) {
+        const uint32_t st = it % STAGES, ph = (it / STAGES) & 1;
+        if (*s_abort) break;
+        if (!ptx::mbar_wait(&empty[st], ph ^ 1, kWaitNs)) {
+          report(p.err, MGQ_ERR_TIMEOUT);
+          *s_abort = 1;
+          break;
+        }
+        const uint32_t bytes = kABytes + kBBytes + (MX ? kSfaBytes + kSfbBytes : 0);
+        ptx::mbar_arrive_expect_tx(&full[st], bytes);
+        const int32_t kx = (int32_t)(tl.kx0 + (int64_t)s * BK);
+        ptx::tma_load_2d(sA + st * kABytes, &tmA, &full[st], kx, (int32_t)tl.row_a);
+        ptx::tma_load_2d(sB + st * kBBytes, &tmB, &full[st], kx, (int32_t)tl.row_b);
+        if (MX) {
+          const int64_t kt = tl.kx0 / BK + s;
+          const uint8_t* fa = p.sfa + ((tl.row_a / BM) * p.sfa_kb4 + kt) * 512;
+          const uint8_t* fb = p.sfb + ((tl.row_b / BM) * p.sfb_kb4 + kt) * 512;
+          ptx::bulk_load(sSFA + st * kSfaBytes, fa, 512, &full[st]);
+          ptx::bulk_load(sSFB + st * kSfbBytes, fb, 512, &full[st]);
+          ptx::bulk_load(sSFB + st * kSfbBytes + 512, fb + p.sfb_kb4 * 512, 512, &full[st]);
+        }
+      }
+      if (*s_abort) break;
+    }
+  } else if (run && warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    int ecur = 0;
+    uint32_t it = 0, tc = 0;
+    Tile tl;
+    const uint32_t sA0 = ptx::smem_u32(sA), sB0 = ptx::smem_u32(sB);
+    const uint32_t sSFA0 = ptx::smem_u32(sSFA), sSFB0 = ptx::smem_u32(sSFB);
+    for (int64_t t = blockIdx.x; get_tile<MODE>(s_off, E, p, t, ecur, tl); t += gridDim.x) {
+      if (tl.nst == 0) continue;
+      if (*s_abort) break;
+      if (!ptx::mbar_wait(tmem_empty, (tc & 1) ^ 1, kWaitNs)) {
+        report(p.err, MGQ_ERR_TIMEOUT);
+        *s_abort = 1;
+        break;
+      }
+      ptx::tc_fence_after();
+      bool ok = true;
+      for (int s = 0; s < tl.nst; ++s, ++it) {
+        const uint32_t st = it % STAGES, ph = (it / STAGES) & 1;
+        if (*s_abort || !ptx::mbar_wait(&full[st], ph, kWaitNs)) {
+          report(p.err, MGQ_ERR_TIMEOUT);
+          *s_abort = 1;
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t sfa_t = tmem + kSfaCol + st * 4, sfb_t = tmem + kSfbCol + st * 8;
+        if (MX) {
+          ptx::tmem_cp_32x128b_x4(sfa_t, ptx::sdesc_sf(sSFA0 + st * kSfaBytes));
+          ptx::tmem_cp_32x128b_x4(sfb_t, ptx::sdesc_sf(sSFB0 + st * kSfbBytes));
+          ptx::tmem_cp_32x128b_x4(sfb_t + 4, ptx::sdesc_sf(sSFB0 + st * kSfbBytes + 512));
+        }
+        const uint64_t ad = ptx::sdesc_kmajor_sw128(sA0 + st * kABytes);
+        const uint64_t bd = ptx::sdesc_kmajor_sw128(sB0 + st * kBBytes);
+#pragma unroll
+        for (int kk = 0; kk < BK / 32; ++kk) {
+          // advance 32 bytes (one K=32 step) inside the 128-byte swizzle atom
+          const uint64_t adk = ad + (uint64_t)(kk * 2), bdk = bd + (uint64_t)(kk * 2);
+          const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
+          if (MX)
+            ptx::mma_mxf8f6f4(tmem, adk, bdk, p.idesc | ptx::idesc_sf_ids(kk, kk), sfa_t, sfb_t, acc);
+          else
+            ptx::mma_f8f6f4(tmem, adk, bdk, p.idesc, acc);
+        }
+        ptx::mma_commit(&empty[st]);   // frees the smem stage once these MMAs finish
+      }
+      if (!ok) break;
+      ptx::mma_commit(tmem_full);      // accumulator complete
+      ++tc;
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogue
+    const uint32_t q = warp & 3;                    // tensor-memory lane quadrant
+    const int64_t row_in_tile = q * 32 + lane;
+    int ecur = 0;
+    uint32_t tc = 0;
+    Tile tl;
+    for (int64_t t = blockIdx.x; run && get_tile<MODE>(s_off, E, p, t, ecur, tl); t += gridDim.x) {
+      const int64_t orow = tl.out_row + row_in_tile;
+      if (tl.nst == 0) {
+        // empty group (wgrad): dW_e = 0, or unchanged when accumulating
+        if (p.beta == 0.0f) {
+          if (p.out_f32) {
+            float* o = static_cast<float*>(p.out) + orow * p.ldo + tl.out_col;
+            for (int c = 0; c < BN; c += 4) *reinterpret_cast<float4*>(o + c) = make_float4(0, 0, 0, 0);
+          } else {
+            uint16_t* o = static_cast<uint16_t*>(p.out) + orow * p.ldo + tl.out_col;
+            for (int c = 0; c < BN; c += 8) *reinterpret_cast<uint4*>(o + c) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        continue;
+      }
+      // the whole warp agrees before the .sync.aligned tensor-memory loads
+      if (__any_sync(0xFFFFFFFFu, *s_abort != 0)) break;
+      const bool got = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(tmem_full, tc & 1, kWaitNs));
+      if (!got) {
+        report(p.err, MGQ_ERR_TIMEOUT);
+        *s_abort = 1;
+        break;
+      }
+      ptx::tc_fence_after();
+      float alpha = 1.0f;
+      if (!MX) alpha = 1.0f / (p.sa[0] * p.sb[MODE == kModeRows ? tl.e : 0]);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        ptx::tmem_ld_32x32b_x32(tmem + ((q * 32) << 16) + c * 32, r);
+        ptx::tmem_ld_wait();
+        const int64_t col = tl.out_col + c * 32;
+        if (p.out_f32) {
+          float* o = static_cast<float*>(p.out) + orow * p.ldo + col;
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            float4 v = make_float4(__uint_as_float(r[i]) * alpha, __uint_as_float(r[i + 1]) * alpha,
+                                   __uint_as_float(r[i + 2]) * alpha, __uint_as_float(r[i + 3]) * alpha);
+            if (p.beta != 0.0f) {
+              float4 old = *reinterpret_cast<float4*>(o + i);
+              v.x += p.beta * old.x; v.y += p.beta * old.y; v.z += p.beta * old.z; v.w += p.beta * old.w;
+            }
+            *reinterpret_cast<float4*>(o + i) = v;
+          }
+        } else {
+          uint16_t* o = static_cast<uint16_t*>(p.out) + orow * p.ldo + col;
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(r[i]) * alpha, __uint_as_float(r[i + 1]) * alpha);
+            v.y = pack_bf16x2(__uint_as_float(r[i + 2]) * alpha, __uint_as_float(r[i + 3]) * alpha);
+            v.z = pack_bf16x2(__uint_as_float(r[i + 4]) * alpha, __uint_as_float(r[i + 5]) * alpha);
+            v.w = pack_bf16x2(__uint_as_float(r[i + 6]) * alpha, __uint_as_float(r[i + 7]) * alpha);
+            *reinterpret_cast<uint4*>(o + i) = v;
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(tmem_empty);
+      ++tc;
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int MODE, bool MX>
+int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, cudaStream_t s) {
+  auto kern = grouped_gemm_kernel<MODE, MX>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
+      return MGQ_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  kern<<<num_sms(), kThreads, kSmemBytes, s>>>(ta, tb, p);
+  MGQ_LAUNCH_CHECK();
+  return MGQ_OK;
+}
+
+int check_operand(const mgq_operand* o) {
+  if (!o || !o->data || !aligned16(o->data)) return MGQ_ERR_INVALID_ARG;
+  if (o->dtype != MGQ_E4M3 && o->dtype != MGQ_E5M2) return MGQ_ERR_UNSUPPORTED;
+  return MGQ_OK;
+}
+
+// Shared driver of the three entry points.
+//  mode rows:     A [rowsA, Kc] (ld), B [E*Nout, Kc] (ld); out [rowsA, Nout]
+//  mode contract: A [Nout_rows, R_cap], B [Kout, R_cap]; out [E*Nout_rows, Kout]
+int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scaling, const int32_t* offsets, int E,
+                int64_t R_cap, int64_t N, int64_t K, float beta, void* out, int out_dtype, void* stream) {
+  int rc;
+  if ((rc = check_operand(A)) != MGQ_OK) return rc;
+  if ((rc = check_operand(B)) != MGQ_OK) return rc;
+  MGQ_CHECK_ARG(offsets && out && aligned16(out) && E >= 1 && E <= kMaxE && R_cap > 0 && R_cap % BM == 0);
+  MGQ_CHECK_ARG(out_dtype == MGQ_OUT_BF16 || out_dtype == MGQ_OUT_F32);
+  MGQ_CHECK_ARG(beta == 0.0f || (mode == kModeContract && out_dtype == MGQ_OUT_F32));
+  MGQ_CHECK_ARG(R_cap < (1ll << 31));
+  if (scaling != MGQ_MX32_E8M0 && scaling != MGQ_TENSOR_F32) return MGQ_ERR_UNSUPPORTED;
+  const bool mx = scaling == MGQ_MX32_E8M0;
+  MGQ_CHECK_ARG(A->scale && B->scale);
+  if (mx) MGQ_CHECK_ARG(aligned16(A->scale) && aligned16(B->scale));
+  GemmParams p;
+  CUtensorMap ta, tb;
+  if (mode == kModeRows) {
+    MGQ_CHECK_ARG(N > 0 && K > 0 && N % BN == 0 && K % BK == 0);
+    MGQ_CHECK_ARG(A->ld >= K && A->ld % 128 == 0 && B->ld >= K && B->ld % 128 == 0);
+    MGQ_CHECK_ARG((int64_t)E * N < (1ll << 31));
+    if (!encode_tmap_u8_2d(&ta, A->data, (uint64_t)K, (uint64_t)R_cap, (uint64_t)A->ld, 128, BM) ||
+        !encode_tmap_u8_2d(&tb, B->data, (uint64_t)K, (uint64_t)E * N, (uint64_t)B->ld, 128, BN))
+      return MGQ_ERR_CUDA;
+    p.sfa_kb4 = A->ld / 128;
+    p.sfb_kb4 = B->ld / 128;
+  } else {
+    MGQ_CHECK_ARG(N > 0 && K > 0 && N % BM == 0 && K % BN == 0);
+    MGQ_CHECK_ARG(A->ld >= R_cap && A->ld % 128 == 0 && B->ld >= R_cap && B->ld % 128 == 0);
+    if (!encode_tmap_u8_2d(&ta, A->data, (uint64_t)R_cap, (uint64_t)N, (uint64_t)A->ld, 128, BM) ||
+        !encode_tmap_u8_2d(&tb, B->data, (uint64_t)R_cap, (uint64_t)K, (uint64_t)B->ld, 128, BN))
+      return MGQ_ERR_CUDA;
+    p.sfa_kb4 = A->ld / 128;
+    p.sfb_kb4 = B->ld / 128;
+  }
+  int* err = error_word();
+  if (!err) return MGQ_ERR_CUDA;
+  p.offsets = offsets;
+  p.E = E;
+  p.N = N;
+  p.K = K;
+  p.R_cap = R_cap;
+  p.sfa = static_cast<const uint8_t*>(A->scale);
+  p.sfb = static_cast<const uint8_t*>(B->scale);
+  p.sa = static_cast<const float*>(A->scale);
+  p.sb = static_cast<const float*>(B->scale);
+  p.out = out;
+  p.ldo = (mode == kModeRows) ? N : K;
+  p.out_f32 = out_dtype == MGQ_OUT_F32;
+  p.beta = beta;
+  p.idesc = mx ? ptx::idesc_mxf8f6f4(A->dtype, B->dtype, BM, BN) : ptx::idesc_f8f6f4(A->dtype, B->dtype, BM, BN);
+  p.err = err;
+  cudaStream_t s = as_stream(stream);
+  if (mode == kModeRows)
+    return mx ? launch_gemm<kModeRows, true>(ta, tb, p, s) : launch_gemm<kModeRows, false>(ta, tb, p, s);
+  return mx ? launch_gemm<kModeContract, true>(ta, tb, p, s) : launch_gemm<kModeContract, false>(ta, tb, p, s);
+}
+
+}  // namespace
+}  // namespace mgq
+
+using namespace mgq;
+
+extern "C" {
+
+int mgq_grouped_gemm_fwd(const mgq_operand* A, const mgq_operand* W, int scaling, const int32_t* offsets, int E,
+                         int64_t R_cap, int64_t N, int64_t K, void* Y, int out_dtype, void* stream) {
+  return run_grouped(kModeRows, A, W, scaling, offsets, E, R_cap, N, K, 0.0f, Y, out_dtype, stream);
+}
+
+int mgq_grouped_gemm_dgrad(const mgq_operand* dY, const mgq_operand* Wcol, int scaling, const int32_t* offsets,
+                           int E, int64_t R_cap, int64_t N, int64_t K, void* dA, int out_dtype, void* stream) {
+  // dA [R_cap, K] = dY [R_cap, N] x Wcol_e [K, N]^T: a row-grouped GEMM with
+  // contraction N and K output columns
+  return run_grouped(kModeRows, dY, Wcol, scaling, offsets, E, R_cap, K, N, 0.0f, dA, out_dtype, stream);
+}
+
+int mgq_grouped_gemm_wgrad(const mgq_operand* dYcol, const mgq_operand* Acol, int scaling, const int32_t* offsets,
+                           int E, int64_t R_cap, int64_t N, int64_t K, float beta, void* dW, int out_dtype,
+                           void* stream) {
+  return run_grouped(kModeContract, dYcol, Acol, scaling, offsets, E, R_cap, N, K, beta, dW, out_dtype, stream);
+}
+
+}  // extern "C"

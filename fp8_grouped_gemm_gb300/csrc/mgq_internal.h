@@ -1,0 +1,46 @@
+// Host-side internals shared by the translation units of libmgq.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mgq.h"
+
+namespace mgq {
+
+// Device address of the current device's error word (cached per device).
+// Returns nullptr if it cannot be resolved.
+int* error_word();
+
+// Encodes a 2D row-major tiled tensor map of unsigned bytes: `inner` bytes per
+// row (contiguous), `outer` rows with a pitch of `pitch` bytes; the box is
+// box_inner x box_outer with 128-byte swizzling (box_inner == 128).
+bool encode_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch,
+                       uint32_t box_inner, uint32_t box_outer);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Number of SMs of the current device (cached).
+int num_sms();
+
+// dst[c, r] = src[r, c] for r < *rows_used (or rows_cap when rows_used is
+// null), c < cols; 64x64 byte tiles (routing.cu).
+int launch_transpose_u8(const uint8_t* src, int64_t src_ld, uint8_t* dst, int64_t dst_ld, const int32_t* rows_used,
+                        int64_t rows_cap, int64_t cols, cudaStream_t s);
+
+}  // namespace mgq
+
+#define MGQ_CHECK_ARG(cond)                 \
+  do {                                      \
+    if (!(cond)) return MGQ_ERR_INVALID_ARG; \
+  } while (0)
+
+#define MGQ_LAUNCH_CHECK()                           \
+  do {                                               \
+    if (cudaPeekAtLastError() != cudaSuccess) {      \
+      (void)cudaGetLastError();                      \
+      return MGQ_ERR_CUDA;                           \
+    }                                                \
+  } while (0)

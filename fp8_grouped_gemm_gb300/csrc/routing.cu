@@ -1,0 +1,407 @@
+// Token dispatch: routing (stable counting sort of the (token, slot) entries
+// by expert) and the fused permute + amax + scale + cast of the token rows.
+//
+// Grouping rows by expert so that one grouped GEMM covers all experts, with
+// expert inputs padded for FP8: "[BUG] Loss difference when training with FP8
+// vs. BF16 MoE" (Megatron-LM issue #1152, repro steps and additional
+// context); padding to the quantisation block as the required layout: "FP8BlockQuantizer
+// not work on TE" (TransformerEngine issue #2393, maintainer replies);
+// dynamic quantisation in front of the scaled grouped mm: "float8 moe
+// training conversion API prototype" (pytorch/ao PR #2275, description).
+#include "device_common.cuh"
+#include "mgq_internal.h"
+
+namespace mgq {
+namespace {
+
+constexpr int kChunk = 1024;        // routing entries per chunk
+constexpr int kRouteThreads = 256;
+constexpr int kMaxExperts = 1024;
+
+// ---- routing pass 1: per-chunk expert histogram -------------------------------
+__global__ void route_count_kernel(const int32_t* __restrict__ idx, int64_t n, int E, int32_t* __restrict__ cnt,
+                                   int* err) {
+  extern __shared__ int s_cnt[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  int64_t base = (int64_t)blockIdx.x * kChunk;
+  for (int i = threadIdx.x; i < kChunk; i += blockDim.x) {
+    int64_t g = base + i;
+    if (g < n) {
+      int e = idx[g];
+      if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+      else report(err, MGQ_ERR_DEVICE_INDEX);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[(int64_t)blockIdx.x * E + e] = s_cnt[e];
+}
+
+// ---- routing pass 2: totals, padded exclusive scan over experts, and the
+// first destination row of every (chunk, expert) pair (in place in cnt) ----
+__global__ void route_scan_kernel(int32_t* __restrict__ cnt, int nchunks, int E, int align,
+                                  int32_t* __restrict__ offsets, int32_t* __restrict__ counts,
+                                  int32_t* __restrict__ src_row) {
+  __shared__ int s_pad[kMaxExperts];
+  __shared__ int s_tot[kMaxExperts];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int tot = 0;
+    for (int c = 0; c < nchunks; ++c) tot += cnt[(int64_t)c * E + e];
+    s_tot[e] = tot;
+    s_pad[e] = (tot + align - 1) / align * align;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {   // E <= 1024: a serial scan is a few microseconds at most
+    int run = 0;
+    for (int e = 0; e < E; ++e) {
+      int p = s_pad[e];
+      s_pad[e] = run;
+      run += p;
+    }
+    offsets[E] = run;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    offsets[e] = s_pad[e];
+    counts[e] = s_tot[e];
+    int run = s_pad[e];
+    for (int c = 0; c < nchunks; ++c) {
+      int v = cnt[(int64_t)c * E + e];
+      cnt[(int64_t)c * E + e] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  // filler rows of every group
+  for (int e = 0; e < E; ++e) {
+    int lo = s_pad[e] + s_tot[e];
+    int hi = (e + 1 < E) ? s_pad[e + 1] : offsets[E];
+    for (int r = lo + threadIdx.x; r < hi; r += blockDim.x) src_row[r] = -1;
+  }
+}
+
+// ---- routing pass 3: stable rank inside each chunk --------------------------
+// Entries of a chunk are taken in order, 256 per round; within a warp,
+// __match_any_sync finds the lanes with the same expert and the rank is the
+// number of such lanes before this one; warps and rounds before it add their
+// counts.
+__global__ void route_rank_kernel(const int32_t* __restrict__ idx, int64_t n, int E,
+                                  const int32_t* __restrict__ base, int32_t* __restrict__ row_id_map,
+                                  int32_t* __restrict__ src_row) {
+  extern __shared__ int smem[];
+  int* s_run = smem;                 // [E] rows already given in this chunk
+  int* s_w = smem + E;               // [8][E] per-warp counts of this round
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_run[e] = 0;
+  const int64_t cbase = (int64_t)blockIdx.x * kChunk;
+  const int32_t* cb = base + (int64_t)blockIdx.x * E;
+  for (int round = 0; round < kChunk / kRouteThreads; ++round) {
+    for (int i = threadIdx.x; i < 8 * E; i += blockDim.x) s_w[i] = 0;
+    __syncthreads();
+    int64_t g = cbase + round * kRouteThreads + threadIdx.x;
+    int key = -1;
+    if (g < n) {
+      key = idx[g];
+      if (key < 0 || key >= E) key = -1;
+    }
+    unsigned peers = __match_any_sync(0xFFFFFFFFu, key);
+    int rank = __popc(peers & ((1u << lane) - 1u));
+    if (key >= 0 && rank == 0) s_w[warp * E + key] = __popc(peers);
+    __syncthreads();
+    if (key >= 0) {
+      int r = cb[key] + s_run[key] + rank;
+      for (int w = 0; w < warp; ++w) r += s_w[w * E + key];
+      row_id_map[g] = r;
+      src_row[r] = (int32_t)g;
+    } else if (g < n) {
+      row_id_map[g] = -1;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      int s = 0;
+      for (int w = 0; w < 8; ++w) s += s_w[w * E + e];
+      s_run[e] += s;
+    }
+    __syncthreads();
+  }
+}
+
+// ---- fused permute + quantise ---------------------------------------------------
+// One warp per token row; lane l handles elements [32 l, 32 l + 32) of each
+// 1024-element slice, i.e. exactly one 32-element MX block. The row is read
+// once (16-byte loads) and its codes and scales are written to the k
+// destination rows.
+
+struct PermuteArgs {
+  const uint16_t* x;
+  int T, H, k, E;
+  const int32_t* row_id_map;
+  const int32_t* offsets;
+  const int32_t* counts;
+  uint8_t* codes;          // [R_cap, H]
+  uint8_t* scales;         // layout per scaling mode
+  uint16_t* out_bf16;      // [R_cap, H] or null
+  const float* tensor_scale;
+  float* amax_out;
+  int64_t R_cap;
+  int e8m0_rceil;
+  int token_blocks;        // CTAs that process tokens; the rest fill padding
+  int* err;
+};
+
+__device__ __forceinline__ void load_block32(const uint16_t* src, uint32_t (&w)[16]) {
+  const uint4* p = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 v = __ldg(p + q);
+    w[4 * q + 0] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
+  }
+}
+
+template <int SC, int DT>
+__global__ void __launch_bounds__(256) permute_quant_kernel(PermuteArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int H = a.H;
+  if ((int)blockIdx.x >= a.token_blocks) {
+    // ---- padding rows of expert e: zero codes (and zero scales) -------------
+    int e = blockIdx.x - a.token_blocks;
+    if (e >= a.E) return;
+    int64_t lo = a.offsets[e] + a.counts[e], hi = a.offsets[e + 1];
+    for (int64_t r = lo + warp; r < hi; r += 8) {
+      for (int c = lane * 16; c < H; c += 32 * 16)
+        *reinterpret_cast<uint4*>(a.codes + r * H + c) = make_uint4(0, 0, 0, 0);
+      if (a.out_bf16)
+        for (int c = lane * 8; c < H; c += 32 * 8)
+          *reinterpret_cast<uint4*>(a.out_bf16 + r * H + c) = make_uint4(0, 0, 0, 0);
+      if (SC == MGQ_MX32_E8M0) {
+        const int64_t kb4 = H / 128;
+        for (int b4 = lane; b4 < H / 128; b4 += 32)
+          *reinterpret_cast<uint32_t*>(a.scales + tiled_scale_offset(r, (int64_t)b4 * 4, kb4)) = 0u;
+      } else if (SC == MGQ_BLK_1x128_F32) {
+        float* s = reinterpret_cast<float*>(a.scales);
+        for (int b = lane; b < H / 128; b += 32) s[(int64_t)b * a.R_cap + r] = 0.0f;
+      }
+    }
+    return;
+  }
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= a.T) return;
+  int dest[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) dest[j] = (j < a.k) ? a.row_id_map[(int64_t)t * a.k + j] : -1;
+  const float ts = (SC == MGQ_TENSOR_F32) ? a.tensor_scale[0] : 1.0f;
+  uint32_t tamax = 0;   // per-tensor amax (bf16 bits in the high half)
+  for (int c0 = 0; c0 < H; c0 += 1024) {
+    const int c = c0 + lane * 32;
+    const bool active = c < H;       // every lane stays in the loop (shuffles below)
+    uint32_t w[16];
+    if (active) {
+      load_block32(a.x + (int64_t)t * H + c, w);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) w[i] = 0;
+    }
+    uint32_t am2 = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) am2 = absmax_bf16x2(am2, w[i]);
+    uint32_t amax_bits = fold_bf16x2(am2);
+    float mult;
+    uint32_t scode = 0;
+    float sinv = 0.0f;
+    if (SC == MGQ_MX32_E8M0) {
+      int e = mx_exponent(amax_bits, FmtInfo<DT>::emax, a.e8m0_rceil != 0);
+      mult = mx_multiplier(e);
+      scode = mx_scale_code(e);
+    } else if (SC == MGQ_BLK_1x128_F32) {
+      // amax over 128 elements = 4 lanes
+      uint32_t m = amax_bits;
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+      float am = __uint_as_float(m);
+      float s = (m == 0) ? 1.0f : __fdiv_rn(FmtInfo<DT>::fmax, am);
+      if (isinf(s)) s = 3.40282347e38f;
+      mult = s;
+      sinv = __fdiv_rn(1.0f, s);
+    } else {  // MGQ_TENSOR_F32
+      mult = ts;
+      tamax = max(tamax, amax_bits);
+    }
+    uint32_t cw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float v0 = __fmul_rn(bf16_lo(w[2 * i]), mult), v1 = __fmul_rn(bf16_hi(w[2 * i]), mult);
+      float v2 = __fmul_rn(bf16_lo(w[2 * i + 1]), mult), v3 = __fmul_rn(bf16_hi(w[2 * i + 1]), mult);
+      cw[i] = cvt_fp8x4<DT>(v0, v1, v2, v3);
+    }
+    // gather the 4 scale bytes of lanes 4j..4j+3 into lane 4j
+    uint32_t s4 = 0;
+    if (SC == MGQ_MX32_E8M0) {
+      uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, scode, 1);
+      uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, scode, 2);
+      uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, scode, 3);
+      s4 = scode | (b1 << 8) | (b2 << 16) | (b3 << 24);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j >= a.k || !active) break;
+      int r = dest[j];
+      if (r < 0) continue;
+      uint4* dst = reinterpret_cast<uint4*>(a.codes + (int64_t)r * H + c);
+      dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+      dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+      if (a.out_bf16) {
+        uint4* ob = reinterpret_cast<uint4*>(a.out_bf16 + (int64_t)r * H + c);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ob[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+      }
+      if (SC == MGQ_MX32_E8M0) {
+        if ((lane & 3) == 0)
+          *reinterpret_cast<uint32_t*>(a.scales + tiled_scale_offset(r, c / 32, H / 128)) = s4;
+      } else if (SC == MGQ_BLK_1x128_F32) {
+        if ((lane & 3) == 0) reinterpret_cast<float*>(a.scales)[(int64_t)(c / 128) * a.R_cap + r] = sinv;
+      }
+    }
+  }
+  if (SC == MGQ_TENSOR_F32 && a.amax_out) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tamax = max(tamax, __shfl_xor_sync(0xFFFFFFFFu, tamax, o));
+    if (lane == 0) atomic_max_nonneg(a.amax_out, __uint_as_float(tamax));
+  }
+}
+
+// ---- byte transpose of the used rows: dst[c, r] = src[r, c] -----------------
+// 64x64 tiles through shared memory; rows >= *rows_used are skipped.
+__global__ void transpose_u8_kernel(const uint8_t* __restrict__ src, int64_t src_ld, uint8_t* __restrict__ dst,
+                                    int64_t dst_ld, const int32_t* __restrict__ rows_used, int64_t rows_cap,
+                                    int64_t cols) {
+  __shared__ uint32_t tile[64][17];   // 64 rows x 64 bytes, padded
+  const int64_t r0 = (int64_t)blockIdx.x * 64, c0 = (int64_t)blockIdx.y * 64;
+  const int64_t nrows = rows_used ? (int64_t)*rows_used : rows_cap;
+  if (r0 >= nrows) return;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;   // 256 threads: 16 x 16
+  for (int rr = ty; rr < 64; rr += 16) {
+    int64_t r = r0 + rr;
+    tile[rr][tx] = (r < nrows) ? *reinterpret_cast<const uint32_t*>(src + r * src_ld + c0 + tx * 4) : 0u;
+  }
+  __syncthreads();
+  // thread writes 4 consecutive rows (bytes) of one output row (column c)
+  for (int cc = ty; cc < 64; cc += 16) {
+    int64_t c = c0 + cc;
+    if (c >= cols) continue;
+    uint32_t v = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      int rr = tx * 4 + q;
+      uint32_t word = tile[rr][cc >> 2];
+      v |= ((word >> ((cc & 3) * 8)) & 0xFFu) << (8 * q);
+    }
+    if (r0 + tx * 4 < nrows) *reinterpret_cast<uint32_t*>(dst + c * dst_ld + r0 + tx * 4) = v;
+  }
+}
+
+}  // namespace
+
+// launched by other translation units (per-tensor column-wise copies)
+int launch_transpose_u8(const uint8_t* src, int64_t src_ld, uint8_t* dst, int64_t dst_ld, const int32_t* rows_used,
+                        int64_t rows_cap, int64_t cols, cudaStream_t s) {
+  dim3 grid((unsigned)((rows_cap + 63) / 64), (unsigned)((cols + 63) / 64));
+  transpose_u8_kernel<<<grid, 256, 0, s>>>(src, src_ld, dst, dst_ld, rows_used, rows_cap, cols);
+  MGQ_LAUNCH_CHECK();
+  return MGQ_OK;
+}
+
+}  // namespace mgq
+
+using namespace mgq;
+
+extern "C" {
+
+size_t mgq_permute_workspace_size(int T, int k, int E) {
+  if (T < 0 || k <= 0 || E <= 0) return 0;
+  int64_t n = (int64_t)T * k;
+  int64_t nchunks = (n + kChunk - 1) / kChunk;
+  if (nchunks == 0) nchunks = 1;
+  return (size_t)(nchunks * E * sizeof(int32_t));
+}
+
+int mgq_moe_permute(const void* x_bf16, int T, int H, const int32_t* topk_idx, int k, int E, int align,
+                    const mgq_qdesc* q, void* out_bf16, int64_t R_cap, int32_t* row_id_map, int32_t* src_row,
+                    int32_t* offsets, int32_t* counts, void* workspace, size_t ws_bytes, void* stream) {
+  MGQ_CHECK_ARG(T >= 0 && H > 0 && k >= 1 && k <= 8 && E >= 1 && E <= kMaxExperts && k <= E);
+  MGQ_CHECK_ARG(align >= 1 && (align % 32 == 0 || align == 1) && H % 128 == 0);
+  MGQ_CHECK_ARG(row_id_map && src_row && offsets && counts && workspace);
+  MGQ_CHECK_ARG(T == 0 || (x_bf16 && topk_idx));
+  const int64_t n = (int64_t)T * k;
+  const int64_t need = ((n + (int64_t)E * (align - 1)) + 127) / 128 * 128;
+  MGQ_CHECK_ARG(R_cap >= need && R_cap % 128 == 0 && R_cap < (1ll << 31));
+  MGQ_CHECK_ARG(ws_bytes >= mgq_permute_workspace_size(T, k, E));
+  MGQ_CHECK_ARG(aligned16(x_bf16) && aligned16(out_bf16));
+  if (q) {
+    MGQ_CHECK_ARG(q->row.data && aligned16(q->row.data));
+    MGQ_CHECK_ARG(q->dtype == MGQ_E4M3 || q->dtype == MGQ_E5M2);
+    if (q->scaling == MGQ_MX32_E8M0 || q->scaling == MGQ_BLK_1x128_F32)
+      MGQ_CHECK_ARG(q->row.scale && aligned16(q->row.scale));
+    else if (q->scaling == MGQ_TENSOR_F32)
+      MGQ_CHECK_ARG(q->tensor_scale != nullptr);
+    else
+      return MGQ_ERR_UNSUPPORTED;
+    if (q->col.data) {
+      if (q->scaling != MGQ_TENSOR_F32) return MGQ_ERR_UNSUPPORTED;
+      MGQ_CHECK_ARG(aligned16(q->col.data) && align % 4 == 0);
+    }
+  } else {
+    MGQ_CHECK_ARG(out_bf16 != nullptr);
+  }
+  int* err = error_word();
+  if (!err) return MGQ_ERR_CUDA;
+  cudaStream_t s = as_stream(stream);
+  int64_t nchunks = (n + kChunk - 1) / kChunk;
+  int32_t* cnt = static_cast<int32_t*>(workspace);
+  if (nchunks > 0) {
+    route_count_kernel<<<(unsigned)nchunks, kRouteThreads, E * sizeof(int), s>>>(topk_idx, n, E, cnt, err);
+    MGQ_LAUNCH_CHECK();
+  }
+  route_scan_kernel<<<1, 1024, 0, s>>>(cnt, (int)nchunks, E, align, offsets, counts, src_row);
+  MGQ_LAUNCH_CHECK();
+  if (nchunks > 0) {
+    route_rank_kernel<<<(unsigned)nchunks, kRouteThreads, 9 * E * sizeof(int), s>>>(topk_idx, n, E, cnt,
+                                                                                     row_id_map, src_row);
+    MGQ_LAUNCH_CHECK();
+  }
+  PermuteArgs a;
+  a.x = static_cast<const uint16_t*>(x_bf16);
+  a.T = T; a.H = H; a.k = k; a.E = E;
+  a.row_id_map = row_id_map; a.offsets = offsets; a.counts = counts;
+  a.codes = q ? static_cast<uint8_t*>(q->row.data) : nullptr;
+  a.scales = q ? static_cast<uint8_t*>(q->row.scale) : nullptr;
+  a.out_bf16 = static_cast<uint16_t*>(out_bf16);
+  a.tensor_scale = q ? q->tensor_scale : nullptr;
+  a.amax_out = q ? q->amax_out : nullptr;
+  a.R_cap = R_cap;
+  a.e8m0_rceil = q ? (q->e8m0_mode == MGQ_E8M0_RCEIL) : 1;
+  a.token_blocks = (T + 7) / 8;
+  a.err = err;
+  dim3 grid((unsigned)(a.token_blocks + E));
+  if (!q) {
+    return MGQ_ERR_UNSUPPORTED;   // bf16-only dispatch is not needed by the layer
+  }
+  const int sc = q->scaling, dt = q->dtype;
+#define MGQ_PERMUTE_LAUNCH(SC, DT) permute_quant_kernel<SC, DT><<<grid, 256, 0, s>>>(a)
+  if (sc == MGQ_MX32_E8M0 && dt == MGQ_E4M3) MGQ_PERMUTE_LAUNCH(MGQ_MX32_E8M0, MGQ_E4M3);
+  else if (sc == MGQ_MX32_E8M0 && dt == MGQ_E5M2) MGQ_PERMUTE_LAUNCH(MGQ_MX32_E8M0, MGQ_E5M2);
+  else if (sc == MGQ_BLK_1x128_F32 && dt == MGQ_E4M3) MGQ_PERMUTE_LAUNCH(MGQ_BLK_1x128_F32, MGQ_E4M3);
+  else if (sc == MGQ_BLK_1x128_F32 && dt == MGQ_E5M2) MGQ_PERMUTE_LAUNCH(MGQ_BLK_1x128_F32, MGQ_E5M2);
+  else if (sc == MGQ_TENSOR_F32 && dt == MGQ_E4M3) MGQ_PERMUTE_LAUNCH(MGQ_TENSOR_F32, MGQ_E4M3);
+  else if (sc == MGQ_TENSOR_F32 && dt == MGQ_E5M2) MGQ_PERMUTE_LAUNCH(MGQ_TENSOR_F32, MGQ_E5M2);
+  else return MGQ_ERR_UNSUPPORTED;
+#undef MGQ_PERMUTE_LAUNCH
+  MGQ_LAUNCH_CHECK();
+  if (q->col.data) {
+    int rc = launch_transpose_u8(static_cast<const uint8_t*>(q->row.data), H, static_cast<uint8_t*>(q->col.data),
+                                 R_cap, offsets + E, R_cap, H, s);
+    if (rc != MGQ_OK) return rc;
+  }
+  return MGQ_OK;
+}
+
+}  // extern "C"

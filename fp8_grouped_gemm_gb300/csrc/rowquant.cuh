@@ -1,0 +1,93 @@
+// Lane-level row-wise block quantiser shared by the fused elementwise kernels.
+// A warp covers a 1024-element slice of one row; lane l owns the 32 elements
+// [32 l, 32 l + 32), which is exactly one MX block (1x32) and a quarter of a
+// 1x128 block. All 32 lanes must call quantize32 (it shuffles).
+#pragma once
+#include "device_common.cuh"
+
+namespace mgq {
+
+struct Block32 {
+  uint32_t cw[8];   // 32 codes
+  uint32_t s4;      // MX: the 4 scale bytes of lanes 4j..4j+3 (valid in lane 4j)
+  float sinv;       // 1x128: float32 scale_inv of the 128-element block
+};
+
+__device__ __forceinline__ uint32_t absmax_bits_f32(const float* v, int n) {
+  uint32_t m = 0;
+  for (int i = 0; i < n; ++i) m = max(m, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+  return m;
+}
+
+// v: the lane's 32 values; amax_bits: float bits of max |v| of this lane's
+// 32 values; ts: per-tensor scale (MGQ_TENSOR_F32)
+template <int SC, int DT>
+__device__ __forceinline__ void quantize32(const float* v, uint32_t amax_bits, float ts, bool rceil, Block32& o) {
+  float mult = ts;
+  o.s4 = 0;
+  o.sinv = 0.0f;
+  if (SC == MGQ_MX32_E8M0) {
+    const int e = mx_exponent(amax_bits, FmtInfo<DT>::emax, rceil);
+    mult = mx_multiplier(e);
+    const uint32_t sc = mx_scale_code(e);
+    const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sc, 1);
+    const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sc, 2);
+    const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sc, 3);
+    o.s4 = sc | (b1 << 8) | (b2 << 16) | (b3 << 24);
+  } else if (SC == MGQ_BLK_1x128_F32) {
+    uint32_t m = amax_bits;
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+    float s = (m == 0) ? 1.0f : __fdiv_rn(FmtInfo<DT>::fmax, __uint_as_float(m));
+    if (isinf(s)) s = 3.40282347e38f;
+    mult = s;
+    o.sinv = __fdiv_rn(1.0f, s);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    o.cw[i] = cvt_fp8x4<DT>(__fmul_rn(v[4 * i], mult), __fmul_rn(v[4 * i + 1], mult),
+                            __fmul_rn(v[4 * i + 2], mult), __fmul_rn(v[4 * i + 3], mult));
+}
+
+// Stores the lane's block of row r, columns [c, c + 32), of a matrix with row
+// pitch ld (elements) and rows_cap rows (1x128 scales are k-block major).
+template <int SC>
+__device__ __forceinline__ void store32(const Block32& o, uint8_t* codes, uint8_t* scales, int64_t r, int64_t c,
+                                        int64_t ld, int64_t rows_cap, uint32_t lane) {
+  uint4* dst = reinterpret_cast<uint4*>(codes + r * ld + c);
+  dst[0] = make_uint4(o.cw[0], o.cw[1], o.cw[2], o.cw[3]);
+  dst[1] = make_uint4(o.cw[4], o.cw[5], o.cw[6], o.cw[7]);
+  if (SC == MGQ_MX32_E8M0) {
+    if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(scales + tiled_scale_offset(r, c / 32, ld / 128)) = o.s4;
+  } else if (SC == MGQ_BLK_1x128_F32) {
+    if ((lane & 3) == 0) reinterpret_cast<float*>(scales)[(c / 128) * rows_cap + r] = o.sinv;
+  }
+}
+
+__device__ __forceinline__ void load_bf16x32(const uint16_t* src, float* v) {
+  const uint4* p = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 w = __ldg(p + q);
+    v[8 * q + 0] = bf16_lo(w.x); v[8 * q + 1] = bf16_hi(w.x);
+    v[8 * q + 2] = bf16_lo(w.y); v[8 * q + 3] = bf16_hi(w.y);
+    v[8 * q + 4] = bf16_lo(w.z); v[8 * q + 5] = bf16_hi(w.z);
+    v[8 * q + 6] = bf16_lo(w.w); v[8 * q + 7] = bf16_hi(w.w);
+  }
+}
+
+__device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float* v) {
+  uint4* p = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    p[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                      pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+}
+
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+}  // namespace mgq

@@ -1,0 +1,238 @@
+/*
+ * mgq.h — C ABI of the GB300 (sm_103a) low-precision MoE routed-expert layer.
+ *
+ * One GPU, stream-ordered, stateless. The caller owns every buffer: the
+ * library never allocates device memory (the only device-resident state is a
+ * per-device error word read by mgq_get_error). Pointers marked "device" must
+ * be device (or managed) memory of the current device; "host" pointers are
+ * read during the call only. `stream` is a cudaStream_t (NULL = legacy
+ * default stream). Every call returns an mgq_status synchronously:
+ * argument errors are detected on the host before anything is launched;
+ * errors found by a kernel (an expert id out of range, a pipeline wait that
+ * timed out) are recorded in the device error word and reported by
+ * mgq_get_error. No call traps, aborts or throws.
+ *
+ * What the operations compute comes from four pages on low-precision MoE
+ * training:
+ *  [MOE-FP8]  "[BUG] Loss difference when training with FP8 vs. BF16 MoE"
+ *             (Megatron-LM issue #1152): grouped GEMM over experts
+ *             (--moe-grouped-gemm, TEGroupedMLP), padding of expert inputs
+ *             for FP8, the hybrid format (e4m3 forward, e5m2 gradients) and
+ *             delayed scaling with a 1024-long amax history reduced by max.
+ *  [GROUPED]  "Numerical fix for moe single grouped weight with fp8 fp4
+ *             primary weight and grad norm spikes" (Megatron-LM PR #5487):
+ *             the MXFP8 and NVFP4 recipes, one contiguous grouped weight for
+ *             all experts, row-wise and column-wise data + scales, gradient
+ *             accumulation fusion, e2m1 packed two per byte.
+ *  [BLOCK]    "FP8BlockQuantizer not work on TE" (TransformerEngine issue
+ *             #2393): 1x128 forward / 128x1 backward block scaling, the
+ *             transpose identity colwise(x) = transpose(rowwise(x^T)), zero
+ *             fill of partial blocks, block-aligned shapes as a hard error.
+ *  [AO-MOE]   "float8 moe training conversion API prototype" (pytorch/ao PR
+ *             #2275): dynamic quantisation followed by a scaled grouped mm;
+ *             SQNR of outputs and gradients against bf16.
+ * Number formats follow OCP OFP8 (e4m3, e5m2) and OCP MX v1.0 (e2m1, E8M0).
+ *
+ * Notation: T tokens, k experts per token, E experts, H hidden, F ffn.
+ * R_cap = capacity (rows) of permuted buffers; the rows in use are
+ * [0, offsets[E]), a device value, so no call needs a host sync.
+ *
+ * Quantised storage (codes: 1 byte per element, e2m1: 2 elements per byte,
+ * element 2i in the low nibble). For a row-major matrix with `rows` rows and
+ * row pitch `ld` elements (the contraction dimension K):
+ *  MGQ_MX32_E8M0     E8M0 scale per 32 consecutive elements of a row, stored
+ *                    in 128x4 tiles: byte of (row r, block b) at
+ *                      ((r/128)*(ld/128) + b/4)*512 + (r%32)*16 + ((r/32)%4)*4 + b%4
+ *                    (ld a multiple of 128; rows padded to 128).
+ *  MGQ_NV16_UE4M3    ue4m3 scale per 16 elements, same tiling with b the
+ *                    16-element block (ld a multiple of 64 elements);
+ *                    plus one float32 global scale s_g per tensor (weights:
+ *                    per expert) in tensor_scale; value = e2m1 * sc / s_g.
+ *  MGQ_BLK_1x128_F32 float32 scale_inv per 128 elements of a row, stored
+ *                    k-block major: scale_inv[b * rows_cap + r].
+ *  MGQ_BLK_128x128_F32 float32 scale_inv per 128x128 tile of each expert's
+ *                    weight: scale_inv[(g * (N/128) + n/128) * (K/128) + k/128].
+ *  MGQ_TENSOR_F32    one float32 scale s per tensor (weights: per expert),
+ *                    code = cast(x * s), value = code / s.
+ * Column-wise ("col") copies hold the transposed matrix quantised with its
+ * own blocks along the old row dimension (transpose identity of [BLOCK]).
+ */
+#ifndef MGQ_H
+#define MGQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MGQ_OK = 0,
+  MGQ_ERR_INVALID_ARG = 1,   /* bad pointer, size, alignment or combination */
+  MGQ_ERR_UNSUPPORTED = 2,   /* valid but not implemented (format / mode)   */
+  MGQ_ERR_CUDA = 3,          /* a CUDA runtime or driver call failed        */
+  MGQ_ERR_TIMEOUT = 4,       /* device: a pipeline wait gave up             */
+  MGQ_ERR_DEVICE_INDEX = 5   /* device: an expert index out of range        */
+} mgq_status;
+
+typedef enum { MGQ_E4M3 = 0, MGQ_E5M2 = 1, MGQ_E2M1 = 2 } mgq_dtype;
+
+typedef enum {
+  MGQ_MX32_E8M0 = 0,
+  MGQ_NV16_UE4M3 = 1,
+  MGQ_BLK_1x128_F32 = 2,
+  MGQ_BLK_128x128_F32 = 3,
+  MGQ_TENSOR_F32 = 4
+} mgq_scaling;
+
+/* Exponent of an E8M0 block scale. RCEIL: the smallest power of two that
+ * keeps the block amax at or below the format's largest value (no element
+ * saturates). FLOOR: floor(log2 amax) - emax (OCP MX v1.0). */
+typedef enum { MGQ_E8M0_RCEIL = 0, MGQ_E8M0_FLOOR = 1 } mgq_e8m0_mode;
+
+typedef enum { MGQ_OUT_BF16 = 0, MGQ_OUT_F32 = 1 } mgq_out_dtype;
+
+/* Quantised output buffers of one layout (device pointers). */
+typedef struct {
+  void* data;     /* codes                                  */
+  void* scale;    /* block scales (NULL for MGQ_TENSOR_F32) */
+} mgq_qbuf;
+
+/* How to quantise, and where to. */
+typedef struct {
+  int dtype;                 /* mgq_dtype                                       */
+  int scaling;               /* mgq_scaling                                     */
+  int e8m0_mode;             /* mgq_e8m0_mode (MX only)                         */
+  mgq_qbuf row;              /* row-wise output; row.data required              */
+  mgq_qbuf col;              /* column-wise (transposed) output; col.data NULL = none */
+  const float* tensor_scale; /* device: s (MGQ_TENSOR_F32) or s_g (NVFP4); per group */
+  float* amax_out;           /* device, optional: atomic max of |x| per group   */
+} mgq_qdesc;
+
+/* A quantised GEMM operand (device pointers). */
+typedef struct {
+  const void* data;          /* codes, row-major, row pitch `ld` elements      */
+  const void* scale;         /* block scales, or device float s per tensor/group */
+  int64_t ld;                /* row pitch in elements                          */
+  int dtype;                 /* mgq_dtype                                       */
+} mgq_operand;
+
+/* ---- status --------------------------------------------------------------- */
+
+const char* mgq_status_string(int status);
+int mgq_version(void);
+
+/* Reads and clears the device error word of the current device after
+ * synchronising `stream`. *device_status receives MGQ_OK or the first device
+ * error recorded since the last call. */
+int mgq_get_error(void* stream, int* device_status);
+
+/* ---- a2: permute + quantise (dispatch) -------------------------------------
+ * [MOE-FP8] grouped GEMM over experts with padded expert inputs; [AO-MOE]
+ * dynamic quantisation before the scaled grouped mm; [BLOCK] padding to the
+ * block is required.
+ *
+ * Routes T tokens to experts and writes each token's row to its k expert
+ * groups. Group e occupies rows [offsets[e], offsets[e]+counts[e]) in token
+ * order (stable), padded with zero rows (codes 0, scales 0) up to a multiple
+ * of `align`: offsets[e+1] = offsets[e] + roundup(counts[e], align).
+ *  x_bf16      device [T, H] bf16
+ *  topk_idx    device [T, k] int32, distinct experts per token in [0, E)
+ *              (out of range: the entry is skipped, MGQ_ERR_DEVICE_INDEX set)
+ *  q           quantisation of the permuted rows (row: [R_cap, H]; col:
+ *              [H, R_cap]); NULL = no quantised output
+ *  out_bf16    device [R_cap, H] bf16 permuted copy, or NULL
+ *  row_id_map  device [T, k] int32: destination row of (t, j)
+ *  src_row     device [R_cap] int32: t*k + j of the row, -1 for padding
+ *  offsets     device [E+1] int32; counts device [E] int32
+ *  workspace   device scratch of mgq_permute_workspace_size() bytes
+ * Requires: align a multiple of 128 when a GEMM consumes the result (32 is
+ * accepted for quantise-only use), H a multiple of 128,
+ * R_cap >= T*k + E*(align-1) rounded up to 128. */
+size_t mgq_permute_workspace_size(int T, int k, int E);
+int mgq_moe_permute(const void* x_bf16, int T, int H, const int32_t* topk_idx, int k,
+                    int E, int align, const mgq_qdesc* q, void* out_bf16, int64_t R_cap,
+                    int32_t* row_id_map, int32_t* src_row, int32_t* offsets,
+                    int32_t* counts, void* workspace, size_t ws_bytes, void* stream);
+
+/* ---- a3/a4: block quantise, row-wise and column-wise -----------------------
+ * [BLOCK] 1x128 forward / 128x1 backward with the transpose identity;
+ * [GROUPED] row-wise and column-wise data and scales of one grouped weight.
+ *  x_bf16  device [G, M, K] bf16 (G groups, e.g. experts)
+ *  q->row  [G, M, K] codes (+ scales); q->col [G, K, M] codes (+ scales)
+ *  per-tensor / NVFP4 modes read one scale per group from q->tensor_scale.
+ * Requires M and K multiples of 128. */
+int mgq_block_quantize(const void* x_bf16, int64_t G, int64_t M, int64_t K,
+                       const mgq_qdesc* q, void* stream);
+
+/* ---- a5/a9/a11: grouped GEMMs ------------------------------------------------
+ * [MOE-FP8] one grouped GEMM for all experts; [AO-MOE] scaled grouped mm;
+ * [GROUPED] single grouped weight [E, N, K], gradient accumulation fusion.
+ * tcgen05 block-scaled MMA with float32 accumulation in tensor memory.
+ *
+ * fwd:   Y[r, :]  = sum_k A[r, k] W_e[:, k]  for rows r of group e
+ *        A [R_cap, K] (ld >= K), W [E, N, K], Y [R_cap, N] (out_dtype)
+ * dgrad: dA[r, :] = sum_n dY[r, n] W_e[n, :]: pass dY [R_cap, N] and the
+ *        column-wise weight copy Wcol [E, K, N]; dA [R_cap, K]
+ * wgrad: dW_e = beta * dW_e + sum_{r in e} dY[r, :]^T A[r, :]: pass the
+ *        column-wise copies dYcol [N, R_cap] and Acol [K, R_cap];
+ *        dW [E, N, K] (out_dtype); an empty group gives zeros (beta 0) or
+ *        leaves dW_e unchanged (beta 1).
+ * scaling: MGQ_MX32_E8M0 (e4m3/e5m2 codes with blocked E8M0 scales) or
+ *        MGQ_TENSOR_F32 (scale = device float s: one for A / dY, E for the
+ *        weight; the product is multiplied by 1/(s_a s_b)).
+ * Requires offsets[e] multiples of 128, N a multiple of 256 (fwd/dgrad) or
+ * 128, K a multiple of 128, 16-byte aligned pointers. */
+int mgq_grouped_gemm_fwd(const mgq_operand* A, const mgq_operand* W, int scaling,
+                         const int32_t* offsets, int E, int64_t R_cap, int64_t N,
+                         int64_t K, void* Y, int out_dtype, void* stream);
+int mgq_grouped_gemm_dgrad(const mgq_operand* dY, const mgq_operand* Wcol, int scaling,
+                           const int32_t* offsets, int E, int64_t R_cap, int64_t N,
+                           int64_t K, void* dA, int out_dtype, void* stream);
+int mgq_grouped_gemm_wgrad(const mgq_operand* dYcol, const mgq_operand* Acol, int scaling,
+                           const int32_t* offsets, int E, int64_t R_cap, int64_t N,
+                           int64_t K, float beta, void* dW, int out_dtype, void* stream);
+
+/* ---- a6/a10: SwiGLU and its derivative, fused with quantisation -------------
+ * h = silu(g) * u, g = gu[:, :F], u = gu[:, F:2F] (float32, rounded to bf16,
+ * then quantised). dG = dh u s (1 + g (1 - s)), dU = dh silu(g), s = sigmoid(g),
+ * rounded to bf16 then quantised ([dG | dU] is one [R_cap, 2F] matrix).
+ * Rows [0, offsets[E]) are processed. */
+int mgq_swiglu_quantize(const void* gu_bf16, int64_t R_cap, int F, const int32_t* offsets,
+                        int E, const mgq_qdesc* q, void* h_bf16, void* stream);
+int mgq_dswiglu_quantize(const void* dh_bf16, const void* gu_bf16, int64_t R_cap, int F,
+                         const int32_t* offsets, int E, const mgq_qdesc* q,
+                         void* dgu_bf16, void* stream);
+
+/* ---- a7: unpermute / combine -------------------------------------------------
+ * out[t] = sum_j probs[t, j] * Y[row_id_map[t, j]] (float32, j ascending) -> bf16. */
+int mgq_moe_unpermute(const void* y_bf16, const int32_t* row_id_map, const float* probs,
+                      int T, int k, int H, void* out_bf16, void* stream);
+
+/* ---- a8: unpermute backward, fused with quantisation of dY -----------------
+ * dY[row(t, j)] = float32(probs[t, j] * dout[t]) quantised into q (row and
+ * col), filler rows zero; dprobs[t, j] = <dout[t], Y[row(t, j)]> (float32). */
+int mgq_moe_unpermute_bwd(const void* dout_bf16, const void* y_bf16,
+                          const int32_t* row_id_map, const int32_t* src_row,
+                          const float* probs, int T, int k, int H, int64_t R_cap,
+                          const int32_t* offsets, int E, const mgq_qdesc* q,
+                          float* dprobs, void* stream);
+
+/* ---- a12: permute backward ----------------------------------------------------
+ * dX[t] = sum_j dA[row_id_map[t, j]] (float32, j ascending) -> bf16. */
+int mgq_moe_permute_bwd(const void* da_bf16, const int32_t* row_id_map, int T, int k,
+                        int H, void* dx_bf16, void* stream);
+
+/* ---- a13: delayed scaling ------------------------------------------------------
+ * [MOE-FP8] --fp8-amax-history-len 1024 --fp8-amax-compute-algo max.
+ * For each of n roles: history[i*L + head] = amax[i]; m = max(history[i*L ..]);
+ * if m > 0 and finite, scale[i] = fmax / m (float32); amax[i] is reset to 0.
+ * head (device int32) advances by one (mod L) after all roles. */
+int mgq_amax_history_update(float* history, int32_t* head, float* amax, float* scale,
+                            int n, int L, float fmax, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MGQ_H */

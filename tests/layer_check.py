@@ -1,0 +1,148 @@
+"""Helpers shared by the GPU parity tests, smoke() and bench: run pieces of the
+CUDA path through the C ABI and compare them with the CPU oracle on the same
+inputs.
+
+Tolerances (written here, used by every GPU test):
+* codes, scales and index arrays: bit-exact;
+* grouped GEMM outputs: relative Frobenius error <= 2e-3 against the oracle's
+  float64 result on the same quantised inputs, rounded to the output dtype
+  (bf16 rounding alone costs about 1.7e-3 of that budget); float32 outputs
+  <= 1e-5 against the unrounded float64 result;
+* elementwise float steps (SwiGLU, combine, ...): relative Frobenius <= 1e-3
+  and at most 1 bf16 ulp on >= 99.99% of the elements.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import formats as OF
+from oracle import gemm as OG
+from oracle import layer as OL
+from oracle import quant as OQ
+from oracle import routing as OR
+
+GEMM_TOL_BF16 = 2e-3
+GEMM_TOL_F32 = 1e-5
+ELEM_TOL = 1e-3
+
+
+def untile_mx_scales(buf, rows: int, ld: int, block: int = 32) -> np.ndarray:
+    """The 128x4-tiled scale bytes of a [rows, ld] matrix -> natural
+    [rows, ld/block] (layout documented in include/mgq.h)."""
+    b = np.asarray(buf).reshape(-1)
+    kb = ld // block
+    rp = (rows + 127) // 128 * 128
+    t = b[: rp * kb].reshape(rp // 128, kb // 4, 32, 4, 4)
+    return t.transpose(0, 3, 2, 1, 4).reshape(rp, kb)[:rows]
+
+
+def tile_mx_scales(nat: np.ndarray) -> np.ndarray:
+    """Inverse of untile_mx_scales (rows padded to 128 with zero bytes)."""
+    rows, kb = nat.shape
+    rp = (rows + 127) // 128 * 128
+    full = np.zeros((rp, kb), dtype=np.uint8)
+    full[:rows] = nat
+    t = full.reshape(rp // 128, 4, 32, kb // 4, 4)      # [rt, q, i, kg, bb]
+    return np.ascontiguousarray(t.transpose(0, 3, 2, 1, 4)).reshape(-1)
+
+
+def bf16_np(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def u8_np(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().numpy()
+
+
+def rel_fro(ref, got) -> float:
+    return OG.rel_frobenius(ref, got)
+
+
+def ulp_bf16(x: np.ndarray) -> np.ndarray:
+    a = np.abs(x)
+    _, e = np.frexp(np.where(a > 0, a, 1.0))
+    return np.exp2(np.maximum(e - 8, -133).astype(np.float64))
+
+
+def check_elementwise(ref: np.ndarray, got: np.ndarray, what: str):
+    """ref: oracle float64 (unrounded); got: GPU bf16 values (float64).
+    Compared with the oracle rounded to bf16: at most 1 bf16 ulp apart on
+    >= 99.99% of the elements and relative Frobenius <= 1e-3."""
+    refr = OF.round_to_bf16(ref)
+    rf = rel_fro(refr, got)
+    ulp = np.maximum(ulp_bf16(refr), ulp_bf16(got))
+    bad = np.abs(got - refr) > ulp * 1.0000001
+    frac = float(np.mean(bad)) if bad.size else 0.0
+    assert rf <= ELEM_TOL, f"{what}: rel Frobenius {rf:.3e}"
+    assert frac <= 1e-4, f"{what}: {frac:.2e} of elements beyond 1 bf16 ulp"
+    return rf
+
+
+def run_fwd_and_check(w, device, check_all: bool = True) -> dict:
+    """One MXFP8 forward of workload ``w`` through ExpertLayer, every step
+    compared with the oracle. Returns the measured errors."""
+    from fp8_grouped_gemm_gb300 import layer as L
+    from fp8_grouped_gemm_gb300 import workloads as W
+    from fp8_grouped_gemm_gb300 import mgq
+
+    x = W.make_activations(w)
+    w1, w2 = W.make_weights(w)
+    idx, probs = W.make_routing(w)
+    lay = L.ExpertLayer(w, device, recipe="mxfp8", keep_bf16=True)
+    xd, w1d, w2d = x.to(device), w1.to(device), w2.to(device)
+    idxd = torch.from_numpy(idx).to(device)
+    pd = torch.from_numpy(probs).to(device)
+    lay.quantize_weights(w1d, w2d)
+    lay.forward(xd, idxd, pd)
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    res = {}
+    E, H, F = w.E, w.H, w.F
+    # routing: bit-exact
+    rim, src, off, cnt = OR.permute_indices(idx, E, L.ALIGN)
+    Rp = int(off[-1])
+    assert np.array_equal(lay.offsets.cpu().numpy(), off)
+    assert np.array_equal(lay.counts.cpu().numpy(), cnt)
+    assert np.array_equal(lay.row_id_map.cpu().numpy(), rim)
+    assert np.array_equal(lay.src_row.cpu().numpy()[:Rp], src)
+    # permute + quantise: bit-exact codes and scales (filler rows zero)
+    xf = W.bf16_to_f64(x)
+    cx, sx = OQ.quantize_mx(xf, "e4m3")
+    want_c = OR.permute_rows(cx, rim, Rp)
+    want_s = OR.permute_rows(sx, rim, Rp)
+    assert np.array_equal(u8_np(lay.xq)[:Rp], want_c)
+    assert np.array_equal(untile_mx_scales(u8_np(lay.xs), lay.R_cap, H)[:Rp], want_s)
+    # weights: bit-exact
+    cw1, sw1 = OQ.quantize_mx(W.bf16_to_f64(w1).reshape(E * 2 * F, H), "e4m3")
+    cw2, sw2 = OQ.quantize_mx(W.bf16_to_f64(w2).reshape(E * H, F), "e4m3")
+    assert np.array_equal(u8_np(lay.w1q).reshape(E * 2 * F, H), cw1)
+    assert np.array_equal(untile_mx_scales(u8_np(lay.w1s), E * 2 * F, H), sw1)
+    assert np.array_equal(u8_np(lay.w2q).reshape(E * H, F), cw2)
+    assert np.array_equal(untile_mx_scales(u8_np(lay.w2s), E * H, F), sw2)
+    # gate/up GEMM on the identical quantised inputs
+    a_deq = OQ.dequantize_mx(want_c, want_s)
+    w1_deq = OQ.dequantize_mx(cw1, sw1).reshape(E, 2 * F, H)
+    gu_ref = OG.grouped_gemm_fwd(a_deq, w1_deq, off)
+    gu = bf16_np(lay.gu)[:Rp]
+    res["gemm1_relfro"] = rel_fro(OF.round_to_bf16(gu_ref), gu)
+    res["gemm1_sqnr_vs_bf16"] = OG.sqnr_db(
+        OG.grouped_gemm_fwd(OR.permute_rows(xf, rim, Rp), W.bf16_to_f64(w1), off), gu)
+    assert res["gemm1_relfro"] <= GEMM_TOL_BF16, res
+    # SwiGLU on the GPU's gate/up output; codes from the GPU-materialised h
+    h_ref = OL.swiglu(gu, F)
+    h_gpu = bf16_np(lay.h_bf16)[:Rp]
+    res["swiglu_relfro"] = check_elementwise(h_ref, h_gpu, "swiglu")
+    ch, sh = OQ.quantize_mx(h_gpu, "e4m3")
+    assert np.array_equal(u8_np(lay.hq)[:Rp], ch)
+    assert np.array_equal(untile_mx_scales(u8_np(lay.hs), lay.R_cap, F)[:Rp], sh)
+    # down GEMM
+    w2_deq = OQ.dequantize_mx(cw2, sw2).reshape(E, H, F)
+    y_ref = OG.grouped_gemm_fwd(OQ.dequantize_mx(ch, sh), w2_deq, off)
+    y = bf16_np(lay.y)[:Rp]
+    res["gemm2_relfro"] = rel_fro(OF.round_to_bf16(y_ref), y)
+    assert res["gemm2_relfro"] <= GEMM_TOL_BF16, res
+    # unpermute on the GPU's y
+    out_ref = OR.unpermute(y, rim, probs)
+    res["unpermute_relfro"] = check_elementwise(out_ref, bf16_np(lay.out), "unpermute")
+    return res

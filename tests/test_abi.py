@@ -1,0 +1,87 @@
+"""The C-ABI library loads and exports every symbol include/mgq.h declares;
+host-side argument validation answers before anything is launched (CPU only:
+no compute call is made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mgq.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mgq_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fp8_grouped_gemm_gb300 import _build, mgq
+    if not os.path.exists(mgq.LIB_PATH):
+        _build.build()
+    return mgq.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from fp8_grouped_gemm_gb300 import mgq
+    names = _declared()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(mgq.EXPORTS) | {n for n in names if n.startswith("mgq_")}
+    assert set(mgq.EXPORTS) <= set(names)
+
+
+def test_status_strings(lib):
+    from fp8_grouped_gemm_gb300 import mgq
+    assert mgq.status_string(mgq.OK) == "ok"
+    assert "invalid" in mgq.status_string(mgq.ERR_INVALID_ARG)
+    assert lib.mgq_version() >= 1
+
+
+def test_workspace_size(lib):
+    from fp8_grouped_gemm_gb300 import mgq
+    assert mgq.permute_workspace_size(16384, 2, 8) == 32 * 8 * 4
+    assert mgq.permute_workspace_size(-1, 2, 8) == 0
+
+
+def test_host_validation_rejects_bad_arguments(lib):
+    """Each call returns MGQ_ERR_INVALID_ARG (or UNSUPPORTED) before touching
+    the GPU when its arguments are wrong."""
+    from fp8_grouped_gemm_gb300 import mgq
+    INV = mgq.ERR_INVALID_ARG
+    # negative token count, misaligned H, k > 8, missing outputs
+    assert lib.mgq_moe_permute(None, -1, 128, None, 2, 8, 128, None, None, 1024, None, None, None, None,
+                               None, 0, None) == INV
+    assert lib.mgq_moe_permute(None, 4, 100, None, 2, 8, 128, None, None, 1024, None, None, None, None,
+                               None, 0, None) == INV
+    assert lib.mgq_moe_permute(None, 4, 128, None, 9, 16, 128, None, None, 1024, None, None, None, None,
+                               None, 0, None) == INV
+    # GEMM: null operands, then an unsupported format
+    a = mgq.Operand(None, None, 128, mgq.E4M3)
+    assert lib.mgq_grouped_gemm_fwd(ctypes.byref(a), ctypes.byref(a), mgq.MX32_E8M0, None, 4, 128, 256, 128,
+                                    None, 0, None) == INV
+    b = mgq.Operand(16, 16, 128, 7)
+    assert lib.mgq_grouped_gemm_fwd(ctypes.byref(b), ctypes.byref(b), mgq.MX32_E8M0, None, 4, 128, 256, 128,
+                                    None, 0, None) == mgq.ERR_UNSUPPORTED
+    # GEMM shapes: N not a multiple of 256 / K not of 128 / misaligned output
+    c = mgq.Operand(16, 16, 128, mgq.E4M3)
+    assert lib.mgq_grouped_gemm_fwd(ctypes.byref(c), ctypes.byref(c), mgq.MX32_E8M0, 16, 4, 128, 200, 128,
+                                    32, 0, None) == INV
+    assert lib.mgq_grouped_gemm_fwd(ctypes.byref(c), ctypes.byref(c), mgq.MX32_E8M0, 16, 4, 128, 256, 100,
+                                    32, 0, None) == INV
+    assert lib.mgq_grouped_gemm_fwd(ctypes.byref(c), ctypes.byref(c), mgq.MX32_E8M0, 16, 4, 128, 256, 128,
+                                    33, 0, None) == INV
+    # beta != 0 only for float32 wgrad
+    assert lib.mgq_grouped_gemm_wgrad(ctypes.byref(c), ctypes.byref(c), mgq.MX32_E8M0, 16, 4, 128, 128, 256,
+                                      ctypes.c_float(1.0), 32, mgq.OUT_BF16, None) == INV
+    # quantiser: K not a multiple of 128; unsupported scaling
+    q = mgq.qdesc(mgq.E4M3, mgq.MX32_E8M0, 16, 16)
+    assert lib.mgq_block_quantize(16, 1, 128, 100, ctypes.byref(q), None) == INV
+    q2 = mgq.qdesc(mgq.E4M3, 9, 16, 16)
+    assert lib.mgq_block_quantize(16, 1, 128, 128, ctypes.byref(q2), None) == mgq.ERR_UNSUPPORTED
+    assert lib.mgq_amax_history_update(None, None, None, None, 1, 1, ctypes.c_float(448.0), None) == INV
+    assert lib.mgq_get_error(None, None) == INV

@@ -1,0 +1,504 @@
+"""Parity of each CUDA kernel with the CPU oracle, through the C ABI.
+
+Sizes span several 128x256 GEMM tiles, ragged token counts (tails of the
+per-warp and per-chunk loops), empty expert groups, k = 1 and k = 8, and
+multi-slice rows. Tolerances are those of tests/layer_check.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import formats as OF
+from oracle import gemm as OG
+from oracle import layer as OL
+from oracle import quant as OQ
+from oracle import routing as OR
+from tests.layer_check import (GEMM_TOL_BF16, GEMM_TOL_F32, bf16_np, check_elementwise, rel_fro,
+                               tile_mx_scales, u8_np, untile_mx_scales)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def mgq():
+    from fp8_grouped_gemm_gb300 import mgq as m
+    m.load()
+    return m
+
+
+def _routing(rng, T, E, k, empty=()):
+    allowed = np.array([e for e in range(E) if e not in empty])
+    idx = np.stack([rng.choice(allowed, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    return idx.reshape(T, k)
+
+
+def _bf16(rng, shape, std=1.0):
+    x = torch.from_numpy((rng.standard_normal(shape) * std).astype(np.float32)).to(torch.bfloat16)
+    return x
+
+
+# ---------------------------------------------------------------------------- permute
+
+PERMUTE_CASES = [
+    # T, E, k, H, align, empty experts
+    (1024, 4, 2, 256, 128, ()),
+    (1001, 6, 2, 384, 128, (2,)),
+    (300, 8, 1, 5120, 128, (0, 5)),
+    (777, 16, 8, 128, 32, (3,)),
+    (5, 4, 4, 1024, 128, ()),
+    (2500, 128, 8, 256, 128, ()),
+]
+
+
+@pytest.mark.parametrize("case", PERMUTE_CASES, ids=lambda c: f"T{c[0]}E{c[1]}k{c[2]}H{c[3]}a{c[4]}")
+@pytest.mark.parametrize("mode", ["mx_e4m3", "mx_e5m2", "tensor_e4m3", "blk_e4m3"])
+def test_permute_quantize(mgq, case, mode):
+    T, E, k, H, align, empty = case
+    rng = np.random.default_rng(T * 7 + E)
+    idx = _routing(rng, T, E, k, empty)
+    x = _bf16(rng, (T, H))
+    if mode.startswith("tensor"):
+        x[:, 3] *= 50                                      # an outlier channel
+    R = mgq.r_cap(T, k, E, align)
+    dev = torch.device(DEV)
+    xd, idxd = x.to(dev), torch.from_numpy(idx).to(dev)
+    rim = torch.full((T, k), -7, dtype=torch.int32, device=dev)
+    src = torch.full((R,), -7, dtype=torch.int32, device=dev)
+    off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    cnt = torch.empty(E, dtype=torch.int32, device=dev)
+    ws = torch.empty(mgq.permute_workspace_size(T, k, E), dtype=torch.uint8, device=dev)
+    codes = torch.full((R, H), 0xAB, dtype=torch.uint8, device=dev)
+    fmt = "e5m2" if "e5m2" in mode else "e4m3"
+    dt = mgq.E5M2 if fmt == "e5m2" else mgq.E4M3
+    xf = bf16_np(x)
+    if mode.startswith("mx"):
+        sc = torch.full((mgq.mx_scale_bytes(R, H),), 0xCD, dtype=torch.uint8, device=dev)
+        q = mgq.qdesc(dt, mgq.MX32_E8M0, codes, sc)
+    elif mode.startswith("blk"):
+        sc = torch.full((H // 128, R), -1.0, dtype=torch.float32, device=dev)
+        q = mgq.qdesc(dt, mgq.BLK_1x128_F32, codes, sc)
+    else:
+        s = torch.tensor([0.37], dtype=torch.float32, device=dev)
+        amax = torch.zeros(1, dtype=torch.float32, device=dev)
+        col = torch.full((H, R), 0xAB, dtype=torch.uint8, device=dev)
+        q = mgq.qdesc(dt, mgq.TENSOR_F32, codes, None, col, None, s, amax)
+    mgq.moe_permute(xd, idxd, E, align, q, R, rim, src, off, cnt, ws)
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    w_rim, w_src, w_off, w_cnt = OR.permute_indices(idx, E, align)
+    Rp = int(w_off[-1])
+    assert np.array_equal(off.cpu().numpy(), w_off)
+    assert np.array_equal(cnt.cpu().numpy(), w_cnt)
+    assert np.array_equal(rim.cpu().numpy(), w_rim)
+    assert np.array_equal(src.cpu().numpy()[:Rp], w_src)
+    if mode.startswith("mx"):
+        c, s = OQ.quantize_mx(xf, fmt)
+        assert np.array_equal(u8_np(codes)[:Rp], OR.permute_rows(c, w_rim, Rp))
+        assert np.array_equal(untile_mx_scales(u8_np(sc), R, H)[:Rp], OR.permute_rows(s, w_rim, Rp))
+    elif mode.startswith("blk"):
+        c, si = OQ.quantize_block_1x128(xf, fmt)
+        assert np.array_equal(u8_np(codes)[:Rp], OR.permute_rows(c, w_rim, Rp))
+        got = sc.cpu().numpy().T[:Rp]
+        assert np.array_equal(got, OR.permute_rows(si, w_rim, Rp, fill=0.0))
+    else:
+        c, am = OQ.quantize_tensor(xf, np.float32(0.37), fmt)
+        want = OR.permute_rows(c, w_rim, Rp)
+        assert np.array_equal(u8_np(codes)[:Rp], want)
+        assert np.array_equal(u8_np(col)[:, :Rp], want.T)
+        assert float(amax.item()) == am
+
+
+def test_permute_bad_expert_index_is_reported(mgq):
+    dev = torch.device(DEV)
+    T, E, k, H = 64, 4, 2, 128
+    idx = np.tile(np.array([[0, 1]], dtype=np.int32), (T, 1))
+    idx[5, 1] = 9                       # out of range: skipped and reported
+    R = mgq.r_cap(T, k, E, 128)
+    bufs = dict(rim=torch.empty(T, k, dtype=torch.int32, device=dev),
+                src=torch.empty(R, dtype=torch.int32, device=dev),
+                off=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                cnt=torch.empty(E, dtype=torch.int32, device=dev))
+    codes = torch.empty(R, H, dtype=torch.uint8, device=dev)
+    sc = torch.empty(mgq.mx_scale_bytes(R, H), dtype=torch.uint8, device=dev)
+    ws = torch.empty(mgq.permute_workspace_size(T, k, E), dtype=torch.uint8, device=dev)
+    mgq.moe_permute(_bf16(np.random.default_rng(0), (T, H)).to(dev), torch.from_numpy(idx).to(dev), E, 128,
+                    mgq.qdesc(mgq.E4M3, mgq.MX32_E8M0, codes, sc), R, bufs["rim"], bufs["src"], bufs["off"],
+                    bufs["cnt"], ws)
+    assert mgq.get_error() == mgq.ERR_DEVICE_INDEX
+    assert mgq.get_error() == mgq.OK                 # read and cleared
+    assert bufs["rim"][5, 1].item() == -1
+    assert bufs["cnt"].cpu().tolist() == [64, 63, 0, 0]
+
+
+# ---------------------------------------------------------------------------- GEMM
+
+def _mx_operand(rng, rows, K, fmt="e4m3", small=False, sc_lo=120, sc_hi=134):
+    f = OF.FORMATS[fmt]
+    if small:
+        sc_lo, sc_hi = 125, 129          # keeps every partial sum exact in float32
+        codes = rng.choice(np.array([0x00, 0x38, 0xB8] if fmt == "e4m3" else [0x00, 0x3C, 0xBC]),
+                           size=(rows, K)).astype(np.uint8)
+    else:
+        codes = rng.choice(f.pos_codes[:-1], size=(rows, K)).astype(np.uint8)
+        codes |= (rng.integers(0, 2, (rows, K)) * f.sign_bit).astype(np.uint8)
+    sc = rng.integers(sc_lo, sc_hi, size=(rows, K // 32)).astype(np.uint8)
+    return codes, sc
+
+
+def _to_dev(a, dev):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+_KEEP = []   # device buffers referenced by raw pointers in Operand structs
+
+
+def _op(mgq, codes, scale, ld, dtype, dev):
+    """Operand over fresh device copies; the copies stay alive (the struct
+    only holds their addresses)."""
+    c, s = _to_dev(codes, dev), _to_dev(scale, dev)
+    _KEEP.append((c, s))
+    if len(_KEEP) > 64:
+        del _KEEP[:32]
+    return mgq.operand(c, s, ld, dtype)
+
+
+GEMM_GROUPS = [
+    [0, 128, 128, 384, 512],          # E=4, one empty group
+    [0, 256],                         # one expert
+    [0, 128, 256, 384, 512, 640, 768, 896, 1024, 1152],
+]
+
+
+@pytest.mark.parametrize("offs", GEMM_GROUPS, ids=lambda o: f"E{len(o) - 1}")
+@pytest.mark.parametrize("small", [True, False], ids=["exact", "random"])
+def test_gemm_fwd_mx(mgq, offs, small):
+    rng = np.random.default_rng(len(offs) + small)
+    dev = torch.device(DEV)
+    E = len(offs) - 1
+    N, K = 512, 384
+    Rp = offs[-1]
+    R_cap = Rp + 256                   # spare rows stay untouched
+    ac, asc = _mx_operand(rng, R_cap, K, small=small)
+    wc, wsc = _mx_operand(rng, E * N, K, small=small)
+    off = np.array(offs, dtype=np.int32)
+    out_dtype = mgq.OUT_F32 if small else mgq.OUT_BF16
+    Y = torch.full((R_cap, N), float("nan"), dtype=torch.float32 if small else torch.bfloat16, device=dev)
+    A = _op(mgq, ac, tile_mx_scales(asc), K, mgq.E4M3, dev)
+    Wo = _op(mgq, wc, tile_mx_scales(wsc), K, mgq.E4M3, dev)
+    tens = [torch.from_numpy(off).to(dev)]
+    mgq.grouped_gemm_fwd(A, Wo, mgq.MX32_E8M0, tens[0], E, R_cap, N, K, Y, out_dtype)
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    ref = OG.grouped_gemm_fwd(OQ.dequantize_mx(ac, asc)[:Rp], OQ.dequantize_mx(wc, wsc).reshape(E, N, K), off)
+    got = Y.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.isnan(got[Rp:]))                 # rows beyond the groups untouched
+    if small:
+        np.testing.assert_array_equal(got[:Rp], ref)  # every sum exact in float32
+    else:
+        assert rel_fro(OF.round_to_bf16(ref), got[:Rp]) <= GEMM_TOL_BF16
+
+
+@pytest.mark.parametrize("fmts", [("e4m3", "e4m3"), ("e5m2", "e4m3")])
+def test_gemm_fwd_tensor_scale(mgq, fmts):
+    rng = np.random.default_rng(11)
+    dev = torch.device(DEV)
+    offs = [0, 256, 256, 640]
+    E, N, K = 3, 768, 256
+    Rp = offs[-1]
+    fa, fw = OF.FORMATS[fmts[0]], OF.FORMATS[fmts[1]]
+    ac = (rng.choice(fa.pos_codes[:-1], size=(Rp, K)) | (rng.integers(0, 2, (Rp, K)) * fa.sign_bit)).astype(np.uint8)
+    wc = (rng.choice(fw.pos_codes[:-1], size=(E * N, K)) | (rng.integers(0, 2, (E * N, K)) * fw.sign_bit)).astype(np.uint8)
+    sa = np.array([3.5], dtype=np.float32)
+    sw = np.array([0.75, 12.0, 0.01], dtype=np.float32)
+    Y = torch.empty(Rp, N, dtype=torch.bfloat16, device=dev)
+    da = mgq.E5M2 if fmts[0] == "e5m2" else mgq.E4M3
+    A = _op(mgq, ac, sa, K, da, dev)
+    Wo = _op(mgq, wc, sw, K, mgq.E4M3, dev)
+    offd = torch.tensor(offs, dtype=torch.int32, device=dev)
+    mgq.grouped_gemm_fwd(A, Wo, mgq.TENSOR_F32, offd, E, Rp, N, K, Y)
+    torch.cuda.synchronize()
+    ref = OG.grouped_gemm_fwd(OQ.dequantize_tensor(ac, sa[0], fmts[0]),
+                              np.stack([OQ.dequantize_tensor(wc[e * N:(e + 1) * N], sw[e], fmts[1])
+                                        for e in range(E)]), np.array(offs))
+    assert rel_fro(OF.round_to_bf16(ref), bf16_np(Y)) <= GEMM_TOL_BF16
+
+
+@pytest.mark.parametrize("scaling", ["tensor", "mx"])
+def test_gemm_dgrad_and_wgrad(mgq, scaling):
+    """dgrad on the column-wise weight copy and wgrad on the column-wise
+    copies of dY and A, with an empty group (wgrad writes zeros, or keeps the
+    accumulator with beta = 1)."""
+    rng = np.random.default_rng(21)
+    dev = torch.device(DEV)
+    offs = np.array([0, 128, 128, 512, 640], dtype=np.int32)
+    E, N, K = 4, 512, 256            # forward W_e is [N, K]
+    Rp = int(offs[-1])
+    offd = torch.from_numpy(offs).to(dev)
+    if scaling == "tensor":
+        f5, f4 = OF.E5M2, OF.E4M3
+        dyc = (rng.choice(f5.pos_codes[:-1], size=(Rp, N)) | (rng.integers(0, 2, (Rp, N)) * 0x80)).astype(np.uint8)
+        wc = (rng.choice(f4.pos_codes[:-1], size=(E, N, K)) | (rng.integers(0, 2, (E, N, K)) * 0x80)).astype(np.uint8)
+        ac = (rng.choice(f4.pos_codes[:-1], size=(Rp, K)) | (rng.integers(0, 2, (Rp, K)) * 0x80)).astype(np.uint8)
+        s_dy = np.array([1000.0], dtype=np.float32)
+        s_w = np.array([2.0, 0.5, 8.0, 1.0], dtype=np.float32)
+        s_a = np.array([4.0], dtype=np.float32)
+        dy_deq = OQ.dequantize_tensor(dyc, s_dy[0], "e5m2")
+        w_deq = np.stack([OQ.dequantize_tensor(wc[e], s_w[e]) for e in range(E)])
+        a_deq = OQ.dequantize_tensor(ac, s_a[0])
+        wcol = np.ascontiguousarray(wc.transpose(0, 2, 1))            # [E, K, N]
+        dgrad_B = _op(mgq, wcol, s_w, N, mgq.E4M3, dev)
+        dgrad_A = _op(mgq, dyc, s_dy, N, mgq.E5M2, dev)
+        wg_A = _op(mgq, np.ascontiguousarray(dyc.T), s_dy, Rp, mgq.E5M2, dev)
+        wg_B = _op(mgq, np.ascontiguousarray(ac.T), s_a, Rp, mgq.E4M3, dev)
+        sc = mgq.TENSOR_F32
+    else:
+        # dgrad: dY row-wise (blocks along N), W column-wise (blocks along N)
+        dyc, dys = _mx_operand(rng, Rp, N, "e5m2")
+        wcol, wcols = _mx_operand(rng, E * K, N)                       # [E*K, N]
+        dy_deq = OQ.dequantize_mx(dyc, dys, "e5m2")
+        w_deq = OQ.dequantize_mx(wcol, wcols).reshape(E, K, N).transpose(0, 2, 1)
+        dgrad_A = _op(mgq, dyc, tile_mx_scales(dys), N, mgq.E5M2, dev)
+        dgrad_B = _op(mgq, wcol, tile_mx_scales(wcols), N, mgq.E4M3, dev)
+        # wgrad: column-wise copies [N, Rp] / [K, Rp] with blocks along the tokens
+        dyt, dyts = _mx_operand(rng, N, Rp, "e5m2")
+        at, ats = _mx_operand(rng, K, Rp)
+        wg_A = _op(mgq, dyt, tile_mx_scales(dyts), Rp, mgq.E5M2, dev)
+        wg_B = _op(mgq, at, tile_mx_scales(ats), Rp, mgq.E4M3, dev)
+        wg_dy = OQ.dequantize_mx(dyt, dyts, "e5m2").T
+        wg_a = OQ.dequantize_mx(at, ats).T
+        sc = mgq.MX32_E8M0
+    dA = torch.empty(Rp, K, dtype=torch.bfloat16, device=dev)
+    mgq.grouped_gemm_dgrad(dgrad_A, dgrad_B, sc, offd, E, Rp, N, K, dA)
+    dW = torch.full((E, N, K), 5.0, dtype=torch.float32, device=dev)
+    mgq.grouped_gemm_wgrad(wg_A, wg_B, sc, offd, E, Rp, N, K, dW, 0.0)
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    ref = OG.grouped_gemm_dgrad(dy_deq, w_deq, offs)
+    assert rel_fro(OF.round_to_bf16(ref), bf16_np(dA)) <= GEMM_TOL_BF16
+    if scaling == "tensor":
+        wg_dy, wg_a = dy_deq, a_deq
+    ref_w = OG.grouped_gemm_wgrad(wg_dy, wg_a, offs, E)
+    got = dW.cpu().numpy().astype(np.float64)
+    assert np.all(got[1] == 0.0)
+    assert rel_fro(ref_w, got) <= GEMM_TOL_F32
+    # beta = 1: accumulate; the empty group keeps its previous value
+    prev = torch.from_numpy(rng.standard_normal((E, N, K)).astype(np.float32)).to(dev)
+    dW2 = prev.clone()
+    mgq.grouped_gemm_wgrad(wg_A, wg_B, sc, offd, E, Rp, N, K, dW2, 1.0)
+    torch.cuda.synchronize()
+    got2 = dW2.cpu().numpy().astype(np.float64)
+    assert np.array_equal(got2[1], prev[1].cpu().numpy().astype(np.float64))
+    assert rel_fro(ref_w + prev.cpu().numpy(), got2) <= GEMM_TOL_F32
+
+
+def test_gemm_grouped_equals_per_group(mgq):
+    """The grouped call equals single-group calls on each expert's rows
+    (grouped vs discrete comparison of Megatron-LM PR #5487's test matrix),
+    bit for bit."""
+    rng = np.random.default_rng(31)
+    dev = torch.device(DEV)
+    offs = np.array([0, 256, 384, 768], dtype=np.int32)
+    E, N, K = 3, 256, 512
+    Rp = int(offs[-1])
+    ac, asc = _mx_operand(rng, Rp, K)
+    wc, wsc = _mx_operand(rng, E * N, K)
+    Y = torch.empty(Rp, N, dtype=torch.bfloat16, device=dev)
+    A = _op(mgq, ac, tile_mx_scales(asc), K, mgq.E4M3, dev)
+    Wo = _op(mgq, wc, tile_mx_scales(wsc), K, mgq.E4M3, dev)
+    offd = torch.from_numpy(offs).to(dev)
+    mgq.grouped_gemm_fwd(A, Wo, mgq.MX32_E8M0, offd, E, Rp, N, K, Y)
+    for e in range(E):
+        lo, hi = int(offs[e]), int(offs[e + 1])
+        Ye = torch.empty(hi - lo, N, dtype=torch.bfloat16, device=dev)
+        Ae = _op(mgq, ac[lo:hi], tile_mx_scales(asc[lo:hi]), K, mgq.E4M3, dev)
+        We = _op(mgq, wc[e * N:(e + 1) * N], tile_mx_scales(wsc[e * N:(e + 1) * N]), K, mgq.E4M3, dev)
+        mgq.grouped_gemm_fwd(Ae, We, mgq.MX32_E8M0, torch.tensor([0, hi - lo], dtype=torch.int32, device=dev), 1,
+                             hi - lo, N, K, Ye)
+        torch.cuda.synchronize()
+        assert torch.equal(Ye, Y[lo:hi])
+
+
+def test_gemm_misaligned_offsets_reported(mgq):
+    dev = torch.device(DEV)
+    rng = np.random.default_rng(3)
+    ac, asc = _mx_operand(rng, 256, 128)
+    wc, wsc = _mx_operand(rng, 2 * 256, 128)
+    Y = torch.zeros(256, 256, dtype=torch.bfloat16, device=dev)
+    A = _op(mgq, ac, tile_mx_scales(asc), 128, mgq.E4M3, dev)
+    Wo = _op(mgq, wc, tile_mx_scales(wsc), 128, mgq.E4M3, dev)
+    mgq.grouped_gemm_fwd(A, Wo, mgq.MX32_E8M0, torch.tensor([0, 100, 256], dtype=torch.int32, device=dev), 2,
+                         256, 256, 128, Y)
+    assert mgq.get_error() == mgq.ERR_INVALID_ARG
+    assert torch.count_nonzero(Y).item() == 0          # nothing written
+
+
+# ---------------------------------------------------------------------------- elementwise
+
+def _layout(rng, T, E, k, dev, align=128):
+    idx = _routing(rng, T, E, k, ())
+    rim, src, off, cnt = OR.permute_indices(idx, E, align)
+    return idx, rim, src, off, cnt
+
+
+@pytest.mark.parametrize("mode", ["mx", "tensor"])
+@pytest.mark.parametrize("F", [512, 768, 1536])
+def test_swiglu_quantize(mgq, mode, F):
+    rng = np.random.default_rng(F)
+    dev = torch.device(DEV)
+    off = np.array([0, 128, 384], dtype=np.int32)
+    R = 512
+    gu = _bf16(rng, (R, 2 * F), 2.0)
+    gu[off[-1]:] = 0
+    offd = torch.from_numpy(off).to(dev)
+    codes = torch.empty(R, F, dtype=torch.uint8, device=dev)
+    h = torch.empty(R, F, dtype=torch.bfloat16, device=dev)
+    if mode == "mx":
+        sc = torch.empty(mgq.mx_scale_bytes(R, F), dtype=torch.uint8, device=dev)
+        q = mgq.qdesc(mgq.E4M3, mgq.MX32_E8M0, codes, sc)
+    else:
+        s = torch.tensor([20.0], device=dev)
+        amax = torch.zeros(1, device=dev)
+        col = torch.empty(F, R, dtype=torch.uint8, device=dev)
+        q = mgq.qdesc(mgq.E4M3, mgq.TENSOR_F32, codes, None, col, None, s, amax)
+    mgq.swiglu_quantize(gu.to(dev), R, F, offd, 2, q, h)
+    torch.cuda.synchronize()
+    n = int(off[-1])
+    hg = bf16_np(h)[:n]
+    check_elementwise(OL.swiglu(bf16_np(gu)[:n], F), hg, "swiglu")
+    if mode == "mx":
+        c, s_ = OQ.quantize_mx(hg)
+        assert np.array_equal(u8_np(codes)[:n], c)
+        assert np.array_equal(untile_mx_scales(u8_np(sc), R, F)[:n], s_)
+    else:
+        c, am = OQ.quantize_tensor(hg, np.float32(20.0))
+        assert np.array_equal(u8_np(codes)[:n], c)
+        assert np.array_equal(u8_np(col)[:, :n], c.T)
+        assert float(amax.item()) == am
+
+
+def test_dswiglu_quantize(mgq):
+    rng = np.random.default_rng(5)
+    dev = torch.device(DEV)
+    F, R = 768, 384
+    off = np.array([0, 256, 384], dtype=np.int32)
+    gu = _bf16(rng, (R, 2 * F), 2.0)
+    dh = _bf16(rng, (R, F), 1e-3)
+    codes = torch.empty(R, 2 * F, dtype=torch.uint8, device=dev)
+    col = torch.empty(2 * F, R, dtype=torch.uint8, device=dev)
+    dgu = torch.empty(R, 2 * F, dtype=torch.bfloat16, device=dev)
+    s = torch.tensor([20000.0], device=dev)
+    amax = torch.zeros(1, device=dev)
+    q = mgq.qdesc(mgq.E5M2, mgq.TENSOR_F32, codes, None, col, None, s, amax)
+    mgq.dswiglu_quantize(dh.to(dev), gu.to(dev), R, F, torch.from_numpy(off).to(dev), 2, q, dgu)
+    torch.cuda.synchronize()
+    g = bf16_np(dgu)
+    check_elementwise(OL.dswiglu(bf16_np(dh), bf16_np(gu), F), g, "dswiglu")
+    c, am = OQ.quantize_tensor(g, np.float32(20000.0), "e5m2")
+    assert np.array_equal(u8_np(codes), c)
+    assert np.array_equal(u8_np(col), c.T)
+    assert float(amax.item()) == am
+
+
+@pytest.mark.parametrize("T,E,k,H", [(1000, 8, 2, 512), (333, 16, 8, 256), (64, 4, 1, 5120)])
+def test_unpermute_and_permute_bwd(mgq, T, E, k, H):
+    rng = np.random.default_rng(T)
+    dev = torch.device(DEV)
+    idx, rim, src, off, cnt = _layout(rng, T, E, k, dev)
+    Rp = int(off[-1])
+    y = _bf16(rng, (Rp, H))
+    probs = rng.random((T, k)).astype(np.float32)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    rimd = torch.from_numpy(rim).to(dev)
+    mgq.moe_unpermute(y.to(dev), rimd, torch.from_numpy(probs).to(dev), out)
+    dx = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    mgq.moe_permute_bwd(y.to(dev), rimd, dx)
+    torch.cuda.synchronize()
+    check_elementwise(OR.unpermute(bf16_np(y), rim, probs), bf16_np(out), "unpermute")
+    check_elementwise(OR.permute_bwd(bf16_np(y), rim), bf16_np(dx), "permute_bwd")
+
+
+@pytest.mark.parametrize("mode", ["tensor", "mx"])
+def test_unpermute_bwd_quantize(mgq, mode):
+    rng = np.random.default_rng(9)
+    dev = torch.device(DEV)
+    T, E, k, H = 700, 8, 2, 1024
+    idx, rim, src, off, cnt = _layout(rng, T, E, k, dev)
+    Rp = int(off[-1])
+    R = Rp + 128
+    dout = _bf16(rng, (T, H), 1e-3)
+    y = _bf16(rng, (R, H))
+    probs = rng.random((T, k)).astype(np.float32)
+    codes = torch.full((R, H), 0xAB, dtype=torch.uint8, device=dev)
+    dprobs = torch.empty(T, k, dtype=torch.float32, device=dev)
+    if mode == "tensor":
+        col = torch.empty(H, R, dtype=torch.uint8, device=dev)
+        s = torch.tensor([30000.0], device=dev)
+        amax = torch.zeros(1, device=dev)
+        q = mgq.qdesc(mgq.E5M2, mgq.TENSOR_F32, codes, None, col, None, s, amax)
+    else:
+        sc = torch.full((mgq.mx_scale_bytes(R, H),), 0xCD, dtype=torch.uint8, device=dev)
+        q = mgq.qdesc(mgq.E5M2, mgq.MX32_E8M0, codes, sc)
+    mgq.moe_unpermute_bwd(dout.to(dev), y.to(dev), torch.from_numpy(rim).to(dev), torch.from_numpy(src).to(dev),
+                          torch.from_numpy(probs).to(dev), R, torch.from_numpy(off).to(dev), E, q, dprobs)
+    torch.cuda.synchronize()
+    dy32, dp = OR.unpermute_bwd(bf16_np(dout), bf16_np(y), rim, probs, Rp)
+    assert rel_fro(dp, dprobs.cpu().numpy()) <= 1e-5
+    if mode == "tensor":
+        c, am = OQ.quantize_tensor(dy32.astype(np.float64), np.float32(30000.0), "e5m2")
+        assert np.array_equal(u8_np(codes)[:Rp], c)
+        assert np.array_equal(u8_np(col)[:, :Rp], c.T)
+        assert float(amax.item()) == am
+    else:
+        c, s_ = OQ.quantize_mx(dy32.astype(np.float64), "e5m2")
+        assert np.array_equal(u8_np(codes)[:Rp], c)
+        assert np.array_equal(untile_mx_scales(u8_np(sc), R, H)[:Rp], s_)
+
+
+@pytest.mark.parametrize("mode", ["mx", "tensor"])
+def test_block_quantize_weights(mgq, mode):
+    rng = np.random.default_rng(13)
+    dev = torch.device(DEV)
+    G, M, K = 3, 256, 640
+    w = _bf16(rng, (G, M, K), 0.02)
+    codes = torch.empty(G, M, K, dtype=torch.uint8, device=dev)
+    wf = bf16_np(w)
+    if mode == "mx":
+        sc = torch.empty(mgq.mx_scale_bytes(G * M, K), dtype=torch.uint8, device=dev)
+        mgq.block_quantize(w.to(dev), mgq.qdesc(mgq.E4M3, mgq.MX32_E8M0, codes, sc))
+        torch.cuda.synchronize()
+        c, s_ = OQ.quantize_mx(wf.reshape(G * M, K))
+        assert np.array_equal(u8_np(codes).reshape(G * M, K), c)
+        assert np.array_equal(untile_mx_scales(u8_np(sc), G * M, K), s_)
+    else:
+        s = torch.tensor([1000.0, 2000.0, 7.5], device=dev)
+        amax = torch.zeros(G, device=dev)
+        col = torch.empty(G, K, M, dtype=torch.uint8, device=dev)
+        mgq.block_quantize(w.to(dev), mgq.qdesc(mgq.E4M3, mgq.TENSOR_F32, codes, None, col, None, s, amax))
+        torch.cuda.synchronize()
+        for g in range(G):
+            c, am = OQ.quantize_tensor(wf[g], np.float32(s[g].item()))
+            assert np.array_equal(u8_np(codes)[g], c)
+            assert np.array_equal(u8_np(col)[g], c.T)
+            assert float(amax[g].item()) == am
+
+
+def test_amax_history_update(mgq):
+    dev = torch.device(DEV)
+    L, n = 4, 3
+    hist = torch.zeros(n, L, device=dev)
+    head = torch.zeros(1, dtype=torch.int32, device=dev)
+    scale = torch.ones(n, device=dev)
+    ref = [OL.DelayedScaling("e4m3", L) for _ in range(n)]
+    rng = np.random.default_rng(0)
+    for step in range(9):
+        a = rng.random(n).astype(np.float32) * (10 if step != 3 else 100)
+        if step == 0:
+            a[1] = 0.0
+        amax = torch.from_numpy(a).to(dev)
+        mgq.amax_history_update(hist, head, amax, scale, 448.0)
+        torch.cuda.synchronize()
+        for i in range(n):
+            ref[i].update(a[i])
+        assert np.array_equal(scale.cpu().numpy(), np.array([r.scale for r in ref], dtype=np.float32))
+        assert torch.count_nonzero(amax).item() == 0

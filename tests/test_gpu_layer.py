@@ -1,0 +1,127 @@
+"""End-to-end parity of the expert layer through the C ABI: every step of a
+forward (MXFP8) and of a training step (hybrid e4m3/e5m2, delayed per-tensor
+scaling) against the oracle on the same inputs, plus the SQNR of the
+quantised GEMMs against unquantised bf16 operands (pytorch/ao PR #2275,
+testing)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import formats as OF
+from oracle import gemm as OG
+from oracle import layer as OL
+from oracle import quant as OQ
+from oracle import routing as OR
+from tests.layer_check import (GEMM_TOL_BF16, GEMM_TOL_F32, bf16_np, check_elementwise, rel_fro,
+                               run_fwd_and_check, u8_np)
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+def test_tiny_forward_mxfp8():
+    from fp8_grouped_gemm_gb300.workloads import WORKLOADS
+    res = run_fwd_and_check(WORKLOADS["tiny"], DEV)
+    assert res["gemm1_sqnr_vs_bf16"] >= 28.0, res
+
+
+def test_mixtral_shaped_forward_scaled_down():
+    """Mixtral-like proportions (outlier channels, top-2 of 8) at a size the
+    oracle checks in full: several 128x256 tiles per expert, ragged groups."""
+    from fp8_grouped_gemm_gb300.workloads import WORKLOADS
+    w = WORKLOADS["mixtral_fwd"].scaled(T=1500, H=1024, F=1792)
+    res = run_fwd_and_check(w, DEV)
+    assert res["gemm1_sqnr_vs_bf16"] >= 28.0, res
+
+
+def _tensor_deq(codes, s, fmt="e4m3"):
+    return OQ.dequantize_tensor(codes, np.float32(s), fmt)
+
+
+def test_delayed_training_steps():
+    from fp8_grouped_gemm_gb300 import layer as L
+    from fp8_grouped_gemm_gb300 import mgq
+    from fp8_grouped_gemm_gb300 import workloads as W
+    w = W.WORKLOADS["mixtral_fwdbwd"].scaled(T=700, H=512, F=768, E=4)
+    E, k, T, H, F = w.E, w.k, w.T, w.H, w.F
+    x = W.make_activations(w)
+    w1, w2 = W.make_weights(w)
+    idx, probs = W.make_routing(w)
+    dout = W.make_dout(w)
+    lay = L.ExpertLayer(w, DEV, recipe="delayed", keep_bf16=True, history=16)
+    xd, w1d, w2d, dd = x.to(DEV), w1.to(DEV), w2.to(DEV), dout.to(DEV)
+    idxd, pd = torch.from_numpy(idx).to(DEV), torch.from_numpy(probs).to(DEV)
+    xf, w1f, w2f, df = bf16_np(x), bf16_np(w1), bf16_np(w2), bf16_np(dout)
+    rim, src, off, cnt = OR.permute_indices(idx, E, L.ALIGN)
+    Rp = int(off[-1])
+    fwd_ds = [OL.DelayedScaling("e4m3", 16) for _ in range(2 + 2 * E)]
+    bwd_ds = [OL.DelayedScaling("e5m2", 16) for _ in range(2)]
+    for step in range(3):
+        fs = lay.fwd_scale.cpu().numpy().copy()
+        bs = lay.bwd_scale.cpu().numpy().copy()
+        assert np.array_equal(fs, np.array([d.scale for d in fwd_ds], dtype=np.float32))
+        assert np.array_equal(bs, np.array([d.scale for d in bwd_ds], dtype=np.float32))
+        lay.quantize_weights(w1d, w2d)
+        lay.forward(xd, idxd, pd)
+        lay.backward(dd, pd)
+        torch.cuda.synchronize()
+        assert mgq.get_error() == mgq.OK
+        # --- forward -----------------------------------------------------
+        cx, am_x = OQ.quantize_tensor(xf, fs[0])
+        want = OR.permute_rows(cx, rim, Rp)
+        assert np.array_equal(u8_np(lay.xq)[:Rp], want)
+        assert np.array_equal(u8_np(lay.xcol)[:, :Rp], want.T)
+        w1c = [OQ.quantize_tensor(w1f[e], fs[2 + e]) for e in range(E)]
+        w2c = [OQ.quantize_tensor(w2f[e], fs[2 + E + e]) for e in range(E)]
+        for e in range(E):
+            assert np.array_equal(u8_np(lay.w1q)[e], w1c[e][0])
+            assert np.array_equal(u8_np(lay.w1col)[e], w1c[e][0].T)
+            assert np.array_equal(u8_np(lay.w2q)[e], w2c[e][0])
+            assert np.array_equal(u8_np(lay.w2col)[e], w2c[e][0].T)
+        xdq = _tensor_deq(want, fs[0])
+        w1dq = np.stack([_tensor_deq(w1c[e][0], fs[2 + e]) for e in range(E)])
+        w2dq = np.stack([_tensor_deq(w2c[e][0], fs[2 + E + e]) for e in range(E)])
+        gu = bf16_np(lay.gu)[:Rp]
+        assert rel_fro(OF.round_to_bf16(OG.grouped_gemm_fwd(xdq, w1dq, off)), gu) <= GEMM_TOL_BF16
+        hg = bf16_np(lay.h_bf16)[:Rp]
+        check_elementwise(OL.swiglu(gu, F), hg, "swiglu")
+        ch, am_h = OQ.quantize_tensor(hg, fs[1])
+        assert np.array_equal(u8_np(lay.hq)[:Rp], ch)
+        assert np.array_equal(u8_np(lay.hcol)[:, :Rp], ch.T)
+        hdq = _tensor_deq(ch, fs[1])
+        y = bf16_np(lay.y)[:Rp]
+        assert rel_fro(OF.round_to_bf16(OG.grouped_gemm_fwd(hdq, w2dq, off)), y) <= GEMM_TOL_BF16
+        check_elementwise(OR.unpermute(y, rim, probs), bf16_np(lay.out), "unpermute")
+        # --- backward ----------------------------------------------------
+        dy32, dp = OR.unpermute_bwd(df, y, rim, probs, Rp)
+        c2, am_dy2 = OQ.quantize_tensor(dy32.astype(np.float64), bs[0], "e5m2")
+        assert np.array_equal(u8_np(lay.dy2q)[:Rp], c2)
+        assert np.array_equal(u8_np(lay.dy2col)[:, :Rp], c2.T)
+        assert rel_fro(dp, lay.dprobs.cpu().numpy()) <= 1e-5
+        dy2dq = _tensor_deq(c2, bs[0], "e5m2")
+        dh = bf16_np(lay.dh)[:Rp]
+        assert rel_fro(OF.round_to_bf16(OG.grouped_gemm_dgrad(dy2dq, w2dq, off)), dh) <= GEMM_TOL_BF16
+        assert rel_fro(OG.grouped_gemm_wgrad(dy2dq, hdq, off, E), lay.dw2.cpu().numpy()) <= GEMM_TOL_F32
+        dgu = bf16_np(lay.dgu_bf16)[:Rp]
+        check_elementwise(OL.dswiglu(dh, gu, F), dgu, "dswiglu")
+        c1, am_dy1 = OQ.quantize_tensor(dgu, bs[1], "e5m2")
+        assert np.array_equal(u8_np(lay.dy1q)[:Rp], c1)
+        assert np.array_equal(u8_np(lay.dy1col)[:, :Rp], c1.T)
+        dy1dq = _tensor_deq(c1, bs[1], "e5m2")
+        dxp = bf16_np(lay.dxp)[:Rp]
+        assert rel_fro(OF.round_to_bf16(OG.grouped_gemm_dgrad(dy1dq, w1dq, off)), dxp) <= GEMM_TOL_BF16
+        assert rel_fro(OG.grouped_gemm_wgrad(dy1dq, xdq, off, E), lay.dw1.cpu().numpy()) <= GEMM_TOL_F32
+        check_elementwise(OR.permute_bwd(dxp, rim), bf16_np(lay.dx), "permute_bwd")
+        # --- amaxes and the next step's scales ----------------------------
+        amaxes = [am_x, am_h] + [w1c[e][1] for e in range(E)] + [w2c[e][1] for e in range(E)]
+        assert np.array_equal(lay.fwd_amax.cpu().numpy(), np.array(amaxes, dtype=np.float32))
+        assert np.array_equal(lay.bwd_amax.cpu().numpy(), np.array([am_dy2, am_dy1], dtype=np.float32))
+        if step >= 1:
+            # after one step of history the e4m3 GEMMs keep the SQNR bar
+            ref = OG.grouped_gemm_fwd(OR.permute_rows(xf, rim, Rp), w1f, off)
+            assert OG.sqnr_db(ref, gu) >= 28.0
+        lay.update_scaling()
+        for d, a in zip(fwd_ds, amaxes):
+            d.update(a)
+        for d, a in zip(bwd_ds, [am_dy2, am_dy1]):
+            d.update(a)
