@@ -29,7 +29,7 @@ FMAX = {E4M3: 448.0, E5M2: 57344.0}
 # every symbol include/mgq.h declares
 EXPORTS = (
     "mgq_status_string", "mgq_version", "mgq_get_error", "mgq_permute_workspace_size",
-    "mgq_moe_permute", "mgq_block_quantize", "mgq_grouped_gemm_fwd", "mgq_grouped_gemm_dgrad",
+    "mgq_moe_permute", "mgq_moe_permute_noalloc", "mgq_block_quantize", "mgq_grouped_gemm_fwd", "mgq_grouped_gemm_dgrad",
     "mgq_grouped_gemm_wgrad", "mgq_swiglu_quantize", "mgq_dswiglu_quantize", "mgq_moe_unpermute",
     "mgq_moe_unpermute_bwd", "mgq_moe_permute_bwd", "mgq_amax_history_update",
 )
@@ -75,6 +75,8 @@ def load() -> ctypes.CDLL:
         lib.mgq_permute_workspace_size.argtypes = [i32, i32, i32]
         lib.mgq_moe_permute.argtypes = [vp, i32, i32, vp, i32, i32, i32, P(QDesc), vp, i64,
                                         vp, vp, vp, vp, vp, sz, vp]
+        lib.mgq_moe_permute_noalloc.argtypes = [vp, i32, i32, vp, i32, i32, i32, P(QDesc), vp, i64,
+                                                vp, vp, vp, vp, vp]
         lib.mgq_block_quantize.argtypes = [vp, i64, i64, i64, P(QDesc), vp]
         gemm = [P(Operand), P(Operand), i32, vp, i32, i64, i64, i64]
         lib.mgq_grouped_gemm_fwd.argtypes = gemm + [vp, i32, vp]
@@ -161,6 +163,18 @@ def moe_permute(x, topk_idx, E, align, q: QDesc | None, R_cap, row_id_map, src_r
                                 _p(row_id_map), _p(src_row), _p(offsets), _p(counts), _p(workspace),
                                 workspace.numel() * workspace.element_size(), _s(stream))
     _check(rc, "mgq_moe_permute")
+
+
+def moe_permute_noalloc(x, topk_idx, E, align, q: QDesc | None, R_cap, row_id_map, src_row, offsets,
+                        counts, out_bf16=None, stream=None):
+    """mgq_moe_permute without a workspace: the routing scratch is the
+    library's fixed 1 MiB device array (for callers that cannot allocate)."""
+    T, H = (x.shape[0], x.shape[1]) if x is not None else (0, 0)
+    k = topk_idx.shape[1]
+    rc = load().mgq_moe_permute_noalloc(_p(x), T, H, _p(topk_idx), k, E, align,
+                                        ctypes.byref(q) if q is not None else None, _p(out_bf16), R_cap,
+                                        _p(row_id_map), _p(src_row), _p(offsets), _p(counts), _s(stream))
+    _check(rc, "mgq_moe_permute_noalloc")
 
 
 def block_quantize(x, q: QDesc, stream=None):

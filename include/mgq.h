@@ -156,6 +156,29 @@ int mgq_moe_permute(const void* x_bf16, int T, int H, const int32_t* topk_idx, i
                     int32_t* row_id_map, int32_t* src_row, int32_t* offsets,
                     int32_t* counts, void* workspace, size_t ws_bytes, void* stream);
 
+/* ---- permute + quantise without a workspace --------------------------------
+ * The pages have no counterpart of this call: it exists for callers that
+ * cannot allocate device memory, such as a plugin whose host framework owns
+ * every device allocation and passes it only inputs and outputs, or a runtime
+ * that forbids allocation while it runs. It computes exactly what
+ * mgq_moe_permute computes (same arguments, same results) but takes the
+ * routing scratch from a fixed 1 MiB device array inside the library instead
+ * of a caller workspace; it allocates nothing.
+ *  - Limit: mgq_permute_workspace_size(T, k, E) must not exceed 1048576 bytes
+ *    (ceil(T*k/1024) * E <= 262144), else MGQ_ERR_INVALID_ARG, nothing launched.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.
+ *  - All calls share the one array: calls whose kernels can overlap on the
+ *    GPU (different streams or host threads) race and must be serialised by
+ *    the caller. Every scratch entry is written before it is read, so the
+ *    previous call's contents need no clearing.
+ *  - Every GPU that loads the library holds the array until the process exits. */
+int mgq_moe_permute_noalloc(const void* x_bf16, int T, int H, const int32_t* topk_idx, int k,
+                            int E, int align, const mgq_qdesc* q, void* out_bf16, int64_t R_cap,
+                            int32_t* row_id_map, int32_t* src_row, int32_t* offsets,
+                            int32_t* counts, void* stream);
+
 /* ---- a3/a4: block quantise, row-wise and column-wise -----------------------
  * [BLOCK] 1x128 forward / 128x1 backward with the transpose identity;
  * [GROUPED] row-wise and column-wise data and scales of one grouped weight.
