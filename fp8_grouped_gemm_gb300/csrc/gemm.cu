@@ -15,7 +15,8 @@
 //              swizzle), plus the 512-byte E8M0 scale chunks (bulk copies)
 //   warp 1     allocates tensor memory; lane 0 issues tcgen05.cp (scales to
 //              tensor memory) and tcgen05.mma (M=128, N=256, K=32 each)
-//   warps 2-5  epilogue: tcgen05.ld of the f32 accumulator, scale, convert, store
+//   warps 2-9  epilogue: tcgen05.ld of the f32 accumulator into registers, release
+//              of the accumulator, then scale, convert, store
 // The tile scheduler walks the expert offset array; every role derives the
 // same tile sequence from it. Every mbarrier wait is bounded: on a timeout the
 // kernel records MGQ_ERR_TIMEOUT, all roles leave their loops, tensor memory is
@@ -29,7 +30,7 @@ namespace {
 
 constexpr int BM = 128, BN = 256, BK = 128;     // BK: bytes = fp8 elements
 constexpr int STAGES = 4;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;     // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfaCol = 256, kSfbCol = 256 + 4 * STAGES;
 constexpr uint64_t kWaitNs = 2000000000ull;     // 2 s: far beyond any tile
@@ -122,9 +123,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sSFB + STAGES * kSfbBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
-  uint64_t* tmem_full = bars + 2 * STAGES;
-  uint64_t* tmem_empty = bars + 2 * STAGES + 1;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2);
+  uint64_t* tmem_full = bars + 2 * STAGES;        // [2]
+  uint64_t* tmem_empty = bars + 2 * STAGES + 2;   // [2]
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   int* s_bad = reinterpret_cast<int*>(s_tmem + 2);
   int32_t* s_off = reinterpret_cast<int32_t*>(bars + 32);
@@ -132,6 +133,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
   const int E = p.E;
+  // accumulator buffers in tensor memory: two 256-column tiles when no
+  // scale-factor columns are needed, else one (columns 256.. hold the scales)
+  constexpr uint32_t kAcc = MX ? 1 : 2;
 
   for (int i = threadIdx.x; i <= E; i += kThreads) s_off[i] = p.offsets[i];
   if (threadIdx.x == 0) {
@@ -139,8 +143,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
     }
-    ptx::mbar_init(tmem_full, 1);
-    ptx::mbar_init(tmem_empty, 4 * 32);
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tmem_full[a], 1);
+      ptx::mbar_init(&tmem_empty[a], 8 * 32);
+    }
     *s_abort = 0;
     *s_bad = 0;
     ptx::fence_mbar_init();
@@ -210,12 +216,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t t = blockIdx.x; get_tile<MODE>(s_off, E, p, t, ecur, tl); t += gridDim.x) {
       if (tl.nst == 0) continue;
       if (*s_abort) break;
-      if (!ptx::mbar_wait(tmem_empty, (tc & 1) ^ 1, kWaitNs)) {
+      const uint32_t a = tc % kAcc, aph = (tc / kAcc) & 1;
+      if (!ptx::mbar_wait(&tmem_empty[a], aph ^ 1, kWaitNs)) {
         report(p.err, MGQ_ERR_TIMEOUT);
         *s_abort = 1;
         break;
       }
       ptx::tc_fence_after();
+      const uint32_t d_tmem = tmem + a * BN;
       bool ok = true;
       for (int s = 0; s < tl.nst; ++s, ++it) {
         const uint32_t st = it % STAGES, ph = (it / STAGES) & 1;
@@ -240,83 +248,94 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t adk = ad + (uint64_t)(kk * 2), bdk = bd + (uint64_t)(kk * 2);
           const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
           if (MX)
-            ptx::mma_mxf8f6f4(tmem, adk, bdk, p.idesc | ptx::idesc_sf_ids(kk, kk), sfa_t, sfb_t, acc);
+            ptx::mma_mxf8f6f4(d_tmem, adk, bdk, p.idesc | ptx::idesc_sf_ids(kk, kk), sfa_t, sfb_t, acc);
           else
-            ptx::mma_f8f6f4(tmem, adk, bdk, p.idesc, acc);
+            ptx::mma_f8f6f4(d_tmem, adk, bdk, p.idesc, acc);
         }
         ptx::mma_commit(&empty[st]);   // frees the smem stage once these MMAs finish
       }
       if (!ok) break;
-      ptx::mma_commit(tmem_full);      // accumulator complete
+      ptx::mma_commit(&tmem_full[a]);  // accumulator complete
       ++tc;
     }
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
-    const uint32_t q = warp & 3;                    // tensor-memory lane quadrant
+    // 8 warps: warp w reads tensor-memory lane quadrant w % 4 (the hardware
+    // rule) and the column half (w - 2) / 4 of the 256-column accumulator. The
+    // whole accumulator is moved to registers first and released to the MMA
+    // issuer; the scaling, conversion and stores overlap the next tile.
+    const uint32_t q = warp & 3;
+    const uint32_t half = (uint32_t)(warp - 2) >> 2;
     const int64_t row_in_tile = q * 32 + lane;
     int ecur = 0;
     uint32_t tc = 0;
     Tile tl;
     for (int64_t t = blockIdx.x; run && get_tile<MODE>(s_off, E, p, t, ecur, tl); t += gridDim.x) {
       const int64_t orow = tl.out_row + row_in_tile;
+      const int64_t col0 = tl.out_col + half * (BN / 2);
       if (tl.nst == 0) {
         // empty group (wgrad): dW_e = 0, or unchanged when accumulating
         if (p.beta == 0.0f) {
           if (p.out_f32) {
-            float* o = static_cast<float*>(p.out) + orow * p.ldo + tl.out_col;
-            for (int c = 0; c < BN; c += 4) *reinterpret_cast<float4*>(o + c) = make_float4(0, 0, 0, 0);
+            float* o = static_cast<float*>(p.out) + orow * p.ldo + col0;
+            for (int c = 0; c < BN / 2; c += 4) *reinterpret_cast<float4*>(o + c) = make_float4(0, 0, 0, 0);
           } else {
-            uint16_t* o = static_cast<uint16_t*>(p.out) + orow * p.ldo + tl.out_col;
-            for (int c = 0; c < BN; c += 8) *reinterpret_cast<uint4*>(o + c) = make_uint4(0, 0, 0, 0);
+            uint16_t* o = static_cast<uint16_t*>(p.out) + orow * p.ldo + col0;
+            for (int c = 0; c < BN / 2; c += 8) *reinterpret_cast<uint4*>(o + c) = make_uint4(0, 0, 0, 0);
           }
         }
         continue;
       }
+      const uint32_t a = tc % kAcc, aph = (tc / kAcc) & 1;
       // the whole warp agrees before the .sync.aligned tensor-memory loads
       if (__any_sync(0xFFFFFFFFu, *s_abort != 0)) break;
-      const bool got = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(tmem_full, tc & 1, kWaitNs));
+      const bool got = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&tmem_full[a], aph, kWaitNs));
       if (!got) {
         report(p.err, MGQ_ERR_TIMEOUT);
         *s_abort = 1;
         break;
       }
       ptx::tc_fence_after();
+      uint32_t r[4][32];
+      const uint32_t taddr = tmem + a * BN + ((q * 32) << 16) + half * (BN / 2);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) ptx::tmem_ld_32x32b_x32(taddr + c * 32, r[c]);
+      ptx::tmem_ld_wait();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&tmem_empty[a]);       // accumulator free for the next tile
+      ++tc;
       float alpha = 1.0f;
       if (!MX) alpha = 1.0f / (p.sa[0] * p.sb[MODE == kModeRows ? tl.e : 0]);
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        ptx::tmem_ld_32x32b_x32(tmem + ((q * 32) << 16) + c * 32, r);
-        ptx::tmem_ld_wait();
-        const int64_t col = tl.out_col + c * 32;
-        if (p.out_f32) {
-          float* o = static_cast<float*>(p.out) + orow * p.ldo + col;
+      if (p.out_f32) {
+        float* o = static_cast<float*>(p.out) + orow * p.ldo + col0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
-            float4 v = make_float4(__uint_as_float(r[i]) * alpha, __uint_as_float(r[i + 1]) * alpha,
-                                   __uint_as_float(r[i + 2]) * alpha, __uint_as_float(r[i + 3]) * alpha);
+            float4 v = make_float4(__uint_as_float(r[c][i]) * alpha, __uint_as_float(r[c][i + 1]) * alpha,
+                                   __uint_as_float(r[c][i + 2]) * alpha, __uint_as_float(r[c][i + 3]) * alpha);
             if (p.beta != 0.0f) {
-              float4 old = *reinterpret_cast<float4*>(o + i);
+              const float4 old = *reinterpret_cast<const float4*>(o + c * 32 + i);
               v.x += p.beta * old.x; v.y += p.beta * old.y; v.z += p.beta * old.z; v.w += p.beta * old.w;
             }
-            *reinterpret_cast<float4*>(o + i) = v;
+            *reinterpret_cast<float4*>(o + c * 32 + i) = v;
           }
-        } else {
-          uint16_t* o = static_cast<uint16_t*>(p.out) + orow * p.ldo + col;
+        }
+      } else {
+        uint16_t* o = static_cast<uint16_t*>(p.out) + orow * p.ldo + col0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
             uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(r[i]) * alpha, __uint_as_float(r[i + 1]) * alpha);
-            v.y = pack_bf16x2(__uint_as_float(r[i + 2]) * alpha, __uint_as_float(r[i + 3]) * alpha);
-            v.z = pack_bf16x2(__uint_as_float(r[i + 4]) * alpha, __uint_as_float(r[i + 5]) * alpha);
-            v.w = pack_bf16x2(__uint_as_float(r[i + 6]) * alpha, __uint_as_float(r[i + 7]) * alpha);
-            *reinterpret_cast<uint4*>(o + i) = v;
+            v.x = pack_bf16x2(__uint_as_float(r[c][i]) * alpha, __uint_as_float(r[c][i + 1]) * alpha);
+            v.y = pack_bf16x2(__uint_as_float(r[c][i + 2]) * alpha, __uint_as_float(r[c][i + 3]) * alpha);
+            v.z = pack_bf16x2(__uint_as_float(r[c][i + 4]) * alpha, __uint_as_float(r[c][i + 5]) * alpha);
+            v.w = pack_bf16x2(__uint_as_float(r[c][i + 6]) * alpha, __uint_as_float(r[c][i + 7]) * alpha);
+            *reinterpret_cast<uint4*>(o + c * 32 + i) = v;
           }
         }
       }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(tmem_empty);
-      ++tc;
     }
   }
   __syncthreads();

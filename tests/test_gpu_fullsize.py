@@ -1,0 +1,187 @@
+"""Parity at the workloads' full sizes, in the launch configuration bench.py
+times (ExpertLayer, persistent GEMM grid over all SMs), on sampled outputs the
+oracle computes one by one: for every expert its first and last rows plus
+random rows, and random output columns. Routing indices are checked in full.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import formats as OF
+from oracle import layer as OL
+from oracle import quant as OQ
+from oracle import routing as OR
+from tests.layer_check import GEMM_TOL_BF16, bf16_np, check_elementwise, rel_fro, u8_np, untile_mx_scales
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+def _weights_on_device(w):
+    g = torch.Generator(device=DEV)
+    g.manual_seed(w.seed * 1000 + 4)
+    w1 = (torch.randn(w.E, 2 * w.F, w.H, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    w2 = (torch.randn(w.E, w.H, w.F, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    return w1, w2
+
+
+def _sample_rows(off, cnt, rng, n_random=4):
+    rows = []
+    for e in range(len(cnt)):
+        c = int(cnt[e])
+        if c == 0:
+            continue
+        lo = int(off[e])
+        pick = {lo, lo + c - 1} | {lo + int(i) for i in rng.integers(0, c, n_random)}
+        rows += [(e, r) for r in sorted(pick)]
+    return rows
+
+
+def _mx_deq_rows(codes_u8, scales_nat, fmt="e4m3"):
+    return OQ.dequantize_mx(codes_u8, scales_nat, fmt)
+
+
+def test_mixtral_forward_full_size_sampled():
+    from fp8_grouped_gemm_gb300 import layer as L
+    from fp8_grouped_gemm_gb300 import mgq
+    from fp8_grouped_gemm_gb300 import workloads as W
+    w = W.WORKLOADS["mixtral_fwd"]
+    E, H, F = w.E, w.H, w.F
+    rng = np.random.default_rng(0)
+    x = W.make_activations(w)
+    idx, probs = W.make_routing(w)
+    w1, w2 = _weights_on_device(w)
+    lay = L.ExpertLayer(w, DEV, keep_bf16=True)
+    lay.quantize_weights(w1, w2)
+    lay.forward(x.to(DEV), torch.from_numpy(idx).to(DEV), torch.from_numpy(probs).to(DEV))
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    rim, src, off, cnt = OR.permute_indices(idx, E, L.ALIGN)
+    Rp = int(off[-1])
+    assert np.array_equal(lay.offsets.cpu().numpy(), off)
+    assert np.array_equal(lay.row_id_map.cpu().numpy(), rim)
+    assert np.array_equal(lay.src_row.cpu().numpy()[:Rp], src)
+    rows = _sample_rows(off, cnt, rng)
+    rr = np.array([r for _, r in rows])
+    ee = np.array([e for e, _ in rows])
+    toks = src[rr] // w.k
+    xf = bf16_np(x)
+    # permuted activation codes / scales of the sampled rows
+    cx, sx = OQ.quantize_mx(xf[toks])
+    xq = u8_np(lay.xq[torch.from_numpy(rr).to(DEV)])
+    xs_all = untile_mx_scales(u8_np(lay.xs), lay.R_cap, H)
+    assert np.array_equal(xq, cx) and np.array_equal(xs_all[rr], sx)
+    # gate/up outputs at sampled columns (gate and matching up columns)
+    cols = np.sort(rng.choice(F, 48, replace=False))
+    cols2 = np.concatenate([cols, cols + F])
+    w1s = w1[:, torch.from_numpy(cols2).to(DEV)]                   # [E, 96, H]
+    w1s_f = bf16_np(w1s)
+    gu_gpu = bf16_np(lay.gu[torch.from_numpy(rr).to(DEV)])        # [S, 2F]
+    w1_rows_q = u8_np(lay.w1q[:, torch.from_numpy(cols2).to(DEV)])
+    w1s_all = untile_mx_scales(u8_np(lay.w1s), E * 2 * F, H).reshape(E, 2 * F, H // 32)
+    refs, gots = [], []
+    for e in range(E):
+        cw, sw = OQ.quantize_mx(w1s_f[e])
+        assert np.array_equal(w1_rows_q[e], cw)
+        assert np.array_equal(w1s_all[e, cols2], sw)
+        sel = ee == e
+        if sel.any():
+            refs.append(_mx_deq_rows(cx[sel], sx[sel]) @ _mx_deq_rows(cw, sw).T)
+            gots.append(gu_gpu[sel][:, cols2])
+    assert rel_fro(OF.round_to_bf16(np.concatenate(refs)), np.concatenate(gots)) <= GEMM_TOL_BF16
+    # SwiGLU + quantisation of the sampled rows (from the GPU's gate/up row)
+    h_gpu = bf16_np(lay.h_bf16[torch.from_numpy(rr).to(DEV)])
+    check_elementwise(OL.swiglu(gu_gpu, F), h_gpu, "swiglu")
+    ch, sh = OQ.quantize_mx(h_gpu)
+    assert np.array_equal(u8_np(lay.hq[torch.from_numpy(rr).to(DEV)]), ch)
+    assert np.array_equal(untile_mx_scales(u8_np(lay.hs), lay.R_cap, F)[rr], sh)
+    # down projection at sampled columns
+    ocols = np.sort(rng.choice(H, 48, replace=False))
+    w2s_f = bf16_np(w2[:, torch.from_numpy(ocols).to(DEV)])        # [E, 48, F]
+    y_gpu = bf16_np(lay.y[torch.from_numpy(rr).to(DEV)])
+    refs, gots = [], []
+    for e in range(E):
+        sel = ee == e
+        if not sel.any():
+            continue
+        cw, sw = OQ.quantize_mx(w2s_f[e])
+        refs.append(_mx_deq_rows(ch[sel], sh[sel]) @ _mx_deq_rows(cw, sw).T)
+        gots.append(y_gpu[sel][:, ocols])
+    assert rel_fro(OF.round_to_bf16(np.concatenate(refs)), np.concatenate(gots)) <= GEMM_TOL_BF16
+    # combine of sampled tokens from the GPU's expert outputs
+    tsel = np.unique(toks)[:64]
+    y_rows = bf16_np(lay.y[torch.from_numpy(rim[tsel].reshape(-1)).to(DEV)]).reshape(len(tsel), w.k, H)
+    ref = np.einsum("tk,tkh->th", probs[tsel].astype(np.float64), y_rows)
+    check_elementwise(ref, bf16_np(lay.out[torch.from_numpy(tsel).to(DEV)]), "unpermute")
+
+
+def test_mixtral_training_step_full_size_sampled():
+    """The fwd+bwd step of the bench workload (hybrid e4m3/e5m2, delayed
+    scaling), after two warm-up steps so the scales are non-trivial; sampled
+    dgrad rows and sampled wgrad elements against the oracle."""
+    from fp8_grouped_gemm_gb300 import layer as L
+    from fp8_grouped_gemm_gb300 import mgq
+    from fp8_grouped_gemm_gb300 import workloads as W
+    w = W.WORKLOADS["mixtral_fwdbwd"]
+    E, H, F = w.E, w.H, w.F
+    rng = np.random.default_rng(1)
+    x = W.make_activations(w)
+    idx, probs = W.make_routing(w)
+    dout = W.make_dout(w)
+    w1, w2 = _weights_on_device(w)
+    lay = L.ExpertLayer(w, DEV, keep_bf16=True)
+    xd, idxd, pd, dd = x.to(DEV), torch.from_numpy(idx).to(DEV), torch.from_numpy(probs).to(DEV), dout.to(DEV)
+    for _ in range(2):
+        lay.quantize_weights(w1, w2)
+        lay.forward(xd, idxd, pd)
+        lay.backward(dd, pd)
+        lay.update_scaling()
+    fs = lay.fwd_scale.cpu().numpy().copy()
+    bs = lay.bwd_scale.cpu().numpy().copy()
+    lay.quantize_weights(w1, w2)
+    lay.forward(xd, idxd, pd)
+    lay.backward(dd, pd)
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    assert np.all(fs != 1.0) and np.all(bs != 1.0)
+    rim, src, off, cnt = OR.permute_indices(idx, E, L.ALIGN)
+    rows = _sample_rows(off, cnt, rng)
+    rr = np.array([r for _, r in rows])
+    ee = np.array([e for e, _ in rows])
+    toks = src[rr] // w.k
+    slots = src[rr] % w.k
+    # dY2 codes of the sampled rows: float32(probs * dout) cast with the e5m2 scale
+    dy32 = (probs[toks, slots][:, None].astype(np.float32) * bf16_np(dout[torch.from_numpy(toks)]).astype(np.float32))
+    c2, _ = OQ.quantize_tensor(dy32.astype(np.float64), bs[0], "e5m2")
+    rrd = torch.from_numpy(rr).to(DEV)
+    assert np.array_equal(u8_np(lay.dy2q[rrd]), c2)
+    # dgrad of the down projection (dh) at sampled columns
+    fcols = np.sort(rng.choice(F, 48, replace=False))
+    w2c = bf16_np(w2[:, :, torch.from_numpy(fcols).to(DEV)])          # [E, H, 48]
+    dh_gpu = bf16_np(lay.dh[rrd])
+    refs, gots = [], []
+    for e in range(E):
+        sel = ee == e
+        if not sel.any():
+            continue
+        cw, _ = OQ.quantize_tensor(w2c[e], fs[2 + E + e])
+        refs.append(OQ.dequantize_tensor(c2[sel], bs[0], "e5m2") @ OQ.dequantize_tensor(cw, fs[2 + E + e]))
+        gots.append(dh_gpu[sel][:, fcols])
+    assert rel_fro(OF.round_to_bf16(np.concatenate(refs)), np.concatenate(gots)) <= GEMM_TOL_BF16
+    # wgrad of the gate/up projection at sampled (n, k) of every expert:
+    # dW1[e, n, k] = sum over the expert's rows of dY1[r, n] * X[r, k]
+    dy1col = lay.dy1col
+    xcol = lay.xcol
+    ns = np.sort(rng.choice(2 * F, 8, replace=False))
+    ks = np.sort(rng.choice(H, 8, replace=False))
+    dw1 = lay.dw1
+    for e in range(E):
+        lo, hi = int(off[e]), int(off[e + 1])
+        dyc = u8_np(dy1col[torch.from_numpy(ns).to(DEV), lo:hi])         # [8, rows]
+        xc = u8_np(xcol[torch.from_numpy(ks).to(DEV), lo:hi])            # [8, rows]
+        ref = OQ.dequantize_tensor(dyc, bs[1], "e5m2") @ OQ.dequantize_tensor(xc, fs[0]).T
+        got = dw1[e][torch.from_numpy(ns).to(DEV)][:, torch.from_numpy(ks).to(DEV)].cpu().numpy()
+        assert rel_fro(ref, got) <= 1e-5, e
+    # the column-wise copies are the transposes of the row-wise codes
+    assert torch.equal(lay.xcol[:, :int(off[-1])].t(), lay.xq[:int(off[-1])])
+    assert torch.equal(lay.dy1col[:, :int(off[-1])].t(), lay.dy1q[:int(off[-1])])
