@@ -165,7 +165,7 @@ class Step:
             ev.setdefault(name, []).append((a, b))
         from fp8_grouped_gemm_gb300 import mgq
         w, E, H, F, R = self.w, self.w.E, self.w.H, self.w.F, lay.R_cap
-        mx = lay.scaling == mgq.MX32_E8M0
+        mx = lay.scaling in (mgq.MX32_E8M0, mgq.BLK_1x128_F32)     # block scales beside the codes
         rec("weight_quant", lambda: lay.quantize_weights(self.w1, self.w2))
         if mx:
             qx = mgq.qdesc(mgq.E4M3, lay.scaling, lay.xq, lay.xs)
@@ -255,28 +255,32 @@ def oracle_sample(w, rows=512, f_slice=1024):
     probs = np.ones((rows, 1), dtype=np.float32)
     t0 = time.perf_counter()
     rim, src, o2, cnt = OR.permute_indices(idx, 1, 128)
-    if w.recipe == "mxfp8":
-        cx, sx = OQ.quantize_mx(x)
-        c1, s1 = OQ.quantize_mx(w1[0])
-        c2, s2 = OQ.quantize_mx(w2[0])
-        gu = OG.grouped_gemm_fwd(OQ.dequantize_mx(cx, sx), OQ.dequantize_mx(c1, s1)[None], off)
-        h = round_to_bf16(OL.swiglu(round_to_bf16(gu), Fs))
-        ch, sh = OQ.quantize_mx(h)
-        y = OG.grouped_gemm_fwd(OQ.dequantize_mx(ch, sh), OQ.dequantize_mx(c2, s2)[None], off)
-        OR.unpermute(round_to_bf16(y), rim, probs)
-        flops = 2.0 * rows * H * 2 * Fs + 2.0 * rows * Fs * H
-    else:
-        s = np.float32(1.0)
-        cx, _ = OQ.quantize_tensor(x, s)
-        c1, _ = OQ.quantize_tensor(w1[0], s)
-        c2, _ = OQ.quantize_tensor(w2[0], s)
-        xd, w1d, w2d = OQ.dequantize_tensor(cx, s), OQ.dequantize_tensor(c1, s)[None], OQ.dequantize_tensor(c2, s)[None]
-        gu = round_to_bf16(OG.grouped_gemm_fwd(xd, w1d, off))
-        h = round_to_bf16(OL.swiglu(gu, Fs))
-        ch, _ = OQ.quantize_tensor(h, s)
-        hd = OQ.dequantize_tensor(ch, s)
-        y = round_to_bf16(OG.grouped_gemm_fwd(hd, w2d, off))
-        OR.unpermute(y, rim, probs)
+    s = np.float32(1.0)
+
+    def q_act(a):
+        if w.recipe == "mxfp8":
+            c, sc = OQ.quantize_mx(a)
+            return OQ.dequantize_mx(c, sc)
+        if w.recipe == "blockwise":
+            c, sc = OQ.quantize_block_1x128(a)
+            return OQ.dequantize_block_1x128(c, sc)
+        c, _ = OQ.quantize_tensor(a, s)
+        return OQ.dequantize_tensor(c, s)
+
+    def q_w(b):
+        if w.recipe == "blockwise":
+            c, sc = OQ.quantize_block_128x128(b)
+            return OQ.dequantize_block_128x128(c, sc)
+        return q_act(b)
+
+    xd, w1d, w2d = q_act(x), q_w(w1[0])[None], q_w(w2[0])[None]
+    gu = round_to_bf16(OG.grouped_gemm_fwd(xd, w1d, off))
+    h = round_to_bf16(OL.swiglu(gu, Fs))
+    hd = q_act(h)
+    y = round_to_bf16(OG.grouped_gemm_fwd(hd, w2d, off))
+    OR.unpermute(y, rim, probs)
+    flops = 2.0 * rows * H * 2 * Fs + 2.0 * rows * Fs * H
+    if w.backward:
         dy32, _ = OR.unpermute_bwd(dout, y, rim, probs, rows)
         cdy, _ = OQ.quantize_tensor(dy32.astype(np.float64), s, "e5m2")
         dyd = OQ.dequantize_tensor(cdy, s, "e5m2")
@@ -288,7 +292,7 @@ def oracle_sample(w, rows=512, f_slice=1024):
         dxp = round_to_bf16(OG.grouped_gemm_dgrad(d1, w1d, off))
         OG.grouped_gemm_wgrad(d1, xd, off, 1)
         OR.permute_bwd(dxp, rim)
-        flops = 3 * (2.0 * rows * H * 2 * Fs + 2.0 * rows * Fs * H)
+        flops *= 3
     return time.perf_counter() - t0, flops
 
 
@@ -310,7 +314,7 @@ def run_reference(args, w, rank, world):
         oracle_sample(w, rows=128, f_slice=256)
     times, flops = [], 0.0
     for _ in range(args.steps):
-        dt, flops = oracle_sample(w)
+        dt, flops = oracle_sample(w, *REF_SAMPLE)
         times.append(dt)
     tot = sum(times)
     value = flops * args.steps / tot / 1e12
@@ -320,16 +324,22 @@ def run_reference(args, w, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE[w.recipe],
         "data": "synthetic", "config": config_of(w, args),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": ncores, "kind": "oracle",
-                         "sample": SAMPLE_DESC},
+                         "sample": sample_desc(*REF_SAMPLE)},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
 METRIC = "grouped FP8 GEMM fwd+bwd TFLOP/s (Mixtral-shaped expert layer step)"
-DTYPE = {"mxfp8": "e4m3 (MXFP8, f32 accumulate)", "delayed": "e4m3/e5m2 (per-tensor delayed, f32 accumulate)"}
-SAMPLE_DESC = ("CPU oracle (numpy, float64 GEMMs) on one expert, 512 routed rows, full hidden size, "
-               "a 1024-wide FFN slice; same step chain; TFLOP/s = sample GEMM FLOPs / wall time")
+DTYPE = {"mxfp8": "e4m3 (MXFP8, f32 accumulate)", "delayed": "e4m3/e5m2 (per-tensor delayed, f32 accumulate)",
+         "blockwise": "e4m3 (1x128 / 128x128 float32 block scales, f32 accumulate)"}
+def sample_desc(rows, f_slice):
+    return (f"CPU oracle (numpy, float64 GEMMs) on one expert, {rows} routed rows, full hidden size, "
+            f"a {f_slice}-wide FFN slice; same step chain as the GPU step; TFLOP/s = sample GEMM FLOPs / wall time")
+
+
+REF_SAMPLE = (512, 1024)        # per --impl reference step (about a second on 16 cores)
+BASELINE_SAMPLE = (2048, 2048)  # the cpu_baseline of our own line (about 10 s)
 
 
 def config_of(w, args):
@@ -465,9 +475,9 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        dt, f = oracle_sample(w)
+        dt, f = oracle_sample(w, *BASELINE_SAMPLE)
         cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
-               "sample": SAMPLE_DESC, "seconds": dt}
+               "sample": sample_desc(*BASELINE_SAMPLE), "seconds": dt}
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,

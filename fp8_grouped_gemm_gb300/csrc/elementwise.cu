@@ -304,6 +304,44 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantRowsArgs a) {
   }
 }
 
+
+// ---- 128x128 tile quantisation of grouped weights [G, N, K] ------------------
+// One CTA per tile; 256 threads, thread i covers row i/2, 64 columns. The tile
+// amax gives s = fmax / amax (float32, IEEE division; 1 for an all-zero tile;
+// FLT_MAX on overflow); codes = cast(x * s); scale_inv = 1 / s at
+// [(g * N/128 + n/128) * K/128 + k/128].
+template <int DT>
+__global__ void __launch_bounds__(256) quant_tile128_kernel(const uint16_t* __restrict__ x, int64_t N, int64_t K,
+                                                            uint8_t* __restrict__ codes, float* __restrict__ sinv) {
+  __shared__ uint32_t s_max[8];
+  const int64_t nb = N / 128, kb = K / 128;
+  const int64_t tile = blockIdx.x;
+  const int64_t g = tile / (nb * kb), rem = tile % (nb * kb);
+  const int64_t n0 = (rem / kb) * 128, k0 = (rem % kb) * 128;
+  const int row = threadIdx.x >> 1, cofs = (threadIdx.x & 1) * 64;
+  const uint16_t* src = x + (g * N + n0 + row) * K + k0 + cofs;
+  float v[64];
+  load_bf16x32(src, v);
+  load_bf16x32(src + 32, v + 32);
+  uint32_t m = warp_max_u32(absmax_bits_f32(v, 64));
+  if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = max(m, s_max[i]);
+  float sc = (m == 0) ? 1.0f : __fdiv_rn(FmtInfo<DT>::fmax, __uint_as_float(m));
+  if (isinf(sc)) sc = 3.40282347e38f;
+  uint32_t cw[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    cw[i] = cvt_fp8x4<DT>(__fmul_rn(v[4 * i], sc), __fmul_rn(v[4 * i + 1], sc), __fmul_rn(v[4 * i + 2], sc),
+                          __fmul_rn(v[4 * i + 3], sc));
+  uint4* dst = reinterpret_cast<uint4*>(codes + (g * N + n0 + row) * K + k0 + cofs);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) dst[q] = make_uint4(cw[4 * q], cw[4 * q + 1], cw[4 * q + 2], cw[4 * q + 3]);
+  if (threadIdx.x == 0) sinv[tile] = __fdiv_rn(1.0f, sc);
+}
+
 // ---- delayed scaling ------------------------------------------------------------
 __global__ void amax_history_kernel(float* hist, int32_t* head, float* amax, float* scale, int n, int L, float fmax) {
   const int h = *head;
@@ -449,6 +487,25 @@ int mgq_moe_unpermute_bwd(const void* dout_bf16, const void* y_bf16, const int32
 }
 
 int mgq_block_quantize(const void* x_bf16, int64_t G, int64_t M, int64_t K, const mgq_qdesc* q, void* stream) {
+  if (q && q->scaling == MGQ_BLK_128x128_F32) {
+    MGQ_CHECK_ARG(q->row.data && q->row.scale && aligned16(q->row.data) && x_bf16 && aligned16(x_bf16));
+    MGQ_CHECK_ARG(G >= 1 && M > 0 && K > 0 && M % 128 == 0 && K % 128 == 0);
+    if (q->col.data) return MGQ_ERR_UNSUPPORTED;
+    const unsigned grid = (unsigned)(G * (M / 128) * (K / 128));
+    cudaStream_t s = as_stream(stream);
+    if (q->dtype == MGQ_E4M3)
+      quant_tile128_kernel<MGQ_E4M3><<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x_bf16), M, K,
+                                                          static_cast<uint8_t*>(q->row.data),
+                                                          static_cast<float*>(q->row.scale));
+    else if (q->dtype == MGQ_E5M2)
+      quant_tile128_kernel<MGQ_E5M2><<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x_bf16), M, K,
+                                                          static_cast<uint8_t*>(q->row.data),
+                                                          static_cast<float*>(q->row.scale));
+    else
+      return MGQ_ERR_UNSUPPORTED;
+    MGQ_LAUNCH_CHECK();
+    return MGQ_OK;
+  }
   int rc = check_q(q);
   if (rc != MGQ_OK) return rc;
   MGQ_CHECK_ARG(x_bf16 && aligned16(x_bf16) && G >= 1 && M > 0 && K > 0 && M % 128 == 0 && K % 128 == 0);

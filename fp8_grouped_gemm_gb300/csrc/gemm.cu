@@ -42,6 +42,11 @@ constexpr size_t kSmemStage = kABytes + kBBytes + kSfaBytes + kSfbBytes;
 constexpr size_t kSmemBytes = 1024 /*align slack*/ + STAGES * kSmemStage + 256 /*barriers*/ + (kMaxE + 8) * 4;
 
 enum { kModeRows = 0, kModeContract = 1 };
+// operand scaling handled by the kernel: E8M0 block scales in the MMA, one
+// float32 scale per tensor (epilogue), or float32 1x128 x 128x128 block scales
+// (promotion: one 128-deep partial product per stage, scaled and summed in
+// registers by the epilogue warps)
+enum { kKindMX = 0, kKindTensor = 1, kKindBlock = 2 };
 
 struct GemmParams {
   const int32_t* offsets;
@@ -53,8 +58,9 @@ struct GemmParams {
   int64_t sfa_kb4;    // 512-byte scale chunks per 128-row tile of A
   const uint8_t* sfb;
   int64_t sfb_kb4;
-  const float* sa;
-  const float* sb;
+  const float* sa;    // tensor: s_a; block: scale_inv_a [K/128][sa_ld]
+  const float* sb;    // tensor: s_b per expert; block: scale_inv_b [E][N/128][K/128]
+  int64_t sa_ld;
   void* out;
   int64_t ldo;
   int out_f32;
@@ -109,7 +115,7 @@ __device__ __forceinline__ bool get_tile(const int32_t* s_off, int E, const Gemm
   return true;
 }
 
-template <int MODE, bool MX>
+template <int MODE, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmParams p) {
@@ -133,8 +139,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
   const int E = p.E;
+  constexpr bool MX = KIND == kKindMX;
+  constexpr bool BLOCK = KIND == kKindBlock;
   // accumulator buffers in tensor memory: two 256-column tiles when no
-  // scale-factor columns are needed, else one (columns 256.. hold the scales)
+  // scale-factor columns are needed, else one (columns 256.. hold the scales).
+  // In block mode the two buffers hold per-stage partial products.
   constexpr uint32_t kAcc = MX ? 1 : 2;
 
   for (int i = threadIdx.x; i <= E; i += kThreads) s_off[i] = p.offsets[i];
@@ -216,17 +225,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t t = blockIdx.x; get_tile<MODE>(s_off, E, p, t, ecur, tl); t += gridDim.x) {
       if (tl.nst == 0) continue;
       if (*s_abort) break;
-      const uint32_t a = tc % kAcc, aph = (tc / kAcc) & 1;
-      if (!ptx::mbar_wait(&tmem_empty[a], aph ^ 1, kWaitNs)) {
-        report(p.err, MGQ_ERR_TIMEOUT);
-        *s_abort = 1;
-        break;
-      }
-      ptx::tc_fence_after();
-      const uint32_t d_tmem = tmem + a * BN;
       bool ok = true;
+      uint32_t a = tc % kAcc;
+      if (!BLOCK) {
+        const uint32_t aph = (tc / kAcc) & 1;
+        if (!ptx::mbar_wait(&tmem_empty[a], aph ^ 1, kWaitNs)) {
+          report(p.err, MGQ_ERR_TIMEOUT);
+          *s_abort = 1;
+          break;
+        }
+        ptx::tc_fence_after();
+      }
       for (int s = 0; s < tl.nst; ++s, ++it) {
         const uint32_t st = it % STAGES, ph = (it / STAGES) & 1;
+        if (BLOCK) {
+          // every stage gets a fresh partial buffer
+          a = tc % kAcc;
+          if (!ptx::mbar_wait(&tmem_empty[a], ((tc / kAcc) & 1) ^ 1, kWaitNs)) {
+            report(p.err, MGQ_ERR_TIMEOUT);
+            *s_abort = 1;
+            ok = false;
+            break;
+          }
+        }
         if (*s_abort || !ptx::mbar_wait(&full[st], ph, kWaitNs)) {
           report(p.err, MGQ_ERR_TIMEOUT);
           *s_abort = 1;
@@ -234,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem + a * BN;
         const uint32_t sfa_t = tmem + kSfaCol + st * 4, sfb_t = tmem + kSfbCol + st * 8;
         if (MX) {
           ptx::tmem_cp_32x128b_x4(sfa_t, ptx::sdesc_sf(sSFA0 + st * kSfaBytes));
@@ -246,17 +268,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < BK / 32; ++kk) {
           // advance 32 bytes (one K=32 step) inside the 128-byte swizzle atom
           const uint64_t adk = ad + (uint64_t)(kk * 2), bdk = bd + (uint64_t)(kk * 2);
-          const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
+          const uint32_t acc = ((BLOCK ? 0 : s) > 0 || kk > 0) ? 1u : 0u;
           if (MX)
             ptx::mma_mxf8f6f4(d_tmem, adk, bdk, p.idesc | ptx::idesc_sf_ids(kk, kk), sfa_t, sfb_t, acc);
           else
             ptx::mma_f8f6f4(d_tmem, adk, bdk, p.idesc, acc);
         }
         ptx::mma_commit(&empty[st]);   // frees the smem stage once these MMAs finish
+        if (BLOCK) {
+          ptx::mma_commit(&tmem_full[a]);  // partial product of this stage complete
+          ++tc;
+        }
       }
       if (!ok) break;
-      ptx::mma_commit(&tmem_full[a]);  // accumulator complete
-      ++tc;
+      if (!BLOCK) {
+        ptx::mma_commit(&tmem_full[a]);  // accumulator complete
+        ++tc;
+      }
     }
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
@@ -286,26 +314,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      const uint32_t a = tc % kAcc, aph = (tc / kAcc) & 1;
-      // the whole warp agrees before the .sync.aligned tensor-memory loads
-      if (__any_sync(0xFFFFFFFFu, *s_abort != 0)) break;
-      const bool got = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&tmem_full[a], aph, kWaitNs));
-      if (!got) {
-        report(p.err, MGQ_ERR_TIMEOUT);
-        *s_abort = 1;
-        break;
-      }
-      ptx::tc_fence_after();
       uint32_t r[4][32];
-      const uint32_t taddr = tmem + a * BN + ((q * 32) << 16) + half * (BN / 2);
+      if (BLOCK) {
+        // promotion: acc += partial(stage) * s_a[row, kb] * s_b[n block, kb]
+        const float* sa_row = p.sa + (tl.row_a + row_in_tile);
+        const float* sb_blk = p.sb + ((int64_t)tl.e * (p.N / 128) + (col0 / 128)) * (p.K / 128);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) ptx::tmem_ld_32x32b_x32(taddr + c * 32, r[c]);
-      ptx::tmem_ld_wait();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&tmem_empty[a]);       // accumulator free for the next tile
-      ++tc;
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[c][i] = 0u;   // +0.0f
+        float sa_next = sa_row[(tl.kx0 / 128) * p.sa_ld];
+        bool alive = true;
+        for (int s = 0; s < tl.nst; ++s) {
+          const uint32_t a = tc % kAcc, aph = (tc / kAcc) & 1;
+          const float f = sa_next * sb_blk[tl.kx0 / 128 + s];
+          if (s + 1 < tl.nst) sa_next = sa_row[(tl.kx0 / 128 + s + 1) * p.sa_ld];
+          if (__any_sync(0xFFFFFFFFu, *s_abort != 0)) { alive = false; break; }
+          const bool got = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&tmem_full[a], aph, kWaitNs));
+          if (!got) {
+            report(p.err, MGQ_ERR_TIMEOUT);
+            *s_abort = 1;
+            alive = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t taddr = tmem + a * BN + ((q * 32) << 16) + half * (BN / 2);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            ptx::tmem_ld_32x32b_x32(taddr + c * 32, v);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              r[c][i] = __float_as_uint(fmaf(__uint_as_float(v[i]), f, __uint_as_float(r[c][i])));
+          }
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(&tmem_empty[a]);
+          ++tc;
+        }
+        if (!alive) break;
+      } else {
+        const uint32_t a = tc % kAcc, aph = (tc / kAcc) & 1;
+        // the whole warp agrees before the .sync.aligned tensor-memory loads
+        if (__any_sync(0xFFFFFFFFu, *s_abort != 0)) break;
+        const bool got = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&tmem_full[a], aph, kWaitNs));
+        if (!got) {
+          report(p.err, MGQ_ERR_TIMEOUT);
+          *s_abort = 1;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t taddr = tmem + a * BN + ((q * 32) << 16) + half * (BN / 2);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) ptx::tmem_ld_32x32b_x32(taddr + c * 32, r[c]);
+        ptx::tmem_ld_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&tmem_empty[a]);       // accumulator free for the next tile
+        ++tc;
+      }
       float alpha = 1.0f;
-      if (!MX) alpha = 1.0f / (p.sa[0] * p.sb[MODE == kModeRows ? tl.e : 0]);
+      if (KIND == kKindTensor) alpha = 1.0f / (p.sa[0] * p.sb[MODE == kModeRows ? tl.e : 0]);
       if (p.out_f32) {
         float* o = static_cast<float*>(p.out) + orow * p.ldo + col0;
 #pragma unroll
@@ -346,9 +414,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int MODE, bool MX>
+template <int MODE, int KIND>
 int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, cudaStream_t s) {
-  auto kern = grouped_gemm_kernel<MODE, MX>;
+  auto kern = grouped_gemm_kernel<MODE, KIND>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -380,8 +448,12 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
   MGQ_CHECK_ARG(out_dtype == MGQ_OUT_BF16 || out_dtype == MGQ_OUT_F32);
   MGQ_CHECK_ARG(beta == 0.0f || (mode == kModeContract && out_dtype == MGQ_OUT_F32));
   MGQ_CHECK_ARG(R_cap < (1ll << 31));
-  if (scaling != MGQ_MX32_E8M0 && scaling != MGQ_TENSOR_F32) return MGQ_ERR_UNSUPPORTED;
-  const bool mx = scaling == MGQ_MX32_E8M0;
+  int kind;
+  if (scaling == MGQ_MX32_E8M0) kind = kKindMX;
+  else if (scaling == MGQ_TENSOR_F32) kind = kKindTensor;
+  else if (scaling == MGQ_BLK_1x128_F32 && mode == kModeRows) kind = kKindBlock;
+  else return MGQ_ERR_UNSUPPORTED;
+  const bool mx = kind == kKindMX;
   MGQ_CHECK_ARG(A->scale && B->scale);
   if (mx) MGQ_CHECK_ARG(aligned16(A->scale) && aligned16(B->scale));
   GemmParams p;
@@ -415,6 +487,7 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
   p.sfb = static_cast<const uint8_t*>(B->scale);
   p.sa = static_cast<const float*>(A->scale);
   p.sb = static_cast<const float*>(B->scale);
+  p.sa_ld = R_cap;
   p.out = out;
   p.ldo = (mode == kModeRows) ? N : K;
   p.out_f32 = out_dtype == MGQ_OUT_F32;
@@ -422,9 +495,13 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
   p.idesc = mx ? ptx::idesc_mxf8f6f4(A->dtype, B->dtype, BM, BN) : ptx::idesc_f8f6f4(A->dtype, B->dtype, BM, BN);
   p.err = err;
   cudaStream_t s = as_stream(stream);
-  if (mode == kModeRows)
-    return mx ? launch_gemm<kModeRows, true>(ta, tb, p, s) : launch_gemm<kModeRows, false>(ta, tb, p, s);
-  return mx ? launch_gemm<kModeContract, true>(ta, tb, p, s) : launch_gemm<kModeContract, false>(ta, tb, p, s);
+  if (mode == kModeRows) {
+    if (kind == kKindMX) return launch_gemm<kModeRows, kKindMX>(ta, tb, p, s);
+    if (kind == kKindTensor) return launch_gemm<kModeRows, kKindTensor>(ta, tb, p, s);
+    return launch_gemm<kModeRows, kKindBlock>(ta, tb, p, s);
+  }
+  if (kind == kKindMX) return launch_gemm<kModeContract, kKindMX>(ta, tb, p, s);
+  return launch_gemm<kModeContract, kKindTensor>(ta, tb, p, s);
 }
 
 }  // namespace

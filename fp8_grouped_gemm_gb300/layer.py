@@ -30,10 +30,11 @@ class ExpertLayer:
         self.w = w
         self.dev = torch.device(device)
         self.recipe = recipe or w.recipe
-        if self.recipe not in ("mxfp8", "delayed"):
+        if self.recipe not in ("mxfp8", "delayed", "blockwise"):
             raise NotImplementedError(self.recipe)
         self.train = self.recipe == "delayed"
-        self.scaling = mgq.MX32_E8M0 if self.recipe == "mxfp8" else mgq.TENSOR_F32
+        self.scaling = {"mxfp8": mgq.MX32_E8M0, "delayed": mgq.TENSOR_F32,
+                        "blockwise": mgq.BLK_1x128_F32}[self.recipe]
         E, k, T, H, F = w.E, w.k, w.T, w.H, w.F
         self.R_cap = mgq.r_cap(T, k, E, ALIGN)
         R = self.R_cap
@@ -43,6 +44,7 @@ class ExpertLayer:
         bf = dict(dtype=torch.bfloat16, device=d)
         f32 = dict(dtype=torch.float32, device=d)
         mx = self.scaling == mgq.MX32_E8M0
+        blk = self.scaling == mgq.BLK_1x128_F32
         # routing
         self.row_id_map = torch.empty(T, k, **i32)
         self.src_row = torch.empty(R, **i32)
@@ -52,9 +54,13 @@ class ExpertLayer:
         # activations
         self.xq = torch.empty(R, H, **u8)
         self.xs = torch.empty(mgq.mx_scale_bytes(R, H), **u8) if mx else None
+        if blk:   # 1x128 scale_inv, k-block major [K/128][R_cap]
+            self.xs = torch.empty(H // 128, R, **f32)
         self.gu = torch.empty(R, 2 * F, **bf)
         self.hq = torch.empty(R, F, **u8)
         self.hs = torch.empty(mgq.mx_scale_bytes(R, F), **u8) if mx else None
+        if blk:
+            self.hs = torch.empty(F // 128, R, **f32)
         self.h_bf16 = torch.empty(R, F, **bf) if keep_bf16 else None
         self.y = torch.empty(R, H, **bf)
         self.out = torch.empty(T, H, **bf)
@@ -63,6 +69,9 @@ class ExpertLayer:
         self.w1s = torch.empty(mgq.mx_scale_bytes(E * 2 * F, H), **u8) if mx else None
         self.w2q = torch.empty(E, H, F, **u8)
         self.w2s = torch.empty(mgq.mx_scale_bytes(E * H, F), **u8) if mx else None
+        if blk:   # 128x128 scale_inv [E][N/128][K/128]
+            self.w1s = torch.empty(E, 2 * F // 128, H // 128, **f32)
+            self.w2s = torch.empty(E, H // 128, F // 128, **f32)
         if self.train:
             # per-tensor scales (delayed): [x, h, w1 x E, w2 x E] in e4m3, [dy2, dy1] in e5m2
             nf = 2 + 2 * E
@@ -103,6 +112,9 @@ class ExpertLayer:
         if self.scaling == mgq.MX32_E8M0:
             mgq.block_quantize(w1, mgq.qdesc(mgq.E4M3, self.scaling, self.w1q, self.w1s), stream)
             mgq.block_quantize(w2, mgq.qdesc(mgq.E4M3, self.scaling, self.w2q, self.w2s), stream)
+        elif self.scaling == mgq.BLK_1x128_F32:
+            mgq.block_quantize(w1, mgq.qdesc(mgq.E4M3, mgq.BLK_128x128_F32, self.w1q, self.w1s), stream)
+            mgq.block_quantize(w2, mgq.qdesc(mgq.E4M3, mgq.BLK_128x128_F32, self.w2q, self.w2s), stream)
         else:
             mgq.block_quantize(w1, mgq.qdesc(mgq.E4M3, self.scaling, self.w1q, None, self.w1col, None,
                                              self._fs(2, E), self._fa(2, E)), stream)
@@ -112,7 +124,7 @@ class ExpertLayer:
     # ---- forward ------------------------------------------------------------------
     def forward(self, x, topk_idx, probs, stream=None):
         w, E, H, F, R = self.w, self.w.E, self.w.H, self.w.F, self.R_cap
-        mx = self.scaling == mgq.MX32_E8M0
+        mx = self.scaling in (mgq.MX32_E8M0, mgq.BLK_1x128_F32)    # scales beside the codes
         if mx:
             qx = mgq.qdesc(mgq.E4M3, self.scaling, self.xq, self.xs)
         else:

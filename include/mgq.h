@@ -202,9 +202,13 @@ int mgq_block_quantize(const void* x_bf16, int64_t G, int64_t M, int64_t K,
  *        column-wise copies dYcol [N, R_cap] and Acol [K, R_cap];
  *        dW [E, N, K] (out_dtype); an empty group gives zeros (beta 0) or
  *        leaves dW_e unchanged (beta 1).
- * scaling: MGQ_MX32_E8M0 (e4m3/e5m2 codes with blocked E8M0 scales) or
+ * scaling: MGQ_MX32_E8M0 (e4m3/e5m2 codes with blocked E8M0 scales),
  *        MGQ_TENSOR_F32 (scale = device float s: one for A / dY, E for the
- *        weight; the product is multiplied by 1/(s_a s_b)).
+ *        weight; the product is multiplied by 1/(s_a s_b)), or, for fwd and
+ *        dgrad, MGQ_BLK_1x128_F32: A with 1x128 float32 scale_inv
+ *        [K/128][R_cap], W with 128x128 float32 scale_inv [E][N/128][K/128]
+ *        ([BLOCK]'s DeepSeek-style recipe; each 128-deep partial product is
+ *        scaled and summed in float32).
  * Requires offsets[e] multiples of 128, N a multiple of 256 (fwd/dgrad) or
  * 128, K a multiple of 128, 16-byte aligned pointers. */
 int mgq_grouped_gemm_fwd(const mgq_operand* A, const mgq_operand* W, int scaling,

@@ -79,9 +79,32 @@ def check_elementwise(ref: np.ndarray, got: np.ndarray, what: str):
     return rf
 
 
-def run_fwd_and_check(w, device, check_all: bool = True) -> dict:
-    """One MXFP8 forward of workload ``w`` through ExpertLayer, every step
-    compared with the oracle. Returns the measured errors."""
+def _q_rows(x, recipe):
+    """Oracle row-wise quantisation of activations: (codes, scales, dequantised)."""
+    if recipe == "mxfp8":
+        c, s = OQ.quantize_mx(x, "e4m3")
+        return c, s, OQ.dequantize_mx(c, s)
+    c, s = OQ.quantize_block_1x128(x, "e4m3")
+    return c, s, OQ.dequantize_block_1x128(c, s)
+
+
+def _q_weight(w, recipe):
+    if recipe == "mxfp8":
+        c, s = OQ.quantize_mx(w, "e4m3")
+        return c, s, OQ.dequantize_mx(c, s)
+    c, s = OQ.quantize_block_128x128(w, "e4m3")
+    return c, s, OQ.dequantize_block_128x128(c, s)
+
+
+def _gpu_row_scales(lay, buf, rows_cap, ld, recipe):
+    if recipe == "mxfp8":
+        return untile_mx_scales(u8_np(buf), rows_cap, ld)
+    return buf.detach().cpu().numpy().T          # [K/128][R_cap] -> [R_cap, K/128]
+
+
+def run_fwd_and_check(w, device, recipe: str = "mxfp8") -> dict:
+    """One forward of workload ``w`` through ExpertLayer (MXFP8 or blockwise
+    FP8), every step compared with the oracle. Returns the measured errors."""
     from fp8_grouped_gemm_gb300 import layer as L
     from fp8_grouped_gemm_gb300 import workloads as W
     from fp8_grouped_gemm_gb300 import mgq
@@ -89,7 +112,7 @@ def run_fwd_and_check(w, device, check_all: bool = True) -> dict:
     x = W.make_activations(w)
     w1, w2 = W.make_weights(w)
     idx, probs = W.make_routing(w)
-    lay = L.ExpertLayer(w, device, recipe="mxfp8", keep_bf16=True)
+    lay = L.ExpertLayer(w, device, recipe=recipe, keep_bf16=True)
     xd, w1d, w2d = x.to(device), w1.to(device), w2.to(device)
     idxd = torch.from_numpy(idx).to(device)
     pd = torch.from_numpy(probs).to(device)
@@ -108,37 +131,44 @@ def run_fwd_and_check(w, device, check_all: bool = True) -> dict:
     assert np.array_equal(lay.src_row.cpu().numpy()[:Rp], src)
     # permute + quantise: bit-exact codes and scales (filler rows zero)
     xf = W.bf16_to_f64(x)
-    cx, sx = OQ.quantize_mx(xf, "e4m3")
+    cx, sx, _ = _q_rows(xf, recipe)
     want_c = OR.permute_rows(cx, rim, Rp)
     want_s = OR.permute_rows(sx, rim, Rp)
     assert np.array_equal(u8_np(lay.xq)[:Rp], want_c)
-    assert np.array_equal(untile_mx_scales(u8_np(lay.xs), lay.R_cap, H)[:Rp], want_s)
+    assert np.array_equal(_gpu_row_scales(lay, lay.xs, lay.R_cap, H, recipe)[:Rp], want_s)
     # weights: bit-exact
-    cw1, sw1 = OQ.quantize_mx(W.bf16_to_f64(w1).reshape(E * 2 * F, H), "e4m3")
-    cw2, sw2 = OQ.quantize_mx(W.bf16_to_f64(w2).reshape(E * H, F), "e4m3")
+    w1f, w2f = W.bf16_to_f64(w1), W.bf16_to_f64(w2)
+    if recipe == "mxfp8":
+        cw1, sw1, dw1 = _q_weight(w1f.reshape(E * 2 * F, H), recipe)
+        cw2, sw2, dw2 = _q_weight(w2f.reshape(E * H, F), recipe)
+        assert np.array_equal(untile_mx_scales(u8_np(lay.w1s), E * 2 * F, H), sw1)
+        assert np.array_equal(untile_mx_scales(u8_np(lay.w2s), E * H, F), sw2)
+    else:
+        q1 = [_q_weight(w1f[e], recipe) for e in range(E)]
+        q2 = [_q_weight(w2f[e], recipe) for e in range(E)]
+        cw1 = np.concatenate([q[0] for q in q1]); dw1 = np.concatenate([q[2] for q in q1])
+        cw2 = np.concatenate([q[0] for q in q2]); dw2 = np.concatenate([q[2] for q in q2])
+        assert np.array_equal(lay.w1s.cpu().numpy(), np.stack([q[1] for q in q1]))
+        assert np.array_equal(lay.w2s.cpu().numpy(), np.stack([q[1] for q in q2]))
     assert np.array_equal(u8_np(lay.w1q).reshape(E * 2 * F, H), cw1)
-    assert np.array_equal(untile_mx_scales(u8_np(lay.w1s), E * 2 * F, H), sw1)
     assert np.array_equal(u8_np(lay.w2q).reshape(E * H, F), cw2)
-    assert np.array_equal(untile_mx_scales(u8_np(lay.w2s), E * H, F), sw2)
     # gate/up GEMM on the identical quantised inputs
-    a_deq = OQ.dequantize_mx(want_c, want_s)
-    w1_deq = OQ.dequantize_mx(cw1, sw1).reshape(E, 2 * F, H)
-    gu_ref = OG.grouped_gemm_fwd(a_deq, w1_deq, off)
+    a_deq = _q_rows(xf, recipe)[2]
+    a_deq = OR.permute_rows(a_deq, rim, Rp, fill=0.0)
+    gu_ref = OG.grouped_gemm_fwd(a_deq, dw1.reshape(E, 2 * F, H), off)
     gu = bf16_np(lay.gu)[:Rp]
     res["gemm1_relfro"] = rel_fro(OF.round_to_bf16(gu_ref), gu)
     res["gemm1_sqnr_vs_bf16"] = OG.sqnr_db(
-        OG.grouped_gemm_fwd(OR.permute_rows(xf, rim, Rp), W.bf16_to_f64(w1), off), gu)
+        OG.grouped_gemm_fwd(OR.permute_rows(xf, rim, Rp), w1f, off), gu)
     assert res["gemm1_relfro"] <= GEMM_TOL_BF16, res
     # SwiGLU on the GPU's gate/up output; codes from the GPU-materialised h
-    h_ref = OL.swiglu(gu, F)
     h_gpu = bf16_np(lay.h_bf16)[:Rp]
-    res["swiglu_relfro"] = check_elementwise(h_ref, h_gpu, "swiglu")
-    ch, sh = OQ.quantize_mx(h_gpu, "e4m3")
+    res["swiglu_relfro"] = check_elementwise(OL.swiglu(gu, F), h_gpu, "swiglu")
+    ch, sh, hdq = _q_rows(h_gpu, recipe)
     assert np.array_equal(u8_np(lay.hq)[:Rp], ch)
-    assert np.array_equal(untile_mx_scales(u8_np(lay.hs), lay.R_cap, F)[:Rp], sh)
+    assert np.array_equal(_gpu_row_scales(lay, lay.hs, lay.R_cap, F, recipe)[:Rp], sh)
     # down GEMM
-    w2_deq = OQ.dequantize_mx(cw2, sw2).reshape(E, H, F)
-    y_ref = OG.grouped_gemm_fwd(OQ.dequantize_mx(ch, sh), w2_deq, off)
+    y_ref = OG.grouped_gemm_fwd(hdq, dw2.reshape(E, H, F), off)
     y = bf16_np(lay.y)[:Rp]
     res["gemm2_relfro"] = rel_fro(OF.round_to_bf16(y_ref), y)
     assert res["gemm2_relfro"] <= GEMM_TOL_BF16, res

@@ -292,6 +292,36 @@ def test_gemm_dgrad_and_wgrad(mgq, scaling):
     assert rel_fro(ref_w + prev.cpu().numpy(), got2) <= GEMM_TOL_F32
 
 
+@pytest.mark.parametrize("offs", [[0, 128, 128, 512], [0, 384]], ids=["E3", "E1"])
+def test_gemm_fwd_blockwise(mgq, offs):
+    """1x128 activation x 128x128 weight float32 block scales (promotion of
+    every 128-deep partial product)."""
+    rng = np.random.default_rng(41)
+    dev = torch.device(DEV)
+    E = len(offs) - 1
+    N, K = 512, 640
+    Rp = offs[-1]
+    R_cap = Rp + 128
+    f = OF.E4M3
+    ac = (rng.choice(f.pos_codes[:-1], size=(R_cap, K)) | (rng.integers(0, 2, (R_cap, K)) * 0x80)).astype(np.uint8)
+    wc = (rng.choice(f.pos_codes[:-1], size=(E * N, K)) | (rng.integers(0, 2, (E * N, K)) * 0x80)).astype(np.uint8)
+    sa = np.exp2(rng.uniform(-12, 4, size=(R_cap, K // 128))).astype(np.float32)      # scale_inv per 1x128
+    sw = np.exp2(rng.uniform(-12, 0, size=(E, N // 128, K // 128))).astype(np.float32)
+    Y = torch.full((R_cap, N), float("nan"), dtype=torch.bfloat16, device=dev)
+    A = _op(mgq, ac, np.ascontiguousarray(sa.T), K, mgq.E4M3, dev)                   # [K/128][R_cap]
+    Wo = _op(mgq, wc, sw, K, mgq.E4M3, dev)
+    offd = torch.tensor(offs, dtype=torch.int32, device=dev)
+    mgq.grouped_gemm_fwd(A, Wo, mgq.BLK_1x128_F32, offd, E, R_cap, N, K, Y)
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    a_deq = OQ.dequantize_block_1x128(ac[:Rp], sa[:Rp])
+    w_deq = np.stack([OQ.dequantize_block_128x128(wc[e * N:(e + 1) * N], sw[e]) for e in range(E)])
+    ref = OG.grouped_gemm_fwd(a_deq, w_deq, np.array(offs))
+    got = bf16_np(Y)
+    assert np.all(np.isnan(got[Rp:]))
+    assert rel_fro(OF.round_to_bf16(ref), got[:Rp]) <= GEMM_TOL_BF16
+
+
 def test_gemm_grouped_equals_per_group(mgq):
     """The grouped call equals single-group calls on each expert's rows
     (grouped vs discrete comparison of Megatron-LM PR #5487's test matrix),
@@ -455,7 +485,7 @@ def test_unpermute_bwd_quantize(mgq, mode):
         assert np.array_equal(untile_mx_scales(u8_np(sc), R, H)[:Rp], s_)
 
 
-@pytest.mark.parametrize("mode", ["mx", "tensor"])
+@pytest.mark.parametrize("mode", ["mx", "tensor", "blk128"])
 def test_block_quantize_weights(mgq, mode):
     rng = np.random.default_rng(13)
     dev = torch.device(DEV)
@@ -463,7 +493,18 @@ def test_block_quantize_weights(mgq, mode):
     w = _bf16(rng, (G, M, K), 0.02)
     codes = torch.empty(G, M, K, dtype=torch.uint8, device=dev)
     wf = bf16_np(w)
-    if mode == "mx":
+    if mode == "blk128":
+        w[1, 5, 7] = 3.0                                   # one large element in one tile
+        w[2] = 0                                           # all-zero tiles: scale 1
+        wf = bf16_np(w)
+        sc = torch.empty(G, M // 128, K // 128, dtype=torch.float32, device=dev)
+        mgq.block_quantize(w.to(dev), mgq.qdesc(mgq.E4M3, mgq.BLK_128x128_F32, codes, sc))
+        torch.cuda.synchronize()
+        for g in range(G):
+            c, si = OQ.quantize_block_128x128(wf[g])
+            assert np.array_equal(u8_np(codes)[g], c)
+            assert np.array_equal(sc[g].cpu().numpy(), si)
+    elif mode == "mx":
         sc = torch.empty(mgq.mx_scale_bytes(G * M, K), dtype=torch.uint8, device=dev)
         mgq.block_quantize(w.to(dev), mgq.qdesc(mgq.E4M3, mgq.MX32_E8M0, codes, sc))
         torch.cuda.synchronize()

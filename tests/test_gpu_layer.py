@@ -34,6 +34,15 @@ def test_mixtral_shaped_forward_scaled_down():
     assert res["gemm1_sqnr_vs_bf16"] >= 28.0, res
 
 
+def test_scout_forward_blockwise_scaled_down():
+    """Llama4-Scout proportions (Zipf(1.2) expert loads, two empty experts,
+    top-1) with 1x128 / 128x128 blockwise FP8 at a size checked in full."""
+    from fp8_grouped_gemm_gb300.workloads import WORKLOADS
+    w = WORKLOADS["scout_fwd"].scaled(T=2048, H=768, F=1024)
+    res = run_fwd_and_check(w, DEV, recipe="blockwise")
+    assert res["gemm1_sqnr_vs_bf16"] >= 28.0, res
+
+
 def _tensor_deq(codes, s, fmt="e4m3"):
     return OQ.dequantize_tensor(codes, np.float32(s), fmt)
 
