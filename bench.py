@@ -42,6 +42,7 @@ import torch  # noqa: E402
 # file is absent; FP8 dense = bf16 x 2 (nominal 4.5 / 2.25 PFLOP/s).
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0
+FP4_OVER_BF16 = 6.0   # nominal dense 13.5 / 2.25 PFLOP/s
 
 
 def peaks():
@@ -167,6 +168,22 @@ class Step:
         w, E, H, F, R = self.w, self.w.E, self.w.H, self.w.F, lay.R_cap
         mx = lay.scaling in (mgq.MX32_E8M0, mgq.BLK_1x128_F32)     # block scales beside the codes
         rec("weight_quant", lambda: lay.quantize_weights(self.w1, self.w2))
+        if lay.nv:
+            a, g = lay.nv_amax, lay.nv_sg
+            qx = mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, lay.xq, lay.xs, tensor_scale=g[0:1], amax_out=a[0:1])
+            rec("permute_quant", lambda: mgq.moe_permute(self.x, self.idx, E, 128, qx, R, lay.row_id_map,
+                                                         lay.src_row, lay.offsets, lay.counts, lay.ws, None))
+            A1 = mgq.operand(lay.xq, lay.xs, H, mgq.E2M1, g[0:1])
+            B1 = mgq.operand(lay.w1q, lay.w1s, H, mgq.E2M1, g[2:2 + E])
+            rec("gemm", lambda: mgq.grouped_gemm_fwd(A1, B1, mgq.NV16_UE4M3, lay.offsets, E, R, 2 * F, H, lay.gu))
+            qh = mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, lay.hq, lay.hs, tensor_scale=g[1:2], amax_out=a[1:2])
+            rec("swiglu_quant", lambda: mgq.swiglu_quantize(lay.gu, R, F, lay.offsets, E, qh, lay.h_bf16))
+            A2 = mgq.operand(lay.hq, lay.hs, F, mgq.E2M1, g[1:2])
+            B2 = mgq.operand(lay.w2q, lay.w2s, F, mgq.E2M1, g[2 + E:2 + 2 * E])
+            rec("gemm", lambda: mgq.grouped_gemm_fwd(A2, B2, mgq.NV16_UE4M3, lay.offsets, E, R, H, F, lay.y))
+            rec("unpermute", lambda: mgq.moe_unpermute(lay.y, lay.row_id_map, self.probs, lay.out))
+            self.events.append(ev)
+            return
         if mx:
             qx = mgq.qdesc(mgq.E4M3, lay.scaling, lay.xq, lay.xs)
         else:
@@ -212,6 +229,24 @@ class Step:
 
 
 def algorithmic_bytes(w, R_pad):
+    if w.recipe == "nvfp4":
+        return algorithmic_bytes_nvfp4(w)
+    return algorithmic_bytes_fp8(w, R_pad)
+
+
+def algorithmic_bytes_nvfp4(w):
+    """NVFP4: codes are 0.5 byte per element plus one scale byte per 16; the
+    tensor amax passes re-read their input once."""
+    T, k, H, F, E = w.T, w.k, w.H, w.F, w.E
+    R = T * k
+    q = 0.5 + 1.0 / 16
+    return {"permute_quant": T * H * 2 * 2 + R * H * q,
+            "swiglu_quant": R * 2 * F * 2 + R * F * 2 * 2 + R * F * q,
+            "unpermute": R * H * 2 + T * H * 2,
+            "weight_quant": E * 3 * F * H * 2 * 2 + E * 3 * F * H * q}
+
+
+def algorithmic_bytes_fp8(w, R_pad):
     """Compulsory HBM bytes of the memory-bound steps (each input read once,
     each output written once; a row quantised once per token is written k
     times)."""
@@ -332,7 +367,8 @@ def run_reference(args, w, rank, world):
 
 METRIC = "grouped FP8 GEMM fwd+bwd TFLOP/s (Mixtral-shaped expert layer step)"
 DTYPE = {"mxfp8": "e4m3 (MXFP8, f32 accumulate)", "delayed": "e4m3/e5m2 (per-tensor delayed, f32 accumulate)",
-         "blockwise": "e4m3 (1x128 / 128x128 float32 block scales, f32 accumulate)"}
+         "blockwise": "e4m3 (1x128 / 128x128 float32 block scales, f32 accumulate)",
+         "nvfp4": "e2m1 (NVFP4: 16-element ue4m3 scales + float32 global scale, f32 accumulate)"}
 def sample_desc(rows, f_slice):
     return (f"CPU oracle (numpy, float64 GEMMs) on one expert, {rows} routed rows, full hidden size, "
             f"a {f_slice}-wide FFN slice; same step chain as the GPU step; TFLOP/s = sample GEMM FLOPs / wall time")
@@ -428,7 +464,8 @@ def main():
     pk, pk_src = peaks()
     gemm_ms = per.get("gemm", float("nan"))
     achieved = flops / (gemm_ms * 1e-3) / 1e12
-    peak_fp8 = pk["bf16_tflops_sustained"] * FP8_OVER_BF16
+    ratio = FP4_OVER_BF16 if w.recipe == "nvfp4" else FP8_OVER_BF16
+    peak_fp8 = pk["bf16_tflops_sustained"] * ratio
     R_pad = int(step.lay.offsets[-1].item())
     ab = algorithmic_bytes(w, R_pad)
     hbm = {k: {"ms": per[k], "GB/s": ab[k] / (per[k] * 1e-3) / 1e9,
@@ -436,7 +473,8 @@ def main():
     roofline = {"bound": "tensor", "kernel": "grouped_gemm_kernel (all grouped GEMM launches of the step)",
                 "achieved": achieved, "peak": peak_fp8, "unit": "TFLOP/s", "frac": achieved / peak_fp8,
                 "traffic": None,
-                "peak_source": f"{pk_src}: bf16 sustained {pk['bf16_tflops_sustained']} TFLOP/s x 2 (fp8/bf16 nominal)",
+                "peak_source": f"{pk_src}: bf16 sustained {pk['bf16_tflops_sustained']} TFLOP/s x {ratio:g} "
+                               f"({'fp4' if w.recipe == 'nvfp4' else 'fp8'}/bf16 nominal)",
                 "gemm_ms_per_step": gemm_ms}
 
     # end to end through host buffers: H2D of the step's inputs, D2H of dX (or the output)

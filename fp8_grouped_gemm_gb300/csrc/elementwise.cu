@@ -342,6 +342,95 @@ __global__ void __launch_bounds__(256) quant_tile128_kernel(const uint16_t* __re
   if (threadIdx.x == 0) sinv[tile] = __fdiv_rn(1.0f, sc);
 }
 
+
+// ---- NVFP4 support: per-group amax, then row quantisation with s_g -------------
+
+// amax[g] = max |x| over group g ([G][per_group] bf16, per_group % 8 == 0).
+// amax must hold +0 (or a smaller value) before the launch.
+__global__ void __launch_bounds__(256) amax_groups_kernel(const uint16_t* __restrict__ x, int64_t per_group,
+                                                          float* __restrict__ amax) {
+  __shared__ uint32_t s_m[8];
+  const int64_t g = blockIdx.y;
+  const uint16_t* base = x + g * per_group;
+  uint32_t m2 = 0;
+  for (int64_t i = ((int64_t)blockIdx.x * 256 + threadIdx.x) * 8; i < per_group; i += (int64_t)gridDim.x * 256 * 8) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(base + i));
+    m2 = absmax_bf16x2(m2, w.x);
+    m2 = absmax_bf16x2(m2, w.y);
+    m2 = absmax_bf16x2(m2, w.z);
+    m2 = absmax_bf16x2(m2, w.w);
+  }
+  uint32_t m = warp_max_u32(fold_bf16x2(m2));
+  if ((threadIdx.x & 31) == 0) s_m[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 1; i < 8; ++i) m = max(m, s_m[i]);
+    atomic_max_nonneg(amax + g, __uint_as_float(m));
+  }
+}
+
+// NVFP4 row quantisation of [rows, K] bf16 in groups of M rows: warp per row;
+// s_g from the group's amax (also written to s_out[g] by the group's first row).
+struct QuantRowsNvArgs {
+  const uint16_t* x;
+  int64_t rows, M, K;
+  const int32_t* rows_used;    // device row count or null
+  uint8_t* codes;              // [rows, K/2]
+  uint8_t* scales;             // tiled ue4m3
+  const float* amax;           // per group
+  float* s_out;                // per group
+};
+
+__global__ void __launch_bounds__(256) quant_rows_nv_kernel(QuantRowsNvArgs a) {
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * kWarps + warp;
+  const int64_t nrows = a.rows_used ? (int64_t)*a.rows_used : a.rows;
+  if (r >= nrows) return;
+  const int64_t g = r / a.M;
+  const float s_g = nv_global_scale(a.amax[g]);
+  if (r % a.M == 0 && lane == 0) a.s_out[g] = s_g;
+  for (int64_t c0 = 0; c0 < a.K; c0 += 1024) {
+    const int64_t c = c0 + 32 * lane;
+    const bool act = c < a.K;
+    float v[32];
+    if (act) {
+      load_bf16x32(a.x + r * a.K + c, v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+    }
+    Block32nv o;
+    quantize32_nv(v, s_g, o);
+    if (act) store32_nv(o, a.codes, a.scales, r, c, a.K, lane);
+  }
+}
+
+// SwiGLU pass of the NVFP4 path: h = bf16(silu(g) * u) written out, and the
+// tensor amax of h accumulated (the quantisation needs it first).
+__global__ void __launch_bounds__(256) swiglu_h_kernel(const uint16_t* __restrict__ gu, const int32_t* rows_used, int F,
+                                                       uint16_t* __restrict__ h, float* amax) {
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * kWarps + warp;
+  if (r >= *rows_used) return;
+  uint32_t tam = 0;
+  for (int c0 = 0; c0 < F; c0 += 1024) {
+    const int c = c0 + 32 * lane;
+    if (c < F) {
+      float g[32], u[32], hv[32];
+      load_bf16x32(gu + r * 2 * F + c, g);
+      load_bf16x32(gu + r * 2 * F + F + c, u);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) hv[i] = round_bf16(__fmul_rn(silu_f(g[i]), u[i]));
+      tam = max(tam, absmax_bits_f32(hv, 32));
+      store_bf16x32(h + r * F + c, hv);
+    }
+  }
+  tam = warp_max_u32(tam);
+  if (lane == 0) atomic_max_nonneg(amax, __uint_as_float(tam));
+}
+
 // ---- delayed scaling ------------------------------------------------------------
 __global__ void amax_history_kernel(float* hist, int32_t* head, float* amax, float* scale, int n, int L, float fmax) {
   const int h = *head;
@@ -374,6 +463,16 @@ int check_q(const mgq_qdesc* q) {
 }
 
 }  // namespace
+
+int launch_amax_groups(const uint16_t* x, int64_t per_group, int64_t G, float* amax, cudaStream_t s) {
+  if (cudaMemsetAsync(amax, 0, (size_t)G * sizeof(float), s) != cudaSuccess) return MGQ_ERR_CUDA;
+  int64_t blocks = (per_group + 256 * 8 * 8 - 1) / (256 * 8 * 8);     // >= 8 loads per thread
+  blocks = blocks < 1 ? 1 : (blocks > 2048 ? 2048 : blocks);
+  amax_groups_kernel<<<dim3((unsigned)blocks, (unsigned)G), 256, 0, s>>>(x, per_group, amax);
+  MGQ_LAUNCH_CHECK();
+  return MGQ_OK;
+}
+
 }  // namespace mgq
 
 using namespace mgq;
@@ -395,6 +494,26 @@ extern "C" {
 
 int mgq_swiglu_quantize(const void* gu_bf16, int64_t R_cap, int F, const int32_t* offsets, int E,
                         const mgq_qdesc* q, void* h_bf16, void* stream) {
+  if (q && q->scaling == MGQ_NV16_UE4M3) {
+    // two passes: h (materialised) and its amax, then the quantisation with s_g
+    MGQ_CHECK_ARG(q->dtype == MGQ_E2M1 && q->row.data && q->row.scale && q->amax_out && q->tensor_scale);
+    MGQ_CHECK_ARG(h_bf16 && aligned16(h_bf16) && gu_bf16 && aligned16(gu_bf16) && offsets && E >= 1);
+    MGQ_CHECK_ARG(aligned16(q->row.data) && aligned16(q->row.scale));
+    MGQ_CHECK_ARG(F > 0 && F % 128 == 0 && R_cap > 0 && R_cap % 128 == 0);
+    if (q->col.data) return MGQ_ERR_UNSUPPORTED;
+    cudaStream_t s = as_stream(stream);
+    if (cudaMemsetAsync(q->amax_out, 0, sizeof(float), s) != cudaSuccess) return MGQ_ERR_CUDA;
+    const unsigned grid = (unsigned)((R_cap + kWarps - 1) / kWarps);
+    swiglu_h_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(gu_bf16), offsets + E, F,
+                                         static_cast<uint16_t*>(h_bf16), q->amax_out);
+    MGQ_LAUNCH_CHECK();
+    QuantRowsNvArgs a{static_cast<const uint16_t*>(h_bf16), R_cap, R_cap, F, offsets + E,
+                      static_cast<uint8_t*>(q->row.data), static_cast<uint8_t*>(q->row.scale), q->amax_out,
+                      q->tensor_scale};
+    quant_rows_nv_kernel<<<grid, 256, 0, s>>>(a);
+    MGQ_LAUNCH_CHECK();
+    return MGQ_OK;
+  }
   int rc = check_q(q);
   if (rc != MGQ_OK) return rc;
   MGQ_CHECK_ARG(gu_bf16 && aligned16(gu_bf16) && aligned16(h_bf16) && offsets && E >= 1);
@@ -487,6 +606,21 @@ int mgq_moe_unpermute_bwd(const void* dout_bf16, const void* y_bf16, const int32
 }
 
 int mgq_block_quantize(const void* x_bf16, int64_t G, int64_t M, int64_t K, const mgq_qdesc* q, void* stream) {
+  if (q && q->scaling == MGQ_NV16_UE4M3) {
+    MGQ_CHECK_ARG(q->dtype == MGQ_E2M1 && q->row.data && q->row.scale && q->amax_out && q->tensor_scale);
+    MGQ_CHECK_ARG(aligned16(q->row.data) && aligned16(q->row.scale) && x_bf16 && aligned16(x_bf16));
+    MGQ_CHECK_ARG(G >= 1 && M > 0 && K > 0 && M % 128 == 0 && K % 128 == 0);
+    if (q->col.data) return MGQ_ERR_UNSUPPORTED;
+    cudaStream_t s = as_stream(stream);
+    int rc = launch_amax_groups(static_cast<const uint16_t*>(x_bf16), M * K, G, q->amax_out, s);
+    if (rc != MGQ_OK) return rc;
+    QuantRowsNvArgs a{static_cast<const uint16_t*>(x_bf16), G * M, M, K, nullptr,
+                      static_cast<uint8_t*>(q->row.data), static_cast<uint8_t*>(q->row.scale), q->amax_out,
+                      q->tensor_scale};
+    quant_rows_nv_kernel<<<(unsigned)((G * M + kWarps - 1) / kWarps), 256, 0, s>>>(a);
+    MGQ_LAUNCH_CHECK();
+    return MGQ_OK;
+  }
   if (q && q->scaling == MGQ_BLK_128x128_F32) {
     MGQ_CHECK_ARG(q->row.data && q->row.scale && aligned16(q->row.data) && x_bf16 && aligned16(x_bf16));
     MGQ_CHECK_ARG(G >= 1 && M > 0 && K > 0 && M % 128 == 0 && K % 128 == 0);

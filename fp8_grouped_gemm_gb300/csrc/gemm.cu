@@ -32,13 +32,17 @@ constexpr int BM = 128, BN = 256, BK = 128;     // BK: bytes = fp8 elements
 constexpr int STAGES = 4;
 constexpr int kThreads = 320;     // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfaCol = 256, kSfbCol = 256 + 4 * STAGES;
+constexpr uint32_t kSfaCol = 256;
+// scale bytes and tensor-memory scale columns per stage (MX: one chunk per
+// 128 rows; NVFP4: four)
+__host__ __device__ constexpr uint32_t sfa_bytes(int kind) { return kind == 3 ? 2048u : 512u; }
+__host__ __device__ constexpr uint32_t sfa_cols(int kind) { return kind == 3 ? 16u : 4u; }
+__host__ __device__ constexpr uint32_t sfb_col0(int kind) { return kSfaCol + sfa_cols(kind) * 4; }
 constexpr uint64_t kWaitNs = 2000000000ull;     // 2 s: far beyond any tile
 constexpr int kMaxE = 1024;
 
 constexpr uint32_t kABytes = BM * BK, kBBytes = BN * BK;
-constexpr uint32_t kSfaBytes = 512, kSfbBytes = 1024;
-constexpr size_t kSmemStage = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+constexpr size_t kSmemStage = kABytes + kBBytes + 2048 + 4096;   // largest (NVFP4) scale chunks
 constexpr size_t kSmemBytes = 1024 /*align slack*/ + STAGES * kSmemStage + 256 /*barriers*/ + (kMaxE + 8) * 4;
 
 enum { kModeRows = 0, kModeContract = 1 };
@@ -46,7 +50,9 @@ enum { kModeRows = 0, kModeContract = 1 };
 // float32 scale per tensor (epilogue), or float32 1x128 x 128x128 block scales
 // (promotion: one 128-deep partial product per stage, scaled and summed in
 // registers by the epilogue warps)
-enum { kKindMX = 0, kKindTensor = 1, kKindBlock = 2 };
+enum { kKindMX = 0, kKindTensor = 1, kKindBlock = 2, kKindNV = 3 };
+// NVFP4 (kKindNV): a 128-byte stage holds 256 e2m1 elements = 4 MMAs of K=64,
+// each with 4 ue4m3 scales per row (one 512-byte scale chunk per 128 rows)
 
 struct GemmParams {
   const int32_t* offsets;
@@ -58,8 +64,8 @@ struct GemmParams {
   int64_t sfa_kb4;    // 512-byte scale chunks per 128-row tile of A
   const uint8_t* sfb;
   int64_t sfb_kb4;
-  const float* sa;    // tensor: s_a; block: scale_inv_a [K/128][sa_ld]
-  const float* sb;    // tensor: s_b per expert; block: scale_inv_b [E][N/128][K/128]
+  const float* sa;    // tensor: s_a; block: scale_inv_a [K/128][sa_ld]; NVFP4: s_g of A
+  const float* sb;    // tensor: s_b per expert; block: scale_inv_b [E][N/128][K/128]; NVFP4: s_g per expert
   int64_t sa_ld;
   void* out;
   int64_t ldo;
@@ -124,9 +130,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   uint8_t* sA = smem;
   uint8_t* sB = sA + STAGES * kABytes;
+  constexpr uint32_t kSfaBytes = sfa_bytes(KIND), kSfbBytes = 2 * sfa_bytes(KIND);
+  constexpr uint32_t kSfbCol = sfb_col0(KIND);
   uint8_t* sSFA = sB + STAGES * kBBytes;
   uint8_t* sSFB = sSFA + STAGES * kSfaBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sSFB + STAGES * kSfbBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sSFA + STAGES * 3 * 2048);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* tmem_full = bars + 2 * STAGES;        // [2]
@@ -139,7 +147,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
   const int E = p.E;
-  constexpr bool MX = KIND == kKindMX;
+  constexpr bool NV = KIND == kKindNV;
+  constexpr bool MX = KIND == kKindMX || NV;     // block scales through tensor memory
   constexpr bool BLOCK = KIND == kKindBlock;
   // accumulator buffers in tensor memory: two 256-column tiles when no
   // scale-factor columns are needed, else one (columns 256.. hold the scales).
@@ -205,12 +214,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tma_load_2d(sA + st * kABytes, &tmA, &full[st], kx, (int32_t)tl.row_a);
         ptx::tma_load_2d(sB + st * kBBytes, &tmB, &full[st], kx, (int32_t)tl.row_b);
         if (MX) {
-          const int64_t kt = tl.kx0 / BK + s;
+          // scale chunks of this stage: MX one 512-byte chunk per 128 rows,
+          // NVFP4 four consecutive chunks (the 4 MMAs of the stage)
+          const int64_t kt = (tl.kx0 / BK + s) * (kSfaBytes / 512);
           const uint8_t* fa = p.sfa + ((tl.row_a / BM) * p.sfa_kb4 + kt) * 512;
           const uint8_t* fb = p.sfb + ((tl.row_b / BM) * p.sfb_kb4 + kt) * 512;
-          ptx::bulk_load(sSFA + st * kSfaBytes, fa, 512, &full[st]);
-          ptx::bulk_load(sSFB + st * kSfbBytes, fb, 512, &full[st]);
-          ptx::bulk_load(sSFB + st * kSfbBytes + 512, fb + p.sfb_kb4 * 512, 512, &full[st]);
+          ptx::bulk_load(sSFA + st * kSfaBytes, fa, kSfaBytes, &full[st]);
+          ptx::bulk_load(sSFB + st * kSfbBytes, fb, kSfaBytes, &full[st]);
+          ptx::bulk_load(sSFB + st * kSfbBytes + kSfaBytes, fb + p.sfb_kb4 * 512, kSfaBytes, &full[st]);
         }
       }
       if (*s_abort) break;
@@ -256,11 +267,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem + a * BN;
-        const uint32_t sfa_t = tmem + kSfaCol + st * 4, sfb_t = tmem + kSfbCol + st * 8;
+        const uint32_t sfa_t = tmem + kSfaCol + st * sfa_cols(KIND), sfb_t = tmem + kSfbCol + st * 2 * sfa_cols(KIND);
         if (MX) {
-          ptx::tmem_cp_32x128b_x4(sfa_t, ptx::sdesc_sf(sSFA0 + st * kSfaBytes));
-          ptx::tmem_cp_32x128b_x4(sfb_t, ptx::sdesc_sf(sSFB0 + st * kSfbBytes));
-          ptx::tmem_cp_32x128b_x4(sfb_t + 4, ptx::sdesc_sf(sSFB0 + st * kSfbBytes + 512));
+#pragma unroll
+          for (uint32_t ch = 0; ch < kSfaBytes / 512; ++ch) {
+            ptx::tmem_cp_32x128b_x4(sfa_t + ch * 4, ptx::sdesc_sf(sSFA0 + st * kSfaBytes + ch * 512));
+            ptx::tmem_cp_32x128b_x4(sfb_t + ch * 8, ptx::sdesc_sf(sSFB0 + st * kSfbBytes + ch * 512));
+            ptx::tmem_cp_32x128b_x4(sfb_t + ch * 8 + 4, ptx::sdesc_sf(sSFB0 + st * kSfbBytes + kSfaBytes + ch * 512));
+          }
         }
         const uint64_t ad = ptx::sdesc_kmajor_sw128(sA0 + st * kABytes);
         const uint64_t bd = ptx::sdesc_kmajor_sw128(sB0 + st * kBBytes);
@@ -269,7 +283,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // advance 32 bytes (one K=32 step) inside the 128-byte swizzle atom
           const uint64_t adk = ad + (uint64_t)(kk * 2), bdk = bd + (uint64_t)(kk * 2);
           const uint32_t acc = ((BLOCK ? 0 : s) > 0 || kk > 0) ? 1u : 0u;
-          if (MX)
+          if (NV)
+            ptx::mma_mxf4nvf4(d_tmem, adk, bdk, p.idesc, sfa_t + kk * 4, sfb_t + kk * 8, acc);
+          else if (MX)
             ptx::mma_mxf8f6f4(d_tmem, adk, bdk, p.idesc | ptx::idesc_sf_ids(kk, kk), sfa_t, sfb_t, acc);
           else
             ptx::mma_f8f6f4(d_tmem, adk, bdk, p.idesc, acc);
@@ -373,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++tc;
       }
       float alpha = 1.0f;
-      if (KIND == kKindTensor) alpha = 1.0f / (p.sa[0] * p.sb[MODE == kModeRows ? tl.e : 0]);
+      if (KIND == kKindTensor || NV) alpha = 1.0f / (p.sa[0] * p.sb[MODE == kModeRows ? tl.e : 0]);
       if (p.out_f32) {
         float* o = static_cast<float*>(p.out) + orow * p.ldo + col0;
 #pragma unroll
@@ -432,7 +448,7 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& 
 
 int check_operand(const mgq_operand* o) {
   if (!o || !o->data || !aligned16(o->data)) return MGQ_ERR_INVALID_ARG;
-  if (o->dtype != MGQ_E4M3 && o->dtype != MGQ_E5M2) return MGQ_ERR_UNSUPPORTED;
+  if (o->dtype != MGQ_E4M3 && o->dtype != MGQ_E5M2 && o->dtype != MGQ_E2M1) return MGQ_ERR_UNSUPPORTED;
   return MGQ_OK;
 }
 
@@ -452,21 +468,30 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
   if (scaling == MGQ_MX32_E8M0) kind = kKindMX;
   else if (scaling == MGQ_TENSOR_F32) kind = kKindTensor;
   else if (scaling == MGQ_BLK_1x128_F32 && mode == kModeRows) kind = kKindBlock;
+  else if (scaling == MGQ_NV16_UE4M3 && mode == kModeRows) kind = kKindNV;
   else return MGQ_ERR_UNSUPPORTED;
   const bool mx = kind == kKindMX;
+  const bool nv = kind == kKindNV;
+  if (nv != (A->dtype == MGQ_E2M1) || nv != (B->dtype == MGQ_E2M1)) return MGQ_ERR_UNSUPPORTED;
   MGQ_CHECK_ARG(A->scale && B->scale);
-  if (mx) MGQ_CHECK_ARG(aligned16(A->scale) && aligned16(B->scale));
+  if (mx || nv) MGQ_CHECK_ARG(aligned16(A->scale) && aligned16(B->scale));
+  if (nv) MGQ_CHECK_ARG(A->global_scale && B->global_scale && K % 256 == 0 && A->ld % 256 == 0 && B->ld % 256 == 0);
+  // operand bytes per element: e2m1 codes are packed two per byte
+  const int64_t ebytes_den = nv ? 2 : 1;
   GemmParams p;
   CUtensorMap ta, tb;
   if (mode == kModeRows) {
     MGQ_CHECK_ARG(N > 0 && K > 0 && N % BN == 0 && K % BK == 0);
     MGQ_CHECK_ARG(A->ld >= K && A->ld % 128 == 0 && B->ld >= K && B->ld % 128 == 0);
     MGQ_CHECK_ARG((int64_t)E * N < (1ll << 31));
-    if (!encode_tmap_u8_2d(&ta, A->data, (uint64_t)K, (uint64_t)R_cap, (uint64_t)A->ld, 128, BM) ||
-        !encode_tmap_u8_2d(&tb, B->data, (uint64_t)K, (uint64_t)E * N, (uint64_t)B->ld, 128, BN))
+    if (!encode_tmap_u8_2d(&ta, A->data, (uint64_t)(K / ebytes_den), (uint64_t)R_cap,
+                           (uint64_t)(A->ld / ebytes_den), 128, BM) ||
+        !encode_tmap_u8_2d(&tb, B->data, (uint64_t)(K / ebytes_den), (uint64_t)E * N,
+                           (uint64_t)(B->ld / ebytes_den), 128, BN))
       return MGQ_ERR_CUDA;
-    p.sfa_kb4 = A->ld / 128;
-    p.sfb_kb4 = B->ld / 128;
+    // 512-byte scale chunks per 128-row tile: MX 32x4-element blocks, NVFP4 16x4
+    p.sfa_kb4 = A->ld / (nv ? 64 : 128);
+    p.sfb_kb4 = B->ld / (nv ? 64 : 128);
   } else {
     MGQ_CHECK_ARG(N > 0 && K > 0 && N % BM == 0 && K % BN == 0);
     MGQ_CHECK_ARG(A->ld >= R_cap && A->ld % 128 == 0 && B->ld >= R_cap && B->ld % 128 == 0);
@@ -481,23 +506,26 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
   p.offsets = offsets;
   p.E = E;
   p.N = N;
-  p.K = K;
+  p.K = K / ebytes_den;          // in bytes of the operand rows: 128 per stage
   p.R_cap = R_cap;
   p.sfa = static_cast<const uint8_t*>(A->scale);
   p.sfb = static_cast<const uint8_t*>(B->scale);
-  p.sa = static_cast<const float*>(A->scale);
-  p.sb = static_cast<const float*>(B->scale);
+  p.sa = nv ? A->global_scale : static_cast<const float*>(A->scale);
+  p.sb = nv ? B->global_scale : static_cast<const float*>(B->scale);
   p.sa_ld = R_cap;
   p.out = out;
   p.ldo = (mode == kModeRows) ? N : K;
   p.out_f32 = out_dtype == MGQ_OUT_F32;
   p.beta = beta;
-  p.idesc = mx ? ptx::idesc_mxf8f6f4(A->dtype, B->dtype, BM, BN) : ptx::idesc_f8f6f4(A->dtype, B->dtype, BM, BN);
+  p.idesc = nv   ? ptx::idesc_mxf4nvf4_ue4m3(BM, BN)
+            : mx ? ptx::idesc_mxf8f6f4(A->dtype, B->dtype, BM, BN)
+                 : ptx::idesc_f8f6f4(A->dtype, B->dtype, BM, BN);
   p.err = err;
   cudaStream_t s = as_stream(stream);
   if (mode == kModeRows) {
     if (kind == kKindMX) return launch_gemm<kModeRows, kKindMX>(ta, tb, p, s);
     if (kind == kKindTensor) return launch_gemm<kModeRows, kKindTensor>(ta, tb, p, s);
+    if (kind == kKindNV) return launch_gemm<kModeRows, kKindNV>(ta, tb, p, s);
     return launch_gemm<kModeRows, kKindBlock>(ta, tb, p, s);
   }
   if (kind == kKindMX) return launch_gemm<kModeContract, kKindMX>(ta, tb, p, s);

@@ -30,6 +30,10 @@ int num_sms();
 int launch_transpose_u8(const uint8_t* src, int64_t src_ld, uint8_t* dst, int64_t dst_ld, const int32_t* rows_used,
                         int64_t rows_cap, int64_t cols, cudaStream_t s);
 
+// amax[g] = max |x| over each of G groups of per_group bf16 values (zeroes
+// amax first; elementwise.cu).
+int launch_amax_groups(const uint16_t* x, int64_t per_group, int64_t G, float* amax, cudaStream_t s);
+
 }  // namespace mgq
 
 #define MGQ_CHECK_ARG(cond)                 \

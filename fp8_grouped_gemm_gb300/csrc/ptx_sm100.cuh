@@ -130,6 +130,18 @@ __device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t adesc, ui
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
+// block-scaled 4-bit: e2m1 operands (two per byte), one ue4m3 scale per 16
+// elements of K (4 per row per K=64 MMA, one 32-bit tensor-memory word)
+__device__ __forceinline__ void mma_mxf4nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::
+          "r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
 // arrive once on `bar` when all previously issued tcgen05 operations of this
 // thread have completed
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -194,6 +206,11 @@ __host__ __device__ constexpr uint32_t idesc_f8f6f4(uint32_t atype, uint32_t bty
 // per MMA.
 __host__ __device__ constexpr uint32_t idesc_mxf8f6f4(uint32_t atype, uint32_t btype, uint32_t M, uint32_t N) {
   return (atype << 7) | (btype << 10) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24);
+}
+// Instruction descriptor, kind::mxf4nvf4 with ue4m3 scales (bit 23 clear):
+// e2m1 operands (format code 1), K = 64 per MMA.
+__host__ __device__ constexpr uint32_t idesc_mxf4nvf4_ue4m3(uint32_t M, uint32_t N) {
+  return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 __host__ __device__ constexpr uint32_t idesc_sf_ids(uint32_t a_id, uint32_t b_id) {
   return (b_id << 4) | (a_id << 29);

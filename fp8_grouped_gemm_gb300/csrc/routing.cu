@@ -10,6 +10,7 @@
 // training conversion API prototype" (pytorch/ao PR #2275, description).
 #include "device_common.cuh"
 #include "mgq_internal.h"
+#include "rowquant.cuh"
 
 namespace mgq {
 namespace {
@@ -143,6 +144,7 @@ struct PermuteArgs {
   uint16_t* out_bf16;      // [R_cap, H] or null
   const float* tensor_scale;
   float* amax_out;
+  float* s_out;            // NVFP4: receives s_g
   int64_t R_cap;
   int e8m0_rceil;
   int token_blocks;        // CTAs that process tokens; the rest fill padding
@@ -269,6 +271,50 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(PermuteArgs a) {
   }
 }
 
+// ---- fused permute + NVFP4 quantisation (after the amax pass over X) -----------
+__global__ void __launch_bounds__(256) permute_quant_nv_kernel(PermuteArgs a) {
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31;
+  const int H = a.H;
+  if ((int)blockIdx.x >= a.token_blocks) {
+    const int e = blockIdx.x - a.token_blocks;
+    if (e >= a.E) return;
+    const int64_t lo = a.offsets[e] + a.counts[e], hi = a.offsets[e + 1];
+    for (int64_t r = lo + warp; r < hi; r += 8) {
+      for (int c = lane * 32; c < H; c += 32 * 32)
+        *reinterpret_cast<uint4*>(a.codes + r * (H / 2) + c / 2) = make_uint4(0, 0, 0, 0);
+      for (int b4 = lane; b4 < H / 64; b4 += 32)
+        *reinterpret_cast<uint32_t*>(a.scales + tiled_scale_offset(r, (int64_t)b4 * 4, H / 64)) = 0u;
+    }
+    return;
+  }
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= a.T) return;
+  const float s_g = nv_global_scale(*a.amax_out);
+  if (t == 0 && lane == 0) *a.s_out = s_g;
+  int dest[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) dest[j] = (j < a.k) ? a.row_id_map[(int64_t)t * a.k + j] : -1;
+  for (int c0 = 0; c0 < H; c0 += 1024) {
+    const int c = c0 + lane * 32;
+    const bool act = c < H;
+    float v[32];
+    if (act) {
+      load_bf16x32(a.x + (int64_t)t * H + c, v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+    }
+    Block32nv o;
+    quantize32_nv(v, s_g, o);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j >= a.k || !act) break;
+      if (dest[j] >= 0) store32_nv(o, a.codes, a.scales, dest[j], c, H, lane);
+    }
+  }
+}
+
 // ---- byte transpose of the used rows: dst[c, r] = src[r, c] -----------------
 // 64x64 tiles through shared memory; rows >= *rows_used are skipped.
 __global__ void transpose_u8_kernel(const uint8_t* __restrict__ src, int64_t src_ld, uint8_t* __restrict__ dst,
@@ -338,8 +384,14 @@ int mgq_moe_permute(const void* x_bf16, int T, int H, const int32_t* topk_idx, i
   MGQ_CHECK_ARG(aligned16(x_bf16) && aligned16(out_bf16));
   if (q) {
     MGQ_CHECK_ARG(q->row.data && aligned16(q->row.data));
-    MGQ_CHECK_ARG(q->dtype == MGQ_E4M3 || q->dtype == MGQ_E5M2);
-    if (q->scaling == MGQ_MX32_E8M0 || q->scaling == MGQ_BLK_1x128_F32)
+    if (q->scaling == MGQ_NV16_UE4M3)
+      MGQ_CHECK_ARG(q->dtype == MGQ_E2M1 && q->row.scale && aligned16(q->row.scale) && q->amax_out &&
+                    q->tensor_scale && !q->col.data);
+    else
+      MGQ_CHECK_ARG(q->dtype == MGQ_E4M3 || q->dtype == MGQ_E5M2);
+    if (q->scaling == MGQ_NV16_UE4M3) {
+      // checked above
+    } else if (q->scaling == MGQ_MX32_E8M0 || q->scaling == MGQ_BLK_1x128_F32)
       MGQ_CHECK_ARG(q->row.scale && aligned16(q->row.scale));
     else if (q->scaling == MGQ_TENSOR_F32)
       MGQ_CHECK_ARG(q->tensor_scale != nullptr);
@@ -377,6 +429,7 @@ int mgq_moe_permute(const void* x_bf16, int T, int H, const int32_t* topk_idx, i
   a.out_bf16 = static_cast<uint16_t*>(out_bf16);
   a.tensor_scale = q ? q->tensor_scale : nullptr;
   a.amax_out = q ? q->amax_out : nullptr;
+  a.s_out = q ? q->tensor_scale : nullptr;
   a.R_cap = R_cap;
   a.e8m0_rceil = q ? (q->e8m0_mode == MGQ_E8M0_RCEIL) : 1;
   a.token_blocks = (T + 7) / 8;
@@ -386,6 +439,13 @@ int mgq_moe_permute(const void* x_bf16, int T, int H, const int32_t* topk_idx, i
     return MGQ_ERR_UNSUPPORTED;   // bf16-only dispatch is not needed by the layer
   }
   const int sc = q->scaling, dt = q->dtype;
+  if (sc == MGQ_NV16_UE4M3) {
+    int rc = launch_amax_groups(a.x, (int64_t)T * H, 1, q->amax_out, s);
+    if (rc != MGQ_OK) return rc;
+    permute_quant_nv_kernel<<<grid, 256, 0, s>>>(a);
+    MGQ_LAUNCH_CHECK();
+    return MGQ_OK;
+  }
 #define MGQ_PERMUTE_LAUNCH(SC, DT) permute_quant_kernel<SC, DT><<<grid, 256, 0, s>>>(a)
   if (sc == MGQ_MX32_E8M0 && dt == MGQ_E4M3) MGQ_PERMUTE_LAUNCH(MGQ_MX32_E8M0, MGQ_E4M3);
   else if (sc == MGQ_MX32_E8M0 && dt == MGQ_E5M2) MGQ_PERMUTE_LAUNCH(MGQ_MX32_E8M0, MGQ_E5M2);

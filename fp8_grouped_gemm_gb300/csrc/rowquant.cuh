@@ -91,3 +91,53 @@ __device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
 }
 
 }  // namespace mgq
+
+namespace mgq {
+
+// ---- NVFP4: e2m1 elements, ue4m3 scale per 16 elements, float32 global scale --
+
+// s_g = 6 * 448 / amax of the tensor (float32 IEEE division); 1 for an
+// all-zero tensor; the largest float32 on overflow.
+__device__ __forceinline__ float nv_global_scale(float amax) {
+  if (amax == 0.0f) return 1.0f;
+  const float s = __fdiv_rn(2688.0f, amax);
+  return isinf(s) ? 3.40282347e38f : s;
+}
+
+struct Block32nv {
+  uint32_t cw[4];   // 32 e2m1 codes, element 2i in the low nibble of byte i
+  uint32_t s4;      // the 4 ue4m3 scale bytes of lanes 2j, 2j+1 (valid in lane 2j)
+};
+
+// Lane's 32 elements = two 16-element blocks. Block scale code =
+// ue4m3(float32(amax_b / 6) * s_g); with sc its value, r = s_g / sc (0 when
+// sc is 0) and each element is e2m1(x * r). All 32 lanes must call it.
+__device__ __forceinline__ void quantize32_nv(const float* v, float s_g, Block32nv& o) {
+  uint32_t sc2 = 0;
+#pragma unroll
+  for (int blk = 0; blk < 2; ++blk) {
+    const float* vb = v + 16 * blk;
+    const float amax_b = __uint_as_float(absmax_bits_f32(vb, 16));
+    const float t = __fmul_rn(__fdiv_rn(amax_b, 6.0f), s_g);
+    const uint32_t code = cvt_ue4m3(t);
+    const float sc = ue4m3_value(code);
+    const float r = (sc == 0.0f) ? 0.0f : __fdiv_rn(s_g, sc);
+    float y[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(vb[i], r);
+    o.cw[2 * blk] = cvt_e2m1x8(y);
+    o.cw[2 * blk + 1] = cvt_e2m1x8(y + 8);
+    sc2 |= code << (8 * blk);
+  }
+  const uint32_t nb = __shfl_down_sync(0xFFFFFFFFu, sc2, 1);
+  o.s4 = sc2 | (nb << 16);
+}
+
+// row r, elements [c, c + 32) of a matrix with `ld` elements per row (ld/2 bytes)
+__device__ __forceinline__ void store32_nv(const Block32nv& o, uint8_t* codes, uint8_t* scales, int64_t r, int64_t c,
+                                           int64_t ld, uint32_t lane) {
+  *reinterpret_cast<uint4*>(codes + r * (ld / 2) + c / 2) = make_uint4(o.cw[0], o.cw[1], o.cw[2], o.cw[3]);
+  if ((lane & 1) == 0) *reinterpret_cast<uint32_t*>(scales + tiled_scale_offset(r, c / 16, ld / 64)) = o.s4;
+}
+
+}  // namespace mgq

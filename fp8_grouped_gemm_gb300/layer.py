@@ -30,11 +30,12 @@ class ExpertLayer:
         self.w = w
         self.dev = torch.device(device)
         self.recipe = recipe or w.recipe
-        if self.recipe not in ("mxfp8", "delayed", "blockwise"):
+        if self.recipe not in ("mxfp8", "delayed", "blockwise", "nvfp4"):
             raise NotImplementedError(self.recipe)
         self.train = self.recipe == "delayed"
         self.scaling = {"mxfp8": mgq.MX32_E8M0, "delayed": mgq.TENSOR_F32,
-                        "blockwise": mgq.BLK_1x128_F32}[self.recipe]
+                        "blockwise": mgq.BLK_1x128_F32, "nvfp4": mgq.NV16_UE4M3}[self.recipe]
+        self.nv = self.recipe == "nvfp4"
         E, k, T, H, F = w.E, w.k, w.T, w.H, w.F
         self.R_cap = mgq.r_cap(T, k, E, ALIGN)
         R = self.R_cap
@@ -51,6 +52,9 @@ class ExpertLayer:
         self.offsets = torch.empty(E + 1, **i32)
         self.counts = torch.empty(E, **i32)
         self.ws = torch.empty(max(16, mgq.permute_workspace_size(T, k, E)), **u8)
+        if self.nv:
+            self._alloc_nvfp4(w, R)
+            return
         # activations
         self.xq = torch.empty(R, H, **u8)
         self.xs = torch.empty(mgq.mx_scale_bytes(R, H), **u8) if mx else None
@@ -98,6 +102,45 @@ class ExpertLayer:
             self.dxp = torch.empty(R, H, **bf)
             self.dx = torch.empty(T, H, **bf)
 
+    def _alloc_nvfp4(self, w, R):
+        """NVFP4 buffers: e2m1 codes two per byte, tiled ue4m3 scales, and the
+        per-tensor (per-expert for weights) amax and global scale s_g:
+        [x, h, w1 x E, w2 x E]."""
+        E, T, H, F = w.E, w.T, w.H, w.F
+        d = self.dev
+        u8 = dict(dtype=torch.uint8, device=d)
+        self.xq = torch.empty(R, H // 2, **u8)
+        self.xs = torch.empty(mgq.nv_scale_bytes(R, H), **u8)
+        self.gu = torch.empty(R, 2 * F, dtype=torch.bfloat16, device=d)
+        self.h_bf16 = torch.empty(R, F, dtype=torch.bfloat16, device=d)
+        self.hq = torch.empty(R, F // 2, **u8)
+        self.hs = torch.empty(mgq.nv_scale_bytes(R, F), **u8)
+        self.y = torch.empty(R, H, dtype=torch.bfloat16, device=d)
+        self.out = torch.empty(T, H, dtype=torch.bfloat16, device=d)
+        self.w1q = torch.empty(E, 2 * F, H // 2, **u8)
+        self.w1s = torch.empty(mgq.nv_scale_bytes(E * 2 * F, H), **u8)
+        self.w2q = torch.empty(E, H, F // 2, **u8)
+        self.w2s = torch.empty(mgq.nv_scale_bytes(E * H, F), **u8)
+        self.nv_amax = torch.zeros(2 + 2 * E, dtype=torch.float32, device=d)
+        self.nv_sg = torch.ones(2 + 2 * E, dtype=torch.float32, device=d)
+
+    def _nv_forward(self, x, topk_idx, probs, stream):
+        E, H, F, R = self.w.E, self.w.H, self.w.F, self.R_cap
+        a, g = self.nv_amax, self.nv_sg
+        qx = mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, self.xq, self.xs, tensor_scale=g[0:1], amax_out=a[0:1])
+        mgq.moe_permute(x, topk_idx, E, ALIGN, qx, R, self.row_id_map, self.src_row, self.offsets,
+                        self.counts, self.ws, None, stream)
+        mgq.grouped_gemm_fwd(mgq.operand(self.xq, self.xs, H, mgq.E2M1, g[0:1]),
+                             mgq.operand(self.w1q, self.w1s, H, mgq.E2M1, g[2:2 + E]),
+                             mgq.NV16_UE4M3, self.offsets, E, R, 2 * F, H, self.gu, mgq.OUT_BF16, stream)
+        qh = mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, self.hq, self.hs, tensor_scale=g[1:2], amax_out=a[1:2])
+        mgq.swiglu_quantize(self.gu, R, F, self.offsets, E, qh, self.h_bf16, stream)
+        mgq.grouped_gemm_fwd(mgq.operand(self.hq, self.hs, F, mgq.E2M1, g[1:2]),
+                             mgq.operand(self.w2q, self.w2s, F, mgq.E2M1, g[2 + E:2 + 2 * E]),
+                             mgq.NV16_UE4M3, self.offsets, E, R, H, F, self.y, mgq.OUT_BF16, stream)
+        mgq.moe_unpermute(self.y, self.row_id_map, probs, self.out, stream)
+        return self.out
+
     # ---- scale views (delayed recipe) ------------------------------------------
     def _fs(self, i, n=1):
         return self.fwd_scale[i:i + n]
@@ -109,7 +152,13 @@ class ExpertLayer:
     def quantize_weights(self, w1, w2, stream=None):
         """w1 bf16 [E, 2F, H], w2 bf16 [E, H, F] on the device."""
         E = self.w.E
-        if self.scaling == mgq.MX32_E8M0:
+        if self.nv:
+            a, g = self.nv_amax, self.nv_sg
+            mgq.block_quantize(w1, mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, self.w1q, self.w1s,
+                                             tensor_scale=g[2:2 + E], amax_out=a[2:2 + E]), stream)
+            mgq.block_quantize(w2, mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, self.w2q, self.w2s,
+                                             tensor_scale=g[2 + E:], amax_out=a[2 + E:]), stream)
+        elif self.scaling == mgq.MX32_E8M0:
             mgq.block_quantize(w1, mgq.qdesc(mgq.E4M3, self.scaling, self.w1q, self.w1s), stream)
             mgq.block_quantize(w2, mgq.qdesc(mgq.E4M3, self.scaling, self.w2q, self.w2s), stream)
         elif self.scaling == mgq.BLK_1x128_F32:
@@ -123,6 +172,8 @@ class ExpertLayer:
 
     # ---- forward ------------------------------------------------------------------
     def forward(self, x, topk_idx, probs, stream=None):
+        if self.nv:
+            return self._nv_forward(x, topk_idx, probs, stream)
         w, E, H, F, R = self.w, self.w.E, self.w.H, self.w.F, self.R_cap
         mx = self.scaling in (mgq.MX32_E8M0, mgq.BLK_1x128_F32)    # scales beside the codes
         if mx:
@@ -188,6 +239,8 @@ class ExpertLayer:
         E = self.w.E
         n_route = 3 if self.w.T * self.w.k > 0 else 1
         fwd = n_route + 1 + 1 + 1 + 1 + 1               # route, permute-quant, gemm1, swiglu, gemm2, unpermute
+        if self.nv:
+            return fwd + 2 + 4                          # + amax passes (x, h); weights: 2 x (amax + rows)
         if not self.train:
             return fwd + 2                              # weight quantisation (row)
         fwd += 2                                        # col transposes of x and h

@@ -53,7 +53,7 @@ class QDesc(ctypes.Structure):
 
 class Operand(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("ld", ctypes.c_int64),
-                ("dtype", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("global_scale", ctypes.c_void_p)]
 
 
 _lib = None
@@ -125,8 +125,8 @@ def qdesc(dtype, scaling, row_data, row_scale=None, col_data=None, col_scale=Non
                  QBuf(_p(col_data), _p(col_scale)), _p(tensor_scale), _p(amax_out))
 
 
-def operand(data, scale, ld, dtype) -> Operand:
-    return Operand(_p(data), _p(scale), int(ld), int(dtype))
+def operand(data, scale, ld, dtype, global_scale=None) -> Operand:
+    return Operand(_p(data), _p(scale), int(ld), int(dtype), _p(global_scale))
 
 
 # ---- sizes of the caller-owned buffers (host arithmetic only) ----------------
@@ -140,6 +140,11 @@ def r_cap(T: int, k: int, E: int, align: int) -> int:
 def mx_scale_bytes(rows: int, ld: int) -> int:
     """Bytes of the 128x4-tiled E8M0 scales of a [rows, ld] matrix."""
     return (rows + 127) // 128 * 128 * (ld // 32)
+
+
+def nv_scale_bytes(rows: int, ld: int) -> int:
+    """Bytes of the 128x4-tiled ue4m3 scales (one per 16 elements) of a [rows, ld] matrix."""
+    return (rows + 127) // 128 * 128 * (ld // 16)
 
 
 def permute_workspace_size(T: int, k: int, E: int) -> int:

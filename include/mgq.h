@@ -106,8 +106,12 @@ typedef struct {
   int e8m0_mode;             /* mgq_e8m0_mode (MX only)                         */
   mgq_qbuf row;              /* row-wise output; row.data required              */
   mgq_qbuf col;              /* column-wise (transposed) output; col.data NULL = none */
-  const float* tensor_scale; /* device: s (MGQ_TENSOR_F32) or s_g (NVFP4); per group */
-  float* amax_out;           /* device, optional: atomic max of |x| per group   */
+  float* tensor_scale;       /* device, per group: MGQ_TENSOR_F32: the scale s to
+                                apply (read); MGQ_NV16_UE4M3: receives s_g
+                                = 2688 / amax (written)                        */
+  float* amax_out;           /* device, per group: max |x| (MGQ_TENSOR_F32:
+                                optional, atomically raised; MGQ_NV16_UE4M3:
+                                required, computed by the call)                 */
 } mgq_qdesc;
 
 /* A quantised GEMM operand (device pointers). */
@@ -116,6 +120,7 @@ typedef struct {
   const void* scale;         /* block scales, or device float s per tensor/group */
   int64_t ld;                /* row pitch in elements                          */
   int dtype;                 /* mgq_dtype                                       */
+  const float* global_scale; /* NVFP4: device s_g per tensor (A) / per expert (W); else NULL */
 } mgq_operand;
 
 /* ---- status --------------------------------------------------------------- */

@@ -81,6 +81,10 @@ def check_elementwise(ref: np.ndarray, got: np.ndarray, what: str):
 
 def _q_rows(x, recipe):
     """Oracle row-wise quantisation of activations: (codes, scales, dequantised)."""
+    if recipe == "nvfp4":
+        sg = OQ.nvfp4_global_scale(np.max(np.abs(x)) if x.size else 0.0)
+        c, s = OQ.quantize_nvfp4(x, sg)
+        return c, s, OQ.dequantize_nvfp4(c, s, sg, x.shape[1])
     if recipe == "mxfp8":
         c, s = OQ.quantize_mx(x, "e4m3")
         return c, s, OQ.dequantize_mx(c, s)
@@ -89,6 +93,8 @@ def _q_rows(x, recipe):
 
 
 def _q_weight(w, recipe):
+    if recipe == "nvfp4":
+        return _q_rows(w, recipe)
     if recipe == "mxfp8":
         c, s = OQ.quantize_mx(w, "e4m3")
         return c, s, OQ.dequantize_mx(c, s)
@@ -97,6 +103,8 @@ def _q_weight(w, recipe):
 
 
 def _gpu_row_scales(lay, buf, rows_cap, ld, recipe):
+    if recipe == "nvfp4":
+        return untile_mx_scales(u8_np(buf), rows_cap, ld, block=16)
     if recipe == "mxfp8":
         return untile_mx_scales(u8_np(buf), rows_cap, ld)
     return buf.detach().cpu().numpy().T          # [K/128][R_cap] -> [R_cap, K/128]
@@ -143,6 +151,16 @@ def run_fwd_and_check(w, device, recipe: str = "mxfp8") -> dict:
         cw2, sw2, dw2 = _q_weight(w2f.reshape(E * H, F), recipe)
         assert np.array_equal(untile_mx_scales(u8_np(lay.w1s), E * 2 * F, H), sw1)
         assert np.array_equal(untile_mx_scales(u8_np(lay.w2s), E * H, F), sw2)
+    elif recipe == "nvfp4":
+        q1 = [_q_weight(w1f[e], recipe) for e in range(E)]
+        q2 = [_q_weight(w2f[e], recipe) for e in range(E)]
+        cw1 = np.concatenate([q[0] for q in q1]); dw1 = np.concatenate([q[2] for q in q1])
+        cw2 = np.concatenate([q[0] for q in q2]); dw2 = np.concatenate([q[2] for q in q2])
+        assert np.array_equal(untile_mx_scales(u8_np(lay.w1s), E * 2 * F, H, 16), np.concatenate([q[1] for q in q1]))
+        assert np.array_equal(untile_mx_scales(u8_np(lay.w2s), E * H, F, 16), np.concatenate([q[1] for q in q2]))
+        sgs = [OQ.nvfp4_global_scale(np.max(np.abs(w1f[e]))) for e in range(E)] + \
+              [OQ.nvfp4_global_scale(np.max(np.abs(w2f[e]))) for e in range(E)]
+        assert np.array_equal(lay.nv_sg.cpu().numpy()[2:], np.array(sgs, dtype=np.float32))
     else:
         q1 = [_q_weight(w1f[e], recipe) for e in range(E)]
         q2 = [_q_weight(w2f[e], recipe) for e in range(E)]
@@ -150,8 +168,8 @@ def run_fwd_and_check(w, device, recipe: str = "mxfp8") -> dict:
         cw2 = np.concatenate([q[0] for q in q2]); dw2 = np.concatenate([q[2] for q in q2])
         assert np.array_equal(lay.w1s.cpu().numpy(), np.stack([q[1] for q in q1]))
         assert np.array_equal(lay.w2s.cpu().numpy(), np.stack([q[1] for q in q2]))
-    assert np.array_equal(u8_np(lay.w1q).reshape(E * 2 * F, H), cw1)
-    assert np.array_equal(u8_np(lay.w2q).reshape(E * H, F), cw2)
+    assert np.array_equal(u8_np(lay.w1q).reshape(E * 2 * F, -1), cw1)
+    assert np.array_equal(u8_np(lay.w2q).reshape(E * H, -1), cw2)
     # gate/up GEMM on the identical quantised inputs
     a_deq = _q_rows(xf, recipe)[2]
     a_deq = OR.permute_rows(a_deq, rim, Rp, fill=0.0)

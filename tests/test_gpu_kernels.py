@@ -52,7 +52,7 @@ PERMUTE_CASES = [
 
 
 @pytest.mark.parametrize("case", PERMUTE_CASES, ids=lambda c: f"T{c[0]}E{c[1]}k{c[2]}H{c[3]}a{c[4]}")
-@pytest.mark.parametrize("mode", ["mx_e4m3", "mx_e5m2", "tensor_e4m3", "blk_e4m3"])
+@pytest.mark.parametrize("mode", ["mx_e4m3", "mx_e5m2", "tensor_e4m3", "blk_e4m3", "nvfp4"])
 def test_permute_quantize(mgq, case, mode):
     T, E, k, H, align, empty = case
     rng = np.random.default_rng(T * 7 + E)
@@ -68,11 +68,16 @@ def test_permute_quantize(mgq, case, mode):
     off = torch.empty(E + 1, dtype=torch.int32, device=dev)
     cnt = torch.empty(E, dtype=torch.int32, device=dev)
     ws = torch.empty(mgq.permute_workspace_size(T, k, E), dtype=torch.uint8, device=dev)
-    codes = torch.full((R, H), 0xAB, dtype=torch.uint8, device=dev)
+    codes = torch.full((R, H // 2 if mode == "nvfp4" else H), 0xAB, dtype=torch.uint8, device=dev)
     fmt = "e5m2" if "e5m2" in mode else "e4m3"
     dt = mgq.E5M2 if fmt == "e5m2" else mgq.E4M3
     xf = bf16_np(x)
-    if mode.startswith("mx"):
+    if mode == "nvfp4":
+        sc = torch.full((mgq.nv_scale_bytes(R, H),), 0xCD, dtype=torch.uint8, device=dev)
+        amax = torch.full((1,), 7.0, dtype=torch.float32, device=dev)     # overwritten by the call
+        sg = torch.zeros(1, dtype=torch.float32, device=dev)
+        q = mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, codes, sc, tensor_scale=sg, amax_out=amax)
+    elif mode.startswith("mx"):
         sc = torch.full((mgq.mx_scale_bytes(R, H),), 0xCD, dtype=torch.uint8, device=dev)
         q = mgq.qdesc(dt, mgq.MX32_E8M0, codes, sc)
     elif mode.startswith("blk"):
@@ -92,7 +97,14 @@ def test_permute_quantize(mgq, case, mode):
     assert np.array_equal(cnt.cpu().numpy(), w_cnt)
     assert np.array_equal(rim.cpu().numpy(), w_rim)
     assert np.array_equal(src.cpu().numpy()[:Rp], w_src)
-    if mode.startswith("mx"):
+    if mode == "nvfp4":
+        am = float(np.max(np.abs(xf)))
+        s_g = OQ.nvfp4_global_scale(am)
+        assert float(amax.item()) == am and float(sg.item()) == float(s_g)
+        c, s = OQ.quantize_nvfp4(xf, s_g)
+        assert np.array_equal(u8_np(codes)[:Rp], OR.permute_rows(c, w_rim, Rp))
+        assert np.array_equal(untile_mx_scales(u8_np(sc), R, H, 16)[:Rp], OR.permute_rows(s, w_rim, Rp))
+    elif mode.startswith("mx"):
         c, s = OQ.quantize_mx(xf, fmt)
         assert np.array_equal(u8_np(codes)[:Rp], OR.permute_rows(c, w_rim, Rp))
         assert np.array_equal(untile_mx_scales(u8_np(sc), R, H)[:Rp], OR.permute_rows(s, w_rim, Rp))
@@ -322,6 +334,42 @@ def test_gemm_fwd_blockwise(mgq, offs):
     assert rel_fro(OF.round_to_bf16(ref), got[:Rp]) <= GEMM_TOL_BF16
 
 
+@pytest.mark.parametrize("offs", [[0, 128, 128, 512], [0, 256]], ids=["E3", "E1"])
+def test_gemm_fwd_nvfp4(mgq, offs):
+    """e2m1 x e2m1 with 16-element ue4m3 block scales (kind::mxf4nvf4,
+    scale_vec::4X) and a float32 global scale per tensor / per expert."""
+    rng = np.random.default_rng(51)
+    dev = torch.device(DEV)
+    E = len(offs) - 1
+    N, K = 512, 768
+    Rp = offs[-1]
+    R_cap = Rp + 128
+    qa = rng.integers(0, 16, size=(R_cap, K)).astype(np.uint8)
+    qw = rng.integers(0, 16, size=(E * N, K)).astype(np.uint8)
+    pack = lambda q: ((q[:, 0::2] & 0xF) | ((q[:, 1::2] & 0xF) << 4)).astype(np.uint8)
+    sca = rng.integers(0x20, 0x58, size=(R_cap, K // 16)).astype(np.uint8)       # ue4m3 codes
+    scw = rng.integers(0x20, 0x58, size=(E * N, K // 16)).astype(np.uint8)
+    sga = np.array([2.5], dtype=np.float32)
+    sgw = np.exp2(rng.uniform(-3, 3, size=E)).astype(np.float32)
+    Y = torch.full((R_cap, N), float("nan"), dtype=torch.bfloat16, device=dev)
+    ga, gw = _to_dev(sga, dev), _to_dev(sgw, dev)
+    A = _op(mgq, pack(qa), tile_mx_scales(sca), K, mgq.E2M1, dev)
+    A.global_scale = ga.data_ptr()
+    Wo = _op(mgq, pack(qw), tile_mx_scales(scw), K, mgq.E2M1, dev)
+    Wo.global_scale = gw.data_ptr()
+    offd = torch.tensor(offs, dtype=torch.int32, device=dev)
+    mgq.grouped_gemm_fwd(A, Wo, mgq.NV16_UE4M3, offd, E, R_cap, N, K, Y)
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    a_deq = OQ.dequantize_nvfp4(pack(qa)[:Rp], sca[:Rp], sga[0], K)
+    w_deq = np.stack([OQ.dequantize_nvfp4(pack(qw)[e * N:(e + 1) * N], scw[e * N:(e + 1) * N], sgw[e], K)
+                      for e in range(E)])
+    ref = OG.grouped_gemm_fwd(a_deq, w_deq, np.array(offs))
+    got = bf16_np(Y)
+    assert np.all(np.isnan(got[Rp:]))
+    assert rel_fro(OF.round_to_bf16(ref), got[:Rp]) <= GEMM_TOL_BF16
+
+
 def test_gemm_grouped_equals_per_group(mgq):
     """The grouped call equals single-group calls on each expert's rows
     (grouped vs discrete comparison of Megatron-LM PR #5487's test matrix),
@@ -485,7 +533,7 @@ def test_unpermute_bwd_quantize(mgq, mode):
         assert np.array_equal(untile_mx_scales(u8_np(sc), R, H)[:Rp], s_)
 
 
-@pytest.mark.parametrize("mode", ["mx", "tensor", "blk128"])
+@pytest.mark.parametrize("mode", ["mx", "tensor", "blk128", "nvfp4"])
 def test_block_quantize_weights(mgq, mode):
     rng = np.random.default_rng(13)
     dev = torch.device(DEV)
@@ -493,6 +541,24 @@ def test_block_quantize_weights(mgq, mode):
     w = _bf16(rng, (G, M, K), 0.02)
     codes = torch.empty(G, M, K, dtype=torch.uint8, device=dev)
     wf = bf16_np(w)
+    if mode == "nvfp4":
+        w[0, 3, 4] = 0.5
+        wf = bf16_np(w)
+        cnv = torch.empty(G, M, K // 2, dtype=torch.uint8, device=dev)
+        sc = torch.empty(mgq.nv_scale_bytes(G * M, K), dtype=torch.uint8, device=dev)
+        amax = torch.empty(G, dtype=torch.float32, device=dev)
+        sg = torch.empty(G, dtype=torch.float32, device=dev)
+        mgq.block_quantize(w.to(dev), mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, cnv, sc, tensor_scale=sg, amax_out=amax))
+        torch.cuda.synchronize()
+        s_all = untile_mx_scales(u8_np(sc), G * M, K, 16).reshape(G, M, K // 16)
+        for g in range(G):
+            am = float(np.max(np.abs(wf[g])))
+            s_g = OQ.nvfp4_global_scale(am)
+            assert float(amax[g].item()) == am and float(sg[g].item()) == float(s_g)
+            c, s_ = OQ.quantize_nvfp4(wf[g], s_g)
+            assert np.array_equal(u8_np(cnv)[g], c)
+            assert np.array_equal(s_all[g], s_)
+        return
     if mode == "blk128":
         w[1, 5, 7] = 3.0                                   # one large element in one tile
         w[2] = 0                                           # all-zero tiles: scale 1

@@ -43,6 +43,16 @@ def test_scout_forward_blockwise_scaled_down():
     assert res["gemm1_sqnr_vs_bf16"] >= 28.0, res
 
 
+def test_finegrained_forward_nvfp4_scaled_down():
+    """Fine-grained MoE proportions (uniform top-8 routing) in NVFP4 (e2m1,
+    16-element ue4m3 scales, float32 global scales) at a size checked in full;
+    SQNR bar 15 dB against bf16."""
+    from fp8_grouped_gemm_gb300.workloads import WORKLOADS
+    w = WORKLOADS["finegrained_fwd"].scaled(T=1024, E=32, H=512, F=768)
+    res = run_fwd_and_check(w, DEV, recipe="nvfp4")
+    assert res["gemm1_sqnr_vs_bf16"] >= 15.0, res
+
+
 def _tensor_deq(codes, s, fmt="e4m3"):
     return OQ.dequantize_tensor(codes, np.float32(s), fmt)
 
