@@ -136,95 +136,23 @@ class Step:
         self.dout = W.make_dout(w).to(dev) if self.train else None
         self.time_kernels = time_kernels
         self.events = []
-
-    def _gemm_timed(self, fn):
-        if not self.time_kernels:
-            return fn()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        fn()
-        b.record()
-        self.events.append((a, b))
+        self.ops = None
 
     def __call__(self):
-        lay = self.lay
+        if self.ops is None:
+            self.ops = self.lay.step_ops(self.w1, self.w2, self.x, self.idx, self.probs, self.dout)
         if not self.time_kernels:
-            lay.quantize_weights(self.w1, self.w2)
-            lay.forward(self.x, self.idx, self.probs)
-            if self.train:
-                lay.backward(self.dout, self.probs)
-                lay.update_scaling()
+            for _, op in self.ops:
+                op()
             return
-        # same sequence, with events around every launch group
+        # the same sequence, with events around every launch group
         ev = {}
-
-        def rec(name, fn):
+        for name, op in self.ops:
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
-            fn()
+            op()
             b.record()
             ev.setdefault(name, []).append((a, b))
-        from fp8_grouped_gemm_gb300 import mgq
-        w, E, H, F, R = self.w, self.w.E, self.w.H, self.w.F, lay.R_cap
-        mx = lay.scaling in (mgq.MX32_E8M0, mgq.BLK_1x128_F32)     # block scales beside the codes
-        rec("weight_quant", lambda: lay.quantize_weights(self.w1, self.w2))
-        if lay.nv:
-            a, g = lay.nv_amax, lay.nv_sg
-            qx = mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, lay.xq, lay.xs, tensor_scale=g[0:1], amax_out=a[0:1])
-            rec("permute_quant", lambda: mgq.moe_permute(self.x, self.idx, E, 128, qx, R, lay.row_id_map,
-                                                         lay.src_row, lay.offsets, lay.counts, lay.ws, None))
-            A1 = mgq.operand(lay.xq, lay.xs, H, mgq.E2M1, g[0:1])
-            B1 = mgq.operand(lay.w1q, lay.w1s, H, mgq.E2M1, g[2:2 + E])
-            rec("gemm", lambda: mgq.grouped_gemm_fwd(A1, B1, mgq.NV16_UE4M3, lay.offsets, E, R, 2 * F, H, lay.gu))
-            qh = mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, lay.hq, lay.hs, tensor_scale=g[1:2], amax_out=a[1:2])
-            rec("swiglu_quant", lambda: mgq.swiglu_quantize(lay.gu, R, F, lay.offsets, E, qh, lay.h_bf16))
-            A2 = mgq.operand(lay.hq, lay.hs, F, mgq.E2M1, g[1:2])
-            B2 = mgq.operand(lay.w2q, lay.w2s, F, mgq.E2M1, g[2 + E:2 + 2 * E])
-            rec("gemm", lambda: mgq.grouped_gemm_fwd(A2, B2, mgq.NV16_UE4M3, lay.offsets, E, R, H, F, lay.y))
-            rec("unpermute", lambda: mgq.moe_unpermute(lay.y, lay.row_id_map, self.probs, lay.out))
-            self.events.append(ev)
-            return
-        if mx:
-            qx = mgq.qdesc(mgq.E4M3, lay.scaling, lay.xq, lay.xs)
-        else:
-            qx = mgq.qdesc(mgq.E4M3, lay.scaling, lay.xq, None, lay.xcol, None, lay._fs(0), lay._fa(0))
-        rec("permute_quant", lambda: mgq.moe_permute(self.x, self.idx, E, 128, qx, R, lay.row_id_map, lay.src_row,
-                                                     lay.offsets, lay.counts, lay.ws, None))
-        sa = lay.xs if mx else lay._fs(0)
-        sw1 = lay.w1s if mx else lay._fs(2, E)
-        A1 = mgq.operand(lay.xq, sa, H, mgq.E4M3)
-        B1 = mgq.operand(lay.w1q, sw1, H, mgq.E4M3)
-        rec("gemm", lambda: mgq.grouped_gemm_fwd(A1, B1, lay.scaling, lay.offsets, E, R, 2 * F, H, lay.gu))
-        if mx:
-            qh = mgq.qdesc(mgq.E4M3, lay.scaling, lay.hq, lay.hs)
-        else:
-            qh = mgq.qdesc(mgq.E4M3, lay.scaling, lay.hq, None, lay.hcol, None, lay._fs(1), lay._fa(1))
-        rec("swiglu_quant", lambda: mgq.swiglu_quantize(lay.gu, R, F, lay.offsets, E, qh, None))
-        sh = lay.hs if mx else lay._fs(1)
-        sw2 = lay.w2s if mx else lay._fs(2 + E, E)
-        A2 = mgq.operand(lay.hq, sh, F, mgq.E4M3)
-        B2 = mgq.operand(lay.w2q, sw2, F, mgq.E4M3)
-        rec("gemm", lambda: mgq.grouped_gemm_fwd(A2, B2, lay.scaling, lay.offsets, E, R, H, F, lay.y))
-        rec("unpermute", lambda: mgq.moe_unpermute(lay.y, lay.row_id_map, self.probs, lay.out))
-        if self.train:
-            sdy2, sdy1 = lay.bwd_scale[0:1], lay.bwd_scale[1:2]
-            q2 = mgq.qdesc(mgq.E5M2, mgq.TENSOR_F32, lay.dy2q, None, lay.dy2col, None, sdy2, lay.bwd_amax[0:1])
-            rec("unpermute_bwd_quant", lambda: mgq.moe_unpermute_bwd(self.dout, lay.y, lay.row_id_map, lay.src_row,
-                                                                     self.probs, R, lay.offsets, E, q2, lay.dprobs))
-            o = [mgq.operand(lay.dy2q, sdy2, H, mgq.E5M2), mgq.operand(lay.w2col, lay._fs(2 + E, E), H, mgq.E4M3),
-                 mgq.operand(lay.dy2col, sdy2, R, mgq.E5M2), mgq.operand(lay.hcol, lay._fs(1), R, mgq.E4M3)]
-            rec("gemm", lambda: mgq.grouped_gemm_dgrad(o[0], o[1], mgq.TENSOR_F32, lay.offsets, E, R, H, F, lay.dh))
-            rec("gemm", lambda: mgq.grouped_gemm_wgrad(o[2], o[3], mgq.TENSOR_F32, lay.offsets, E, R, H, F, lay.dw2))
-            q1 = mgq.qdesc(mgq.E5M2, mgq.TENSOR_F32, lay.dy1q, None, lay.dy1col, None, sdy1, lay.bwd_amax[1:2])
-            rec("dswiglu_quant", lambda: mgq.dswiglu_quantize(lay.dh, lay.gu, R, F, lay.offsets, E, q1, None))
-            p = [mgq.operand(lay.dy1q, sdy1, 2 * F, mgq.E5M2), mgq.operand(lay.w1col, lay._fs(2, E), 2 * F, mgq.E4M3),
-                 mgq.operand(lay.dy1col, sdy1, R, mgq.E5M2), mgq.operand(lay.xcol, lay._fs(0), R, mgq.E4M3)]
-            rec("gemm", lambda: mgq.grouped_gemm_dgrad(p[0], p[1], mgq.TENSOR_F32, lay.offsets, E, R, 2 * F, H,
-                                                       lay.dxp))
-            rec("gemm", lambda: mgq.grouped_gemm_wgrad(p[2], p[3], mgq.TENSOR_F32, lay.offsets, E, R, 2 * F, H,
-                                                       lay.dw1))
-            rec("permute_bwd", lambda: mgq.moe_permute_bwd(lay.dxp, lay.row_id_map, lay.dx))
-            rec("scaling_update", lambda: lay.update_scaling())
         self.events.append(ev)
 
 
@@ -316,16 +244,23 @@ def oracle_sample(w, rows=512, f_slice=1024):
     OR.unpermute(y, rim, probs)
     flops = 2.0 * rows * H * 2 * Fs + 2.0 * rows * Fs * H
     if w.backward:
+        def q_grad(a):
+            if w.recipe == "mxfp8":          # row-wise copy for dgrad, column-wise for wgrad
+                c, sc = OQ.quantize_mx(a, "e5m2")
+                ct, st = OQ.quantize_mx(a.T, "e5m2")
+                return OQ.dequantize_mx(c, sc, "e5m2"), OQ.dequantize_mx(ct, st, "e5m2").T
+            c, _ = OQ.quantize_tensor(a, s, "e5m2")
+            d = OQ.dequantize_tensor(c, s, "e5m2")
+            return d, d
+
         dy32, _ = OR.unpermute_bwd(dout, y, rim, probs, rows)
-        cdy, _ = OQ.quantize_tensor(dy32.astype(np.float64), s, "e5m2")
-        dyd = OQ.dequantize_tensor(cdy, s, "e5m2")
-        dh = round_to_bf16(OG.grouped_gemm_dgrad(dyd, w2d, off))
-        OG.grouped_gemm_wgrad(dyd, hd, off, 1)
+        dy_r, dy_c = q_grad(dy32.astype(np.float64))
+        dh = round_to_bf16(OG.grouped_gemm_dgrad(dy_r, w2d, off))
+        OG.grouped_gemm_wgrad(dy_c, hd, off, 1)
         dgu = round_to_bf16(OL.dswiglu(dh, gu, Fs))
-        cd1, _ = OQ.quantize_tensor(dgu, s, "e5m2")
-        d1 = OQ.dequantize_tensor(cd1, s, "e5m2")
-        dxp = round_to_bf16(OG.grouped_gemm_dgrad(d1, w1d, off))
-        OG.grouped_gemm_wgrad(d1, xd, off, 1)
+        d1_r, d1_c = q_grad(dgu)
+        dxp = round_to_bf16(OG.grouped_gemm_dgrad(d1_r, w1d, off))
+        OG.grouped_gemm_wgrad(d1_c, xd, off, 1)
         OR.permute_bwd(dxp, rim)
         flops *= 3
     return time.perf_counter() - t0, flops
@@ -356,7 +291,7 @@ def run_reference(args, w, rank, world):
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot / args.steps * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE[w.recipe],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype_of(w),
         "data": "synthetic", "config": config_of(w, args),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": ncores, "kind": "oracle",
                          "sample": sample_desc(*REF_SAMPLE)},
@@ -366,9 +301,15 @@ def run_reference(args, w, rank, world):
 
 
 METRIC = "grouped FP8 GEMM fwd+bwd TFLOP/s (Mixtral-shaped expert layer step)"
-DTYPE = {"mxfp8": "e4m3 (MXFP8, f32 accumulate)", "delayed": "e4m3/e5m2 (per-tensor delayed, f32 accumulate)",
+DTYPE = {"mxfp8": "e4m3 fwd / e5m2 grads (MXFP8: E8M0 per 32, f32 accumulate)", "delayed": "e4m3/e5m2 (per-tensor delayed, f32 accumulate)",
          "blockwise": "e4m3 (1x128 / 128x128 float32 block scales, f32 accumulate)",
          "nvfp4": "e2m1 (NVFP4: 16-element ue4m3 scales + float32 global scale, f32 accumulate)"}
+def dtype_of(w):
+    if w.recipe == "mxfp8" and not w.backward:
+        return "e4m3 (MXFP8: E8M0 per 32, f32 accumulate)"
+    return DTYPE[w.recipe]
+
+
 def sample_desc(rows, f_slice):
     return (f"CPU oracle (numpy, float64 GEMMs) on one expert, {rows} routed rows, full hidden size, "
             f"a {f_slice}-wide FFN slice; same step chain as the GPU step; TFLOP/s = sample GEMM FLOPs / wall time")
@@ -520,7 +461,7 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": DTYPE[w.recipe], "data": "synthetic (seeded; shapes of the workload)",
+            "vs_baseline": None, "dtype": dtype_of(w), "data": "synthetic (seeded; shapes of the workload)",
             "config": config_of(w, args), "roofline": roofline, "hbm_kernels": hbm,
             "kernel_ms_per_step": per, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "clocks": clk,

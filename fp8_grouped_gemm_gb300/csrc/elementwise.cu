@@ -458,7 +458,10 @@ int check_q(const mgq_qdesc* q) {
   } else {
     return MGQ_ERR_UNSUPPORTED;
   }
-  if (q->col.data && (q->scaling != MGQ_TENSOR_F32 || !aligned16(q->col.data))) return MGQ_ERR_UNSUPPORTED;
+  if (q->col.data && !aligned16(q->col.data)) return MGQ_ERR_INVALID_ARG;
+  if (q->col.data && q->scaling == MGQ_MX32_E8M0 && (!q->col.scale || !aligned16(q->col.scale)))
+    return MGQ_ERR_INVALID_ARG;
+  if (q->col.data && q->scaling == MGQ_BLK_1x128_F32) return MGQ_ERR_UNSUPPORTED;
   return MGQ_OK;
 }
 
@@ -519,14 +522,14 @@ int mgq_swiglu_quantize(const void* gu_bf16, int64_t R_cap, int F, const int32_t
   MGQ_CHECK_ARG(gu_bf16 && aligned16(gu_bf16) && aligned16(h_bf16) && offsets && E >= 1);
   MGQ_CHECK_ARG(F > 0 && F % 128 == 0 && R_cap > 0 && R_cap % 128 == 0);
   cudaStream_t s = as_stream(stream);
+  if (q->col.data)
+    return rowcol_swiglu(static_cast<const uint16_t*>(gu_bf16), R_cap, F, offsets + E, static_cast<uint16_t*>(h_bf16),
+                         q, s);
   SwigluArgs a{static_cast<const uint16_t*>(gu_bf16), offsets + E, R_cap, F,
                static_cast<uint8_t*>(q->row.data), static_cast<uint8_t*>(q->row.scale),
                static_cast<uint16_t*>(h_bf16), q->tensor_scale, q->amax_out, q->e8m0_mode == MGQ_E8M0_RCEIL};
   const unsigned grid = (unsigned)((R_cap + kWarps - 1) / kWarps);
   MGQ_DISPATCH_Q(q, swiglu_quant_kernel, grid, a);
-  if (q->col.data)
-    return launch_transpose_u8(static_cast<const uint8_t*>(q->row.data), F, static_cast<uint8_t*>(q->col.data),
-                               R_cap, offsets + E, R_cap, F, s);
   return MGQ_OK;
 }
 
@@ -537,14 +540,14 @@ int mgq_dswiglu_quantize(const void* dh_bf16, const void* gu_bf16, int64_t R_cap
   MGQ_CHECK_ARG(dh_bf16 && gu_bf16 && aligned16(dh_bf16) && aligned16(gu_bf16) && aligned16(dgu_bf16));
   MGQ_CHECK_ARG(offsets && E >= 1 && F > 0 && F % 128 == 0 && R_cap > 0 && R_cap % 128 == 0);
   cudaStream_t s = as_stream(stream);
+  if (q->col.data)
+    return rowcol_dswiglu(static_cast<const uint16_t*>(dh_bf16), static_cast<const uint16_t*>(gu_bf16), R_cap, F,
+                          offsets + E, static_cast<uint16_t*>(dgu_bf16), q, s);
   DswigluArgs a{static_cast<const uint16_t*>(dh_bf16), static_cast<const uint16_t*>(gu_bf16), offsets + E, R_cap, F,
                 static_cast<uint8_t*>(q->row.data), static_cast<uint8_t*>(q->row.scale),
                 static_cast<uint16_t*>(dgu_bf16), q->tensor_scale, q->amax_out, q->e8m0_mode == MGQ_E8M0_RCEIL};
   const unsigned grid = (unsigned)((R_cap + kWarps - 1) / kWarps);
   MGQ_DISPATCH_Q(q, dswiglu_quant_kernel, grid, a);
-  if (q->col.data)
-    return launch_transpose_u8(static_cast<const uint8_t*>(q->row.data), 2 * (int64_t)F,
-                               static_cast<uint8_t*>(q->col.data), R_cap, offsets + E, R_cap, 2 * (int64_t)F, s);
   return MGQ_OK;
 }
 
@@ -598,10 +601,13 @@ int mgq_moe_unpermute_bwd(const void* dout_bf16, const void* y_bf16, const int32
   a.rceil = q->e8m0_mode == MGQ_E8M0_RCEIL;
   a.token_blocks = (T + kWarps - 1) / kWarps;
   const unsigned grid = (unsigned)(a.token_blocks + E);
+  if (q->col.data && q->scaling != MGQ_TENSOR_F32 && q->scaling != MGQ_MX32_E8M0) return MGQ_ERR_UNSUPPORTED;
   MGQ_DISPATCH_Q(q, unpermute_bwd_kernel, grid, a);
-  if (q->col.data)
+  if (q->col.data && q->scaling == MGQ_TENSOR_F32)
     return launch_transpose_u8(static_cast<const uint8_t*>(q->row.data), H, static_cast<uint8_t*>(q->col.data),
                                R_cap, offsets + E, R_cap, H, s);
+  if (q->col.data)
+    return col_gather_dy(static_cast<const uint16_t*>(dout_bf16), probs, src_row, k, H, R_cap, offsets + E, q, s);
   return MGQ_OK;
 }
 
@@ -644,18 +650,12 @@ int mgq_block_quantize(const void* x_bf16, int64_t G, int64_t M, int64_t K, cons
   if (rc != MGQ_OK) return rc;
   MGQ_CHECK_ARG(x_bf16 && aligned16(x_bf16) && G >= 1 && M > 0 && K > 0 && M % 128 == 0 && K % 128 == 0);
   cudaStream_t s = as_stream(stream);
+  if (q->col.data) return rowcol_plain(static_cast<const uint16_t*>(x_bf16), G, M, K, q, s);
   QuantRowsArgs a{static_cast<const uint16_t*>(x_bf16), G * M, M, K, static_cast<uint8_t*>(q->row.data),
                   static_cast<uint8_t*>(q->row.scale), q->tensor_scale, q->amax_out,
                   q->e8m0_mode == MGQ_E8M0_RCEIL};
   const unsigned grid = (unsigned)((G * M + kWarps - 1) / kWarps);
   MGQ_DISPATCH_Q(q, quant_rows_kernel, grid, a);
-  if (q->col.data) {
-    for (int64_t g = 0; g < G; ++g) {
-      rc = launch_transpose_u8(static_cast<const uint8_t*>(q->row.data) + g * M * K, K,
-                               static_cast<uint8_t*>(q->col.data) + g * M * K, M, nullptr, M, K, s);
-      if (rc != MGQ_OK) return rc;
-    }
-  }
   return MGQ_OK;
 }
 

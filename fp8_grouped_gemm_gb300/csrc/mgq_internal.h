@@ -34,6 +34,21 @@ int launch_transpose_u8(const uint8_t* src, int64_t src_ld, uint8_t* dst, int64_
 // amax first; elementwise.cu).
 int launch_amax_groups(const uint16_t* x, int64_t per_group, int64_t G, float* amax, cudaStream_t s);
 
+// Row-wise + column-wise quantisation in one pass (quant_tile.cu); q->col.data
+// must be set. Per-tensor or MX scaling.
+int rowcol_plain(const uint16_t* x, int64_t G, int64_t M, int64_t K, const mgq_qdesc* q, cudaStream_t s);
+int rowcol_swiglu(const uint16_t* gu, int64_t R_cap, int64_t F, const int32_t* rows_used, uint16_t* h_out,
+                  const mgq_qdesc* q, cudaStream_t s);
+int rowcol_dswiglu(const uint16_t* dh, const uint16_t* gu, int64_t R_cap, int64_t F, const int32_t* rows_used,
+                   uint16_t* out, const mgq_qdesc* q, cudaStream_t s);
+
+// Column-wise copies only (MX or per-tensor), of the permuted X rows and of
+// dY = probs * dout rows, gathered through src_row (quant_tile.cu).
+int col_gather_x(const uint16_t* x, const int32_t* src_row, int k, int64_t H, int64_t R_cap, const int32_t* rows_used,
+                 const mgq_qdesc* q, cudaStream_t s);
+int col_gather_dy(const uint16_t* dout, const float* probs, const int32_t* src_row, int k, int64_t H, int64_t R_cap,
+                  const int32_t* rows_used, const mgq_qdesc* q, cudaStream_t s);
+
 }  // namespace mgq
 
 #define MGQ_CHECK_ARG(cond)                 \

@@ -1,0 +1,312 @@
+// Row-wise and column-wise quantisation in one pass over 64 x 128 tiles.
+//
+// The backward GEMMs need every quantised activation and weight twice: blocks
+// along the rows for one GEMM and along the columns (written transposed) for
+// the other ("Numerical fix for moe single grouped weight with fp8 fp4
+// primary weight and grad norm spikes", Megatron-LM PR #5487: rowwise and
+// columnwise data and scales of one grouped tensor; "FP8BlockQuantizer not
+// work on TE", TransformerEngine issue #2393: 128x1 backward blocks with the
+// transpose done in shared memory, transpose(colwise(x)) = rowwise(x^T)).
+//
+// A CTA reads its tile once from its source functor (a plain bf16 matrix,
+// SwiGLU of the gate/up output, or dSwiGLU), keeps the float values in shared
+// memory, and writes
+//   row-wise codes [rows, C] (blocks of 32 along C for MX), and
+//   column-wise codes [C, M] per group of M rows (blocks of 32 along the rows),
+// with per-tensor scales (the column copy is then the transposed cast) or
+// E8M0 block scales in the 128x4-tiled layout.
+#include "mgq_internal.h"
+#include "rowquant.cuh"
+
+namespace mgq {
+namespace {
+
+constexpr int TR = 64, TC = 128;   // tile rows x columns
+
+struct SrcPlain {
+  static constexpr int kParts = 1;
+  const uint16_t* x;
+  int64_t ld;
+  __device__ __forceinline__ void load8(int64_t r, int64_t c, float* v, float*) const {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(x + r * ld + c));
+    v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+    v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+  }
+};
+
+__device__ __forceinline__ void load8_bf16(const uint16_t* p, float* v) {
+  const uint4 w = __ldg(reinterpret_cast<const uint4*>(p));
+  v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+  v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+}
+__device__ __forceinline__ void store8_bf16(uint16_t* p, const float* v) {
+  *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                            pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+}
+
+// h = bf16(silu(g) * u), g = gu[:, :F], u = gu[:, F:]; h optionally written out
+struct SrcSwiglu {
+  static constexpr int kParts = 1;
+  const uint16_t* gu;
+  int64_t F;
+  uint16_t* h_out;
+  __device__ __forceinline__ void load8(int64_t r, int64_t c, float* v, float*) const {
+    float g[8], u[8];
+    load8_bf16(gu + r * 2 * F + c, g);
+    load8_bf16(gu + r * 2 * F + F + c, u);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = round_bf16(__fmul_rn(__fdiv_rn(g[i], 1.0f + expf(-g[i])), u[i]));
+    if (h_out) store8_bf16(h_out + r * F + c, v);
+  }
+};
+
+// dSwiGLU: for ffn columns f..f+7 of row r, part 0 = dG = dh u s (1 + g (1 - s))
+// and part 1 = dU = dh silu(g), s = sigmoid(g); both written to [dG | dU]
+// (columns f and F + f) when requested. One read of dh, g, u serves both.
+struct SrcDswiglu {
+  static constexpr int kParts = 2;
+  const uint16_t* dh;
+  const uint16_t* gu;
+  int64_t F;
+  uint16_t* out;
+  __device__ __forceinline__ void load8(int64_t r, int64_t f, float* dg, float* du) const {
+    float d[8], g[8], u[8];
+    load8_bf16(dh + r * F + f, d);
+    load8_bf16(gu + r * 2 * F + f, g);
+    load8_bf16(gu + r * 2 * F + F + f, u);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float s = __fdiv_rn(1.0f, 1.0f + expf(-g[i]));
+      dg[i] = round_bf16(d[i] * u[i] * s * (1.0f + g[i] * (1.0f - s)));
+      du[i] = round_bf16(d[i] * g[i] * s);
+    }
+    if (out) {
+      store8_bf16(out + r * 2 * F + f, dg);
+      store8_bf16(out + r * 2 * F + F + f, du);
+    }
+  }
+};
+
+// row r of the permuted matrix: X[t] for the (token, slot) entry e = src_row[r]
+// (t = e / k), zeros for filler rows
+struct SrcGatherX {
+  static constexpr int kParts = 1;
+  const uint16_t* x;
+  const int32_t* src_row;
+  int k;
+  int64_t H;
+  __device__ __forceinline__ void load8(int64_t r, int64_t c, float* v, float*) const {
+    const int e = src_row[r];
+    if (e < 0) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+      return;
+    }
+    load8_bf16(x + (int64_t)(e / k) * H + c, v);
+  }
+};
+
+// row r of dY = float32(probs[e] * dout[t]) for the entry e = src_row[r]
+// (the unpermute backward), zeros for filler rows
+struct SrcGatherDy {
+  static constexpr int kParts = 1;
+  const uint16_t* dout;
+  const float* probs;
+  const int32_t* src_row;
+  int k;
+  int64_t H;
+  __device__ __forceinline__ void load8(int64_t r, int64_t c, float* v, float*) const {
+    const int e = src_row[r];
+    if (e < 0) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+      return;
+    }
+    load8_bf16(dout + (int64_t)(e / k) * H + c, v);
+    const float p = probs[e];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(p, v[i]);
+  }
+};
+
+struct RowColArgs {
+  int64_t rows_cap;          // rows of the row-wise output
+  const int32_t* rows_used;  // device row count or null (= rows_cap)
+  int64_t C;                 // columns of the output rows
+  int64_t part_off;          // column offset of part 1 (two-part sources)
+  int64_t M;                 // rows per group (column-wise output [G][C][M])
+  uint8_t* row_codes;        // [rows, C]
+  uint8_t* row_scales;       // MX: tiled over [rows, C]
+  uint8_t* col_codes;        // [G][C][M] or null
+  uint8_t* col_scales;       // MX: tiled over [G*C, M]
+  const float* tensor_scale; // per group (TENSOR)
+  float* amax_out;           // per group, optional
+  int rceil;
+};
+
+template <class Src, int SC, int DT>
+__global__ void __launch_bounds__(256) quant_rowcol_kernel(const Src src, const RowColArgs a) {
+  constexpr int P = Src::kParts;
+  constexpr int R = TR / P;                 // tile rows: 64 (one part) or 32 (two parts)
+  __shared__ float tile[P][R][TC + 1];
+  __shared__ uint32_t s_amax[8];
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const uint32_t lane = tid & 31;
+  const int64_t c0 = (int64_t)blockIdx.x * TC, r0 = (int64_t)blockIdx.y * R;
+  const int64_t nrows = a.rows_used ? (int64_t)*a.rows_used : a.rows_cap;
+  if (r0 >= nrows) return;
+  const int64_t g = r0 / a.M;
+  const float ts = (SC == MGQ_TENSOR_F32) ? a.tensor_scale[g] : 1.0f;
+  // ---- load: R rows x 16 chunks of 8 columns
+  uint32_t am = 0;
+#pragma unroll
+  for (int i = 0; i < 4 / P; ++i) {
+    const int chunk = tid + 256 * i;
+    const int rr = chunk >> 4, cc = (chunk & 15) * 8;
+    float v[P][8];
+    if (r0 + rr < nrows) {
+      src.load8(r0 + rr, c0 + cc, v[0], v[P - 1]);
+    } else {
+#pragma unroll
+      for (int p = 0; p < P; ++p)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[p][j] = 0.0f;
+    }
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+      am = max(am, absmax_bits_f32(v[p], 8));
+#pragma unroll
+      for (int j = 0; j < 8; ++j) tile[p][rr][cc + j] = v[p][j];
+    }
+  }
+  __syncthreads();
+  // ---- row-wise: the 64 (part, row) pairs, 8 per warp; lane l takes columns 4l..4l+3
+  for (int pr = warp * 8; a.row_codes && pr < warp * 8 + 8; ++pr) {
+    const int p = pr / R, rr = pr % R;
+    const int64_t r = r0 + rr;
+    const int64_t cb = c0 + p * a.part_off;       // first output column of this part
+    float v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = tile[p][rr][4 * lane + j];
+    float mult = ts;
+    uint32_t scode = 0;
+    if (SC == MGQ_MX32_E8M0) {
+      uint32_t m = absmax_bits_f32(v, 4);          // block of 32 = 8 lanes
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+      const int e = mx_exponent(m, FmtInfo<DT>::emax, a.rceil != 0);
+      mult = mx_multiplier(e);
+      scode = mx_scale_code(e);
+    }
+    const uint32_t w = cvt_fp8x4<DT>(__fmul_rn(v[0], mult), __fmul_rn(v[1], mult), __fmul_rn(v[2], mult),
+                                     __fmul_rn(v[3], mult));
+    if (SC == MGQ_MX32_E8M0) {
+      // the 4 block scales of this row segment (lanes 0, 8, 16, 24) into lane 0
+      const uint32_t s1 = __shfl_sync(0xFFFFFFFFu, scode, 8), s2 = __shfl_sync(0xFFFFFFFFu, scode, 16),
+                     s3 = __shfl_sync(0xFFFFFFFFu, scode, 24);
+      if (lane == 0 && r < nrows)
+        *reinterpret_cast<uint32_t*>(a.row_scales + tiled_scale_offset(r, cb / 32, a.C / 128)) =
+            scode | (s1 << 8) | (s2 << 16) | (s3 << 24);
+    }
+    if (r < nrows) *reinterpret_cast<uint32_t*>(a.row_codes + r * a.C + cb + 4 * lane) = w;
+  }
+  // ---- column-wise: thread t takes column t % 128 and 32 rows: the half t / 128
+  // of the tile (one part) or part t / 128 (two parts)
+  if (a.col_codes) {
+    const int cc = tid & 127, sel = tid >> 7;
+    const int p = P == 2 ? sel : 0, rbase = P == 2 ? 0 : 32 * sel;
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = tile[p][rbase + i][cc];
+    float mult = ts;
+    const int64_t rg = r0 - g * a.M + rbase;                     // row inside the group
+    const int64_t crow = g * a.C + c0 + p * a.part_off + cc;     // row of the column-wise output
+    if (SC == MGQ_MX32_E8M0) {
+      const int e = mx_exponent(absmax_bits_f32(v, 32), FmtInfo<DT>::emax, a.rceil != 0);
+      mult = mx_multiplier(e);
+      a.col_scales[tiled_scale_offset(crow, rg / 32, a.M / 128)] = (uint8_t)mx_scale_code(e);
+    }
+    uint32_t cw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      cw[i] = cvt_fp8x4<DT>(__fmul_rn(v[4 * i], mult), __fmul_rn(v[4 * i + 1], mult), __fmul_rn(v[4 * i + 2], mult),
+                            __fmul_rn(v[4 * i + 3], mult));
+    uint4* dst = reinterpret_cast<uint4*>(a.col_codes + crow * a.M + rg);
+    dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+    dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+  }
+  if (SC == MGQ_TENSOR_F32 && a.amax_out) {
+    am = warp_max_u32(am);
+    if (lane == 0) s_amax[warp] = am;
+    __syncthreads();
+    if (tid == 0) {
+      for (int i = 1; i < 8; ++i) am = max(am, s_amax[i]);
+      atomic_max_nonneg(a.amax_out + g, __uint_as_float(am));
+    }
+  }
+}
+
+template <class Src>
+int launch_rowcol(const Src& src, const mgq_qdesc* q, RowColArgs a, cudaStream_t s) {
+  const int64_t rows_per_tile = TR / Src::kParts;
+  const dim3 grid((unsigned)(a.C / Src::kParts / TC), (unsigned)((a.rows_cap + rows_per_tile - 1) / rows_per_tile));
+  const int sc = q->scaling, dt = q->dtype;
+  if (sc == MGQ_MX32_E8M0 && dt == MGQ_E4M3) quant_rowcol_kernel<Src, MGQ_MX32_E8M0, MGQ_E4M3><<<grid, 256, 0, s>>>(src, a);
+  else if (sc == MGQ_MX32_E8M0 && dt == MGQ_E5M2) quant_rowcol_kernel<Src, MGQ_MX32_E8M0, MGQ_E5M2><<<grid, 256, 0, s>>>(src, a);
+  else if (sc == MGQ_TENSOR_F32 && dt == MGQ_E4M3) quant_rowcol_kernel<Src, MGQ_TENSOR_F32, MGQ_E4M3><<<grid, 256, 0, s>>>(src, a);
+  else if (sc == MGQ_TENSOR_F32 && dt == MGQ_E5M2) quant_rowcol_kernel<Src, MGQ_TENSOR_F32, MGQ_E5M2><<<grid, 256, 0, s>>>(src, a);
+  else return MGQ_ERR_UNSUPPORTED;
+  MGQ_LAUNCH_CHECK();
+  return MGQ_OK;
+}
+
+RowColArgs make_args(const mgq_qdesc* q, int64_t rows_cap, const int32_t* rows_used, int64_t C, int64_t M,
+                     int64_t part_off = 0) {
+  RowColArgs a;
+  a.rows_cap = rows_cap;
+  a.rows_used = rows_used;
+  a.C = C;
+  a.part_off = part_off;
+  a.M = M;
+  a.row_codes = static_cast<uint8_t*>(q->row.data);
+  a.row_scales = static_cast<uint8_t*>(q->row.scale);
+  a.col_codes = static_cast<uint8_t*>(q->col.data);
+  a.col_scales = static_cast<uint8_t*>(q->col.scale);
+  a.tensor_scale = q->tensor_scale;
+  a.amax_out = q->amax_out;
+  a.rceil = q->e8m0_mode == MGQ_E8M0_RCEIL;
+  return a;
+}
+
+}  // namespace
+
+int rowcol_plain(const uint16_t* x, int64_t G, int64_t M, int64_t K, const mgq_qdesc* q, cudaStream_t s) {
+  return launch_rowcol(SrcPlain{x, K}, q, make_args(q, G * M, nullptr, K, M), s);
+}
+
+int rowcol_swiglu(const uint16_t* gu, int64_t R_cap, int64_t F, const int32_t* rows_used, uint16_t* h_out,
+                  const mgq_qdesc* q, cudaStream_t s) {
+  return launch_rowcol(SrcSwiglu{gu, F, h_out}, q, make_args(q, R_cap, rows_used, F, R_cap), s);
+}
+
+int rowcol_dswiglu(const uint16_t* dh, const uint16_t* gu, int64_t R_cap, int64_t F, const int32_t* rows_used,
+                   uint16_t* out, const mgq_qdesc* q, cudaStream_t s) {
+  return launch_rowcol(SrcDswiglu{dh, gu, F, out}, q, make_args(q, R_cap, rows_used, 2 * F, R_cap, F), s);
+}
+
+int col_gather_x(const uint16_t* x, const int32_t* src_row, int k, int64_t H, int64_t R_cap, const int32_t* rows_used,
+                 const mgq_qdesc* q, cudaStream_t s) {
+  RowColArgs a = make_args(q, R_cap, rows_used, H, R_cap);
+  a.row_codes = nullptr;       // the row-wise codes come from the permute kernel
+  return launch_rowcol(SrcGatherX{x, src_row, k, H}, q, a, s);
+}
+
+int col_gather_dy(const uint16_t* dout, const float* probs, const int32_t* src_row, int k, int64_t H, int64_t R_cap,
+                  const int32_t* rows_used, const mgq_qdesc* q, cudaStream_t s) {
+  RowColArgs a = make_args(q, R_cap, rows_used, H, R_cap);
+  a.row_codes = nullptr;       // the row-wise codes come from the unpermute-backward kernel
+  return launch_rowcol(SrcGatherDy{dout, probs, src_row, k, H}, q, a, s);
+}
+
+}  // namespace mgq

@@ -398,8 +398,9 @@ int mgq_moe_permute(const void* x_bf16, int T, int H, const int32_t* topk_idx, i
     else
       return MGQ_ERR_UNSUPPORTED;
     if (q->col.data) {
-      if (q->scaling != MGQ_TENSOR_F32) return MGQ_ERR_UNSUPPORTED;
-      MGQ_CHECK_ARG(aligned16(q->col.data) && align % 4 == 0);
+      if (q->scaling != MGQ_TENSOR_F32 && q->scaling != MGQ_MX32_E8M0) return MGQ_ERR_UNSUPPORTED;
+      MGQ_CHECK_ARG(aligned16(q->col.data) && align % 32 == 0);
+      if (q->scaling == MGQ_MX32_E8M0) MGQ_CHECK_ARG(q->col.scale && aligned16(q->col.scale));
     }
   } else {
     MGQ_CHECK_ARG(out_bf16 != nullptr);
@@ -457,8 +458,12 @@ int mgq_moe_permute(const void* x_bf16, int T, int H, const int32_t* topk_idx, i
 #undef MGQ_PERMUTE_LAUNCH
   MGQ_LAUNCH_CHECK();
   if (q->col.data) {
-    int rc = launch_transpose_u8(static_cast<const uint8_t*>(q->row.data), H, static_cast<uint8_t*>(q->col.data),
-                                 R_cap, offsets + E, R_cap, H, s);
+    // per-tensor: the column copy is the transposed cast of the row codes;
+    // MX: blocks of 32 along the permuted rows, from the gathered bf16 rows
+    int rc = q->scaling == MGQ_TENSOR_F32
+                 ? launch_transpose_u8(static_cast<const uint8_t*>(q->row.data), H,
+                                       static_cast<uint8_t*>(q->col.data), R_cap, offsets + E, R_cap, H, s)
+                 : col_gather_x(a.x, src_row, k, H, R_cap, offsets + E, q, s);
     if (rc != MGQ_OK) return rc;
   }
   return MGQ_OK;

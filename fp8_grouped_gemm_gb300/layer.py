@@ -26,13 +26,16 @@ ALIGN = 128       # group padding: the grouped GEMM tiles rows by 128
 
 class ExpertLayer:
     def __init__(self, w: Workload, device, recipe: str | None = None, keep_bf16: bool = False,
-                 history: int = 1024):
+                 history: int = 1024, train: bool | None = None):
         self.w = w
         self.dev = torch.device(device)
         self.recipe = recipe or w.recipe
         if self.recipe not in ("mxfp8", "delayed", "blockwise", "nvfp4"):
             raise NotImplementedError(self.recipe)
-        self.train = self.recipe == "delayed"
+        self.train = (w.backward or self.recipe == "delayed") if train is None else train
+        self.delayed = self.recipe == "delayed"
+        if self.train and self.recipe not in ("delayed", "mxfp8"):
+            raise NotImplementedError(f"backward with {self.recipe}")
         self.scaling = {"mxfp8": mgq.MX32_E8M0, "delayed": mgq.TENSOR_F32,
                         "blockwise": mgq.BLK_1x128_F32, "nvfp4": mgq.NV16_UE4M3}[self.recipe]
         self.nv = self.recipe == "nvfp4"
@@ -77,15 +80,17 @@ class ExpertLayer:
             self.w1s = torch.empty(E, 2 * F // 128, H // 128, **f32)
             self.w2s = torch.empty(E, H // 128, F // 128, **f32)
         if self.train:
-            # per-tensor scales (delayed): [x, h, w1 x E, w2 x E] in e4m3, [dy2, dy1] in e5m2
-            nf = 2 + 2 * E
-            self.fwd_scale = torch.ones(nf, **f32)
-            self.fwd_amax = torch.zeros(nf, **f32)
-            self.fwd_hist = torch.zeros(nf, history, **f32)
-            self.bwd_scale = torch.ones(2, **f32)
-            self.bwd_amax = torch.zeros(2, **f32)
-            self.bwd_hist = torch.zeros(2, history, **f32)
-            self.heads = torch.zeros(2, **i32)
+            if self.delayed:
+                # per-tensor scales (delayed): [x, h, w1 x E, w2 x E] in e4m3, [dy2, dy1] in e5m2
+                nf = 2 + 2 * E
+                self.fwd_scale = torch.ones(nf, **f32)
+                self.fwd_amax = torch.zeros(nf, **f32)
+                self.fwd_hist = torch.zeros(nf, history, **f32)
+                self.bwd_scale = torch.ones(2, **f32)
+                self.bwd_amax = torch.zeros(2, **f32)
+                self.bwd_hist = torch.zeros(2, history, **f32)
+                self.heads = torch.zeros(2, **i32)
+            # column-wise copies (MX: with their own E8M0 scales, blocks along the old rows)
             self.xcol = torch.empty(H, R, **u8)
             self.hcol = torch.empty(F, R, **u8)
             self.w1col = torch.empty(E, H, 2 * F, **u8)
@@ -101,6 +106,16 @@ class ExpertLayer:
             self.dw2 = torch.empty(E, H, F, **f32)
             self.dxp = torch.empty(R, H, **bf)
             self.dx = torch.empty(T, H, **bf)
+            if mx:
+                ms = mgq.mx_scale_bytes
+                self.xcs = torch.empty(ms(H, R), **u8)
+                self.hcs = torch.empty(ms(F, R), **u8)
+                self.w1cs = torch.empty(ms(E * H, 2 * F), **u8)
+                self.w2cs = torch.empty(ms(E * F, H), **u8)
+                self.dy2s = torch.empty(ms(R, H), **u8)
+                self.dy2cs = torch.empty(ms(H, R), **u8)
+                self.dy1s = torch.empty(ms(R, 2 * F), **u8)
+                self.dy1cs = torch.empty(ms(2 * F, R), **u8)
 
     def _alloc_nvfp4(self, w, R):
         """NVFP4 buffers: e2m1 codes two per byte, tiled ue4m3 scales, and the
@@ -124,23 +139,6 @@ class ExpertLayer:
         self.nv_amax = torch.zeros(2 + 2 * E, dtype=torch.float32, device=d)
         self.nv_sg = torch.ones(2 + 2 * E, dtype=torch.float32, device=d)
 
-    def _nv_forward(self, x, topk_idx, probs, stream):
-        E, H, F, R = self.w.E, self.w.H, self.w.F, self.R_cap
-        a, g = self.nv_amax, self.nv_sg
-        qx = mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, self.xq, self.xs, tensor_scale=g[0:1], amax_out=a[0:1])
-        mgq.moe_permute(x, topk_idx, E, ALIGN, qx, R, self.row_id_map, self.src_row, self.offsets,
-                        self.counts, self.ws, None, stream)
-        mgq.grouped_gemm_fwd(mgq.operand(self.xq, self.xs, H, mgq.E2M1, g[0:1]),
-                             mgq.operand(self.w1q, self.w1s, H, mgq.E2M1, g[2:2 + E]),
-                             mgq.NV16_UE4M3, self.offsets, E, R, 2 * F, H, self.gu, mgq.OUT_BF16, stream)
-        qh = mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, self.hq, self.hs, tensor_scale=g[1:2], amax_out=a[1:2])
-        mgq.swiglu_quantize(self.gu, R, F, self.offsets, E, qh, self.h_bf16, stream)
-        mgq.grouped_gemm_fwd(mgq.operand(self.hq, self.hs, F, mgq.E2M1, g[1:2]),
-                             mgq.operand(self.w2q, self.w2s, F, mgq.E2M1, g[2 + E:2 + 2 * E]),
-                             mgq.NV16_UE4M3, self.offsets, E, R, H, F, self.y, mgq.OUT_BF16, stream)
-        mgq.moe_unpermute(self.y, self.row_id_map, probs, self.out, stream)
-        return self.out
-
     # ---- scale views (delayed recipe) ------------------------------------------
     def _fs(self, i, n=1):
         return self.fwd_scale[i:i + n]
@@ -148,87 +146,140 @@ class ExpertLayer:
     def _fa(self, i, n=1):
         return self.fwd_amax[i:i + n]
 
-    # ---- weights ------------------------------------------------------------------
-    def quantize_weights(self, w1, w2, stream=None):
-        """w1 bf16 [E, 2F, H], w2 bf16 [E, H, F] on the device."""
-        E = self.w.E
+    # ---- the call sequence, as named operations (one C-ABI call each) ------------
+    # The ops capture only persistent buffers; running them in order is the
+    # step. bench.py brackets each with CUDA events to time the kernels.
+
+    def weight_ops(self, w1, w2, stream=None):
+        """Quantisation of w1 bf16 [E, 2F, H] and w2 bf16 [E, H, F]."""
+        E, Q = self.w.E, mgq.block_quantize
         if self.nv:
             a, g = self.nv_amax, self.nv_sg
-            mgq.block_quantize(w1, mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, self.w1q, self.w1s,
-                                             tensor_scale=g[2:2 + E], amax_out=a[2:2 + E]), stream)
-            mgq.block_quantize(w2, mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, self.w2q, self.w2s,
-                                             tensor_scale=g[2 + E:], amax_out=a[2 + E:]), stream)
+            q1 = mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, self.w1q, self.w1s, tensor_scale=g[2:2 + E], amax_out=a[2:2 + E])
+            q2 = mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, self.w2q, self.w2s, tensor_scale=g[2 + E:], amax_out=a[2 + E:])
         elif self.scaling == mgq.MX32_E8M0:
-            mgq.block_quantize(w1, mgq.qdesc(mgq.E4M3, self.scaling, self.w1q, self.w1s), stream)
-            mgq.block_quantize(w2, mgq.qdesc(mgq.E4M3, self.scaling, self.w2q, self.w2s), stream)
+            c1 = (self.w1col, self.w1cs) if self.train else (None, None)
+            c2 = (self.w2col, self.w2cs) if self.train else (None, None)
+            q1 = mgq.qdesc(mgq.E4M3, self.scaling, self.w1q, self.w1s, *c1)
+            q2 = mgq.qdesc(mgq.E4M3, self.scaling, self.w2q, self.w2s, *c2)
         elif self.scaling == mgq.BLK_1x128_F32:
-            mgq.block_quantize(w1, mgq.qdesc(mgq.E4M3, mgq.BLK_128x128_F32, self.w1q, self.w1s), stream)
-            mgq.block_quantize(w2, mgq.qdesc(mgq.E4M3, mgq.BLK_128x128_F32, self.w2q, self.w2s), stream)
+            q1 = mgq.qdesc(mgq.E4M3, mgq.BLK_128x128_F32, self.w1q, self.w1s)
+            q2 = mgq.qdesc(mgq.E4M3, mgq.BLK_128x128_F32, self.w2q, self.w2s)
         else:
-            mgq.block_quantize(w1, mgq.qdesc(mgq.E4M3, self.scaling, self.w1q, None, self.w1col, None,
-                                             self._fs(2, E), self._fa(2, E)), stream)
-            mgq.block_quantize(w2, mgq.qdesc(mgq.E4M3, self.scaling, self.w2q, None, self.w2col, None,
-                                             self._fs(2 + E, E), self._fa(2 + E, E)), stream)
+            q1 = mgq.qdesc(mgq.E4M3, self.scaling, self.w1q, None, self.w1col, None, self._fs(2, E), self._fa(2, E))
+            q2 = mgq.qdesc(mgq.E4M3, self.scaling, self.w2q, None, self.w2col, None, self._fs(2 + E, E),
+                           self._fa(2 + E, E))
+        return [("weight_quant", lambda: Q(w1, q1, stream)), ("weight_quant", lambda: Q(w2, q2, stream))]
 
-    # ---- forward ------------------------------------------------------------------
-    def forward(self, x, topk_idx, probs, stream=None):
+    def fwd_ops(self, x, topk_idx, probs, stream=None):
+        E, H, F, R = self.w.E, self.w.H, self.w.F, self.R_cap
+        sc = self.scaling
         if self.nv:
-            return self._nv_forward(x, topk_idx, probs, stream)
-        w, E, H, F, R = self.w, self.w.E, self.w.H, self.w.F, self.R_cap
-        mx = self.scaling in (mgq.MX32_E8M0, mgq.BLK_1x128_F32)    # scales beside the codes
-        if mx:
-            qx = mgq.qdesc(mgq.E4M3, self.scaling, self.xq, self.xs)
+            a, g = self.nv_amax, self.nv_sg
+            dt = mgq.E2M1
+            qx = mgq.qdesc(dt, sc, self.xq, self.xs, tensor_scale=g[0:1], amax_out=a[0:1])
+            qh = mgq.qdesc(dt, sc, self.hq, self.hs, tensor_scale=g[1:2], amax_out=a[1:2])
+            A1, B1 = (mgq.operand(self.xq, self.xs, H, dt, g[0:1]),
+                      mgq.operand(self.w1q, self.w1s, H, dt, g[2:2 + E]))
+            A2, B2 = (mgq.operand(self.hq, self.hs, F, dt, g[1:2]),
+                      mgq.operand(self.w2q, self.w2s, F, dt, g[2 + E:2 + 2 * E]))
         else:
-            qx = mgq.qdesc(mgq.E4M3, self.scaling, self.xq, None, self.xcol, None, self._fs(0), self._fa(0))
-        mgq.moe_permute(x, topk_idx, E, ALIGN, qx, R, self.row_id_map, self.src_row, self.offsets,
-                        self.counts, self.ws, None, stream)
-        sa = self.xs if mx else self._fs(0)
-        sw1 = self.w1s if mx else self._fs(2, E)
-        mgq.grouped_gemm_fwd(mgq.operand(self.xq, sa, H, mgq.E4M3), mgq.operand(self.w1q, sw1, H, mgq.E4M3),
-                             self.scaling, self.offsets, E, R, 2 * F, H, self.gu, mgq.OUT_BF16, stream)
-        if mx:
-            qh = mgq.qdesc(mgq.E4M3, self.scaling, self.hq, self.hs)
-        else:
-            qh = mgq.qdesc(mgq.E4M3, self.scaling, self.hq, None, self.hcol, None, self._fs(1), self._fa(1))
-        mgq.swiglu_quantize(self.gu, R, F, self.offsets, E, qh, self.h_bf16, stream)
-        sh = self.hs if mx else self._fs(1)
-        sw2 = self.w2s if mx else self._fs(2 + E, E)
-        mgq.grouped_gemm_fwd(mgq.operand(self.hq, sh, F, mgq.E4M3), mgq.operand(self.w2q, sw2, F, mgq.E4M3),
-                             self.scaling, self.offsets, E, R, H, F, self.y, mgq.OUT_BF16, stream)
-        mgq.moe_unpermute(self.y, self.row_id_map, probs, self.out, stream)
-        return self.out
+            dt = mgq.E4M3
+            if sc in (mgq.MX32_E8M0, mgq.BLK_1x128_F32):       # block scales beside the codes
+                cx = (self.xcol, self.xcs) if self.train else (None, None)
+                ch = (self.hcol, self.hcs) if self.train else (None, None)
+                qx = mgq.qdesc(dt, sc, self.xq, self.xs, *cx)
+                qh = mgq.qdesc(dt, sc, self.hq, self.hs, *ch)
+                sa, sw1, sh, sw2 = self.xs, self.w1s, self.hs, self.w2s
+            else:                                               # delayed per-tensor
+                qx = mgq.qdesc(dt, sc, self.xq, None, self.xcol, None, self._fs(0), self._fa(0))
+                qh = mgq.qdesc(dt, sc, self.hq, None, self.hcol, None, self._fs(1), self._fa(1))
+                sa, sw1, sh, sw2 = self._fs(0), self._fs(2, E), self._fs(1), self._fs(2 + E, E)
+            A1, B1 = mgq.operand(self.xq, sa, H, dt), mgq.operand(self.w1q, sw1, H, dt)
+            A2, B2 = mgq.operand(self.hq, sh, F, dt), mgq.operand(self.w2q, sw2, F, dt)
+        return [
+            ("permute_quant", lambda: mgq.moe_permute(x, topk_idx, E, ALIGN, qx, R, self.row_id_map, self.src_row,
+                                                      self.offsets, self.counts, self.ws, None, stream)),
+            ("gemm", lambda: mgq.grouped_gemm_fwd(A1, B1, sc, self.offsets, E, R, 2 * F, H, self.gu,
+                                                  mgq.OUT_BF16, stream)),
+            ("swiglu_quant", lambda: mgq.swiglu_quantize(self.gu, R, F, self.offsets, E, qh, self.h_bf16, stream)),
+            ("gemm", lambda: mgq.grouped_gemm_fwd(A2, B2, sc, self.offsets, E, R, H, F, self.y, mgq.OUT_BF16,
+                                                  stream)),
+            ("unpermute", lambda: mgq.moe_unpermute(self.y, self.row_id_map, probs, self.out, stream)),
+        ]
 
-    # ---- backward (delayed per-tensor recipe) --------------------------------------
-    def backward(self, dout, probs, stream=None):
+    def bwd_ops(self, dout, probs, stream=None):
         assert self.train
         E, H, F, R = self.w.E, self.w.H, self.w.F, self.R_cap
-        sdy2, sdy1 = self.bwd_scale[0:1], self.bwd_scale[1:2]
-        q2 = mgq.qdesc(mgq.E5M2, mgq.TENSOR_F32, self.dy2q, None, self.dy2col, None, sdy2, self.bwd_amax[0:1])
-        mgq.moe_unpermute_bwd(dout, self.y, self.row_id_map, self.src_row, probs, R, self.offsets, E, q2,
-                              self.dprobs, stream)
+        if self.delayed:
+            sc = mgq.TENSOR_F32
+            sdy2, sdy1 = self.bwd_scale[0:1], self.bwd_scale[1:2]
+            q2 = mgq.qdesc(mgq.E5M2, sc, self.dy2q, None, self.dy2col, None, sdy2, self.bwd_amax[0:1])
+            q1 = mgq.qdesc(mgq.E5M2, sc, self.dy1q, None, self.dy1col, None, sdy1, self.bwd_amax[1:2])
+            # per-tensor: the column-wise copy shares the row-wise scale
+            s_dy2r = s_dy2c = sdy2
+            s_dy1r = s_dy1c = sdy1
+            s_w2c, s_w1c = self._fs(2 + E, E), self._fs(2, E)
+            s_hc, s_xc = self._fs(1), self._fs(0)
+        else:
+            sc = mgq.MX32_E8M0
+            q2 = mgq.qdesc(mgq.E5M2, sc, self.dy2q, self.dy2s, self.dy2col, self.dy2cs)
+            q1 = mgq.qdesc(mgq.E5M2, sc, self.dy1q, self.dy1s, self.dy1col, self.dy1cs)
+            s_dy2r, s_dy2c, s_dy1r, s_dy1c = self.dy2s, self.dy2cs, self.dy1s, self.dy1cs
+            s_w2c, s_w1c, s_hc, s_xc = self.w2cs, self.w1cs, self.hcs, self.xcs
+        O = mgq.operand
         # down projection: dh = dY2 W2 ; dW2 = dY2^T h
-        mgq.grouped_gemm_dgrad(mgq.operand(self.dy2q, sdy2, H, mgq.E5M2),
-                               mgq.operand(self.w2col, self._fs(2 + E, E), H, mgq.E4M3),
-                               mgq.TENSOR_F32, self.offsets, E, R, H, F, self.dh, mgq.OUT_BF16, stream)
-        mgq.grouped_gemm_wgrad(mgq.operand(self.dy2col, sdy2, R, mgq.E5M2),
-                               mgq.operand(self.hcol, self._fs(1), R, mgq.E4M3),
-                               mgq.TENSOR_F32, self.offsets, E, R, H, F, self.dw2, 0.0, mgq.OUT_F32, stream)
-        q1 = mgq.qdesc(mgq.E5M2, mgq.TENSOR_F32, self.dy1q, None, self.dy1col, None, sdy1, self.bwd_amax[1:2])
-        mgq.dswiglu_quantize(self.dh, self.gu, R, F, self.offsets, E, q1, self.dgu_bf16, stream)
+        d2 = (O(self.dy2q, s_dy2r, H, mgq.E5M2), O(self.w2col, s_w2c, H, mgq.E4M3))
+        w2 = (O(self.dy2col, s_dy2c, R, mgq.E5M2), O(self.hcol, s_hc, R, mgq.E4M3))
         # gate/up projection: dXp = dY1 W1 ; dW1 = dY1^T X
-        mgq.grouped_gemm_dgrad(mgq.operand(self.dy1q, sdy1, 2 * F, mgq.E5M2),
-                               mgq.operand(self.w1col, self._fs(2, E), 2 * F, mgq.E4M3),
-                               mgq.TENSOR_F32, self.offsets, E, R, 2 * F, H, self.dxp, mgq.OUT_BF16, stream)
-        mgq.grouped_gemm_wgrad(mgq.operand(self.dy1col, sdy1, R, mgq.E5M2),
-                               mgq.operand(self.xcol, self._fs(0), R, mgq.E4M3),
-                               mgq.TENSOR_F32, self.offsets, E, R, 2 * F, H, self.dw1, 0.0, mgq.OUT_F32, stream)
-        mgq.moe_permute_bwd(self.dxp, self.row_id_map, self.dx, stream)
+        d1 = (O(self.dy1q, s_dy1r, 2 * F, mgq.E5M2), O(self.w1col, s_w1c, 2 * F, mgq.E4M3))
+        w1 = (O(self.dy1col, s_dy1c, R, mgq.E5M2), O(self.xcol, s_xc, R, mgq.E4M3))
+        return [
+            ("unpermute_bwd_quant", lambda: mgq.moe_unpermute_bwd(dout, self.y, self.row_id_map, self.src_row, probs,
+                                                                  R, self.offsets, E, q2, self.dprobs, stream)),
+            ("gemm", lambda: mgq.grouped_gemm_dgrad(*d2, sc, self.offsets, E, R, H, F, self.dh, mgq.OUT_BF16,
+                                                    stream)),
+            ("gemm", lambda: mgq.grouped_gemm_wgrad(*w2, sc, self.offsets, E, R, H, F, self.dw2, 0.0,
+                                                    mgq.OUT_F32, stream)),
+            ("dswiglu_quant", lambda: mgq.dswiglu_quantize(self.dh, self.gu, R, F, self.offsets, E, q1,
+                                                           self.dgu_bf16, stream)),
+            ("gemm", lambda: mgq.grouped_gemm_dgrad(*d1, sc, self.offsets, E, R, 2 * F, H, self.dxp,
+                                                    mgq.OUT_BF16, stream)),
+            ("gemm", lambda: mgq.grouped_gemm_wgrad(*w1, sc, self.offsets, E, R, 2 * F, H, self.dw1, 0.0,
+                                                    mgq.OUT_F32, stream)),
+            ("permute_bwd", lambda: mgq.moe_permute_bwd(self.dxp, self.row_id_map, self.dx, stream)),
+        ]
+
+    def update_ops(self, stream=None):
+        return [("scaling_update", lambda: self.update_scaling(stream))] if self.delayed else []
+
+    def step_ops(self, w1, w2, x, topk_idx, probs, dout=None, stream=None):
+        """One whole step: weights, forward, and (training) backward + scaling."""
+        ops = self.weight_ops(w1, w2, stream) + self.fwd_ops(x, topk_idx, probs, stream)
+        if self.train:
+            ops += self.bwd_ops(dout, probs, stream) + self.update_ops(stream)
+        return ops
+
+    # ---- convenience wrappers ---------------------------------------------------------
+    def quantize_weights(self, w1, w2, stream=None):
+        for _, op in self.weight_ops(w1, w2, stream):
+            op()
+
+    def forward(self, x, topk_idx, probs, stream=None):
+        for _, op in self.fwd_ops(x, topk_idx, probs, stream):
+            op()
+        return self.out
+
+    def backward(self, dout, probs, stream=None):
+        for _, op in self.bwd_ops(dout, probs, stream):
+            op()
         return self.dx
 
     def update_scaling(self, stream=None):
         """Delayed scaling: push this step's amaxes into the histories and
-        derive the scales of the next step."""
-        assert self.train
+        derive the scales of the next step (nothing to do for MX scaling)."""
+        if not self.delayed:
+            return
         mgq.amax_history_update(self.fwd_hist, self.heads[0:1], self.fwd_amax, self.fwd_scale,
                                 mgq.FMAX[mgq.E4M3], stream)
         mgq.amax_history_update(self.bwd_hist, self.heads[1:2], self.bwd_amax, self.bwd_scale,
@@ -243,7 +294,8 @@ class ExpertLayer:
             return fwd + 2 + 4                          # + amax passes (x, h); weights: 2 x (amax + rows)
         if not self.train:
             return fwd + 2                              # weight quantisation (row)
-        fwd += 2                                        # col transposes of x and h
-        wq = 2 + 2 * E                                  # weight rows + per-expert col transposes
-        bwd = 2 + 2 + 2 + 2 + 1                         # unpermute_bwd(+T), dgrad/wgrad x2, dswiglu(+T), permute_bwd
-        return fwd + wq + bwd + 2                       # + two history updates
+        fwd += 1                                        # column copy of x (h's is fused into SwiGLU)
+        wq = 2                                          # weights: rows + columns in one pass each
+        bwd = 2 + 2 + 1 + 2 + 1                         # unpermute_bwd + its column copy, dgrad/wgrad,
+                                                        # dswiglu (fused columns), dgrad/wgrad, permute_bwd
+        return fwd + wq + bwd + (2 if self.delayed else 0)

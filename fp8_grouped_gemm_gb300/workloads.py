@@ -16,6 +16,7 @@ mixtral_fwd             8   2  16384  4096  14336  top-k      MXFP8 e4m3
 scout_fwd               16  1  16384  5120  8192   Zipf(1.2)  blockwise
 finegrained_fwd         128 8  32768  2048  768    uniform    NVFP4
 mixtral_fwdbwd          8   2  16384  4096  14336  top-k      delayed
+mixtral_fwdbwd_mx       8   2  16384  4096  14336  top-k      MXFP8 (train)
 ======================  ==  =  =====  ====  =====  =========  ===========
 
 Draws: activations bf16(N(0,1)) (Mixtral shapes: 0.1% of the hidden channels,
@@ -83,6 +84,10 @@ WORKLOADS = {
                                 "nvfp4"),
     "mixtral_fwdbwd": Workload("mixtral_fwdbwd", 5, 8, 2, 16384, 4096, 14336, "topk",
                                "delayed", backward=True, outlier_frac=0.001),
+    # the same layer trained with MXFP8 block scales in both passes (e4m3
+    # forward, e5m2 gradients; column-wise 32x1 requantisation for wgrad)
+    "mixtral_fwdbwd_mx": Workload("mixtral_fwdbwd_mx", 5, 8, 2, 16384, 4096, 14336, "topk",
+                                  "mxfp8", backward=True, outlier_frac=0.001),
 }
 
 

@@ -419,7 +419,7 @@ def _layout(rng, T, E, k, dev, align=128):
     return idx, rim, src, off, cnt
 
 
-@pytest.mark.parametrize("mode", ["mx", "tensor"])
+@pytest.mark.parametrize("mode", ["mx", "tensor", "mx_col"])
 @pytest.mark.parametrize("F", [512, 768, 1536])
 def test_swiglu_quantize(mgq, mode, F):
     rng = np.random.default_rng(F)
@@ -434,6 +434,11 @@ def test_swiglu_quantize(mgq, mode, F):
     if mode == "mx":
         sc = torch.empty(mgq.mx_scale_bytes(R, F), dtype=torch.uint8, device=dev)
         q = mgq.qdesc(mgq.E4M3, mgq.MX32_E8M0, codes, sc)
+    elif mode == "mx_col":
+        sc = torch.empty(mgq.mx_scale_bytes(R, F), dtype=torch.uint8, device=dev)
+        col = torch.full((F, R), 0xAB, dtype=torch.uint8, device=dev)
+        csc = torch.full((mgq.mx_scale_bytes(F, R),), 0xCD, dtype=torch.uint8, device=dev)
+        q = mgq.qdesc(mgq.E4M3, mgq.MX32_E8M0, codes, sc, col, csc)
     else:
         s = torch.tensor([20.0], device=dev)
         amax = torch.zeros(1, device=dev)
@@ -444,10 +449,15 @@ def test_swiglu_quantize(mgq, mode, F):
     n = int(off[-1])
     hg = bf16_np(h)[:n]
     check_elementwise(OL.swiglu(bf16_np(gu)[:n], F), hg, "swiglu")
-    if mode == "mx":
+    if mode in ("mx", "mx_col"):
         c, s_ = OQ.quantize_mx(hg)
         assert np.array_equal(u8_np(codes)[:n], c)
         assert np.array_equal(untile_mx_scales(u8_np(sc), R, F)[:n], s_)
+        if mode == "mx_col":
+            # column-wise: blocks of 32 along the rows (row groups are 128-aligned)
+            cc, cs = OQ.quantize_mx(hg.T)
+            assert np.array_equal(u8_np(col)[:, :n], cc)
+            assert np.array_equal(untile_mx_scales(u8_np(csc), F, R)[:, :n // 32], cs)
     else:
         c, am = OQ.quantize_tensor(hg, np.float32(20.0))
         assert np.array_equal(u8_np(codes)[:n], c)
@@ -455,7 +465,8 @@ def test_swiglu_quantize(mgq, mode, F):
         assert float(amax.item()) == am
 
 
-def test_dswiglu_quantize(mgq):
+@pytest.mark.parametrize("mode", ["tensor", "mx_col"])
+def test_dswiglu_quantize(mgq, mode):
     rng = np.random.default_rng(5)
     dev = torch.device(DEV)
     F, R = 768, 384
@@ -467,15 +478,28 @@ def test_dswiglu_quantize(mgq):
     dgu = torch.empty(R, 2 * F, dtype=torch.bfloat16, device=dev)
     s = torch.tensor([20000.0], device=dev)
     amax = torch.zeros(1, device=dev)
-    q = mgq.qdesc(mgq.E5M2, mgq.TENSOR_F32, codes, None, col, None, s, amax)
+    if mode == "tensor":
+        q = mgq.qdesc(mgq.E5M2, mgq.TENSOR_F32, codes, None, col, None, s, amax)
+    else:
+        sc = torch.empty(mgq.mx_scale_bytes(R, 2 * F), dtype=torch.uint8, device=dev)
+        csc = torch.empty(mgq.mx_scale_bytes(2 * F, R), dtype=torch.uint8, device=dev)
+        q = mgq.qdesc(mgq.E5M2, mgq.MX32_E8M0, codes, sc, col, csc)
     mgq.dswiglu_quantize(dh.to(dev), gu.to(dev), R, F, torch.from_numpy(off).to(dev), 2, q, dgu)
     torch.cuda.synchronize()
     g = bf16_np(dgu)
     check_elementwise(OL.dswiglu(bf16_np(dh), bf16_np(gu), F), g, "dswiglu")
-    c, am = OQ.quantize_tensor(g, np.float32(20000.0), "e5m2")
-    assert np.array_equal(u8_np(codes), c)
-    assert np.array_equal(u8_np(col), c.T)
-    assert float(amax.item()) == am
+    if mode == "tensor":
+        c, am = OQ.quantize_tensor(g, np.float32(20000.0), "e5m2")
+        assert np.array_equal(u8_np(codes), c)
+        assert np.array_equal(u8_np(col), c.T)
+        assert float(amax.item()) == am
+    else:
+        c, s_ = OQ.quantize_mx(g, "e5m2")
+        assert np.array_equal(u8_np(codes), c)
+        assert np.array_equal(untile_mx_scales(u8_np(sc), R, 2 * F), s_)
+        cc, cs = OQ.quantize_mx(g.T, "e5m2")
+        assert np.array_equal(u8_np(col), cc)
+        assert np.array_equal(untile_mx_scales(u8_np(csc), 2 * F, R), cs)
 
 
 @pytest.mark.parametrize("T,E,k,H", [(1000, 8, 2, 512), (333, 16, 8, 256), (64, 4, 1, 5120)])
@@ -533,7 +557,7 @@ def test_unpermute_bwd_quantize(mgq, mode):
         assert np.array_equal(untile_mx_scales(u8_np(sc), R, H)[:Rp], s_)
 
 
-@pytest.mark.parametrize("mode", ["mx", "tensor", "blk128", "nvfp4"])
+@pytest.mark.parametrize("mode", ["mx", "tensor", "blk128", "nvfp4", "mx_col"])
 def test_block_quantize_weights(mgq, mode):
     rng = np.random.default_rng(13)
     dev = torch.device(DEV)
@@ -541,6 +565,24 @@ def test_block_quantize_weights(mgq, mode):
     w = _bf16(rng, (G, M, K), 0.02)
     codes = torch.empty(G, M, K, dtype=torch.uint8, device=dev)
     wf = bf16_np(w)
+    if mode == "mx_col":
+        # row-wise MX (blocks along K) and column-wise MX (blocks of 32 along
+        # each expert's rows, stored transposed [G, K, M]) in one pass
+        wf = bf16_np(w)
+        sc = torch.empty(mgq.mx_scale_bytes(G * M, K), dtype=torch.uint8, device=dev)
+        col = torch.empty(G, K, M, dtype=torch.uint8, device=dev)
+        csc = torch.empty(mgq.mx_scale_bytes(G * K, M), dtype=torch.uint8, device=dev)
+        mgq.block_quantize(w.to(dev), mgq.qdesc(mgq.E4M3, mgq.MX32_E8M0, codes, sc, col, csc))
+        torch.cuda.synchronize()
+        c, s_ = OQ.quantize_mx(wf.reshape(G * M, K))
+        assert np.array_equal(u8_np(codes).reshape(G * M, K), c)
+        assert np.array_equal(untile_mx_scales(u8_np(sc), G * M, K), s_)
+        cs_all = untile_mx_scales(u8_np(csc), G * K, M).reshape(G, K, M // 32)
+        for g in range(G):
+            cc, cs = OQ.quantize_mx(wf[g].T)
+            assert np.array_equal(u8_np(col)[g], cc)
+            assert np.array_equal(cs_all[g], cs)
+        return
     if mode == "nvfp4":
         w[0, 3, 4] = 0.5
         wf = bf16_np(w)

@@ -144,3 +144,80 @@ def test_delayed_training_steps():
             d.update(a)
         for d, a in zip(bwd_ds, [am_dy2, am_dy1]):
             d.update(a)
+
+
+def test_mxfp8_training_step_scaled_down():
+    """MXFP8 in both passes (e4m3 forward, e5m2 gradients, E8M0 per 32): the
+    column-wise copies requantise with 32x1 blocks along each expert's tokens
+    (and along N for the weights) instead of transposing the row codes."""
+    from fp8_grouped_gemm_gb300 import layer as L
+    from fp8_grouped_gemm_gb300 import mgq
+    from fp8_grouped_gemm_gb300 import workloads as W
+    from tests.layer_check import untile_mx_scales
+    w = W.WORKLOADS["mixtral_fwdbwd_mx"].scaled(T=700, H=512, F=768, E=4)
+    E, k, T, H, F = w.E, w.k, w.T, w.H, w.F
+    x = W.make_activations(w)
+    w1, w2 = W.make_weights(w)
+    idx, probs = W.make_routing(w)
+    dout = W.make_dout(w)
+    lay = L.ExpertLayer(w, DEV, keep_bf16=True)
+    assert lay.train and not lay.delayed
+    lay.quantize_weights(w1.to(DEV), w2.to(DEV))
+    lay.forward(x.to(DEV), torch.from_numpy(idx).to(DEV), torch.from_numpy(probs).to(DEV))
+    lay.backward(dout.to(DEV), torch.from_numpy(probs).to(DEV))
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    R = lay.R_cap
+    rim, src, off, cnt = OR.permute_indices(idx, E, L.ALIGN)
+    Rp = int(off[-1])
+    sc = lambda t, rows, ld: untile_mx_scales(u8_np(t), rows, ld)
+
+    def row_col(m, fmt, rq, rs, cq, cs):
+        """m [Rp, C]: check the row-wise and column-wise MX copies; returns both dequantised."""
+        c, s = OQ.quantize_mx(m, fmt)
+        assert np.array_equal(u8_np(rq)[:Rp], c)
+        assert np.array_equal(sc(rs, R, m.shape[1])[:Rp], s)
+        ct, st = OQ.quantize_mx(m.T, fmt)
+        assert np.array_equal(u8_np(cq)[:, :Rp], ct)
+        assert np.array_equal(sc(cs, m.shape[1], R)[:, :Rp // 32], st)
+        return OQ.dequantize_mx(c, s, fmt), OQ.dequantize_mx(ct, st, fmt).T
+
+    xp = OR.permute_rows(bf16_np(x), rim, Rp)
+    x_r, x_c = row_col(xp, "e4m3", lay.xq, lay.xs, lay.xcol, lay.xcs)
+    w1f, w2f = bf16_np(w1), bf16_np(w2)
+    w1_r, w1_c, w2_r, w2_c = [], [], [], []
+    w1cs = sc(lay.w1cs, E * H, 2 * F).reshape(E, H, 2 * F // 32)
+    w2cs = sc(lay.w2cs, E * F, H).reshape(E, F, H // 32)
+    for e in range(E):
+        ct, st = OQ.quantize_mx(w1f[e].T)
+        assert np.array_equal(u8_np(lay.w1col)[e], ct) and np.array_equal(w1cs[e], st)
+        w1_c.append(OQ.dequantize_mx(ct, st).T)
+        ct, st = OQ.quantize_mx(w2f[e].T)
+        assert np.array_equal(u8_np(lay.w2col)[e], ct) and np.array_equal(w2cs[e], st)
+        w2_c.append(OQ.dequantize_mx(ct, st).T)
+    w1_c, w2_c = np.stack(w1_c), np.stack(w2_c)
+    w1_r = OQ.dequantize_mx(*OQ.quantize_mx(w1f.reshape(E * 2 * F, H))).reshape(E, 2 * F, H)
+    w2_r = OQ.dequantize_mx(*OQ.quantize_mx(w2f.reshape(E * H, F))).reshape(E, H, F)
+    gu = bf16_np(lay.gu)[:Rp]
+    assert rel_fro(OF.round_to_bf16(OG.grouped_gemm_fwd(x_r, w1_r, off)), gu) <= GEMM_TOL_BF16
+    hg = bf16_np(lay.h_bf16)[:Rp]
+    check_elementwise(OL.swiglu(gu, F), hg, "swiglu")
+    h_r, h_c = row_col(hg, "e4m3", lay.hq, lay.hs, lay.hcol, lay.hcs)
+    y = bf16_np(lay.y)[:Rp]
+    assert rel_fro(OF.round_to_bf16(OG.grouped_gemm_fwd(h_r, w2_r, off)), y) <= GEMM_TOL_BF16
+    # backward
+    dy32, dp = OR.unpermute_bwd(bf16_np(dout), y, rim, probs, Rp)
+    assert rel_fro(dp, lay.dprobs.cpu().numpy()) <= 1e-5
+    dy2_r, dy2_c = row_col(dy32.astype(np.float64), "e5m2", lay.dy2q, lay.dy2s, lay.dy2col, lay.dy2cs)
+    dh = bf16_np(lay.dh)[:Rp]
+    assert rel_fro(OF.round_to_bf16(OG.grouped_gemm_dgrad(dy2_r, w2_c, off)), dh) <= GEMM_TOL_BF16
+    assert rel_fro(OG.grouped_gemm_wgrad(dy2_c, h_c, off, E), lay.dw2.cpu().numpy()) <= GEMM_TOL_F32
+    dgu = bf16_np(lay.dgu_bf16)[:Rp]
+    check_elementwise(OL.dswiglu(dh, gu, F), dgu, "dswiglu")
+    dy1_r, dy1_c = row_col(dgu, "e5m2", lay.dy1q, lay.dy1s, lay.dy1col, lay.dy1cs)
+    dxp = bf16_np(lay.dxp)[:Rp]
+    assert rel_fro(OF.round_to_bf16(OG.grouped_gemm_dgrad(dy1_r, w1_c, off)), dxp) <= GEMM_TOL_BF16
+    assert rel_fro(OG.grouped_gemm_wgrad(dy1_c, x_c, off, E), lay.dw1.cpu().numpy()) <= GEMM_TOL_F32
+    check_elementwise(OR.permute_bwd(dxp, rim), bf16_np(lay.dx), "permute_bwd")
+    # quantised-vs-bf16 SQNR of the e4m3 forward GEMM
+    assert OG.sqnr_db(OG.grouped_gemm_fwd(xp, w1f, off), gu) >= 28.0
