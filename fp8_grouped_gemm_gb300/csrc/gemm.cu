@@ -21,6 +21,8 @@
 // same tile sequence from it. Every mbarrier wait is bounded: on a timeout the
 // kernel records MGQ_ERR_TIMEOUT, all roles leave their loops, tensor memory is
 // freed and the kernel returns.
+#include <cstdlib>
+
 #include "device_common.cuh"
 #include "mgq_internal.h"
 #include "ptx_sm100.cuh"
@@ -446,6 +448,309 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& 
   return MGQ_OK;
 }
 
+
+// ============================================================================
+// 2-CTA variant (cta_group::2) for per-tensor FP8: a cluster of two CTAs on two
+// SMs computes 256 x 256 tiles. Each CTA loads its 128 rows of A and its 128
+// rows (N half) of B; one thread of CTA 0 issues M=256 MMAs that read both
+// CTAs' shared memory, and each CTA's tensor memory receives its 128 rows of
+// the accumulator. Half of the B tile per SM means 32 KB per stage, so the
+// pipeline is 6 stages deep in the same shared memory.
+//   - TMA loads of both CTAs complete on CTA 0's `full` barrier (which CTA 0
+//     arms with the pair's byte count); the MMA commit is multicast to both
+//     CTAs' `empty` and `tmem_full` barriers; both CTAs' epilogue warps arrive
+//     on CTA 0's `tmem_empty`.
+constexpr int PSTAGES = 6;
+constexpr uint32_t kPairTile = 128 * 128;                      // bytes of one A or B half tile
+constexpr size_t kPairSmem = 1024 + PSTAGES * 2 * kPairTile + 256 + (2 * kMaxE + 16) * 4;
+
+template <int MODE>
+__device__ __forceinline__ bool get_pair_tile(const int32_t* s_off, const int32_t* s_cum, int E, const GemmParams& p,
+                                              int64_t t, int& ecur, Tile& tl) {
+  if (MODE == kModeRows) {
+    // pair tiles of 256 rows per expert (the last may reach past the group;
+    // those rows are computed on whatever follows and never stored)
+    const int64_t nN = p.N / BN;
+    const int64_t total = (int64_t)s_cum[E] * nN;
+    if (t >= total) return false;
+    while (ecur < E - 1 && (int64_t)s_cum[ecur + 1] * nN <= t) ++ecur;
+    const int e = ecur;
+    const int64_t mt = s_cum[e + 1] - s_cum[e];
+    const int64_t local = t - (int64_t)s_cum[e] * nN;
+    const int64_t n = local / mt, m = local % mt;
+    tl.e = e;
+    tl.nst = (int)(p.K / BK);
+    tl.row_a = s_off[e] + 256 * m;
+    tl.row_b = (int64_t)e * p.N + BN * n;
+    tl.kx0 = 0;
+    tl.out_row = tl.row_a;
+    tl.out_col = BN * n;
+  } else {
+    const int64_t mN = p.N / 256, nK = p.K / BN;
+    const int64_t tpe = mN * nK;
+    if (t >= tpe * E) return false;
+    const int e = (int)(t / tpe);
+    const int64_t local = t % tpe;
+    const int64_t m = local / nK, n = local % nK;
+    tl.e = e;
+    tl.nst = (s_off[e + 1] - s_off[e]) / BK;
+    tl.row_a = 256 * m;
+    tl.row_b = BN * n;
+    tl.kx0 = s_off[e];
+    tl.out_row = (int64_t)e * p.N + 256 * m;
+    tl.out_col = BN * n;
+  }
+  return true;
+}
+
+template <int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                             const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + PSTAGES * kPairTile;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + PSTAGES * kPairTile);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + PSTAGES;
+  uint64_t* tmem_full = bars + 2 * PSTAGES;        // [2]
+  uint64_t* tmem_empty = bars + 2 * PSTAGES + 2;   // [2]
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * PSTAGES + 4);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  int* s_bad = reinterpret_cast<int*>(s_tmem + 2);
+  int32_t* s_off = reinterpret_cast<int32_t*>(bars + 32);
+  int32_t* s_cum = s_off + (kMaxE + 8);
+
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31;
+  const int E = p.E;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const bool leader = rank == 0;
+  const int64_t pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+  for (int i = threadIdx.x; i <= E; i += kThreads) s_off[i] = p.offsets[i];
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < PSTAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tmem_full[a], 1);
+      ptx::mbar_init(&tmem_empty[a], 2 * 8);      // one arrival per epilogue warp of each CTA
+    }
+    *s_abort = 0;
+    *s_bad = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(s_tmem, kTmemCols);
+    ptx::tmem_relinquish_pair();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    bool bad = s_off[0] != 0;
+    int cum = 0;
+    for (int e = 0; e < E; ++e) {
+      bad |= (s_off[e + 1] < s_off[e]) || (s_off[e + 1] % BM) != 0;
+      s_cum[e] = cum;
+      cum += (s_off[e + 1] - s_off[e] + 255) / 256;
+    }
+    s_cum[E] = cum;
+    bad |= (int64_t)s_off[E] > p.R_cap;
+    if (bad) {
+      *s_bad = 1;
+      report(p.err, MGQ_ERR_INVALID_ARG);
+    }
+  }
+  ptx::tc_fence_before();
+  ptx::cluster_sync();                 // both CTAs' barriers initialised, tensor memory allocated
+  ptx::tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const bool run = (*s_bad == 0);
+
+  if (run && warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    int ecur = 0;
+    uint32_t it = 0;
+    Tile tl;
+    for (int64_t t = pair; get_pair_tile<MODE>(s_off, s_cum, E, p, t, ecur, tl); t += npairs) {
+      for (int s = 0; s < tl.nst; ++s, ++it) {
+        const uint32_t st = it % PSTAGES, ph = (it / PSTAGES) & 1;
+        if (*s_abort) break;
+        if (!ptx::mbar_wait(&empty[st], ph ^ 1, kWaitNs)) {
+          report(p.err, MGQ_ERR_TIMEOUT);
+          *s_abort = 1;
+          break;
+        }
+        if (leader) ptx::mbar_arrive_expect_tx(&full[st], 4 * kPairTile);   // both CTAs' A and B halves
+        const uint32_t bar0 = ptx::mapa_shared(ptx::smem_u32(&full[st]), 0);
+        const int32_t kx = (int32_t)(tl.kx0 + (int64_t)s * BK);
+        ptx::tma_load_2d_pair(sA + st * kPairTile, &tmA, bar0, kx, (int32_t)(tl.row_a + 128 * rank));
+        ptx::tma_load_2d_pair(sB + st * kPairTile, &tmB, bar0, kx, (int32_t)(tl.row_b + 128 * rank));
+      }
+      if (*s_abort) break;
+    }
+  } else if (run && leader && warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (CTA 0)
+    int ecur = 0;
+    uint32_t it = 0, tc = 0;
+    Tile tl;
+    const uint32_t sA0 = ptx::smem_u32(sA), sB0 = ptx::smem_u32(sB);
+    for (int64_t t = pair; get_pair_tile<MODE>(s_off, s_cum, E, p, t, ecur, tl); t += npairs) {
+      if (tl.nst == 0) continue;
+      if (*s_abort) break;
+      const uint32_t a = tc & 1, aph = (tc >> 1) & 1;
+      if (!ptx::mbar_wait(&tmem_empty[a], aph ^ 1, kWaitNs)) {
+        report(p.err, MGQ_ERR_TIMEOUT);
+        *s_abort = 1;
+        break;
+      }
+      ptx::tc_fence_after();
+      bool ok = true;
+      for (int s = 0; s < tl.nst; ++s, ++it) {
+        const uint32_t st = it % PSTAGES, ph = (it / PSTAGES) & 1;
+        if (*s_abort || !ptx::mbar_wait(&full[st], ph, kWaitNs)) {
+          report(p.err, MGQ_ERR_TIMEOUT);
+          *s_abort = 1;
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint64_t ad = ptx::sdesc_kmajor_sw128(sA0 + st * kPairTile);
+        const uint64_t bd = ptx::sdesc_kmajor_sw128(sB0 + st * kPairTile);
+#pragma unroll
+        for (int kk = 0; kk < BK / 32; ++kk)
+          ptx::mma_f8f6f4_pair(tmem + a * BN, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), p.idesc,
+                               (s > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_commit_pair(&empty[st], 0x3);        // frees the stage in both CTAs
+      }
+      if (!ok) break;
+      ptx::mma_commit_pair(&tmem_full[a], 0x3);       // both halves of the accumulator complete
+      ++tc;
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const uint32_t q = warp & 3;
+    const uint32_t half = (uint32_t)(warp - 2) >> 2;
+    const int64_t row_in_tile = 128 * rank + q * 32 + lane;
+    const uint32_t empty_remote0 = ptx::mapa_shared(ptx::smem_u32(&tmem_empty[0]), 0);
+    const uint32_t empty_remote1 = ptx::mapa_shared(ptx::smem_u32(&tmem_empty[1]), 0);
+    int ecur = 0;
+    uint32_t tc = 0;
+    Tile tl;
+    for (int64_t t = pair; run && get_pair_tile<MODE>(s_off, s_cum, E, p, t, ecur, tl); t += npairs) {
+      const int64_t orow = tl.out_row + row_in_tile;
+      const int64_t col0 = tl.out_col + half * (BN / 2);
+      // rows of the last pair tile past the expert's group are not stored
+      const bool store = MODE == kModeContract || orow < s_off[tl.e + 1];
+      if (tl.nst == 0) {
+        if (p.beta == 0.0f && store) {
+          if (p.out_f32) {
+            float* o = static_cast<float*>(p.out) + orow * p.ldo + col0;
+            for (int c = 0; c < BN / 2; c += 4) *reinterpret_cast<float4*>(o + c) = make_float4(0, 0, 0, 0);
+          } else {
+            uint16_t* o = static_cast<uint16_t*>(p.out) + orow * p.ldo + col0;
+            for (int c = 0; c < BN / 2; c += 8) *reinterpret_cast<uint4*>(o + c) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        continue;
+      }
+      const uint32_t a = tc & 1, aph = (tc >> 1) & 1;
+      if (__any_sync(0xFFFFFFFFu, *s_abort != 0)) break;
+      const bool got = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&tmem_full[a], aph, kWaitNs));
+      if (!got) {
+        report(p.err, MGQ_ERR_TIMEOUT);
+        *s_abort = 1;
+        break;
+      }
+      ptx::tc_fence_after();
+      uint32_t r[4][32];
+      const uint32_t taddr = tmem + a * BN + ((q * 32) << 16) + half * (BN / 2);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) ptx::tmem_ld_32x32b_x32(taddr + c * 32, r[c]);
+      ptx::tmem_ld_wait();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(a ? empty_remote1 : empty_remote0);
+      ++tc;
+      if (!store) continue;
+      const float alpha = 1.0f / (p.sa[0] * p.sb[MODE == kModeRows ? tl.e : 0]);
+      if (p.out_f32) {
+        float* o = static_cast<float*>(p.out) + orow * p.ldo + col0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            float4 v = make_float4(__uint_as_float(r[c][i]) * alpha, __uint_as_float(r[c][i + 1]) * alpha,
+                                   __uint_as_float(r[c][i + 2]) * alpha, __uint_as_float(r[c][i + 3]) * alpha);
+            if (p.beta != 0.0f) {
+              const float4 old = *reinterpret_cast<const float4*>(o + c * 32 + i);
+              v.x += p.beta * old.x; v.y += p.beta * old.y; v.z += p.beta * old.z; v.w += p.beta * old.w;
+            }
+            *reinterpret_cast<float4*>(o + c * 32 + i) = v;
+          }
+        }
+      } else {
+        uint16_t* o = static_cast<uint16_t*>(p.out) + orow * p.ldo + col0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(r[c][i]) * alpha, __uint_as_float(r[c][i + 1]) * alpha);
+            v.y = pack_bf16x2(__uint_as_float(r[c][i + 2]) * alpha, __uint_as_float(r[c][i + 3]) * alpha);
+            v.z = pack_bf16x2(__uint_as_float(r[c][i + 4]) * alpha, __uint_as_float(r[c][i + 5]) * alpha);
+            v.w = pack_bf16x2(__uint_as_float(r[c][i + 6]) * alpha, __uint_as_float(r[c][i + 7]) * alpha);
+            *reinterpret_cast<uint4*>(o + c * 32 + i) = v;
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  ptx::tc_fence_before();
+  ptx::cluster_sync();                 // the peer's MMAs and reads are finished before freeing
+  ptx::tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tmem_dealloc_pair(tmem, kTmemCols);
+  }
+}
+
+template <int MODE>
+int launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, cudaStream_t s) {
+  auto kern = grouped_gemm_pair_kernel<MODE>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPairSmem) != cudaSuccess)
+      return MGQ_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  kern<<<num_sms() / 2 * 2, kThreads, kPairSmem, s>>>(ta, tb, p);
+  MGQ_LAUNCH_CHECK();
+  return MGQ_OK;
+}
+
+// The 2-CTA kernel serves per-tensor FP8 (wgrad needs output rows in
+// multiples of 256); MGQ_GEMM_1CTA=1 in the environment selects the 1-CTA
+// kernel for every call (both compute the same values).
+bool use_pair_kernel(int mode, int64_t N) {
+  static const bool force_1cta = [] {
+    const char* e = getenv("MGQ_GEMM_1CTA");
+    return e && e[0] == '1';
+  }();
+  if (force_1cta) return false;
+  return mode == kModeRows || N % 256 == 0;
+}
+
 int check_operand(const mgq_operand* o) {
   if (!o || !o->data || !aligned16(o->data)) return MGQ_ERR_INVALID_ARG;
   if (o->dtype != MGQ_E4M3 && o->dtype != MGQ_E5M2 && o->dtype != MGQ_E2M1) return MGQ_ERR_UNSUPPORTED;
@@ -522,6 +827,16 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
                  : ptx::idesc_f8f6f4(A->dtype, B->dtype, BM, BN);
   p.err = err;
   cudaStream_t s = as_stream(stream);
+  if (kind == kKindTensor && use_pair_kernel(mode, N)) {
+    // the pair kernel loads 128-row halves of B
+    CUtensorMap tb2;
+    const bool ok = mode == kModeRows
+                        ? encode_tmap_u8_2d(&tb2, B->data, (uint64_t)K, (uint64_t)E * N, (uint64_t)B->ld, 128, 128)
+                        : encode_tmap_u8_2d(&tb2, B->data, (uint64_t)R_cap, (uint64_t)K, (uint64_t)B->ld, 128, 128);
+    if (!ok) return MGQ_ERR_CUDA;
+    p.idesc = ptx::idesc_f8f6f4(A->dtype, B->dtype, 256, BN);
+    return mode == kModeRows ? launch_gemm_pair<kModeRows>(ta, tb2, p, s) : launch_gemm_pair<kModeContract>(ta, tb2, p, s);
+  }
   if (mode == kModeRows) {
     if (kind == kKindMX) return launch_gemm<kModeRows, kKindMX>(ta, tb, p, s);
     if (kind == kKindTensor) return launch_gemm<kModeRows, kKindTensor>(ta, tb, p, s);
