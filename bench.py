@@ -403,7 +403,7 @@ def main():
             per[name] += sum(a.elapsed_time(b) for a, b in pairs)
     per = {k: v / args.steps for k, v in per.items()}          # ms per step
     pk, pk_src = peaks()
-    gemm_ms = per.get("gemm", float("nan"))
+    gemm_ms = sum(v for k, v in per.items() if k.startswith("gemm"))
     achieved = flops / (gemm_ms * 1e-3) / 1e12
     ratio = FP4_OVER_BF16 if w.recipe == "nvfp4" else FP8_OVER_BF16
     peak_fp8 = pk["bf16_tflops_sustained"] * ratio

@@ -74,6 +74,7 @@ struct GemmParams {
   int out_f32;
   float beta;
   uint32_t idesc;
+  int tma_store;      // pair kernel: write the output through TMA stores
   int* err;
 };
 
@@ -462,7 +463,8 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& 
 //     on CTA 0's `tmem_empty`.
 constexpr int PSTAGES = 6;
 constexpr uint32_t kPairTile = 128 * 128;                      // bytes of one A or B half tile
-constexpr size_t kPairSmem = 1024 + PSTAGES * 2 * kPairTile + 256 + (2 * kMaxE + 16) * 4;
+constexpr uint32_t kStageOut = 32 * 64;                          // per epilogue warp: 32 rows x 64 bytes
+constexpr size_t kPairSmem = 1024 + PSTAGES * 2 * kPairTile + 8 * kStageOut + 256 + (2 * kMaxE + 16) * 4;
 
 template <int MODE>
 __device__ __forceinline__ bool get_pair_tile(const int32_t* s_off, const int32_t* s_cum, int E, const GemmParams& p,
@@ -506,13 +508,14 @@ __device__ __forceinline__ bool get_pair_tile(const int32_t* s_off, const int32_
 template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                             const GemmParams p) {
+                             const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   uint8_t* sA = smem;
   uint8_t* sB = sA + PSTAGES * kPairTile;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + PSTAGES * kPairTile);
+  uint8_t* sOut = sB + PSTAGES * kPairTile;        // [8 warps][32 rows][64 bytes] epilogue staging
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + 8 * kStageOut);
   uint64_t* full = bars;
   uint64_t* empty = bars + PSTAGES;
   uint64_t* tmem_full = bars + 2 * PSTAGES;        // [2]
@@ -679,8 +682,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_cluster(a ? empty_remote1 : empty_remote0);
       ++tc;
-      if (!store) continue;
+      if (!store) continue;    // the warp's 32 rows lie wholly inside or past the group
       const float alpha = 1.0f / (p.sa[0] * p.sb[MODE == kModeRows ? tl.e : 0]);
+      if (p.tma_store) {
+        // TMA stores: the warp stages 32 rows x 64 bytes at a time and the
+        // tensor-memory copy engine writes them as whole lines
+        uint8_t* stg = sOut + (warp - 2) * kStageOut;
+        const int32_t y0 = (int32_t)(tl.out_row + 128 * rank + q * 32);
+        // 64-byte column chunks of the warp's 128 columns: 8 (float32) or 4 (bf16);
+        // fully unrolled so the accumulator registers are indexed statically
+        auto put = [&](int ch, int j, uint4 v, int ncols) {
+          if (j == 0) {
+            if (lane == 0) ptx::bulk_wait_read0();   // previous chunk read out of the buffer
+            __syncwarp();
+          }
+          reinterpret_cast<uint4*>(stg + lane * 64)[j] = v;
+          if (j == 3) {
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              ptx::tma_store_2d(&tmO, stg, (int32_t)(col0 + ch * ncols), y0);
+              ptx::bulk_commit();
+            }
+          }
+        };
+        if (p.out_f32) {
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int c = ch >> 1, i0 = (ch & 1) * 16 + 4 * j;
+              put(ch, j,
+                  make_uint4(__float_as_uint(__uint_as_float(r[c][i0]) * alpha),
+                             __float_as_uint(__uint_as_float(r[c][i0 + 1]) * alpha),
+                             __float_as_uint(__uint_as_float(r[c][i0 + 2]) * alpha),
+                             __float_as_uint(__uint_as_float(r[c][i0 + 3]) * alpha)),
+                  16);
+            }
+        } else {
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int i0 = 8 * j;
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(r[ch][i0]) * alpha, __uint_as_float(r[ch][i0 + 1]) * alpha);
+              v.y = pack_bf16x2(__uint_as_float(r[ch][i0 + 2]) * alpha, __uint_as_float(r[ch][i0 + 3]) * alpha);
+              v.z = pack_bf16x2(__uint_as_float(r[ch][i0 + 4]) * alpha, __uint_as_float(r[ch][i0 + 5]) * alpha);
+              v.w = pack_bf16x2(__uint_as_float(r[ch][i0 + 6]) * alpha, __uint_as_float(r[ch][i0 + 7]) * alpha);
+              put(ch, j, v, 32);
+            }
+        }
+        continue;
+      }
       if (p.out_f32) {
         float* o = static_cast<float*>(p.out) + orow * p.ldo + col0;
 #pragma unroll
@@ -713,6 +767,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
   }
+  if (warp >= 2 && lane == 0) ptx::bulk_wait0();   // this warp's TMA stores are complete
   __syncthreads();
   ptx::tc_fence_before();
   ptx::cluster_sync();                 // the peer's MMAs and reads are finished before freeing
@@ -724,7 +779,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 template <int MODE>
-int launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, cudaStream_t s) {
+int launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const GemmParams& p,
+                     cudaStream_t s) {
   auto kern = grouped_gemm_pair_kernel<MODE>;
   static bool attr_set[64] = {false};
   int dev = 0;
@@ -734,7 +790,7 @@ int launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmPar
       return MGQ_ERR_CUDA;
     attr_set[dev] = true;
   }
-  kern<<<num_sms() / 2 * 2, kThreads, kPairSmem, s>>>(ta, tb, p);
+  kern<<<num_sms() / 2 * 2, kThreads, kPairSmem, s>>>(ta, tb, to, p);
   MGQ_LAUNCH_CHECK();
   return MGQ_OK;
 }
@@ -742,6 +798,16 @@ int launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmPar
 // The 2-CTA kernel serves per-tensor FP8 (wgrad needs output rows in
 // multiples of 256); MGQ_GEMM_1CTA=1 in the environment selects the 1-CTA
 // kernel for every call (both compute the same values).
+// MGQ_GEMM_DIRECT_STORE=1 makes the pair kernel store from registers
+// instead of through TMA (same values).
+bool direct_store_forced() {
+  static const bool f = [] {
+    const char* e = getenv("MGQ_GEMM_DIRECT_STORE");
+    return e && e[0] == '1';
+  }();
+  return f;
+}
+
 bool use_pair_kernel(int mode, int64_t N) {
   static const bool force_1cta = [] {
     const char* e = getenv("MGQ_GEMM_1CTA");
@@ -822,6 +888,7 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
   p.ldo = (mode == kModeRows) ? N : K;
   p.out_f32 = out_dtype == MGQ_OUT_F32;
   p.beta = beta;
+  p.tma_store = 0;
   p.idesc = nv   ? ptx::idesc_mxf4nvf4_ue4m3(BM, BN)
             : mx ? ptx::idesc_mxf8f6f4(A->dtype, B->dtype, BM, BN)
                  : ptx::idesc_f8f6f4(A->dtype, B->dtype, BM, BN);
@@ -835,7 +902,14 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
                         : encode_tmap_u8_2d(&tb2, B->data, (uint64_t)R_cap, (uint64_t)K, (uint64_t)B->ld, 128, 128);
     if (!ok) return MGQ_ERR_CUDA;
     p.idesc = ptx::idesc_f8f6f4(A->dtype, B->dtype, 256, BN);
-    return mode == kModeRows ? launch_gemm_pair<kModeRows>(ta, tb2, p, s) : launch_gemm_pair<kModeContract>(ta, tb2, p, s);
+    // output map: [rows, ldo] elements, boxes of 64 bytes x 32 rows
+    CUtensorMap to;
+    const int eb = p.out_f32 ? 4 : 2;
+    const uint64_t orows = mode == kModeRows ? (uint64_t)R_cap : (uint64_t)E * N;
+    p.tma_store = (beta == 0.0f && !direct_store_forced()) ? 1 : 0;
+    if (!encode_tmap_2d(&to, out, eb, (uint64_t)p.ldo, orows, (uint64_t)p.ldo * eb, 64 / eb, 32)) return MGQ_ERR_CUDA;
+    return mode == kModeRows ? launch_gemm_pair<kModeRows>(ta, tb2, to, p, s)
+                             : launch_gemm_pair<kModeContract>(ta, tb2, to, p, s);
   }
   if (mode == kModeRows) {
     if (kind == kKindMX) return launch_gemm<kModeRows, kKindMX>(ta, tb, p, s);

@@ -216,6 +216,25 @@ __host__ __device__ constexpr uint32_t idesc_sf_ids(uint32_t a_id, uint32_t b_id
   return (b_id << 4) | (a_id << 29);
 }
 
+// ---- TMA stores ----------------------------------------------------------------
+
+// make this thread's generic-proxy shared-memory writes visible to the TMA (async proxy)
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// 2D tiled store shared -> global; x (innermost) a multiple of 16 bytes
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* src, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// wait until no committed bulk store of this thread still reads shared memory
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// wait until every committed bulk store of this thread has completed
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // ---- clusters and the 2-CTA (cta_group::2) pair -----------------------------
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

@@ -1,4 +1,4 @@
-// Row-wise and column-wise quantisation in one pass over 64 x 128 tiles.
+// Row-wise and column-wise quantisation in one pass over 128 x 128 tiles.
 //
 // The backward GEMMs need every quantised activation and weight twice: blocks
 // along the rows for one GEMM and along the columns (written transposed) for
@@ -21,10 +21,13 @@
 namespace mgq {
 namespace {
 
-constexpr int TR = 64, TC = 128;   // tile rows x columns
+constexpr int TR = 128, TC = 128;  // tile rows x columns (per part)
 
+// kExactBf16: every value the source produces is a bf16 value, so the tile
+// keeps it as 2 bytes in shared memory.
 struct SrcPlain {
   static constexpr int kParts = 1;
+  static constexpr bool kExactBf16 = true;
   const uint16_t* x;
   int64_t ld;
   __device__ __forceinline__ void load8(int64_t r, int64_t c, float* v, float*) const {
@@ -47,6 +50,7 @@ __device__ __forceinline__ void store8_bf16(uint16_t* p, const float* v) {
 // h = bf16(silu(g) * u), g = gu[:, :F], u = gu[:, F:]; h optionally written out
 struct SrcSwiglu {
   static constexpr int kParts = 1;
+  static constexpr bool kExactBf16 = true;
   const uint16_t* gu;
   int64_t F;
   uint16_t* h_out;
@@ -55,7 +59,7 @@ struct SrcSwiglu {
     load8_bf16(gu + r * 2 * F + c, g);
     load8_bf16(gu + r * 2 * F + F + c, u);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = round_bf16(__fmul_rn(__fdiv_rn(g[i], 1.0f + expf(-g[i])), u[i]));
+    for (int i = 0; i < 8; ++i) v[i] = round_bf16(__fmul_rn(__fdividef(g[i], 1.0f + __expf(-g[i])), u[i]));
     if (h_out) store8_bf16(h_out + r * F + c, v);
   }
 };
@@ -65,6 +69,7 @@ struct SrcSwiglu {
 // (columns f and F + f) when requested. One read of dh, g, u serves both.
 struct SrcDswiglu {
   static constexpr int kParts = 2;
+  static constexpr bool kExactBf16 = true;
   const uint16_t* dh;
   const uint16_t* gu;
   int64_t F;
@@ -76,7 +81,7 @@ struct SrcDswiglu {
     load8_bf16(gu + r * 2 * F + F + f, u);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float s = __fdiv_rn(1.0f, 1.0f + expf(-g[i]));
+      const float s = __fdividef(1.0f, 1.0f + __expf(-g[i]));
       dg[i] = round_bf16(d[i] * u[i] * s * (1.0f + g[i] * (1.0f - s)));
       du[i] = round_bf16(d[i] * g[i] * s);
     }
@@ -91,6 +96,7 @@ struct SrcDswiglu {
 // (t = e / k), zeros for filler rows
 struct SrcGatherX {
   static constexpr int kParts = 1;
+  static constexpr bool kExactBf16 = true;
   const uint16_t* x;
   const int32_t* src_row;
   int k;
@@ -110,6 +116,7 @@ struct SrcGatherX {
 // (the unpermute backward), zeros for filler rows
 struct SrcGatherDy {
   static constexpr int kParts = 1;
+  static constexpr bool kExactBf16 = false;   // float32 products
   const uint16_t* dout;
   const float* probs;
   const int32_t* src_row;
@@ -144,23 +151,46 @@ struct RowColArgs {
   int rceil;
 };
 
+// shared-memory tile element: bf16 bits (exact sources) or float
+template <bool B16> struct TileT;
+template <> struct TileT<true> {
+  using T = uint16_t;
+  static constexpr int kPad = 2;
+  __device__ static T put(float v) { return (T)(__float_as_uint(v) >> 16); }
+  __device__ static float get(T v) { return __uint_as_float((uint32_t)v << 16); }
+};
+template <> struct TileT<false> {
+  using T = float;
+  static constexpr int kPad = 1;
+  __device__ static T put(float v) { return v; }
+  __device__ static float get(T v) { return v; }
+};
+
+template <class Src>
+constexpr size_t rowcol_smem() {
+  return (size_t)Src::kParts * TR * (TC + TileT<Src::kExactBf16>::kPad) * sizeof(typename TileT<Src::kExactBf16>::T);
+}
+
 template <class Src, int SC, int DT>
 __global__ void __launch_bounds__(256) quant_rowcol_kernel(const Src src, const RowColArgs a) {
+  using TT = TileT<Src::kExactBf16>;
+  using T = typename TT::T;
   constexpr int P = Src::kParts;
-  constexpr int R = TR / P;                 // tile rows: 64 (one part) or 32 (two parts)
-  __shared__ float tile[P][R][TC + 1];
+  constexpr int LD = TC + TT::kPad;
+  extern __shared__ uint8_t smem_raw[];
+  T* tile = reinterpret_cast<T*>(smem_raw);                 // [P][TR][LD]
   __shared__ uint32_t s_amax[8];
   const int tid = threadIdx.x, warp = tid >> 5;
   const uint32_t lane = tid & 31;
-  const int64_t c0 = (int64_t)blockIdx.x * TC, r0 = (int64_t)blockIdx.y * R;
+  const int64_t c0 = (int64_t)blockIdx.x * TC, r0 = (int64_t)blockIdx.y * TR;
   const int64_t nrows = a.rows_used ? (int64_t)*a.rows_used : a.rows_cap;
   if (r0 >= nrows) return;
   const int64_t g = r0 / a.M;
   const float ts = (SC == MGQ_TENSOR_F32) ? a.tensor_scale[g] : 1.0f;
-  // ---- load: R rows x 16 chunks of 8 columns
+  // ---- load: TR rows x 16 chunks of 8 columns, 8 chunks per thread
   uint32_t am = 0;
-#pragma unroll
-  for (int i = 0; i < 4 / P; ++i) {
+#pragma unroll 4
+  for (int i = 0; i < 8; ++i) {
     const int chunk = tid + 256 * i;
     const int rr = chunk >> 4, cc = (chunk & 15) * 8;
     float v[P][8];
@@ -176,18 +206,18 @@ __global__ void __launch_bounds__(256) quant_rowcol_kernel(const Src src, const 
     for (int p = 0; p < P; ++p) {
       am = max(am, absmax_bits_f32(v[p], 8));
 #pragma unroll
-      for (int j = 0; j < 8; ++j) tile[p][rr][cc + j] = v[p][j];
+      for (int j = 0; j < 8; ++j) tile[(p * TR + rr) * LD + cc + j] = TT::put(v[p][j]);
     }
   }
   __syncthreads();
-  // ---- row-wise: the 64 (part, row) pairs, 8 per warp; lane l takes columns 4l..4l+3
-  for (int pr = warp * 8; a.row_codes && pr < warp * 8 + 8; ++pr) {
-    const int p = pr / R, rr = pr % R;
+  // ---- row-wise: the P*TR (part, row) pairs, P*16 per warp; lane l takes columns 4l..4l+3
+  for (int pr = warp * P * 16; a.row_codes && pr < (warp + 1) * P * 16; ++pr) {
+    const int p = pr / TR, rr = pr % TR;
     const int64_t r = r0 + rr;
     const int64_t cb = c0 + p * a.part_off;       // first output column of this part
     float v[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) v[j] = tile[p][rr][4 * lane + j];
+    for (int j = 0; j < 4; ++j) v[j] = TT::get(tile[(p * TR + rr) * LD + 4 * lane + j]);
     float mult = ts;
     uint32_t scode = 0;
     if (SC == MGQ_MX32_E8M0) {
@@ -211,30 +241,35 @@ __global__ void __launch_bounds__(256) quant_rowcol_kernel(const Src src, const 
     }
     if (r < nrows) *reinterpret_cast<uint32_t*>(a.row_codes + r * a.C + cb + 4 * lane) = w;
   }
-  // ---- column-wise: thread t takes column t % 128 and 32 rows: the half t / 128
-  // of the tile (one part) or part t / 128 (two parts)
+  // ---- column-wise: thread t takes column t % 128 and 128 / (3 - P) rows: the
+  // half t / 128 of the tile (one part) or all rows of part t / 128 (two
+  // parts); each 32-row block is one MX block and 32 contiguous output bytes
   if (a.col_codes) {
     const int cc = tid & 127, sel = tid >> 7;
-    const int p = P == 2 ? sel : 0, rbase = P == 2 ? 0 : 32 * sel;
-    float v[32];
+    const int p = P == 2 ? sel : 0, rbase = P == 2 ? 0 : (TR / 2) * sel;
+    constexpr int NB = P == 2 ? TR / 32 : TR / 64;        // 32-row blocks per thread
+    const int64_t crow = g * a.C + c0 + p * a.part_off + cc;   // row of the column-wise output
+#pragma unroll 1
+    for (int b = 0; b < NB; ++b) {
+      float v[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = tile[p][rbase + i][cc];
-    float mult = ts;
-    const int64_t rg = r0 - g * a.M + rbase;                     // row inside the group
-    const int64_t crow = g * a.C + c0 + p * a.part_off + cc;     // row of the column-wise output
-    if (SC == MGQ_MX32_E8M0) {
-      const int e = mx_exponent(absmax_bits_f32(v, 32), FmtInfo<DT>::emax, a.rceil != 0);
-      mult = mx_multiplier(e);
-      a.col_scales[tiled_scale_offset(crow, rg / 32, a.M / 128)] = (uint8_t)mx_scale_code(e);
+      for (int i = 0; i < 32; ++i) v[i] = TT::get(tile[(p * TR + rbase + 32 * b + i) * LD + cc]);
+      float mult = ts;
+      const int64_t rg = r0 - g * a.M + rbase + 32 * b;   // row inside the group
+      if (SC == MGQ_MX32_E8M0) {
+        const int e = mx_exponent(absmax_bits_f32(v, 32), FmtInfo<DT>::emax, a.rceil != 0);
+        mult = mx_multiplier(e);
+        a.col_scales[tiled_scale_offset(crow, rg / 32, a.M / 128)] = (uint8_t)mx_scale_code(e);
+      }
+      uint32_t cw[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        cw[i] = cvt_fp8x4<DT>(__fmul_rn(v[4 * i], mult), __fmul_rn(v[4 * i + 1], mult),
+                              __fmul_rn(v[4 * i + 2], mult), __fmul_rn(v[4 * i + 3], mult));
+      uint4* dst = reinterpret_cast<uint4*>(a.col_codes + crow * a.M + rg);
+      dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+      dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
     }
-    uint32_t cw[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      cw[i] = cvt_fp8x4<DT>(__fmul_rn(v[4 * i], mult), __fmul_rn(v[4 * i + 1], mult), __fmul_rn(v[4 * i + 2], mult),
-                            __fmul_rn(v[4 * i + 3], mult));
-    uint4* dst = reinterpret_cast<uint4*>(a.col_codes + crow * a.M + rg);
-    dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-    dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
   }
   if (SC == MGQ_TENSOR_F32 && a.amax_out) {
     am = warp_max_u32(am);
@@ -247,18 +282,32 @@ __global__ void __launch_bounds__(256) quant_rowcol_kernel(const Src src, const 
   }
 }
 
-template <class Src>
-int launch_rowcol(const Src& src, const mgq_qdesc* q, RowColArgs a, cudaStream_t s) {
-  const int64_t rows_per_tile = TR / Src::kParts;
-  const dim3 grid((unsigned)(a.C / Src::kParts / TC), (unsigned)((a.rows_cap + rows_per_tile - 1) / rows_per_tile));
-  const int sc = q->scaling, dt = q->dtype;
-  if (sc == MGQ_MX32_E8M0 && dt == MGQ_E4M3) quant_rowcol_kernel<Src, MGQ_MX32_E8M0, MGQ_E4M3><<<grid, 256, 0, s>>>(src, a);
-  else if (sc == MGQ_MX32_E8M0 && dt == MGQ_E5M2) quant_rowcol_kernel<Src, MGQ_MX32_E8M0, MGQ_E5M2><<<grid, 256, 0, s>>>(src, a);
-  else if (sc == MGQ_TENSOR_F32 && dt == MGQ_E4M3) quant_rowcol_kernel<Src, MGQ_TENSOR_F32, MGQ_E4M3><<<grid, 256, 0, s>>>(src, a);
-  else if (sc == MGQ_TENSOR_F32 && dt == MGQ_E5M2) quant_rowcol_kernel<Src, MGQ_TENSOR_F32, MGQ_E5M2><<<grid, 256, 0, s>>>(src, a);
-  else return MGQ_ERR_UNSUPPORTED;
+template <class Src, int SC, int DT>
+int launch_rowcol_t(const Src& src, const RowColArgs& a, dim3 grid, cudaStream_t s) {
+  constexpr size_t smem = rowcol_smem<Src>();
+  auto kern = quant_rowcol_kernel<Src, SC, DT>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (smem > 48 * 1024 && dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return MGQ_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  kern<<<grid, 256, smem, s>>>(src, a);
   MGQ_LAUNCH_CHECK();
   return MGQ_OK;
+}
+
+template <class Src>
+int launch_rowcol(const Src& src, const mgq_qdesc* q, RowColArgs a, cudaStream_t s) {
+  const dim3 grid((unsigned)(a.C / Src::kParts / TC), (unsigned)((a.rows_cap + TR - 1) / TR));
+  const int sc = q->scaling, dt = q->dtype;
+  if (sc == MGQ_MX32_E8M0 && dt == MGQ_E4M3) return launch_rowcol_t<Src, MGQ_MX32_E8M0, MGQ_E4M3>(src, a, grid, s);
+  if (sc == MGQ_MX32_E8M0 && dt == MGQ_E5M2) return launch_rowcol_t<Src, MGQ_MX32_E8M0, MGQ_E5M2>(src, a, grid, s);
+  if (sc == MGQ_TENSOR_F32 && dt == MGQ_E4M3) return launch_rowcol_t<Src, MGQ_TENSOR_F32, MGQ_E4M3>(src, a, grid, s);
+  if (sc == MGQ_TENSOR_F32 && dt == MGQ_E5M2) return launch_rowcol_t<Src, MGQ_TENSOR_F32, MGQ_E5M2>(src, a, grid, s);
+  return MGQ_ERR_UNSUPPORTED;
 }
 
 RowColArgs make_args(const mgq_qdesc* q, int64_t rows_cap, const int32_t* rows_used, int64_t C, int64_t M,

@@ -200,11 +200,11 @@ class ExpertLayer:
         return [
             ("permute_quant", lambda: mgq.moe_permute(x, topk_idx, E, ALIGN, qx, R, self.row_id_map, self.src_row,
                                                       self.offsets, self.counts, self.ws, None, stream)),
-            ("gemm", lambda: mgq.grouped_gemm_fwd(A1, B1, sc, self.offsets, E, R, 2 * F, H, self.gu,
-                                                  mgq.OUT_BF16, stream)),
+            ("gemm_fwd_gateup", lambda: mgq.grouped_gemm_fwd(A1, B1, sc, self.offsets, E, R, 2 * F, H, self.gu,
+                                                             mgq.OUT_BF16, stream)),
             ("swiglu_quant", lambda: mgq.swiglu_quantize(self.gu, R, F, self.offsets, E, qh, self.h_bf16, stream)),
-            ("gemm", lambda: mgq.grouped_gemm_fwd(A2, B2, sc, self.offsets, E, R, H, F, self.y, mgq.OUT_BF16,
-                                                  stream)),
+            ("gemm_fwd_down", lambda: mgq.grouped_gemm_fwd(A2, B2, sc, self.offsets, E, R, H, F, self.y,
+                                                           mgq.OUT_BF16, stream)),
             ("unpermute", lambda: mgq.moe_unpermute(self.y, self.row_id_map, probs, self.out, stream)),
         ]
 
@@ -237,16 +237,16 @@ class ExpertLayer:
         return [
             ("unpermute_bwd_quant", lambda: mgq.moe_unpermute_bwd(dout, self.y, self.row_id_map, self.src_row, probs,
                                                                   R, self.offsets, E, q2, self.dprobs, stream)),
-            ("gemm", lambda: mgq.grouped_gemm_dgrad(*d2, sc, self.offsets, E, R, H, F, self.dh, mgq.OUT_BF16,
-                                                    stream)),
-            ("gemm", lambda: mgq.grouped_gemm_wgrad(*w2, sc, self.offsets, E, R, H, F, self.dw2, 0.0,
-                                                    mgq.OUT_F32, stream)),
+            ("gemm_dgrad_down", lambda: mgq.grouped_gemm_dgrad(*d2, sc, self.offsets, E, R, H, F, self.dh,
+                                                               mgq.OUT_BF16, stream)),
+            ("gemm_wgrad_down", lambda: mgq.grouped_gemm_wgrad(*w2, sc, self.offsets, E, R, H, F, self.dw2, 0.0,
+                                                               mgq.OUT_F32, stream)),
             ("dswiglu_quant", lambda: mgq.dswiglu_quantize(self.dh, self.gu, R, F, self.offsets, E, q1,
                                                            self.dgu_bf16, stream)),
-            ("gemm", lambda: mgq.grouped_gemm_dgrad(*d1, sc, self.offsets, E, R, 2 * F, H, self.dxp,
-                                                    mgq.OUT_BF16, stream)),
-            ("gemm", lambda: mgq.grouped_gemm_wgrad(*w1, sc, self.offsets, E, R, 2 * F, H, self.dw1, 0.0,
-                                                    mgq.OUT_F32, stream)),
+            ("gemm_dgrad_gateup", lambda: mgq.grouped_gemm_dgrad(*d1, sc, self.offsets, E, R, 2 * F, H, self.dxp,
+                                                                 mgq.OUT_BF16, stream)),
+            ("gemm_wgrad_gateup", lambda: mgq.grouped_gemm_wgrad(*w1, sc, self.offsets, E, R, 2 * F, H, self.dw1,
+                                                                 0.0, mgq.OUT_F32, stream)),
             ("permute_bwd", lambda: mgq.moe_permute_bwd(self.dxp, self.row_id_map, self.dx, stream)),
         ]
 
