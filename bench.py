@@ -275,6 +275,48 @@ def cpu_threads():
 
 # ----------------------------------------------------------------------------- main
 
+GEMM_SOURCES = ("fp8_grouped_gemm_gb300/csrc/gemm.cu", "fp8_grouped_gemm_gb300/csrc/ptx_sm100.cuh",
+                "fp8_grouped_gemm_gb300/csrc/device_common.cuh", "fp8_grouped_gemm_gb300/csrc/mgq_internal.h")
+
+
+def measured_gemm_traffic(workload: str):
+    """Mean DRAM bytes per grouped-GEMM launch from the committed ncu summary of
+    this workload, if the GEMM sources are still the ones it measured; else None."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"grouped_gemm_dram_traffic_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    rec = {}
+    with open(path) as f:
+        for line in f:
+            if line.startswith("traffic_record:"):
+                rec = dict(kv.split("=", 1) for kv in line.split()[1:])
+    h = hashlib.sha256()
+    for src in GEMM_SOURCES:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    if rec.get("sources_sha256") != h.hexdigest():
+        return None
+    return {"bytes_per_launch": int(rec["bytes_per_launch"]),
+            "algorithmic_bytes_per_launch": int(rec["algorithmic_bytes_per_launch"])}
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest value of x over all ranks (x itself without a process group)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(flops_per_rank_step: float, world: int, ms_step: float) -> float:
+    """Whole-job TFLOP/s: every rank runs its own replica of the step (weak
+    scaling), so the job does world x the work in the slowest rank's time."""
+    return flops_per_rank_step * world / (ms_step * 1e-3) / 1e12
+
+
 def run_reference(args, w, rank, world):
     """The CPU oracle, timed on the host cores, one bounded sample per step."""
     if rank != 0:
@@ -378,14 +420,10 @@ def main():
     t1.record()
     barrier()
     clk = clocks.stop()
-    ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(t0.elapsed_time(t1), dev if world > 1 else None)
     ms_step = ms / args.steps
     flops = w.gemm_flops()
-    value = flops * world / (ms_step * 1e-3) / 1e12
+    value = job_value(flops, world, ms_step)
     launches = step.lay.gpu_launches_per_step() * args.steps
 
     # per-kernel timing: the same steps with events around every launch
@@ -411,9 +449,11 @@ def main():
     ab = algorithmic_bytes(w, R_pad)
     hbm = {k: {"ms": per[k], "GB/s": ab[k] / (per[k] * 1e-3) / 1e9,
                "frac": ab[k] / (per[k] * 1e-3) / 1e9 / pk["hbm_gbs"]} for k in ab if k in per}
-    roofline = {"bound": "tensor", "kernel": "grouped_gemm_kernel (all grouped GEMM launches of the step)",
+    tr = measured_gemm_traffic(w.name) if not args.tokens else None
+    roofline = {"bound": "tensor", "kernel": "grouped GEMM (all grouped GEMM launches of the step)",
                 "achieved": achieved, "peak": peak_fp8, "unit": "TFLOP/s", "frac": achieved / peak_fp8,
-                "traffic": None,
+                "traffic": tr["bytes_per_launch"] if tr else None,
+                "algorithmic_bytes_per_launch": tr["algorithmic_bytes_per_launch"] if tr else None,
                 "peak_source": f"{pk_src}: bf16 sustained {pk['bf16_tflops_sustained']} TFLOP/s x {ratio:g} "
                                f"({'fp4' if w.recipe == 'nvfp4' else 'fp8'}/bf16 nominal)",
                 "gemm_ms_per_step": gemm_ms}

@@ -40,7 +40,7 @@ constexpr uint32_t kSfaCol = 256;
 __host__ __device__ constexpr uint32_t sfa_bytes(int kind) { return kind == 3 ? 2048u : 512u; }
 __host__ __device__ constexpr uint32_t sfa_cols(int kind) { return kind == 3 ? 16u : 4u; }
 __host__ __device__ constexpr uint32_t sfb_col0(int kind) { return kSfaCol + sfa_cols(kind) * 4; }
-constexpr uint64_t kWaitNs = 2000000000ull;     // 2 s: far beyond any tile
+constexpr uint64_t kWaitNs = 2000000000ull;     // default wait limit, 2 s: far beyond any tile
 constexpr int kMaxE = 1024;
 
 constexpr uint32_t kABytes = BM * BK, kBBytes = BN * BK;
@@ -75,6 +75,9 @@ struct GemmParams {
   float beta;
   uint32_t idesc;
   int tma_store;      // pair kernel: write the output through TMA stores
+  int debug_stall;    // failure-detection test: the producer issues no loads, so
+                      // every consumer wait runs out and reports MGQ_ERR_TIMEOUT
+  uint64_t wait_ns;   // limit of every mbarrier wait
   int* err;
 };
 
@@ -197,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *s_tmem;
   const bool run = (*s_bad == 0);
 
-  if (run && warp == 0 && lane == 0) {
+  if (run && warp == 0 && lane == 0 && !p.debug_stall) {
     // ------------------------------------------------------------ producer
     int ecur = 0;
     uint32_t it = 0;
@@ -206,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < tl.nst; ++s, ++it) {
         const uint32_t st = it % STAGES, ph = (it / STAGES) & 1;
         if (*s_abort) break;
-        if (!ptx::mbar_wait(&empty[st], ph ^ 1, kWaitNs)) {
+        if (!ptx::mbar_wait(&empty[st], ph ^ 1, p.wait_ns)) {
           report(p.err, MGQ_ERR_TIMEOUT);
           *s_abort = 1;
           break;
@@ -243,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t a = tc % kAcc;
       if (!BLOCK) {
         const uint32_t aph = (tc / kAcc) & 1;
-        if (!ptx::mbar_wait(&tmem_empty[a], aph ^ 1, kWaitNs)) {
+        if (!ptx::mbar_wait(&tmem_empty[a], aph ^ 1, p.wait_ns)) {
           report(p.err, MGQ_ERR_TIMEOUT);
           *s_abort = 1;
           break;
@@ -255,14 +258,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (BLOCK) {
           // every stage gets a fresh partial buffer
           a = tc % kAcc;
-          if (!ptx::mbar_wait(&tmem_empty[a], ((tc / kAcc) & 1) ^ 1, kWaitNs)) {
+          if (!ptx::mbar_wait(&tmem_empty[a], ((tc / kAcc) & 1) ^ 1, p.wait_ns)) {
             report(p.err, MGQ_ERR_TIMEOUT);
             *s_abort = 1;
             ok = false;
             break;
           }
         }
-        if (*s_abort || !ptx::mbar_wait(&full[st], ph, kWaitNs)) {
+        if (*s_abort || !ptx::mbar_wait(&full[st], ph, p.wait_ns)) {
           report(p.err, MGQ_ERR_TIMEOUT);
           *s_abort = 1;
           ok = false;
@@ -349,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float f = sa_next * sb_blk[tl.kx0 / 128 + s];
           if (s + 1 < tl.nst) sa_next = sa_row[(tl.kx0 / 128 + s + 1) * p.sa_ld];
           if (__any_sync(0xFFFFFFFFu, *s_abort != 0)) { alive = false; break; }
-          const bool got = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&tmem_full[a], aph, kWaitNs));
+          const bool got = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&tmem_full[a], aph, p.wait_ns));
           if (!got) {
             report(p.err, MGQ_ERR_TIMEOUT);
             *s_abort = 1;
@@ -376,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a = tc % kAcc, aph = (tc / kAcc) & 1;
         // the whole warp agrees before the .sync.aligned tensor-memory loads
         if (__any_sync(0xFFFFFFFFu, *s_abort != 0)) break;
-        const bool got = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&tmem_full[a], aph, kWaitNs));
+        const bool got = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&tmem_full[a], aph, p.wait_ns));
         if (!got) {
           report(p.err, MGQ_ERR_TIMEOUT);
           *s_abort = 1;
@@ -577,7 +580,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *s_tmem;
   const bool run = (*s_bad == 0);
 
-  if (run && warp == 0 && lane == 0) {
+  if (run && warp == 0 && lane == 0 && !p.debug_stall) {
     // ------------------------------------------------------------ producer (both CTAs)
     int ecur = 0;
     uint32_t it = 0;
@@ -586,7 +589,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int s = 0; s < tl.nst; ++s, ++it) {
         const uint32_t st = it % PSTAGES, ph = (it / PSTAGES) & 1;
         if (*s_abort) break;
-        if (!ptx::mbar_wait(&empty[st], ph ^ 1, kWaitNs)) {
+        if (!ptx::mbar_wait(&empty[st], ph ^ 1, p.wait_ns)) {
           report(p.err, MGQ_ERR_TIMEOUT);
           *s_abort = 1;
           break;
@@ -609,7 +612,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (tl.nst == 0) continue;
       if (*s_abort) break;
       const uint32_t a = tc & 1, aph = (tc >> 1) & 1;
-      if (!ptx::mbar_wait(&tmem_empty[a], aph ^ 1, kWaitNs)) {
+      if (!ptx::mbar_wait(&tmem_empty[a], aph ^ 1, p.wait_ns)) {
         report(p.err, MGQ_ERR_TIMEOUT);
         *s_abort = 1;
         break;
@@ -618,7 +621,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int s = 0; s < tl.nst; ++s, ++it) {
         const uint32_t st = it % PSTAGES, ph = (it / PSTAGES) & 1;
-        if (*s_abort || !ptx::mbar_wait(&full[st], ph, kWaitNs)) {
+        if (*s_abort || !ptx::mbar_wait(&full[st], ph, p.wait_ns)) {
           report(p.err, MGQ_ERR_TIMEOUT);
           *s_abort = 1;
           ok = false;
@@ -666,7 +669,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       const uint32_t a = tc & 1, aph = (tc >> 1) & 1;
       if (__any_sync(0xFFFFFFFFu, *s_abort != 0)) break;
-      const bool got = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&tmem_full[a], aph, kWaitNs));
+      const bool got = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&tmem_full[a], aph, p.wait_ns));
       if (!got) {
         report(p.err, MGQ_ERR_TIMEOUT);
         *s_abort = 1;
@@ -798,6 +801,18 @@ int launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtenso
 // The 2-CTA kernel serves per-tensor FP8 (wgrad needs output rows in
 // multiples of 256); MGQ_GEMM_1CTA=1 in the environment selects the 1-CTA
 // kernel for every call (both compute the same values).
+// Failure-detection knobs (read at every launch): MGQ_DEBUG_GEMM_STALL=1 makes
+// the producer issue no loads, so the pipeline waits run out and the kernel
+// reports MGQ_ERR_TIMEOUT and exits cleanly; MGQ_DEBUG_WAIT_MS sets the wait
+// limit (default 2000 ms).
+void debug_knobs(int* stall, uint64_t* wait_ns) {
+  const char* e = getenv("MGQ_DEBUG_GEMM_STALL");
+  *stall = (e && e[0] == '1') ? 1 : 0;
+  const char* w = getenv("MGQ_DEBUG_WAIT_MS");
+  const long ms = w ? atol(w) : 0;
+  *wait_ns = ms > 0 ? (uint64_t)ms * 1000000ull : kWaitNs;
+}
+
 // MGQ_GEMM_DIRECT_STORE=1 makes the pair kernel store from registers
 // instead of through TMA (same values).
 bool direct_store_forced() {
@@ -889,6 +904,7 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
   p.out_f32 = out_dtype == MGQ_OUT_F32;
   p.beta = beta;
   p.tma_store = 0;
+  debug_knobs(&p.debug_stall, &p.wait_ns);
   p.idesc = nv   ? ptx::idesc_mxf4nvf4_ue4m3(BM, BN)
             : mx ? ptx::idesc_mxf8f6f4(A->dtype, B->dtype, BM, BN)
                  : ptx::idesc_f8f6f4(A->dtype, B->dtype, BM, BN);
