@@ -44,8 +44,18 @@ constexpr uint64_t kWaitNs = 2000000000ull;     // default wait limit, 2 s: far 
 constexpr int kMaxE = 1024;
 
 constexpr uint32_t kABytes = BM * BK, kBBytes = BN * BK;
-constexpr size_t kSmemStage = kABytes + kBBytes + 2048 + 4096;   // largest (NVFP4) scale chunks
-constexpr size_t kSmemBytes = 1024 /*align slack*/ + STAGES * kSmemStage + 256 /*barriers*/ + (kMaxE + 8) * 4;
+// per stage: A + B tiles and the scale chunks (MX 512 + 1024 bytes, NVFP4 2048 + 4096)
+__host__ __device__ constexpr uint32_t sf_stage_bytes(int kind) {
+  return kind == 0 ? 3 * 512u : kind == 3 ? 3 * 2048u : 0u;
+}
+// epilogue staging for TMA stores: 8 warps x 32 rows x 64 bytes (none for NVFP4,
+// whose larger scale chunks leave no room)
+constexpr uint32_t kStageOut = 32 * 64;
+__host__ __device__ constexpr uint32_t staging_bytes(int kind) { return kind == 3 ? 0u : 8 * kStageOut; }
+__host__ __device__ constexpr size_t smem_bytes(int kind) {
+  return 1024 /*align slack*/ + STAGES * (size_t)(kABytes + kBBytes + sf_stage_bytes(kind)) + staging_bytes(kind) +
+         256 /*barriers*/ + (kMaxE + 8) * 4;
+}
 
 enum { kModeRows = 0, kModeContract = 1 };
 // operand scaling handled by the kernel: E8M0 block scales in the MMA, one
@@ -127,10 +137,96 @@ __device__ __forceinline__ bool get_tile(const int32_t* s_off, int E, const Gemm
   return true;
 }
 
+// Stores one thread's 128 accumulator columns (its row `orow`, columns col0..)
+// scaled by alpha: through TMA (the warp stages 32 rows x 64 bytes at a time in
+// `stg`; whole lines reach memory) or, when accumulating into float32 (beta) or
+// without staging, directly from registers.
+__device__ __forceinline__ void epilogue_store(const GemmParams& p, const uint32_t (&r)[4][32], float alpha,
+                                               int64_t orow, int64_t col0, bool use_tma, uint8_t* stg,
+                                               const CUtensorMap* tmO, int32_t y0, uint32_t lane) {
+  if (use_tma) {
+    // 64-byte column chunks: 8 (float32) or 4 (bf16); fully unrolled so the
+    // accumulator registers are indexed statically
+    auto put = [&](int ch, int j, uint4 v, int ncols) {
+      if (j == 0) {
+        if (lane == 0) ptx::bulk_wait_read0();   // previous chunk read out of the buffer
+        __syncwarp();
+      }
+      reinterpret_cast<uint4*>(stg + lane * 64)[j] = v;
+      if (j == 3) {
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_2d(tmO, stg, (int32_t)(col0 + ch * ncols), y0);
+          ptx::bulk_commit();
+        }
+      }
+    };
+    if (p.out_f32) {
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int c = ch >> 1, i0 = (ch & 1) * 16 + 4 * j;
+          put(ch, j,
+              make_uint4(__float_as_uint(__uint_as_float(r[c][i0]) * alpha),
+                         __float_as_uint(__uint_as_float(r[c][i0 + 1]) * alpha),
+                         __float_as_uint(__uint_as_float(r[c][i0 + 2]) * alpha),
+                         __float_as_uint(__uint_as_float(r[c][i0 + 3]) * alpha)),
+              16);
+        }
+    } else {
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i0 = 8 * j;
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(r[ch][i0]) * alpha, __uint_as_float(r[ch][i0 + 1]) * alpha);
+          v.y = pack_bf16x2(__uint_as_float(r[ch][i0 + 2]) * alpha, __uint_as_float(r[ch][i0 + 3]) * alpha);
+          v.z = pack_bf16x2(__uint_as_float(r[ch][i0 + 4]) * alpha, __uint_as_float(r[ch][i0 + 5]) * alpha);
+          v.w = pack_bf16x2(__uint_as_float(r[ch][i0 + 6]) * alpha, __uint_as_float(r[ch][i0 + 7]) * alpha);
+          put(ch, j, v, 32);
+        }
+    }
+    return;
+  }
+  if (p.out_f32) {
+    float* o = static_cast<float*>(p.out) + orow * p.ldo + col0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        float4 v = make_float4(__uint_as_float(r[c][i]) * alpha, __uint_as_float(r[c][i + 1]) * alpha,
+                               __uint_as_float(r[c][i + 2]) * alpha, __uint_as_float(r[c][i + 3]) * alpha);
+        if (p.beta != 0.0f) {
+          const float4 old = *reinterpret_cast<const float4*>(o + c * 32 + i);
+          v.x += p.beta * old.x; v.y += p.beta * old.y; v.z += p.beta * old.z; v.w += p.beta * old.w;
+        }
+        *reinterpret_cast<float4*>(o + c * 32 + i) = v;
+      }
+    }
+  } else {
+    uint16_t* o = static_cast<uint16_t*>(p.out) + orow * p.ldo + col0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+      for (int i = 0; i < 32; i += 8) {
+        uint4 v;
+        v.x = pack_bf16x2(__uint_as_float(r[c][i]) * alpha, __uint_as_float(r[c][i + 1]) * alpha);
+        v.y = pack_bf16x2(__uint_as_float(r[c][i + 2]) * alpha, __uint_as_float(r[c][i + 3]) * alpha);
+        v.z = pack_bf16x2(__uint_as_float(r[c][i + 4]) * alpha, __uint_as_float(r[c][i + 5]) * alpha);
+        v.w = pack_bf16x2(__uint_as_float(r[c][i + 6]) * alpha, __uint_as_float(r[c][i + 7]) * alpha);
+        *reinterpret_cast<uint4*>(o + c * 32 + i) = v;
+      }
+    }
+  }
+}
+
 template <int MODE, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const GemmParams p) {
+                        const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -140,7 +236,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kSfbCol = sfb_col0(KIND);
   uint8_t* sSFA = sB + STAGES * kBBytes;
   uint8_t* sSFB = sSFA + STAGES * kSfaBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sSFA + STAGES * 3 * 2048);
+  uint8_t* sOut = sSFA + STAGES * sf_stage_bytes(KIND);       // epilogue staging (TMA stores)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + staging_bytes(KIND));
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* tmem_full = bars + 2 * STAGES;        // [2]
@@ -396,38 +493,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float alpha = 1.0f;
       if (KIND == kKindTensor || NV) alpha = 1.0f / (p.sa[0] * p.sb[MODE == kModeRows ? tl.e : 0]);
-      if (p.out_f32) {
-        float* o = static_cast<float*>(p.out) + orow * p.ldo + col0;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            float4 v = make_float4(__uint_as_float(r[c][i]) * alpha, __uint_as_float(r[c][i + 1]) * alpha,
-                                   __uint_as_float(r[c][i + 2]) * alpha, __uint_as_float(r[c][i + 3]) * alpha);
-            if (p.beta != 0.0f) {
-              const float4 old = *reinterpret_cast<const float4*>(o + c * 32 + i);
-              v.x += p.beta * old.x; v.y += p.beta * old.y; v.z += p.beta * old.z; v.w += p.beta * old.w;
-            }
-            *reinterpret_cast<float4*>(o + c * 32 + i) = v;
-          }
-        }
-      } else {
-        uint16_t* o = static_cast<uint16_t*>(p.out) + orow * p.ldo + col0;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(r[c][i]) * alpha, __uint_as_float(r[c][i + 1]) * alpha);
-            v.y = pack_bf16x2(__uint_as_float(r[c][i + 2]) * alpha, __uint_as_float(r[c][i + 3]) * alpha);
-            v.z = pack_bf16x2(__uint_as_float(r[c][i + 4]) * alpha, __uint_as_float(r[c][i + 5]) * alpha);
-            v.w = pack_bf16x2(__uint_as_float(r[c][i + 6]) * alpha, __uint_as_float(r[c][i + 7]) * alpha);
-            *reinterpret_cast<uint4*>(o + c * 32 + i) = v;
-          }
-        }
-      }
+      epilogue_store(p, r, alpha, orow, col0, staging_bytes(KIND) != 0 && p.tma_store,
+                     sOut + (warp - 2) * kStageOut, &tmO, (int32_t)(tl.out_row + q * 32), lane);
     }
   }
+  if (warp >= 2 && lane == 0) ptx::bulk_wait0();   // this warp's TMA stores are complete
   __syncthreads();
   if (warp == 1) {
     __syncwarp();
@@ -437,8 +507,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int MODE, int KIND>
-int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, cudaStream_t s) {
+int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const GemmParams& p,
+                cudaStream_t s) {
   auto kern = grouped_gemm_kernel<MODE, KIND>;
+  constexpr size_t kSmemBytes = smem_bytes(KIND);
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -447,7 +519,7 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& 
       return MGQ_ERR_CUDA;
     attr_set[dev] = true;
   }
-  kern<<<num_sms(), kThreads, kSmemBytes, s>>>(ta, tb, p);
+  kern<<<num_sms(), kThreads, kSmemBytes, s>>>(ta, tb, to, p);
   MGQ_LAUNCH_CHECK();
   return MGQ_OK;
 }
@@ -466,7 +538,6 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& 
 //     on CTA 0's `tmem_empty`.
 constexpr int PSTAGES = 6;
 constexpr uint32_t kPairTile = 128 * 128;                      // bytes of one A or B half tile
-constexpr uint32_t kStageOut = 32 * 64;                          // per epilogue warp: 32 rows x 64 bytes
 constexpr size_t kPairSmem = 1024 + PSTAGES * 2 * kPairTile + 8 * kStageOut + 256 + (2 * kMaxE + 16) * 4;
 
 template <int MODE>
@@ -687,87 +758,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ++tc;
       if (!store) continue;    // the warp's 32 rows lie wholly inside or past the group
       const float alpha = 1.0f / (p.sa[0] * p.sb[MODE == kModeRows ? tl.e : 0]);
-      if (p.tma_store) {
-        // TMA stores: the warp stages 32 rows x 64 bytes at a time and the
-        // tensor-memory copy engine writes them as whole lines
-        uint8_t* stg = sOut + (warp - 2) * kStageOut;
-        const int32_t y0 = (int32_t)(tl.out_row + 128 * rank + q * 32);
-        // 64-byte column chunks of the warp's 128 columns: 8 (float32) or 4 (bf16);
-        // fully unrolled so the accumulator registers are indexed statically
-        auto put = [&](int ch, int j, uint4 v, int ncols) {
-          if (j == 0) {
-            if (lane == 0) ptx::bulk_wait_read0();   // previous chunk read out of the buffer
-            __syncwarp();
-          }
-          reinterpret_cast<uint4*>(stg + lane * 64)[j] = v;
-          if (j == 3) {
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              ptx::tma_store_2d(&tmO, stg, (int32_t)(col0 + ch * ncols), y0);
-              ptx::bulk_commit();
-            }
-          }
-        };
-        if (p.out_f32) {
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int c = ch >> 1, i0 = (ch & 1) * 16 + 4 * j;
-              put(ch, j,
-                  make_uint4(__float_as_uint(__uint_as_float(r[c][i0]) * alpha),
-                             __float_as_uint(__uint_as_float(r[c][i0 + 1]) * alpha),
-                             __float_as_uint(__uint_as_float(r[c][i0 + 2]) * alpha),
-                             __float_as_uint(__uint_as_float(r[c][i0 + 3]) * alpha)),
-                  16);
-            }
-        } else {
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int i0 = 8 * j;
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(r[ch][i0]) * alpha, __uint_as_float(r[ch][i0 + 1]) * alpha);
-              v.y = pack_bf16x2(__uint_as_float(r[ch][i0 + 2]) * alpha, __uint_as_float(r[ch][i0 + 3]) * alpha);
-              v.z = pack_bf16x2(__uint_as_float(r[ch][i0 + 4]) * alpha, __uint_as_float(r[ch][i0 + 5]) * alpha);
-              v.w = pack_bf16x2(__uint_as_float(r[ch][i0 + 6]) * alpha, __uint_as_float(r[ch][i0 + 7]) * alpha);
-              put(ch, j, v, 32);
-            }
-        }
-        continue;
-      }
-      if (p.out_f32) {
-        float* o = static_cast<float*>(p.out) + orow * p.ldo + col0;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            float4 v = make_float4(__uint_as_float(r[c][i]) * alpha, __uint_as_float(r[c][i + 1]) * alpha,
-                                   __uint_as_float(r[c][i + 2]) * alpha, __uint_as_float(r[c][i + 3]) * alpha);
-            if (p.beta != 0.0f) {
-              const float4 old = *reinterpret_cast<const float4*>(o + c * 32 + i);
-              v.x += p.beta * old.x; v.y += p.beta * old.y; v.z += p.beta * old.z; v.w += p.beta * old.w;
-            }
-            *reinterpret_cast<float4*>(o + c * 32 + i) = v;
-          }
-        }
-      } else {
-        uint16_t* o = static_cast<uint16_t*>(p.out) + orow * p.ldo + col0;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(r[c][i]) * alpha, __uint_as_float(r[c][i + 1]) * alpha);
-            v.y = pack_bf16x2(__uint_as_float(r[c][i + 2]) * alpha, __uint_as_float(r[c][i + 3]) * alpha);
-            v.z = pack_bf16x2(__uint_as_float(r[c][i + 4]) * alpha, __uint_as_float(r[c][i + 5]) * alpha);
-            v.w = pack_bf16x2(__uint_as_float(r[c][i + 6]) * alpha, __uint_as_float(r[c][i + 7]) * alpha);
-            *reinterpret_cast<uint4*>(o + c * 32 + i) = v;
-          }
-        }
-      }
+      epilogue_store(p, r, alpha, orow, col0, p.tma_store != 0, sOut + (warp - 2) * kStageOut, &tmO,
+                     (int32_t)(tl.out_row + 128 * rank + q * 32), lane);
     }
   }
   if (warp >= 2 && lane == 0) ptx::bulk_wait0();   // this warp's TMA stores are complete
@@ -927,14 +919,21 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
     return mode == kModeRows ? launch_gemm_pair<kModeRows>(ta, tb2, to, p, s)
                              : launch_gemm_pair<kModeContract>(ta, tb2, to, p, s);
   }
-  if (mode == kModeRows) {
-    if (kind == kKindMX) return launch_gemm<kModeRows, kKindMX>(ta, tb, p, s);
-    if (kind == kKindTensor) return launch_gemm<kModeRows, kKindTensor>(ta, tb, p, s);
-    if (kind == kKindNV) return launch_gemm<kModeRows, kKindNV>(ta, tb, p, s);
-    return launch_gemm<kModeRows, kKindBlock>(ta, tb, p, s);
+  CUtensorMap to;
+  {
+    const int eb = p.out_f32 ? 4 : 2;
+    const uint64_t orows = mode == kModeRows ? (uint64_t)R_cap : (uint64_t)E * N;
+    if (!encode_tmap_2d(&to, out, eb, (uint64_t)p.ldo, orows, (uint64_t)p.ldo * eb, 64 / eb, 32)) return MGQ_ERR_CUDA;
+    p.tma_store = (beta == 0.0f && !direct_store_forced()) ? 1 : 0;
   }
-  if (kind == kKindMX) return launch_gemm<kModeContract, kKindMX>(ta, tb, p, s);
-  return launch_gemm<kModeContract, kKindTensor>(ta, tb, p, s);
+  if (mode == kModeRows) {
+    if (kind == kKindMX) return launch_gemm<kModeRows, kKindMX>(ta, tb, to, p, s);
+    if (kind == kKindTensor) return launch_gemm<kModeRows, kKindTensor>(ta, tb, to, p, s);
+    if (kind == kKindNV) return launch_gemm<kModeRows, kKindNV>(ta, tb, to, p, s);
+    return launch_gemm<kModeRows, kKindBlock>(ta, tb, to, p, s);
+  }
+  if (kind == kKindMX) return launch_gemm<kModeContract, kKindMX>(ta, tb, to, p, s);
+  return launch_gemm<kModeContract, kKindTensor>(ta, tb, to, p, s);
 }
 
 }  // namespace
