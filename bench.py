@@ -156,10 +156,10 @@ class Step:
         self.events.append(ev)
 
 
-def algorithmic_bytes(w, R_pad):
+def algorithmic_bytes(w, R_pad, cols):
     if w.recipe == "nvfp4":
         return algorithmic_bytes_nvfp4(w)
-    return algorithmic_bytes_fp8(w, R_pad)
+    return algorithmic_bytes_fp8(w, R_pad, cols)
 
 
 def algorithmic_bytes_nvfp4(w):
@@ -174,20 +174,24 @@ def algorithmic_bytes_nvfp4(w):
             "weight_quant": E * 3 * F * H * 2 * 2 + E * 3 * F * H * q}
 
 
-def algorithmic_bytes_fp8(w, R_pad):
-    """Compulsory HBM bytes of the memory-bound steps (each input read once,
-    each output written once; a row quantised once per token is written k
-    times)."""
+def algorithmic_bytes_fp8(w, R_pad, cols):
+    """Compulsory HBM bytes of the memory-bound steps: each input read once,
+    each output written once (a row quantised once per token is written k
+    times). A quantised output is one byte per element plus, with MX scaling,
+    one E8M0 byte per 32; `cols` adds the column-wise copies (MX training;
+    per-tensor scaling reads the row-wise codes MN-major and writes none)."""
     T, k, H, F, E = w.T, w.k, w.H, w.F, w.E
     R = T * k
+    q = 1 + 1 / 32 if w.recipe == "mxfp8" else 1
+    c = 1 if cols else 0
     b = {}
-    b["permute_quant"] = T * H * 2 + R * H * 1 + (R * H * 1 if w.backward else 0)   # + col copy (transpose)
-    b["swiglu_quant"] = R * 2 * F * 2 + R * F * 1 + (2 * R * F if w.backward else 0)
+    b["permute_quant"] = T * H * 2 + (1 + c) * R * H * q
+    b["swiglu_quant"] = R * 2 * F * 2 + (1 + c) * R * F * q
     b["unpermute"] = R * H * 2 + T * H * 2
-    b["weight_quant"] = E * 3 * F * H * (2 + 1) + (E * 3 * F * H * 2 if w.backward else 0)
+    b["weight_quant"] = E * 3 * F * H * 2 + (1 + c) * E * 3 * F * H * q
     if w.backward:
-        b["unpermute_bwd_quant"] = T * H * 2 + R * H * 2 + R * H * 1 + 2 * R * H
-        b["dswiglu_quant"] = R * F * 2 + R * 2 * F * 2 + R * 2 * F * 1 + 2 * R * 2 * F
+        b["unpermute_bwd_quant"] = T * H * 2 + R * H * 2 + (1 + c) * R * H * q
+        b["dswiglu_quant"] = R * F * 2 + R * 2 * F * 2 + (1 + c) * R * 2 * F * q
         b["permute_bwd"] = R * H * 2 + T * H * 2
     return b
 
@@ -446,7 +450,7 @@ def main():
     ratio = FP4_OVER_BF16 if w.recipe == "nvfp4" else FP8_OVER_BF16
     peak_fp8 = pk["bf16_tflops_sustained"] * ratio
     R_pad = int(step.lay.offsets[-1].item())
-    ab = algorithmic_bytes(w, R_pad)
+    ab = algorithmic_bytes(w, R_pad, cols=step.lay.train and not step.lay.mn)
     hbm = {k: {"ms": per[k], "GB/s": ab[k] / (per[k] * 1e-3) / 1e9,
                "frac": ab[k] / (per[k] * 1e-3) / 1e9 / pk["hbm_gbs"]} for k in ab if k in per}
     tr = measured_gemm_traffic(w.name) if not args.tokens else None

@@ -85,6 +85,7 @@ struct GemmParams {
   float beta;
   uint32_t idesc;
   int tma_store;      // pair kernel: write the output through TMA stores
+  int a_mn, b_mn;     // pair kernel: operand stored MN-major (contraction down the rows)
   int debug_stall;    // failure-detection test: the producer issues no loads, so
                       // every consumer wait runs out and reports MGQ_ERR_TIMEOUT
   uint64_t wait_ns;   // limit of every mbarrier wait
@@ -668,8 +669,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (leader) ptx::mbar_arrive_expect_tx(&full[st], 4 * kPairTile);   // both CTAs' A and B halves
         const uint32_t bar0 = ptx::mapa_shared(ptx::smem_u32(&full[st]), 0);
         const int32_t kx = (int32_t)(tl.kx0 + (int64_t)s * BK);
-        ptx::tma_load_2d_pair(sA + st * kPairTile, &tmA, bar0, kx, (int32_t)(tl.row_a + 128 * rank));
-        ptx::tma_load_2d_pair(sB + st * kPairTile, &tmB, bar0, kx, (int32_t)(tl.row_b + 128 * rank));
+        // K-major: box (128 contraction bytes, 128 rows); MN-major: box (128
+        // columns of M/N, 128 contraction rows)
+        const int32_t am = (int32_t)(tl.row_a + 128 * rank);
+        if (p.a_mn) ptx::tma_load_2d_pair(sA + st * kPairTile, &tmA, bar0, am, kx);
+        else ptx::tma_load_2d_pair(sA + st * kPairTile, &tmA, bar0, kx, am);
+        if (p.b_mn)
+          ptx::tma_load_2d_pair(sB + st * kPairTile, &tmB, bar0, (int32_t)(tl.out_col + 128 * rank),
+                                (int32_t)((MODE == kModeRows ? (int64_t)tl.e * p.K : 0) + kx));
+        else
+          ptx::tma_load_2d_pair(sB + st * kPairTile, &tmB, bar0, kx, (int32_t)(tl.row_b + 128 * rank));
       }
       if (*s_abort) break;
     }
@@ -699,11 +708,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         }
         ptx::tc_fence_after();
-        const uint64_t ad = ptx::sdesc_kmajor_sw128(sA0 + st * kPairTile);
-        const uint64_t bd = ptx::sdesc_kmajor_sw128(sB0 + st * kPairTile);
+        // a K=32 step: 32 bytes along a K-major row, 32 rows (4096 bytes) of
+        // an MN-major tile; descriptor addresses count 16-byte units
+        const uint64_t ad = p.a_mn ? ptx::sdesc_mnmajor_sw128(sA0 + st * kPairTile)
+                                   : ptx::sdesc_kmajor_sw128(sA0 + st * kPairTile);
+        const uint64_t bd = p.b_mn ? ptx::sdesc_mnmajor_sw128(sB0 + st * kPairTile)
+                                   : ptx::sdesc_kmajor_sw128(sB0 + st * kPairTile);
+        const uint64_t astep = p.a_mn ? 256 : 2, bstep = p.b_mn ? 256 : 2;
 #pragma unroll
         for (int kk = 0; kk < BK / 32; ++kk)
-          ptx::mma_f8f6f4_pair(tmem + a * BN, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), p.idesc,
+          ptx::mma_f8f6f4_pair(tmem + a * BN, ad + kk * astep, bd + kk * bstep, p.idesc,
                                (s > 0 || kk > 0) ? 1u : 0u);
         ptx::mma_commit_pair(&empty[st], 0x3);        // frees the stage in both CTAs
       }
@@ -850,6 +864,13 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
   else return MGQ_ERR_UNSUPPORTED;
   const bool mx = kind == kKindMX;
   const bool nv = kind == kKindNV;
+  if ((A->layout != MGQ_LAYOUT_K && A->layout != MGQ_LAYOUT_MN) ||
+      (B->layout != MGQ_LAYOUT_K && B->layout != MGQ_LAYOUT_MN))
+    return MGQ_ERR_INVALID_ARG;
+  // MN-major operands: per-tensor FP8 on the 2-CTA kernel; A only in wgrad
+  const bool a_mn = A->layout == MGQ_LAYOUT_MN, b_mn = B->layout == MGQ_LAYOUT_MN;
+  if ((a_mn || b_mn) && (kind != kKindTensor || !use_pair_kernel(mode, N) || (a_mn && mode != kModeContract)))
+    return MGQ_ERR_UNSUPPORTED;
   if (nv != (A->dtype == MGQ_E2M1) || nv != (B->dtype == MGQ_E2M1)) return MGQ_ERR_UNSUPPORTED;
   MGQ_CHECK_ARG(A->scale && B->scale);
   if (mx || nv) MGQ_CHECK_ARG(aligned16(A->scale) && aligned16(B->scale));
@@ -858,23 +879,25 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
   const int64_t ebytes_den = nv ? 2 : 1;
   GemmParams p;
   CUtensorMap ta, tb;
+  // K-major operands here; MN-major ones (2-CTA kernel) get their maps below
+  MGQ_CHECK_ARG(A->ld % 128 == 0 && B->ld % 128 == 0);
   if (mode == kModeRows) {
     MGQ_CHECK_ARG(N > 0 && K > 0 && N % BN == 0 && K % BK == 0);
-    MGQ_CHECK_ARG(A->ld >= K && A->ld % 128 == 0 && B->ld >= K && B->ld % 128 == 0);
+    MGQ_CHECK_ARG(A->ld >= K && (b_mn || B->ld >= K));
     MGQ_CHECK_ARG((int64_t)E * N < (1ll << 31));
     if (!encode_tmap_u8_2d(&ta, A->data, (uint64_t)(K / ebytes_den), (uint64_t)R_cap,
                            (uint64_t)(A->ld / ebytes_den), 128, BM) ||
-        !encode_tmap_u8_2d(&tb, B->data, (uint64_t)(K / ebytes_den), (uint64_t)E * N,
-                           (uint64_t)(B->ld / ebytes_den), 128, BN))
+        (!b_mn && !encode_tmap_u8_2d(&tb, B->data, (uint64_t)(K / ebytes_den), (uint64_t)E * N,
+                                     (uint64_t)(B->ld / ebytes_den), 128, BN)))
       return MGQ_ERR_CUDA;
     // 512-byte scale chunks per 128-row tile: MX 32x4-element blocks, NVFP4 16x4
     p.sfa_kb4 = A->ld / (nv ? 64 : 128);
     p.sfb_kb4 = B->ld / (nv ? 64 : 128);
   } else {
     MGQ_CHECK_ARG(N > 0 && K > 0 && N % BM == 0 && K % BN == 0);
-    MGQ_CHECK_ARG(A->ld >= R_cap && A->ld % 128 == 0 && B->ld >= R_cap && B->ld % 128 == 0);
-    if (!encode_tmap_u8_2d(&ta, A->data, (uint64_t)R_cap, (uint64_t)N, (uint64_t)A->ld, 128, BM) ||
-        !encode_tmap_u8_2d(&tb, B->data, (uint64_t)R_cap, (uint64_t)K, (uint64_t)B->ld, 128, BN))
+    MGQ_CHECK_ARG((a_mn || A->ld >= R_cap) && (b_mn || B->ld >= R_cap));
+    if ((!a_mn && !encode_tmap_u8_2d(&ta, A->data, (uint64_t)R_cap, (uint64_t)N, (uint64_t)A->ld, 128, BM)) ||
+        (!b_mn && !encode_tmap_u8_2d(&tb, B->data, (uint64_t)R_cap, (uint64_t)K, (uint64_t)B->ld, 128, BN)))
       return MGQ_ERR_CUDA;
     p.sfa_kb4 = A->ld / 128;
     p.sfb_kb4 = B->ld / 128;
@@ -896,6 +919,8 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
   p.out_f32 = out_dtype == MGQ_OUT_F32;
   p.beta = beta;
   p.tma_store = 0;
+  p.a_mn = 0;
+  p.b_mn = 0;
   debug_knobs(&p.debug_stall, &p.wait_ns);
   p.idesc = nv   ? ptx::idesc_mxf4nvf4_ue4m3(BM, BN)
             : mx ? ptx::idesc_mxf8f6f4(A->dtype, B->dtype, BM, BN)
@@ -903,13 +928,33 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
   p.err = err;
   cudaStream_t s = as_stream(stream);
   if (kind == kKindTensor && use_pair_kernel(mode, N)) {
-    // the pair kernel loads 128-row halves of B
+    // the pair kernel loads 128-row halves of B (K-major) or 128-column
+    // halves (MN-major); MN-major operands are stored with the contraction
+    // index down the rows:
+    //   rows mode, B: W [E, Kc, ld >= N]; contract mode, A: dY [R_cap, ld >= N],
+    //   B: X [R_cap, ld >= K]
     CUtensorMap tb2;
-    const bool ok = mode == kModeRows
-                        ? encode_tmap_u8_2d(&tb2, B->data, (uint64_t)K, (uint64_t)E * N, (uint64_t)B->ld, 128, 128)
-                        : encode_tmap_u8_2d(&tb2, B->data, (uint64_t)R_cap, (uint64_t)K, (uint64_t)B->ld, 128, 128);
+    bool ok;
+    if (a_mn) {
+      MGQ_CHECK_ARG(A->ld >= N);
+      if (!encode_tmap_u8_2d(&ta, A->data, (uint64_t)N, (uint64_t)R_cap, (uint64_t)A->ld, 128, 128))
+        return MGQ_ERR_CUDA;
+    }
+    if (b_mn && mode == kModeRows) {
+      MGQ_CHECK_ARG(B->ld >= N && (int64_t)E * K < (1ll << 31));
+      ok = encode_tmap_u8_2d(&tb2, B->data, (uint64_t)N, (uint64_t)E * K, (uint64_t)B->ld, 128, 128);
+    } else if (b_mn) {
+      MGQ_CHECK_ARG(B->ld >= K);
+      ok = encode_tmap_u8_2d(&tb2, B->data, (uint64_t)K, (uint64_t)R_cap, (uint64_t)B->ld, 128, 128);
+    } else {
+      ok = mode == kModeRows
+               ? encode_tmap_u8_2d(&tb2, B->data, (uint64_t)K, (uint64_t)E * N, (uint64_t)B->ld, 128, 128)
+               : encode_tmap_u8_2d(&tb2, B->data, (uint64_t)R_cap, (uint64_t)K, (uint64_t)B->ld, 128, 128);
+    }
     if (!ok) return MGQ_ERR_CUDA;
-    p.idesc = ptx::idesc_f8f6f4(A->dtype, B->dtype, 256, BN);
+    p.a_mn = a_mn;
+    p.b_mn = b_mn;
+    p.idesc = ptx::idesc_f8f6f4(A->dtype, B->dtype, 256, BN) | ptx::idesc_mn_major(a_mn, b_mn);
     // output map: [rows, ldo] elements, boxes of 64 bytes x 32 rows
     CUtensorMap to;
     const int eb = p.out_f32 ? 4 : 2;

@@ -193,6 +193,15 @@ constexpr uint32_t kSwizzleNone = 0, kSwizzle128B = 2;
 __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   return sdesc(saddr, 16, 1024, kSwizzle128B);
 }
+// MN-major operand tile (the contraction index runs down the rows): K rows x
+// 128 bytes of M (or N) loaded by TMA with 128-byte swizzling. Groups of 8
+// K-rows are 1024 bytes apart (stride byte offset); the leading byte offset,
+// the distance between 128-byte chunks along M/N, never applies to an operand
+// that is 128 bytes wide and is set to the same 1024 bytes. One K=32 step
+// advances the start address by 32 rows (4096 bytes).
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr) {
+  return sdesc(saddr, 1024, 1024, kSwizzle128B);
+}
 // scale-factor chunk for tcgen05.cp 32x128b: 32 rows of 16 bytes, contiguous
 __device__ __forceinline__ uint64_t sdesc_sf(uint32_t saddr) { return sdesc(saddr, 0, 128, kSwizzleNone); }
 
@@ -200,6 +209,11 @@ __device__ __forceinline__ uint64_t sdesc_sf(uint32_t saddr) { return sdesc(sadd
 // A/B formats (0 e4m3, 1 e5m2), both K-major, N >> 3 at bit 17, M >> 4 at 24.
 __host__ __device__ constexpr uint32_t idesc_f8f6f4(uint32_t atype, uint32_t btype, uint32_t M, uint32_t N) {
   return (1u << 4) | (atype << 7) | (btype << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+// operand majorness bits of the instruction descriptor: A (bit 15) and B
+// (bit 16) read MN-major when set
+__host__ __device__ constexpr uint32_t idesc_mn_major(bool a_mn, bool b_mn) {
+  return (a_mn ? 1u << 15 : 0u) | (b_mn ? 1u << 16 : 0u);
 }
 // Instruction descriptor, kind::mxf8f6f4 block scaling with E8M0 scales
 // (bit 23); the scale-factor ids (B: bits [4,6), A: bits [29,31)) are or-ed in

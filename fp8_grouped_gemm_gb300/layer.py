@@ -11,6 +11,14 @@ backward: moe_unpermute_bwd (+ quantise dY, dprobs) -> grouped_gemm_dgrad and
           and grouped_gemm_wgrad (gate/up) -> moe_permute_bwd
 then:     amax_history_update (delayed scaling)
 
+The backward GEMMs contract over the other dimension of their operands (dgrad
+over the weight's rows, wgrad over the tokens). With block scales (MXFP8) each
+of those operands is requantised column-wise with blocks along the new
+contraction. With per-tensor scales the column-wise copy would hold the same
+codes transposed, so by default the delayed recipe writes none and hands the
+row-wise codes to the GEMMs as MN-major operands (``col_copies=True`` keeps
+the explicit copies).
+
 Every step runs in the library's kernels; this module only allocates buffers
 and passes pointers.
 """
@@ -26,7 +34,7 @@ ALIGN = 128       # group padding: the grouped GEMM tiles rows by 128
 
 class ExpertLayer:
     def __init__(self, w: Workload, device, recipe: str | None = None, keep_bf16: bool = False,
-                 history: int = 1024, train: bool | None = None):
+                 history: int = 1024, train: bool | None = None, col_copies: bool = False):
         self.w = w
         self.dev = torch.device(device)
         self.recipe = recipe or w.recipe
@@ -34,6 +42,8 @@ class ExpertLayer:
             raise NotImplementedError(self.recipe)
         self.train = (w.backward or self.recipe == "delayed") if train is None else train
         self.delayed = self.recipe == "delayed"
+        # per-tensor backward GEMMs read the row-wise codes MN-major
+        self.mn = self.delayed and not col_copies
         if self.train and self.recipe not in ("delayed", "mxfp8"):
             raise NotImplementedError(f"backward with {self.recipe}")
         self.scaling = {"mxfp8": mgq.MX32_E8M0, "delayed": mgq.TENSOR_F32,
@@ -91,16 +101,17 @@ class ExpertLayer:
                 self.bwd_hist = torch.zeros(2, history, **f32)
                 self.heads = torch.zeros(2, **i32)
             # column-wise copies (MX: with their own E8M0 scales, blocks along the old rows)
-            self.xcol = torch.empty(H, R, **u8)
-            self.hcol = torch.empty(F, R, **u8)
-            self.w1col = torch.empty(E, H, 2 * F, **u8)
-            self.w2col = torch.empty(E, F, H, **u8)
+            cols = not self.mn
+            self.xcol = torch.empty(H, R, **u8) if cols else None
+            self.hcol = torch.empty(F, R, **u8) if cols else None
+            self.w1col = torch.empty(E, H, 2 * F, **u8) if cols else None
+            self.w2col = torch.empty(E, F, H, **u8) if cols else None
             self.dy2q = torch.empty(R, H, **u8)
-            self.dy2col = torch.empty(H, R, **u8)
+            self.dy2col = torch.empty(H, R, **u8) if cols else None
             self.dprobs = torch.empty(T, k, **f32)
             self.dh = torch.empty(R, F, **bf)
             self.dy1q = torch.empty(R, 2 * F, **u8)
-            self.dy1col = torch.empty(2 * F, R, **u8)
+            self.dy1col = torch.empty(2 * F, R, **u8) if cols else None
             self.dgu_bf16 = torch.empty(R, 2 * F, **bf) if keep_bf16 else None
             self.dw1 = torch.empty(E, 2 * F, H, **f32)
             self.dw2 = torch.empty(E, H, F, **f32)
@@ -228,12 +239,20 @@ class ExpertLayer:
             s_dy2r, s_dy2c, s_dy1r, s_dy1c = self.dy2s, self.dy2cs, self.dy1s, self.dy1cs
             s_w2c, s_w1c, s_hc, s_xc = self.w2cs, self.w1cs, self.hcs, self.xcs
         O = mgq.operand
-        # down projection: dh = dY2 W2 ; dW2 = dY2^T h
-        d2 = (O(self.dy2q, s_dy2r, H, mgq.E5M2), O(self.w2col, s_w2c, H, mgq.E4M3))
-        w2 = (O(self.dy2col, s_dy2c, R, mgq.E5M2), O(self.hcol, s_hc, R, mgq.E4M3))
-        # gate/up projection: dXp = dY1 W1 ; dW1 = dY1^T X
-        d1 = (O(self.dy1q, s_dy1r, 2 * F, mgq.E5M2), O(self.w1col, s_w1c, 2 * F, mgq.E4M3))
-        w1 = (O(self.dy1col, s_dy1c, R, mgq.E5M2), O(self.xcol, s_xc, R, mgq.E4M3))
+        if self.mn:
+            # the row-wise codes, read transposed by the tensor cores
+            MN = mgq.LAYOUT_MN
+            d2 = (O(self.dy2q, s_dy2r, H, mgq.E5M2), O(self.w2q, s_w2c, F, mgq.E4M3, layout=MN))
+            w2 = (O(self.dy2q, s_dy2c, H, mgq.E5M2, layout=MN), O(self.hq, s_hc, F, mgq.E4M3, layout=MN))
+            d1 = (O(self.dy1q, s_dy1r, 2 * F, mgq.E5M2), O(self.w1q, s_w1c, H, mgq.E4M3, layout=MN))
+            w1 = (O(self.dy1q, s_dy1c, 2 * F, mgq.E5M2, layout=MN), O(self.xq, s_xc, H, mgq.E4M3, layout=MN))
+        else:
+            # down projection: dh = dY2 W2 ; dW2 = dY2^T h
+            d2 = (O(self.dy2q, s_dy2r, H, mgq.E5M2), O(self.w2col, s_w2c, H, mgq.E4M3))
+            w2 = (O(self.dy2col, s_dy2c, R, mgq.E5M2), O(self.hcol, s_hc, R, mgq.E4M3))
+            # gate/up projection: dXp = dY1 W1 ; dW1 = dY1^T X
+            d1 = (O(self.dy1q, s_dy1r, 2 * F, mgq.E5M2), O(self.w1col, s_w1c, 2 * F, mgq.E4M3))
+            w1 = (O(self.dy1col, s_dy1c, R, mgq.E5M2), O(self.xcol, s_xc, R, mgq.E4M3))
         return [
             ("unpermute_bwd_quant", lambda: mgq.moe_unpermute_bwd(dout, self.y, self.row_id_map, self.src_row, probs,
                                                                   R, self.offsets, E, q2, self.dprobs, stream)),
@@ -294,8 +313,10 @@ class ExpertLayer:
             return fwd + 2 + 4                          # + amax passes (x, h); weights: 2 x (amax + rows)
         if not self.train:
             return fwd + 2                              # weight quantisation (row)
-        fwd += 1                                        # column copy of x (h's is fused into SwiGLU)
-        wq = 2                                          # weights: rows + columns in one pass each
-        bwd = 2 + 2 + 1 + 2 + 1                         # unpermute_bwd + its column copy, dgrad/wgrad,
-                                                        # dswiglu (fused columns), dgrad/wgrad, permute_bwd
+        wq = 2                                          # weights: rows (+ columns) in one pass each
+        bwd = 1 + 2 + 1 + 2 + 1                         # unpermute_bwd, dgrad/wgrad, dswiglu (fused
+                                                        # columns), dgrad/wgrad, permute_bwd
+        if not self.mn:
+            fwd += 1                                    # column copy of x (h's is fused into SwiGLU)
+            bwd += 1                                    # column copy of dY2
         return fwd + wq + bwd + (2 if self.delayed else 0)

@@ -23,6 +23,7 @@ E4M3, E5M2, E2M1 = 0, 1, 2
 MX32_E8M0, NV16_UE4M3, BLK_1x128_F32, BLK_128x128_F32, TENSOR_F32 = range(5)
 RCEIL, FLOOR = 0, 1
 OUT_BF16, OUT_F32 = 0, 1
+LAYOUT_K, LAYOUT_MN = 0, 1
 
 FMAX = {E4M3: 448.0, E5M2: 57344.0}
 
@@ -53,7 +54,7 @@ class QDesc(ctypes.Structure):
 
 class Operand(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("ld", ctypes.c_int64),
-                ("dtype", ctypes.c_int), ("global_scale", ctypes.c_void_p)]
+                ("dtype", ctypes.c_int), ("global_scale", ctypes.c_void_p), ("layout", ctypes.c_int)]
 
 
 _lib = None
@@ -125,8 +126,8 @@ def qdesc(dtype, scaling, row_data, row_scale=None, col_data=None, col_scale=Non
                  QBuf(_p(col_data), _p(col_scale)), _p(tensor_scale), _p(amax_out))
 
 
-def operand(data, scale, ld, dtype, global_scale=None) -> Operand:
-    return Operand(_p(data), _p(scale), int(ld), int(dtype), _p(global_scale))
+def operand(data, scale, ld, dtype, global_scale=None, layout=0) -> Operand:
+    return Operand(_p(data), _p(scale), int(ld), int(dtype), _p(global_scale), int(layout))
 
 
 # ---- sizes of the caller-owned buffers (host arithmetic only) ----------------

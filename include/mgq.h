@@ -114,6 +114,14 @@ typedef struct {
                                 required, computed by the call)                 */
 } mgq_qdesc;
 
+/* Which dimension of a GEMM operand is contiguous in memory. */
+typedef enum {
+  MGQ_LAYOUT_K = 0,          /* rows are the operand's M (or N) index, the
+                                contraction index runs along each row          */
+  MGQ_LAYOUT_MN = 1          /* rows are the contraction index (the transposed
+                                storage); per-tensor FP8 dgrad / wgrad only     */
+} mgq_layout;
+
 /* A quantised GEMM operand (device pointers). */
 typedef struct {
   const void* data;          /* codes, row-major, row pitch `ld` elements      */
@@ -121,6 +129,7 @@ typedef struct {
   int64_t ld;                /* row pitch in elements                          */
   int dtype;                 /* mgq_dtype                                       */
   const float* global_scale; /* NVFP4: device s_g per tensor (A) / per expert (W); else NULL */
+  int layout;                /* mgq_layout; 0 (MGQ_LAYOUT_K) unless stated      */
 } mgq_operand;
 
 /* ---- status --------------------------------------------------------------- */
@@ -214,6 +223,14 @@ int mgq_block_quantize(const void* x_bf16, int64_t G, int64_t M, int64_t K,
  *        [K/128][R_cap], W with 128x128 float32 scale_inv [E][N/128][K/128]
  *        ([BLOCK]'s DeepSeek-style recipe; each 128-deep partial product is
  *        scaled and summed in float32).
+ * Operand layout (MGQ_TENSOR_F32 only): with per-tensor scales the
+ *        column-wise copy holds the same codes as the row-wise one,
+ *        transposed, so dgrad accepts the forward weight W [E, N, K] (ld >= K)
+ *        in place of Wcol with layout MGQ_LAYOUT_MN, and wgrad accepts dY
+ *        [R_cap, N] (ld >= N) and A [R_cap, K] (ld >= K) in place of dYcol and
+ *        Acol with layout MGQ_LAYOUT_MN: the tensor cores read them
+ *        transposed. Requires the 2-CTA kernel (wgrad: N a multiple of 256);
+ *        MGQ_ERR_UNSUPPORTED otherwise and for every other scaling.
  * Requires offsets[e] multiples of 128, N a multiple of 256 (fwd/dgrad) or
  * 128, K a multiple of 128, 16-byte aligned pointers. */
 int mgq_grouped_gemm_fwd(const mgq_operand* A, const mgq_operand* W, int scaling,

@@ -85,3 +85,46 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.mgq_block_quantize(16, 1, 128, 128, ctypes.byref(q2), None) == mgq.ERR_UNSUPPORTED
     assert lib.mgq_amax_history_update(None, None, None, None, 1, 1, ctypes.c_float(448.0), None) == INV
     assert lib.mgq_get_error(None, None) == INV
+
+
+def test_operand_layout_validation(lib):
+    """MN-major operands: per-tensor scaling in dgrad (B) and wgrad (A, B)
+    only; anything else is refused on the host."""
+    from fp8_grouped_gemm_gb300 import mgq
+    UNS, INV = mgq.ERR_UNSUPPORTED, mgq.ERR_INVALID_ARG
+    k = mgq.Operand(16, 16, 256, mgq.E4M3)
+    mn = mgq.Operand(16, 16, 256, mgq.E4M3, None, mgq.LAYOUT_MN)
+    bad = mgq.Operand(16, 16, 256, mgq.E4M3, None, 5)
+    args = (16, 4, 256, 256, 256)
+    # MX block scales run along the contraction: no MN-major reading
+    assert lib.mgq_grouped_gemm_dgrad(ctypes.byref(k), ctypes.byref(mn), mgq.MX32_E8M0, *args, 32, 0,
+                                      None) == UNS
+    # the forward activations (and dgrad's dY) are K-major
+    assert lib.mgq_grouped_gemm_fwd(ctypes.byref(mn), ctypes.byref(k), mgq.TENSOR_F32, *args, 32, 0,
+                                    None) == UNS
+    assert lib.mgq_grouped_gemm_fwd(ctypes.byref(bad), ctypes.byref(k), mgq.TENSOR_F32, *args, 32, 0,
+                                    None) == INV
+
+
+def test_struct_layouts_match_the_header(tmp_path):
+    """The ctypes mirrors of mgq_operand / mgq_qdesc have the C layout (sizes
+    and field offsets from a program compiled against include/mgq.h)."""
+    import shutil
+    import subprocess
+    from fp8_grouped_gemm_gb300 import mgq
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "probe.c"
+    src.write_text(
+        "#include <stdio.h>\n#include <stddef.h>\n#include \"mgq.h\"\n"
+        "int main(void){printf(\"%zu %zu %zu %zu %zu %zu %zu\\n\", sizeof(mgq_operand),"
+        " offsetof(mgq_operand, ld), offsetof(mgq_operand, dtype), offsetof(mgq_operand, global_scale),"
+        " offsetof(mgq_operand, layout), sizeof(mgq_qdesc), offsetof(mgq_qdesc, amax_out));return 0;}\n")
+    exe = tmp_path / "probe"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], check=True, capture_output=True,
+                                          text=True).stdout.split()]
+    O, Q = mgq.Operand, mgq.QDesc
+    assert got == [ctypes.sizeof(O), O.ld.offset, O.dtype.offset, O.global_scale.offset, O.layout.offset,
+                   ctypes.sizeof(Q), Q.amax_out.offset]

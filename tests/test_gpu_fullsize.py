@@ -169,19 +169,16 @@ def test_mixtral_training_step_full_size_sampled():
         gots.append(dh_gpu[sel][:, fcols])
     assert rel_fro(OF.round_to_bf16(np.concatenate(refs)), np.concatenate(gots)) <= GEMM_TOL_BF16
     # wgrad of the gate/up projection at sampled (n, k) of every expert:
-    # dW1[e, n, k] = sum over the expert's rows of dY1[r, n] * X[r, k]
-    dy1col = lay.dy1col
-    xcol = lay.xcol
+    # dW1[e, n, k] = sum over the expert's rows of dY1[r, n] * X[r, k]; the
+    # GEMM read the row-wise codes dY1 [R, 2F] and X [R, H] MN-major
+    assert lay.mn and lay.xcol is None
     ns = np.sort(rng.choice(2 * F, 8, replace=False))
     ks = np.sort(rng.choice(H, 8, replace=False))
     dw1 = lay.dw1
     for e in range(E):
         lo, hi = int(off[e]), int(off[e + 1])
-        dyc = u8_np(dy1col[torch.from_numpy(ns).to(DEV), lo:hi])         # [8, rows]
-        xc = u8_np(xcol[torch.from_numpy(ks).to(DEV), lo:hi])            # [8, rows]
+        dyc = u8_np(lay.dy1q[lo:hi][:, torch.from_numpy(ns).to(DEV)]).T     # [8, rows]
+        xc = u8_np(lay.xq[lo:hi][:, torch.from_numpy(ks).to(DEV)]).T        # [8, rows]
         ref = OQ.dequantize_tensor(dyc, bs[1], "e5m2") @ OQ.dequantize_tensor(xc, fs[0]).T
         got = dw1[e][torch.from_numpy(ns).to(DEV)][:, torch.from_numpy(ks).to(DEV)].cpu().numpy()
         assert rel_fro(ref, got) <= 1e-5, e
-    # the column-wise copies are the transposes of the row-wise codes
-    assert torch.equal(lay.xcol[:, :int(off[-1])].t(), lay.xq[:int(off[-1])])
-    assert torch.equal(lay.dy1col[:, :int(off[-1])].t(), lay.dy1q[:int(off[-1])])

@@ -304,6 +304,75 @@ def test_gemm_dgrad_and_wgrad(mgq, scaling):
     assert rel_fro(ref_w + prev.cpu().numpy(), got2) <= GEMM_TOL_F32
 
 
+@pytest.mark.parametrize("exact", [True, False], ids=["exact", "random"])
+def test_gemm_mn_major_operands(mgq, exact):
+    """Per-tensor dgrad and wgrad reading the row-wise codes transposed
+    (MGQ_LAYOUT_MN): dgrad on the forward weight W [E, N, K], wgrad on dY
+    [R, N] and A [R, K] themselves, against the oracle and against the same
+    GEMMs on explicit column-wise copies."""
+    rng = np.random.default_rng(23 + exact)
+    dev = torch.device(DEV)
+    offs = np.array([0, 128, 128, 512, 640, 1024], dtype=np.int32)
+    E, N, K = 5, 768, 512
+    Rp = int(offs[-1])
+    offd = torch.from_numpy(offs).to(dev)
+    f5, f4 = OF.E5M2, OF.E4M3
+
+    def codes(fmt, shape):
+        if exact:    # +-1, +-2 and 0: every float32 partial sum is exact
+            pool = np.array([0x00, 0x3C, 0xBC, 0x40, 0xC0] if fmt is f5 else [0x00, 0x38, 0xB8, 0x40, 0xC0])
+            return rng.choice(pool, size=shape).astype(np.uint8)
+        return (rng.choice(fmt.pos_codes[:-1], size=shape) | (rng.integers(0, 2, shape) * 0x80)).astype(np.uint8)
+
+    dyc, wc, ac = codes(f5, (Rp, N)), codes(f4, (E, N, K)), codes(f4, (Rp, K))
+    s_dy = np.array([0.5 if exact else 1000.0], dtype=np.float32)
+    s_w = np.array([2.0, 0.5, 8.0, 1.0, 4.0], dtype=np.float32)
+    s_a = np.array([4.0], dtype=np.float32)
+    dy_deq = OQ.dequantize_tensor(dyc, s_dy[0], "e5m2")
+    w_deq = np.stack([OQ.dequantize_tensor(wc[e], s_w[e]) for e in range(E)])
+    a_deq = OQ.dequantize_tensor(ac, s_a[0])
+    MN, sc = mgq.LAYOUT_MN, mgq.TENSOR_F32
+    dY = _op(mgq, dyc, s_dy, N, mgq.E5M2, dev)
+    W_mn = _op(mgq, wc, s_w, K, mgq.E4M3, dev)
+    W_mn.layout = MN
+    W_col = _op(mgq, np.ascontiguousarray(wc.transpose(0, 2, 1)), s_w, N, mgq.E4M3, dev)
+    dY_mn = _op(mgq, dyc, s_dy, N, mgq.E5M2, dev)
+    dY_mn.layout = MN
+    A_mn = _op(mgq, ac, s_a, K, mgq.E4M3, dev)
+    A_mn.layout = MN
+    dY_col = _op(mgq, np.ascontiguousarray(dyc.T), s_dy, Rp, mgq.E5M2, dev)
+    A_col = _op(mgq, np.ascontiguousarray(ac.T), s_a, Rp, mgq.E4M3, dev)
+    od = mgq.OUT_F32 if exact else mgq.OUT_BF16
+    ddt = torch.float32 if exact else torch.bfloat16
+    dA_mn = torch.full((Rp, K), float("nan"), dtype=ddt, device=dev)
+    dA_k = torch.full((Rp, K), float("nan"), dtype=ddt, device=dev)
+    mgq.grouped_gemm_dgrad(dY, W_mn, sc, offd, E, Rp, N, K, dA_mn, od)
+    mgq.grouped_gemm_dgrad(dY, W_col, sc, offd, E, Rp, N, K, dA_k, od)
+    dW_mn = torch.full((E, N, K), 5.0, dtype=torch.float32, device=dev)
+    dW_k = torch.full((E, N, K), 5.0, dtype=torch.float32, device=dev)
+    mgq.grouped_gemm_wgrad(dY_mn, A_mn, sc, offd, E, Rp, N, K, dW_mn, 0.0)
+    mgq.grouped_gemm_wgrad(dY_col, A_col, sc, offd, E, Rp, N, K, dW_k, 0.0)
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    ref = OG.grouped_gemm_dgrad(dy_deq, w_deq, offs)
+    ref_w = OG.grouped_gemm_wgrad(dy_deq, a_deq, offs, E)
+    got = dA_mn.float().cpu().numpy().astype(np.float64)
+    got_w = dW_mn.cpu().numpy().astype(np.float64)
+    assert np.all(got_w[1] == 0.0)                            # the empty group
+    if exact:
+        np.testing.assert_array_equal(got, ref)
+        np.testing.assert_array_equal(got_w, ref_w)
+    else:
+        assert rel_fro(OF.round_to_bf16(ref), got) <= GEMM_TOL_BF16
+        assert rel_fro(ref_w, got_w) <= GEMM_TOL_F32
+    # the explicit column-wise copies give the same products
+    if exact:
+        assert torch.equal(dA_mn, dA_k) and torch.equal(dW_mn, dW_k)
+    else:
+        assert rel_fro(dA_k.float().cpu().numpy(), got) <= 1e-4
+        assert rel_fro(dW_k.cpu().numpy(), got_w) <= 1e-4
+
+
 @pytest.mark.parametrize("offs", [[0, 128, 128, 512], [0, 384]], ids=["E3", "E1"])
 def test_gemm_fwd_blockwise(mgq, offs):
     """1x128 activation x 128x128 weight float32 block scales (promotion of
