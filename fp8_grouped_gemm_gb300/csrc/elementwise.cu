@@ -20,6 +20,21 @@ namespace {
 
 constexpr int kWarps = 8;
 
+// CTA-wide max of the warps' per-tensor amax (float bits), one atomic per CTA.
+// Every thread of the CTA must call it.
+__device__ __forceinline__ void cta_amax_atomic(uint32_t tam, float* out) {
+  __shared__ uint32_t s_am[kWarps];
+  tam = warp_max_u32(tam);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) s_am[warp] = tam;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t m = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = max(m, s_am[w]);
+    atomic_max_nonneg(out, __uint_as_float(m));
+  }
+}
+
 // ---- SwiGLU + quantise: warp per row ----------------------------------------
 struct SwigluArgs {
   const uint16_t* gu;   // [R_cap, 2F]
@@ -42,11 +57,11 @@ __global__ void __launch_bounds__(256) swiglu_quant_kernel(SwigluArgs a) {
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
   const int64_t r = (int64_t)blockIdx.x * kWarps + warp;
-  if (r >= *a.rows_used) return;
+  const bool row_ok = r < *a.rows_used;
   const int F = a.F;
   const float ts = (SC == MGQ_TENSOR_F32) ? a.tensor_scale[0] : 1.0f;
   uint32_t tam = 0;
-  for (int c0 = 0; c0 < F; c0 += 1024) {
+  for (int c0 = 0; row_ok && c0 < F; c0 += 1024) {
     const int c = c0 + 32 * lane;
     const bool act = c < F;
     float h[32];
@@ -69,10 +84,7 @@ __global__ void __launch_bounds__(256) swiglu_quant_kernel(SwigluArgs a) {
       if (a.h_out) store_bf16x32(a.h_out + r * F + c, h);
     }
   }
-  if (SC == MGQ_TENSOR_F32 && a.amax_out) {
-    tam = warp_max_u32(tam);
-    if (lane == 0) atomic_max_nonneg(a.amax_out, __uint_as_float(tam));
-  }
+  if (SC == MGQ_TENSOR_F32 && a.amax_out) cta_amax_atomic(tam, a.amax_out);
 }
 
 // ---- dSwiGLU + quantise: warp per row ---------------------------------------
@@ -95,11 +107,11 @@ __global__ void __launch_bounds__(256) dswiglu_quant_kernel(DswigluArgs a) {
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
   const int64_t r = (int64_t)blockIdx.x * kWarps + warp;
-  if (r >= *a.rows_used) return;
+  const bool row_ok = r < *a.rows_used;
   const int F = a.F;
   const float ts = (SC == MGQ_TENSOR_F32) ? a.tensor_scale[0] : 1.0f;
   uint32_t tam = 0;
-  for (int c0 = 0; c0 < F; c0 += 1024) {
+  for (int c0 = 0; row_ok && c0 < F; c0 += 1024) {
     const int c = c0 + 32 * lane;
     const bool act = c < F;
     float dg[32], du[32];
@@ -132,41 +144,71 @@ __global__ void __launch_bounds__(256) dswiglu_quant_kernel(DswigluArgs a) {
       }
     }
   }
-  if (SC == MGQ_TENSOR_F32 && a.amax_out) {
-    tam = warp_max_u32(tam);
-    if (lane == 0) atomic_max_nonneg(a.amax_out, __uint_as_float(tam));
-  }
+  if (SC == MGQ_TENSOR_F32 && a.amax_out) cta_amax_atomic(tam, a.amax_out);
 }
 
 // ---- combine: out[t] = sum_j w_j * y[row(t, j)] (w = probs, or 1) -----------
+// KMAX: the largest k the instance serves (2 or 8)
+template <int KMAX>
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ rim,
                                                       const float* __restrict__ probs, int T, int k, int H,
                                                       uint16_t* __restrict__ out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarps + warp;
   if (t >= T) return;
-  int rows[8];
-  float w[8];
+  int rows[KMAX];
+  float w[KMAX];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
+  for (int j = 0; j < KMAX; ++j) {
     rows[j] = j < k ? rim[(int64_t)t * k + j] : -1;
     w[j] = (j < k && probs) ? probs[(int64_t)t * k + j] : 1.0f;
   }
-  for (int c = lane * 8; c < H; c += 256) {
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  // four 256-element column blocks per iteration, rows in pairs: every lane
+  // keeps 8 independent 16-byte loads in flight
+  for (int c0 = 0; c0 < H; c0 += 1024) {
+    float acc[4][8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (j >= k) break;
-      if (rows[j] < 0) continue;
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(y + (int64_t)rows[j] * H + c));
-      acc[0] = fmaf(w[j], bf16_lo(v.x), acc[0]); acc[1] = fmaf(w[j], bf16_hi(v.x), acc[1]);
-      acc[2] = fmaf(w[j], bf16_lo(v.y), acc[2]); acc[3] = fmaf(w[j], bf16_hi(v.y), acc[3]);
-      acc[4] = fmaf(w[j], bf16_lo(v.z), acc[4]); acc[5] = fmaf(w[j], bf16_hi(v.z), acc[5]);
-      acc[6] = fmaf(w[j], bf16_lo(v.w), acc[6]); acc[7] = fmaf(w[j], bf16_hi(v.w), acc[7]);
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[q][i] = 0.0f;
+#pragma unroll
+    for (int j0 = 0; j0 < KMAX; j0 += 2) {
+      if (j0 >= k) break;
+      uint4 v[2][4];
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const int j = j0 + jj;
+        const int r = j < k ? rows[j] : -1;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int c = c0 + q * 256 + lane * 8;
+          v[jj][q] = (r >= 0 && c < H) ? __ldg(reinterpret_cast<const uint4*>(y + (int64_t)r * H + c))
+                                       : make_uint4(0, 0, 0, 0);
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const int j = j0 + jj;
+        if (j >= k || rows[j] < 0) continue;    // a missing row adds nothing (not even -0.0)
+        const float wj = w[j];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 u = v[jj][q];
+          acc[q][0] = fmaf(wj, bf16_lo(u.x), acc[q][0]); acc[q][1] = fmaf(wj, bf16_hi(u.x), acc[q][1]);
+          acc[q][2] = fmaf(wj, bf16_lo(u.y), acc[q][2]); acc[q][3] = fmaf(wj, bf16_hi(u.y), acc[q][3]);
+          acc[q][4] = fmaf(wj, bf16_lo(u.z), acc[q][4]); acc[q][5] = fmaf(wj, bf16_hi(u.z), acc[q][5]);
+          acc[q][6] = fmaf(wj, bf16_lo(u.w), acc[q][6]); acc[q][7] = fmaf(wj, bf16_hi(u.w), acc[q][7]);
+        }
+      }
     }
-    *reinterpret_cast<uint4*>(out + (int64_t)t * H + c) =
-        make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
-                   pack_bf16x2(acc[6], acc[7]));
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int c = c0 + q * 256 + lane * 8;
+      if (c < H)
+        *reinterpret_cast<uint4*>(out + (int64_t)t * H + c) =
+            make_uint4(pack_bf16x2(acc[q][0], acc[q][1]), pack_bf16x2(acc[q][2], acc[q][3]),
+                       pack_bf16x2(acc[q][4], acc[q][5]), pack_bf16x2(acc[q][6], acc[q][7]));
+    }
   }
 }
 
@@ -189,17 +231,28 @@ struct UnpermBwdArgs {
   int token_blocks;
 };
 
+// One warp per routing entry (t, j): row r = row_id_map[t, j] receives the
+// codes of probs[t, j] * dout[t] and dprobs[t, j] = <dout[t], Y[r]>. Lane l
+// covers elements [32 l, 32 l + 32) of each 1024-element chunk; the loads of
+// the next chunk are issued before the current one is processed, so every
+// warp keeps two chunks of dout and Y in flight.
 template <int SC, int DT>
 __global__ void __launch_bounds__(256) unpermute_bwd_kernel(UnpermBwdArgs a) {
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
   const int H = a.H;
   if ((int)blockIdx.x >= a.token_blocks) {
-    // filler rows of expert e: zero codes and scales
+    // filler rows of expert e (the tail of its group, where src_row < 0;
+    // found by binary search): zero codes and scales
     const int e = blockIdx.x - a.token_blocks;
     if (e >= a.E) return;
-    for (int64_t r = a.offsets[e] + warp; r < a.offsets[e + 1]; r += kWarps) {
-      if (a.src_row[r] >= 0) continue;
+    int64_t lo = a.offsets[e], hi = a.offsets[e + 1];
+    while (lo < hi) {
+      const int64_t mid = (lo + hi) >> 1;
+      if (a.src_row[mid] >= 0) lo = mid + 1;
+      else hi = mid;
+    }
+    for (int64_t r = lo + warp; r < a.offsets[e + 1]; r += kWarps) {
       for (int c = lane * 16; c < H; c += 512) *reinterpret_cast<uint4*>(a.codes + r * H + c) = make_uint4(0, 0, 0, 0);
       if (SC == MGQ_MX32_E8M0)
         for (int b4 = lane; b4 < H / 128; b4 += 32)
@@ -207,60 +260,71 @@ __global__ void __launch_bounds__(256) unpermute_bwd_kernel(UnpermBwdArgs a) {
     }
     return;
   }
-  const int t = blockIdx.x * kWarps + warp;
-  if (t >= a.T) return;
-  const float ts = (SC == MGQ_TENSOR_F32) ? a.tensor_scale[0] : 1.0f;
-  int rows[8];
-  float pr[8], dp[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    rows[j] = j < a.k ? a.rim[(int64_t)t * a.k + j] : -1;
-    pr[j] = j < a.k ? a.probs[(int64_t)t * a.k + j] : 0.0f;
-    dp[j] = 0.0f;
-  }
+  const int64_t g = (int64_t)blockIdx.x * kWarps + warp;     // routing entry t * k + j
+  const bool valid = g < (int64_t)a.T * a.k;
+  const int r = valid ? a.rim[g] : -1;
   uint32_t tam = 0;
-  for (int c0 = 0; c0 < H; c0 += 1024) {
-    const int c = c0 + 32 * lane;
-    const bool act = c < H;
-    float d[32];
-    if (act) {
-      load_bf16x32(a.dout + (int64_t)t * H + c, d);
-    } else {
+  if (r >= 0) {
+    const float ts = (SC == MGQ_TENSOR_F32) ? a.tensor_scale[0] : 1.0f;
+    const float pr = a.probs[g];
+    const uint16_t* drow = a.dout + (g / a.k) * H;
+    const uint16_t* yrow = a.y + (int64_t)r * H;
+    float dp = 0.0f;
+    auto load = [&](int c0, uint4 (&d)[4], uint4 (&y)[4]) {
+      const int c = c0 + 32 * (int)lane;
+      if (c < H) {
+        const uint4* pd = reinterpret_cast<const uint4*>(drow + c);
+        const uint4* py = reinterpret_cast<const uint4*>(yrow + c);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) d[i] = 0.0f;
-    }
-#pragma unroll 1
-    for (int j = 0; j < a.k; ++j) {
+        for (int q = 0; q < 4; ++q) {
+          d[q] = __ldg(pd + q);
+          y[q] = __ldg(py + q);
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) d[q] = y[q] = make_uint4(0, 0, 0, 0);
+      }
+    };
+    auto process = [&](int c0, const uint4 (&d)[4], const uint4 (&y)[4]) {
+      const int c = c0 + 32 * (int)lane;
       float v[32];
+      float s = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(pr[j], d[i]);
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t dw[4] = {d[q].x, d[q].y, d[q].z, d[q].w};
+        const uint32_t yw[4] = {y[q].x, y[q].y, y[q].z, y[q].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float d0 = bf16_lo(dw[i]), d1 = bf16_hi(dw[i]);
+          s = fmaf(d0, bf16_lo(yw[i]), s);
+          s = fmaf(d1, bf16_hi(yw[i]), s);
+          v[8 * q + 2 * i] = __fmul_rn(pr, d0);
+          v[8 * q + 2 * i + 1] = __fmul_rn(pr, d1);
+        }
+      }
+      dp += s;
       const uint32_t am = absmax_bits_f32(v, 32);
       tam = max(tam, am);
       Block32 o;
       quantize32<SC, DT>(v, am, ts, a.rceil != 0, o);
-      if (act && rows[j] >= 0) {
-        store32<SC>(o, a.codes, a.scales, rows[j], c, H, a.R_cap, lane);
-        float yv[32];
-        load_bf16x32(a.y + (int64_t)rows[j] * H + c, yv);
-        float s = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s = fmaf(d[i], yv[i], s);
-        dp[j] += s;
-      }
+      if (c < H) store32<SC>(o, a.codes, a.scales, r, c, H, a.R_cap, lane);
+    };
+    uint4 d0[4], y0[4], d1[4], y1[4];
+    load(0, d0, y0);
+    for (int c0 = 0; c0 < H; c0 += 2048) {
+      load(c0 + 1024, d1, y1);
+      process(c0, d0, y0);
+      if (c0 + 1024 >= H) break;
+      load(c0 + 2048, d0, y0);
+      process(c0 + 1024, d1, y1);
     }
-  }
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    if (j >= a.k) break;
-    float s = dp[j];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
-    if (lane == 0) a.dprobs[(int64_t)t * a.k + j] = s;
+    for (int o = 16; o > 0; o >>= 1) dp += __shfl_xor_sync(0xFFFFFFFFu, dp, o);
+    if (lane == 0) a.dprobs[g] = dp;
+  } else if (valid && lane == 0) {
+    a.dprobs[g] = 0.0f;
   }
-  if (SC == MGQ_TENSOR_F32 && a.amax_out) {
-    tam = warp_max_u32(tam);
-    if (lane == 0) atomic_max_nonneg(a.amax_out, __uint_as_float(tam));
-  }
+  if (SC == MGQ_TENSOR_F32 && a.amax_out) cta_amax_atomic(tam, a.amax_out);
 }
 
 // ---- row-wise quantisation of [G*M, K] (grouped weights) ---------------------
@@ -278,12 +342,12 @@ template <int SC, int DT>
 __global__ void __launch_bounds__(256) quant_rows_kernel(QuantRowsArgs a) {
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
+  // a CTA's 8 rows lie in one group (M is a multiple of 128)
   const int64_t r = (int64_t)blockIdx.x * kWarps + warp;
-  if (r >= a.rows) return;
-  const int64_t g = r / a.M;
+  const int64_t g = ((int64_t)blockIdx.x * kWarps) / a.M;
   const float ts = (SC == MGQ_TENSOR_F32) ? a.tensor_scale[g] : 1.0f;
   uint32_t tam = 0;
-  for (int64_t c0 = 0; c0 < a.K; c0 += 1024) {
+  for (int64_t c0 = 0; r < a.rows && c0 < a.K; c0 += 1024) {
     const int64_t c = c0 + 32 * lane;
     const bool act = c < a.K;
     float v[32];
@@ -299,10 +363,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantRowsArgs a) {
     quantize32<SC, DT>(v, am, ts, a.rceil != 0, o);
     if (act) store32<SC>(o, a.codes, a.scales, r, c, a.K, a.rows, lane);
   }
-  if (SC == MGQ_TENSOR_F32 && a.amax_out) {
-    tam = warp_max_u32(tam);
-    if (lane == 0) atomic_max_nonneg(a.amax_out + g, __uint_as_float(tam));
-  }
+  if (SC == MGQ_TENSOR_F32 && a.amax_out) cta_amax_atomic(tam, a.amax_out + g);
 }
 
 
@@ -433,15 +494,25 @@ __global__ void __launch_bounds__(256) swiglu_h_kernel(const uint16_t* __restric
 }
 
 // ---- delayed scaling ------------------------------------------------------------
+// One warp per role: the lanes read the ring coalesced (entry h already
+// replaced by this step's amax) and reduce the max with shuffles; fmaxf drops
+// NaN entries in any order, so the result equals a serial scan.
 __global__ void amax_history_kernel(float* hist, int32_t* head, float* amax, float* scale, int n, int L, float fmax) {
   const int h = *head;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  for (int i = warp; i < n; i += nwarps) {
     float* ring = hist + (int64_t)i * L;
-    ring[h] = amax[i];
+    const float a = amax[i];
     float m = 0.0f;
-    for (int j = 0; j < L; ++j) m = fmaxf(m, ring[j]);
-    if (m > 0.0f && isfinite(m)) scale[i] = __fdiv_rn(fmax, m);
-    amax[i] = 0.0f;
+    for (int j = lane; j < L; j += 32) m = fmaxf(m, j == h ? a : ring[j]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    __syncwarp();
+    if (lane == 0) {
+      ring[h] = a;
+      if (m > 0.0f && isfinite(m)) scale[i] = __fdiv_rn(fmax, m);
+      amax[i] = 0.0f;
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) *head = (h + 1) % L;
@@ -558,7 +629,7 @@ int mgq_moe_unpermute(const void* y_bf16, const int32_t* row_id_map, const float
   MGQ_CHECK_ARG(T == 0 || (y_bf16 && row_id_map && probs && out_bf16));
   MGQ_CHECK_ARG(aligned16(y_bf16) && aligned16(out_bf16));
   if (T == 0) return MGQ_OK;
-  combine_kernel<<<(T + kWarps - 1) / kWarps, 256, 0, as_stream(stream)>>>(
+  (k <= 2 ? combine_kernel<2> : combine_kernel<8>)<<<(T + kWarps - 1) / kWarps, 256, 0, as_stream(stream)>>>(
       static_cast<const uint16_t*>(y_bf16), row_id_map, probs, T, k, H, static_cast<uint16_t*>(out_bf16));
   MGQ_LAUNCH_CHECK();
   return MGQ_OK;
@@ -570,7 +641,7 @@ int mgq_moe_permute_bwd(const void* da_bf16, const int32_t* row_id_map, int T, i
   MGQ_CHECK_ARG(T == 0 || (da_bf16 && row_id_map && dx_bf16));
   MGQ_CHECK_ARG(aligned16(da_bf16) && aligned16(dx_bf16));
   if (T == 0) return MGQ_OK;
-  combine_kernel<<<(T + kWarps - 1) / kWarps, 256, 0, as_stream(stream)>>>(
+  (k <= 2 ? combine_kernel<2> : combine_kernel<8>)<<<(T + kWarps - 1) / kWarps, 256, 0, as_stream(stream)>>>(
       static_cast<const uint16_t*>(da_bf16), row_id_map, nullptr, T, k, H, static_cast<uint16_t*>(dx_bf16));
   MGQ_LAUNCH_CHECK();
   return MGQ_OK;
@@ -600,7 +671,7 @@ int mgq_moe_unpermute_bwd(const void* dout_bf16, const void* y_bf16, const int32
   a.amax_out = q->amax_out;
   a.dprobs = dprobs;
   a.rceil = q->e8m0_mode == MGQ_E8M0_RCEIL;
-  a.token_blocks = (T + kWarps - 1) / kWarps;
+  a.token_blocks = (int)(((int64_t)T * k + kWarps - 1) / kWarps);
   const unsigned grid = (unsigned)(a.token_blocks + E);
   if (q->col.data && q->scaling != MGQ_TENSOR_F32 && q->scaling != MGQ_MX32_E8M0) return MGQ_ERR_UNSUPPORTED;
   MGQ_DISPATCH_Q(q, unpermute_bwd_kernel, grid, a);
@@ -663,7 +734,7 @@ int mgq_block_quantize(const void* x_bf16, int64_t G, int64_t M, int64_t K, cons
 int mgq_amax_history_update(float* history, int32_t* head, float* amax, float* scale, int n, int L, float fmax,
                             void* stream) {
   MGQ_CHECK_ARG(history && head && amax && scale && n >= 1 && L >= 1 && fmax > 0.0f);
-  amax_history_kernel<<<1, 256, 0, as_stream(stream)>>>(history, head, amax, scale, n, L, fmax);
+  amax_history_kernel<<<1, 1024, 0, as_stream(stream)>>>(history, head, amax, scale, n, L, fmax);
   MGQ_LAUNCH_CHECK();
   return MGQ_OK;
 }

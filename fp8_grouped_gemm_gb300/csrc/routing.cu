@@ -19,112 +19,133 @@ constexpr int kChunk = 1024;        // routing entries per chunk
 constexpr int kRouteThreads = 256;
 constexpr int kMaxExperts = 1024;
 
-// ---- routing pass 1: per-chunk expert histogram -------------------------------
-__global__ void route_count_kernel(const int32_t* __restrict__ idx, int64_t n, int E, int32_t* __restrict__ cnt,
-                                   int* err) {
-  extern __shared__ int s_cnt[];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
-  __syncthreads();
-  int64_t base = (int64_t)blockIdx.x * kChunk;
-  for (int i = threadIdx.x; i < kChunk; i += blockDim.x) {
-    int64_t g = base + i;
-    if (g < n) {
-      int e = idx[g];
-      if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
-      else report(err, MGQ_ERR_DEVICE_INDEX);
-    }
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[(int64_t)blockIdx.x * E + e] = s_cnt[e];
-}
-
-// ---- routing pass 2: totals, padded exclusive scan over experts, and the
-// first destination row of every (chunk, expert) pair (in place in cnt) ----
-__global__ void route_scan_kernel(int32_t* __restrict__ cnt, int nchunks, int E, int align,
-                                  int32_t* __restrict__ offsets, int32_t* __restrict__ counts,
-                                  int32_t* __restrict__ src_row) {
-  __shared__ int s_pad[kMaxExperts];
-  __shared__ int s_tot[kMaxExperts];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int tot = 0;
-    for (int c = 0; c < nchunks; ++c) tot += cnt[(int64_t)c * E + e];
-    s_tot[e] = tot;
-    s_pad[e] = (tot + align - 1) / align * align;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {   // E <= 1024: a serial scan is a few microseconds at most
-    int run = 0;
-    for (int e = 0; e < E; ++e) {
-      int p = s_pad[e];
-      s_pad[e] = run;
-      run += p;
-    }
-    offsets[E] = run;
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    offsets[e] = s_pad[e];
-    counts[e] = s_tot[e];
-    int run = s_pad[e];
-    for (int c = 0; c < nchunks; ++c) {
-      int v = cnt[(int64_t)c * E + e];
-      cnt[(int64_t)c * E + e] = run;
-      run += v;
-    }
-  }
-  __syncthreads();
-  // filler rows of every group
-  for (int e = 0; e < E; ++e) {
-    int lo = s_pad[e] + s_tot[e];
-    int hi = (e + 1 < E) ? s_pad[e + 1] : offsets[E];
-    for (int r = lo + threadIdx.x; r < hi; r += blockDim.x) src_row[r] = -1;
-  }
-}
-
-// ---- routing pass 3: stable rank inside each chunk --------------------------
+// ---- routing pass 1: per-chunk histogram and stable rank inside the chunk ----
 // Entries of a chunk are taken in order, 256 per round; within a warp,
 // __match_any_sync finds the lanes with the same expert and the rank is the
 // number of such lanes before this one; warps and rounds before it add their
-// counts.
-__global__ void route_rank_kernel(const int32_t* __restrict__ idx, int64_t n, int E,
-                                  const int32_t* __restrict__ base, int32_t* __restrict__ row_id_map,
-                                  int32_t* __restrict__ src_row) {
+// counts. The rank inside the chunk is parked in row_id_map (the permute
+// kernel adds the chunk's base row); the chunk's counts go to cnt[chunk][e].
+__global__ void route_count_rank_kernel(const int32_t* __restrict__ idx, int64_t n, int E,
+                                        int32_t* __restrict__ cnt, int32_t* __restrict__ row_id_map, int* err) {
   extern __shared__ int smem[];
-  int* s_run = smem;                 // [E] rows already given in this chunk
+  int* s_run = smem;                 // [E] entries of this chunk already ranked
   int* s_w = smem + E;               // [8][E] per-warp counts of this round
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_run[e] = 0;
   const int64_t cbase = (int64_t)blockIdx.x * kChunk;
-  const int32_t* cb = base + (int64_t)blockIdx.x * E;
   for (int round = 0; round < kChunk / kRouteThreads; ++round) {
     for (int i = threadIdx.x; i < 8 * E; i += blockDim.x) s_w[i] = 0;
     __syncthreads();
-    int64_t g = cbase + round * kRouteThreads + threadIdx.x;
+    const int64_t g = cbase + round * kRouteThreads + threadIdx.x;
     int key = -1;
     if (g < n) {
       key = idx[g];
-      if (key < 0 || key >= E) key = -1;
+      if (key < 0 || key >= E) {
+        report(err, MGQ_ERR_DEVICE_INDEX);
+        key = -1;
+      }
     }
-    unsigned peers = __match_any_sync(0xFFFFFFFFu, key);
-    int rank = __popc(peers & ((1u << lane) - 1u));
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, key);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
     if (key >= 0 && rank == 0) s_w[warp * E + key] = __popc(peers);
     __syncthreads();
     if (key >= 0) {
-      int r = cb[key] + s_run[key] + rank;
+      int r = s_run[key] + rank;
       for (int w = 0; w < warp; ++w) r += s_w[w * E + key];
       row_id_map[g] = r;
-      src_row[r] = (int32_t)g;
     } else if (g < n) {
       row_id_map[g] = -1;
     }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-      int s = 0;
-      for (int w = 0; w < 8; ++w) s += s_w[w * E + e];
-      s_run[e] += s;
+      int sum = 0;
+      for (int w = 0; w < 8; ++w) sum += s_w[w * E + e];
+      s_run[e] += sum;
     }
     __syncthreads();
   }
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[(int64_t)blockIdx.x * E + e] = s_run[e];
+}
+
+// inclusive warp scan
+__device__ __forceinline__ int warp_incl_scan(int v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xFFFFFFFFu, v, o);
+    if (lane >= o) v += u;
+  }
+  return v;
+}
+
+// ---- routing pass 2 (one CTA of 1024 threads): totals, padded exclusive
+// scan over experts, and the first destination row of every (chunk, expert)
+// pair (in place in cnt); filler rows of every group get src_row -1 ----------
+__global__ void __launch_bounds__(1024) route_scan_kernel(int32_t* __restrict__ cnt, int nchunks, int E, int align,
+                                                          int32_t* __restrict__ offsets, int32_t* __restrict__ counts,
+                                                          int32_t* __restrict__ src_row) {
+  __shared__ int s_tot[kMaxExperts];
+  __shared__ int s_off[kMaxExperts + 1];
+  __shared__ int s_wsum[32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // expert totals: one warp per expert, lanes over chunks
+  for (int e = warp; e < E; e += 32) {
+    int t = 0;
+    for (int c = lane; c < nchunks; c += 32) t += cnt[(int64_t)c * E + e];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+    if (lane == 0) s_tot[e] = t;
+  }
+  __syncthreads();
+  // exclusive scan of the padded totals (E <= 1024: one per thread)
+  const int e0 = threadIdx.x;
+  const int pad = e0 < E ? (s_tot[e0] + align - 1) / align * align : 0;
+  const int incl = warp_incl_scan(pad, lane);
+  if (lane == 31) s_wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int v = warp_incl_scan(s_wsum[lane], lane);
+    s_wsum[lane] = v;
+  }
+  __syncthreads();
+  const int excl = incl - pad + (warp > 0 ? s_wsum[warp - 1] : 0);
+  if (e0 < E) {
+    s_off[e0] = excl;
+    offsets[e0] = excl;
+    counts[e0] = s_tot[e0];
+  }
+  if (e0 == 0) {
+    s_off[E] = s_wsum[31];
+    offsets[E] = s_wsum[31];
+  }
+  __syncthreads();
+  // per-(chunk, expert) base rows: one warp per expert, exclusive scan over chunks
+  for (int e = warp; e < E; e += 32) {
+    int run = s_off[e];
+    for (int c0 = 0; c0 < nchunks; c0 += 32) {
+      const int c = c0 + lane;
+      const int v = c < nchunks ? cnt[(int64_t)c * E + e] : 0;
+      const int inc = warp_incl_scan(v, lane);
+      if (c < nchunks) cnt[(int64_t)c * E + e] = run + inc - v;
+      run += __shfl_sync(0xFFFFFFFFu, inc, 31);
+    }
+  }
+  // filler rows of every group
+  for (int e = warp; e < E; e += 32)
+    for (int r = s_off[e] + s_tot[e] + lane; r < s_off[e + 1]; r += 32) src_row[r] = -1;
+}
+
+// Final destination row of routing entry g (lane-level): the chunk's base row
+// for the entry's expert plus the entry's rank inside the chunk; written back
+// to row_id_map with the inverse map src_row. -1 for an invalid entry.
+__device__ __forceinline__ int resolve_row(const int32_t* __restrict__ idx, int32_t* row_id_map,
+                                           const int32_t* __restrict__ base, int32_t* src_row, int E, int64_t g) {
+  const int local = row_id_map[g];
+  if (local < 0) return -1;
+  const int e = idx[g];
+  const int r = base[(g / kChunk) * E + e] + local;
+  row_id_map[g] = r;
+  src_row[r] = (int32_t)g;
+  return r;
 }
 
 // ---- fused permute + quantise ---------------------------------------------------
@@ -136,7 +157,6 @@ __global__ void route_rank_kernel(const int32_t* __restrict__ idx, int64_t n, in
 struct PermuteArgs {
   const uint16_t* x;
   int T, H, k, E;
-  const int32_t* row_id_map;
   const int32_t* offsets;
   const int32_t* counts;
   uint8_t* codes;          // [R_cap, H]
@@ -149,7 +169,19 @@ struct PermuteArgs {
   int e8m0_rceil;
   int token_blocks;        // CTAs that process tokens; the rest fill padding
   int* err;
+  const int32_t* idx;      // [T, k] expert ids
+  const int32_t* base;     // [chunks][E] first row of each (chunk, expert)
+  int32_t* rim;            // row_id_map: rank inside the chunk in, final row out
+  int32_t* src_row;
 };
+
+// Every lane gets the k destination rows of token t (lane j resolves entry j).
+__device__ __forceinline__ void token_rows(const PermuteArgs& a, int t, uint32_t lane, int (&dest)[8]) {
+  int mine = -1;
+  if ((int)lane < a.k) mine = resolve_row(a.idx, a.rim, a.base, a.src_row, a.E, (int64_t)t * a.k + lane);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) dest[j] = __shfl_sync(0xFFFFFFFFu, mine, j);
+}
 
 __device__ __forceinline__ void load_block32(const uint16_t* src, uint32_t (&w)[16]) {
   const uint4* p = reinterpret_cast<const uint4*>(src);
@@ -188,21 +220,30 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(PermuteArgs a) {
   }
   const int t = blockIdx.x * 8 + warp;
   if (t >= a.T) return;
-  int dest[8];
+  // the first chunk's loads go out before the destination rows are resolved,
+  // and every chunk's loads before the previous chunk is processed
+  auto load_chunk = [&](int c0, uint32_t (&w)[16]) {
+    const int c = c0 + lane * 32;
+    if (c < H) {
+      load_block32(a.x + (int64_t)t * H + c, w);
+    } else {
 #pragma unroll
-  for (int j = 0; j < 8; ++j) dest[j] = (j < a.k) ? a.row_id_map[(int64_t)t * a.k + j] : -1;
+      for (int i = 0; i < 16; ++i) w[i] = 0;
+    }
+  };
+  uint32_t wnext[16];
+  load_chunk(0, wnext);
+  int dest[8];
+  token_rows(a, t, lane, dest);
   const float ts = (SC == MGQ_TENSOR_F32) ? a.tensor_scale[0] : 1.0f;
   uint32_t tamax = 0;   // per-tensor amax (bf16 bits in the high half)
   for (int c0 = 0; c0 < H; c0 += 1024) {
     const int c = c0 + lane * 32;
     const bool active = c < H;       // every lane stays in the loop (shuffles below)
     uint32_t w[16];
-    if (active) {
-      load_block32(a.x + (int64_t)t * H + c, w);
-    } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) w[i] = 0;
-    }
+    for (int i = 0; i < 16; ++i) w[i] = wnext[i];
+    if (c0 + 1024 < H) load_chunk(c0 + 1024, wnext);
     uint32_t am2 = 0;
 #pragma unroll
     for (int i = 0; i < 16; ++i) am2 = absmax_bf16x2(am2, w[i]);
@@ -293,8 +334,7 @@ __global__ void __launch_bounds__(256) permute_quant_nv_kernel(PermuteArgs a) {
   const float s_g = nv_global_scale(*a.amax_out);
   if (t == 0 && lane == 0) *a.s_out = s_g;
   int dest[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) dest[j] = (j < a.k) ? a.row_id_map[(int64_t)t * a.k + j] : -1;
+  token_rows(a, t, lane, dest);
   for (int c0 = 0; c0 < H; c0 += 1024) {
     const int c = c0 + lane * 32;
     const bool act = c < H;
@@ -410,21 +450,19 @@ int mgq_moe_permute(const void* x_bf16, int T, int H, const int32_t* topk_idx, i
   cudaStream_t s = as_stream(stream);
   int64_t nchunks = (n + kChunk - 1) / kChunk;
   int32_t* cnt = static_cast<int32_t*>(workspace);
+  // two routing launches; the permute kernel below resolves the final rows
   if (nchunks > 0) {
-    route_count_kernel<<<(unsigned)nchunks, kRouteThreads, E * sizeof(int), s>>>(topk_idx, n, E, cnt, err);
+    route_count_rank_kernel<<<(unsigned)nchunks, kRouteThreads, 9 * E * sizeof(int), s>>>(topk_idx, n, E, cnt,
+                                                                                           row_id_map, err);
     MGQ_LAUNCH_CHECK();
   }
   route_scan_kernel<<<1, 1024, 0, s>>>(cnt, (int)nchunks, E, align, offsets, counts, src_row);
   MGQ_LAUNCH_CHECK();
-  if (nchunks > 0) {
-    route_rank_kernel<<<(unsigned)nchunks, kRouteThreads, 9 * E * sizeof(int), s>>>(topk_idx, n, E, cnt,
-                                                                                     row_id_map, src_row);
-    MGQ_LAUNCH_CHECK();
-  }
   PermuteArgs a;
   a.x = static_cast<const uint16_t*>(x_bf16);
   a.T = T; a.H = H; a.k = k; a.E = E;
-  a.row_id_map = row_id_map; a.offsets = offsets; a.counts = counts;
+  a.offsets = offsets; a.counts = counts;
+  a.idx = topk_idx; a.base = cnt; a.rim = row_id_map; a.src_row = src_row;
   a.codes = q ? static_cast<uint8_t*>(q->row.data) : nullptr;
   a.scales = q ? static_cast<uint8_t*>(q->row.scale) : nullptr;
   a.out_bf16 = static_cast<uint16_t*>(out_bf16);

@@ -307,7 +307,7 @@ class ExpertLayer:
     def gpu_launches_per_step(self) -> int:
         """Kernels this object launches per forward (+ backward) step."""
         E = self.w.E
-        n_route = 3 if self.w.T * self.w.k > 0 else 1
+        n_route = 2 if self.w.T * self.w.k > 0 else 1
         fwd = n_route + 1 + 1 + 1 + 1 + 1               # route, permute-quant, gemm1, swiglu, gemm2, unpermute
         if self.nv:
             return fwd + 2 + 4                          # + amax passes (x, h); weights: 2 x (amax + rows)
