@@ -237,7 +237,7 @@ struct UnpermBwdArgs {
 // the next chunk are issued before the current one is processed, so every
 // warp keeps two chunks of dout and Y in flight.
 template <int SC, int DT>
-__global__ void __launch_bounds__(256) unpermute_bwd_kernel(UnpermBwdArgs a) {
+__global__ void __launch_bounds__(256, SC == MGQ_TENSOR_F32 ? 3 : 2) unpermute_bwd_kernel(UnpermBwdArgs a) {
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
   const int H = a.H;

@@ -537,9 +537,21 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
 //     arms with the pair's byte count); the MMA commit is multicast to both
 //     CTAs' `empty` and `tmem_full` barriers; both CTAs' epilogue warps arrive
 //     on CTA 0's `tmem_empty`.
+//   - MX (E8M0 block scales): each CTA also loads, per stage, the 512-byte
+//     scale chunk of its own 128 rows of A and the two chunks of all 256 rows
+//     of B (the scales of B are needed whole in both CTAs); CTA 0 copies them
+//     into both CTAs' tensor memory with pair scale copies. Tensor memory then
+//     has no room for a second accumulator: the epilogue moves it to registers
+//     and releases it before storing.
 constexpr int PSTAGES = 6;
 constexpr uint32_t kPairTile = 128 * 128;                      // bytes of one A or B half tile
-constexpr size_t kPairSmem = 1024 + PSTAGES * 2 * kPairTile + 8 * kStageOut + 256 + (2 * kMaxE + 16) * 4;
+constexpr uint32_t kPairSfa = 512, kPairSfb = 1024;            // MX scale bytes per stage
+__host__ __device__ constexpr uint32_t pair_sf_bytes(int kind) { return kind == kKindMX ? kPairSfa + kPairSfb : 0u; }
+__host__ __device__ constexpr size_t pair_smem(int kind) {
+  return 1024 + PSTAGES * (2 * kPairTile + pair_sf_bytes(kind)) + 8 * kStageOut + 256 + (2 * kMaxE + 16) * 4;
+}
+// tensor-memory columns: accumulator(s), then the MX scale slots of every stage
+constexpr uint32_t kPairSfaCol = 256, kPairSfbCol = kPairSfaCol + PSTAGES * 4;
 
 template <int MODE>
 __device__ __forceinline__ bool get_pair_tile(const int32_t* s_off, const int32_t* s_cum, int E, const GemmParams& p,
@@ -580,17 +592,22 @@ __device__ __forceinline__ bool get_pair_tile(const int32_t* s_off, const int32_
   return true;
 }
 
-template <int MODE>
+template <int MODE, int KIND>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                             const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
+                             const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmSFA,
+                             const __grid_constant__ CUtensorMap tmSFB, const GemmParams p) {
+  constexpr bool MX = KIND == kKindMX;
+  constexpr int kAccBufs = MX ? 1 : 2;             // MX: scale slots leave room for one accumulator
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   uint8_t* sA = smem;
   uint8_t* sB = sA + PSTAGES * kPairTile;
   uint8_t* sOut = sB + PSTAGES * kPairTile;        // [8 warps][32 rows][64 bytes] epilogue staging
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + 8 * kStageOut);
+  uint8_t* sSFA = sOut + 8 * kStageOut;            // MX: [stage] 512-byte chunk of this CTA's A rows
+  uint8_t* sSFB = sSFA + PSTAGES * kPairSfa;       // MX: [stage] two chunks of all B rows
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + 8 * kStageOut + PSTAGES * pair_sf_bytes(KIND));
   uint64_t* full = bars;
   uint64_t* empty = bars + PSTAGES;
   uint64_t* tmem_full = bars + 2 * PSTAGES;        // [2]
@@ -625,6 +642,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB);
+    if (MX) {
+      ptx::prefetch_tmap(&tmSFA);
+      ptx::prefetch_tmap(&tmSFB);
+    }
   }
   if (warp == 1) {
     ptx::tmem_alloc_pair(s_tmem, kTmemCols);
@@ -666,7 +687,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           *s_abort = 1;
           break;
         }
-        if (leader) ptx::mbar_arrive_expect_tx(&full[st], 4 * kPairTile);   // both CTAs' A and B halves
+        // both CTAs' A and B halves (and MX scale chunks)
+        if (leader) ptx::mbar_arrive_expect_tx(&full[st], 4 * kPairTile + 2 * pair_sf_bytes(KIND));
         const uint32_t bar0 = ptx::mapa_shared(ptx::smem_u32(&full[st]), 0);
         const int32_t kx = (int32_t)(tl.kx0 + (int64_t)s * BK);
         // K-major: box (128 contraction bytes, 128 rows); MN-major: box (128
@@ -679,6 +701,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 (int32_t)((MODE == kModeRows ? (int64_t)tl.e * p.K : 0) + kx));
         else
           ptx::tma_load_2d_pair(sB + st * kPairTile, &tmB, bar0, kx, (int32_t)(tl.row_b + 128 * rank));
+        if (MX) {
+          // scale chunk (row tile, k tile) is row tile * kb4 + kx / 128 of the
+          // [chunks][128 words] view of the scales
+          const int32_t kt = kx / BK;
+          ptx::tma_load_2d_pair(sSFA + st * kPairSfa, &tmSFA, bar0, 0,
+                                (int32_t)(((tl.row_a + 128 * rank) / 128) * p.sfa_kb4 + kt));
+          ptx::tma_load_2d_pair(sSFB + st * kPairSfb, &tmSFB, bar0, 0, (int32_t)((tl.row_b / 128) * p.sfb_kb4 + kt));
+          ptx::tma_load_2d_pair(sSFB + st * kPairSfb + 512, &tmSFB, bar0, 0,
+                                (int32_t)((tl.row_b / 128 + 1) * p.sfb_kb4 + kt));
+        }
       }
       if (*s_abort) break;
     }
@@ -688,10 +720,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t it = 0, tc = 0;
     Tile tl;
     const uint32_t sA0 = ptx::smem_u32(sA), sB0 = ptx::smem_u32(sB);
+    const uint32_t sSFA0 = ptx::smem_u32(sSFA), sSFB0 = ptx::smem_u32(sSFB);
     for (int64_t t = pair; get_pair_tile<MODE>(s_off, s_cum, E, p, t, ecur, tl); t += npairs) {
       if (tl.nst == 0) continue;
       if (*s_abort) break;
-      const uint32_t a = tc & 1, aph = (tc >> 1) & 1;
+      const uint32_t a = tc % kAccBufs, aph = (tc / kAccBufs) & 1;
       if (!ptx::mbar_wait(&tmem_empty[a], aph ^ 1, p.wait_ns)) {
         report(p.err, MGQ_ERR_TIMEOUT);
         *s_abort = 1;
@@ -715,10 +748,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint64_t bd = p.b_mn ? ptx::sdesc_mnmajor_sw128(sB0 + st * kPairTile)
                                    : ptx::sdesc_kmajor_sw128(sB0 + st * kPairTile);
         const uint64_t astep = p.a_mn ? 256 : 2, bstep = p.b_mn ? 256 : 2;
+        if (MX) {
+          // this stage's scales into both CTAs' tensor memory (ordered before
+          // the MMAs below, which read them)
+          const uint32_t sfa_t = tmem + kPairSfaCol + st * 4, sfb_t = tmem + kPairSfbCol + st * 8;
+          ptx::tmem_cp_32x128b_x4_pair(sfa_t, ptx::sdesc_sf(sSFA0 + st * kPairSfa));
+          ptx::tmem_cp_32x128b_x4_pair(sfb_t, ptx::sdesc_sf(sSFB0 + st * kPairSfb));
+          ptx::tmem_cp_32x128b_x4_pair(sfb_t + 4, ptx::sdesc_sf(sSFB0 + st * kPairSfb + 512));
 #pragma unroll
-        for (int kk = 0; kk < BK / 32; ++kk)
-          ptx::mma_f8f6f4_pair(tmem + a * BN, ad + kk * astep, bd + kk * bstep, p.idesc,
-                               (s > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < BK / 32; ++kk)
+            ptx::mma_mxf8f6f4_pair(tmem + a * BN, ad + kk * astep, bd + kk * bstep,
+                                   p.idesc | ptx::idesc_sf_ids(kk, kk), sfa_t, sfb_t, (s > 0 || kk > 0) ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk)
+            ptx::mma_f8f6f4_pair(tmem + a * BN, ad + kk * astep, bd + kk * bstep, p.idesc,
+                                 (s > 0 || kk > 0) ? 1u : 0u);
+        }
         ptx::mma_commit_pair(&empty[st], 0x3);        // frees the stage in both CTAs
       }
       if (!ok) break;
@@ -752,7 +798,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      const uint32_t a = tc & 1, aph = (tc >> 1) & 1;
+      const uint32_t a = tc % kAccBufs, aph = (tc / kAccBufs) & 1;
       if (__any_sync(0xFFFFFFFFu, *s_abort != 0)) break;
       const bool got = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&tmem_full[a], aph, p.wait_ns));
       if (!got) {
@@ -771,7 +817,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) ptx::mbar_arrive_cluster(a ? empty_remote1 : empty_remote0);
       ++tc;
       if (!store) continue;    // the warp's 32 rows lie wholly inside or past the group
-      const float alpha = 1.0f / (p.sa[0] * p.sb[MODE == kModeRows ? tl.e : 0]);
+      const float alpha = MX ? 1.0f : 1.0f / (p.sa[0] * p.sb[MODE == kModeRows ? tl.e : 0]);
       epilogue_store(p, r, alpha, orow, col0, p.tma_store != 0, sOut + (warp - 2) * kStageOut, &tmO,
                      (int32_t)(tl.out_row + 128 * rank + q * 32), lane);
     }
@@ -787,19 +833,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int MODE>
-int launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const GemmParams& p,
-                     cudaStream_t s) {
-  auto kern = grouped_gemm_pair_kernel<MODE>;
+template <int MODE, int KIND>
+int launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const CUtensorMap& tsfa,
+                     const CUtensorMap& tsfb, const GemmParams& p, cudaStream_t s) {
+  auto kern = grouped_gemm_pair_kernel<MODE, KIND>;
+  constexpr size_t kSmem = pair_smem(KIND);
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPairSmem) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem) != cudaSuccess)
       return MGQ_ERR_CUDA;
     attr_set[dev] = true;
   }
-  kern<<<num_sms() / 2 * 2, kThreads, kPairSmem, s>>>(ta, tb, to, p);
+  kern<<<num_sms() / 2 * 2, kThreads, kSmem, s>>>(ta, tb, to, tsfa, tsfb, p);
   MGQ_LAUNCH_CHECK();
   return MGQ_OK;
 }
@@ -927,7 +974,7 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
                  : ptx::idesc_f8f6f4(A->dtype, B->dtype, BM, BN);
   p.err = err;
   cudaStream_t s = as_stream(stream);
-  if (kind == kKindTensor && use_pair_kernel(mode, N)) {
+  if ((kind == kKindTensor || kind == kKindMX) && use_pair_kernel(mode, N)) {
     // the pair kernel loads 128-row halves of B (K-major) or 128-column
     // halves (MN-major); MN-major operands are stored with the contraction
     // index down the rows:
@@ -954,15 +1001,27 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
     if (!ok) return MGQ_ERR_CUDA;
     p.a_mn = a_mn;
     p.b_mn = b_mn;
-    p.idesc = ptx::idesc_f8f6f4(A->dtype, B->dtype, 256, BN) | ptx::idesc_mn_major(a_mn, b_mn);
+    p.idesc = mx ? ptx::idesc_mxf8f6f4(A->dtype, B->dtype, 256, BN)
+                 : ptx::idesc_f8f6f4(A->dtype, B->dtype, 256, BN) | ptx::idesc_mn_major(a_mn, b_mn);
+    // MX scales as [chunks][128 words]: chunk (row tile, k tile) = row tile * kb4 + k tile
+    CUtensorMap tsfa = ta, tsfb = ta;
+    if (mx) {
+      const int64_t rows_a = mode == kModeRows ? R_cap : N, rows_b = mode == kModeRows ? (int64_t)E * N : K;
+      if (!encode_tmap_2d(&tsfa, A->scale, 4, 128, (uint64_t)(rows_a / 128 * p.sfa_kb4), 512, 128, 1) ||
+          !encode_tmap_2d(&tsfb, B->scale, 4, 128, (uint64_t)(rows_b / 128 * p.sfb_kb4), 512, 128, 1))
+        return MGQ_ERR_CUDA;
+    }
     // output map: [rows, ldo] elements, boxes of 64 bytes x 32 rows
     CUtensorMap to;
     const int eb = p.out_f32 ? 4 : 2;
     const uint64_t orows = mode == kModeRows ? (uint64_t)R_cap : (uint64_t)E * N;
     p.tma_store = (beta == 0.0f && !direct_store_forced()) ? 1 : 0;
     if (!encode_tmap_2d(&to, out, eb, (uint64_t)p.ldo, orows, (uint64_t)p.ldo * eb, 64 / eb, 32)) return MGQ_ERR_CUDA;
-    return mode == kModeRows ? launch_gemm_pair<kModeRows>(ta, tb2, to, p, s)
-                             : launch_gemm_pair<kModeContract>(ta, tb2, to, p, s);
+    if (mx)
+      return mode == kModeRows ? launch_gemm_pair<kModeRows, kKindMX>(ta, tb2, to, tsfa, tsfb, p, s)
+                               : launch_gemm_pair<kModeContract, kKindMX>(ta, tb2, to, tsfa, tsfb, p, s);
+    return mode == kModeRows ? launch_gemm_pair<kModeRows, kKindTensor>(ta, tb2, to, tsfa, tsfb, p, s)
+                             : launch_gemm_pair<kModeContract, kKindTensor>(ta, tb2, to, tsfa, tsfb, p, s);
   }
   CUtensorMap to;
   {
