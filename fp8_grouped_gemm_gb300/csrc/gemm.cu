@@ -48,13 +48,15 @@ constexpr uint32_t kABytes = BM * BK, kBBytes = BN * BK;
 __host__ __device__ constexpr uint32_t sf_stage_bytes(int kind) {
   return kind == 0 ? 3 * 512u : kind == 3 ? 3 * 2048u : 0u;
 }
-// epilogue staging for TMA stores: 8 warps x 32 rows x 64 bytes (none for NVFP4,
-// whose larger scale chunks leave no room)
+// epilogue staging for TMA stores: 8 warps x 32 rows x 64 bytes
 constexpr uint32_t kStageOut = 32 * 64;
-__host__ __device__ constexpr uint32_t staging_bytes(int kind) { return kind == 3 ? 0u : 8 * kStageOut; }
+__host__ __device__ constexpr uint32_t staging_bytes(int) { return 8 * kStageOut; }
+// pipeline depth: NVFP4's larger scale chunks leave room for 3 stages next to
+// the staging buffers (its 128-byte stages hold 256 elements of K)
+__host__ __device__ constexpr int stages_of(int kind) { return kind == 3 ? 3 : STAGES; }
 __host__ __device__ constexpr size_t smem_bytes(int kind) {
-  return 1024 /*align slack*/ + STAGES * (size_t)(kABytes + kBBytes + sf_stage_bytes(kind)) + staging_bytes(kind) +
-         256 /*barriers*/ + (kMaxE + 8) * 4;
+  return 1024 /*align slack*/ + stages_of(kind) * (size_t)(kABytes + kBBytes + sf_stage_bytes(kind)) +
+         staging_bytes(kind) + 256 /*barriers*/ + (kMaxE + 8) * 4;
 }
 
 enum { kModeRows = 0, kModeContract = 1 };
@@ -228,22 +230,23 @@ template <int MODE, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
+  constexpr int STG = stages_of(KIND);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   uint8_t* sA = smem;
-  uint8_t* sB = sA + STAGES * kABytes;
+  uint8_t* sB = sA + STG * kABytes;
   constexpr uint32_t kSfaBytes = sfa_bytes(KIND), kSfbBytes = 2 * sfa_bytes(KIND);
   constexpr uint32_t kSfbCol = sfb_col0(KIND);
-  uint8_t* sSFA = sB + STAGES * kBBytes;
-  uint8_t* sSFB = sSFA + STAGES * kSfaBytes;
-  uint8_t* sOut = sSFA + STAGES * sf_stage_bytes(KIND);       // epilogue staging (TMA stores)
+  uint8_t* sSFA = sB + STG * kBBytes;
+  uint8_t* sSFB = sSFA + STG * kSfaBytes;
+  uint8_t* sOut = sSFA + STG * sf_stage_bytes(KIND);       // epilogue staging (TMA stores)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + staging_bytes(KIND));
   uint64_t* full = bars;
-  uint64_t* empty = bars + STAGES;
-  uint64_t* tmem_full = bars + 2 * STAGES;        // [2]
-  uint64_t* tmem_empty = bars + 2 * STAGES + 2;   // [2]
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
+  uint64_t* empty = bars + STG;
+  uint64_t* tmem_full = bars + 2 * STG;        // [2]
+  uint64_t* tmem_empty = bars + 2 * STG + 2;   // [2]
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * STG + 4);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   int* s_bad = reinterpret_cast<int*>(s_tmem + 2);
   int32_t* s_off = reinterpret_cast<int32_t*>(bars + 32);
@@ -261,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   for (int i = threadIdx.x; i <= E; i += kThreads) s_off[i] = p.offsets[i];
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < STG; ++s) {
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
     }
@@ -305,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     Tile tl;
     for (int64_t t = blockIdx.x; get_tile<MODE>(s_off, E, p, t, ecur, tl); t += gridDim.x) {
       for (int s = 0; s < tl.nst; ++s, ++it) {
-        const uint32_t st = it % STAGES, ph = (it / STAGES) & 1;
+        const uint32_t st = it % STG, ph = (it / STG) & 1;
         if (*s_abort) break;
         if (!ptx::mbar_wait(&empty[st], ph ^ 1, p.wait_ns)) {
           report(p.err, MGQ_ERR_TIMEOUT);
@@ -352,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
       }
       for (int s = 0; s < tl.nst; ++s, ++it) {
-        const uint32_t st = it % STAGES, ph = (it / STAGES) & 1;
+        const uint32_t st = it % STG, ph = (it / STG) & 1;
         if (BLOCK) {
           // every stage gets a fresh partial buffer
           a = tc % kAcc;
@@ -494,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float alpha = 1.0f;
       if (KIND == kKindTensor || NV) alpha = 1.0f / (p.sa[0] * p.sb[MODE == kModeRows ? tl.e : 0]);
-      epilogue_store(p, r, alpha, orow, col0, staging_bytes(KIND) != 0 && p.tma_store,
+      epilogue_store(p, r, alpha, orow, col0, p.tma_store != 0,
                      sOut + (warp - 2) * kStageOut, &tmO, (int32_t)(tl.out_row + q * 32), lane);
     }
   }
@@ -751,10 +754,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (MX) {
           // this stage's scales into both CTAs' tensor memory (ordered before
           // the MMAs below, which read them)
+          {
+            const uint32_t fa = tmem + kPairSfaCol + st * 4, fb = tmem + kPairSfbCol + st * 8;
+            ptx::tmem_cp_32x128b_x4_pair(fa, ptx::sdesc_sf(sSFA0 + st * kPairSfa));
+            ptx::tmem_cp_32x128b_x4_pair(fb, ptx::sdesc_sf(sSFB0 + st * kPairSfb));
+            ptx::tmem_cp_32x128b_x4_pair(fb + 4, ptx::sdesc_sf(sSFB0 + st * kPairSfb + 512));
+          }
           const uint32_t sfa_t = tmem + kPairSfaCol + st * 4, sfb_t = tmem + kPairSfbCol + st * 8;
-          ptx::tmem_cp_32x128b_x4_pair(sfa_t, ptx::sdesc_sf(sSFA0 + st * kPairSfa));
-          ptx::tmem_cp_32x128b_x4_pair(sfb_t, ptx::sdesc_sf(sSFB0 + st * kPairSfb));
-          ptx::tmem_cp_32x128b_x4_pair(sfb_t + 4, ptx::sdesc_sf(sSFB0 + st * kPairSfb + 512));
 #pragma unroll
           for (int kk = 0; kk < BK / 32; ++kk)
             ptx::mma_mxf8f6f4_pair(tmem + a * BN, ad + kk * astep, bd + kk * bstep,
@@ -853,7 +859,11 @@ int launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtenso
 
 // The 2-CTA kernel serves per-tensor FP8 (wgrad needs output rows in
 // multiples of 256); MGQ_GEMM_1CTA=1 in the environment selects the 1-CTA
-// kernel for every call (both compute the same values).
+// kernel for every call (both compute the same values). MX goes to the 1-CTA
+// kernel unless MGQ_GEMM_MX_PAIR=1: measured on the Mixtral gate/up and down
+// shapes, the pair scale copies (three 32x128b.warpx4 copies per 128-deep
+// stage, executed in order with the MMAs) cost the pair kernel about a fifth
+// of its MMA rate, which leaves it behind the 1-CTA kernel.
 // Failure-detection knobs (read at every launch): MGQ_DEBUG_GEMM_STALL=1 makes
 // the producer issue no loads, so the pipeline waits run out and the kernel
 // reports MGQ_ERR_TIMEOUT and exits cleanly; MGQ_DEBUG_WAIT_MS sets the wait
@@ -883,6 +893,14 @@ bool use_pair_kernel(int mode, int64_t N) {
   }();
   if (force_1cta) return false;
   return mode == kModeRows || N % 256 == 0;
+}
+
+bool mx_pair_selected() {
+  static const bool f = [] {
+    const char* e = getenv("MGQ_GEMM_MX_PAIR");
+    return e && e[0] == '1';
+  }();
+  return f;
 }
 
 int check_operand(const mgq_operand* o) {
@@ -974,7 +992,7 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
                  : ptx::idesc_f8f6f4(A->dtype, B->dtype, BM, BN);
   p.err = err;
   cudaStream_t s = as_stream(stream);
-  if ((kind == kKindTensor || kind == kKindMX) && use_pair_kernel(mode, N)) {
+  if ((kind == kKindTensor || (kind == kKindMX && mx_pair_selected())) && use_pair_kernel(mode, N)) {
     // the pair kernel loads 128-row halves of B (K-major) or 128-column
     // halves (MN-major); MN-major operands are stored with the contraction
     // index down the rows:

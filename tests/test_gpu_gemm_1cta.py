@@ -1,7 +1,8 @@
-"""The grouped GEMM parity tests again, with every call on the 1-CTA kernel
-(MGQ_GEMM_1CTA=1): by default per-tensor and MX calls go to the 2-CTA pair
-kernel, so this keeps the 1-CTA MX and per-tensor paths under the same
-oracle checks. The variable is read once per process, hence the subprocess."""
+"""The grouped GEMM parity tests again under the other kernel selections:
+MGQ_GEMM_1CTA=1 puts every call on the 1-CTA kernel (per-tensor calls
+otherwise go to the 2-CTA pair kernel), MGQ_GEMM_MX_PAIR=1 puts MX calls on
+the pair kernel (otherwise 1-CTA). Both are read once per process, hence the
+subprocesses."""
 import os
 import subprocess
 import sys
@@ -13,8 +14,9 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def test_gemm_parity_on_the_1cta_kernel():
-    env = dict(os.environ, MGQ_GEMM_1CTA="1")
+@pytest.mark.parametrize("var", ["MGQ_GEMM_1CTA", "MGQ_GEMM_MX_PAIR"])
+def test_gemm_parity_under_other_kernel_selection(var):
+    env = dict(os.environ, **{var: "1"})
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-p", "no:cacheprovider", "-m", "gpu",
                         os.path.join(ROOT, "tests", "test_gpu_kernels.py"), "-k", "gemm and not mn_major"],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
