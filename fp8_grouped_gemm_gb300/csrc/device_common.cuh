@@ -32,6 +32,14 @@ __device__ __forceinline__ float round_bf16(float x) {
   return __bfloat162float(__float2bfloat16_rn(x));
 }
 
+// SwiGLU pieces with the fast intrinsics (their float32 error is far below the
+// bf16 rounding of every result they feed). Every kernel that evaluates SwiGLU
+// or its derivative uses these, so fused and separate paths agree bit for bit.
+__device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+__device__ __forceinline__ float sigmoid_fast(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
+// h = bf16(silu(g) u)
+__device__ __forceinline__ float swiglu_bf16(float g, float u) { return round_bf16(__fmul_rn(silu_fast(g), u)); }
+
 // ---------------------------------------------------------------------------
 // Saturating round-to-nearest-even casts (PTX cvt .rn.satfinite). The first
 // source operand of the x2 forms lands in the upper half of the result.

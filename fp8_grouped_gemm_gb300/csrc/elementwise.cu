@@ -49,8 +49,6 @@ struct SwigluArgs {
   int rceil;
 };
 
-// fast intrinsics: their float32 error is far below the bf16 rounding of the result
-__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 template <int SC, int DT>
 __global__ void __launch_bounds__(256) swiglu_quant_kernel(SwigluArgs a) {
@@ -70,7 +68,7 @@ __global__ void __launch_bounds__(256) swiglu_quant_kernel(SwigluArgs a) {
       load_bf16x32(a.gu + r * 2 * F + c, g);
       load_bf16x32(a.gu + r * 2 * F + F + c, u);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) h[i] = round_bf16(__fmul_rn(silu_f(g[i]), u[i]));
+      for (int i = 0; i < 32; ++i) h[i] = swiglu_bf16(g[i], u[i]);
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i) h[i] = 0.0f;
@@ -122,7 +120,7 @@ __global__ void __launch_bounds__(256) dswiglu_quant_kernel(DswigluArgs a) {
       load_bf16x32(a.gu + r * 2 * F + F + c, u);
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const float s = __fdividef(1.0f, 1.0f + __expf(-g[i]));
+        const float s = sigmoid_fast(g[i]);
         dg[i] = round_bf16(d[i] * u[i] * s * (1.0f + g[i] * (1.0f - s)));
         du[i] = round_bf16(d[i] * g[i] * s);
       }
@@ -484,7 +482,7 @@ __global__ void __launch_bounds__(256) swiglu_h_kernel(const uint16_t* __restric
       load_bf16x32(gu + r * 2 * F + c, g);
       load_bf16x32(gu + r * 2 * F + F + c, u);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) hv[i] = round_bf16(__fmul_rn(silu_f(g[i]), u[i]));
+      for (int i = 0; i < 32; ++i) hv[i] = swiglu_bf16(g[i], u[i]);
       tam = max(tam, absmax_bits_f32(hv, 32));
       store_bf16x32(h + r * F + c, hv);
     }

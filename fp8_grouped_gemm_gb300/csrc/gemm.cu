@@ -86,8 +86,21 @@ struct GemmParams {
   int out_f32;
   float beta;
   uint32_t idesc;
-  int tma_store;      // pair kernel: write the output through TMA stores
+  int tma_store;      // write the output through TMA stores
   int a_mn, b_mn;     // pair kernel: operand stored MN-major (contraction down the rows)
+  int64_t b_half2;    // rows from the first to the second 128-row half of a B tile
+                      // (128; SwiGLU: F, the up rows matching the gate rows)
+  // SwiGLU epilogue (gate/up GEMM): h = bf16(silu(g) u) of the bf16-rounded
+  // accumulator columns, quantised row-wise; the plain output (g | u) only
+  // when `out` is set
+  int swiglu;
+  int64_t F;
+  uint8_t* h_codes;   // [R_cap, F]
+  uint8_t* h_scales;  // MX: tiled E8M0 scales of [R_cap, F]
+  const float* h_scale;  // per-tensor: the scale multiplying h
+  float* h_amax;      // per-tensor: max |h| (atomically raised), or null
+  uint16_t* h_bf16;   // [R_cap, F] or null
+  int h_dtype, h_rceil;
   int debug_stall;    // failure-detection test: the producer issues no loads, so
                       // every consumer wait runs out and reports MGQ_ERR_TIMEOUT
   uint64_t wait_ns;   // limit of every mbarrier wait
@@ -118,10 +131,11 @@ __device__ __forceinline__ bool get_tile(const int32_t* s_off, int E, const Gemm
     tl.e = e;
     tl.nst = (int)(p.K / BK);
     tl.row_a = s_off[e] + BM * m;
-    tl.row_b = (int64_t)e * p.N + BN * n;
+    // SwiGLU: gate rows 128 n.. and (b_half2 = F later) the matching up rows
+    tl.row_b = (int64_t)e * p.N + (p.swiglu ? 128 : BN) * n;
     tl.kx0 = 0;
     tl.out_row = tl.row_a;
-    tl.out_col = BN * n;
+    tl.out_col = (p.swiglu ? 128 : BN) * n;
   } else {
     const int64_t mN = p.N / BM, nK = p.K / BN;
     const int64_t tpe = mN * nK;
@@ -226,10 +240,100 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, const uint32
   }
 }
 
+// Accumulator column of a thread's chunk c (of 4 x 32): the 128-column half
+// `half` of the tile, or for SwiGLU the gate columns half*64.. (c = 0, 1) and
+// the matching up columns 128 + half*64.. (c = 2, 3).
+__device__ __forceinline__ uint32_t acc_col(int swiglu, uint32_t half, int c) {
+  return swiglu ? (c < 2 ? half * 64 + 32 * c : 128 + half * 64 + 32 * (c - 2)) : half * 128 + 32 * c;
+}
+
+// SwiGLU epilogue of the gate/up GEMM for one thread's row `orow` and ffn
+// columns f0..f0+63: g, u = bf16(acc * alpha) (the values the plain GEMM would
+// write), h = bf16(silu(g) u), quantised with the GEMM's scaling kind (MX:
+// E8M0 per 32 columns; per-tensor: *p.h_scale, max |h| into tam). The codes,
+// and (p.out set) g and u, go out through TMA stores from the warp's staging
+// buffer; MX scales and the optional bf16 h by plain stores.
+template <int KIND>
+__device__ __forceinline__ void epilogue_swiglu(const GemmParams& p, const uint32_t (&r)[4][32], float alpha,
+                                                int64_t orow, int64_t f0, uint8_t* stg, const CUtensorMap* tmO,
+                                                const CUtensorMap* tmH, int32_t y0, uint32_t lane, uint32_t& tam) {
+  // one 64-byte row per lane in the staging buffer, stored as 32 rows x 64 bytes
+  auto stage = [&](int j, uint4 v, const CUtensorMap* m, int64_t x) {
+    if (j == 0) {
+      if (lane == 0) ptx::bulk_wait_read0();
+      __syncwarp();
+    }
+    reinterpret_cast<uint4*>(stg + lane * 64)[j] = v;
+    if (j == 3) {
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::tma_store_2d(m, stg, (int32_t)x, y0);
+        ptx::bulk_commit();
+      }
+    }
+  };
+  auto bf = [&](uint32_t bits) { return round_bf16(__uint_as_float(bits) * alpha); };
+  if (p.out) {
+    // g and u as bf16: columns f0 + 32c and F + f0 + 32c of [R_cap, 2F]
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t* v = &r[c][8 * j];
+        stage(j,
+              make_uint4(pack_bf16x2(bf(v[0]), bf(v[1])), pack_bf16x2(bf(v[2]), bf(v[3])),
+                         pack_bf16x2(bf(v[4]), bf(v[5])), pack_bf16x2(bf(v[6]), bf(v[7]))),
+              tmO, (c < 2 ? 0 : p.F) + f0 + 32 * (c & 1));
+      }
+  }
+  const float ts = KIND == kKindTensor ? *p.h_scale : 1.0f;
+  const bool e5 = p.h_dtype == MGQ_E5M2;
+  uint32_t hw[16];        // the 64 codes
+  uint32_t sc2 = 0;       // MX: the two block scales
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    uint32_t hp[16];      // h as bf16 pairs (exact)
+    uint32_t am2 = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float h0 = swiglu_bf16(bf(r[c][2 * i]), bf(r[2 + c][2 * i]));
+      const float h1 = swiglu_bf16(bf(r[c][2 * i + 1]), bf(r[2 + c][2 * i + 1]));
+      hp[i] = pack_bf16x2(h0, h1);
+      am2 = absmax_bf16x2(am2, hp[i]);
+    }
+    if (p.h_bf16) {
+      uint4* d = reinterpret_cast<uint4*>(p.h_bf16 + orow * p.F + f0 + 32 * c);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) d[q] = make_uint4(hp[4 * q], hp[4 * q + 1], hp[4 * q + 2], hp[4 * q + 3]);
+    }
+    const uint32_t am = fold_bf16x2(am2);
+    float mult = ts;
+    if (KIND == kKindMX) {
+      const int e = mx_exponent(am, e5 ? FmtInfo<MGQ_E5M2>::emax : FmtInfo<MGQ_E4M3>::emax, p.h_rceil != 0);
+      mult = mx_multiplier(e);
+      sc2 |= mx_scale_code(e) << (8 * c);
+    } else {
+      tam = max(tam, am);
+    }
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const float a0 = __fmul_rn(bf16_lo(hp[2 * w]), mult), a1 = __fmul_rn(bf16_hi(hp[2 * w]), mult);
+      const float a2 = __fmul_rn(bf16_lo(hp[2 * w + 1]), mult), a3 = __fmul_rn(bf16_hi(hp[2 * w + 1]), mult);
+      hw[8 * c + w] = e5 ? cvt_fp8x4<MGQ_E5M2>(a0, a1, a2, a3) : cvt_fp8x4<MGQ_E4M3>(a0, a1, a2, a3);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) stage(j, make_uint4(hw[4 * j], hw[4 * j + 1], hw[4 * j + 2], hw[4 * j + 3]), tmH, f0);
+  if (KIND == kKindMX)
+    *reinterpret_cast<uint16_t*>(p.h_scales + tiled_scale_offset(orow, f0 / 32, p.F / 128)) = (uint16_t)sc2;
+}
+
 template <int MODE, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
+                        const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmH,
+                        const GemmParams p) {
   constexpr int STG = stages_of(KIND);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -319,16 +423,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive_expect_tx(&full[st], bytes);
         const int32_t kx = (int32_t)(tl.kx0 + (int64_t)s * BK);
         ptx::tma_load_2d(sA + st * kABytes, &tmA, &full[st], kx, (int32_t)tl.row_a);
+        // B in two 128-row halves (contiguous, or gate and up rows for SwiGLU)
         ptx::tma_load_2d(sB + st * kBBytes, &tmB, &full[st], kx, (int32_t)tl.row_b);
+        ptx::tma_load_2d(sB + st * kBBytes + kBBytes / 2, &tmB, &full[st], kx, (int32_t)(tl.row_b + p.b_half2));
         if (MX) {
           // scale chunks of this stage: MX one 512-byte chunk per 128 rows,
           // NVFP4 four consecutive chunks (the 4 MMAs of the stage)
           const int64_t kt = (tl.kx0 / BK + s) * (kSfaBytes / 512);
           const uint8_t* fa = p.sfa + ((tl.row_a / BM) * p.sfa_kb4 + kt) * 512;
           const uint8_t* fb = p.sfb + ((tl.row_b / BM) * p.sfb_kb4 + kt) * 512;
+          const uint8_t* fb2 = p.sfb + (((tl.row_b + p.b_half2) / BM) * p.sfb_kb4 + kt) * 512;
           ptx::bulk_load(sSFA + st * kSfaBytes, fa, kSfaBytes, &full[st]);
           ptx::bulk_load(sSFB + st * kSfbBytes, fb, kSfaBytes, &full[st]);
-          ptx::bulk_load(sSFB + st * kSfbBytes + kSfaBytes, fb + p.sfb_kb4 * 512, kSfaBytes, &full[st]);
+          ptx::bulk_load(sSFB + st * kSfbBytes + kSfaBytes, fb2, kSfaBytes, &full[st]);
         }
       }
       if (*s_abort) break;
@@ -418,6 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t q = warp & 3;
     const uint32_t half = (uint32_t)(warp - 2) >> 2;
     const int64_t row_in_tile = q * 32 + lane;
+    uint32_t h_tam = 0;    // per-tensor SwiGLU: this thread's max |h| (float bits)
     int ecur = 0;
     uint32_t tc = 0;
     Tile tl;
@@ -487,9 +595,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t taddr = tmem + a * BN + ((q * 32) << 16) + half * (BN / 2);
+        const uint32_t tbase = tmem + a * BN + ((q * 32) << 16);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) ptx::tmem_ld_32x32b_x32(taddr + c * 32, r[c]);
+        for (int c = 0; c < 4; ++c) ptx::tmem_ld_32x32b_x32(tbase + acc_col(MODE == kModeRows && p.swiglu, half, c), r[c]);
         ptx::tmem_ld_wait();
         ptx::tc_fence_before();
         ptx::mbar_arrive(&tmem_empty[a]);       // accumulator free for the next tile
@@ -497,8 +605,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float alpha = 1.0f;
       if (KIND == kKindTensor || NV) alpha = 1.0f / (p.sa[0] * p.sb[MODE == kModeRows ? tl.e : 0]);
-      epilogue_store(p, r, alpha, orow, col0, p.tma_store != 0,
-                     sOut + (warp - 2) * kStageOut, &tmO, (int32_t)(tl.out_row + q * 32), lane);
+      if (MODE == kModeRows && (KIND == kKindTensor || KIND == kKindMX) && p.swiglu)
+        epilogue_swiglu<KIND == kKindMX ? kKindMX : kKindTensor>(p, r, alpha, orow, tl.out_col + half * 64,
+                                                                 sOut + (warp - 2) * kStageOut, &tmO, &tmH,
+                                                                 (int32_t)(tl.out_row + q * 32), lane, h_tam);
+      else
+        epilogue_store(p, r, alpha, orow, col0, p.tma_store != 0, sOut + (warp - 2) * kStageOut, &tmO,
+                       (int32_t)(tl.out_row + q * 32), lane);
+    }
+    if (MODE == kModeRows && KIND == kKindTensor && p.swiglu && p.h_amax) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) h_tam = max(h_tam, __shfl_xor_sync(0xFFFFFFFFu, h_tam, o));
+      if (lane == 0) atomic_max_nonneg(p.h_amax, __uint_as_float(h_tam));
     }
   }
   if (warp >= 2 && lane == 0) ptx::bulk_wait0();   // this warp's TMA stores are complete
@@ -511,8 +629,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int MODE, int KIND>
-int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const GemmParams& p,
-                cudaStream_t s) {
+int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const CUtensorMap& th,
+                const GemmParams& p, cudaStream_t s) {
   auto kern = grouped_gemm_kernel<MODE, KIND>;
   constexpr size_t kSmemBytes = smem_bytes(KIND);
   static bool attr_set[64] = {false};
@@ -523,7 +641,7 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
       return MGQ_ERR_CUDA;
     attr_set[dev] = true;
   }
-  kern<<<num_sms(), kThreads, kSmemBytes, s>>>(ta, tb, to, p);
+  kern<<<num_sms(), kThreads, kSmemBytes, s>>>(ta, tb, to, th, p);
   MGQ_LAUNCH_CHECK();
   return MGQ_OK;
 }
@@ -573,10 +691,10 @@ __device__ __forceinline__ bool get_pair_tile(const int32_t* s_off, const int32_
     tl.e = e;
     tl.nst = (int)(p.K / BK);
     tl.row_a = s_off[e] + 256 * m;
-    tl.row_b = (int64_t)e * p.N + BN * n;
+    tl.row_b = (int64_t)e * p.N + (p.swiglu ? 128 : BN) * n;
     tl.kx0 = 0;
     tl.out_row = tl.row_a;
-    tl.out_col = BN * n;
+    tl.out_col = (p.swiglu ? 128 : BN) * n;
   } else {
     const int64_t mN = p.N / 256, nK = p.K / BN;
     const int64_t tpe = mN * nK;
@@ -599,7 +717,8 @@ template <int MODE, int KIND>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmSFA,
-                             const __grid_constant__ CUtensorMap tmSFB, const GemmParams p) {
+                             const __grid_constant__ CUtensorMap tmSFB, const __grid_constant__ CUtensorMap tmH,
+                             const GemmParams p) {
   constexpr bool MX = KIND == kKindMX;
   constexpr int kAccBufs = MX ? 1 : 2;             // MX: scale slots leave room for one accumulator
   extern __shared__ uint8_t smem_raw[];
@@ -703,7 +822,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ptx::tma_load_2d_pair(sB + st * kPairTile, &tmB, bar0, (int32_t)(tl.out_col + 128 * rank),
                                 (int32_t)((MODE == kModeRows ? (int64_t)tl.e * p.K : 0) + kx));
         else
-          ptx::tma_load_2d_pair(sB + st * kPairTile, &tmB, bar0, kx, (int32_t)(tl.row_b + 128 * rank));
+          ptx::tma_load_2d_pair(sB + st * kPairTile, &tmB, bar0, kx, (int32_t)(tl.row_b + p.b_half2 * rank));
         if (MX) {
           // scale chunk (row tile, k tile) is row tile * kb4 + kx / 128 of the
           // [chunks][128 words] view of the scales
@@ -712,7 +831,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 (int32_t)(((tl.row_a + 128 * rank) / 128) * p.sfa_kb4 + kt));
           ptx::tma_load_2d_pair(sSFB + st * kPairSfb, &tmSFB, bar0, 0, (int32_t)((tl.row_b / 128) * p.sfb_kb4 + kt));
           ptx::tma_load_2d_pair(sSFB + st * kPairSfb + 512, &tmSFB, bar0, 0,
-                                (int32_t)((tl.row_b / 128 + 1) * p.sfb_kb4 + kt));
+                                (int32_t)(((tl.row_b + p.b_half2) / 128) * p.sfb_kb4 + kt));
         }
       }
       if (*s_abort) break;
@@ -782,6 +901,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t q = warp & 3;
     const uint32_t half = (uint32_t)(warp - 2) >> 2;
     const int64_t row_in_tile = 128 * rank + q * 32 + lane;
+    uint32_t h_tam = 0;    // per-tensor SwiGLU: this thread's max |h| (float bits)
     const uint32_t empty_remote0 = ptx::mapa_shared(ptx::smem_u32(&tmem_empty[0]), 0);
     const uint32_t empty_remote1 = ptx::mapa_shared(ptx::smem_u32(&tmem_empty[1]), 0);
     int ecur = 0;
@@ -814,9 +934,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_after();
       uint32_t r[4][32];
-      const uint32_t taddr = tmem + a * BN + ((q * 32) << 16) + half * (BN / 2);
+      const uint32_t tbase = tmem + a * BN + ((q * 32) << 16);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) ptx::tmem_ld_32x32b_x32(taddr + c * 32, r[c]);
+      for (int c = 0; c < 4; ++c) ptx::tmem_ld_32x32b_x32(tbase + acc_col(MODE == kModeRows && p.swiglu, half, c), r[c]);
       ptx::tmem_ld_wait();
       ptx::tc_fence_before();
       __syncwarp();
@@ -824,8 +944,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ++tc;
       if (!store) continue;    // the warp's 32 rows lie wholly inside or past the group
       const float alpha = MX ? 1.0f : 1.0f / (p.sa[0] * p.sb[MODE == kModeRows ? tl.e : 0]);
-      epilogue_store(p, r, alpha, orow, col0, p.tma_store != 0, sOut + (warp - 2) * kStageOut, &tmO,
-                     (int32_t)(tl.out_row + 128 * rank + q * 32), lane);
+      if (MODE == kModeRows && p.swiglu)
+        epilogue_swiglu<KIND>(p, r, alpha, orow, tl.out_col + half * 64, sOut + (warp - 2) * kStageOut, &tmO, &tmH,
+                              (int32_t)(tl.out_row + 128 * rank + q * 32), lane, h_tam);
+      else
+        epilogue_store(p, r, alpha, orow, col0, p.tma_store != 0, sOut + (warp - 2) * kStageOut, &tmO,
+                       (int32_t)(tl.out_row + 128 * rank + q * 32), lane);
+    }
+    if (MODE == kModeRows && KIND == kKindTensor && p.swiglu && p.h_amax) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) h_tam = max(h_tam, __shfl_xor_sync(0xFFFFFFFFu, h_tam, o));
+      if (lane == 0) atomic_max_nonneg(p.h_amax, __uint_as_float(h_tam));
     }
   }
   if (warp >= 2 && lane == 0) ptx::bulk_wait0();   // this warp's TMA stores are complete
@@ -841,7 +970,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 template <int MODE, int KIND>
 int launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const CUtensorMap& tsfa,
-                     const CUtensorMap& tsfb, const GemmParams& p, cudaStream_t s) {
+                     const CUtensorMap& tsfb, const CUtensorMap& th, const GemmParams& p, cudaStream_t s) {
   auto kern = grouped_gemm_pair_kernel<MODE, KIND>;
   constexpr size_t kSmem = pair_smem(KIND);
   static bool attr_set[64] = {false};
@@ -852,7 +981,7 @@ int launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtenso
       return MGQ_ERR_CUDA;
     attr_set[dev] = true;
   }
-  kern<<<num_sms() / 2 * 2, kThreads, kSmem, s>>>(ta, tb, to, tsfa, tsfb, p);
+  kern<<<num_sms() / 2 * 2, kThreads, kSmem, s>>>(ta, tb, to, tsfa, tsfb, th, p);
   MGQ_LAUNCH_CHECK();
   return MGQ_OK;
 }
@@ -912,12 +1041,19 @@ int check_operand(const mgq_operand* o) {
 // Shared driver of the three entry points.
 //  mode rows:     A [rowsA, Kc] (ld), B [E*Nout, Kc] (ld); out [rowsA, Nout]
 //  mode contract: A [Nout_rows, R_cap], B [Kout, R_cap]; out [E*Nout_rows, Kout]
+// SwiGLU epilogue request of the gate/up GEMM (N = 2F)
+struct SwigluOut {
+  const mgq_qdesc* qh;
+  void* h_bf16;
+};
+
 int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scaling, const int32_t* offsets, int E,
-                int64_t R_cap, int64_t N, int64_t K, float beta, void* out, int out_dtype, void* stream) {
+                int64_t R_cap, int64_t N, int64_t K, float beta, void* out, int out_dtype, void* stream,
+                const SwigluOut* sw = nullptr) {
   int rc;
   if ((rc = check_operand(A)) != MGQ_OK) return rc;
   if ((rc = check_operand(B)) != MGQ_OK) return rc;
-  MGQ_CHECK_ARG(offsets && out && aligned16(out) && E >= 1 && E <= kMaxE && R_cap > 0 && R_cap % BM == 0);
+  MGQ_CHECK_ARG(offsets && (out || sw) && aligned16(out) && E >= 1 && E <= kMaxE && R_cap > 0 && R_cap % BM == 0);
   MGQ_CHECK_ARG(out_dtype == MGQ_OUT_BF16 || out_dtype == MGQ_OUT_F32);
   MGQ_CHECK_ARG(beta == 0.0f || (mode == kModeContract && out_dtype == MGQ_OUT_F32));
   MGQ_CHECK_ARG(R_cap < (1ll << 31));
@@ -953,7 +1089,7 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
     if (!encode_tmap_u8_2d(&ta, A->data, (uint64_t)(K / ebytes_den), (uint64_t)R_cap,
                            (uint64_t)(A->ld / ebytes_den), 128, BM) ||
         (!b_mn && !encode_tmap_u8_2d(&tb, B->data, (uint64_t)(K / ebytes_den), (uint64_t)E * N,
-                                     (uint64_t)(B->ld / ebytes_den), 128, BN)))
+                                     (uint64_t)(B->ld / ebytes_den), 128, 128)))
       return MGQ_ERR_CUDA;
     // 512-byte scale chunks per 128-row tile: MX 32x4-element blocks, NVFP4 16x4
     p.sfa_kb4 = A->ld / (nv ? 64 : 128);
@@ -962,7 +1098,7 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
     MGQ_CHECK_ARG(N > 0 && K > 0 && N % BM == 0 && K % BN == 0);
     MGQ_CHECK_ARG((a_mn || A->ld >= R_cap) && (b_mn || B->ld >= R_cap));
     if ((!a_mn && !encode_tmap_u8_2d(&ta, A->data, (uint64_t)R_cap, (uint64_t)N, (uint64_t)A->ld, 128, BM)) ||
-        (!b_mn && !encode_tmap_u8_2d(&tb, B->data, (uint64_t)R_cap, (uint64_t)K, (uint64_t)B->ld, 128, BN)))
+        (!b_mn && !encode_tmap_u8_2d(&tb, B->data, (uint64_t)R_cap, (uint64_t)K, (uint64_t)B->ld, 128, 128)))
       return MGQ_ERR_CUDA;
     p.sfa_kb4 = A->ld / 128;
     p.sfb_kb4 = B->ld / 128;
@@ -986,6 +1122,41 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
   p.tma_store = 0;
   p.a_mn = 0;
   p.b_mn = 0;
+  p.b_half2 = 128;
+  p.swiglu = 0;
+  p.F = 0;
+  p.h_codes = nullptr;
+  p.h_scales = nullptr;
+  p.h_scale = nullptr;
+  p.h_amax = nullptr;
+  p.h_bf16 = nullptr;
+  p.h_dtype = MGQ_E4M3;
+  p.h_rceil = 1;
+  CUtensorMap th = ta;    // SwiGLU codes map (unused otherwise)
+  if (sw) {
+    // gate/up tiles: gate rows 128 n.. and up rows F + 128 n..; h quantised
+    // row-wise with the GEMM's own scaling (MX or per-tensor)
+    const mgq_qdesc* qh = sw->qh;
+    const int64_t F = N / 2;
+    if (mode != kModeRows || (kind != kKindTensor && kind != kKindMX) || b_mn) return MGQ_ERR_UNSUPPORTED;
+    MGQ_CHECK_ARG(qh && qh->row.data && aligned16(qh->row.data) && N % 256 == 0 && aligned16(sw->h_bf16));
+    if (qh->scaling != scaling || qh->col.data) return MGQ_ERR_UNSUPPORTED;
+    if (qh->dtype != MGQ_E4M3 && qh->dtype != MGQ_E5M2) return MGQ_ERR_UNSUPPORTED;
+    if (mx) MGQ_CHECK_ARG(qh->row.scale && aligned16(qh->row.scale));
+    else MGQ_CHECK_ARG(qh->tensor_scale != nullptr);
+    MGQ_CHECK_ARG(out_dtype == MGQ_OUT_BF16);
+    p.swiglu = 1;
+    p.F = F;
+    p.b_half2 = F;
+    p.h_codes = static_cast<uint8_t*>(qh->row.data);
+    p.h_scales = static_cast<uint8_t*>(qh->row.scale);
+    p.h_scale = qh->tensor_scale;
+    p.h_amax = qh->amax_out;
+    p.h_bf16 = static_cast<uint16_t*>(sw->h_bf16);
+    p.h_dtype = qh->dtype;
+    p.h_rceil = qh->e8m0_mode == MGQ_E8M0_RCEIL;
+    if (!encode_tmap_2d(&th, qh->row.data, 1, (uint64_t)F, (uint64_t)R_cap, (uint64_t)F, 64, 32)) return MGQ_ERR_CUDA;
+  }
   debug_knobs(&p.debug_stall, &p.wait_ns);
   p.idesc = nv   ? ptx::idesc_mxf4nvf4_ue4m3(BM, BN)
             : mx ? ptx::idesc_mxf8f6f4(A->dtype, B->dtype, BM, BN)
@@ -1030,32 +1201,34 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
         return MGQ_ERR_CUDA;
     }
     // output map: [rows, ldo] elements, boxes of 64 bytes x 32 rows
-    CUtensorMap to;
+    CUtensorMap to = th;
     const int eb = p.out_f32 ? 4 : 2;
     const uint64_t orows = mode == kModeRows ? (uint64_t)R_cap : (uint64_t)E * N;
     p.tma_store = (beta == 0.0f && !direct_store_forced()) ? 1 : 0;
-    if (!encode_tmap_2d(&to, out, eb, (uint64_t)p.ldo, orows, (uint64_t)p.ldo * eb, 64 / eb, 32)) return MGQ_ERR_CUDA;
+    if (out && !encode_tmap_2d(&to, out, eb, (uint64_t)p.ldo, orows, (uint64_t)p.ldo * eb, 64 / eb, 32))
+      return MGQ_ERR_CUDA;
     if (mx)
-      return mode == kModeRows ? launch_gemm_pair<kModeRows, kKindMX>(ta, tb2, to, tsfa, tsfb, p, s)
-                               : launch_gemm_pair<kModeContract, kKindMX>(ta, tb2, to, tsfa, tsfb, p, s);
-    return mode == kModeRows ? launch_gemm_pair<kModeRows, kKindTensor>(ta, tb2, to, tsfa, tsfb, p, s)
-                             : launch_gemm_pair<kModeContract, kKindTensor>(ta, tb2, to, tsfa, tsfb, p, s);
+      return mode == kModeRows ? launch_gemm_pair<kModeRows, kKindMX>(ta, tb2, to, tsfa, tsfb, th, p, s)
+                               : launch_gemm_pair<kModeContract, kKindMX>(ta, tb2, to, tsfa, tsfb, th, p, s);
+    return mode == kModeRows ? launch_gemm_pair<kModeRows, kKindTensor>(ta, tb2, to, tsfa, tsfb, th, p, s)
+                             : launch_gemm_pair<kModeContract, kKindTensor>(ta, tb2, to, tsfa, tsfb, th, p, s);
   }
-  CUtensorMap to;
+  CUtensorMap to = th;
   {
     const int eb = p.out_f32 ? 4 : 2;
     const uint64_t orows = mode == kModeRows ? (uint64_t)R_cap : (uint64_t)E * N;
-    if (!encode_tmap_2d(&to, out, eb, (uint64_t)p.ldo, orows, (uint64_t)p.ldo * eb, 64 / eb, 32)) return MGQ_ERR_CUDA;
+    if (out && !encode_tmap_2d(&to, out, eb, (uint64_t)p.ldo, orows, (uint64_t)p.ldo * eb, 64 / eb, 32))
+      return MGQ_ERR_CUDA;
     p.tma_store = (beta == 0.0f && !direct_store_forced()) ? 1 : 0;
   }
   if (mode == kModeRows) {
-    if (kind == kKindMX) return launch_gemm<kModeRows, kKindMX>(ta, tb, to, p, s);
-    if (kind == kKindTensor) return launch_gemm<kModeRows, kKindTensor>(ta, tb, to, p, s);
-    if (kind == kKindNV) return launch_gemm<kModeRows, kKindNV>(ta, tb, to, p, s);
-    return launch_gemm<kModeRows, kKindBlock>(ta, tb, to, p, s);
+    if (kind == kKindMX) return launch_gemm<kModeRows, kKindMX>(ta, tb, to, th, p, s);
+    if (kind == kKindTensor) return launch_gemm<kModeRows, kKindTensor>(ta, tb, to, th, p, s);
+    if (kind == kKindNV) return launch_gemm<kModeRows, kKindNV>(ta, tb, to, th, p, s);
+    return launch_gemm<kModeRows, kKindBlock>(ta, tb, to, th, p, s);
   }
-  if (kind == kKindMX) return launch_gemm<kModeContract, kKindMX>(ta, tb, to, p, s);
-  return launch_gemm<kModeContract, kKindTensor>(ta, tb, to, p, s);
+  if (kind == kKindMX) return launch_gemm<kModeContract, kKindMX>(ta, tb, to, th, p, s);
+  return launch_gemm<kModeContract, kKindTensor>(ta, tb, to, th, p, s);
 }
 
 }  // namespace
@@ -1081,6 +1254,15 @@ int mgq_grouped_gemm_wgrad(const mgq_operand* dYcol, const mgq_operand* Acol, in
                            int E, int64_t R_cap, int64_t N, int64_t K, float beta, void* dW, int out_dtype,
                            void* stream) {
   return run_grouped(kModeContract, dYcol, Acol, scaling, offsets, E, R_cap, N, K, beta, dW, out_dtype, stream);
+}
+
+int mgq_grouped_gemm_fwd_swiglu(const mgq_operand* A, const mgq_operand* W1, int scaling, const int32_t* offsets,
+                                int E, int64_t R_cap, int64_t F, int64_t K, const mgq_qdesc* qh, void* gu_bf16,
+                                void* h_bf16, void* stream) {
+  if (F <= 0 || F % 128 != 0) return MGQ_ERR_INVALID_ARG;
+  const SwigluOut sw{qh, h_bf16};
+  return run_grouped(kModeRows, A, W1, scaling, offsets, E, R_cap, 2 * F, K, 0.0f, gu_bf16, MGQ_OUT_BF16, stream,
+                     &sw);
 }
 
 }  // extern "C"

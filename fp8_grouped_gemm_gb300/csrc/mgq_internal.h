@@ -18,7 +18,7 @@ int* error_word();
 bool encode_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch,
                        uint32_t box_inner, uint32_t box_outer);
 
-// 2D row-major tensor map of 16-bit or 32-bit elements (elem_bytes 2 or 4),
+// 2D row-major tensor map of 8-, 16- or 32-bit elements (elem_bytes 1, 2 or 4),
 // no swizzle: `inner` elements per row, `outer` rows, pitch bytes.
 bool encode_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner, uint64_t outer,
                     uint64_t pitch, uint32_t box_inner, uint32_t box_outer);

@@ -59,7 +59,7 @@ struct SrcSwiglu {
     load8_bf16(gu + r * 2 * F + c, g);
     load8_bf16(gu + r * 2 * F + F + c, u);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = round_bf16(__fmul_rn(__fdividef(g[i], 1.0f + __expf(-g[i])), u[i]));
+    for (int i = 0; i < 8; ++i) v[i] = swiglu_bf16(g[i], u[i]);
     if (h_out) store8_bf16(h_out + r * F + c, v);
   }
 };
@@ -81,7 +81,7 @@ struct SrcDswiglu {
     load8_bf16(gu + r * 2 * F + F + f, u);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float s = __fdividef(1.0f, 1.0f + __expf(-g[i]));
+      const float s = sigmoid_fast(g[i]);
       dg[i] = round_bf16(d[i] * u[i] * s * (1.0f + g[i] * (1.0f - s)));
       du[i] = round_bf16(d[i] * g[i] * s);
     }

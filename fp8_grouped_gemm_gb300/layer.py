@@ -6,6 +6,8 @@ per-tensor recipe, of the backward step:
 
 forward:  moe_permute (+ quantise) -> grouped_gemm_fwd (gate/up) ->
           swiglu_quantize -> grouped_gemm_fwd (down) -> moe_unpermute
+          (MXFP8 inference and the delayed recipe fuse the gate/up GEMM and
+          SwiGLU + quantise into grouped_gemm_fwd_swiglu)
 backward: moe_unpermute_bwd (+ quantise dY, dprobs) -> grouped_gemm_dgrad and
           grouped_gemm_wgrad (down) -> dswiglu_quantize -> grouped_gemm_dgrad
           and grouped_gemm_wgrad (gate/up) -> moe_permute_bwd
@@ -34,7 +36,8 @@ ALIGN = 128       # group padding: the grouped GEMM tiles rows by 128
 
 class ExpertLayer:
     def __init__(self, w: Workload, device, recipe: str | None = None, keep_bf16: bool = False,
-                 history: int = 1024, train: bool | None = None, col_copies: bool = False):
+                 history: int = 1024, train: bool | None = None, col_copies: bool = False,
+                 fuse_swiglu: bool = True):
         self.w = w
         self.dev = torch.device(device)
         self.recipe = recipe or w.recipe
@@ -44,6 +47,11 @@ class ExpertLayer:
         self.delayed = self.recipe == "delayed"
         # per-tensor backward GEMMs read the row-wise codes MN-major
         self.mn = self.delayed and not col_copies
+        self.keep_bf16 = keep_bf16
+        # SwiGLU in the gate/up GEMM epilogue: MX or per-tensor scaling, and no
+        # column-wise copy of h wanted (MX training needs one; NVFP4 needs the
+        # whole tensor's amax first; blockwise spans both epilogue halves)
+        self.fused_swiglu = fuse_swiglu and ((self.recipe == "mxfp8" and not self.train) or self.mn)
         if self.train and self.recipe not in ("delayed", "mxfp8"):
             raise NotImplementedError(f"backward with {self.recipe}")
         self.scaling = {"mxfp8": mgq.MX32_E8M0, "delayed": mgq.TENSOR_F32,
@@ -208,12 +216,22 @@ class ExpertLayer:
                 sa, sw1, sh, sw2 = self._fs(0), self._fs(2, E), self._fs(1), self._fs(2 + E, E)
             A1, B1 = mgq.operand(self.xq, sa, H, dt), mgq.operand(self.w1q, sw1, H, dt)
             A2, B2 = mgq.operand(self.hq, sh, F, dt), mgq.operand(self.w2q, sw2, F, dt)
-        return [
-            ("permute_quant", lambda: mgq.moe_permute(x, topk_idx, E, ALIGN, qx, R, self.row_id_map, self.src_row,
-                                                      self.offsets, self.counts, self.ws, None, stream)),
-            ("gemm_fwd_gateup", lambda: mgq.grouped_gemm_fwd(A1, B1, sc, self.offsets, E, R, 2 * F, H, self.gu,
-                                                             mgq.OUT_BF16, stream)),
-            ("swiglu_quant", lambda: mgq.swiglu_quantize(self.gu, R, F, self.offsets, E, qh, self.h_bf16, stream)),
+        permute = ("permute_quant", lambda: mgq.moe_permute(x, topk_idx, E, ALIGN, qx, R, self.row_id_map,
+                                                            self.src_row, self.offsets, self.counts, self.ws, None,
+                                                            stream))
+        if self.fused_swiglu:
+            # g | u only where something reads them (backward, or checks)
+            gu = self.gu if (self.train or self.keep_bf16) else None
+            gateup = [("gemm_fwd_gateup_swiglu",
+                       lambda: mgq.grouped_gemm_fwd_swiglu(A1, B1, sc, self.offsets, E, R, F, H, qh, gu, self.h_bf16,
+                                                           stream))]
+        else:
+            gateup = [
+                ("gemm_fwd_gateup", lambda: mgq.grouped_gemm_fwd(A1, B1, sc, self.offsets, E, R, 2 * F, H, self.gu,
+                                                                 mgq.OUT_BF16, stream)),
+                ("swiglu_quant", lambda: mgq.swiglu_quantize(self.gu, R, F, self.offsets, E, qh, self.h_bf16,
+                                                             stream))]
+        return [permute] + gateup + [
             ("gemm_fwd_down", lambda: mgq.grouped_gemm_fwd(A2, B2, sc, self.offsets, E, R, H, F, self.y,
                                                            mgq.OUT_BF16, stream)),
             ("unpermute", lambda: mgq.moe_unpermute(self.y, self.row_id_map, probs, self.out, stream)),
@@ -309,6 +327,8 @@ class ExpertLayer:
         E = self.w.E
         n_route = 2 if self.w.T * self.w.k > 0 else 1
         fwd = n_route + 1 + 1 + 1 + 1 + 1               # route, permute-quant, gemm1, swiglu, gemm2, unpermute
+        if self.fused_swiglu:
+            fwd -= 1                                    # SwiGLU in the gate/up GEMM epilogue
         if self.nv:
             return fwd + 2 + 4                          # + amax passes (x, h); weights: 2 x (amax + rows)
         if not self.train:

@@ -243,6 +243,25 @@ int mgq_grouped_gemm_wgrad(const mgq_operand* dYcol, const mgq_operand* Acol, in
                            const int32_t* offsets, int E, int64_t R_cap, int64_t N,
                            int64_t K, float beta, void* dW, int out_dtype, void* stream);
 
+/* ---- f1: gate/up GEMM with SwiGLU + quantisation in its epilogue ------------
+ * The forward gate/up GEMM of mgq_grouped_gemm_fwd (A [R_cap, K], W1 [E, 2F, K]
+ * with the gate rows 0..F-1 and the up rows F..2F-1 of each expert) whose
+ * epilogue applies SwiGLU: for every row, g and u are the GEMM outputs rounded
+ * to bf16 (the values mgq_grouped_gemm_fwd writes), h = bf16(silu(g) u), and h
+ * is quantised row-wise into qh exactly as mgq_swiglu_quantize would quantise
+ * it (same codes, scales and amax). The tiles pair gate rows f.. with the up
+ * rows F + f.., so each tile holds both halves of 128 ffn columns.
+ *  scaling  MGQ_MX32_E8M0 or MGQ_TENSOR_F32 (qh->scaling must match; qh->col
+ *           must be NULL: no column-wise copy from the epilogue)
+ *  gu_bf16  [R_cap, 2F] receives g | u when not NULL (the backward's
+ *           dSwiGLU input); h_bf16 [R_cap, F] receives h when not NULL
+ * Requirements as mgq_grouped_gemm_fwd with N = 2F, F a multiple of 128.
+ * MGQ_ERR_UNSUPPORTED for other scalings. */
+int mgq_grouped_gemm_fwd_swiglu(const mgq_operand* A, const mgq_operand* W1, int scaling,
+                                const int32_t* offsets, int E, int64_t R_cap, int64_t F,
+                                int64_t K, const mgq_qdesc* qh, void* gu_bf16, void* h_bf16,
+                                void* stream);
+
 /* ---- a6/a10: SwiGLU and its derivative, fused with quantisation -------------
  * h = silu(g) * u, g = gu[:, :F], u = gu[:, F:2F] (float32, rounded to bf16,
  * then quantised). dG = dh u s (1 + g (1 - s)), dU = dh silu(g), s = sigmoid(g),

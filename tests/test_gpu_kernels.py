@@ -720,3 +720,62 @@ def test_amax_history_update(mgq):
             ref[i].update(a[i])
         assert np.array_equal(scale.cpu().numpy(), np.array([r.scale for r in ref], dtype=np.float32))
         assert torch.count_nonzero(amax).item() == 0
+
+
+@pytest.mark.parametrize("scaling", ["tensor", "mx"])
+def test_gemm_fwd_swiglu_equals_separate_steps(mgq, scaling):
+    """The gate/up GEMM with SwiGLU + quantisation in its epilogue writes the
+    same bytes as grouped_gemm_fwd followed by swiglu_quantize: g | u, h, the
+    h codes and scales, and the per-tensor amax (groups of 128 and 384 rows,
+    an empty group, pair tiles reaching past a group)."""
+    rng = np.random.default_rng(31)
+    dev = torch.device(DEV)
+    offs = np.array([0, 128, 128, 512, 640], dtype=np.int32)
+    E, F, K = 4, 384, 256
+    Rp = int(offs[-1])
+    R_cap = Rp + 128
+    offd = torch.from_numpy(offs).to(dev)
+    if scaling == "mx":
+        ac, asc = _mx_operand(rng, R_cap, K, sc_lo=118, sc_hi=124)
+        wc, wsc = _mx_operand(rng, E * 2 * F, K, sc_lo=118, sc_hi=124)
+        A = _op(mgq, ac, tile_mx_scales(asc), K, mgq.E4M3, dev)
+        W1 = _op(mgq, wc, tile_mx_scales(wsc), K, mgq.E4M3, dev)
+        sc = mgq.MX32_E8M0
+    else:
+        f4 = OF.E4M3
+        ac = (rng.choice(f4.pos_codes[:-1], size=(R_cap, K)) | (rng.integers(0, 2, (R_cap, K)) * 0x80)).astype(np.uint8)
+        wc = (rng.choice(f4.pos_codes[:-1], size=(E * 2 * F, K)) |
+              (rng.integers(0, 2, (E * 2 * F, K)) * 0x80)).astype(np.uint8)
+        A = _op(mgq, ac, np.array([64.0], dtype=np.float32), K, mgq.E4M3, dev)
+        W1 = _op(mgq, wc, np.array([40.0, 16.0, 8.0, 30.0], dtype=np.float32), K, mgq.E4M3, dev)
+        sc = mgq.TENSOR_F32
+
+    def outputs():
+        o = dict(gu=torch.full((R_cap, 2 * F), 3.0, dtype=torch.bfloat16, device=dev),
+                 h=torch.full((R_cap, F), 3.0, dtype=torch.bfloat16, device=dev),
+                 hq=torch.full((R_cap, F), 0xAB, dtype=torch.uint8, device=dev),
+                 hs=torch.full((mgq.mx_scale_bytes(R_cap, F),), 0xCD, dtype=torch.uint8, device=dev),
+                 ts=torch.tensor([2.5], device=dev), am=torch.zeros(1, device=dev))
+        if sc == mgq.MX32_E8M0:
+            o["q"] = mgq.qdesc(mgq.E4M3, sc, o["hq"], o["hs"])
+        else:
+            o["q"] = mgq.qdesc(mgq.E4M3, sc, o["hq"], None, None, None, o["ts"], o["am"])
+        return o
+
+    sep, fus = outputs(), outputs()
+    mgq.grouped_gemm_fwd(A, W1, sc, offd, E, R_cap, 2 * F, K, sep["gu"])
+    mgq.swiglu_quantize(sep["gu"], R_cap, F, offd, E, sep["q"], sep["h"])
+    mgq.grouped_gemm_fwd_swiglu(A, W1, sc, offd, E, R_cap, F, K, fus["q"], fus["gu"], fus["h"])
+    # without the optional outputs the codes are the same
+    bare = outputs()
+    mgq.grouped_gemm_fwd_swiglu(A, W1, sc, offd, E, R_cap, F, K, bare["q"])
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    for key in ("gu", "h", "hq", "hs", "am"):
+        assert torch.equal(sep[key], fus[key]), key
+    assert torch.equal(sep["hq"], bare["hq"]) and torch.equal(sep["am"], bare["am"])
+    assert torch.all(bare["gu"] == 3.0)
+    assert torch.all(fus["hq"][Rp:] == 0xAB)          # rows past the groups untouched
+    # and h against the oracle's SwiGLU of the GEMM output
+    gu = bf16_np(sep["gu"])[:Rp]
+    check_elementwise(OL.swiglu(gu, F), bf16_np(fus["h"])[:Rp], "swiglu")
