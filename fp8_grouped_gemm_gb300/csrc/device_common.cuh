@@ -39,6 +39,15 @@ __device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f 
 __device__ __forceinline__ float sigmoid_fast(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
 // h = bf16(silu(g) u)
 __device__ __forceinline__ float swiglu_bf16(float g, float u) { return round_bf16(__fmul_rn(silu_fast(g), u)); }
+// dSwiGLU of one element with s = sigmoid(g): dG = bf16(dh u s (1 + g (1 - s))),
+// dU = bf16(dh g s), every operation spelled out so no kernel contracts it
+// differently
+__device__ __forceinline__ void dswiglu_bf16(float d, float g, float u, float& dg, float& du) {
+  const float s = sigmoid_fast(g);
+  const float t = __fmaf_rn(g, __fsub_rn(1.0f, s), 1.0f);
+  dg = round_bf16(__fmul_rn(__fmul_rn(__fmul_rn(d, u), s), t));
+  du = round_bf16(__fmul_rn(__fmul_rn(d, g), s));
+}
 
 // ---------------------------------------------------------------------------
 // Saturating round-to-nearest-even casts (PTX cvt .rn.satfinite). The first

@@ -120,9 +120,7 @@ __global__ void __launch_bounds__(256) dswiglu_quant_kernel(DswigluArgs a) {
       load_bf16x32(a.gu + r * 2 * F + F + c, u);
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const float s = sigmoid_fast(g[i]);
-        dg[i] = round_bf16(d[i] * u[i] * s * (1.0f + g[i] * (1.0f - s)));
-        du[i] = round_bf16(d[i] * g[i] * s);
+        dswiglu_bf16(d[i], g[i], u[i], dg[i], du[i]);
       }
     } else {
 #pragma unroll

@@ -99,8 +99,13 @@ struct GemmParams {
   uint8_t* h_scales;  // MX: tiled E8M0 scales of [R_cap, F]
   const float* h_scale;  // per-tensor: the scale multiplying h
   float* h_amax;      // per-tensor: max |h| (atomically raised), or null
-  uint16_t* h_bf16;   // [R_cap, F] or null
+  uint16_t* h_bf16;   // [R_cap, F] or null (dSwiGLU: [R_cap, 2F])
   int h_dtype, h_rceil;
+  // dSwiGLU epilogue (down-projection dgrad, per-tensor): [dG | dU] from
+  // dh = bf16(acc) and the forward's g | u, quantised row-wise into h_codes
+  // [R_cap, 2F] with h_scale; dh itself only when `out` is set
+  int dswiglu;
+  const uint16_t* gu_in;   // [R_cap, 2F]
   int debug_stall;    // failure-detection test: the producer issues no loads, so
                       // every consumer wait runs out and reports MGQ_ERR_TIMEOUT
   uint64_t wait_ns;   // limit of every mbarrier wait
@@ -327,6 +332,114 @@ __device__ __forceinline__ void epilogue_swiglu(const GemmParams& p, const uint3
   for (int j = 0; j < 4; ++j) stage(j, make_uint4(hw[4 * j], hw[4 * j + 1], hw[4 * j + 2], hw[4 * j + 3]), tmH, f0);
   if (KIND == kKindMX)
     *reinterpret_cast<uint16_t*>(p.h_scales + tiled_scale_offset(orow, f0 / 32, p.F / 128)) = (uint16_t)sc2;
+}
+
+// g and u of 16 columns (col0 + 16 c ..) of one row of the forward's gu
+__device__ __forceinline__ void dswiglu_load_gu(const GemmParams& p, int64_t orow, int64_t col0, int c,
+                                                uint4 (&gq)[2], uint4 (&uq)[2]) {
+  const uint16_t* grow = p.gu_in + orow * 2 * p.F + col0 + 16 * c;
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    gq[q] = __ldg(reinterpret_cast<const uint4*>(grow) + q);
+    uq[q] = __ldg(reinterpret_cast<const uint4*>(grow + p.F) + q);
+  }
+}
+
+// dSwiGLU epilogue of the down-projection dgrad (per-tensor) for one thread's
+// row `orow` and columns col0..col0+127, in 8 chunks of 16: each reads its
+// accumulator columns from tensor memory (`tcol` = the first) and the matching
+// g and u of the forward's gu (chunk 0 already in gq / uq, requested by the
+// caller before the accumulator was ready; each further chunk is loaded when it is processed);
+// dh = bf16(acc * alpha), [dG | dU] = dswiglu_bf16, quantised with *p.h_scale
+// (max |.| into tam). Codes and (p.out set) dh go out through TMA stores from
+// the warp's staging buffer; the optional bf16 dG | dU by plain stores.
+// Warp-collective (tensor-memory loads).
+__device__ __forceinline__ void epilogue_dswiglu(const GemmParams& p, uint32_t tcol, float alpha, int64_t orow,
+                                                 int64_t col0, uint8_t* stg, const CUtensorMap* tmO,
+                                                 const CUtensorMap* tmH, int32_t y0, uint32_t lane, uint32_t& tam,
+                                                 uint4 (&gq)[2], uint4 (&uq)[2]) {
+  auto stage = [&](int j, uint4 v, const CUtensorMap* m, int64_t x) {
+    if (j == 0) {
+      if (lane == 0) ptx::bulk_wait_read0();
+      __syncwarp();
+    }
+    reinterpret_cast<uint4*>(stg + lane * 64)[j] = v;
+    if (j == 3) {
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::tma_store_2d(m, stg, (int32_t)x, y0);
+        ptx::bulk_commit();
+      }
+    }
+  };
+  const int64_t F = p.F;
+  const float ts = *p.h_scale;
+  const bool e5 = p.h_dtype == MGQ_E5M2;
+  uint32_t cg[16], cu[16];    // codes of four 16-column chunks: dG, dU
+  uint32_t dhw[16];           // dh of two chunks as bf16 pairs (the 64-byte rows of its stores)
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    if (c > 0) dswiglu_load_gu(p, orow, col0, c, gq, uq);
+    uint32_t v[16];
+    ptx::tmem_ld_32x32b_x16(tcol + 16 * c, v);
+    ptx::tmem_ld_wait();
+    float d[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) d[i] = round_bf16(__uint_as_float(v[i]) * alpha);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dhw[8 * (c & 1) + i] = pack_bf16x2(d[2 * i], d[2 * i + 1]);
+    if (p.out && (c & 1)) {   // dh: 32 columns at col0 + 16 (c - 1)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) stage(j, make_uint4(dhw[4 * j], dhw[4 * j + 1], dhw[4 * j + 2], dhw[4 * j + 3]),
+                                        tmO, col0 + 16 * (c - 1));
+    }
+    uint32_t dgp[8], dup[8];   // bf16 pairs (exact)
+    uint32_t am2 = 0;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint32_t gw[4] = {gq[q].x, gq[q].y, gq[q].z, gq[q].w};
+      const uint32_t uw[4] = {uq[q].x, uq[q].y, uq[q].z, uq[q].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int k = 8 * q + 2 * i;
+        float g0, g1, u0, u1;
+        dswiglu_bf16(d[k], bf16_lo(gw[i]), bf16_lo(uw[i]), g0, u0);
+        dswiglu_bf16(d[k + 1], bf16_hi(gw[i]), bf16_hi(uw[i]), g1, u1);
+        dgp[4 * q + i] = pack_bf16x2(g0, g1);
+        dup[4 * q + i] = pack_bf16x2(u0, u1);
+        am2 = absmax_bf16x2(absmax_bf16x2(am2, dgp[4 * q + i]), dup[4 * q + i]);
+      }
+    }
+    tam = max(tam, fold_bf16x2(am2));
+    if (p.h_bf16) {
+      uint4* og = reinterpret_cast<uint4*>(p.h_bf16 + orow * 2 * F + col0 + 16 * c);
+      uint4* ou = reinterpret_cast<uint4*>(p.h_bf16 + orow * 2 * F + F + col0 + 16 * c);
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        og[q] = make_uint4(dgp[4 * q], dgp[4 * q + 1], dgp[4 * q + 2], dgp[4 * q + 3]);
+        ou[q] = make_uint4(dup[4 * q], dup[4 * q + 1], dup[4 * q + 2], dup[4 * q + 3]);
+      }
+    }
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float a0 = __fmul_rn(bf16_lo(dgp[2 * w]), ts), a1 = __fmul_rn(bf16_hi(dgp[2 * w]), ts);
+      const float a2 = __fmul_rn(bf16_lo(dgp[2 * w + 1]), ts), a3 = __fmul_rn(bf16_hi(dgp[2 * w + 1]), ts);
+      const float b0 = __fmul_rn(bf16_lo(dup[2 * w]), ts), b1 = __fmul_rn(bf16_hi(dup[2 * w]), ts);
+      const float b2 = __fmul_rn(bf16_lo(dup[2 * w + 1]), ts), b3 = __fmul_rn(bf16_hi(dup[2 * w + 1]), ts);
+      cg[4 * (c & 3) + w] = e5 ? cvt_fp8x4<MGQ_E5M2>(a0, a1, a2, a3) : cvt_fp8x4<MGQ_E4M3>(a0, a1, a2, a3);
+      cu[4 * (c & 3) + w] = e5 ? cvt_fp8x4<MGQ_E5M2>(b0, b1, b2, b3) : cvt_fp8x4<MGQ_E4M3>(b0, b1, b2, b3);
+    }
+    if ((c & 3) == 3) {   // 64 columns of codes: dG at col0 + 16 (c - 3), dU F further
+#pragma unroll
+      for (int j = 0; j < 4; ++j) stage(j, make_uint4(cg[4 * j], cg[4 * j + 1], cg[4 * j + 2], cg[4 * j + 3]), tmH,
+                                        col0 + 16 * (c - 3));
+#pragma unroll
+      for (int j = 0; j < 4; ++j) stage(j, make_uint4(cu[4 * j], cu[4 * j + 1], cu[4 * j + 2], cu[4 * j + 3]), tmH,
+                                        F + col0 + 16 * (c - 3));
+    }
+
+  }
 }
 
 template <int MODE, int KIND>
@@ -586,6 +699,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!alive) break;
       } else {
         const uint32_t a = tc % kAcc, aph = (tc / kAcc) & 1;
+        uint4 gq[2], uq[2];    // dSwiGLU: the first g / u chunk, requested before the accumulator is ready
+        if (MODE == kModeRows && KIND == kKindTensor && p.dswiglu) dswiglu_load_gu(p, orow, col0, 0, gq, uq);
         // the whole warp agrees before the .sync.aligned tensor-memory loads
         if (__any_sync(0xFFFFFFFFu, *s_abort != 0)) break;
         const bool got = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&tmem_full[a], aph, p.wait_ns));
@@ -596,6 +711,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tc_fence_after();
         const uint32_t tbase = tmem + a * BN + ((q * 32) << 16);
+        if (MODE == kModeRows && KIND == kKindTensor && p.dswiglu) {
+          epilogue_dswiglu(p, tbase + half * (BN / 2), 1.0f / (p.sa[0] * p.sb[tl.e]), orow, col0,
+                           sOut + (warp - 2) * kStageOut, &tmO, &tmH, (int32_t)(tl.out_row + q * 32), lane, h_tam,
+                           gq, uq);
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(&tmem_empty[a]);
+          ++tc;
+          continue;
+        }
 #pragma unroll
         for (int c = 0; c < 4; ++c) ptx::tmem_ld_32x32b_x32(tbase + acc_col(MODE == kModeRows && p.swiglu, half, c), r[c]);
         ptx::tmem_ld_wait();
@@ -613,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         epilogue_store(p, r, alpha, orow, col0, p.tma_store != 0, sOut + (warp - 2) * kStageOut, &tmO,
                        (int32_t)(tl.out_row + q * 32), lane);
     }
-    if (MODE == kModeRows && KIND == kKindTensor && p.swiglu && p.h_amax) {
+    if (MODE == kModeRows && KIND == kKindTensor && (p.swiglu || p.dswiglu) && p.h_amax) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) h_tam = max(h_tam, __shfl_xor_sync(0xFFFFFFFFu, h_tam, o));
       if (lane == 0) atomic_max_nonneg(p.h_amax, __uint_as_float(h_tam));
@@ -925,6 +1049,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         continue;
       }
       const uint32_t a = tc % kAccBufs, aph = (tc / kAccBufs) & 1;
+      uint4 gq[2], uq[2];    // dSwiGLU: the first g / u chunk, requested before the accumulator is ready
+      if (MODE == kModeRows && KIND == kKindTensor && p.dswiglu && store) dswiglu_load_gu(p, orow, col0, 0, gq, uq);
       if (__any_sync(0xFFFFFFFFu, *s_abort != 0)) break;
       const bool got = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&tmem_full[a], aph, p.wait_ns));
       if (!got) {
@@ -933,8 +1059,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         break;
       }
       ptx::tc_fence_after();
-      uint32_t r[4][32];
       const uint32_t tbase = tmem + a * BN + ((q * 32) << 16);
+      if (MODE == kModeRows && KIND == kKindTensor && p.dswiglu) {
+        // tensor memory read chunk by chunk beside the gu loads, released after
+        // (the other accumulator buffer keeps the MMAs going meanwhile)
+        if (store)
+          epilogue_dswiglu(p, tbase + half * (BN / 2), 1.0f / (p.sa[0] * p.sb[tl.e]), orow, col0,
+                           sOut + (warp - 2) * kStageOut, &tmO, &tmH, (int32_t)(tl.out_row + 128 * rank + q * 32),
+                           lane, h_tam, gq, uq);
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive_cluster(a ? empty_remote1 : empty_remote0);
+        ++tc;
+        continue;
+      }
+      uint32_t r[4][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) ptx::tmem_ld_32x32b_x32(tbase + acc_col(MODE == kModeRows && p.swiglu, half, c), r[c]);
       ptx::tmem_ld_wait();
@@ -951,7 +1090,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         epilogue_store(p, r, alpha, orow, col0, p.tma_store != 0, sOut + (warp - 2) * kStageOut, &tmO,
                        (int32_t)(tl.out_row + 128 * rank + q * 32), lane);
     }
-    if (MODE == kModeRows && KIND == kKindTensor && p.swiglu && p.h_amax) {
+    if (MODE == kModeRows && KIND == kKindTensor && (p.swiglu || p.dswiglu) && p.h_amax) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) h_tam = max(h_tam, __shfl_xor_sync(0xFFFFFFFFu, h_tam, o));
       if (lane == 0) atomic_max_nonneg(p.h_amax, __uint_as_float(h_tam));
@@ -1046,14 +1185,20 @@ struct SwigluOut {
   const mgq_qdesc* qh;
   void* h_bf16;
 };
+// dSwiGLU epilogue request of the down-projection dgrad (N = F)
+struct DswigluOut {
+  const void* gu;
+  const mgq_qdesc* q;
+  void* dgu_bf16;
+};
 
 int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scaling, const int32_t* offsets, int E,
                 int64_t R_cap, int64_t N, int64_t K, float beta, void* out, int out_dtype, void* stream,
-                const SwigluOut* sw = nullptr) {
+                const SwigluOut* sw = nullptr, const DswigluOut* dsw = nullptr) {
   int rc;
   if ((rc = check_operand(A)) != MGQ_OK) return rc;
   if ((rc = check_operand(B)) != MGQ_OK) return rc;
-  MGQ_CHECK_ARG(offsets && (out || sw) && aligned16(out) && E >= 1 && E <= kMaxE && R_cap > 0 && R_cap % BM == 0);
+  MGQ_CHECK_ARG(offsets && (out || sw || dsw) && aligned16(out) && E >= 1 && E <= kMaxE && R_cap > 0 && R_cap % BM == 0);
   MGQ_CHECK_ARG(out_dtype == MGQ_OUT_BF16 || out_dtype == MGQ_OUT_F32);
   MGQ_CHECK_ARG(beta == 0.0f || (mode == kModeContract && out_dtype == MGQ_OUT_F32));
   MGQ_CHECK_ARG(R_cap < (1ll << 31));
@@ -1132,7 +1277,9 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
   p.h_bf16 = nullptr;
   p.h_dtype = MGQ_E4M3;
   p.h_rceil = 1;
-  CUtensorMap th = ta;    // SwiGLU codes map (unused otherwise)
+  p.dswiglu = 0;
+  p.gu_in = nullptr;
+  CUtensorMap th = ta;    // SwiGLU / dSwiGLU codes map (unused otherwise)
   if (sw) {
     // gate/up tiles: gate rows 128 n.. and up rows F + 128 n..; h quantised
     // row-wise with the GEMM's own scaling (MX or per-tensor)
@@ -1156,6 +1303,26 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
     p.h_dtype = qh->dtype;
     p.h_rceil = qh->e8m0_mode == MGQ_E8M0_RCEIL;
     if (!encode_tmap_2d(&th, qh->row.data, 1, (uint64_t)F, (uint64_t)R_cap, (uint64_t)F, 64, 32)) return MGQ_ERR_CUDA;
+  }
+  if (dsw) {
+    // down-projection dgrad (N = F output columns): [dG | dU] quantised
+    // row-wise per tensor into dsw->q ([R_cap, 2F] codes)
+    const mgq_qdesc* q = dsw->q;
+    if (mode != kModeRows || kind != kKindTensor || q->scaling != MGQ_TENSOR_F32 || q->col.data)
+      return MGQ_ERR_UNSUPPORTED;
+    if (q->dtype != MGQ_E4M3 && q->dtype != MGQ_E5M2) return MGQ_ERR_UNSUPPORTED;
+    MGQ_CHECK_ARG(q->row.data && aligned16(q->row.data) && q->tensor_scale && dsw->gu && aligned16(dsw->gu) &&
+                  aligned16(dsw->dgu_bf16) && N % 128 == 0 && out_dtype == MGQ_OUT_BF16);
+    p.dswiglu = 1;
+    p.F = N;
+    p.gu_in = static_cast<const uint16_t*>(dsw->gu);
+    p.h_codes = static_cast<uint8_t*>(q->row.data);
+    p.h_scale = q->tensor_scale;
+    p.h_amax = q->amax_out;
+    p.h_bf16 = static_cast<uint16_t*>(dsw->dgu_bf16);
+    p.h_dtype = q->dtype;
+    if (!encode_tmap_2d(&th, q->row.data, 1, (uint64_t)(2 * N), (uint64_t)R_cap, (uint64_t)(2 * N), 64, 32))
+      return MGQ_ERR_CUDA;
   }
   debug_knobs(&p.debug_stall, &p.wait_ns);
   p.idesc = nv   ? ptx::idesc_mxf4nvf4_ue4m3(BM, BN)
@@ -1254,6 +1421,16 @@ int mgq_grouped_gemm_wgrad(const mgq_operand* dYcol, const mgq_operand* Acol, in
                            int E, int64_t R_cap, int64_t N, int64_t K, float beta, void* dW, int out_dtype,
                            void* stream) {
   return run_grouped(kModeContract, dYcol, Acol, scaling, offsets, E, R_cap, N, K, beta, dW, out_dtype, stream);
+}
+
+int mgq_grouped_gemm_dgrad_dswiglu(const mgq_operand* dY, const mgq_operand* W2, int scaling,
+                                   const int32_t* offsets, int E, int64_t R_cap, int64_t H, int64_t F,
+                                   const void* gu_bf16, const mgq_qdesc* q, void* dh_bf16, void* dgu_bf16,
+                                   void* stream) {
+  if (!q) return MGQ_ERR_INVALID_ARG;
+  const DswigluOut dsw{gu_bf16, q, dgu_bf16};
+  return run_grouped(kModeRows, dY, W2, scaling, offsets, E, R_cap, F, H, 0.0f, dh_bf16, MGQ_OUT_BF16, stream,
+                     nullptr, &dsw);
 }
 
 int mgq_grouped_gemm_fwd_swiglu(const mgq_operand* A, const mgq_operand* W1, int scaling, const int32_t* offsets,

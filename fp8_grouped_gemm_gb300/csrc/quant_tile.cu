@@ -81,9 +81,7 @@ struct SrcDswiglu {
     load8_bf16(gu + r * 2 * F + F + f, u);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float s = sigmoid_fast(g[i]);
-      dg[i] = round_bf16(d[i] * u[i] * s * (1.0f + g[i] * (1.0f - s)));
-      du[i] = round_bf16(d[i] * g[i] * s);
+      dswiglu_bf16(d[i], g[i], u[i], dg[i], du[i]);
     }
     if (out) {
       store8_bf16(out + r * 2 * F + f, dg);

@@ -7,7 +7,9 @@ per-tensor recipe, of the backward step:
 forward:  moe_permute (+ quantise) -> grouped_gemm_fwd (gate/up) ->
           swiglu_quantize -> grouped_gemm_fwd (down) -> moe_unpermute
           (MXFP8 inference and the delayed recipe fuse the gate/up GEMM and
-          SwiGLU + quantise into grouped_gemm_fwd_swiglu)
+          SwiGLU + quantise into grouped_gemm_fwd_swiglu; the delayed recipe
+          also fuses the down dgrad and dSwiGLU + quantise into
+          grouped_gemm_dgrad_dswiglu)
 backward: moe_unpermute_bwd (+ quantise dY, dprobs) -> grouped_gemm_dgrad and
           grouped_gemm_wgrad (down) -> dswiglu_quantize -> grouped_gemm_dgrad
           and grouped_gemm_wgrad (gate/up) -> moe_permute_bwd
@@ -271,15 +273,24 @@ class ExpertLayer:
             # gate/up projection: dXp = dY1 W1 ; dW1 = dY1^T X
             d1 = (O(self.dy1q, s_dy1r, 2 * F, mgq.E5M2), O(self.w1col, s_w1c, 2 * F, mgq.E4M3))
             w1 = (O(self.dy1col, s_dy1c, R, mgq.E5M2), O(self.xcol, s_xc, R, mgq.E4M3))
-        return [
+        ops = [
             ("unpermute_bwd_quant", lambda: mgq.moe_unpermute_bwd(dout, self.y, self.row_id_map, self.src_row, probs,
                                                                   R, self.offsets, E, q2, self.dprobs, stream)),
-            ("gemm_dgrad_down", lambda: mgq.grouped_gemm_dgrad(*d2, sc, self.offsets, E, R, H, F, self.dh,
-                                                               mgq.OUT_BF16, stream)),
-            ("gemm_wgrad_down", lambda: mgq.grouped_gemm_wgrad(*w2, sc, self.offsets, E, R, H, F, self.dw2, 0.0,
-                                                               mgq.OUT_F32, stream)),
-            ("dswiglu_quant", lambda: mgq.dswiglu_quantize(self.dh, self.gu, R, F, self.offsets, E, q1,
-                                                           self.dgu_bf16, stream)),
+        ]
+        wgrad_down = ("gemm_wgrad_down", lambda: mgq.grouped_gemm_wgrad(*w2, sc, self.offsets, E, R, H, F, self.dw2,
+                                                                         0.0, mgq.OUT_F32, stream))
+        if self.fused_swiglu and self.delayed:
+            # dh only where a check reads it
+            dh = self.dh if self.keep_bf16 else None
+            ops += [("gemm_dgrad_down_dswiglu",
+                     lambda: mgq.grouped_gemm_dgrad_dswiglu(*d2, sc, self.offsets, E, R, H, F, self.gu, q1, dh,
+                                                            self.dgu_bf16, stream)), wgrad_down]
+        else:
+            ops += [("gemm_dgrad_down", lambda: mgq.grouped_gemm_dgrad(*d2, sc, self.offsets, E, R, H, F, self.dh,
+                                                                       mgq.OUT_BF16, stream)), wgrad_down,
+                    ("dswiglu_quant", lambda: mgq.dswiglu_quantize(self.dh, self.gu, R, F, self.offsets, E, q1,
+                                                                   self.dgu_bf16, stream))]
+        return ops + [
             ("gemm_dgrad_gateup", lambda: mgq.grouped_gemm_dgrad(*d1, sc, self.offsets, E, R, 2 * F, H, self.dxp,
                                                                  mgq.OUT_BF16, stream)),
             ("gemm_wgrad_gateup", lambda: mgq.grouped_gemm_wgrad(*w1, sc, self.offsets, E, R, 2 * F, H, self.dw1,
@@ -336,6 +347,8 @@ class ExpertLayer:
         wq = 2                                          # weights: rows (+ columns) in one pass each
         bwd = 1 + 2 + 1 + 2 + 1                         # unpermute_bwd, dgrad/wgrad, dswiglu (fused
                                                         # columns), dgrad/wgrad, permute_bwd
+        if self.fused_swiglu and self.delayed:
+            bwd -= 1                                    # dSwiGLU in the down dgrad epilogue
         if not self.mn:
             fwd += 1                                    # column copy of x (h's is fused into SwiGLU)
             bwd += 1                                    # column copy of dY2

@@ -31,7 +31,8 @@ FMAX = {E4M3: 448.0, E5M2: 57344.0}
 EXPORTS = (
     "mgq_status_string", "mgq_version", "mgq_get_error", "mgq_permute_workspace_size",
     "mgq_moe_permute", "mgq_moe_permute_noalloc", "mgq_block_quantize", "mgq_grouped_gemm_fwd", "mgq_grouped_gemm_dgrad",
-    "mgq_grouped_gemm_wgrad", "mgq_grouped_gemm_fwd_swiglu", "mgq_swiglu_quantize", "mgq_dswiglu_quantize", "mgq_moe_unpermute",
+    "mgq_grouped_gemm_wgrad", "mgq_grouped_gemm_fwd_swiglu",
+    "mgq_grouped_gemm_dgrad_dswiglu", "mgq_swiglu_quantize", "mgq_dswiglu_quantize", "mgq_moe_unpermute",
     "mgq_moe_unpermute_bwd", "mgq_moe_permute_bwd", "mgq_amax_history_update",
 )
 
@@ -84,6 +85,7 @@ def load() -> ctypes.CDLL:
         lib.mgq_grouped_gemm_dgrad.argtypes = gemm + [vp, i32, vp]
         lib.mgq_grouped_gemm_wgrad.argtypes = gemm + [ctypes.c_float, vp, i32, vp]
         lib.mgq_grouped_gemm_fwd_swiglu.argtypes = gemm + [P(QDesc), vp, vp, vp]
+        lib.mgq_grouped_gemm_dgrad_dswiglu.argtypes = gemm + [vp, P(QDesc), vp, vp, vp]
         lib.mgq_swiglu_quantize.argtypes = [vp, i64, i32, vp, i32, P(QDesc), vp, vp]
         lib.mgq_dswiglu_quantize.argtypes = [vp, vp, i64, i32, vp, i32, P(QDesc), vp, vp]
         lib.mgq_moe_unpermute.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
@@ -218,6 +220,15 @@ def grouped_gemm_fwd_swiglu(A: Operand, W1: Operand, scaling, offsets, E, R_cap,
     _check(load().mgq_grouped_gemm_fwd_swiglu(ctypes.byref(A), ctypes.byref(W1), scaling, _p(offsets), E, R_cap,
                                               F, K, ctypes.byref(qh), _p(gu), _p(h), _s(stream)),
            "mgq_grouped_gemm_fwd_swiglu")
+
+
+def grouped_gemm_dgrad_dswiglu(dY: Operand, W2: Operand, scaling, offsets, E, R_cap, H, F, gu, q: QDesc, dh=None,
+                               dgu=None, stream=None):
+    """Down-projection dgrad with dSwiGLU + row-wise quantisation of [dG | dU]
+    in its epilogue (dh [R_cap, F] and dgu [R_cap, 2F] bf16 only when given)."""
+    _check(load().mgq_grouped_gemm_dgrad_dswiglu(ctypes.byref(dY), ctypes.byref(W2), scaling, _p(offsets), E,
+                                                 R_cap, H, F, _p(gu), ctypes.byref(q), _p(dh), _p(dgu), _s(stream)),
+           "mgq_grouped_gemm_dgrad_dswiglu")
 
 
 def swiglu_quantize(gu, R_cap, F, offsets, E, q: QDesc, h_out=None, stream=None):

@@ -262,6 +262,22 @@ int mgq_grouped_gemm_fwd_swiglu(const mgq_operand* A, const mgq_operand* W1, int
                                 int64_t K, const mgq_qdesc* qh, void* gu_bf16, void* h_bf16,
                                 void* stream);
 
+/* ---- f1: down-projection dgrad with dSwiGLU + quantisation in its epilogue --
+ * The dgrad of the down projection (as mgq_grouped_gemm_dgrad with N = H and
+ * K = F: dh = dY W2_e, dY [R_cap, H], W2 as the Wcol operand there or the
+ * forward weight [E, H, F] with MGQ_LAYOUT_MN) whose epilogue rounds dh to
+ * bf16 and applies the SwiGLU derivative with the forward's gu_bf16 [R_cap, 2F]
+ * (g | u), then quantises [dG | dU] row-wise into q exactly as
+ * mgq_dswiglu_quantize would (same codes and amax).
+ *  scaling  MGQ_TENSOR_F32 only (q->scaling too; q->col must be NULL)
+ *  dh_bf16  [R_cap, F] receives dh when not NULL; dgu_bf16 [R_cap, 2F]
+ *           receives dG | dU when not NULL
+ * MGQ_ERR_UNSUPPORTED for other scalings. */
+int mgq_grouped_gemm_dgrad_dswiglu(const mgq_operand* dY, const mgq_operand* W2, int scaling,
+                                   const int32_t* offsets, int E, int64_t R_cap, int64_t H,
+                                   int64_t F, const void* gu_bf16, const mgq_qdesc* q,
+                                   void* dh_bf16, void* dgu_bf16, void* stream);
+
 /* ---- a6/a10: SwiGLU and its derivative, fused with quantisation -------------
  * h = silu(g) * u, g = gu[:, :F], u = gu[:, F:2F] (float32, rounded to bf16,
  * then quantised). dG = dh u s (1 + g (1 - s)), dU = dh silu(g), s = sigmoid(g),

@@ -779,3 +779,53 @@ def test_gemm_fwd_swiglu_equals_separate_steps(mgq, scaling):
     # and h against the oracle's SwiGLU of the GEMM output
     gu = bf16_np(sep["gu"])[:Rp]
     check_elementwise(OL.swiglu(gu, F), bf16_np(fus["h"])[:Rp], "swiglu")
+
+
+@pytest.mark.parametrize("w_layout", ["mn_major", "k_major"])
+def test_gemm_dgrad_dswiglu_equals_separate_steps(mgq, w_layout):
+    """The down-projection dgrad with dSwiGLU + quantisation in its epilogue
+    writes the same bytes as grouped_gemm_dgrad followed by dswiglu_quantize
+    (W2 read MN-major or as its column-wise copy, per-tensor e5m2 gradients,
+    an empty group, pair tiles reaching past a group)."""
+    rng = np.random.default_rng(37)
+    dev = torch.device(DEV)
+    offs = np.array([0, 128, 128, 512, 640], dtype=np.int32)
+    E, H, F = 4, 256, 512
+    Rp = int(offs[-1])
+    R_cap = Rp + 128
+    offd = torch.from_numpy(offs).to(dev)
+    f5, f4 = OF.E5M2, OF.E4M3
+    dyc = (rng.choice(f5.pos_codes[:-1], size=(R_cap, H)) | (rng.integers(0, 2, (R_cap, H)) * 0x80)).astype(np.uint8)
+    wc = (rng.choice(f4.pos_codes[:-1], size=(E, H, F)) | (rng.integers(0, 2, (E, H, F)) * 0x80)).astype(np.uint8)
+    dY = _op(mgq, dyc, np.array([2048.0], dtype=np.float32), H, mgq.E5M2, dev)
+    s_w = np.array([40.0, 16.0, 8.0, 30.0], dtype=np.float32)
+    if w_layout == "mn_major":
+        W2 = _op(mgq, wc, s_w, F, mgq.E4M3, dev)
+        W2.layout = mgq.LAYOUT_MN
+    else:
+        W2 = _op(mgq, np.ascontiguousarray(wc.transpose(0, 2, 1)), s_w, H, mgq.E4M3, dev)   # [E, F, H]
+    gu = (torch.randn(R_cap, 2 * F, device=dev) * 2).to(torch.bfloat16)
+
+    def outputs():
+        o = dict(dh=torch.full((R_cap, F), 3.0, dtype=torch.bfloat16, device=dev),
+                 dgu=torch.full((R_cap, 2 * F), 3.0, dtype=torch.bfloat16, device=dev),
+                 q=torch.full((R_cap, 2 * F), 0xAB, dtype=torch.uint8, device=dev),
+                 ts=torch.tensor([5000.0], device=dev), am=torch.zeros(1, device=dev))
+        o["qd"] = mgq.qdesc(mgq.E5M2, mgq.TENSOR_F32, o["q"], None, None, None, o["ts"], o["am"])
+        return o
+
+    sep, fus, bare = outputs(), outputs(), outputs()
+    sc = mgq.TENSOR_F32
+    mgq.grouped_gemm_dgrad(dY, W2, sc, offd, E, R_cap, H, F, sep["dh"])
+    mgq.dswiglu_quantize(sep["dh"], gu, R_cap, F, offd, E, sep["qd"], sep["dgu"])
+    mgq.grouped_gemm_dgrad_dswiglu(dY, W2, sc, offd, E, R_cap, H, F, gu, fus["qd"], fus["dh"], fus["dgu"])
+    mgq.grouped_gemm_dgrad_dswiglu(dY, W2, sc, offd, E, R_cap, H, F, gu, bare["qd"])
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    for key in ("dh", "dgu", "q", "am"):
+        assert torch.equal(sep[key][:Rp] if key != "am" else sep[key], fus[key][:Rp] if key != "am" else fus[key]), key
+    assert torch.equal(sep["q"][:Rp], bare["q"][:Rp]) and torch.equal(sep["am"], bare["am"])
+    assert torch.all(bare["dh"] == 3.0)
+    assert torch.all(fus["q"][Rp:] == 0xAB)
+    # and dSwiGLU against the oracle
+    check_elementwise(OL.dswiglu(bf16_np(sep["dh"])[:Rp], bf16_np(gu)[:Rp], F), bf16_np(fus["dgu"])[:Rp], "dswiglu")
