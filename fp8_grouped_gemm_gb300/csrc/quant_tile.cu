@@ -25,11 +25,17 @@ constexpr int TR = 128, TC = 128;  // tile rows x columns (per part)
 
 // kExactBf16: every value the source produces is a bf16 value, so the tile
 // keeps it as 2 bytes in shared memory.
+// kRaw: the source hands out its bf16 bits unchanged (load_raw), so the tile
+// is filled by 16-byte copies with all loads of a thread in flight at once.
 struct SrcPlain {
   static constexpr int kParts = 1;
   static constexpr bool kExactBf16 = true;
+  static constexpr bool kRaw = true;
   const uint16_t* x;
   int64_t ld;
+  __device__ __forceinline__ uint4 load_raw(int64_t r, int64_t c) const {
+    return __ldg(reinterpret_cast<const uint4*>(x + r * ld + c));
+  }
   __device__ __forceinline__ void load8(int64_t r, int64_t c, float* v, float*) const {
     const uint4 w = __ldg(reinterpret_cast<const uint4*>(x + r * ld + c));
     v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
@@ -51,6 +57,7 @@ __device__ __forceinline__ void store8_bf16(uint16_t* p, const float* v) {
 struct SrcSwiglu {
   static constexpr int kParts = 1;
   static constexpr bool kExactBf16 = true;
+  static constexpr bool kRaw = false;
   const uint16_t* gu;
   int64_t F;
   uint16_t* h_out;
@@ -70,6 +77,7 @@ struct SrcSwiglu {
 struct SrcDswiglu {
   static constexpr int kParts = 2;
   static constexpr bool kExactBf16 = true;
+  static constexpr bool kRaw = false;
   const uint16_t* dh;
   const uint16_t* gu;
   int64_t F;
@@ -95,10 +103,15 @@ struct SrcDswiglu {
 struct SrcGatherX {
   static constexpr int kParts = 1;
   static constexpr bool kExactBf16 = true;
+  static constexpr bool kRaw = true;
   const uint16_t* x;
   const int32_t* src_row;
   int k;
   int64_t H;
+  __device__ __forceinline__ uint4 load_raw(int64_t r, int64_t c) const {
+    const int e = src_row[r];
+    return e < 0 ? make_uint4(0, 0, 0, 0) : __ldg(reinterpret_cast<const uint4*>(x + (int64_t)(e / k) * H + c));
+  }
   __device__ __forceinline__ void load8(int64_t r, int64_t c, float* v, float*) const {
     const int e = src_row[r];
     if (e < 0) {
@@ -115,6 +128,7 @@ struct SrcGatherX {
 struct SrcGatherDy {
   static constexpr int kParts = 1;
   static constexpr bool kExactBf16 = false;   // float32 products
+  static constexpr bool kRaw = false;
   const uint16_t* dout;
   const float* probs;
   const int32_t* src_row;
@@ -153,13 +167,13 @@ struct RowColArgs {
 template <bool B16> struct TileT;
 template <> struct TileT<true> {
   using T = uint16_t;
-  static constexpr int kPad = 2;
+  static constexpr int kPad = 8;             // rows stay 16-byte aligned
   __device__ static T put(float v) { return (T)(__float_as_uint(v) >> 16); }
   __device__ static float get(T v) { return __uint_as_float((uint32_t)v << 16); }
 };
 template <> struct TileT<false> {
   using T = float;
-  static constexpr int kPad = 1;
+  static constexpr int kPad = 4;             // rows stay 16-byte aligned
   __device__ static T put(float v) { return v; }
   __device__ static float get(T v) { return v; }
 };
@@ -170,7 +184,8 @@ constexpr size_t rowcol_smem() {
 }
 
 template <class Src, int SC, int DT>
-__global__ void __launch_bounds__(256) quant_rowcol_kernel(const Src src, const RowColArgs a) {
+__global__ void __launch_bounds__(256, (Src::kParts == 2 || !Src::kExactBf16) ? 3 : 4)
+    quant_rowcol_kernel(const Src src, const RowColArgs a) {
   using TT = TileT<Src::kExactBf16>;
   using T = typename TT::T;
   constexpr int P = Src::kParts;
@@ -187,6 +202,25 @@ __global__ void __launch_bounds__(256) quant_rowcol_kernel(const Src src, const 
   const float ts = (SC == MGQ_TENSOR_F32) ? a.tensor_scale[g] : 1.0f;
   // ---- load: TR rows x 16 chunks of 8 columns, 8 chunks per thread
   uint32_t am = 0;
+  if constexpr (Src::kRaw) {
+    // all eight 16-byte loads in flight, then copied into the tile as they are
+    uint4 w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int chunk = tid + 256 * i;
+      const int rr = chunk >> 4, cc = (chunk & 15) * 8;
+      w[i] = (r0 + rr < nrows) ? src.load_raw(r0 + rr, c0 + cc) : make_uint4(0, 0, 0, 0);
+    }
+    uint32_t am2 = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int chunk = tid + 256 * i;
+      const int rr = chunk >> 4, cc = (chunk & 15) * 8;
+      am2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(am2, w[i].x), w[i].y), w[i].z), w[i].w);
+      *reinterpret_cast<uint4*>(&tile[rr * LD + cc]) = w[i];
+    }
+    am = fold_bf16x2(am2);
+  } else {
 #pragma unroll 4
   for (int i = 0; i < 8; ++i) {
     const int chunk = tid + 256 * i;
@@ -207,66 +241,115 @@ __global__ void __launch_bounds__(256) quant_rowcol_kernel(const Src src, const 
       for (int j = 0; j < 8; ++j) tile[(p * TR + rr) * LD + cc + j] = TT::put(v[p][j]);
     }
   }
-  __syncthreads();
-  // ---- row-wise: the P*TR (part, row) pairs, P*16 per warp; lane l takes columns 4l..4l+3
-  for (int pr = warp * P * 16; a.row_codes && pr < (warp + 1) * P * 16; ++pr) {
-    const int p = pr / TR, rr = pr % TR;
-    const int64_t r = r0 + rr;
-    const int64_t cb = c0 + p * a.part_off;       // first output column of this part
-    float v[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) v[j] = TT::get(tile[(p * TR + rr) * LD + 4 * lane + j]);
-    float mult = ts;
-    uint32_t scode = 0;
-    if (SC == MGQ_MX32_E8M0) {
-      uint32_t m = absmax_bits_f32(v, 4);          // block of 32 = 8 lanes
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-      const int e = mx_exponent(m, FmtInfo<DT>::emax, a.rceil != 0);
-      mult = mx_multiplier(e);
-      scode = mx_scale_code(e);
-    }
-    const uint32_t w = cvt_fp8x4<DT>(__fmul_rn(v[0], mult), __fmul_rn(v[1], mult), __fmul_rn(v[2], mult),
-                                     __fmul_rn(v[3], mult));
-    if (SC == MGQ_MX32_E8M0) {
-      // the 4 block scales of this row segment (lanes 0, 8, 16, 24) into lane 0
-      const uint32_t s1 = __shfl_sync(0xFFFFFFFFu, scode, 8), s2 = __shfl_sync(0xFFFFFFFFu, scode, 16),
-                     s3 = __shfl_sync(0xFFFFFFFFu, scode, 24);
-      if (lane == 0 && r < nrows)
-        *reinterpret_cast<uint32_t*>(a.row_scales + tiled_scale_offset(r, cb / 32, a.C / 128)) =
-            scode | (s1 << 8) | (s2 << 16) | (s3 << 24);
-    }
-    if (r < nrows) *reinterpret_cast<uint32_t*>(a.row_codes + r * a.C + cb + 4 * lane) = w;
   }
-  // ---- column-wise: thread t takes column t % 128 and 128 / (3 - P) rows: the
-  // half t / 128 of the tile (one part) or all rows of part t / 128 (two
-  // parts); each 32-row block is one MX block and 32 contiguous output bytes
-  if (a.col_codes) {
-    const int cc = tid & 127, sel = tid >> 7;
-    const int p = P == 2 ? sel : 0, rbase = P == 2 ? 0 : (TR / 2) * sel;
-    constexpr int NB = P == 2 ? TR / 32 : TR / 64;        // 32-row blocks per thread
-    const int64_t crow = g * a.C + c0 + p * a.part_off + cc;   // row of the column-wise output
-#pragma unroll 1
-    for (int b = 0; b < NB; ++b) {
-      float v[32];
+  __syncthreads();
+  // ---- row-wise: the P*TR (part, row) pairs, 4 per warp at a time; 8 lanes
+  // per row, lane takes 16 columns (half an MX block: the pair l, l^1 shares one)
+  {
+    const int seg = lane & 7;
+    for (int pr0 = warp * P * 16; a.row_codes && pr0 < (warp + 1) * P * 16; pr0 += 4) {
+      const int pr = pr0 + (int)(lane >> 3);
+      const int p = pr / TR, rr = pr % TR;
+      const int64_t r = r0 + rr;
+      const int64_t cb = c0 + p * a.part_off;     // first output column of this part
+      float v[16];
+      const T* src = &tile[(p * TR + rr) * LD + 16 * seg];
+      if constexpr (Src::kExactBf16) {
+        const uint4 w0 = reinterpret_cast<const uint4*>(src)[0], w1 = reinterpret_cast<const uint4*>(src)[1];
+        const uint32_t ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = TT::get(tile[(p * TR + rbase + 32 * b + i) * LD + cc]);
-      float mult = ts;
-      const int64_t rg = r0 - g * a.M + rbase + 32 * b;   // row inside the group
-      if (SC == MGQ_MX32_E8M0) {
-        const int e = mx_exponent(absmax_bits_f32(v, 32), FmtInfo<DT>::emax, a.rceil != 0);
-        mult = mx_multiplier(e);
-        a.col_scales[tiled_scale_offset(crow, rg / 32, a.M / 128)] = (uint8_t)mx_scale_code(e);
+        for (int i = 0; i < 8; ++i) {
+          v[2 * i] = bf16_lo(ww[i]);
+          v[2 * i + 1] = bf16_hi(ww[i]);
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 f = reinterpret_cast<const float4*>(src)[q];
+          v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
+        }
       }
-      uint32_t cw[8];
+      float mult = ts;
+      uint32_t scode = 0;
+      if (SC == MGQ_MX32_E8M0) {
+        uint32_t m = absmax_bits_f32(v, 16);
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));        // the other half of the block
+        const int e = mx_exponent(m, FmtInfo<DT>::emax, a.rceil != 0);
+        mult = mx_multiplier(e);
+        scode = mx_scale_code(e);
+      }
+      uint32_t cw[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < 4; ++i)
         cw[i] = cvt_fp8x4<DT>(__fmul_rn(v[4 * i], mult), __fmul_rn(v[4 * i + 1], mult),
                               __fmul_rn(v[4 * i + 2], mult), __fmul_rn(v[4 * i + 3], mult));
-      uint4* dst = reinterpret_cast<uint4*>(a.col_codes + crow * a.M + rg);
-      dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-      dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+      if (SC == MGQ_MX32_E8M0) {
+        // the row's 4 block scales (lanes seg 0, 2, 4, 6 of its 8) into seg 0
+        const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, scode, 2), s2 = __shfl_down_sync(0xFFFFFFFFu, scode, 4),
+                       s3 = __shfl_down_sync(0xFFFFFFFFu, scode, 6);
+        if (seg == 0 && r < nrows)
+          *reinterpret_cast<uint32_t*>(a.row_scales + tiled_scale_offset(r, cb / 32, a.C / 128)) =
+              scode | (s1 << 8) | (s2 << 16) | (s3 << 24);
+      }
+      if (r < nrows)
+        *reinterpret_cast<uint4*>(a.row_codes + r * a.C + cb + 16 * seg) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+    }
+  }
+  // ---- column-wise: thread takes 2 adjacent columns of one 32-row block (one
+  // MX block each); its 32 output bytes per column are contiguous
+  if (a.col_codes) {
+    const int cp = tid & 63, rb = (tid >> 6) & 3;
+#pragma unroll 1
+    for (int p = 0; p < P; ++p) {
+      const int cc = 2 * cp;
+      const int64_t crow = g * a.C + c0 + p * a.part_off + cc;  // row of the column-wise output
+      const int64_t rg = r0 - g * a.M + 32 * rb;                // row inside the group
+      // the two columns' 32 values: bf16 pairs (exact sources) or floats
+      uint32_t w[32];
+      float v0[Src::kExactBf16 ? 1 : 32], v1[Src::kExactBf16 ? 1 : 32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const T* src = &tile[(p * TR + 32 * rb + i) * LD + cc];
+        if constexpr (Src::kExactBf16) {
+          w[i] = *reinterpret_cast<const uint32_t*>(src);
+        } else {
+          const float2 f = *reinterpret_cast<const float2*>(src);
+          v0[i] = f.x;
+          v1[i] = f.y;
+        }
+      }
+      uint32_t amh[2];
+      if constexpr (Src::kExactBf16) {
+        uint32_t m2 = 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) m2 = absmax_bf16x2(m2, w[i]);
+        amh[0] = m2 << 16;
+        amh[1] = m2 & 0xFFFF0000u;
+      } else {
+        amh[0] = absmax_bits_f32(v0, 32);
+        amh[1] = absmax_bits_f32(v1, 32);
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        auto val = [&](int i) {
+          if constexpr (Src::kExactBf16) return h ? bf16_hi(w[i]) : bf16_lo(w[i]);
+          else return h ? v1[i] : v0[i];
+        };
+        float mult = ts;
+        if (SC == MGQ_MX32_E8M0) {
+          const int e = mx_exponent(amh[h], FmtInfo<DT>::emax, a.rceil != 0);
+          mult = mx_multiplier(e);
+          a.col_scales[tiled_scale_offset(crow + h, rg / 32, a.M / 128)] = (uint8_t)mx_scale_code(e);
+        }
+        uint32_t cw[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          cw[i] = cvt_fp8x4<DT>(__fmul_rn(val(4 * i), mult), __fmul_rn(val(4 * i + 1), mult),
+                                __fmul_rn(val(4 * i + 2), mult), __fmul_rn(val(4 * i + 3), mult));
+        uint4* dst = reinterpret_cast<uint4*>(a.col_codes + (crow + h) * a.M + rg);
+        dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+      }
     }
   }
   if (SC == MGQ_TENSOR_F32 && a.amax_out) {
