@@ -535,6 +535,16 @@ int check_q(const mgq_qdesc* q) {
 
 }  // namespace
 
+// NVFP4 row-wise quantisation of a bf16 matrix whose amax is already in
+// *amax (s_g written to *s_out): the second pass of the fused SwiGLU GEMM
+int launch_quant_rows_nv(const uint16_t* x, int64_t rows, const int32_t* rows_used, int64_t K, uint8_t* codes,
+                         uint8_t* scales, const float* amax, float* s_out, cudaStream_t s) {
+  QuantRowsNvArgs a{x, rows, rows, K, rows_used, codes, scales, amax, s_out};
+  quant_rows_nv_kernel<<<(unsigned)((rows + kWarps - 1) / kWarps), 256, 0, s>>>(a);
+  MGQ_LAUNCH_CHECK();
+  return MGQ_OK;
+}
+
 int launch_amax_groups(const uint16_t* x, int64_t per_group, int64_t G, float* amax, cudaStream_t s) {
   if (cudaMemsetAsync(amax, 0, (size_t)G * sizeof(float), s) != cudaSuccess) return MGQ_ERR_CUDA;
   int64_t blocks = (per_group + 256 * 8 * 8 - 1) / (256 * 8 * 8);     // >= 8 loads per thread

@@ -48,9 +48,12 @@ constexpr uint32_t kABytes = BM * BK, kBBytes = BN * BK;
 __host__ __device__ constexpr uint32_t sf_stage_bytes(int kind) {
   return kind == 0 ? 3 * 512u : kind == 3 ? 3 * 2048u : 0u;
 }
-// epilogue staging for TMA stores: 8 warps x 32 rows x 64 bytes
+// epilogue staging for TMA stores: per warp 32 rows x 64 bytes, in two slots
+// for NVFP4 (whose short contractions leave little mainloop to hide each
+// store's read-out behind; the other kinds have no shared memory to spare)
 constexpr uint32_t kStageOut = 32 * 64;
-__host__ __device__ constexpr uint32_t staging_bytes(int) { return 8 * kStageOut; }
+__host__ __device__ constexpr uint32_t staging_slots(int kind) { return kind == 3 ? 2u : 1u; }
+__host__ __device__ constexpr uint32_t staging_bytes(int kind) { return 8 * kStageOut * staging_slots(kind); }
 // pipeline depth: NVFP4's larger scale chunks leave room for 3 stages next to
 // the staging buffers (its 128-byte stages hold 256 elements of K)
 __host__ __device__ constexpr int stages_of(int kind) { return kind == 3 ? 3 : STAGES; }
@@ -159,31 +162,49 @@ __device__ __forceinline__ bool get_tile(const int32_t* s_off, int E, const Gemm
   return true;
 }
 
+// A warp's TMA-store staging: `nslots` buffers of 32 rows x 64 bytes used in
+// turn. A row of `rowbytes` (32 or 64) per lane is filled 16 bytes at a time;
+// after its last piece the whole 32-row box goes out as one TMA store. Before a
+// buffer is refilled, the store that last used it has finished reading it.
+// Every lane of the warp calls put (the counter stays warp-uniform).
+struct Stager {
+  uint8_t* base;
+  uint32_t nslots;
+  uint32_t n;
+  __device__ __forceinline__ void put(uint32_t lane, int j, uint4 v, const CUtensorMap* m, int64_t x, int32_t y,
+                                      int rowbytes) {
+    uint8_t* buf = base + (nslots > 1 ? (n & 1u) * kStageOut : 0u);
+    if (j == 0) {
+      if (lane == 0) {
+        if (nslots > 1) ptx::bulk_wait_read1();
+        else ptx::bulk_wait_read0();
+      }
+      __syncwarp();
+    }
+    reinterpret_cast<uint4*>(buf + lane * rowbytes)[j] = v;
+    if (j == rowbytes / 16 - 1) {
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::tma_store_2d(m, buf, (int32_t)x, y);
+        ptx::bulk_commit();
+      }
+      ++n;
+    }
+  }
+};
+
 // Stores one thread's 128 accumulator columns (its row `orow`, columns col0..)
 // scaled by alpha: through TMA (the warp stages 32 rows x 64 bytes at a time in
 // `stg`; whole lines reach memory) or, when accumulating into float32 (beta) or
 // without staging, directly from registers.
 __device__ __forceinline__ void epilogue_store(const GemmParams& p, const uint32_t (&r)[4][32], float alpha,
-                                               int64_t orow, int64_t col0, bool use_tma, uint8_t* stg,
+                                               int64_t orow, int64_t col0, bool use_tma, Stager& sg,
                                                const CUtensorMap* tmO, int32_t y0, uint32_t lane) {
   if (use_tma) {
     // 64-byte column chunks: 8 (float32) or 4 (bf16); fully unrolled so the
     // accumulator registers are indexed statically
-    auto put = [&](int ch, int j, uint4 v, int ncols) {
-      if (j == 0) {
-        if (lane == 0) ptx::bulk_wait_read0();   // previous chunk read out of the buffer
-        __syncwarp();
-      }
-      reinterpret_cast<uint4*>(stg + lane * 64)[j] = v;
-      if (j == 3) {
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          ptx::tma_store_2d(tmO, stg, (int32_t)(col0 + ch * ncols), y0);
-          ptx::bulk_commit();
-        }
-      }
-    };
+    auto put = [&](int ch, int j, uint4 v, int ncols) { sg.put(lane, j, v, tmO, col0 + ch * ncols, y0, 64); };
     if (p.out_f32) {
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch)
@@ -260,24 +281,9 @@ __device__ __forceinline__ uint32_t acc_col(int swiglu, uint32_t half, int c) {
 // buffer; MX scales and the optional bf16 h by plain stores.
 template <int KIND>
 __device__ __forceinline__ void epilogue_swiglu(const GemmParams& p, const uint32_t (&r)[4][32], float alpha,
-                                                int64_t orow, int64_t f0, uint8_t* stg, const CUtensorMap* tmO,
+                                                int64_t orow, int64_t f0, Stager& sg, const CUtensorMap* tmO,
                                                 const CUtensorMap* tmH, int32_t y0, uint32_t lane, uint32_t& tam) {
-  // one 64-byte row per lane in the staging buffer, stored as 32 rows x 64 bytes
-  auto stage = [&](int j, uint4 v, const CUtensorMap* m, int64_t x) {
-    if (j == 0) {
-      if (lane == 0) ptx::bulk_wait_read0();
-      __syncwarp();
-    }
-    reinterpret_cast<uint4*>(stg + lane * 64)[j] = v;
-    if (j == 3) {
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        ptx::tma_store_2d(m, stg, (int32_t)x, y0);
-        ptx::bulk_commit();
-      }
-    }
-  };
+  auto stage = [&](int j, uint4 v, const CUtensorMap* m, int64_t x) { sg.put(lane, j, v, m, x, y0, 64); };
   auto bf = [&](uint32_t bits) { return round_bf16(__uint_as_float(bits) * alpha); };
   if (p.out) {
     // g and u as bf16: columns f0 + 32c and F + f0 + 32c of [R_cap, 2F]
@@ -292,7 +298,7 @@ __device__ __forceinline__ void epilogue_swiglu(const GemmParams& p, const uint3
               tmO, (c < 2 ? 0 : p.F) + f0 + 32 * (c & 1));
       }
   }
-  const float ts = KIND == kKindTensor ? *p.h_scale : 1.0f;
+  const float ts = KIND == kKindTensor ? *p.h_scale : 1.0f;   // (NVFP4: h_scale receives s_g later)
   const bool e5 = p.h_dtype == MGQ_E5M2;
   uint32_t hw[16];        // the 64 codes
   uint32_t sc2 = 0;       // MX: the two block scales
@@ -307,31 +313,42 @@ __device__ __forceinline__ void epilogue_swiglu(const GemmParams& p, const uint3
       hp[i] = pack_bf16x2(h0, h1);
       am2 = absmax_bf16x2(am2, hp[i]);
     }
-    if (p.h_bf16) {
-      uint4* d = reinterpret_cast<uint4*>(p.h_bf16 + orow * p.F + f0 + 32 * c);
+    if (KIND == kKindNV) {
+      // NVFP4 needs the amax of all of h before any block is cast: h goes out
+      // in bf16 (tmH maps h_bf16) for the second pass, and into tam
 #pragma unroll
-      for (int q = 0; q < 4; ++q) d[q] = make_uint4(hp[4 * q], hp[4 * q + 1], hp[4 * q + 2], hp[4 * q + 3]);
-    }
-    const uint32_t am = fold_bf16x2(am2);
-    float mult = ts;
-    if (KIND == kKindMX) {
-      const int e = mx_exponent(am, e5 ? FmtInfo<MGQ_E5M2>::emax : FmtInfo<MGQ_E4M3>::emax, p.h_rceil != 0);
-      mult = mx_multiplier(e);
-      sc2 |= mx_scale_code(e) << (8 * c);
+      for (int q = 0; q < 4; ++q) stage(q, make_uint4(hp[4 * q], hp[4 * q + 1], hp[4 * q + 2], hp[4 * q + 3]), tmH,
+                                        f0 + 32 * c);
+      tam = max(tam, fold_bf16x2(am2));
     } else {
-      tam = max(tam, am);
-    }
+      if (p.h_bf16) {
+        uint4* d = reinterpret_cast<uint4*>(p.h_bf16 + orow * p.F + f0 + 32 * c);
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
-      const float a0 = __fmul_rn(bf16_lo(hp[2 * w]), mult), a1 = __fmul_rn(bf16_hi(hp[2 * w]), mult);
-      const float a2 = __fmul_rn(bf16_lo(hp[2 * w + 1]), mult), a3 = __fmul_rn(bf16_hi(hp[2 * w + 1]), mult);
-      hw[8 * c + w] = e5 ? cvt_fp8x4<MGQ_E5M2>(a0, a1, a2, a3) : cvt_fp8x4<MGQ_E4M3>(a0, a1, a2, a3);
+        for (int q = 0; q < 4; ++q) d[q] = make_uint4(hp[4 * q], hp[4 * q + 1], hp[4 * q + 2], hp[4 * q + 3]);
+      }
+      const uint32_t am = fold_bf16x2(am2);
+      float mult = ts;
+      if (KIND == kKindMX) {
+        const int e = mx_exponent(am, e5 ? FmtInfo<MGQ_E5M2>::emax : FmtInfo<MGQ_E4M3>::emax, p.h_rceil != 0);
+        mult = mx_multiplier(e);
+        sc2 |= mx_scale_code(e) << (8 * c);
+      } else {
+        tam = max(tam, am);
+      }
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        const float a0 = __fmul_rn(bf16_lo(hp[2 * w]), mult), a1 = __fmul_rn(bf16_hi(hp[2 * w]), mult);
+        const float a2 = __fmul_rn(bf16_lo(hp[2 * w + 1]), mult), a3 = __fmul_rn(bf16_hi(hp[2 * w + 1]), mult);
+        hw[8 * c + w] = e5 ? cvt_fp8x4<MGQ_E5M2>(a0, a1, a2, a3) : cvt_fp8x4<MGQ_E4M3>(a0, a1, a2, a3);
+      }
     }
   }
+  if (KIND != kKindNV) {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) stage(j, make_uint4(hw[4 * j], hw[4 * j + 1], hw[4 * j + 2], hw[4 * j + 3]), tmH, f0);
-  if (KIND == kKindMX)
-    *reinterpret_cast<uint16_t*>(p.h_scales + tiled_scale_offset(orow, f0 / 32, p.F / 128)) = (uint16_t)sc2;
+    for (int j = 0; j < 4; ++j) stage(j, make_uint4(hw[4 * j], hw[4 * j + 1], hw[4 * j + 2], hw[4 * j + 3]), tmH, f0);
+    if (KIND == kKindMX)
+      *reinterpret_cast<uint16_t*>(p.h_scales + tiled_scale_offset(orow, f0 / 32, p.F / 128)) = (uint16_t)sc2;
+  }
 }
 
 // g and u of 16 columns (col0 + 16 c ..) of one row of the forward's gu
@@ -355,24 +372,10 @@ __device__ __forceinline__ void dswiglu_load_gu(const GemmParams& p, int64_t oro
 // the warp's staging buffer; the optional bf16 dG | dU by plain stores.
 // Warp-collective (tensor-memory loads).
 __device__ __forceinline__ void epilogue_dswiglu(const GemmParams& p, uint32_t tcol, float alpha, int64_t orow,
-                                                 int64_t col0, uint8_t* stg, const CUtensorMap* tmO,
+                                                 int64_t col0, Stager& sg, const CUtensorMap* tmO,
                                                  const CUtensorMap* tmH, int32_t y0, uint32_t lane, uint32_t& tam,
                                                  uint4 (&gq)[2], uint4 (&uq)[2]) {
-  auto stage = [&](int j, uint4 v, const CUtensorMap* m, int64_t x) {
-    if (j == 0) {
-      if (lane == 0) ptx::bulk_wait_read0();
-      __syncwarp();
-    }
-    reinterpret_cast<uint4*>(stg + lane * 64)[j] = v;
-    if (j == 3) {
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        ptx::tma_store_2d(m, stg, (int32_t)x, y0);
-        ptx::bulk_commit();
-      }
-    }
-  };
+  auto stage = [&](int j, uint4 v, const CUtensorMap* m, int64_t x) { sg.put(lane, j, v, m, x, y0, 64); };
   const int64_t F = p.F;
   const float ts = *p.h_scale;
   const bool e5 = p.h_dtype == MGQ_E5M2;
@@ -638,6 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t q = warp & 3;
     const uint32_t half = (uint32_t)(warp - 2) >> 2;
     const int64_t row_in_tile = q * 32 + lane;
+    Stager sg{sOut + (warp - 2) * kStageOut * staging_slots(KIND), staging_slots(KIND), 0u};
     uint32_t h_tam = 0;    // per-tensor SwiGLU: this thread's max |h| (float bits)
     int ecur = 0;
     uint32_t tc = 0;
@@ -713,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tbase = tmem + a * BN + ((q * 32) << 16);
         if (MODE == kModeRows && KIND == kKindTensor && p.dswiglu) {
           epilogue_dswiglu(p, tbase + half * (BN / 2), 1.0f / (p.sa[0] * p.sb[tl.e]), orow, col0,
-                           sOut + (warp - 2) * kStageOut, &tmO, &tmH, (int32_t)(tl.out_row + q * 32), lane, h_tam,
+                           sg, &tmO, &tmH, (int32_t)(tl.out_row + q * 32), lane, h_tam,
                            gq, uq);
           ptx::tc_fence_before();
           ptx::mbar_arrive(&tmem_empty[a]);
@@ -729,15 +733,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float alpha = 1.0f;
       if (KIND == kKindTensor || NV) alpha = 1.0f / (p.sa[0] * p.sb[MODE == kModeRows ? tl.e : 0]);
-      if (MODE == kModeRows && (KIND == kKindTensor || KIND == kKindMX) && p.swiglu)
-        epilogue_swiglu<KIND == kKindMX ? kKindMX : kKindTensor>(p, r, alpha, orow, tl.out_col + half * 64,
-                                                                 sOut + (warp - 2) * kStageOut, &tmO, &tmH,
+      if (MODE == kModeRows && KIND != kKindBlock && p.swiglu)
+        epilogue_swiglu<KIND == kKindBlock ? kKindTensor : KIND>(p, r, alpha, orow, tl.out_col + half * 64,
+                                                                 sg, &tmO, &tmH,
                                                                  (int32_t)(tl.out_row + q * 32), lane, h_tam);
       else
-        epilogue_store(p, r, alpha, orow, col0, p.tma_store != 0, sOut + (warp - 2) * kStageOut, &tmO,
+        epilogue_store(p, r, alpha, orow, col0, p.tma_store != 0, sg, &tmO,
                        (int32_t)(tl.out_row + q * 32), lane);
     }
-    if (MODE == kModeRows && KIND == kKindTensor && (p.swiglu || p.dswiglu) && p.h_amax) {
+    if (MODE == kModeRows && (KIND == kKindTensor || KIND == kKindNV) && (p.swiglu || p.dswiglu) && p.h_amax) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) h_tam = max(h_tam, __shfl_xor_sync(0xFFFFFFFFu, h_tam, o));
       if (lane == 0) atomic_max_nonneg(p.h_amax, __uint_as_float(h_tam));
@@ -1025,6 +1029,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t q = warp & 3;
     const uint32_t half = (uint32_t)(warp - 2) >> 2;
     const int64_t row_in_tile = 128 * rank + q * 32 + lane;
+    Stager sg{sOut + (warp - 2) * kStageOut, 1u, 0u};
     uint32_t h_tam = 0;    // per-tensor SwiGLU: this thread's max |h| (float bits)
     const uint32_t empty_remote0 = ptx::mapa_shared(ptx::smem_u32(&tmem_empty[0]), 0);
     const uint32_t empty_remote1 = ptx::mapa_shared(ptx::smem_u32(&tmem_empty[1]), 0);
@@ -1065,7 +1070,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // (the other accumulator buffer keeps the MMAs going meanwhile)
         if (store)
           epilogue_dswiglu(p, tbase + half * (BN / 2), 1.0f / (p.sa[0] * p.sb[tl.e]), orow, col0,
-                           sOut + (warp - 2) * kStageOut, &tmO, &tmH, (int32_t)(tl.out_row + 128 * rank + q * 32),
+                           sg, &tmO, &tmH, (int32_t)(tl.out_row + 128 * rank + q * 32),
                            lane, h_tam, gq, uq);
         ptx::tc_fence_before();
         __syncwarp();
@@ -1084,13 +1089,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!store) continue;    // the warp's 32 rows lie wholly inside or past the group
       const float alpha = MX ? 1.0f : 1.0f / (p.sa[0] * p.sb[MODE == kModeRows ? tl.e : 0]);
       if (MODE == kModeRows && p.swiglu)
-        epilogue_swiglu<KIND>(p, r, alpha, orow, tl.out_col + half * 64, sOut + (warp - 2) * kStageOut, &tmO, &tmH,
+        epilogue_swiglu<KIND>(p, r, alpha, orow, tl.out_col + half * 64, sg, &tmO, &tmH,
                               (int32_t)(tl.out_row + 128 * rank + q * 32), lane, h_tam);
       else
-        epilogue_store(p, r, alpha, orow, col0, p.tma_store != 0, sOut + (warp - 2) * kStageOut, &tmO,
+        epilogue_store(p, r, alpha, orow, col0, p.tma_store != 0, sg, &tmO,
                        (int32_t)(tl.out_row + 128 * rank + q * 32), lane);
     }
-    if (MODE == kModeRows && KIND == kKindTensor && (p.swiglu || p.dswiglu) && p.h_amax) {
+    if (MODE == kModeRows && (KIND == kKindTensor || KIND == kKindNV) && (p.swiglu || p.dswiglu) && p.h_amax) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) h_tam = max(h_tam, __shfl_xor_sync(0xFFFFFFFFu, h_tam, o));
       if (lane == 0) atomic_max_nonneg(p.h_amax, __uint_as_float(h_tam));
@@ -1285,12 +1290,18 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
     // row-wise with the GEMM's own scaling (MX or per-tensor)
     const mgq_qdesc* qh = sw->qh;
     const int64_t F = N / 2;
-    if (mode != kModeRows || (kind != kKindTensor && kind != kKindMX) || b_mn) return MGQ_ERR_UNSUPPORTED;
+    if (mode != kModeRows || kind == kKindBlock || b_mn) return MGQ_ERR_UNSUPPORTED;
     MGQ_CHECK_ARG(qh && qh->row.data && aligned16(qh->row.data) && N % 256 == 0 && aligned16(sw->h_bf16));
     if (qh->scaling != scaling || qh->col.data) return MGQ_ERR_UNSUPPORTED;
-    if (qh->dtype != MGQ_E4M3 && qh->dtype != MGQ_E5M2) return MGQ_ERR_UNSUPPORTED;
-    if (mx) MGQ_CHECK_ARG(qh->row.scale && aligned16(qh->row.scale));
-    else MGQ_CHECK_ARG(qh->tensor_scale != nullptr);
+    if (nv) {
+      // h in bf16 and its amax from the epilogue, then the NVFP4 cast
+      if (qh->dtype != MGQ_E2M1) return MGQ_ERR_UNSUPPORTED;
+      MGQ_CHECK_ARG(qh->row.scale && aligned16(qh->row.scale) && qh->amax_out && qh->tensor_scale && sw->h_bf16);
+    } else {
+      if (qh->dtype != MGQ_E4M3 && qh->dtype != MGQ_E5M2) return MGQ_ERR_UNSUPPORTED;
+      if (mx) MGQ_CHECK_ARG(qh->row.scale && aligned16(qh->row.scale));
+      else MGQ_CHECK_ARG(qh->tensor_scale != nullptr);
+    }
     MGQ_CHECK_ARG(out_dtype == MGQ_OUT_BF16);
     p.swiglu = 1;
     p.F = F;
@@ -1302,7 +1313,9 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
     p.h_bf16 = static_cast<uint16_t*>(sw->h_bf16);
     p.h_dtype = qh->dtype;
     p.h_rceil = qh->e8m0_mode == MGQ_E8M0_RCEIL;
-    if (!encode_tmap_2d(&th, qh->row.data, 1, (uint64_t)F, (uint64_t)R_cap, (uint64_t)F, 64, 32)) return MGQ_ERR_CUDA;
+    const bool ok = nv ? encode_tmap_2d(&th, sw->h_bf16, 2, (uint64_t)F, (uint64_t)R_cap, (uint64_t)F * 2, 32, 32)
+                       : encode_tmap_2d(&th, qh->row.data, 1, (uint64_t)F, (uint64_t)R_cap, (uint64_t)F, 64, 32);
+    if (!ok) return MGQ_ERR_CUDA;
   }
   if (dsw) {
     // down-projection dgrad (N = F output columns): [dG | dU] quantised
@@ -1391,7 +1404,14 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
   if (mode == kModeRows) {
     if (kind == kKindMX) return launch_gemm<kModeRows, kKindMX>(ta, tb, to, th, p, s);
     if (kind == kKindTensor) return launch_gemm<kModeRows, kKindTensor>(ta, tb, to, th, p, s);
-    if (kind == kKindNV) return launch_gemm<kModeRows, kKindNV>(ta, tb, to, th, p, s);
+    if (kind == kKindNV) {
+      if (sw && cudaMemsetAsync(sw->qh->amax_out, 0, sizeof(float), s) != cudaSuccess) return MGQ_ERR_CUDA;
+      rc = launch_gemm<kModeRows, kKindNV>(ta, tb, to, th, p, s);
+      if (rc != MGQ_OK || !sw) return rc;
+      return launch_quant_rows_nv(static_cast<const uint16_t*>(sw->h_bf16), R_cap, offsets + E, N / 2,
+                                  static_cast<uint8_t*>(sw->qh->row.data), static_cast<uint8_t*>(sw->qh->row.scale),
+                                  sw->qh->amax_out, sw->qh->tensor_scale, s);
+    }
     return launch_gemm<kModeRows, kKindBlock>(ta, tb, to, th, p, s);
   }
   if (kind == kKindMX) return launch_gemm<kModeContract, kKindMX>(ta, tb, to, th, p, s);

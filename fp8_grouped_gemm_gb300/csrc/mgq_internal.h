@@ -38,6 +38,10 @@ int launch_transpose_u8(const uint8_t* src, int64_t src_ld, uint8_t* dst, int64_
 // amax[g] = max |x| over each of G groups of per_group bf16 values (zeroes
 // amax first; elementwise.cu).
 int launch_amax_groups(const uint16_t* x, int64_t per_group, int64_t G, float* amax, cudaStream_t s);
+// NVFP4 row-wise codes of x [rows, K] (rows_used on the device, or null) with
+// s_g = 2688 / *amax, written to *s_out
+int launch_quant_rows_nv(const uint16_t* x, int64_t rows, const int32_t* rows_used, int64_t K, uint8_t* codes,
+                         uint8_t* scales, const float* amax, float* s_out, cudaStream_t s);
 
 // Row-wise + column-wise quantisation in one pass (quant_tile.cu); q->col.data
 // must be set. Per-tensor or MX scaling.

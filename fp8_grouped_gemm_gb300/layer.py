@@ -50,10 +50,11 @@ class ExpertLayer:
         # per-tensor backward GEMMs read the row-wise codes MN-major
         self.mn = self.delayed and not col_copies
         self.keep_bf16 = keep_bf16
-        # SwiGLU in the gate/up GEMM epilogue: MX or per-tensor scaling, and no
-        # column-wise copy of h wanted (MX training needs one; NVFP4 needs the
-        # whole tensor's amax first; blockwise spans both epilogue halves)
-        self.fused_swiglu = fuse_swiglu and ((self.recipe == "mxfp8" and not self.train) or self.mn)
+        # SwiGLU in the gate/up GEMM epilogue: MX, per-tensor or NVFP4 (whose
+        # epilogue writes h and its amax, cast by a second pass), and no
+        # column-wise copy of h wanted (MX training needs one; the blockwise
+        # 1x128 block spans both epilogue halves)
+        self.fused_swiglu = fuse_swiglu and ((self.recipe in ("mxfp8", "nvfp4") and not self.train) or self.mn)
         if self.train and self.recipe not in ("delayed", "mxfp8"):
             raise NotImplementedError(f"backward with {self.recipe}")
         self.scaling = {"mxfp8": mgq.MX32_E8M0, "delayed": mgq.TENSOR_F32,

@@ -722,7 +722,7 @@ def test_amax_history_update(mgq):
         assert torch.count_nonzero(amax).item() == 0
 
 
-@pytest.mark.parametrize("scaling", ["tensor", "mx"])
+@pytest.mark.parametrize("scaling", ["tensor", "mx", "nvfp4"])
 def test_gemm_fwd_swiglu_equals_separate_steps(mgq, scaling):
     """The gate/up GEMM with SwiGLU + quantisation in its epilogue writes the
     same bytes as grouped_gemm_fwd followed by swiglu_quantize: g | u, h, the
@@ -741,6 +741,19 @@ def test_gemm_fwd_swiglu_equals_separate_steps(mgq, scaling):
         A = _op(mgq, ac, tile_mx_scales(asc), K, mgq.E4M3, dev)
         W1 = _op(mgq, wc, tile_mx_scales(wsc), K, mgq.E4M3, dev)
         sc = mgq.MX32_E8M0
+    elif scaling == "nvfp4":
+        pack = lambda q: ((q[:, 0::2] & 0xF) | ((q[:, 1::2] & 0xF) << 4)).astype(np.uint8)
+        sca = rng.integers(0x20, 0x50, size=(R_cap, K // 16)).astype(np.uint8)
+        scw = rng.integers(0x20, 0x50, size=(E * 2 * F, K // 16)).astype(np.uint8)
+        A = _op(mgq, pack(rng.integers(0, 16, size=(R_cap, K)).astype(np.uint8)), tile_mx_scales(sca), K,
+                mgq.E2M1, dev)
+        W1 = _op(mgq, pack(rng.integers(0, 16, size=(E * 2 * F, K)).astype(np.uint8)), tile_mx_scales(scw), K,
+                 mgq.E2M1, dev)
+        ga = _to_dev(np.array([2.5], dtype=np.float32), dev)
+        gw = _to_dev(np.exp2(rng.uniform(-2, 2, size=E)).astype(np.float32), dev)
+        _KEEP.append((ga, gw))
+        A.global_scale, W1.global_scale = ga.data_ptr(), gw.data_ptr()
+        sc = mgq.NV16_UE4M3
     else:
         f4 = OF.E4M3
         ac = (rng.choice(f4.pos_codes[:-1], size=(R_cap, K)) | (rng.integers(0, 2, (R_cap, K)) * 0x80)).astype(np.uint8)
@@ -751,14 +764,19 @@ def test_gemm_fwd_swiglu_equals_separate_steps(mgq, scaling):
         sc = mgq.TENSOR_F32
 
     def outputs():
+        nv = sc == mgq.NV16_UE4M3
         o = dict(gu=torch.full((R_cap, 2 * F), 3.0, dtype=torch.bfloat16, device=dev),
                  h=torch.full((R_cap, F), 3.0, dtype=torch.bfloat16, device=dev),
-                 hq=torch.full((R_cap, F), 0xAB, dtype=torch.uint8, device=dev),
-                 hs=torch.full((mgq.mx_scale_bytes(R_cap, F),), 0xCD, dtype=torch.uint8, device=dev),
-                 ts=torch.tensor([2.5], device=dev), am=torch.zeros(1, device=dev))
+                 hq=torch.full((R_cap, F // 2 if nv else F), 0xAB, dtype=torch.uint8, device=dev),
+                 hs=torch.full(((mgq.nv_scale_bytes if nv else mgq.mx_scale_bytes)(R_cap, F),), 0xCD,
+                               dtype=torch.uint8, device=dev),
+                 ts=torch.tensor([2.5], device=dev), am=torch.full((1,), 7.0, device=dev))
         if sc == mgq.MX32_E8M0:
             o["q"] = mgq.qdesc(mgq.E4M3, sc, o["hq"], o["hs"])
+        elif nv:   # s_g is written to ts, the amax (zeroed by the call) to am
+            o["q"] = mgq.qdesc(mgq.E2M1, sc, o["hq"], o["hs"], tensor_scale=o["ts"], amax_out=o["am"])
         else:
+            o["am"].zero_()
             o["q"] = mgq.qdesc(mgq.E4M3, sc, o["hq"], None, None, None, o["ts"], o["am"])
         return o
 
@@ -766,12 +784,13 @@ def test_gemm_fwd_swiglu_equals_separate_steps(mgq, scaling):
     mgq.grouped_gemm_fwd(A, W1, sc, offd, E, R_cap, 2 * F, K, sep["gu"])
     mgq.swiglu_quantize(sep["gu"], R_cap, F, offd, E, sep["q"], sep["h"])
     mgq.grouped_gemm_fwd_swiglu(A, W1, sc, offd, E, R_cap, F, K, fus["q"], fus["gu"], fus["h"])
-    # without the optional outputs the codes are the same
+    # without the optional outputs the codes are the same (NVFP4 needs h itself)
     bare = outputs()
-    mgq.grouped_gemm_fwd_swiglu(A, W1, sc, offd, E, R_cap, F, K, bare["q"])
+    mgq.grouped_gemm_fwd_swiglu(A, W1, sc, offd, E, R_cap, F, K, bare["q"],
+                                h=bare["h"] if sc == mgq.NV16_UE4M3 else None)
     torch.cuda.synchronize()
     assert mgq.get_error() == mgq.OK
-    for key in ("gu", "h", "hq", "hs", "am"):
+    for key in ("gu", "h", "hq", "hs", "am", "ts"):
         assert torch.equal(sep[key], fus[key]), key
     assert torch.equal(sep["hq"], bare["hq"]) and torch.equal(sep["am"], bare["am"])
     assert torch.all(bare["gu"] == 3.0)
