@@ -671,12 +671,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i) r[c][i] = 0u;   // +0.0f
+        // both scales are loaded one stage ahead of their partial product
         float sa_next = sa_row[(tl.kx0 / 128) * p.sa_ld];
+        float sb_next = sb_blk[tl.kx0 / 128];
         bool alive = true;
         for (int s = 0; s < tl.nst; ++s) {
           const uint32_t a = tc % kAcc, aph = (tc / kAcc) & 1;
-          const float f = sa_next * sb_blk[tl.kx0 / 128 + s];
-          if (s + 1 < tl.nst) sa_next = sa_row[(tl.kx0 / 128 + s + 1) * p.sa_ld];
+          const float f = sa_next * sb_next;
+          if (s + 1 < tl.nst) {
+            sa_next = sa_row[(tl.kx0 / 128 + s + 1) * p.sa_ld];
+            sb_next = sb_blk[tl.kx0 / 128 + s + 1];
+          }
           if (__any_sync(0xFFFFFFFFu, *s_abort != 0)) { alive = false; break; }
           const bool got = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&tmem_full[a], aph, p.wait_ns));
           if (!got) {
@@ -687,14 +692,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ptx::tc_fence_after();
           const uint32_t taddr = tmem + a * BN + ((q * 32) << 16) + half * (BN / 2);
+          // 16 columns per load keep the partial and the accumulator in registers
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t v[32];
-            ptx::tmem_ld_32x32b_x32(taddr + c * 32, v);
+          for (int c = 0; c < 8; ++c) {
+            uint32_t v[16];
+            ptx::tmem_ld_32x32b_x16(taddr + c * 16, v);
             ptx::tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              r[c][i] = __float_as_uint(fmaf(__uint_as_float(v[i]), f, __uint_as_float(r[c][i])));
+            for (int i = 0; i < 16; ++i)
+              r[c / 2][(c & 1) * 16 + i] =
+                  __float_as_uint(fmaf(__uint_as_float(v[i]), f, __uint_as_float(r[c / 2][(c & 1) * 16 + i])));
           }
           ptx::tc_fence_before();
           ptx::mbar_arrive(&tmem_empty[a]);
