@@ -21,6 +21,9 @@
 // same tile sequence from it. Every mbarrier wait is bounded: on a timeout the
 // kernel records MGQ_ERR_TIMEOUT, all roles leave their loops, tensor memory is
 // freed and the kernel returns.
+// The dSwiGLU instantiations leave the plain epilogue after their `continue`
+// unreachable by design.
+#pragma nv_diag_suppress 128
 #include <cstdlib>
 
 #include "device_common.cuh"
@@ -445,7 +448,9 @@ __device__ __forceinline__ void epilogue_dswiglu(const GemmParams& p, uint32_t t
   }
 }
 
-template <int MODE, int KIND>
+// DSW: the down-projection dgrad with the dSwiGLU epilogue (a separate
+// instantiation, so the other epilogues keep their registers)
+template <int MODE, int KIND, bool DSW = false>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmH,
@@ -711,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         const uint32_t a = tc % kAcc, aph = (tc / kAcc) & 1;
         uint4 gq[2], uq[2];    // dSwiGLU: the first g / u chunk, requested before the accumulator is ready
-        if (MODE == kModeRows && KIND == kKindTensor && p.dswiglu) dswiglu_load_gu(p, orow, col0, 0, gq, uq);
+        if (DSW) dswiglu_load_gu(p, orow, col0, 0, gq, uq);
         // the whole warp agrees before the .sync.aligned tensor-memory loads
         if (__any_sync(0xFFFFFFFFu, *s_abort != 0)) break;
         const bool got = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&tmem_full[a], aph, p.wait_ns));
@@ -722,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tc_fence_after();
         const uint32_t tbase = tmem + a * BN + ((q * 32) << 16);
-        if (MODE == kModeRows && KIND == kKindTensor && p.dswiglu) {
+        if (DSW) {
           epilogue_dswiglu(p, tbase + half * (BN / 2), 1.0f / (p.sa[0] * p.sb[tl.e]), orow, col0,
                            sg, &tmO, &tmH, (int32_t)(tl.out_row + q * 32), lane, h_tam,
                            gq, uq);
@@ -748,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         epilogue_store(p, r, alpha, orow, col0, p.tma_store != 0, sg, &tmO,
                        (int32_t)(tl.out_row + q * 32), lane);
     }
-    if (MODE == kModeRows && (KIND == kKindTensor || KIND == kKindNV) && (p.swiglu || p.dswiglu) && p.h_amax) {
+    if (MODE == kModeRows && (KIND == kKindTensor || KIND == kKindNV) && (p.swiglu || DSW) && p.h_amax) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) h_tam = max(h_tam, __shfl_xor_sync(0xFFFFFFFFu, h_tam, o));
       if (lane == 0) atomic_max_nonneg(p.h_amax, __uint_as_float(h_tam));
@@ -763,10 +768,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int MODE, int KIND>
+template <int MODE, int KIND, bool DSW = false>
 int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const CUtensorMap& th,
                 const GemmParams& p, cudaStream_t s) {
-  auto kern = grouped_gemm_kernel<MODE, KIND>;
+  auto kern = grouped_gemm_kernel<MODE, KIND, DSW>;
   constexpr size_t kSmemBytes = smem_bytes(KIND);
   static bool attr_set[64] = {false};
   int dev = 0;
@@ -848,7 +853,7 @@ __device__ __forceinline__ bool get_pair_tile(const int32_t* s_off, const int32_
   return true;
 }
 
-template <int MODE, int KIND>
+template <int MODE, int KIND, bool DSW = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmSFA,
@@ -1062,7 +1067,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       const uint32_t a = tc % kAccBufs, aph = (tc / kAccBufs) & 1;
       uint4 gq[2], uq[2];    // dSwiGLU: the first g / u chunk, requested before the accumulator is ready
-      if (MODE == kModeRows && KIND == kKindTensor && p.dswiglu && store) dswiglu_load_gu(p, orow, col0, 0, gq, uq);
+      if (DSW && store) dswiglu_load_gu(p, orow, col0, 0, gq, uq);
       if (__any_sync(0xFFFFFFFFu, *s_abort != 0)) break;
       const bool got = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&tmem_full[a], aph, p.wait_ns));
       if (!got) {
@@ -1072,7 +1077,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_after();
       const uint32_t tbase = tmem + a * BN + ((q * 32) << 16);
-      if (MODE == kModeRows && KIND == kKindTensor && p.dswiglu) {
+      if (DSW) {
         // tensor memory read chunk by chunk beside the gu loads, released after
         // (the other accumulator buffer keeps the MMAs going meanwhile)
         if (store)
@@ -1102,7 +1107,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         epilogue_store(p, r, alpha, orow, col0, p.tma_store != 0, sg, &tmO,
                        (int32_t)(tl.out_row + 128 * rank + q * 32), lane);
     }
-    if (MODE == kModeRows && (KIND == kKindTensor || KIND == kKindNV) && (p.swiglu || p.dswiglu) && p.h_amax) {
+    if (MODE == kModeRows && (KIND == kKindTensor || KIND == kKindNV) && (p.swiglu || DSW) && p.h_amax) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) h_tam = max(h_tam, __shfl_xor_sync(0xFFFFFFFFu, h_tam, o));
       if (lane == 0) atomic_max_nonneg(p.h_amax, __uint_as_float(h_tam));
@@ -1119,10 +1124,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int MODE, int KIND>
+template <int MODE, int KIND, bool DSW = false>
 int launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const CUtensorMap& tsfa,
                      const CUtensorMap& tsfb, const CUtensorMap& th, const GemmParams& p, cudaStream_t s) {
-  auto kern = grouped_gemm_pair_kernel<MODE, KIND>;
+  auto kern = grouped_gemm_pair_kernel<MODE, KIND, DSW>;
   constexpr size_t kSmem = pair_smem(KIND);
   static bool attr_set[64] = {false};
   int dev = 0;
@@ -1397,6 +1402,7 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
     if (mx)
       return mode == kModeRows ? launch_gemm_pair<kModeRows, kKindMX>(ta, tb2, to, tsfa, tsfb, th, p, s)
                                : launch_gemm_pair<kModeContract, kKindMX>(ta, tb2, to, tsfa, tsfb, th, p, s);
+    if (p.dswiglu) return launch_gemm_pair<kModeRows, kKindTensor, true>(ta, tb2, to, tsfa, tsfb, th, p, s);
     return mode == kModeRows ? launch_gemm_pair<kModeRows, kKindTensor>(ta, tb2, to, tsfa, tsfb, th, p, s)
                              : launch_gemm_pair<kModeContract, kKindTensor>(ta, tb2, to, tsfa, tsfb, th, p, s);
   }
@@ -1410,7 +1416,9 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
   }
   if (mode == kModeRows) {
     if (kind == kKindMX) return launch_gemm<kModeRows, kKindMX>(ta, tb, to, th, p, s);
-    if (kind == kKindTensor) return launch_gemm<kModeRows, kKindTensor>(ta, tb, to, th, p, s);
+    if (kind == kKindTensor)
+      return p.dswiglu ? launch_gemm<kModeRows, kKindTensor, true>(ta, tb, to, th, p, s)
+                       : launch_gemm<kModeRows, kKindTensor>(ta, tb, to, th, p, s);
     if (kind == kKindNV) {
       if (sw && cudaMemsetAsync(sw->qh->amax_out, 0, sizeof(float), s) != cudaSuccess) return MGQ_ERR_CUDA;
       rc = launch_gemm<kModeRows, kKindNV>(ta, tb, to, th, p, s);
