@@ -369,7 +369,7 @@ __device__ __forceinline__ void dswiglu_load_gu(const GemmParams& p, int64_t oro
 // row `orow` and columns col0..col0+127, in 8 chunks of 16: each reads its
 // accumulator columns from tensor memory (`tcol` = the first) and the matching
 // g and u of the forward's gu (chunk 0 already in gq / uq, requested by the
-// caller before the accumulator was ready; each further chunk is loaded when it is processed);
+// caller before the accumulator was ready; further chunks in pairs, 32 columns per request);
 // dh = bf16(acc * alpha), [dG | dU] = dswiglu_bf16, quantised with *p.h_scale
 // (max |.| into tam). Codes and (p.out set) dh go out through TMA stores from
 // the warp's staging buffer; the optional bf16 dG | dU by plain stores.
@@ -384,9 +384,18 @@ __device__ __forceinline__ void epilogue_dswiglu(const GemmParams& p, uint32_t t
   const bool e5 = p.h_dtype == MGQ_E5M2;
   uint32_t cg[16], cu[16];    // codes of four 16-column chunks: dG, dU
   uint32_t dhw[16];           // dh of two chunks as bf16 pairs (the 64-byte rows of its stores)
+  uint4 g2[2], u2[2];          // the odd chunk of a pair, requested with the even one
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
-    if (c > 0) dswiglu_load_gu(p, orow, col0, c, gq, uq);
+    if (c > 0 && (c & 1) == 0) dswiglu_load_gu(p, orow, col0, c, gq, uq);
+    if ((c & 1) == 0) dswiglu_load_gu(p, orow, col0, c + 1, g2, u2);
+    if (c & 1) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        gq[q] = g2[q];
+        uq[q] = u2[q];
+      }
+    }
     uint32_t v[16];
     ptx::tmem_ld_32x32b_x16(tcol + 16 * c, v);
     ptx::tmem_ld_wait();
