@@ -173,12 +173,24 @@ struct PermuteArgs {
   const int32_t* base;     // [chunks][E] first row of each (chunk, expert)
   int32_t* rim;            // row_id_map: rank inside the chunk in, final row out
   int32_t* src_row;
+  int resolve;             // 0: rim already holds the final rows
 };
 
-// Every lane gets the k destination rows of token t (lane j resolves entry j).
+// ---- routing pass 3 (standalone routing only): final rows and src_row -------
+__global__ void route_finalize_kernel(const int32_t* __restrict__ idx, int64_t n, int E,
+                                      const int32_t* __restrict__ base, int32_t* __restrict__ row_id_map,
+                                      int32_t* __restrict__ src_row) {
+  const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (g < n) resolve_row(idx, row_id_map, base, src_row, E, g);
+}
+
+// Every lane gets the k destination rows of token t (lane j resolves entry j,
+// or reads it when the routing is already final).
 __device__ __forceinline__ void token_rows(const PermuteArgs& a, int t, uint32_t lane, int (&dest)[8]) {
   int mine = -1;
-  if ((int)lane < a.k) mine = resolve_row(a.idx, a.rim, a.base, a.src_row, a.E, (int64_t)t * a.k + lane);
+  if ((int)lane < a.k)
+    mine = a.resolve ? resolve_row(a.idx, a.rim, a.base, a.src_row, a.E, (int64_t)t * a.k + lane)
+                     : a.rim[(int64_t)t * a.k + lane];
 #pragma unroll
   for (int j = 0; j < 8; ++j) dest[j] = __shfl_sync(0xFFFFFFFFu, mine, j);
 }
@@ -410,47 +422,51 @@ size_t mgq_permute_workspace_size(int T, int k, int E) {
   return (size_t)(nchunks * E * sizeof(int32_t));
 }
 
-int mgq_moe_permute(const void* x_bf16, int T, int H, const int32_t* topk_idx, int k, int E, int align,
-                    const mgq_qdesc* q, void* out_bf16, int64_t R_cap, int32_t* row_id_map, int32_t* src_row,
-                    int32_t* offsets, int32_t* counts, void* workspace, size_t ws_bytes, void* stream) {
-  MGQ_CHECK_ARG(T >= 0 && H > 0 && k >= 1 && k <= 8 && E >= 1 && E <= kMaxExperts && k <= E);
-  MGQ_CHECK_ARG(align >= 1 && (align % 32 == 0 || align == 1) && H % 128 == 0);
-  MGQ_CHECK_ARG(row_id_map && src_row && offsets && counts && workspace);
-  MGQ_CHECK_ARG(T == 0 || (x_bf16 && topk_idx));
+}  // extern "C"
+
+namespace mgq {
+namespace {
+
+int check_permute_q(const mgq_qdesc* q, int align) {
+  if (!q) return MGQ_ERR_UNSUPPORTED;   // bf16-only dispatch is not needed by the layer
+  MGQ_CHECK_ARG(q->row.data && aligned16(q->row.data));
+  if (q->scaling == MGQ_NV16_UE4M3) {
+    MGQ_CHECK_ARG(q->dtype == MGQ_E2M1 && q->row.scale && aligned16(q->row.scale) && q->amax_out &&
+                  q->tensor_scale && !q->col.data);
+    return MGQ_OK;
+  }
+  MGQ_CHECK_ARG(q->dtype == MGQ_E4M3 || q->dtype == MGQ_E5M2);
+  if (q->scaling == MGQ_MX32_E8M0 || q->scaling == MGQ_BLK_1x128_F32)
+    MGQ_CHECK_ARG(q->row.scale && aligned16(q->row.scale));
+  else if (q->scaling == MGQ_TENSOR_F32)
+    MGQ_CHECK_ARG(q->tensor_scale != nullptr);
+  else
+    return MGQ_ERR_UNSUPPORTED;
+  if (q->col.data) {
+    if (q->scaling != MGQ_TENSOR_F32 && q->scaling != MGQ_MX32_E8M0) return MGQ_ERR_UNSUPPORTED;
+    MGQ_CHECK_ARG(aligned16(q->col.data) && align % 32 == 0);
+    if (q->scaling == MGQ_MX32_E8M0) MGQ_CHECK_ARG(q->col.scale && aligned16(q->col.scale));
+  }
+  return MGQ_OK;
+}
+
+int check_route_args(int T, int k, int E, int align, int64_t R_cap, const void* rim, const void* src_row,
+                     const void* offsets, const void* counts) {
+  MGQ_CHECK_ARG(T >= 0 && k >= 1 && k <= 8 && E >= 1 && E <= kMaxExperts && k <= E);
+  MGQ_CHECK_ARG(align >= 1 && (align % 32 == 0 || align == 1));
+  MGQ_CHECK_ARG(rim && src_row && offsets && counts);
   const int64_t n = (int64_t)T * k;
   const int64_t need = ((n + (int64_t)E * (align - 1)) + 127) / 128 * 128;
   MGQ_CHECK_ARG(R_cap >= need && R_cap % 128 == 0 && R_cap < (1ll << 31));
-  MGQ_CHECK_ARG(ws_bytes >= mgq_permute_workspace_size(T, k, E));
-  MGQ_CHECK_ARG(aligned16(x_bf16) && aligned16(out_bf16));
-  if (q) {
-    MGQ_CHECK_ARG(q->row.data && aligned16(q->row.data));
-    if (q->scaling == MGQ_NV16_UE4M3)
-      MGQ_CHECK_ARG(q->dtype == MGQ_E2M1 && q->row.scale && aligned16(q->row.scale) && q->amax_out &&
-                    q->tensor_scale && !q->col.data);
-    else
-      MGQ_CHECK_ARG(q->dtype == MGQ_E4M3 || q->dtype == MGQ_E5M2);
-    if (q->scaling == MGQ_NV16_UE4M3) {
-      // checked above
-    } else if (q->scaling == MGQ_MX32_E8M0 || q->scaling == MGQ_BLK_1x128_F32)
-      MGQ_CHECK_ARG(q->row.scale && aligned16(q->row.scale));
-    else if (q->scaling == MGQ_TENSOR_F32)
-      MGQ_CHECK_ARG(q->tensor_scale != nullptr);
-    else
-      return MGQ_ERR_UNSUPPORTED;
-    if (q->col.data) {
-      if (q->scaling != MGQ_TENSOR_F32 && q->scaling != MGQ_MX32_E8M0) return MGQ_ERR_UNSUPPORTED;
-      MGQ_CHECK_ARG(aligned16(q->col.data) && align % 32 == 0);
-      if (q->scaling == MGQ_MX32_E8M0) MGQ_CHECK_ARG(q->col.scale && aligned16(q->col.scale));
-    }
-  } else {
-    MGQ_CHECK_ARG(out_bf16 != nullptr);
-  }
-  int* err = error_word();
-  if (!err) return MGQ_ERR_CUDA;
-  cudaStream_t s = as_stream(stream);
-  int64_t nchunks = (n + kChunk - 1) / kChunk;
-  int32_t* cnt = static_cast<int32_t*>(workspace);
-  // two routing launches; the permute kernel below resolves the final rows
+  return MGQ_OK;
+}
+
+// routing passes 1 and 2 (and 3 when `finalize`; otherwise the permute
+// kernel resolves the rows itself from the chunk ranks and bases)
+int route_impl(const int32_t* topk_idx, int T, int k, int E, int align, int32_t* row_id_map, int32_t* src_row,
+               int32_t* offsets, int32_t* counts, int32_t* cnt, bool finalize, int* err, cudaStream_t s) {
+  const int64_t n = (int64_t)T * k;
+  const int64_t nchunks = (n + kChunk - 1) / kChunk;
   if (nchunks > 0) {
     route_count_rank_kernel<<<(unsigned)nchunks, kRouteThreads, 9 * E * sizeof(int), s>>>(topk_idx, n, E, cnt,
                                                                                            row_id_map, err);
@@ -458,25 +474,35 @@ int mgq_moe_permute(const void* x_bf16, int T, int H, const int32_t* topk_idx, i
   }
   route_scan_kernel<<<1, 1024, 0, s>>>(cnt, (int)nchunks, E, align, offsets, counts, src_row);
   MGQ_LAUNCH_CHECK();
+  if (finalize && n > 0) {
+    route_finalize_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(topk_idx, n, E, cnt, row_id_map, src_row);
+    MGQ_LAUNCH_CHECK();
+  }
+  return MGQ_OK;
+}
+
+// permute + quantise of the token rows to their routed rows (row_id_map final,
+// or chunk ranks to resolve with `idx` and the chunk bases `cnt`)
+int permute_impl(const void* x_bf16, int T, int H, int k, int E, const mgq_qdesc* q, void* out_bf16, int64_t R_cap,
+                 int32_t* row_id_map, int32_t* src_row, const int32_t* offsets, const int32_t* counts,
+                 const int32_t* idx, const int32_t* cnt, bool resolve, int* err, cudaStream_t s) {
   PermuteArgs a;
   a.x = static_cast<const uint16_t*>(x_bf16);
   a.T = T; a.H = H; a.k = k; a.E = E;
   a.offsets = offsets; a.counts = counts;
-  a.idx = topk_idx; a.base = cnt; a.rim = row_id_map; a.src_row = src_row;
-  a.codes = q ? static_cast<uint8_t*>(q->row.data) : nullptr;
-  a.scales = q ? static_cast<uint8_t*>(q->row.scale) : nullptr;
+  a.idx = idx; a.base = cnt; a.rim = row_id_map; a.src_row = src_row;
+  a.resolve = resolve ? 1 : 0;
+  a.codes = static_cast<uint8_t*>(q->row.data);
+  a.scales = static_cast<uint8_t*>(q->row.scale);
   a.out_bf16 = static_cast<uint16_t*>(out_bf16);
-  a.tensor_scale = q ? q->tensor_scale : nullptr;
-  a.amax_out = q ? q->amax_out : nullptr;
-  a.s_out = q ? q->tensor_scale : nullptr;
+  a.tensor_scale = q->tensor_scale;
+  a.amax_out = q->amax_out;
+  a.s_out = q->tensor_scale;
   a.R_cap = R_cap;
-  a.e8m0_rceil = q ? (q->e8m0_mode == MGQ_E8M0_RCEIL) : 1;
+  a.e8m0_rceil = q->e8m0_mode == MGQ_E8M0_RCEIL;
   a.token_blocks = (T + 7) / 8;
   a.err = err;
   dim3 grid((unsigned)(a.token_blocks + E));
-  if (!q) {
-    return MGQ_ERR_UNSUPPORTED;   // bf16-only dispatch is not needed by the layer
-  }
   const int sc = q->scaling, dt = q->dtype;
   if (sc == MGQ_NV16_UE4M3) {
     int rc = launch_amax_groups(a.x, (int64_t)T * H, 1, q->amax_out, s);
@@ -505,6 +531,58 @@ int mgq_moe_permute(const void* x_bf16, int T, int H, const int32_t* topk_idx, i
     if (rc != MGQ_OK) return rc;
   }
   return MGQ_OK;
+}
+
+}  // namespace
+}  // namespace mgq
+
+extern "C" {
+
+int mgq_moe_permute(const void* x_bf16, int T, int H, const int32_t* topk_idx, int k, int E, int align,
+                    const mgq_qdesc* q, void* out_bf16, int64_t R_cap, int32_t* row_id_map, int32_t* src_row,
+                    int32_t* offsets, int32_t* counts, void* workspace, size_t ws_bytes, void* stream) {
+  int rc = check_route_args(T, k, E, align, R_cap, row_id_map, src_row, offsets, counts);
+  if (rc != MGQ_OK) return rc;
+  MGQ_CHECK_ARG(H > 0 && H % 128 == 0 && workspace && (T == 0 || (x_bf16 && topk_idx)));
+  MGQ_CHECK_ARG(ws_bytes >= mgq_permute_workspace_size(T, k, E));
+  MGQ_CHECK_ARG(aligned16(x_bf16) && aligned16(out_bf16));
+  if ((rc = check_permute_q(q, align)) != MGQ_OK) return rc;
+  int* err = error_word();
+  if (!err) return MGQ_ERR_CUDA;
+  cudaStream_t s = as_stream(stream);
+  int32_t* cnt = static_cast<int32_t*>(workspace);
+  // two routing launches; the permute kernel resolves the final rows
+  if ((rc = route_impl(topk_idx, T, k, E, align, row_id_map, src_row, offsets, counts, cnt, false, err, s)) != MGQ_OK)
+    return rc;
+  return permute_impl(x_bf16, T, H, k, E, q, out_bf16, R_cap, row_id_map, src_row, offsets, counts, topk_idx, cnt,
+                      true, err, s);
+}
+
+int mgq_moe_route(const int32_t* topk_idx, int T, int k, int E, int align, int64_t R_cap, int32_t* row_id_map,
+                  int32_t* src_row, int32_t* offsets, int32_t* counts, void* workspace, size_t ws_bytes,
+                  void* stream) {
+  int rc = check_route_args(T, k, E, align, R_cap, row_id_map, src_row, offsets, counts);
+  if (rc != MGQ_OK) return rc;
+  MGQ_CHECK_ARG(workspace && (T == 0 || topk_idx) && ws_bytes >= mgq_permute_workspace_size(T, k, E));
+  int* err = error_word();
+  if (!err) return MGQ_ERR_CUDA;
+  return route_impl(topk_idx, T, k, E, align, row_id_map, src_row, offsets, counts,
+                    static_cast<int32_t*>(workspace), true, err, as_stream(stream));
+}
+
+int mgq_moe_permute_routed(const void* x_bf16, int T, int H, int k, int E, const mgq_qdesc* q, void* out_bf16,
+                           int64_t R_cap, const int32_t* row_id_map, const int32_t* src_row,
+                           const int32_t* offsets, const int32_t* counts, void* stream) {
+  int rc = check_route_args(T, k, E, 1, R_cap, row_id_map, src_row, offsets, counts);
+  if (rc != MGQ_OK) return rc;
+  MGQ_CHECK_ARG(H > 0 && H % 128 == 0 && (T == 0 || x_bf16) && aligned16(x_bf16) && aligned16(out_bf16));
+  if ((rc = check_permute_q(q, 32)) != MGQ_OK) return rc;
+  int* err = error_word();
+  if (!err) return MGQ_ERR_CUDA;
+  // the kernels only read row_id_map and src_row when the rows are final
+  return permute_impl(x_bf16, T, H, k, E, q, out_bf16, R_cap, const_cast<int32_t*>(row_id_map),
+                      const_cast<int32_t*>(src_row), offsets, counts, nullptr, nullptr, false, err,
+                      as_stream(stream));
 }
 
 }  // extern "C"

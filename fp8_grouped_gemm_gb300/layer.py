@@ -219,9 +219,12 @@ class ExpertLayer:
                 sa, sw1, sh, sw2 = self._fs(0), self._fs(2, E), self._fs(1), self._fs(2 + E, E)
             A1, B1 = mgq.operand(self.xq, sa, H, dt), mgq.operand(self.w1q, sw1, H, dt)
             A2, B2 = mgq.operand(self.hq, sh, F, dt), mgq.operand(self.w2q, sw2, F, dt)
-        permute = ("permute_quant", lambda: mgq.moe_permute(x, topk_idx, E, ALIGN, qx, R, self.row_id_map,
-                                                            self.src_row, self.offsets, self.counts, self.ws, None,
-                                                            stream))
+        # routing (index work) and the permute + quantise (HBM-bound) as two ops
+        permute = [("route", lambda: mgq.moe_route(topk_idx, E, ALIGN, R, self.row_id_map, self.src_row,
+                                                   self.offsets, self.counts, self.ws, stream)),
+                   ("permute_quant", lambda: mgq.moe_permute_routed(x, self.w.k, E, qx, R, self.row_id_map,
+                                                                    self.src_row, self.offsets, self.counts, None,
+                                                                    stream))]
         if self.fused_swiglu:
             # g | u only where something reads them (backward, or checks)
             gu = self.gu if (self.train or self.keep_bf16) else None
@@ -234,7 +237,7 @@ class ExpertLayer:
                                                                  mgq.OUT_BF16, stream)),
                 ("swiglu_quant", lambda: mgq.swiglu_quantize(self.gu, R, F, self.offsets, E, qh, self.h_bf16,
                                                              stream))]
-        return [permute] + gateup + [
+        return permute + gateup + [
             ("gemm_fwd_down", lambda: mgq.grouped_gemm_fwd(A2, B2, sc, self.offsets, E, R, H, F, self.y,
                                                            mgq.OUT_BF16, stream)),
             ("unpermute", lambda: mgq.moe_unpermute(self.y, self.row_id_map, probs, self.out, stream)),
@@ -337,7 +340,7 @@ class ExpertLayer:
     def gpu_launches_per_step(self) -> int:
         """Kernels this object launches per forward (+ backward) step."""
         E = self.w.E
-        n_route = 2 if self.w.T * self.w.k > 0 else 1
+        n_route = 3 if self.w.T * self.w.k > 0 else 1   # count + rank, scan, finalize
         fwd = n_route + 1 + 1 + 1 + 1 + 1               # route, permute-quant, gemm1, swiglu, gemm2, unpermute
         if self.fused_swiglu:
             fwd -= 1                                    # SwiGLU in the gate/up GEMM epilogue

@@ -30,7 +30,7 @@ FMAX = {E4M3: 448.0, E5M2: 57344.0}
 # every symbol include/mgq.h declares
 EXPORTS = (
     "mgq_status_string", "mgq_version", "mgq_get_error", "mgq_permute_workspace_size",
-    "mgq_moe_permute", "mgq_moe_permute_noalloc", "mgq_block_quantize", "mgq_grouped_gemm_fwd", "mgq_grouped_gemm_dgrad",
+    "mgq_moe_permute", "mgq_moe_route", "mgq_moe_permute_routed", "mgq_moe_permute_noalloc", "mgq_block_quantize", "mgq_grouped_gemm_fwd", "mgq_grouped_gemm_dgrad",
     "mgq_grouped_gemm_wgrad", "mgq_grouped_gemm_fwd_swiglu",
     "mgq_grouped_gemm_dgrad_dswiglu", "mgq_swiglu_quantize", "mgq_dswiglu_quantize", "mgq_moe_unpermute",
     "mgq_moe_unpermute_bwd", "mgq_moe_permute_bwd", "mgq_amax_history_update",
@@ -77,6 +77,8 @@ def load() -> ctypes.CDLL:
         lib.mgq_permute_workspace_size.argtypes = [i32, i32, i32]
         lib.mgq_moe_permute.argtypes = [vp, i32, i32, vp, i32, i32, i32, P(QDesc), vp, i64,
                                         vp, vp, vp, vp, vp, sz, vp]
+        lib.mgq_moe_route.argtypes = [vp, i32, i32, i32, i32, i64, vp, vp, vp, vp, vp, sz, vp]
+        lib.mgq_moe_permute_routed.argtypes = [vp, i32, i32, i32, i32, P(QDesc), vp, i64, vp, vp, vp, vp, vp]
         lib.mgq_moe_permute_noalloc.argtypes = [vp, i32, i32, vp, i32, i32, i32, P(QDesc), vp, i64,
                                                 vp, vp, vp, vp, vp]
         lib.mgq_block_quantize.argtypes = [vp, i64, i64, i64, P(QDesc), vp]
@@ -172,6 +174,23 @@ def moe_permute(x, topk_idx, E, align, q: QDesc | None, R_cap, row_id_map, src_r
                                 _p(row_id_map), _p(src_row), _p(offsets), _p(counts), _p(workspace),
                                 workspace.numel() * workspace.element_size(), _s(stream))
     _check(rc, "mgq_moe_permute")
+
+
+def moe_route(topk_idx, E, align, R_cap, row_id_map, src_row, offsets, counts, workspace, stream=None):
+    """Routing alone (row_id_map, src_row, offsets, counts as mgq_moe_permute)."""
+    T, k = topk_idx.shape
+    _check(load().mgq_moe_route(_p(topk_idx), T, k, E, align, R_cap, _p(row_id_map), _p(src_row), _p(offsets),
+                                _p(counts), _p(workspace), workspace.numel() * workspace.element_size(),
+                                _s(stream)), "mgq_moe_route")
+
+
+def moe_permute_routed(x, k, E, q: QDesc, R_cap, row_id_map, src_row, offsets, counts, out_bf16=None,
+                       stream=None):
+    """Permute + quantise on final routing arrays from moe_route."""
+    T, H = x.shape
+    _check(load().mgq_moe_permute_routed(_p(x), T, H, k, E, ctypes.byref(q), _p(out_bf16), R_cap, _p(row_id_map),
+                                         _p(src_row), _p(offsets), _p(counts), _s(stream)),
+           "mgq_moe_permute_routed")
 
 
 def moe_permute_noalloc(x, topk_idx, E, align, q: QDesc | None, R_cap, row_id_map, src_row, offsets,

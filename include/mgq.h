@@ -170,6 +170,25 @@ int mgq_moe_permute(const void* x_bf16, int T, int H, const int32_t* topk_idx, i
                     int32_t* row_id_map, int32_t* src_row, int32_t* offsets,
                     int32_t* counts, void* workspace, size_t ws_bytes, void* stream);
 
+/* ---- the two halves of mgq_moe_permute -------------------------------------
+ * mgq_moe_route does the routing alone: it writes row_id_map, src_row,
+ * offsets and counts exactly as mgq_moe_permute does (same arguments and
+ * requirements, no x and no quantisation).
+ * mgq_moe_permute_routed then does the permute + quantise on those final
+ * routing arrays (read only): the codes and scales equal those of
+ * mgq_moe_permute with the same routing. It requires the arrays from
+ * mgq_moe_route (or mgq_moe_permute) for this T, k, E, and, for a column-wise
+ * copy, an `align` that was a multiple of 32.
+ * Splitting lets a caller route once and permute several tensors, or run the
+ * routing (index work, latency-bound) beside other work. */
+int mgq_moe_route(const int32_t* topk_idx, int T, int k, int E, int align, int64_t R_cap,
+                  int32_t* row_id_map, int32_t* src_row, int32_t* offsets, int32_t* counts,
+                  void* workspace, size_t ws_bytes, void* stream);
+int mgq_moe_permute_routed(const void* x_bf16, int T, int H, int k, int E, const mgq_qdesc* q,
+                           void* out_bf16, int64_t R_cap, const int32_t* row_id_map,
+                           const int32_t* src_row, const int32_t* offsets,
+                           const int32_t* counts, void* stream);
+
 /* ---- permute + quantise without a workspace --------------------------------
  * The pages have no counterpart of this call: it exists for callers that
  * cannot allocate device memory, such as a plugin whose host framework owns

@@ -848,3 +848,49 @@ def test_gemm_dgrad_dswiglu_equals_separate_steps(mgq, w_layout):
     assert torch.all(fus["q"][Rp:] == 0xAB)
     # and dSwiGLU against the oracle
     check_elementwise(OL.dswiglu(bf16_np(sep["dh"])[:Rp], bf16_np(gu)[:Rp], F), bf16_np(fus["dgu"])[:Rp], "dswiglu")
+
+
+@pytest.mark.parametrize("mode", ["mx", "tensor", "nvfp4"])
+def test_route_then_permute_routed_equals_permute(mgq, mode):
+    """mgq_moe_route followed by mgq_moe_permute_routed writes what one
+    mgq_moe_permute call writes (routing arrays, codes, scales, amax)."""
+    rng = np.random.default_rng(61)
+    dev = torch.device(DEV)
+    T, E, k, H = 1000, 6, 2, 512
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    x = torch.from_numpy((rng.standard_normal((T, H)) * 3).astype(np.float32)).to(torch.bfloat16).to(dev)
+    idxd = torch.from_numpy(idx).to(dev)
+    R_cap = mgq.r_cap(T, k, E, 128)
+    ws = torch.empty(max(16, mgq.permute_workspace_size(T, k, E)), dtype=torch.uint8, device=dev)
+
+    def bufs():
+        nv = mode == "nvfp4"
+        b = dict(rim=torch.full((T, k), -7, dtype=torch.int32, device=dev),
+                 src=torch.full((R_cap,), -7, dtype=torch.int32, device=dev),
+                 off=torch.zeros(E + 1, dtype=torch.int32, device=dev),
+                 cnt=torch.zeros(E, dtype=torch.int32, device=dev),
+                 q=torch.full((R_cap, H // 2 if nv else H), 0xAB, dtype=torch.uint8, device=dev),
+                 s=torch.full(((mgq.nv_scale_bytes if nv else mgq.mx_scale_bytes)(R_cap, H),), 0xCD,
+                              dtype=torch.uint8, device=dev),
+                 ts=torch.tensor([3.0], device=dev), am=torch.zeros(1, device=dev))
+        if mode == "mx":
+            b["qd"] = mgq.qdesc(mgq.E4M3, mgq.MX32_E8M0, b["q"], b["s"])
+        elif mode == "nvfp4":
+            b["qd"] = mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, b["q"], b["s"], tensor_scale=b["ts"], amax_out=b["am"])
+        else:
+            b["qd"] = mgq.qdesc(mgq.E4M3, mgq.TENSOR_F32, b["q"], None, None, None, b["ts"], b["am"])
+        return b
+
+    one, two = bufs(), bufs()
+    mgq.moe_permute(x, idxd, E, 128, one["qd"], R_cap, one["rim"], one["src"], one["off"], one["cnt"], ws)
+    mgq.moe_route(idxd, E, 128, R_cap, two["rim"], two["src"], two["off"], two["cnt"], ws)
+    mgq.moe_permute_routed(x, k, E, two["qd"], R_cap, two["rim"], two["src"], two["off"], two["cnt"])
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    Rp = int(one["off"][-1].item())
+    for key in ("rim", "off", "cnt", "q", "s", "am", "ts"):
+        assert torch.equal(one[key], two[key]), key
+    assert torch.equal(one["src"][:Rp], two["src"][:Rp])
+    rim, src, off, cnt = OR.permute_indices(idx, E, 128)
+    assert np.array_equal(two["rim"].cpu().numpy(), rim)
+    assert np.array_equal(two["src"].cpu().numpy()[:Rp], src)
