@@ -12,6 +12,8 @@
 // "FP8BlockQuantizer not work on TE", TransformerEngine issue #2393, transpose
 // identity); delayed scaling with a 1024-long history and max (issue #1152,
 // repro steps).
+#include <algorithm>
+
 #include "mgq_internal.h"
 #include "rowquant.cuh"
 
@@ -144,14 +146,19 @@ __global__ void __launch_bounds__(256) dswiglu_quant_kernel(DswigluArgs a) {
 }
 
 // ---- combine: out[t] = sum_j w_j * y[row(t, j)] (w = probs, or 1) -----------
+// CTAs of the combine kernels: at most three resident waves
+unsigned combine_grid(int T, int k) {
+  return (unsigned)std::min<int64_t>((T + kWarps - 1) / kWarps, (int64_t)num_sms() * (k <= 2 ? 3 : 2));
+}
+
 // KMAX: the largest k the instance serves (2 or 8)
 template <int KMAX>
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ rim,
                                                       const float* __restrict__ probs, int T, int k, int H,
                                                       uint16_t* __restrict__ out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kWarps + warp;
-  if (t >= T) return;
+  // CTAs stride over the tokens (a few resident waves, no tail wave)
+  for (int t = blockIdx.x * kWarps + warp; t < T; t += gridDim.x * kWarps) {
   int rows[KMAX];
   float w[KMAX];
 #pragma unroll
@@ -207,6 +214,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
     }
   }
 }
+}
 
 // ---- unpermute backward + quantise of dY, and dprobs ------------------------
 struct UnpermBwdArgs {
@@ -256,10 +264,10 @@ __global__ void __launch_bounds__(256, SC == MGQ_TENSOR_F32 ? 3 : 2) unpermute_b
     }
     return;
   }
-  const int64_t g = (int64_t)blockIdx.x * kWarps + warp;     // routing entry t * k + j
-  const bool valid = g < (int64_t)a.T * a.k;
-  const int r = valid ? a.rim[g] : -1;
   uint32_t tam = 0;
+  // the entry CTAs stride over the routing entries t * k + j
+  for (int64_t g = (int64_t)blockIdx.x * kWarps + warp; g < (int64_t)a.T * a.k; g += (int64_t)a.token_blocks * kWarps) {
+  const int r = a.rim[g];
   if (r >= 0) {
     const float ts = (SC == MGQ_TENSOR_F32) ? a.tensor_scale[0] : 1.0f;
     const float pr = a.probs[g];
@@ -317,8 +325,9 @@ __global__ void __launch_bounds__(256, SC == MGQ_TENSOR_F32 ? 3 : 2) unpermute_b
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) dp += __shfl_xor_sync(0xFFFFFFFFu, dp, o);
     if (lane == 0) a.dprobs[g] = dp;
-  } else if (valid && lane == 0) {
+  } else if (lane == 0) {
     a.dprobs[g] = 0.0f;
+  }
   }
   if (SC == MGQ_TENSOR_F32 && a.amax_out) cta_amax_atomic(tam, a.amax_out);
 }
@@ -635,7 +644,7 @@ int mgq_moe_unpermute(const void* y_bf16, const int32_t* row_id_map, const float
   MGQ_CHECK_ARG(T == 0 || (y_bf16 && row_id_map && probs && out_bf16));
   MGQ_CHECK_ARG(aligned16(y_bf16) && aligned16(out_bf16));
   if (T == 0) return MGQ_OK;
-  (k <= 2 ? combine_kernel<2> : combine_kernel<8>)<<<(T + kWarps - 1) / kWarps, 256, 0, as_stream(stream)>>>(
+  (k <= 2 ? combine_kernel<2> : combine_kernel<8>)<<<combine_grid(T, k), 256, 0, as_stream(stream)>>>(
       static_cast<const uint16_t*>(y_bf16), row_id_map, probs, T, k, H, static_cast<uint16_t*>(out_bf16));
   MGQ_LAUNCH_CHECK();
   return MGQ_OK;
@@ -647,7 +656,7 @@ int mgq_moe_permute_bwd(const void* da_bf16, const int32_t* row_id_map, int T, i
   MGQ_CHECK_ARG(T == 0 || (da_bf16 && row_id_map && dx_bf16));
   MGQ_CHECK_ARG(aligned16(da_bf16) && aligned16(dx_bf16));
   if (T == 0) return MGQ_OK;
-  (k <= 2 ? combine_kernel<2> : combine_kernel<8>)<<<(T + kWarps - 1) / kWarps, 256, 0, as_stream(stream)>>>(
+  (k <= 2 ? combine_kernel<2> : combine_kernel<8>)<<<combine_grid(T, k), 256, 0, as_stream(stream)>>>(
       static_cast<const uint16_t*>(da_bf16), row_id_map, nullptr, T, k, H, static_cast<uint16_t*>(dx_bf16));
   MGQ_LAUNCH_CHECK();
   return MGQ_OK;
@@ -677,7 +686,9 @@ int mgq_moe_unpermute_bwd(const void* dout_bf16, const void* y_bf16, const int32
   a.amax_out = q->amax_out;
   a.dprobs = dprobs;
   a.rceil = q->e8m0_mode == MGQ_E8M0_RCEIL;
-  a.token_blocks = (int)(((int64_t)T * k + kWarps - 1) / kWarps);
+  // entry CTAs: at most a few resident waves (they stride over the entries)
+  a.token_blocks = (int)std::min<int64_t>(((int64_t)T * k + kWarps - 1) / kWarps,
+                                          (int64_t)num_sms() * (q->scaling == MGQ_TENSOR_F32 ? 3 : 2));
   const unsigned grid = (unsigned)(a.token_blocks + E);
   if (q->col.data && q->scaling != MGQ_TENSOR_F32 && q->scaling != MGQ_MX32_E8M0) return MGQ_ERR_UNSUPPORTED;
   MGQ_DISPATCH_Q(q, unpermute_bwd_kernel, grid, a);

@@ -8,6 +8,8 @@
 // not work on TE" (TransformerEngine issue #2393, maintainer replies);
 // dynamic quantisation in front of the scaled grouped mm: "float8 moe
 // training conversion API prototype" (pytorch/ao PR #2275, description).
+#include <algorithm>
+
 #include "device_common.cuh"
 #include "mgq_internal.h"
 #include "rowquant.cuh"
@@ -205,7 +207,7 @@ __device__ __forceinline__ void load_block32(const uint16_t* src, uint32_t (&w)[
 }
 
 template <int SC, int DT>
-__global__ void __launch_bounds__(256) permute_quant_kernel(PermuteArgs a) {
+__global__ void __launch_bounds__(256, 4) permute_quant_kernel(PermuteArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = a.H;
   if ((int)blockIdx.x >= a.token_blocks) {
@@ -230,32 +232,35 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(PermuteArgs a) {
     }
     return;
   }
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= a.T) return;
-  // the first chunk's loads go out before the destination rows are resolved,
-  // and every chunk's loads before the previous chunk is processed
-  auto load_chunk = [&](int c0, uint32_t (&w)[16]) {
+  // token CTAs stride over the tokens (a few waves' worth of CTAs, no tail
+  // wave); a warp keeps the next 1024-element chunk in flight, across token
+  // boundaries too
+  const int tstride = a.token_blocks * 8;
+  auto load_chunk = [&](int tt, int c0, uint32_t (&w)[16]) {
     const int c = c0 + lane * 32;
     if (c < H) {
-      load_block32(a.x + (int64_t)t * H + c, w);
+      load_block32(a.x + (int64_t)tt * H + c, w);
     } else {
 #pragma unroll
       for (int i = 0; i < 16; ++i) w[i] = 0;
     }
   };
-  uint32_t wnext[16];
-  load_chunk(0, wnext);
-  int dest[8];
-  token_rows(a, t, lane, dest);
   const float ts = (SC == MGQ_TENSOR_F32) ? a.tensor_scale[0] : 1.0f;
   uint32_t tamax = 0;   // per-tensor amax (bf16 bits in the high half)
+  int t = blockIdx.x * 8 + warp;
+  uint32_t wnext[16];
+  if (t < a.T) load_chunk(t, 0, wnext);
+  for (; t < a.T; t += tstride) {
+  int dest[8];
+  token_rows(a, t, lane, dest);
   for (int c0 = 0; c0 < H; c0 += 1024) {
     const int c = c0 + lane * 32;
     const bool active = c < H;       // every lane stays in the loop (shuffles below)
     uint32_t w[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) w[i] = wnext[i];
-    if (c0 + 1024 < H) load_chunk(c0 + 1024, wnext);
+    if (c0 + 1024 < H) load_chunk(t, c0 + 1024, wnext);
+    else if (t + tstride < a.T) load_chunk(t + tstride, 0, wnext);
     uint32_t am2 = 0;
 #pragma unroll
     for (int i = 0; i < 16; ++i) am2 = absmax_bf16x2(am2, w[i]);
@@ -317,6 +322,7 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(PermuteArgs a) {
       }
     }
   }
+  }
   if (SC == MGQ_TENSOR_F32 && a.amax_out) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) tamax = max(tamax, __shfl_xor_sync(0xFFFFFFFFu, tamax, o));
@@ -341,10 +347,10 @@ __global__ void __launch_bounds__(256) permute_quant_nv_kernel(PermuteArgs a) {
     }
     return;
   }
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= a.T) return;
   const float s_g = nv_global_scale(*a.amax_out);
-  if (t == 0 && lane == 0) *a.s_out = s_g;
+  if (blockIdx.x == 0 && warp == 0 && lane == 0) *a.s_out = s_g;
+  // token CTAs stride over the tokens
+  for (int t = blockIdx.x * 8 + warp; t < a.T; t += a.token_blocks * 8) {
   int dest[8];
   token_rows(a, t, lane, dest);
   for (int c0 = 0; c0 < H; c0 += 1024) {
@@ -364,6 +370,7 @@ __global__ void __launch_bounds__(256) permute_quant_nv_kernel(PermuteArgs a) {
       if (j >= a.k || !act) break;
       if (dest[j] >= 0) store32_nv(o, a.codes, a.scales, dest[j], c, H, lane);
     }
+  }
   }
 }
 
@@ -500,7 +507,11 @@ int permute_impl(const void* x_bf16, int T, int H, int k, int E, const mgq_qdesc
   a.s_out = q->tensor_scale;
   a.R_cap = R_cap;
   a.e8m0_rceil = q->e8m0_mode == MGQ_E8M0_RCEIL;
-  a.token_blocks = (T + 7) / 8;
+  // token CTAs: FP8 kernels stride over the tokens from at most four resident
+  // waves (keeping the next chunk in flight across tokens); the NVFP4 kernel,
+  // whose tokens fan out to many destinations, runs one token per warp
+  a.token_blocks = q->scaling == MGQ_NV16_UE4M3 ? (T + 7) / 8
+                                                : (int)std::min<int64_t>((T + 7) / 8, (int64_t)num_sms() * 4);
   a.err = err;
   dim3 grid((unsigned)(a.token_blocks + E));
   const int sc = q->scaling, dt = q->dtype;
