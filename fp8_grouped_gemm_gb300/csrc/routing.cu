@@ -88,16 +88,27 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int32_t* __restrict__ 
   __shared__ int s_tot[kMaxExperts];
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_wsum[32];
+  __shared__ int s_seg[32][33];      // [warp = chunk segment][lane = expert of the block]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // expert totals: one warp per expert, lanes over chunks
-  for (int e = warp; e < E; e += 32) {
+  // Blocks of 32 experts (lane = expert); warp w takes the contiguous chunk
+  // segment [w S, (w + 1) S), so every load reads 32 consecutive experts of
+  // one chunk. Pass 1: per-segment sums -> expert totals.
+  const int S = (nchunks + 31) / 32;
+  const int c_lo = warp * S, c_hi = min(nchunks, c_lo + S);
+  for (int eb = 0; eb < E; eb += 32) {
+    const int e = eb + lane;
     int t = 0;
-    for (int c = lane; c < nchunks; c += 32) t += cnt[(int64_t)c * E + e];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
-    if (lane == 0) s_tot[e] = t;
+    if (e < E)
+      for (int c = c_lo; c < c_hi; ++c) t += cnt[(int64_t)c * E + e];
+    s_seg[warp][lane] = t;
+    __syncthreads();
+    if (warp == 0 && e < E) {
+      int tot = 0;
+      for (int w = 0; w < 32; ++w) tot += s_seg[w][lane];
+      s_tot[e] = tot;
+    }
+    __syncthreads();
   }
-  __syncthreads();
   // exclusive scan of the padded totals (E <= 1024: one per thread)
   const int e0 = threadIdx.x;
   const int pad = e0 < E ? (s_tot[e0] + align - 1) / align * align : 0;
@@ -120,16 +131,25 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int32_t* __restrict__ 
     offsets[E] = s_wsum[31];
   }
   __syncthreads();
-  // per-(chunk, expert) base rows: one warp per expert, exclusive scan over chunks
-  for (int e = warp; e < E; e += 32) {
-    int run = s_off[e];
-    for (int c0 = 0; c0 < nchunks; c0 += 32) {
-      const int c = c0 + lane;
-      const int v = c < nchunks ? cnt[(int64_t)c * E + e] : 0;
-      const int inc = warp_incl_scan(v, lane);
-      if (c < nchunks) cnt[(int64_t)c * E + e] = run + inc - v;
-      run += __shfl_sync(0xFFFFFFFFu, inc, 31);
+  // Pass 2: per-(chunk, expert) base rows (in place): the expert's offset plus
+  // the segments before this warp's, then a running sum along the segment.
+  for (int eb = 0; eb < E; eb += 32) {
+    const int e = eb + lane;
+    int t = 0;
+    if (e < E)
+      for (int c = c_lo; c < c_hi; ++c) t += cnt[(int64_t)c * E + e];
+    s_seg[warp][lane] = t;
+    __syncthreads();
+    if (e < E) {
+      int run = s_off[e];
+      for (int w = 0; w < warp; ++w) run += s_seg[w][lane];
+      for (int c = c_lo; c < c_hi; ++c) {
+        const int v = cnt[(int64_t)c * E + e];
+        cnt[(int64_t)c * E + e] = run;
+        run += v;
+      }
     }
+    __syncthreads();
   }
   // filler rows of every group
   for (int e = warp; e < E; e += 32)
