@@ -481,7 +481,7 @@ int check_route_args(int T, int k, int E, int align, int64_t R_cap, const void* 
                      const void* offsets, const void* counts) {
   MGQ_CHECK_ARG(T >= 0 && k >= 1 && k <= 8 && E >= 1 && E <= kMaxExperts && k <= E);
   MGQ_CHECK_ARG(align >= 1 && (align % 32 == 0 || align == 1));
-  MGQ_CHECK_ARG(rim && src_row && offsets && counts);
+  MGQ_CHECK_ARG((T == 0 || rim) && src_row && offsets && counts);   // no entries: row_id_map may be null
   const int64_t n = (int64_t)T * k;
   const int64_t need = ((n + (int64_t)E * (align - 1)) + 127) / 128 * 128;
   MGQ_CHECK_ARG(R_cap >= need && R_cap % 128 == 0 && R_cap < (1ll << 31));

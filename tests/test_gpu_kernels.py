@@ -48,6 +48,7 @@ PERMUTE_CASES = [
     (777, 16, 8, 128, 32, (3,)),
     (5, 4, 4, 1024, 128, ()),
     (2500, 128, 8, 256, 128, ()),
+    (3000, 1024, 2, 128, 32, ()),      # the largest expert count: most groups empty or tiny
 ]
 
 
@@ -894,3 +895,50 @@ def test_route_then_permute_routed_equals_permute(mgq, mode):
     rim, src, off, cnt = OR.permute_indices(idx, E, 128)
     assert np.array_equal(two["rim"].cpu().numpy(), rim)
     assert np.array_equal(two["src"].cpu().numpy()[:Rp], src)
+
+
+def test_empty_batch_through_every_call(mgq):
+    """T = 0 tokens: routing gives empty groups (offsets all zero), the
+    permute writes nothing, the GEMMs compute nothing (wgrad writes zeros for
+    the empty groups, or keeps dW with beta = 1), and the combine steps return
+    at once; no call reports an error."""
+    dev = torch.device(DEV)
+    E, k, H, N = 4, 2, 256, 256
+    T = 0
+    R_cap = mgq.r_cap(T, k, E, 128)
+    idx = torch.empty(0, k, dtype=torch.int32, device=dev)
+    rim = torch.empty(0, k, dtype=torch.int32, device=dev)
+    src = torch.full((R_cap,), -9, dtype=torch.int32, device=dev)
+    off = torch.full((E + 1,), -9, dtype=torch.int32, device=dev)
+    cnt = torch.full((E,), -9, dtype=torch.int32, device=dev)
+    ws = torch.empty(max(16, mgq.permute_workspace_size(T, k, E)), dtype=torch.uint8, device=dev)
+    mgq.moe_route(idx, E, 128, R_cap, rim, src, off, cnt, ws)
+    x = torch.empty(0, H, dtype=torch.bfloat16, device=dev)
+    codes = torch.full((R_cap, H), 0xAB, dtype=torch.uint8, device=dev)
+    s = torch.tensor([1.0], device=dev)
+    q = mgq.qdesc(mgq.E4M3, mgq.TENSOR_F32, codes, None, None, None, s, None)
+    mgq.moe_permute_routed(x, k, E, q, R_cap, rim, src, off, cnt)
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    assert torch.all(off == 0) and torch.all(cnt == 0)
+    assert torch.all(codes == 0xAB)
+    # GEMMs over all-empty groups
+    w = torch.zeros(E * N, H, dtype=torch.uint8, device=dev)
+    A = mgq.operand(codes, s, H, mgq.E4M3)
+    W = mgq.operand(w, torch.ones(E, device=dev), H, mgq.E4M3)
+    Y = torch.full((R_cap, N), 3.0, dtype=torch.bfloat16, device=dev)
+    mgq.grouped_gemm_fwd(A, W, mgq.TENSOR_F32, off, E, R_cap, N, H, Y)
+    dW = torch.full((E, N, H), 5.0, dtype=torch.float32, device=dev)
+    dYc = mgq.operand(torch.zeros(N, R_cap, dtype=torch.uint8, device=dev), s, R_cap, mgq.E5M2)
+    Ac = mgq.operand(torch.zeros(H, R_cap, dtype=torch.uint8, device=dev), s, R_cap, mgq.E4M3)
+    mgq.grouped_gemm_wgrad(dYc, Ac, mgq.TENSOR_F32, off, E, R_cap, N, H, dW, 0.0)
+    dW1 = torch.full((E, N, H), 5.0, dtype=torch.float32, device=dev)
+    mgq.grouped_gemm_wgrad(dYc, Ac, mgq.TENSOR_F32, off, E, R_cap, N, H, dW1, 1.0)
+    out = torch.empty(0, H, dtype=torch.bfloat16, device=dev)
+    mgq.moe_unpermute(Y, rim, torch.empty(0, k, device=dev), out)
+    mgq.moe_permute_bwd(Y, rim, out)
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    assert torch.all(Y == 3.0)                 # no rows to compute
+    assert torch.all(dW == 0.0)                # empty groups: zeros
+    assert torch.all(dW1 == 5.0)               # beta = 1: untouched
