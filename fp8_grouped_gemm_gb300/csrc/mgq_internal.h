@@ -51,10 +51,11 @@ int rowcol_swiglu(const uint16_t* gu, int64_t R_cap, int64_t F, const int32_t* r
 int rowcol_dswiglu(const uint16_t* dh, const uint16_t* gu, int64_t R_cap, int64_t F, const int32_t* rows_used,
                    uint16_t* out, const mgq_qdesc* q, cudaStream_t s);
 
-// Column-wise copies only (MX or per-tensor), of the permuted X rows and of
+// Column-wise copies (MX or per-tensor) of the permuted X rows, with the
+// row-wise codes too when `with_rows`, and column-wise copies only of
 // dY = probs * dout rows, gathered through src_row (quant_tile.cu).
-int col_gather_x(const uint16_t* x, const int32_t* src_row, int k, int64_t H, int64_t R_cap, const int32_t* rows_used,
-                 const mgq_qdesc* q, cudaStream_t s);
+int gather_x_rowcol(const uint16_t* x, const int32_t* src_row, int k, int64_t H, int64_t R_cap,
+                    const int32_t* rows_used, bool with_rows, const mgq_qdesc* q, cudaStream_t s);
 int col_gather_dy(const uint16_t* dout, const float* probs, const int32_t* src_row, int k, int64_t H, int64_t R_cap,
                   const int32_t* rows_used, const mgq_qdesc* q, cudaStream_t s);
 

@@ -23,28 +23,29 @@ namespace {
 
 constexpr int TR = 128, TC = 128;  // tile rows x columns (per part)
 
+// Source kinds (kKind):
+//  kPlain    the tile is a block of a bf16 matrix (load_raw: 16-byte copies)
+//  kGather   row r of the tile is a gathered bf16 row (row_offset), optionally
+//            multiplied by a per-row float32 factor; the row offsets are
+//            resolved once per tile into shared memory
+//  kComputed the values are computed elementwise from kLoads bf16 operands
+//            (fetch, then make), loads of several chunks in flight at once
 // kExactBf16: every value the source produces is a bf16 value, so the tile
 // keeps it as 2 bytes in shared memory.
-// kRaw: the source hands out its bf16 bits unchanged (load_raw), so the tile
-// is filled by 16-byte copies with all loads of a thread in flight at once.
+enum SrcKind { kPlain, kGather, kComputed };
+
 struct SrcPlain {
+  static constexpr int kKind = kPlain;
   static constexpr int kParts = 1;
   static constexpr bool kExactBf16 = true;
-  static constexpr bool kRaw = true;
   const uint16_t* x;
   int64_t ld;
   __device__ __forceinline__ uint4 load_raw(int64_t r, int64_t c) const {
     return __ldg(reinterpret_cast<const uint4*>(x + r * ld + c));
   }
-  __device__ __forceinline__ void load8(int64_t r, int64_t c, float* v, float*) const {
-    const uint4 w = __ldg(reinterpret_cast<const uint4*>(x + r * ld + c));
-    v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
-    v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
-  }
 };
 
-__device__ __forceinline__ void load8_bf16(const uint16_t* p, float* v) {
-  const uint4 w = __ldg(reinterpret_cast<const uint4*>(p));
+__device__ __forceinline__ void unpack8_bf16(const uint4 w, float* v) {
   v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
   v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
 }
@@ -55,19 +56,24 @@ __device__ __forceinline__ void store8_bf16(uint16_t* p, const float* v) {
 
 // h = bf16(silu(g) * u), g = gu[:, :F], u = gu[:, F:]; h optionally written out
 struct SrcSwiglu {
+  static constexpr int kKind = kComputed;
   static constexpr int kParts = 1;
   static constexpr bool kExactBf16 = true;
-  static constexpr bool kRaw = false;
+  static constexpr int kLoads = 2;
   const uint16_t* gu;
   int64_t F;
   uint16_t* h_out;
-  __device__ __forceinline__ void load8(int64_t r, int64_t c, float* v, float*) const {
+  __device__ __forceinline__ void fetch(int64_t r, int64_t c, uint4* w) const {
+    w[0] = __ldg(reinterpret_cast<const uint4*>(gu + r * 2 * F + c));
+    w[1] = __ldg(reinterpret_cast<const uint4*>(gu + r * 2 * F + F + c));
+  }
+  __device__ __forceinline__ void make(const uint4* w, int64_t r, int64_t c, bool valid, float* v, float*) const {
     float g[8], u[8];
-    load8_bf16(gu + r * 2 * F + c, g);
-    load8_bf16(gu + r * 2 * F + F + c, u);
+    unpack8_bf16(w[0], g);
+    unpack8_bf16(w[1], u);
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] = swiglu_bf16(g[i], u[i]);
-    if (h_out) store8_bf16(h_out + r * F + c, v);
+    if (h_out && valid) store8_bf16(h_out + r * F + c, v);
   }
 };
 
@@ -75,23 +81,28 @@ struct SrcSwiglu {
 // and part 1 = dU = dh silu(g), s = sigmoid(g); both written to [dG | dU]
 // (columns f and F + f) when requested. One read of dh, g, u serves both.
 struct SrcDswiglu {
+  static constexpr int kKind = kComputed;
   static constexpr int kParts = 2;
   static constexpr bool kExactBf16 = true;
-  static constexpr bool kRaw = false;
+  static constexpr int kLoads = 3;
   const uint16_t* dh;
   const uint16_t* gu;
   int64_t F;
   uint16_t* out;
-  __device__ __forceinline__ void load8(int64_t r, int64_t f, float* dg, float* du) const {
+  __device__ __forceinline__ void fetch(int64_t r, int64_t f, uint4* w) const {
+    w[0] = __ldg(reinterpret_cast<const uint4*>(dh + r * F + f));
+    w[1] = __ldg(reinterpret_cast<const uint4*>(gu + r * 2 * F + f));
+    w[2] = __ldg(reinterpret_cast<const uint4*>(gu + r * 2 * F + F + f));
+  }
+  __device__ __forceinline__ void make(const uint4* w, int64_t r, int64_t f, bool valid, float* dg,
+                                       float* du) const {
     float d[8], g[8], u[8];
-    load8_bf16(dh + r * F + f, d);
-    load8_bf16(gu + r * 2 * F + f, g);
-    load8_bf16(gu + r * 2 * F + F + f, u);
+    unpack8_bf16(w[0], d);
+    unpack8_bf16(w[1], g);
+    unpack8_bf16(w[2], u);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      dswiglu_bf16(d[i], g[i], u[i], dg[i], du[i]);
-    }
-    if (out) {
+    for (int i = 0; i < 8; ++i) dswiglu_bf16(d[i], g[i], u[i], dg[i], du[i]);
+    if (out && valid) {
       store8_bf16(out + r * 2 * F + f, dg);
       store8_bf16(out + r * 2 * F + F + f, du);
     }
@@ -101,51 +112,39 @@ struct SrcDswiglu {
 // row r of the permuted matrix: X[t] for the (token, slot) entry e = src_row[r]
 // (t = e / k), zeros for filler rows
 struct SrcGatherX {
+  static constexpr int kKind = kGather;
   static constexpr int kParts = 1;
   static constexpr bool kExactBf16 = true;
-  static constexpr bool kRaw = true;
   const uint16_t* x;
   const int32_t* src_row;
   int k;
   int64_t H;
-  __device__ __forceinline__ uint4 load_raw(int64_t r, int64_t c) const {
+  // element offset of the source row of r (-1: zero row) and its factor
+  __device__ __forceinline__ int64_t row_offset(int64_t r, float&) const {
     const int e = src_row[r];
-    return e < 0 ? make_uint4(0, 0, 0, 0) : __ldg(reinterpret_cast<const uint4*>(x + (int64_t)(e / k) * H + c));
+    return e < 0 ? -1 : (int64_t)(e / k) * H;
   }
-  __device__ __forceinline__ void load8(int64_t r, int64_t c, float* v, float*) const {
-    const int e = src_row[r];
-    if (e < 0) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = 0.0f;
-      return;
-    }
-    load8_bf16(x + (int64_t)(e / k) * H + c, v);
-  }
+  __device__ __forceinline__ const uint16_t* base() const { return x; }
 };
 
 // row r of dY = float32(probs[e] * dout[t]) for the entry e = src_row[r]
 // (the unpermute backward), zeros for filler rows
 struct SrcGatherDy {
+  static constexpr int kKind = kGather;
   static constexpr int kParts = 1;
   static constexpr bool kExactBf16 = false;   // float32 products
-  static constexpr bool kRaw = false;
   const uint16_t* dout;
   const float* probs;
   const int32_t* src_row;
   int k;
   int64_t H;
-  __device__ __forceinline__ void load8(int64_t r, int64_t c, float* v, float*) const {
+  __device__ __forceinline__ int64_t row_offset(int64_t r, float& p) const {
     const int e = src_row[r];
-    if (e < 0) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = 0.0f;
-      return;
-    }
-    load8_bf16(dout + (int64_t)(e / k) * H + c, v);
-    const float p = probs[e];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(p, v[i]);
+    if (e < 0) return -1;
+    p = probs[e];
+    return (int64_t)(e / k) * H;
   }
+  __device__ __forceinline__ const uint16_t* base() const { return dout; }
 };
 
 struct RowColArgs {
@@ -202,45 +201,89 @@ __global__ void __launch_bounds__(256, (Src::kParts == 2 || !Src::kExactBf16) ? 
   const float ts = (SC == MGQ_TENSOR_F32) ? a.tensor_scale[g] : 1.0f;
   // ---- load: TR rows x 16 chunks of 8 columns, 8 chunks per thread
   uint32_t am = 0;
-  if constexpr (Src::kRaw) {
-    // all eight 16-byte loads in flight, then copied into the tile as they are
+  if constexpr (Src::kKind == kPlain || Src::kKind == kGather) {
+    // gathered rows: the source offsets (and factors) of the tile's rows first
+    __shared__ int64_t s_off[Src::kKind == kGather ? TR : 1];
+    __shared__ float s_fac[Src::kKind == kGather ? TR : 1];
+    if constexpr (Src::kKind == kGather) {
+      if (tid < TR) {
+        float f = 0.0f;
+        const int64_t off = (r0 + tid < nrows) ? src.row_offset(r0 + tid, f) : -1;
+        s_off[tid] = off;
+        s_fac[tid] = f;
+      }
+      __syncthreads();
+    }
+    // all eight 16-byte loads in flight, then copied into the tile
     uint4 w[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int chunk = tid + 256 * i;
       const int rr = chunk >> 4, cc = (chunk & 15) * 8;
-      w[i] = (r0 + rr < nrows) ? src.load_raw(r0 + rr, c0 + cc) : make_uint4(0, 0, 0, 0);
+      if constexpr (Src::kKind == kGather) {
+        const int64_t off = s_off[rr];
+        w[i] = off >= 0 ? __ldg(reinterpret_cast<const uint4*>(src.base() + off + c0 + cc)) : make_uint4(0, 0, 0, 0);
+      } else {
+        w[i] = (r0 + rr < nrows) ? src.load_raw(r0 + rr, c0 + cc) : make_uint4(0, 0, 0, 0);
+      }
     }
-    uint32_t am2 = 0;
+    if constexpr (Src::kExactBf16) {
+      uint32_t am2 = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int chunk = tid + 256 * i;
-      const int rr = chunk >> 4, cc = (chunk & 15) * 8;
-      am2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(am2, w[i].x), w[i].y), w[i].z), w[i].w);
-      *reinterpret_cast<uint4*>(&tile[rr * LD + cc]) = w[i];
-    }
-    am = fold_bf16x2(am2);
-  } else {
-#pragma unroll 4
-  for (int i = 0; i < 8; ++i) {
-    const int chunk = tid + 256 * i;
-    const int rr = chunk >> 4, cc = (chunk & 15) * 8;
-    float v[P][8];
-    if (r0 + rr < nrows) {
-      src.load8(r0 + rr, c0 + cc, v[0], v[P - 1]);
+      for (int i = 0; i < 8; ++i) {
+        const int chunk = tid + 256 * i;
+        const int rr = chunk >> 4, cc = (chunk & 15) * 8;
+        am2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(am2, w[i].x), w[i].y), w[i].z), w[i].w);
+        *reinterpret_cast<uint4*>(&tile[rr * LD + cc]) = w[i];
+      }
+      am = fold_bf16x2(am2);
     } else {
 #pragma unroll
-      for (int p = 0; p < P; ++p)
+      for (int i = 0; i < 8; ++i) {
+        const int chunk = tid + 256 * i;
+        const int rr = chunk >> 4, cc = (chunk & 15) * 8;
+        const float f = Src::kKind == kGather ? s_fac[rr] : 1.0f;
+        float v[8];
+        unpack8_bf16(w[i], v);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[p][j] = 0.0f;
+        for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(f, v[j]);
+        am = max(am, absmax_bits_f32(v, 8));
+        float4* d = reinterpret_cast<float4*>(&tile[rr * LD + cc]);
+        d[0] = make_float4(v[0], v[1], v[2], v[3]);
+        d[1] = make_float4(v[4], v[5], v[6], v[7]);
+      }
     }
+  } else {
+    // computed values: the operands of kBatch chunks loaded together
+    constexpr int kBatch = 4;
+#pragma unroll 1
+    for (int b = 0; b < 8; b += kBatch) {
+      uint4 w[kBatch][Src::kLoads];
 #pragma unroll
-    for (int p = 0; p < P; ++p) {
-      am = max(am, absmax_bits_f32(v[p], 8));
+      for (int j = 0; j < kBatch; ++j) {
+        const int chunk = tid + 256 * (b + j);
+        const int rr = chunk >> 4, cc = (chunk & 15) * 8;
+        if (r0 + rr < nrows) {
+          src.fetch(r0 + rr, c0 + cc, w[j]);
+        } else {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) tile[(p * TR + rr) * LD + cc + j] = TT::put(v[p][j]);
+          for (int l = 0; l < Src::kLoads; ++l) w[j][l] = make_uint4(0, 0, 0, 0);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int chunk = tid + 256 * (b + j);
+        const int rr = chunk >> 4, cc = (chunk & 15) * 8;
+        float v[P][8];
+        src.make(w[j], r0 + rr, c0 + cc, r0 + rr < nrows, v[0], v[P - 1]);
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+          am = max(am, absmax_bits_f32(v[p], 8));
+#pragma unroll
+          for (int q = 0; q < 8; ++q) tile[(p * TR + rr) * LD + cc + q] = TT::put(v[p][q]);
+        }
+      }
     }
-  }
   }
   __syncthreads();
   // ---- row-wise: the P*TR (part, row) pairs, 4 per warp at a time; 8 lanes
@@ -253,26 +296,30 @@ __global__ void __launch_bounds__(256, (Src::kParts == 2 || !Src::kExactBf16) ? 
       const int64_t r = r0 + rr;
       const int64_t cb = c0 + p * a.part_off;     // first output column of this part
       float v[16];
+      uint32_t m = 0;   // |v| maximum as float bits (MX)
       const T* src = &tile[(p * TR + rr) * LD + 16 * seg];
       if constexpr (Src::kExactBf16) {
         const uint4 w0 = reinterpret_cast<const uint4*>(src)[0], w1 = reinterpret_cast<const uint4*>(src)[1];
         const uint32_t ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        uint32_t m2 = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           v[2 * i] = bf16_lo(ww[i]);
           v[2 * i + 1] = bf16_hi(ww[i]);
+          m2 = absmax_bf16x2(m2, ww[i]);
         }
+        m = fold_bf16x2(m2);
       } else {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const float4 f = reinterpret_cast<const float4*>(src)[q];
           v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
         }
+        if (SC == MGQ_MX32_E8M0) m = absmax_bits_f32(v, 16);
       }
       float mult = ts;
       uint32_t scode = 0;
       if (SC == MGQ_MX32_E8M0) {
-        uint32_t m = absmax_bits_f32(v, 16);
         m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));        // the other half of the block
         const int e = mx_exponent(m, FmtInfo<DT>::emax, a.rceil != 0);
         mult = mx_multiplier(e);
@@ -386,9 +433,14 @@ int launch_rowcol(const Src& src, const mgq_qdesc* q, RowColArgs a, cudaStream_t
   const int sc = q->scaling, dt = q->dtype;
   if (sc == MGQ_MX32_E8M0 && dt == MGQ_E4M3) return launch_rowcol_t<Src, MGQ_MX32_E8M0, MGQ_E4M3>(src, a, grid, s);
   if (sc == MGQ_MX32_E8M0 && dt == MGQ_E5M2) return launch_rowcol_t<Src, MGQ_MX32_E8M0, MGQ_E5M2>(src, a, grid, s);
-  if (sc == MGQ_TENSOR_F32 && dt == MGQ_E4M3) return launch_rowcol_t<Src, MGQ_TENSOR_F32, MGQ_E4M3>(src, a, grid, s);
-  if (sc == MGQ_TENSOR_F32 && dt == MGQ_E5M2) return launch_rowcol_t<Src, MGQ_TENSOR_F32, MGQ_E5M2>(src, a, grid, s);
-  return MGQ_ERR_UNSUPPORTED;
+  // per-tensor column copies of gathered rows are transposed casts of the row codes
+  if constexpr (Src::kKind == kGather) {
+    return MGQ_ERR_UNSUPPORTED;
+  } else {
+    if (sc == MGQ_TENSOR_F32 && dt == MGQ_E4M3) return launch_rowcol_t<Src, MGQ_TENSOR_F32, MGQ_E4M3>(src, a, grid, s);
+    if (sc == MGQ_TENSOR_F32 && dt == MGQ_E5M2) return launch_rowcol_t<Src, MGQ_TENSOR_F32, MGQ_E5M2>(src, a, grid, s);
+    return MGQ_ERR_UNSUPPORTED;
+  }
 }
 
 RowColArgs make_args(const mgq_qdesc* q, int64_t rows_cap, const int32_t* rows_used, int64_t C, int64_t M,
@@ -425,10 +477,10 @@ int rowcol_dswiglu(const uint16_t* dh, const uint16_t* gu, int64_t R_cap, int64_
   return launch_rowcol(SrcDswiglu{dh, gu, F, out}, q, make_args(q, R_cap, rows_used, 2 * F, R_cap, F), s);
 }
 
-int col_gather_x(const uint16_t* x, const int32_t* src_row, int k, int64_t H, int64_t R_cap, const int32_t* rows_used,
-                 const mgq_qdesc* q, cudaStream_t s) {
+int gather_x_rowcol(const uint16_t* x, const int32_t* src_row, int k, int64_t H, int64_t R_cap,
+                    const int32_t* rows_used, bool with_rows, const mgq_qdesc* q, cudaStream_t s) {
   RowColArgs a = make_args(q, R_cap, rows_used, H, R_cap);
-  a.row_codes = nullptr;       // the row-wise codes come from the permute kernel
+  if (!with_rows) a.row_codes = nullptr;   // the row-wise codes come from the permute kernel
   return launch_rowcol(SrcGatherX{x, src_row, k, H}, q, a, s);
 }
 

@@ -508,11 +508,19 @@ int route_impl(const int32_t* topk_idx, int T, int k, int E, int align, int32_t*
   return MGQ_OK;
 }
 
+// MX with a column-wise copy and no bf16 copy: one tile pass over the
+// permuted rows writes both copies (needs the final src_row)
+bool permute_fused_rowcol(const mgq_qdesc* q, const void* out_bf16) {
+  return q->scaling == MGQ_MX32_E8M0 && q->col.data && !out_bf16;
+}
+
 // permute + quantise of the token rows to their routed rows (row_id_map final,
 // or chunk ranks to resolve with `idx` and the chunk bases `cnt`)
 int permute_impl(const void* x_bf16, int T, int H, int k, int E, const mgq_qdesc* q, void* out_bf16, int64_t R_cap,
                  int32_t* row_id_map, int32_t* src_row, const int32_t* offsets, const int32_t* counts,
                  const int32_t* idx, const int32_t* cnt, bool resolve, int* err, cudaStream_t s) {
+  if (!resolve && permute_fused_rowcol(q, out_bf16))
+    return gather_x_rowcol(static_cast<const uint16_t*>(x_bf16), src_row, k, H, R_cap, offsets + E, true, q, s);
   PermuteArgs a;
   a.x = static_cast<const uint16_t*>(x_bf16);
   a.T = T; a.H = H; a.k = k; a.E = E;
@@ -558,7 +566,7 @@ int permute_impl(const void* x_bf16, int T, int H, int k, int E, const mgq_qdesc
     int rc = q->scaling == MGQ_TENSOR_F32
                  ? launch_transpose_u8(static_cast<const uint8_t*>(q->row.data), H,
                                        static_cast<uint8_t*>(q->col.data), R_cap, offsets + E, R_cap, H, s)
-                 : col_gather_x(a.x, src_row, k, H, R_cap, offsets + E, q, s);
+                 : gather_x_rowcol(a.x, src_row, k, H, R_cap, offsets + E, false, q, s);
     if (rc != MGQ_OK) return rc;
   }
   return MGQ_OK;
@@ -582,11 +590,13 @@ int mgq_moe_permute(const void* x_bf16, int T, int H, const int32_t* topk_idx, i
   if (!err) return MGQ_ERR_CUDA;
   cudaStream_t s = as_stream(stream);
   int32_t* cnt = static_cast<int32_t*>(workspace);
-  // two routing launches; the permute kernel resolves the final rows
-  if ((rc = route_impl(topk_idx, T, k, E, align, row_id_map, src_row, offsets, counts, cnt, false, err, s)) != MGQ_OK)
+  // two routing launches and the permute kernel resolving the final rows, or
+  // (fused row + column copies) three routing launches and the tile pass
+  const bool fused = permute_fused_rowcol(q, out_bf16);
+  if ((rc = route_impl(topk_idx, T, k, E, align, row_id_map, src_row, offsets, counts, cnt, fused, err, s)) != MGQ_OK)
     return rc;
   return permute_impl(x_bf16, T, H, k, E, q, out_bf16, R_cap, row_id_map, src_row, offsets, counts, topk_idx, cnt,
-                      true, err, s);
+                      !fused, err, s);
 }
 
 int mgq_moe_route(const int32_t* topk_idx, int T, int k, int E, int align, int64_t R_cap, int32_t* row_id_map,

@@ -354,6 +354,8 @@ class ExpertLayer:
         if self.fused_swiglu and self.delayed:
             bwd -= 1                                    # dSwiGLU in the down dgrad epilogue
         if not self.mn:
-            fwd += 1                                    # column copy of x (h's is fused into SwiGLU)
+            if self.delayed:
+                fwd += 1                                # column copy of x (MX: fused into the permute;
+                                                        # h's is fused into SwiGLU)
             bwd += 1                                    # column copy of dY2
         return fwd + wq + bwd + (2 if self.delayed else 0)

@@ -53,7 +53,8 @@ PERMUTE_CASES = [
 
 
 @pytest.mark.parametrize("case", PERMUTE_CASES, ids=lambda c: f"T{c[0]}E{c[1]}k{c[2]}H{c[3]}a{c[4]}")
-@pytest.mark.parametrize("mode", ["mx_e4m3", "mx_e5m2", "tensor_e4m3", "blk_e4m3", "nvfp4"])
+@pytest.mark.parametrize("mode", ["mx_e4m3", "mx_e5m2", "mx_col_e4m3", "mx_col_e5m2", "tensor_e4m3", "blk_e4m3",
+                                  "nvfp4"])
 def test_permute_quantize(mgq, case, mode):
     T, E, k, H, align, empty = case
     rng = np.random.default_rng(T * 7 + E)
@@ -78,6 +79,12 @@ def test_permute_quantize(mgq, case, mode):
         amax = torch.full((1,), 7.0, dtype=torch.float32, device=dev)     # overwritten by the call
         sg = torch.zeros(1, dtype=torch.float32, device=dev)
         q = mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, codes, sc, tensor_scale=sg, amax_out=amax)
+    elif mode.startswith("mx_col"):
+        # row-wise and column-wise (blocks of 32 along the permuted rows) copies
+        sc = torch.full((mgq.mx_scale_bytes(R, H),), 0xCD, dtype=torch.uint8, device=dev)
+        col = torch.full((H, R), 0xAB, dtype=torch.uint8, device=dev)
+        csc = torch.full((mgq.mx_scale_bytes(H, R),), 0xCD, dtype=torch.uint8, device=dev)
+        q = mgq.qdesc(dt, mgq.MX32_E8M0, codes, sc, col, csc)
     elif mode.startswith("mx"):
         sc = torch.full((mgq.mx_scale_bytes(R, H),), 0xCD, dtype=torch.uint8, device=dev)
         q = mgq.qdesc(dt, mgq.MX32_E8M0, codes, sc)
@@ -109,6 +116,12 @@ def test_permute_quantize(mgq, case, mode):
         c, s = OQ.quantize_mx(xf, fmt)
         assert np.array_equal(u8_np(codes)[:Rp], OR.permute_rows(c, w_rim, Rp))
         assert np.array_equal(untile_mx_scales(u8_np(sc), R, H)[:Rp], OR.permute_rows(s, w_rim, Rp))
+        if mode.startswith("mx_col"):
+            # groups are padded to multiples of 32 rows: no block straddles two
+            xp = OR.permute_rows(xf, w_rim, Rp, fill=0.0)
+            cc, cs = OQ.quantize_mx(xp.T, fmt)
+            assert np.array_equal(u8_np(col)[:, :Rp], cc)
+            assert np.array_equal(untile_mx_scales(u8_np(csc), H, R)[:, :Rp // 32], cs)
     elif mode.startswith("blk"):
         c, si = OQ.quantize_block_1x128(xf, fmt)
         assert np.array_equal(u8_np(codes)[:Rp], OR.permute_rows(c, w_rim, Rp))
@@ -590,7 +603,7 @@ def test_unpermute_and_permute_bwd(mgq, T, E, k, H):
     check_elementwise(OR.permute_bwd(bf16_np(y), rim), bf16_np(dx), "permute_bwd")
 
 
-@pytest.mark.parametrize("mode", ["tensor", "mx"])
+@pytest.mark.parametrize("mode", ["tensor", "mx", "mx_col"])
 def test_unpermute_bwd_quantize(mgq, mode):
     rng = np.random.default_rng(9)
     dev = torch.device(DEV)
@@ -608,6 +621,11 @@ def test_unpermute_bwd_quantize(mgq, mode):
         s = torch.tensor([30000.0], device=dev)
         amax = torch.zeros(1, device=dev)
         q = mgq.qdesc(mgq.E5M2, mgq.TENSOR_F32, codes, None, col, None, s, amax)
+    elif mode == "mx_col":
+        sc = torch.full((mgq.mx_scale_bytes(R, H),), 0xCD, dtype=torch.uint8, device=dev)
+        col = torch.full((H, R), 0xAB, dtype=torch.uint8, device=dev)
+        csc = torch.full((mgq.mx_scale_bytes(H, R),), 0xCD, dtype=torch.uint8, device=dev)
+        q = mgq.qdesc(mgq.E5M2, mgq.MX32_E8M0, codes, sc, col, csc)
     else:
         sc = torch.full((mgq.mx_scale_bytes(R, H),), 0xCD, dtype=torch.uint8, device=dev)
         q = mgq.qdesc(mgq.E5M2, mgq.MX32_E8M0, codes, sc)
@@ -625,6 +643,10 @@ def test_unpermute_bwd_quantize(mgq, mode):
         c, s_ = OQ.quantize_mx(dy32.astype(np.float64), "e5m2")
         assert np.array_equal(u8_np(codes)[:Rp], c)
         assert np.array_equal(untile_mx_scales(u8_np(sc), R, H)[:Rp], s_)
+        if mode == "mx_col":
+            cc, cs = OQ.quantize_mx(dy32.astype(np.float64).T, "e5m2")
+            assert np.array_equal(u8_np(col)[:, :Rp], cc)
+            assert np.array_equal(untile_mx_scales(u8_np(csc), H, R)[:, :Rp // 32], cs)
 
 
 @pytest.mark.parametrize("mode", ["mx", "tensor", "blk128", "nvfp4", "mx_col"])
@@ -851,7 +873,7 @@ def test_gemm_dgrad_dswiglu_equals_separate_steps(mgq, w_layout):
     check_elementwise(OL.dswiglu(bf16_np(sep["dh"])[:Rp], bf16_np(gu)[:Rp], F), bf16_np(fus["dgu"])[:Rp], "dswiglu")
 
 
-@pytest.mark.parametrize("mode", ["mx", "tensor", "nvfp4"])
+@pytest.mark.parametrize("mode", ["mx", "mx_col", "tensor", "nvfp4"])
 def test_route_then_permute_routed_equals_permute(mgq, mode):
     """mgq_moe_route followed by mgq_moe_permute_routed writes what one
     mgq_moe_permute call writes (routing arrays, codes, scales, amax)."""
@@ -873,9 +895,13 @@ def test_route_then_permute_routed_equals_permute(mgq, mode):
                  q=torch.full((R_cap, H // 2 if nv else H), 0xAB, dtype=torch.uint8, device=dev),
                  s=torch.full(((mgq.nv_scale_bytes if nv else mgq.mx_scale_bytes)(R_cap, H),), 0xCD,
                               dtype=torch.uint8, device=dev),
-                 ts=torch.tensor([3.0], device=dev), am=torch.zeros(1, device=dev))
+                 ts=torch.tensor([3.0], device=dev), am=torch.zeros(1, device=dev),
+                 c=torch.full((H, R_cap), 0xAB, dtype=torch.uint8, device=dev),
+                 cs=torch.full((mgq.mx_scale_bytes(H, R_cap),), 0xCD, dtype=torch.uint8, device=dev))
         if mode == "mx":
             b["qd"] = mgq.qdesc(mgq.E4M3, mgq.MX32_E8M0, b["q"], b["s"])
+        elif mode == "mx_col":
+            b["qd"] = mgq.qdesc(mgq.E4M3, mgq.MX32_E8M0, b["q"], b["s"], b["c"], b["cs"])
         elif mode == "nvfp4":
             b["qd"] = mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, b["q"], b["s"], tensor_scale=b["ts"], amax_out=b["am"])
         else:
@@ -889,7 +915,7 @@ def test_route_then_permute_routed_equals_permute(mgq, mode):
     torch.cuda.synchronize()
     assert mgq.get_error() == mgq.OK
     Rp = int(one["off"][-1].item())
-    for key in ("rim", "off", "cnt", "q", "s", "am", "ts"):
+    for key in ("rim", "off", "cnt", "q", "s", "am", "ts", "c", "cs"):
         assert torch.equal(one[key], two[key]), key
     assert torch.equal(one["src"][:Rp], two["src"][:Rp])
     rim, src, off, cnt = OR.permute_indices(idx, E, 128)
