@@ -39,14 +39,21 @@ __device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f 
 __device__ __forceinline__ float sigmoid_fast(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
 // h = bf16(silu(g) u)
 __device__ __forceinline__ float swiglu_bf16(float g, float u) { return round_bf16(__fmul_rn(silu_fast(g), u)); }
-// dSwiGLU of one element with s = sigmoid(g): dG = bf16(dh u s (1 + g (1 - s))),
-// dU = bf16(dh g s), every operation spelled out so no kernel contracts it
-// differently
-__device__ __forceinline__ void dswiglu_bf16(float d, float g, float u, float& dg, float& du) {
+// silu(g) u in float32, before the bf16 rounding
+__device__ __forceinline__ float swiglu_f32(float g, float u) { return __fmul_rn(silu_fast(g), u); }
+// dSwiGLU of one element with s = sigmoid(g): dG = dh u s (1 + g (1 - s)),
+// dU = dh g s in float32 (before the bf16 rounding), every operation spelled
+// out so no kernel contracts it differently
+__device__ __forceinline__ void dswiglu_f32(float d, float g, float u, float& dg, float& du) {
   const float s = sigmoid_fast(g);
   const float t = __fmaf_rn(g, __fsub_rn(1.0f, s), 1.0f);
-  dg = round_bf16(__fmul_rn(__fmul_rn(__fmul_rn(d, u), s), t));
-  du = round_bf16(__fmul_rn(__fmul_rn(d, g), s));
+  dg = __fmul_rn(__fmul_rn(__fmul_rn(d, u), s), t);
+  du = __fmul_rn(__fmul_rn(d, g), s);
+}
+__device__ __forceinline__ void dswiglu_bf16(float d, float g, float u, float& dg, float& du) {
+  dswiglu_f32(d, g, u, dg, du);
+  dg = round_bf16(dg);
+  du = round_bf16(du);
 }
 
 // ---------------------------------------------------------------------------
@@ -136,6 +143,15 @@ __device__ __forceinline__ int64_t tiled_scale_offset(int64_t r, int64_t b, int6
 __device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t acc, uint32_t w) {
   return __vmaxu2(acc, w & 0x7FFF7FFFu);
 }
+// running |x| maximum of packed bf16 pairs in the bf16 unit: the magnitude of
+// each half is max(|acc|, |w|), a NaN operand gives NaN; the sign bits are
+// garbage (clear them with absmax_bf16x2_final)
+__device__ __forceinline__ uint32_t absmax_acc_bf16x2(uint32_t acc, uint32_t w) {
+  uint32_t r;
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(acc), "r"(w));
+  return r;
+}
+__device__ __forceinline__ uint32_t absmax_bf16x2_final(uint32_t acc) { return acc & 0x7FFF7FFFu; }
 __device__ __forceinline__ uint32_t fold_bf16x2(uint32_t w) {   // max of the halves, as float bits
   uint32_t a = w & 0xFFFFu, b = w >> 16;
   return (a > b ? a : b) << 16;

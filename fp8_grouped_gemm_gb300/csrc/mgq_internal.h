@@ -56,8 +56,8 @@ int rowcol_dswiglu(const uint16_t* dh, const uint16_t* gu, int64_t R_cap, int64_
 // dY = probs * dout rows, gathered through src_row (quant_tile.cu).
 int gather_x_rowcol(const uint16_t* x, const int32_t* src_row, int k, int64_t H, int64_t R_cap,
                     const int32_t* rows_used, bool with_rows, const mgq_qdesc* q, cudaStream_t s);
-int col_gather_dy(const uint16_t* dout, const float* probs, const int32_t* src_row, int k, int64_t H, int64_t R_cap,
-                  const int32_t* rows_used, const mgq_qdesc* q, cudaStream_t s);
+int col_gather_dy(const uint16_t* dout, const float* probs, const int32_t* src_row, int k, int64_t H,
+                  int64_t R_cap, const int32_t* rows_used, const mgq_qdesc* q, cudaStream_t s);
 
 }  // namespace mgq
 

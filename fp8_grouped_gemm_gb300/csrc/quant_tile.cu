@@ -18,47 +18,41 @@
 #include "mgq_internal.h"
 #include "rowquant.cuh"
 
+#include <algorithm>
+#include <type_traits>
+
 namespace mgq {
 namespace {
 
 constexpr int TR = 128, TC = 128;  // tile rows x columns (per part)
+constexpr int LD = TC + 8;          // bf16 tile row pitch in elements (rows stay 16-byte aligned)
 
-// Source kinds (kKind):
-//  kPlain    the tile is a block of a bf16 matrix (load_raw: 16-byte copies)
-//  kGather   row r of the tile is a gathered bf16 row (row_offset), optionally
-//            multiplied by a per-row float32 factor; the row offsets are
-//            resolved once per tile into shared memory
-//  kComputed the values are computed elementwise from kLoads bf16 operands
-//            (fetch, then make), loads of several chunks in flight at once
-// kExactBf16: every value the source produces is a bf16 value, so the tile
-// keeps it as 2 bytes in shared memory.
-enum SrcKind { kPlain, kGather, kComputed };
-
+// Sources. Every value a source produces is a bf16 value, or (kFactor) a bf16
+// value times a per-row float32 factor, so tiles hold bf16 in shared memory.
+//  plain (SrcPlain): a block of a bf16 matrix, one tile per CTA
+//  streamed (SrcGatherX, SrcGatherDy, kStream): row r of the tile is the bf16
+//    row at element offset row_offset(r) of base() (-1: a zero row); these run
+//    on the pipelined kernel, which stages tiles with cp.async
+//  computed (SrcSwiglu, SrcDswiglu): values computed elementwise from kLoads
+//    bf16 operands (fetch, then make), loads of several chunks in flight
 struct SrcPlain {
-  static constexpr int kKind = kPlain;
+  static constexpr bool kComputed = false;
+  static constexpr bool kStream = false;      // one tile per CTA (4 CTAs per SM) is faster for dense rows
   static constexpr int kParts = 1;
-  static constexpr bool kExactBf16 = true;
   const uint16_t* x;
   int64_t ld;
-  __device__ __forceinline__ uint4 load_raw(int64_t r, int64_t c) const {
-    return __ldg(reinterpret_cast<const uint4*>(x + r * ld + c));
-  }
 };
 
 __device__ __forceinline__ void unpack8_bf16(const uint4 w, float* v) {
   v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
   v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
 }
-__device__ __forceinline__ void store8_bf16(uint16_t* p, const float* v) {
-  *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                                            pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-}
 
 // h = bf16(silu(g) * u), g = gu[:, :F], u = gu[:, F:]; h optionally written out
 struct SrcSwiglu {
-  static constexpr int kKind = kComputed;
+  static constexpr bool kComputed = true;
+  static constexpr bool kStream = false;
   static constexpr int kParts = 1;
-  static constexpr bool kExactBf16 = true;
   static constexpr int kLoads = 2;
   const uint16_t* gu;
   int64_t F;
@@ -67,13 +61,16 @@ struct SrcSwiglu {
     w[0] = __ldg(reinterpret_cast<const uint4*>(gu + r * 2 * F + c));
     w[1] = __ldg(reinterpret_cast<const uint4*>(gu + r * 2 * F + F + c));
   }
-  __device__ __forceinline__ void make(const uint4* w, int64_t r, int64_t c, bool valid, float* v, float*) const {
+  // out[0]: the 8 values of h as packed bf16
+  __device__ __forceinline__ void make(const uint4* w, int64_t r, int64_t c, bool valid, uint4* out) const {
     float g[8], u[8];
     unpack8_bf16(w[0], g);
     unpack8_bf16(w[1], u);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = swiglu_bf16(g[i], u[i]);
-    if (h_out && valid) store8_bf16(h_out + r * F + c, v);
+    out[0] = make_uint4(pack_bf16x2(swiglu_f32(g[0], u[0]), swiglu_f32(g[1], u[1])),
+                        pack_bf16x2(swiglu_f32(g[2], u[2]), swiglu_f32(g[3], u[3])),
+                        pack_bf16x2(swiglu_f32(g[4], u[4]), swiglu_f32(g[5], u[5])),
+                        pack_bf16x2(swiglu_f32(g[6], u[6]), swiglu_f32(g[7], u[7])));
+    if (h_out && valid) *reinterpret_cast<uint4*>(h_out + r * F + c) = out[0];
   }
 };
 
@@ -81,9 +78,9 @@ struct SrcSwiglu {
 // and part 1 = dU = dh silu(g), s = sigmoid(g); both written to [dG | dU]
 // (columns f and F + f) when requested. One read of dh, g, u serves both.
 struct SrcDswiglu {
-  static constexpr int kKind = kComputed;
+  static constexpr bool kComputed = true;
+  static constexpr bool kStream = false;
   static constexpr int kParts = 2;
-  static constexpr bool kExactBf16 = true;
   static constexpr int kLoads = 3;
   const uint16_t* dh;
   const uint16_t* gu;
@@ -94,17 +91,21 @@ struct SrcDswiglu {
     w[1] = __ldg(reinterpret_cast<const uint4*>(gu + r * 2 * F + f));
     w[2] = __ldg(reinterpret_cast<const uint4*>(gu + r * 2 * F + F + f));
   }
-  __device__ __forceinline__ void make(const uint4* w, int64_t r, int64_t f, bool valid, float* dg,
-                                       float* du) const {
-    float d[8], g[8], u[8];
+  // o[0], o[1]: the 8 values of dG and of dU as packed bf16
+  __device__ __forceinline__ void make(const uint4* w, int64_t r, int64_t f, bool valid, uint4* o) const {
+    float d[8], g[8], u[8], dg[8], du[8];
     unpack8_bf16(w[0], d);
     unpack8_bf16(w[1], g);
     unpack8_bf16(w[2], u);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) dswiglu_bf16(d[i], g[i], u[i], dg[i], du[i]);
+    for (int i = 0; i < 8; ++i) dswiglu_f32(d[i], g[i], u[i], dg[i], du[i]);
+    o[0] = make_uint4(pack_bf16x2(dg[0], dg[1]), pack_bf16x2(dg[2], dg[3]), pack_bf16x2(dg[4], dg[5]),
+                      pack_bf16x2(dg[6], dg[7]));
+    o[1] = make_uint4(pack_bf16x2(du[0], du[1]), pack_bf16x2(du[2], du[3]), pack_bf16x2(du[4], du[5]),
+                      pack_bf16x2(du[6], du[7]));
     if (out && valid) {
-      store8_bf16(out + r * 2 * F + f, dg);
-      store8_bf16(out + r * 2 * F + F + f, du);
+      *reinterpret_cast<uint4*>(out + r * 2 * F + f) = o[0];
+      *reinterpret_cast<uint4*>(out + r * 2 * F + F + f) = o[1];
     }
   }
 };
@@ -112,14 +113,13 @@ struct SrcDswiglu {
 // row r of the permuted matrix: X[t] for the (token, slot) entry e = src_row[r]
 // (t = e / k), zeros for filler rows
 struct SrcGatherX {
-  static constexpr int kKind = kGather;
-  static constexpr int kParts = 1;
-  static constexpr bool kExactBf16 = true;
+  static constexpr bool kStream = true;
+  static constexpr bool kFactor = false;
+  static constexpr bool kColumnsOnly = false;
   const uint16_t* x;
   const int32_t* src_row;
   int k;
   int64_t H;
-  // element offset of the source row of r (-1: zero row) and its factor
   __device__ __forceinline__ int64_t row_offset(int64_t r, float&) const {
     const int e = src_row[r];
     return e < 0 ? -1 : (int64_t)(e / k) * H;
@@ -128,11 +128,12 @@ struct SrcGatherX {
 };
 
 // row r of dY = float32(probs[e] * dout[t]) for the entry e = src_row[r]
-// (the unpermute backward), zeros for filler rows
+// (the unpermute backward), zeros for filler rows; column-wise codes only
+// (the row-wise codes come from the token-major kernel)
 struct SrcGatherDy {
-  static constexpr int kKind = kGather;
-  static constexpr int kParts = 1;
-  static constexpr bool kExactBf16 = false;   // float32 products
+  static constexpr bool kStream = true;
+  static constexpr bool kFactor = true;
+  static constexpr bool kColumnsOnly = true;
   const uint16_t* dout;
   const float* probs;
   const int32_t* src_row;
@@ -162,99 +163,176 @@ struct RowColArgs {
   int rceil;
 };
 
-// shared-memory tile element: bf16 bits (exact sources) or float
-template <bool B16> struct TileT;
-template <> struct TileT<true> {
-  using T = uint16_t;
-  static constexpr int kPad = 8;             // rows stay 16-byte aligned
-  __device__ static T put(float v) { return (T)(__float_as_uint(v) >> 16); }
-  __device__ static float get(T v) { return __uint_as_float((uint32_t)v << 16); }
-};
-template <> struct TileT<false> {
-  using T = float;
-  static constexpr int kPad = 4;             // rows stay 16-byte aligned
-  __device__ static T put(float v) { return v; }
-  __device__ static float get(T v) { return v; }
-};
+// ---- the quantisation of one tile (shared by both kernels) -----------------
 
-template <class Src>
-constexpr size_t rowcol_smem() {
-  return (size_t)Src::kParts * TR * (TC + TileT<Src::kExactBf16>::kPad) * sizeof(typename TileT<Src::kExactBf16>::T);
+// one column-wise block: the 32 values of output row crow, rows rg..rg+31 of
+// its group (amax_bits: float bits of their |v| maximum, MX)
+template <int SC, int DT>
+__device__ __forceinline__ void col_block_out(const float* v, uint32_t amax_bits, float ts, const RowColArgs& a,
+                                              int64_t crow, int64_t rg) {
+  float mult = ts;
+  if (SC == MGQ_MX32_E8M0) {
+    const int e = mx_exponent(amax_bits, FmtInfo<DT>::emax, a.rceil != 0);
+    mult = mx_multiplier(e);
+    a.col_scales[tiled_scale_offset(crow, rg / 32, a.M / 128)] = (uint8_t)mx_scale_code(e);
+  }
+  uint32_t cw[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    cw[i] = cvt_fp8x4<DT>(__fmul_rn(v[4 * i], mult), __fmul_rn(v[4 * i + 1], mult), __fmul_rn(v[4 * i + 2], mult),
+                          __fmul_rn(v[4 * i + 3], mult));
+  uint4* dst = reinterpret_cast<uint4*>(a.col_codes + crow * a.M + rg);
+  dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+  dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
 }
 
+// Row-wise codes of a bf16 tile [P][TR][LD]: the P*TR (part, row) pairs, 8 per
+// warp at a time; 4 lanes per row, lane takes one 32-column block. The lane
+// reads its four 16-byte chunks in the order q ^ sw (sw = 0 for blocks 0, 1 and
+// 2 for blocks 2, 3), so the 8 lanes of a quarter warp hit 8 different bank groups.
+template <int P, int SC, int DT>
+__device__ __forceinline__ void row_phase(const uint16_t* tile, int64_t r0, int64_t nrows, int64_t c0, float ts,
+                                          const RowColArgs& a, int warp, uint32_t lane) {
+  const int seg = lane & 3;
+  const int sw = (seg >> 1) * 2;
+#pragma unroll 1
+  for (int pr0 = warp * P * 16; pr0 < (warp + 1) * P * 16; pr0 += 8) {
+    const int pr = pr0 + (int)(lane >> 2);
+    const int p = pr / TR, rr = pr % TR;
+    const int64_t r = r0 + rr;
+    const int64_t cb = c0 + p * a.part_off + 32 * seg;   // first output column of the block
+    const uint4* src = reinterpret_cast<const uint4*>(&tile[(p * TR + rr) * LD + 32 * seg]);
+    uint32_t ww[16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 w = src[q ^ sw];
+      ww[4 * q] = w.x; ww[4 * q + 1] = w.y; ww[4 * q + 2] = w.z; ww[4 * q + 3] = w.w;
+    }
+    float mult = ts;
+    if (SC == MGQ_MX32_E8M0) {
+      uint32_t acc = 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc = absmax_acc_bf16x2(acc, ww[i]);
+      const int e = mx_exponent(fold_bf16x2(absmax_bf16x2_final(acc)), FmtInfo<DT>::emax, a.rceil != 0);
+      mult = mx_multiplier(e);
+      if (r < nrows) a.row_scales[tiled_scale_offset(r, cb / 32, a.C / 128)] = (uint8_t)mx_scale_code(e);
+    }
+    uint32_t cw[8];        // codes in the order held (chunk q ^ sw in cw[2q], cw[2q + 1])
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      cw[i] = cvt_fp8x4<DT>(__fmul_rn(bf16_lo(ww[2 * i]), mult), __fmul_rn(bf16_hi(ww[2 * i]), mult),
+                            __fmul_rn(bf16_lo(ww[2 * i + 1]), mult), __fmul_rn(bf16_hi(ww[2 * i + 1]), mult));
+    if (r < nrows) {
+      uint8_t* dst = a.row_codes + r * a.C + cb;
+      *reinterpret_cast<uint4*>(dst + 8 * sw) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+      *reinterpret_cast<uint4*>(dst + (16 - 8 * sw)) = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+    }
+  }
+}
+
+// Column-wise codes of a bf16 tile [P][TR][LD]: thread takes 2 adjacent
+// columns of one 32-row block (one MX block each); its 32 output bytes per
+// column are contiguous. FAC: values are fac[row] * tile (float32 products).
+// am: running |v| maximum (float bits) for the per-tensor amax.
+template <int P, int SC, int DT, bool FAC>
+__device__ __forceinline__ void col_phase(const uint16_t* tile, const float* fac, int64_t g, int64_t r0, int64_t c0,
+                                          float ts, const RowColArgs& a, int tid, uint32_t& am) {
+  const int cp = tid & 63, rb = (tid >> 6) & 3;
+  const int cc = 2 * cp;
+  const int64_t rg = r0 - g * a.M + 32 * rb;                 // row inside the group
+#pragma unroll 1
+  for (int p = 0; p < P; ++p) {
+    const int64_t crow = g * a.C + c0 + p * a.part_off + cc;  // row of the column-wise output
+    if constexpr (FAC) {
+      // one column at a time (32 products live)
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          v[i] = __fmul_rn(fac[32 * rb + i], __uint_as_float((uint32_t)tile[(p * TR + 32 * rb + i) * LD + cc + h] << 16));
+        const uint32_t m = absmax_bits_f32(v, 32);
+        am = max(am, m);
+        col_block_out<SC, DT>(v, m, ts, a, crow + h, rg);
+      }
+    } else {
+      uint32_t w[32];      // the two columns' 32 values as bf16 pairs
+#pragma unroll
+      for (int i = 0; i < 32; ++i) w[i] = *reinterpret_cast<const uint32_t*>(&tile[(p * TR + 32 * rb + i) * LD + cc]);
+      uint32_t amh[2] = {0, 0};
+      if (SC == MGQ_MX32_E8M0 || a.amax_out) {
+        uint32_t acc = 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc = absmax_acc_bf16x2(acc, w[i]);
+        acc = absmax_bf16x2_final(acc);
+        amh[0] = acc << 16;
+        amh[1] = acc & 0xFFFF0000u;
+        am = max(am, max(amh[0], amh[1]));
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = h ? bf16_hi(w[i]) : bf16_lo(w[i]);
+        col_block_out<SC, DT>(v, amh[h], ts, a, crow + h, rg);
+      }
+    }
+  }
+}
+
+// per-tensor amax of group g: CTA reduction, one atomic
+__device__ __forceinline__ void flush_amax(uint32_t am, float* amax_out, int64_t g, uint32_t* s_amax, int tid) {
+  am = warp_max_u32(am);
+  if ((tid & 31) == 0) s_amax[tid >> 5] = am;
+  __syncthreads();
+  if (tid == 0) {
+    for (int i = 1; i < 8; ++i) am = max(am, s_amax[i]);
+    atomic_max_nonneg(amax_out + g, __uint_as_float(am));
+  }
+  __syncthreads();
+}
+
+// ---- plain and computed sources: one tile per CTA ---------------------------
+
 template <class Src, int SC, int DT>
-__global__ void __launch_bounds__(256, (Src::kParts == 2 || !Src::kExactBf16) ? 3 : 4)
+__global__ void __launch_bounds__(256, Src::kParts == 2 ? 3 : 4)
     quant_rowcol_kernel(const Src src, const RowColArgs a) {
-  using TT = TileT<Src::kExactBf16>;
-  using T = typename TT::T;
   constexpr int P = Src::kParts;
-  constexpr int LD = TC + TT::kPad;
-  extern __shared__ uint8_t smem_raw[];
-  T* tile = reinterpret_cast<T*>(smem_raw);                 // [P][TR][LD]
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  uint16_t* tile = reinterpret_cast<uint16_t*>(smem_raw);   // [P][TR][LD]
   __shared__ uint32_t s_amax[8];
   const int tid = threadIdx.x, warp = tid >> 5;
   const uint32_t lane = tid & 31;
-  const int64_t c0 = (int64_t)blockIdx.x * TC, r0 = (int64_t)blockIdx.y * TR;
   const int64_t nrows = a.rows_used ? (int64_t)*a.rows_used : a.rows_cap;
-  if (r0 >= nrows) return;
-  const int64_t g = r0 / a.M;
-  const float ts = (SC == MGQ_TENSOR_F32) ? a.tensor_scale[g] : 1.0f;
-  // ---- load: TR rows x 16 chunks of 8 columns, 8 chunks per thread
-  uint32_t am = 0;
-  if constexpr (Src::kKind == kPlain || Src::kKind == kGather) {
-    // gathered rows: the source offsets (and factors) of the tile's rows first
-    __shared__ int64_t s_off[Src::kKind == kGather ? TR : 1];
-    __shared__ float s_fac[Src::kKind == kGather ? TR : 1];
-    if constexpr (Src::kKind == kGather) {
-      if (tid < TR) {
-        float f = 0.0f;
-        const int64_t off = (r0 + tid < nrows) ? src.row_offset(r0 + tid, f) : -1;
-        s_off[tid] = off;
-        s_fac[tid] = f;
-      }
-      __syncthreads();
-    }
-    // all eight 16-byte loads in flight, then copied into the tile
-    uint4 w[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int chunk = tid + 256 * i;
-      const int rr = chunk >> 4, cc = (chunk & 15) * 8;
-      if constexpr (Src::kKind == kGather) {
-        const int64_t off = s_off[rr];
-        w[i] = off >= 0 ? __ldg(reinterpret_cast<const uint4*>(src.base() + off + c0 + cc)) : make_uint4(0, 0, 0, 0);
-      } else {
-        w[i] = (r0 + rr < nrows) ? src.load_raw(r0 + rr, c0 + cc) : make_uint4(0, 0, 0, 0);
-      }
-    }
-    if constexpr (Src::kExactBf16) {
-      uint32_t am2 = 0;
+  const int n_rt = (int)((nrows + TR - 1) / TR);     // fewer than 2^31 rows
+  const int64_t c0 = (int64_t)blockIdx.x * TC;
+#pragma unroll 1
+  for (int rt = blockIdx.y; rt < n_rt; rt += gridDim.y) {
+    const int64_t r0 = (int64_t)rt * TR;
+    const int64_t g = (int)r0 / (int)a.M;
+    const float ts = (SC == MGQ_TENSOR_F32) ? a.tensor_scale[g] : 1.0f;
+    // ---- load: TR rows x 16 chunks of 8 columns, 8 chunks per thread
+    uint32_t am2 = 0;
+    if constexpr (!Src::kComputed) {
+      // plain: all eight 16-byte loads in flight, then copied into the tile
+      uint4 w[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int chunk = tid + 256 * i;
         const int rr = chunk >> 4, cc = (chunk & 15) * 8;
-        am2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(am2, w[i].x), w[i].y), w[i].z), w[i].w);
+        w[i] = (r0 + rr < nrows) ? __ldg(reinterpret_cast<const uint4*>(src.x + (r0 + rr) * src.ld + c0 + cc))
+                                 : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int chunk = tid + 256 * i;
+        const int rr = chunk >> 4, cc = (chunk & 15) * 8;
+        if (SC == MGQ_TENSOR_F32)
+          am2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(am2, w[i].x), w[i].y), w[i].z), w[i].w);
         *reinterpret_cast<uint4*>(&tile[rr * LD + cc]) = w[i];
       }
-      am = fold_bf16x2(am2);
     } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int chunk = tid + 256 * i;
-        const int rr = chunk >> 4, cc = (chunk & 15) * 8;
-        const float f = Src::kKind == kGather ? s_fac[rr] : 1.0f;
-        float v[8];
-        unpack8_bf16(w[i], v);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(f, v[j]);
-        am = max(am, absmax_bits_f32(v, 8));
-        float4* d = reinterpret_cast<float4*>(&tile[rr * LD + cc]);
-        d[0] = make_float4(v[0], v[1], v[2], v[3]);
-        d[1] = make_float4(v[4], v[5], v[6], v[7]);
-      }
-    }
-  } else {
-    // computed values: the operands of kBatch chunks loaded together
+    // the operands of kBatch chunks loaded together
     constexpr int kBatch = 4;
 #pragma unroll 1
     for (int b = 0; b < 8; b += kBatch) {
@@ -274,147 +352,124 @@ __global__ void __launch_bounds__(256, (Src::kParts == 2 || !Src::kExactBf16) ? 
       for (int j = 0; j < kBatch; ++j) {
         const int chunk = tid + 256 * (b + j);
         const int rr = chunk >> 4, cc = (chunk & 15) * 8;
-        float v[P][8];
-        src.make(w[j], r0 + rr, c0 + cc, r0 + rr < nrows, v[0], v[P - 1]);
+        uint4 o[P];
+        src.make(w[j], r0 + rr, c0 + cc, r0 + rr < nrows, o);
 #pragma unroll
         for (int p = 0; p < P; ++p) {
-          am = max(am, absmax_bits_f32(v[p], 8));
-#pragma unroll
-          for (int q = 0; q < 8; ++q) tile[(p * TR + rr) * LD + cc + q] = TT::put(v[p][q]);
+          if (SC == MGQ_TENSOR_F32)
+            am2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(am2, o[p].x), o[p].y), o[p].z), o[p].w);
+          *reinterpret_cast<uint4*>(&tile[(p * TR + rr) * LD + cc]) = o[p];
         }
       }
     }
-  }
-  __syncthreads();
-  // ---- row-wise: the P*TR (part, row) pairs, 4 per warp at a time; 8 lanes
-  // per row, lane takes 16 columns (half an MX block: the pair l, l^1 shares one)
-  {
-    const int seg = lane & 7;
-    for (int pr0 = warp * P * 16; a.row_codes && pr0 < (warp + 1) * P * 16; pr0 += 4) {
-      const int pr = pr0 + (int)(lane >> 3);
-      const int p = pr / TR, rr = pr % TR;
-      const int64_t r = r0 + rr;
-      const int64_t cb = c0 + p * a.part_off;     // first output column of this part
-      float v[16];
-      uint32_t m = 0;   // |v| maximum as float bits (MX)
-      const T* src = &tile[(p * TR + rr) * LD + 16 * seg];
-      if constexpr (Src::kExactBf16) {
-        const uint4 w0 = reinterpret_cast<const uint4*>(src)[0], w1 = reinterpret_cast<const uint4*>(src)[1];
-        const uint32_t ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-        uint32_t m2 = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          v[2 * i] = bf16_lo(ww[i]);
-          v[2 * i + 1] = bf16_hi(ww[i]);
-          m2 = absmax_bf16x2(m2, ww[i]);
-        }
-        m = fold_bf16x2(m2);
-      } else {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 f = reinterpret_cast<const float4*>(src)[q];
-          v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
-        }
-        if (SC == MGQ_MX32_E8M0) m = absmax_bits_f32(v, 16);
-      }
-      float mult = ts;
-      uint32_t scode = 0;
-      if (SC == MGQ_MX32_E8M0) {
-        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));        // the other half of the block
-        const int e = mx_exponent(m, FmtInfo<DT>::emax, a.rceil != 0);
-        mult = mx_multiplier(e);
-        scode = mx_scale_code(e);
-      }
-      uint32_t cw[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        cw[i] = cvt_fp8x4<DT>(__fmul_rn(v[4 * i], mult), __fmul_rn(v[4 * i + 1], mult),
-                              __fmul_rn(v[4 * i + 2], mult), __fmul_rn(v[4 * i + 3], mult));
-      if (SC == MGQ_MX32_E8M0) {
-        // the row's 4 block scales (lanes seg 0, 2, 4, 6 of its 8) into seg 0
-        const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, scode, 2), s2 = __shfl_down_sync(0xFFFFFFFFu, scode, 4),
-                       s3 = __shfl_down_sync(0xFFFFFFFFu, scode, 6);
-        if (seg == 0 && r < nrows)
-          *reinterpret_cast<uint32_t*>(a.row_scales + tiled_scale_offset(r, cb / 32, a.C / 128)) =
-              scode | (s1 << 8) | (s2 << 16) | (s3 << 24);
-      }
-      if (r < nrows)
-        *reinterpret_cast<uint4*>(a.row_codes + r * a.C + cb + 16 * seg) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
     }
-  }
-  // ---- column-wise: thread takes 2 adjacent columns of one 32-row block (one
-  // MX block each); its 32 output bytes per column are contiguous
-  if (a.col_codes) {
-    const int cp = tid & 63, rb = (tid >> 6) & 3;
-#pragma unroll 1
-    for (int p = 0; p < P; ++p) {
-      const int cc = 2 * cp;
-      const int64_t crow = g * a.C + c0 + p * a.part_off + cc;  // row of the column-wise output
-      const int64_t rg = r0 - g * a.M + 32 * rb;                // row inside the group
-      // the two columns' 32 values: bf16 pairs (exact sources) or floats
-      uint32_t w[32];
-      float v0[Src::kExactBf16 ? 1 : 32], v1[Src::kExactBf16 ? 1 : 32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const T* src = &tile[(p * TR + 32 * rb + i) * LD + cc];
-        if constexpr (Src::kExactBf16) {
-          w[i] = *reinterpret_cast<const uint32_t*>(src);
-        } else {
-          const float2 f = *reinterpret_cast<const float2*>(src);
-          v0[i] = f.x;
-          v1[i] = f.y;
-        }
-      }
-      uint32_t amh[2];
-      if constexpr (Src::kExactBf16) {
-        uint32_t m2 = 0;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) m2 = absmax_bf16x2(m2, w[i]);
-        amh[0] = m2 << 16;
-        amh[1] = m2 & 0xFFFF0000u;
-      } else {
-        amh[0] = absmax_bits_f32(v0, 32);
-        amh[1] = absmax_bits_f32(v1, 32);
-      }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        auto val = [&](int i) {
-          if constexpr (Src::kExactBf16) return h ? bf16_hi(w[i]) : bf16_lo(w[i]);
-          else return h ? v1[i] : v0[i];
-        };
-        float mult = ts;
-        if (SC == MGQ_MX32_E8M0) {
-          const int e = mx_exponent(amh[h], FmtInfo<DT>::emax, a.rceil != 0);
-          mult = mx_multiplier(e);
-          a.col_scales[tiled_scale_offset(crow + h, rg / 32, a.M / 128)] = (uint8_t)mx_scale_code(e);
-        }
-        uint32_t cw[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          cw[i] = cvt_fp8x4<DT>(__fmul_rn(val(4 * i), mult), __fmul_rn(val(4 * i + 1), mult),
-                                __fmul_rn(val(4 * i + 2), mult), __fmul_rn(val(4 * i + 3), mult));
-        uint4* dst = reinterpret_cast<uint4*>(a.col_codes + (crow + h) * a.M + rg);
-        dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-        dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-      }
-    }
-  }
-  if (SC == MGQ_TENSOR_F32 && a.amax_out) {
-    am = warp_max_u32(am);
-    if (lane == 0) s_amax[warp] = am;
     __syncthreads();
-    if (tid == 0) {
-      for (int i = 1; i < 8; ++i) am = max(am, s_amax[i]);
-      atomic_max_nonneg(a.amax_out + g, __uint_as_float(am));
-    }
+    if (a.row_codes) row_phase<P, SC, DT>(tile, r0, nrows, c0, ts, a, warp, lane);
+    uint32_t am_unused = 0;
+    if (a.col_codes) col_phase<P, SC, DT, false>(tile, nullptr, g, r0, c0, ts, a, tid, am_unused);
+    if (SC == MGQ_TENSOR_F32 && a.amax_out) flush_amax(fold_bf16x2(am2), a.amax_out, g, s_amax, tid);
+    __syncthreads();   // the tile is reused by the next row tile
   }
 }
 
+// ---- streamed sources: pipelined over the CTA's items -----------------------
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
+  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(valid ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// The items (row tile, column tile) in row-major order are split into one
+// contiguous range per CTA. A CTA resolves the source offsets (and factors) of
+// a row tile once, into the slot of the row tile's parity, and stages the
+// next item's tile with cp.async (zero fill for zero rows) while it quantises
+// the current one: two tile buffers, two offset slots.
 template <class Src, int SC, int DT>
-int launch_rowcol_t(const Src& src, const RowColArgs& a, dim3 grid, cudaStream_t s) {
-  constexpr size_t smem = rowcol_smem<Src>();
-  auto kern = quant_rowcol_kernel<Src, SC, DT>;
-  static bool attr_set[64] = {false};
+__global__ void __launch_bounds__(256, 3) quant_rowcol_stream_kernel(const Src src, const RowColArgs a) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  uint16_t* tiles = reinterpret_cast<uint16_t*>(smem_raw);   // [2][TR][LD]
+  __shared__ int64_t s_off[2][TR];
+  __shared__ float s_fac[2][TR];
+  __shared__ uint32_t s_amax[8];
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const uint32_t lane = tid & 31;
+  const int64_t nrows = a.rows_used ? (int64_t)*a.rows_used : a.rows_cap;
+  const int64_t n_ct = a.C / TC;
+  const int64_t n_items = (nrows + TR - 1) / TR * n_ct;
+  const int64_t i0 = n_items * blockIdx.x / gridDim.x, i1 = n_items * (blockIdx.x + 1) / gridDim.x;
+  if (i0 >= i1) return;
+  auto resolve = [&](int rt) {                    // offsets of row tile rt, slot rt & 1
+    if (tid < TR) {
+      const int64_t r = (int64_t)rt * TR + tid;
+      float f = 0.0f;
+      const int64_t off = r < nrows ? src.row_offset(r, f) : -1;
+      s_off[rt & 1][tid] = off;
+      s_fac[rt & 1][tid] = f;
+    }
+  };
+  auto issue = [&](int rt, int ct, int buf) {     // cp.async of the item's tile
+    uint16_t* t = tiles + buf * TR * LD;
+    const int64_t c0 = (int64_t)ct * TC;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int chunk = tid + 256 * j;
+      const int rr = chunk >> 4, cc = (chunk & 15) * 8;
+      const int64_t off = s_off[rt & 1][rr];
+      cp_async16(&t[rr * LD + cc], src.base() + (off >= 0 ? off + c0 + cc : 0), off >= 0);
+    }
+    cp_async_commit();
+  };
+  // item coordinates advance incrementally (row tile, column tile)
+  int rt = (int)(i0 / n_ct), ct = (int)(i0 - (int64_t)rt * n_ct);
+  resolve(rt);
+  __syncthreads();
+  issue(rt, ct, 0);
+  int64_t g = (int)((int64_t)rt * TR) / (int)a.M;
+  float ts = (SC == MGQ_TENSOR_F32) ? a.tensor_scale[g] : 1.0f;
+  uint32_t am = 0;
+#pragma unroll 1
+  for (int64_t item = i0; item < i1; ++item) {
+    const int buf = (int)((item - i0) & 1);
+    int rt_n = rt, ct_n = ct + 1;
+    if (ct_n == (int)n_ct) {
+      ct_n = 0;
+      ++rt_n;
+    }
+    if (item + 1 < i1) {
+      if (rt_n != rt) {
+        resolve(rt_n);
+        __syncthreads();
+      }
+      issue(rt_n, ct_n, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const int64_t r0 = (int64_t)rt * TR, c0 = (int64_t)ct * TC;
+    const uint16_t* t = tiles + buf * TR * LD;
+    if (!Src::kColumnsOnly && a.row_codes) row_phase<1, SC, DT>(t, r0, nrows, c0, ts, a, warp, lane);
+    col_phase<1, SC, DT, Src::kFactor>(t, s_fac[rt & 1], g, r0, c0, ts, a, tid, am);
+    __syncthreads();   // the buffer is refilled two items on
+    if (rt_n != rt || item + 1 == i1) {
+      if (SC == MGQ_TENSOR_F32 && a.amax_out) flush_amax(am, a.amax_out, g, s_amax, tid);
+      am = 0;
+      g = (int)((int64_t)rt_n * TR) / (int)a.M;
+      if (SC == MGQ_TENSOR_F32 && item + 1 < i1) ts = a.tensor_scale[g];
+    }
+    rt = rt_n;
+    ct = ct_n;
+  }
+}
+
+// the dynamic shared memory limit of one kernel, set once per device
+// (attr_set: a flag array owned by the kernel's launcher)
+template <class Kern>
+int set_smem(Kern kern, size_t smem, bool* attr_set) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (smem > 48 * 1024 && dev < 64 && !attr_set[dev]) {
@@ -422,23 +477,43 @@ int launch_rowcol_t(const Src& src, const RowColArgs& a, dim3 grid, cudaStream_t
       return MGQ_ERR_CUDA;
     attr_set[dev] = true;
   }
-  kern<<<grid, 256, smem, s>>>(src, a);
+  return MGQ_OK;
+}
+
+template <class Src, int SC, int DT>
+int launch_rowcol_t(const Src& src, const RowColArgs& a, cudaStream_t s) {
+  static bool attr_set[64] = {false};   // one per instantiation
+  if constexpr (!Src::kStream) {
+    constexpr size_t smem = (size_t)Src::kParts * TR * LD * sizeof(uint16_t);
+    auto kern = quant_rowcol_kernel<Src, SC, DT>;
+    if (set_smem(kern, smem, attr_set) != MGQ_OK) return MGQ_ERR_CUDA;
+    const dim3 grid((unsigned)(a.C / Src::kParts / TC), (unsigned)std::min<int64_t>((a.rows_cap + TR - 1) / TR, 65535));
+    kern<<<grid, 256, smem, s>>>(src, a);
+  } else {
+    constexpr size_t smem = 2 * TR * LD * sizeof(uint16_t);
+    auto kern = quant_rowcol_stream_kernel<Src, SC, DT>;
+    if (set_smem(kern, smem, attr_set) != MGQ_OK) return MGQ_ERR_CUDA;
+    const int64_t items = (a.rows_cap + TR - 1) / TR * (a.C / TC);
+    const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>(items, (int64_t)num_sms() * 3));
+    kern<<<(unsigned)ctas, 256, smem, s>>>(src, a);
+  }
   MGQ_LAUNCH_CHECK();
   return MGQ_OK;
 }
 
 template <class Src>
 int launch_rowcol(const Src& src, const mgq_qdesc* q, RowColArgs a, cudaStream_t s) {
-  const dim3 grid((unsigned)(a.C / Src::kParts / TC), (unsigned)((a.rows_cap + TR - 1) / TR));
+  if (a.rows_cap >= (1ll << 31) || a.M >= (1ll << 31)) return MGQ_ERR_UNSUPPORTED;
+  if (Src::kStream && !a.col_codes) return MGQ_ERR_UNSUPPORTED;   // a row + column pass
   const int sc = q->scaling, dt = q->dtype;
-  if (sc == MGQ_MX32_E8M0 && dt == MGQ_E4M3) return launch_rowcol_t<Src, MGQ_MX32_E8M0, MGQ_E4M3>(src, a, grid, s);
-  if (sc == MGQ_MX32_E8M0 && dt == MGQ_E5M2) return launch_rowcol_t<Src, MGQ_MX32_E8M0, MGQ_E5M2>(src, a, grid, s);
+  if (sc == MGQ_MX32_E8M0 && dt == MGQ_E4M3) return launch_rowcol_t<Src, MGQ_MX32_E8M0, MGQ_E4M3>(src, a, s);
+  if (sc == MGQ_MX32_E8M0 && dt == MGQ_E5M2) return launch_rowcol_t<Src, MGQ_MX32_E8M0, MGQ_E5M2>(src, a, s);
   // per-tensor column copies of gathered rows are transposed casts of the row codes
-  if constexpr (Src::kKind == kGather) {
+  if constexpr (std::is_same<Src, SrcGatherX>::value || std::is_same<Src, SrcGatherDy>::value) {
     return MGQ_ERR_UNSUPPORTED;
   } else {
-    if (sc == MGQ_TENSOR_F32 && dt == MGQ_E4M3) return launch_rowcol_t<Src, MGQ_TENSOR_F32, MGQ_E4M3>(src, a, grid, s);
-    if (sc == MGQ_TENSOR_F32 && dt == MGQ_E5M2) return launch_rowcol_t<Src, MGQ_TENSOR_F32, MGQ_E5M2>(src, a, grid, s);
+    if (sc == MGQ_TENSOR_F32 && dt == MGQ_E4M3) return launch_rowcol_t<Src, MGQ_TENSOR_F32, MGQ_E4M3>(src, a, s);
+    if (sc == MGQ_TENSOR_F32 && dt == MGQ_E5M2) return launch_rowcol_t<Src, MGQ_TENSOR_F32, MGQ_E5M2>(src, a, s);
     return MGQ_ERR_UNSUPPORTED;
   }
 }
@@ -484,8 +559,8 @@ int gather_x_rowcol(const uint16_t* x, const int32_t* src_row, int k, int64_t H,
   return launch_rowcol(SrcGatherX{x, src_row, k, H}, q, a, s);
 }
 
-int col_gather_dy(const uint16_t* dout, const float* probs, const int32_t* src_row, int k, int64_t H, int64_t R_cap,
-                  const int32_t* rows_used, const mgq_qdesc* q, cudaStream_t s) {
+int col_gather_dy(const uint16_t* dout, const float* probs, const int32_t* src_row, int k, int64_t H,
+                  int64_t R_cap, const int32_t* rows_used, const mgq_qdesc* q, cudaStream_t s) {
   RowColArgs a = make_args(q, R_cap, rows_used, H, R_cap);
   a.row_codes = nullptr;       // the row-wise codes come from the unpermute-backward kernel
   return launch_rowcol(SrcGatherDy{dout, probs, src_row, k, H}, q, a, s);

@@ -649,6 +649,46 @@ def test_unpermute_bwd_quantize(mgq, mode):
             assert np.array_equal(untile_mx_scales(u8_np(csc), H, R)[:, :Rp // 32], cs)
 
 
+@pytest.mark.parametrize("fmt,e8m0", [("e4m3", "rceil"), ("e5m2", "rceil"), ("e4m3", "floor"), ("e5m2", "floor")])
+def test_block_quantize_mx_special_values(mgq, fmt, e8m0):
+    """Row- and column-wise MX codes of a tile pass over NaN, +-inf, signed
+    zeros, bf16 subnormals, an all-subnormal block and the largest bf16 values
+    equal the oracle's (a NaN / inf block: scale 0xFF and NaN codes)."""
+    rng = np.random.default_rng(29)
+    dev = torch.device(DEV)
+    G, M, K = 2, 256, 256
+    w = rng.standard_normal((G, M, K)).astype(np.float32) * 0.02
+    w[0, 0, 5] = np.nan                       # NaN: row block (0, 0) and column block (5, 0)
+    w[0, 40, 1] = np.inf
+    w[0, 70, 140] = -np.inf
+    w[1, 3, 200] = -0.0
+    w[1, 10, 0:32] = rng.standard_normal(32) * 1e-39          # an all-subnormal row block
+    w[1, 64:96, 9] = rng.standard_normal(32) * 2e-39          # an all-subnormal column block
+    w[1, 20, :] = 0.0
+    w[1, 30, 64:96] = 3.38e38 * np.sign(rng.standard_normal(32))   # near the largest bf16
+    w[0, 100, 7] = 1e-39                                      # subnormals among normal values
+    w[0, 101, 7] = -4e-40
+    wt = torch.from_numpy(w).to(torch.bfloat16)
+    wf = bf16_np(wt)
+    dt = mgq.E4M3 if fmt == "e4m3" else mgq.E5M2
+    mode = mgq.RCEIL if e8m0 == "rceil" else mgq.FLOOR
+    codes = torch.empty(G, M, K, dtype=torch.uint8, device=dev)
+    sc = torch.empty(mgq.mx_scale_bytes(G * M, K), dtype=torch.uint8, device=dev)
+    col = torch.empty(G, K, M, dtype=torch.uint8, device=dev)
+    csc = torch.empty(mgq.mx_scale_bytes(G * K, M), dtype=torch.uint8, device=dev)
+    mgq.block_quantize(wt.to(dev), mgq.qdesc(dt, mgq.MX32_E8M0, codes, sc, col, csc, e8m0_mode=mode))
+    torch.cuda.synchronize()
+    c, s_ = OQ.quantize_mx(wf.reshape(G * M, K), fmt, e8m0)
+    assert np.array_equal(u8_np(codes).reshape(G * M, K), c)
+    assert np.array_equal(untile_mx_scales(u8_np(sc), G * M, K), s_)
+    cs_all = untile_mx_scales(u8_np(csc), G * K, M).reshape(G, K, M // 32)
+    for g in range(G):
+        cc, cs = OQ.quantize_mx(wf[g].T, fmt, e8m0)
+        assert np.array_equal(u8_np(col)[g], cc)
+        assert np.array_equal(cs_all[g], cs)
+    assert s_[0, 0] == 255 and s_[40, 0] == 255                 # the NaN and inf blocks
+
+
 @pytest.mark.parametrize("mode", ["mx", "tensor", "blk128", "nvfp4", "mx_col"])
 def test_block_quantize_weights(mgq, mode):
     rng = np.random.default_rng(13)
