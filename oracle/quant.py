@@ -21,6 +21,12 @@ Sources:
   issue #1152, repro steps).
 * NVFP4: e2m1 codes packed two per byte (Megatron-LM PR #5487, review
   comments), 16-element e4m3 block scales and one float32 scale per tensor.
+* NVFP4 weights with 16x16 blocks (the NVFP4 primary-weight path of the same
+  PR's coverage matrix, where one grouped weight carries row-wise and
+  column-wise data): the pages fix no weight block shape. Reading taken here:
+  one ue4m3 scale per 16x16 block of each expert's weight, from the block's
+  amax by the 1x16 rule, shared by the row-wise and the column-wise copy, so
+  the two copies hold the same element codes, transposed.
 """
 from __future__ import annotations
 
@@ -253,3 +259,39 @@ def dequantize_nvfp4(packed, sc_code, s_g, K):
     v = decode(q, E2M1)
     sc = np.repeat(decode(sc_code, UE4M3), NVFP4_BLOCK, axis=1)[:, :K]
     return v * sc / np.float64(np.float32(s_g))
+
+
+def quantize_nvfp4_2d(w, s_g):
+    """NVFP4 quantisation of one weight ``w`` [M, K] (M, K multiples of 16)
+    with 16x16 blocks and global scale ``s_g``.
+
+    Block scale code = ue4m3 cast of float32(float32(amax_b / 6) * s_g) over
+    the 16x16 block; with sc its value, r = float32(s_g / sc) (0 when sc == 0)
+    and each element code is the e2m1 cast of float32(x * r). Returns
+    (row codes [M, K/2], row scale codes [M, K/16], column codes [K, M/2],
+    column scale codes [K, M/16]): each 1x16 block of either copy carries the
+    scale of its 16x16 block; element 2i in the low nibble."""
+    x = np.asarray(w, dtype=np.float64)
+    M, K = x.shape
+    B = NVFP4_BLOCK
+    if M % B or K % B:
+        raise ValueError("M and K must be multiples of 16")
+    blocks = np.abs(x).reshape(M // B, B, K // B, B)
+    amax_b = f32(blocks.max(axis=(1, 3)))                       # [M/16, K/16]
+    s_g = np.float32(s_g)
+    t = (amax_b / np.float32(6.0)).astype(np.float32) * s_g
+    sc_code = encode(t.astype(np.float32).astype(np.float64), UE4M3)
+    sc = decode(sc_code, UE4M3).astype(np.float32)
+    with np.errstate(divide="ignore"):
+        r = np.where(sc == 0, np.float32(0), s_g / np.where(sc == 0, np.float32(1), sc))
+    r = r.astype(np.float32)
+    r_full = np.repeat(np.repeat(r, B, axis=0), B, axis=1)      # [M, K]
+    y = f32(x) * r_full
+    q = encode(f32(y).astype(np.float64), E2M1)                 # [M, K] element codes
+
+    def pack(c):
+        return ((c[:, 0::2] & 0xF) | ((c[:, 1::2] & 0xF) << 4)).astype(np.uint8)
+
+    row_sc = np.repeat(sc_code, B, axis=0)                      # [M, K/16]
+    col_sc = np.repeat(sc_code.T, B, axis=0)                    # [K, M/16]
+    return pack(q), row_sc.astype(np.uint8), pack(np.ascontiguousarray(q.T)), col_sc.astype(np.uint8)

@@ -199,3 +199,73 @@ def test_nvfp4_packing_order():
     x[0, 0], x[0, 1] = 6.0, 1.0     # e2m1 codes 7 and 2
     packed, _ = Q.quantize_nvfp4(x, np.float32(1.0))
     assert packed[0, 0] == 0x27
+
+
+# ---- NVFP4 weights with 16x16 blocks -------------------------------------------
+
+def _diag_block_weight(rng, nbm, nbk):
+    """Each 16x16 block holds its largest magnitude A_b once in every row and
+    every column (on its diagonal, random signs), the rest smaller."""
+    B = 16
+    w = rng.uniform(-1.0, 1.0, (nbm * B, nbk * B)) * 0.5
+    for i in range(nbm):
+        for j in range(nbk):
+            A = rng.uniform(1.0, 4.0)
+            for d in range(B):
+                w[i * B + d, j * B + d] = A * rng.choice([-1.0, 1.0])
+    return F.round_to_bf16(w)
+
+
+def test_nvfp4_2d_equals_1d_when_every_row_and_column_holds_the_block_max():
+    """With the block maximum in every row and every column of each 16x16
+    block, the 2D block scale equals each 1x16 row block's and each 16x1
+    column block's own scale: the row copy is the 1x16 quantisation of w and
+    the column copy the 1x16 quantisation of w^T."""
+    rng = np.random.default_rng(41)
+    w = _diag_block_weight(rng, 3, 4)
+    s_g = Q.nvfp4_global_scale(float(np.max(np.abs(w))))
+    rc, rs, cc, cs = Q.quantize_nvfp4_2d(w, s_g)
+    rc1, rs1 = Q.quantize_nvfp4(w, s_g)
+    cc1, cs1 = Q.quantize_nvfp4(w.T, s_g)
+    np.testing.assert_array_equal(rc, rc1)
+    np.testing.assert_array_equal(rs, rs1)
+    np.testing.assert_array_equal(cc, cc1)
+    np.testing.assert_array_equal(cs, cs1)
+
+
+def test_nvfp4_2d_block_scale_is_shared_across_rows():
+    """One large element sets the scale of its whole 16x16 block: with s_g = 1
+    and amax 6 the scale is 1.0 (ue4m3 0x38), so 0.4 in another row of the
+    block is cast as e2m1(0.4) = 0.5 (code 1), where its own 1x16 row block
+    would have scaled it to 6 (code 7)."""
+    w = np.zeros((16, 16))
+    w[0, 3] = 6.0
+    w[5, 9] = 0.4
+    w = F.round_to_bf16(w)
+    rc, rs, cc, cs = Q.quantize_nvfp4_2d(w, np.float32(1.0))
+    assert np.all(rs == 0x38) and np.all(cs == 0x38)
+    q = Q.unpack_e2m1(rc, 16)
+    assert q[0, 3] == 0x7 and q[5, 9] == 0x1
+    assert int(np.count_nonzero(q)) == 2
+    # the column copy holds the same element codes, transposed
+    np.testing.assert_array_equal(Q.unpack_e2m1(cc, 16), q.T)
+    rc1, _ = Q.quantize_nvfp4(w[5:6], np.float32(1.0))
+    assert Q.unpack_e2m1(rc1, 16)[0, 9] == 0x7
+
+
+def test_nvfp4_2d_dequantised_error_bound():
+    """|dequant(q) - w| is at most half the e2m1 spacing at y = |w| s_g / sc,
+    plus the saturated excess max(0, y - 6) (the ue4m3 scale may round below
+    amax_b s_g / 6), times sc / s_g, up to the float32 rounding of r."""
+    rng = np.random.default_rng(43)
+    w = F.round_to_bf16(rng.standard_normal((64, 96)) * 0.02)
+    s_g = Q.nvfp4_global_scale(float(np.max(np.abs(w))))
+    rc, rs, cc, cs = Q.quantize_nvfp4_2d(w, s_g)
+    deq = Q.dequantize_nvfp4(rc, rs, s_g, 96)
+    sc = np.repeat(F.decode(rs, F.UE4M3), 16, axis=1)
+    y = np.abs(w) * np.float64(s_g) / np.where(sc == 0, 1, sc)
+    spacing = np.where(y < 2, 0.5, np.where(y < 4, 1.0, 2.0))
+    bound = (0.5 * spacing + np.maximum(0.0, y - 6.0)) * sc / np.float64(s_g) * (1 + 2.0 ** -20)
+    assert np.all(np.abs(deq - w) <= bound + 1e-30)
+    assert np.max(y) > 6.0                      # the case the excess term covers occurs here
+    np.testing.assert_array_equal(Q.dequantize_nvfp4(cc, cs, s_g, 64), deq.T)
