@@ -716,6 +716,18 @@ int mgq_block_quantize(const void* x_bf16, int64_t G, int64_t M, int64_t K, cons
     MGQ_LAUNCH_CHECK();
     return MGQ_OK;
   }
+  if (q && q->scaling == MGQ_NV16x16_UE4M3) {
+    MGQ_CHECK_ARG(q->dtype == MGQ_E2M1 && q->row.data && q->row.scale && q->amax_out && q->tensor_scale);
+    MGQ_CHECK_ARG(aligned16(q->row.data) && aligned16(q->row.scale) && x_bf16 && aligned16(x_bf16));
+    MGQ_CHECK_ARG(!q->col.data || (q->col.scale && aligned16(q->col.data) && aligned16(q->col.scale)));
+    MGQ_CHECK_ARG(G >= 1 && M > 0 && K > 0 && M % 128 == 0 && K % 128 == 0);
+    cudaStream_t s = as_stream(stream);
+    int rc = launch_amax_groups(static_cast<const uint16_t*>(x_bf16), M * K, G, q->amax_out, s);
+    if (rc != MGQ_OK) return rc;
+    return quant_nv2d(static_cast<const uint16_t*>(x_bf16), G, M, K, static_cast<uint8_t*>(q->row.data),
+                      static_cast<uint8_t*>(q->row.scale), static_cast<uint8_t*>(q->col.data),
+                      static_cast<uint8_t*>(q->col.scale), q->amax_out, q->tensor_scale, s);
+  }
   if (q && q->scaling == MGQ_BLK_128x128_F32) {
     MGQ_CHECK_ARG(q->row.data && q->row.scale && aligned16(q->row.data) && x_bf16 && aligned16(x_bf16));
     MGQ_CHECK_ARG(G >= 1 && M > 0 && K > 0 && M % 128 == 0 && K % 128 == 0);

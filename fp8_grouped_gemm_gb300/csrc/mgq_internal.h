@@ -59,6 +59,12 @@ int gather_x_rowcol(const uint16_t* x, const int32_t* src_row, int k, int64_t H,
 int col_gather_dy(const uint16_t* dout, const float* probs, const int32_t* src_row, int k, int64_t H,
                   int64_t R_cap, const int32_t* rows_used, const mgq_qdesc* q, cudaStream_t s);
 
+// NVFP4 weights with 16x16 blocks: row-wise [G*M, K/2] and (when col_codes
+// is set) column-wise [G*K, M/2] codes with tiled ue4m3 scales; s_g per group
+// from amax (written to s_out) (quant_tile.cu)
+int quant_nv2d(const uint16_t* x, int64_t G, int64_t M, int64_t K, uint8_t* row_codes, uint8_t* row_scales,
+               uint8_t* col_codes, uint8_t* col_scales, const float* amax, float* s_out, cudaStream_t s);
+
 }  // namespace mgq
 
 #define MGQ_CHECK_ARG(cond)                 \

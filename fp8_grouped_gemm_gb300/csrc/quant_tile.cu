@@ -536,6 +536,103 @@ RowColArgs make_args(const mgq_qdesc* q, int64_t rows_cap, const int32_t* rows_u
   return a;
 }
 
+// ---- NVFP4 weights with 16x16 blocks ------------------------------------------
+// One 128x128 tile of a group's [M, K] weight per CTA, staged in shared
+// memory: the 64 block amaxes (4 threads per 16x16 block), then the ue4m3
+// scale code and multiplier r = s_g / sc of each block by the 1x16 rule, then
+// the row-wise copy ([G*M, K/2], one 1x16 block per thread step) and the
+// column-wise copy ([G*K, M/2], a thread takes 64 rows of one column). Both
+// copies' 1x16 blocks carry the scale of their 16x16 block.
+__global__ void __launch_bounds__(256) quant_nv2d_kernel(const uint16_t* x, int64_t M, int64_t K, uint8_t* row_codes,
+                                                         uint8_t* row_scales, uint8_t* col_codes, uint8_t* col_scales,
+                                                         const float* amax, float* s_out) {
+  __shared__ __align__(16) uint16_t tile[TR * LD];
+  __shared__ uint8_t s_code[64];
+  __shared__ float s_r[64];
+  const int tid = threadIdx.x;
+  const int64_t c0 = (int64_t)blockIdx.x * TC, r0 = (int64_t)blockIdx.y * TR;
+  const int64_t g = r0 / M, m0 = r0 - g * M;    // group, first row inside it
+  const float s_g = nv_global_scale(amax[g]);
+  if (blockIdx.x == 0 && m0 == 0 && tid == 0) s_out[g] = s_g;
+  {
+    uint4 w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int chunk = tid + 256 * i;
+      w[i] = __ldg(reinterpret_cast<const uint4*>(x + (r0 + (chunk >> 4)) * K + c0 + (chunk & 15) * 8));
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int chunk = tid + 256 * i;
+      *reinterpret_cast<uint4*>(&tile[(chunk >> 4) * LD + (chunk & 15) * 8]) = w[i];
+    }
+  }
+  __syncthreads();
+  {
+    // block b = (br, bc); this thread's quarter: rows 16 br + 4 q .. + 3
+    const int b = tid >> 2, q = tid & 3, br = b >> 3, bc = b & 7;
+    uint32_t acc = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4* p = reinterpret_cast<const uint4*>(&tile[(16 * br + 4 * q + j) * LD + 16 * bc]);
+      const uint4 w0 = p[0], w1 = p[1];
+      acc = absmax_acc_bf16x2(absmax_acc_bf16x2(absmax_acc_bf16x2(absmax_acc_bf16x2(acc, w0.x), w0.y), w0.z), w0.w);
+      acc = absmax_acc_bf16x2(absmax_acc_bf16x2(absmax_acc_bf16x2(absmax_acc_bf16x2(acc, w1.x), w1.y), w1.z), w1.w);
+    }
+    uint32_t m = fold_bf16x2(absmax_bf16x2_final(acc));
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+    if (q == 0) {
+      const float t = __fmul_rn(__fdiv_rn(__uint_as_float(m), 6.0f), s_g);
+      const uint32_t code = cvt_ue4m3(t);
+      const float sc = ue4m3_value(code);
+      s_code[b] = (uint8_t)code;
+      s_r[b] = (sc == 0.0f) ? 0.0f : __fdiv_rn(s_g, sc);
+    }
+  }
+  __syncthreads();
+  // row-wise copy: items (row, 16-column block), 4 per thread
+#pragma unroll 1
+  for (int j = 0; j < 4; ++j) {
+    const int item = tid + 256 * j, row = item >> 3, blk = item & 7;
+    const int b = (row >> 4) * 8 + blk;
+    const float r = s_r[b];
+    const uint4* p = reinterpret_cast<const uint4*>(&tile[row * LD + 16 * blk]);
+    const uint4 w0 = p[0], w1 = p[1];
+    const uint32_t ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    float y[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      y[2 * i] = __fmul_rn(bf16_lo(ww[i]), r);
+      y[2 * i + 1] = __fmul_rn(bf16_hi(ww[i]), r);
+    }
+    const int64_t grow = r0 + row, c = c0 + 16 * blk;
+    *reinterpret_cast<uint2*>(row_codes + grow * (K / 2) + c / 2) = make_uint2(cvt_e2m1x8(y), cvt_e2m1x8(y + 8));
+    row_scales[tiled_scale_offset(grow, c / 16, K / 64)] = s_code[b];
+  }
+  if (!col_codes) return;
+  // column-wise copy: column col, row blocks 4 hb .. 4 hb + 3 (64 rows, 32 bytes)
+  {
+    const int col = tid & 127, hb = tid >> 7;
+    const int64_t crow = g * K + c0 + col;        // row of the column-wise copy
+    uint32_t out[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int rb = 4 * hb + k, b = rb * 8 + (col >> 4);
+      const float r = s_r[b];
+      float y[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(__uint_as_float((uint32_t)tile[(16 * rb + i) * LD + col] << 16), r);
+      out[2 * k] = cvt_e2m1x8(y);
+      out[2 * k + 1] = cvt_e2m1x8(y + 8);
+      col_scales[tiled_scale_offset(crow, (m0 + 16 * rb) / 16, M / 64)] = s_code[b];
+    }
+    uint4* dst = reinterpret_cast<uint4*>(col_codes + crow * (M / 2) + (m0 + 64 * hb) / 2);
+    dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+    dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+  }
+}
+
 }  // namespace
 
 int rowcol_plain(const uint16_t* x, int64_t G, int64_t M, int64_t K, const mgq_qdesc* q, cudaStream_t s) {
@@ -564,6 +661,15 @@ int col_gather_dy(const uint16_t* dout, const float* probs, const int32_t* src_r
   RowColArgs a = make_args(q, R_cap, rows_used, H, R_cap);
   a.row_codes = nullptr;       // the row-wise codes come from the unpermute-backward kernel
   return launch_rowcol(SrcGatherDy{dout, probs, src_row, k, H}, q, a, s);
+}
+
+int quant_nv2d(const uint16_t* x, int64_t G, int64_t M, int64_t K, uint8_t* row_codes, uint8_t* row_scales,
+               uint8_t* col_codes, uint8_t* col_scales, const float* amax, float* s_out, cudaStream_t s) {
+  if ((G * M) / TR > 65535) return MGQ_ERR_UNSUPPORTED;
+  const dim3 grid((unsigned)(K / TC), (unsigned)(G * M / TR));
+  quant_nv2d_kernel<<<grid, 256, 0, s>>>(x, M, K, row_codes, row_scales, col_codes, col_scales, amax, s_out);
+  MGQ_LAUNCH_CHECK();
+  return MGQ_OK;
 }
 
 }  // namespace mgq

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libmgq.so")
 # enums of mgq.h
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE_INDEX = range(6)
 E4M3, E5M2, E2M1 = 0, 1, 2
-MX32_E8M0, NV16_UE4M3, BLK_1x128_F32, BLK_128x128_F32, TENSOR_F32 = range(5)
+MX32_E8M0, NV16_UE4M3, BLK_1x128_F32, BLK_128x128_F32, TENSOR_F32, NV16x16_UE4M3 = range(6)
 RCEIL, FLOOR = 0, 1
 OUT_BF16, OUT_F32 = 0, 1
 LAYOUT_K, LAYOUT_MN = 0, 1

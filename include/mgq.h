@@ -48,6 +48,14 @@
  *                    16-element block (ld a multiple of 64 elements);
  *                    plus one float32 global scale s_g per tensor (weights:
  *                    per expert) in tensor_scale; value = e2m1 * sc / s_g.
+ *  MGQ_NV16x16_UE4M3 weights only (mgq_block_quantize): one ue4m3 scale per
+ *                    16x16 block of each group's [M, K], by the NVFP4 rule
+ *                    on the block's amax; written as MGQ_NV16_UE4M3 row-wise
+ *                    and column-wise copies whose 1x16 blocks carry their
+ *                    16x16 block's scale, so both copies hold the same
+ *                    element codes, transposed. Reading of [GROUPED]'s NVFP4
+ *                    primary-weight path (one grouped weight with row-wise
+ *                    and column-wise data); the page fixes no block shape.
  *  MGQ_BLK_1x128_F32 float32 scale_inv per 128 elements of a row, stored
  *                    k-block major: scale_inv[b * rows_cap + r].
  *  MGQ_BLK_128x128_F32 float32 scale_inv per 128x128 tile of each expert's
@@ -83,7 +91,8 @@ typedef enum {
   MGQ_NV16_UE4M3 = 1,
   MGQ_BLK_1x128_F32 = 2,
   MGQ_BLK_128x128_F32 = 3,
-  MGQ_TENSOR_F32 = 4
+  MGQ_TENSOR_F32 = 4,
+  MGQ_NV16x16_UE4M3 = 5
 } mgq_scaling;
 
 /* Exponent of an E8M0 block scale. RCEIL: the smallest power of two that
@@ -217,7 +226,11 @@ int mgq_moe_permute_noalloc(const void* x_bf16, int T, int H, const int32_t* top
  * [GROUPED] row-wise and column-wise data and scales of one grouped weight.
  *  x_bf16  device [G, M, K] bf16 (G groups, e.g. experts)
  *  q->row  [G, M, K] codes (+ scales); q->col [G, K, M] codes (+ scales)
- *  per-tensor / NVFP4 modes read one scale per group from q->tensor_scale.
+ *  per-tensor mode reads one scale per group from q->tensor_scale.
+ *  NVFP4 (MGQ_NV16_UE4M3, row-wise only; MGQ_NV16x16_UE4M3, row-wise and
+ *    optionally column-wise, dtype MGQ_E2M1): an amax pre-pass writes each
+ *    group's amax to q->amax_out [G] and s_g = 6*448/amax to
+ *    q->tensor_scale [G]; codes [G, M, K/2] / [G, K, M/2] bytes.
  * Requires M and K multiples of 128. */
 int mgq_block_quantize(const void* x_bf16, int64_t G, int64_t M, int64_t K,
                        const mgq_qdesc* q, void* stream);

@@ -453,6 +453,81 @@ def test_gemm_fwd_nvfp4(mgq, offs):
     assert rel_fro(OF.round_to_bf16(ref), got[:Rp]) <= GEMM_TOL_BF16
 
 
+def test_nvfp4_2d_weights_fwd_and_dgrad(mgq):
+    """NVFP4 weights with 16x16 blocks in one pass (row-wise and column-wise
+    copies, one amax pre-pass, s_g per expert) equal the oracle's; the forward
+    GEMM on the row-wise copy and the dgrad on the column-wise copy (both read
+    as ordinary 1x16 NVFP4 operands) equal the oracle's GEMMs of the
+    dequantised operands."""
+    rng = np.random.default_rng(71)
+    dev = torch.device(DEV)
+    E, N, K = 3, 256, 512
+    offs = np.array([0, 128, 384, 512], dtype=np.int32)
+    Rp = int(offs[-1])
+    R_cap = Rp + 128
+    w = _bf16(rng, (E, N, K), 0.02)
+    w[1, 7, 100] = 0.5                                    # an outlier block in expert 1
+    wf = bf16_np(w)
+    rowc = torch.full((E, N, K // 2), 0xAB, dtype=torch.uint8, device=dev)
+    rows = torch.full((mgq.nv_scale_bytes(E * N, K),), 0xCD, dtype=torch.uint8, device=dev)
+    colc = torch.full((E, K, N // 2), 0xAB, dtype=torch.uint8, device=dev)
+    cols = torch.full((mgq.nv_scale_bytes(E * K, N),), 0xCD, dtype=torch.uint8, device=dev)
+    amax = torch.full((E,), -1.0, dtype=torch.float32, device=dev)
+    sg = torch.zeros(E, dtype=torch.float32, device=dev)
+    mgq.block_quantize(w.to(dev), mgq.qdesc(mgq.E2M1, mgq.NV16x16_UE4M3, rowc, rows, colc, cols,
+                                            tensor_scale=sg, amax_out=amax))
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    rs_all = untile_mx_scales(u8_np(rows), E * N, K, 16).reshape(E, N, K // 16)
+    cs_all = untile_mx_scales(u8_np(cols), E * K, N, 16).reshape(E, K, N // 16)
+    w_deq, wt_deq = [], []
+    for e in range(E):
+        am = float(np.max(np.abs(wf[e])))
+        s_g = OQ.nvfp4_global_scale(am)
+        assert float(amax[e].item()) == am and float(sg[e].item()) == float(s_g)
+        rc, rs, cc, cs = OQ.quantize_nvfp4_2d(wf[e], s_g)
+        assert np.array_equal(u8_np(rowc)[e], rc)
+        assert np.array_equal(rs_all[e], rs)
+        assert np.array_equal(u8_np(colc)[e], cc)
+        assert np.array_equal(cs_all[e], cs)
+        w_deq.append(OQ.dequantize_nvfp4(rc, rs, s_g, K))
+        wt_deq.append(OQ.dequantize_nvfp4(cc, cs, s_g, N))
+    w_deq, wt_deq = np.stack(w_deq), np.stack(wt_deq)
+    assert np.array_equal(wt_deq, w_deq.transpose(0, 2, 1))
+
+    def act(rows_, cols_, std):
+        x = _bf16(rng, (rows_, cols_), std)
+        x[Rp:] = 0
+        c = torch.empty(rows_, cols_ // 2, dtype=torch.uint8, device=dev)
+        sc = torch.empty(mgq.nv_scale_bytes(rows_, cols_), dtype=torch.uint8, device=dev)
+        am, g = torch.empty(1, device=dev), torch.empty(1, device=dev)
+        mgq.block_quantize(x.to(dev), mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, c, sc, tensor_scale=g, amax_out=am))
+        torch.cuda.synchronize()
+        op = _op(mgq, u8_np(c), u8_np(sc), cols_, mgq.E2M1, dev)
+        op.global_scale = g.data_ptr()
+        deq = OQ.dequantize_nvfp4(u8_np(c)[:Rp], untile_mx_scales(u8_np(sc), rows_, cols_, 16)[:Rp],
+                                  np.float32(g.item()), cols_)
+        return op, deq, (c, sc, g)
+
+    offd = torch.from_numpy(offs).to(dev)
+    A, a_deq, keep_a = act(R_cap, K, 1.0)
+    W_row = _op(mgq, u8_np(rowc).reshape(E * N, K // 2), u8_np(rows), K, mgq.E2M1, dev)
+    W_row.global_scale = sg.data_ptr()
+    Y = torch.full((R_cap, N), float("nan"), dtype=torch.bfloat16, device=dev)
+    mgq.grouped_gemm_fwd(A, W_row, mgq.NV16_UE4M3, offd, E, R_cap, N, K, Y)
+    dY, dy_deq, keep_dy = act(R_cap, N, 1e-3)
+    W_col = _op(mgq, u8_np(colc).reshape(E * K, N // 2), u8_np(cols), N, mgq.E2M1, dev)
+    W_col.global_scale = sg.data_ptr()
+    dA = torch.full((R_cap, K), float("nan"), dtype=torch.bfloat16, device=dev)
+    mgq.grouped_gemm_dgrad(dY, W_col, mgq.NV16_UE4M3, offd, E, R_cap, N, K, dA)
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    ref = OG.grouped_gemm_fwd(a_deq, w_deq, offs)
+    assert rel_fro(OF.round_to_bf16(ref), bf16_np(Y)[:Rp]) <= GEMM_TOL_BF16
+    ref_d = OG.grouped_gemm_dgrad(dy_deq, w_deq, offs)
+    assert rel_fro(OF.round_to_bf16(ref_d), bf16_np(dA)[:Rp]) <= GEMM_TOL_BF16
+
+
 def test_gemm_grouped_equals_per_group(mgq):
     """The grouped call equals single-group calls on each expert's rows
     (grouped vs discrete comparison of Megatron-LM PR #5487's test matrix),
