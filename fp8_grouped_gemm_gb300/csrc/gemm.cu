@@ -94,6 +94,7 @@ struct GemmParams {
   uint32_t idesc;
   int tma_store;      // write the output through TMA stores
   int a_mn, b_mn;     // pair kernel: operand stored MN-major (contraction down the rows)
+  int kdiv;           // contract mode: group rows per byte of the operands (2: e2m1)
   int64_t b_half2;    // rows from the first to the second 128-row half of a B tile
                       // (128; SwiGLU: F, the up rows matching the gate rows)
   // SwiGLU epilogue (gate/up GEMM): h = bf16(silu(g) u) of the bf16-rounded
@@ -155,10 +156,11 @@ __device__ __forceinline__ bool get_tile(const int32_t* s_off, int E, const Gemm
     const int64_t local = t % tpe;
     const int64_t m = local / nK, n = local % nK;
     tl.e = e;
-    tl.nst = (s_off[e + 1] - s_off[e]) / BK;
+    // a stage covers BK bytes of the group's rows (2 BK rows for e2m1)
+    tl.nst = (s_off[e + 1] - s_off[e]) / (BK * p.kdiv);
     tl.row_a = BM * m;
     tl.row_b = BN * n;
-    tl.kx0 = s_off[e];
+    tl.kx0 = s_off[e] / p.kdiv;
     tl.out_row = (int64_t)e * p.N + BM * m;
     tl.out_col = BN * n;
   }
@@ -524,7 +526,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     // the group layout must be 128-row aligned and inside the buffers
     bool bad = s_off[0] != 0;
-    for (int e = 0; e < E; ++e) bad |= (s_off[e + 1] < s_off[e]) || (s_off[e + 1] % BM) != 0;
+    // (contract mode over e2m1: whole 256-row stages)
+    const int align = MODE == kModeContract ? BM * p.kdiv : BM;
+    for (int e = 0; e < E; ++e) bad |= (s_off[e + 1] < s_off[e]) || (s_off[e + 1] % align) != 0;
     bad |= (int64_t)s_off[E] > p.R_cap;
     if (bad) {
       *s_bad = 1;
@@ -1232,7 +1236,7 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
   if (scaling == MGQ_MX32_E8M0) kind = kKindMX;
   else if (scaling == MGQ_TENSOR_F32) kind = kKindTensor;
   else if (scaling == MGQ_BLK_1x128_F32 && mode == kModeRows) kind = kKindBlock;
-  else if (scaling == MGQ_NV16_UE4M3 && mode == kModeRows) kind = kKindNV;
+  else if (scaling == MGQ_NV16_UE4M3) kind = kKindNV;
   else return MGQ_ERR_UNSUPPORTED;
   const bool mx = kind == kKindMX;
   const bool nv = kind == kKindNV;
@@ -1268,18 +1272,23 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
   } else {
     MGQ_CHECK_ARG(N > 0 && K > 0 && N % BM == 0 && K % BN == 0);
     MGQ_CHECK_ARG((a_mn || A->ld >= R_cap) && (b_mn || B->ld >= R_cap));
-    if ((!a_mn && !encode_tmap_u8_2d(&ta, A->data, (uint64_t)R_cap, (uint64_t)N, (uint64_t)A->ld, 128, BM)) ||
-        (!b_mn && !encode_tmap_u8_2d(&tb, B->data, (uint64_t)R_cap, (uint64_t)K, (uint64_t)B->ld, 128, 128)))
+    if (nv) MGQ_CHECK_ARG(R_cap % 256 == 0);
+    if ((!a_mn && !encode_tmap_u8_2d(&ta, A->data, (uint64_t)(R_cap / ebytes_den), (uint64_t)N,
+                                     (uint64_t)(A->ld / ebytes_den), 128, BM)) ||
+        (!b_mn && !encode_tmap_u8_2d(&tb, B->data, (uint64_t)(R_cap / ebytes_den), (uint64_t)K,
+                                     (uint64_t)(B->ld / ebytes_den), 128, 128)))
       return MGQ_ERR_CUDA;
-    p.sfa_kb4 = A->ld / 128;
-    p.sfb_kb4 = B->ld / 128;
+    p.sfa_kb4 = A->ld / (nv ? 64 : 128);
+    p.sfb_kb4 = B->ld / (nv ? 64 : 128);
   }
   int* err = error_word();
   if (!err) return MGQ_ERR_CUDA;
   p.offsets = offsets;
   p.E = E;
   p.N = N;
-  p.K = K / ebytes_den;          // in bytes of the operand rows: 128 per stage
+  // rows: contraction length in bytes of the operand rows (128 per stage);
+  // contract: output columns
+  p.K = mode == kModeRows ? K / ebytes_den : K;
   p.R_cap = R_cap;
   p.sfa = static_cast<const uint8_t*>(A->scale);
   p.sfb = static_cast<const uint8_t*>(B->scale);
@@ -1293,6 +1302,7 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
   p.tma_store = 0;
   p.a_mn = 0;
   p.b_mn = 0;
+  p.kdiv = (nv && mode == kModeContract) ? 2 : 1;
   p.b_half2 = 128;
   p.swiglu = 0;
   p.F = 0;
@@ -1439,6 +1449,7 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
     return launch_gemm<kModeRows, kKindBlock>(ta, tb, to, th, p, s);
   }
   if (kind == kKindMX) return launch_gemm<kModeContract, kKindMX>(ta, tb, to, th, p, s);
+  if (kind == kKindNV) return launch_gemm<kModeContract, kKindNV>(ta, tb, to, th, p, s);
   return launch_gemm<kModeContract, kKindTensor>(ta, tb, to, th, p, s);
 }
 

@@ -528,6 +528,77 @@ def test_nvfp4_2d_weights_fwd_and_dgrad(mgq):
     assert rel_fro(OF.round_to_bf16(ref_d), bf16_np(dA)[:Rp]) <= GEMM_TOL_BF16
 
 
+def _nv_operand(rng, rows, cols):
+    """Random e2m1 codes [rows, cols] packed along cols, random ue4m3 block
+    scales [rows, cols/16]."""
+    q = rng.integers(0, 16, size=(rows, cols)).astype(np.uint8)
+    packed = ((q[:, 0::2] & 0xF) | ((q[:, 1::2] & 0xF) << 4)).astype(np.uint8)
+    sc = rng.integers(0x20, 0x58, size=(rows, cols // 16)).astype(np.uint8)
+    return packed, sc
+
+
+def test_gemm_wgrad_nvfp4(mgq):
+    """NVFP4 wgrad: dW_e = sum over the rows of group e of dY^T A, from the
+    column-wise copies dYcol [N, R_cap] and Acol [K, R_cap] (e2m1 packed along
+    the rows, 16-row ue4m3 blocks, one global scale each); groups of whole
+    256-row stages, one empty (zeros with beta 0, kept with beta 1)."""
+    rng = np.random.default_rng(73)
+    dev = torch.device(DEV)
+    offs = np.array([0, 256, 256, 768], dtype=np.int32)
+    E, N, K = 3, 256, 512
+    Rp = int(offs[-1])
+    R_cap = Rp + 256
+    dyt, dyts = _nv_operand(rng, N, R_cap)
+    at, ats = _nv_operand(rng, K, R_cap)
+    sg_dy = np.array([1.5e4], dtype=np.float32)
+    sg_a = np.array([3.0], dtype=np.float32)
+    A_op = _op(mgq, dyt, tile_mx_scales(dyts), R_cap, mgq.E2M1, dev)
+    B_op = _op(mgq, at, tile_mx_scales(ats), R_cap, mgq.E2M1, dev)
+    gdy, ga = _to_dev(sg_dy, dev), _to_dev(sg_a, dev)
+    A_op.global_scale = gdy.data_ptr()
+    B_op.global_scale = ga.data_ptr()
+    offd = torch.from_numpy(offs).to(dev)
+    dW = torch.full((E, N, K), 5.0, dtype=torch.float32, device=dev)
+    mgq.grouped_gemm_wgrad(A_op, B_op, mgq.NV16_UE4M3, offd, E, R_cap, N, K, dW, 0.0)
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    dy_deq = OQ.dequantize_nvfp4(dyt, dyts, sg_dy[0], R_cap).T[:Rp]
+    a_deq = OQ.dequantize_nvfp4(at, ats, sg_a[0], R_cap).T[:Rp]
+    ref = OG.grouped_gemm_wgrad(dy_deq, a_deq, offs, E)
+    got = dW.cpu().numpy().astype(np.float64)
+    assert np.all(got[1] == 0.0)
+    assert rel_fro(ref, got) <= GEMM_TOL_F32
+    prev = torch.from_numpy(rng.standard_normal((E, N, K)).astype(np.float32)).to(dev)
+    dW2 = prev.clone()
+    mgq.grouped_gemm_wgrad(A_op, B_op, mgq.NV16_UE4M3, offd, E, R_cap, N, K, dW2, 1.0)
+    torch.cuda.synchronize()
+    got2 = dW2.cpu().numpy().astype(np.float64)
+    assert np.array_equal(got2[1], prev[1].cpu().numpy().astype(np.float64))
+    assert rel_fro(ref + prev.cpu().numpy(), got2) <= GEMM_TOL_F32
+
+
+def test_gemm_wgrad_nvfp4_needs_256_row_groups(mgq):
+    """A group boundary inside a 256-row e2m1 stage is reported by the kernel
+    (MGQ_ERR_INVALID_ARG through the error word) and nothing is written."""
+    rng = np.random.default_rng(74)
+    dev = torch.device(DEV)
+    offs = np.array([0, 128, 512], dtype=np.int32)
+    E, N, K = 2, 256, 256
+    R_cap = 512
+    dyt, dyts = _nv_operand(rng, N, R_cap)
+    at, ats = _nv_operand(rng, K, R_cap)
+    A_op = _op(mgq, dyt, tile_mx_scales(dyts), R_cap, mgq.E2M1, dev)
+    B_op = _op(mgq, at, tile_mx_scales(ats), R_cap, mgq.E2M1, dev)
+    g1 = torch.ones(1, device=dev)
+    A_op.global_scale = g1.data_ptr()
+    B_op.global_scale = g1.data_ptr()
+    dW = torch.full((E, N, K), 5.0, dtype=torch.float32, device=dev)
+    mgq.grouped_gemm_wgrad(A_op, B_op, mgq.NV16_UE4M3, torch.from_numpy(offs).to(dev), E, R_cap, N, K, dW, 0.0)
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.ERR_INVALID_ARG
+    assert torch.all(dW == 5.0).item()
+
+
 def test_gemm_grouped_equals_per_group(mgq):
     """The grouped call equals single-group calls on each expert's rows
     (grouped vs discrete comparison of Megatron-LM PR #5487's test matrix),
