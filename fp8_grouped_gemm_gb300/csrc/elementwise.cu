@@ -229,11 +229,33 @@ struct UnpermBwdArgs {
   uint8_t* codes;        // [R_cap, H]
   uint8_t* scales;
   const float* tensor_scale;
-  float* amax_out;
+  float* amax_out;       // per-tensor: max |dY| (optional); NVFP4: the pre-pass amax (input)
+  float* s_out;          // NVFP4: s_g (output)
   float* dprobs;
   int rceil;
   int token_blocks;
 };
+
+// amax of dY = probs[t, j] * dout[t] over the routed entries (row_id_map >= 0):
+// float32 products round monotonically, so the maximum of |fl(p d)| over a
+// token's row is fl(|p| max |d|). One warp per token (strided), one atomic per CTA.
+__global__ void __launch_bounds__(256) dy_amax_kernel(const uint16_t* dout, const float* probs, const int32_t* rim,
+                                                      int T, int k, int H, float* amax) {
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31;
+  uint32_t tam = 0;
+  for (int64_t t = (int64_t)blockIdx.x * kWarps + warp; t < T; t += (int64_t)gridDim.x * kWarps) {
+    uint32_t acc = 0;
+    for (int c = 8 * lane; c < H; c += 256) {
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(dout + t * H + c));
+      acc = absmax_acc_bf16x2(absmax_acc_bf16x2(absmax_acc_bf16x2(absmax_acc_bf16x2(acc, w.x), w.y), w.z), w.w);
+    }
+    const float dmax = __uint_as_float(warp_max_u32(fold_bf16x2(absmax_bf16x2_final(acc))));
+    if (lane < (uint32_t)k && rim[t * k + lane] >= 0)
+      tam = max(tam, __float_as_uint(__fmul_rn(fabsf(probs[t * k + lane]), dmax)));
+  }
+  cta_amax_atomic(tam, amax);
+}
 
 // One warp per routing entry (t, j): row r = row_id_map[t, j] receives the
 // codes of probs[t, j] * dout[t] and dprobs[t, j] = <dout[t], Y[r]>. Lane l
@@ -256,14 +278,20 @@ __global__ void __launch_bounds__(256, SC == MGQ_TENSOR_F32 ? 3 : 2) unpermute_b
       if (a.src_row[mid] >= 0) lo = mid + 1;
       else hi = mid;
     }
+    constexpr int kBytesDen = SC == MGQ_NV16_UE4M3 ? 2 : 1;     // e2m1: two codes per byte
+    constexpr int kBlk = SC == MGQ_NV16_UE4M3 ? 16 : 32;          // elements per scale byte
     for (int64_t r = lo + warp; r < a.offsets[e + 1]; r += kWarps) {
-      for (int c = lane * 16; c < H; c += 512) *reinterpret_cast<uint4*>(a.codes + r * H + c) = make_uint4(0, 0, 0, 0);
-      if (SC == MGQ_MX32_E8M0)
-        for (int b4 = lane; b4 < H / 128; b4 += 32)
-          *reinterpret_cast<uint32_t*>(a.scales + tiled_scale_offset(r, (int64_t)b4 * 4, H / 128)) = 0u;
+      for (int c = lane * 16; c < H / kBytesDen; c += 512)
+        *reinterpret_cast<uint4*>(a.codes + r * (H / kBytesDen) + c) = make_uint4(0, 0, 0, 0);
+      if (SC == MGQ_MX32_E8M0 || SC == MGQ_NV16_UE4M3)
+        for (int b4 = lane; b4 < H / (4 * kBlk); b4 += 32)
+          *reinterpret_cast<uint32_t*>(a.scales + tiled_scale_offset(r, (int64_t)b4 * 4, H / (4 * kBlk))) = 0u;
     }
     return;
   }
+  // NVFP4: s_g from the dY amax pre-pass, published by the first warp
+  const float s_g = SC == MGQ_NV16_UE4M3 ? nv_global_scale(a.amax_out[0]) : 1.0f;
+  if (SC == MGQ_NV16_UE4M3 && blockIdx.x == 0 && threadIdx.x == 0) a.s_out[0] = s_g;
   uint32_t tam = 0;
   // the entry CTAs stride over the routing entries t * k + j
   for (int64_t g = (int64_t)blockIdx.x * kWarps + warp; g < (int64_t)a.T * a.k; g += (int64_t)a.token_blocks * kWarps) {
@@ -307,11 +335,17 @@ __global__ void __launch_bounds__(256, SC == MGQ_TENSOR_F32 ? 3 : 2) unpermute_b
         }
       }
       dp += s;
-      const uint32_t am = absmax_bits_f32(v, 32);
-      tam = max(tam, am);
-      Block32 o;
-      quantize32<SC, DT>(v, am, ts, a.rceil != 0, o);
-      if (c < H) store32<SC>(o, a.codes, a.scales, r, c, H, a.R_cap, lane);
+      if constexpr (SC == MGQ_NV16_UE4M3) {
+        Block32nv o;
+        quantize32_nv(v, s_g, o);
+        if (c < H) store32_nv(o, a.codes, a.scales, r, c, H, lane);
+      } else {
+        const uint32_t am = absmax_bits_f32(v, 32);
+        tam = max(tam, am);
+        Block32 o;
+        quantize32<SC, DT>(v, am, ts, a.rceil != 0, o);
+        if (c < H) store32<SC>(o, a.codes, a.scales, r, c, H, a.R_cap, lane);
+      }
     };
     uint4 d0[4], y0[4], d1[4], y1[4];
     load(0, d0, y0);
@@ -498,6 +532,34 @@ __global__ void __launch_bounds__(256) swiglu_h_kernel(const uint16_t* __restric
   if (lane == 0) atomic_max_nonneg(amax, __uint_as_float(tam));
 }
 
+// [dG | dU] = dSwiGLU(dh, g, u) (bf16, as the quantising kernels round them)
+// and its amax: the first pass of the NVFP4 dSwiGLU quantisation
+__global__ void __launch_bounds__(256) dswiglu_dgu_kernel(const uint16_t* __restrict__ dh,
+                                                          const uint16_t* __restrict__ gu, const int32_t* rows_used,
+                                                          int F, uint16_t* __restrict__ dgu, float* amax) {
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * kWarps + warp;
+  if (r >= *rows_used) return;
+  uint32_t tam = 0;
+  for (int c0 = 0; c0 < F; c0 += 1024) {
+    const int c = c0 + 32 * lane;
+    if (c < F) {
+      float d[32], g[32], u[32], dg[32], du[32];
+      load_bf16x32(dh + r * F + c, d);
+      load_bf16x32(gu + r * 2 * F + c, g);
+      load_bf16x32(gu + r * 2 * F + F + c, u);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) dswiglu_bf16(d[i], g[i], u[i], dg[i], du[i]);
+      tam = max(tam, max(absmax_bits_f32(dg, 32), absmax_bits_f32(du, 32)));
+      store_bf16x32(dgu + r * 2 * F + c, dg);
+      store_bf16x32(dgu + r * 2 * F + F + c, du);
+    }
+  }
+  tam = warp_max_u32(tam);
+  if (lane == 0) atomic_max_nonneg(amax, __uint_as_float(tam));
+}
+
 // ---- delayed scaling ------------------------------------------------------------
 // One warp per role: the lanes read the ring coalesced (entry h already
 // replaced by this step's amax) and reduce the max with shuffles; fmaxf drops
@@ -527,6 +589,14 @@ bool dtype_ok(int dt) { return dt == MGQ_E4M3 || dt == MGQ_E5M2; }
 
 int check_q(const mgq_qdesc* q) {
   if (!q || !q->row.data || !aligned16(q->row.data)) return MGQ_ERR_INVALID_ARG;
+  if (q->scaling == MGQ_NV16_UE4M3) {
+    // e2m1 codes, tiled ue4m3 scales, the amax pre-pass output and s_g
+    if (q->dtype != MGQ_E2M1 || !q->row.scale || !aligned16(q->row.scale) || !q->amax_out || !q->tensor_scale)
+      return MGQ_ERR_INVALID_ARG;
+    if (q->col.data && (!aligned16(q->col.data) || !q->col.scale || !aligned16(q->col.scale)))
+      return MGQ_ERR_INVALID_ARG;
+    return MGQ_OK;
+  }
   if (!dtype_ok(q->dtype)) return MGQ_ERR_UNSUPPORTED;
   if (q->scaling == MGQ_MX32_E8M0 || q->scaling == MGQ_BLK_1x128_F32) {
     if (!q->row.scale || !aligned16(q->row.scale)) return MGQ_ERR_INVALID_ARG;
@@ -590,13 +660,15 @@ int mgq_swiglu_quantize(const void* gu_bf16, int64_t R_cap, int F, const int32_t
     MGQ_CHECK_ARG(h_bf16 && aligned16(h_bf16) && gu_bf16 && aligned16(gu_bf16) && offsets && E >= 1);
     MGQ_CHECK_ARG(aligned16(q->row.data) && aligned16(q->row.scale));
     MGQ_CHECK_ARG(F > 0 && F % 128 == 0 && R_cap > 0 && R_cap % 128 == 0);
-    if (q->col.data) return MGQ_ERR_UNSUPPORTED;
+    if (q->col.data) MGQ_CHECK_ARG(q->col.scale && aligned16(q->col.data) && aligned16(q->col.scale));
     cudaStream_t s = as_stream(stream);
     if (cudaMemsetAsync(q->amax_out, 0, sizeof(float), s) != cudaSuccess) return MGQ_ERR_CUDA;
     const unsigned grid = (unsigned)((R_cap + kWarps - 1) / kWarps);
     swiglu_h_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(gu_bf16), offsets + E, F,
                                          static_cast<uint16_t*>(h_bf16), q->amax_out);
     MGQ_LAUNCH_CHECK();
+    // row-wise and column-wise copies of h in one tile pass
+    if (q->col.data) return rowcol_rows(static_cast<const uint16_t*>(h_bf16), R_cap, offsets + E, F, q, s);
     QuantRowsNvArgs a{static_cast<const uint16_t*>(h_bf16), R_cap, R_cap, F, offsets + E,
                       static_cast<uint8_t*>(q->row.data), static_cast<uint8_t*>(q->row.scale), q->amax_out,
                       q->tensor_scale};
@@ -627,6 +699,21 @@ int mgq_dswiglu_quantize(const void* dh_bf16, const void* gu_bf16, int64_t R_cap
   MGQ_CHECK_ARG(dh_bf16 && gu_bf16 && aligned16(dh_bf16) && aligned16(gu_bf16) && aligned16(dgu_bf16));
   MGQ_CHECK_ARG(offsets && E >= 1 && F > 0 && F % 128 == 0 && R_cap > 0 && R_cap % 128 == 0);
   cudaStream_t s = as_stream(stream);
+  if (q->scaling == MGQ_NV16_UE4M3) {
+    // two passes: [dG | dU] (materialised, dgu_bf16 required) and its amax,
+    // then the quantisation with s_g (rows, or rows and columns)
+    MGQ_CHECK_ARG(dgu_bf16 != nullptr);
+    if (cudaMemsetAsync(q->amax_out, 0, sizeof(float), s) != cudaSuccess) return MGQ_ERR_CUDA;
+    const unsigned grid = (unsigned)((R_cap + kWarps - 1) / kWarps);
+    dswiglu_dgu_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(dh_bf16),
+                                            static_cast<const uint16_t*>(gu_bf16), offsets + E, F,
+                                            static_cast<uint16_t*>(dgu_bf16), q->amax_out);
+    MGQ_LAUNCH_CHECK();
+    if (q->col.data) return rowcol_rows(static_cast<const uint16_t*>(dgu_bf16), R_cap, offsets + E, 2 * (int64_t)F, q, s);
+    return launch_quant_rows_nv(static_cast<const uint16_t*>(dgu_bf16), R_cap, offsets + E, 2 * (int64_t)F,
+                                static_cast<uint8_t*>(q->row.data), static_cast<uint8_t*>(q->row.scale), q->amax_out,
+                                q->tensor_scale, s);
+  }
   if (q->col.data)
     return rowcol_dswiglu(static_cast<const uint16_t*>(dh_bf16), static_cast<const uint16_t*>(gu_bf16), R_cap, F,
                           offsets + E, static_cast<uint16_t*>(dgu_bf16), q, s);
@@ -671,6 +758,18 @@ int mgq_moe_unpermute_bwd(const void* dout_bf16, const void* y_bf16, const int32
   MGQ_CHECK_ARG(T == 0 || (dout_bf16 && y_bf16 && row_id_map && probs));
   MGQ_CHECK_ARG(aligned16(dout_bf16) && aligned16(y_bf16) && R_cap > 0 && R_cap % 128 == 0);
   cudaStream_t s = as_stream(stream);
+  const bool nv = q->scaling == MGQ_NV16_UE4M3;
+  if (nv) {
+    if (T > 0) {
+      if (cudaMemsetAsync(q->amax_out, 0, sizeof(float), s) != cudaSuccess) return MGQ_ERR_CUDA;
+      const int blocks = (int)std::min<int64_t>((T + kWarps - 1) / kWarps, (int64_t)num_sms() * 4);
+      dy_amax_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint16_t*>(dout_bf16), probs, row_id_map, T, k, H,
+                                            q->amax_out);
+      MGQ_LAUNCH_CHECK();
+    } else if (cudaMemsetAsync(q->amax_out, 0, sizeof(float), s) != cudaSuccess) {
+      return MGQ_ERR_CUDA;
+    }
+  }
   UnpermBwdArgs a;
   a.dout = static_cast<const uint16_t*>(dout_bf16);
   a.y = static_cast<const uint16_t*>(y_bf16);
@@ -684,14 +783,20 @@ int mgq_moe_unpermute_bwd(const void* dout_bf16, const void* y_bf16, const int32
   a.scales = static_cast<uint8_t*>(q->row.scale);
   a.tensor_scale = q->tensor_scale;
   a.amax_out = q->amax_out;
+  a.s_out = q->tensor_scale;
   a.dprobs = dprobs;
   a.rceil = q->e8m0_mode == MGQ_E8M0_RCEIL;
   // entry CTAs: at most a few resident waves (they stride over the entries)
   a.token_blocks = (int)std::min<int64_t>(((int64_t)T * k + kWarps - 1) / kWarps,
                                           (int64_t)num_sms() * (q->scaling == MGQ_TENSOR_F32 ? 3 : 2));
   const unsigned grid = (unsigned)(a.token_blocks + E);
-  if (q->col.data && q->scaling != MGQ_TENSOR_F32 && q->scaling != MGQ_MX32_E8M0) return MGQ_ERR_UNSUPPORTED;
-  MGQ_DISPATCH_Q(q, unpermute_bwd_kernel, grid, a);
+  if (q->col.data && q->scaling != MGQ_TENSOR_F32 && q->scaling != MGQ_MX32_E8M0 && !nv) return MGQ_ERR_UNSUPPORTED;
+  if (nv) {
+    unpermute_bwd_kernel<MGQ_NV16_UE4M3, MGQ_E2M1><<<grid, 256, 0, s>>>(a);
+    MGQ_LAUNCH_CHECK();
+  } else {
+    MGQ_DISPATCH_Q(q, unpermute_bwd_kernel, grid, a);
+  }
   if (q->col.data && q->scaling == MGQ_TENSOR_F32)
     return launch_transpose_u8(static_cast<const uint8_t*>(q->row.data), H, static_cast<uint8_t*>(q->col.data),
                                R_cap, offsets + E, R_cap, H, s);
@@ -705,10 +810,12 @@ int mgq_block_quantize(const void* x_bf16, int64_t G, int64_t M, int64_t K, cons
     MGQ_CHECK_ARG(q->dtype == MGQ_E2M1 && q->row.data && q->row.scale && q->amax_out && q->tensor_scale);
     MGQ_CHECK_ARG(aligned16(q->row.data) && aligned16(q->row.scale) && x_bf16 && aligned16(x_bf16));
     MGQ_CHECK_ARG(G >= 1 && M > 0 && K > 0 && M % 128 == 0 && K % 128 == 0);
-    if (q->col.data) return MGQ_ERR_UNSUPPORTED;
+    if (q->col.data) MGQ_CHECK_ARG(q->col.scale && aligned16(q->col.data) && aligned16(q->col.scale));
     cudaStream_t s = as_stream(stream);
     int rc = launch_amax_groups(static_cast<const uint16_t*>(x_bf16), M * K, G, q->amax_out, s);
     if (rc != MGQ_OK) return rc;
+    // 1x16 blocks both ways: rows along K, columns along each group's M rows
+    if (q->col.data) return rowcol_plain(static_cast<const uint16_t*>(x_bf16), G, M, K, q, s);
     QuantRowsNvArgs a{static_cast<const uint16_t*>(x_bf16), G * M, M, K, nullptr,
                       static_cast<uint8_t*>(q->row.data), static_cast<uint8_t*>(q->row.scale), q->amax_out,
                       q->tensor_scale};

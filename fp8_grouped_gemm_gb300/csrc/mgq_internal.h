@@ -46,6 +46,10 @@ int launch_quant_rows_nv(const uint16_t* x, int64_t rows, const int32_t* rows_us
 // Row-wise + column-wise quantisation in one pass (quant_tile.cu); q->col.data
 // must be set. Per-tensor or MX scaling.
 int rowcol_plain(const uint16_t* x, int64_t G, int64_t M, int64_t K, const mgq_qdesc* q, cudaStream_t s);
+// row-wise and column-wise copies of a bf16 [rows_cap, C] matrix whose rows in
+// use are *rows_used (one group: column copy [C, rows_cap]) (quant_tile.cu)
+int rowcol_rows(const uint16_t* x, int64_t rows_cap, const int32_t* rows_used, int64_t C, const mgq_qdesc* q,
+                cudaStream_t s);
 int rowcol_swiglu(const uint16_t* gu, int64_t R_cap, int64_t F, const int32_t* rows_used, uint16_t* h_out,
                   const mgq_qdesc* q, cudaStream_t s);
 int rowcol_dswiglu(const uint16_t* dh, const uint16_t* gu, int64_t R_cap, int64_t F, const int32_t* rows_used,

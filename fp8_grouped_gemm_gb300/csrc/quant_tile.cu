@@ -159,31 +159,56 @@ struct RowColArgs {
   uint8_t* col_codes;        // [G][C][M] or null
   uint8_t* col_scales;       // MX: tiled over [G*C, M]
   const float* tensor_scale; // per group (TENSOR)
-  float* amax_out;           // per group, optional
+  float* amax_out;           // per group: TENSOR optional output; NVFP4 the pre-pass amax (input)
+  float* s_out;              // NVFP4: s_g per group (output)
   int rceil;
 };
 
 // ---- the quantisation of one tile (shared by both kernels) -----------------
 
+// One NVFP4 block of 16 values (scaled in place): scale code =
+// ue4m3(float32(amax_b / 6) * s_g); with sc its value, r = s_g / sc (0 when sc
+// is 0) and each element is e2m1(v * r). Returns the scale code.
+__device__ __forceinline__ uint32_t nv_block16(float* v, float amax_b, float s_g, uint2& codes) {
+  const float t = __fmul_rn(__fdiv_rn(amax_b, 6.0f), s_g);
+  const uint32_t code = cvt_ue4m3(t);
+  const float sc = ue4m3_value(code);
+  const float r = (sc == 0.0f) ? 0.0f : __fdiv_rn(s_g, sc);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], r);
+  codes = make_uint2(cvt_e2m1x8(v), cvt_e2m1x8(v + 8));
+  return code;
+}
+
 // one column-wise block: the 32 values of output row crow, rows rg..rg+31 of
 // its group (amax_bits: float bits of their |v| maximum, MX)
 template <int SC, int DT>
-__device__ __forceinline__ void col_block_out(const float* v, uint32_t amax_bits, float ts, const RowColArgs& a,
+__device__ __forceinline__ void col_block_out(float* v, uint32_t amax_bits, float ts, const RowColArgs& a,
                                               int64_t crow, int64_t rg) {
-  float mult = ts;
-  if (SC == MGQ_MX32_E8M0) {
-    const int e = mx_exponent(amax_bits, FmtInfo<DT>::emax, a.rceil != 0);
-    mult = mx_multiplier(e);
-    a.col_scales[tiled_scale_offset(crow, rg / 32, a.M / 128)] = (uint8_t)mx_scale_code(e);
-  }
-  uint32_t cw[8];
+  if constexpr (SC == MGQ_NV16_UE4M3) {
+    // two 16-row blocks, e2m1 packed along the rows; ts is s_g
+    uint2 c0, c1;
+    const uint32_t s0 = nv_block16(v, __uint_as_float(absmax_bits_f32(v, 16)), ts, c0);
+    const uint32_t s1 = nv_block16(v + 16, __uint_as_float(absmax_bits_f32(v + 16, 16)), ts, c1);
+    *reinterpret_cast<uint4*>(a.col_codes + crow * (a.M / 2) + rg / 2) = make_uint4(c0.x, c0.y, c1.x, c1.y);
+    *reinterpret_cast<uint16_t*>(a.col_scales + tiled_scale_offset(crow, rg / 16, a.M / 64)) =
+        (uint16_t)(s0 | (s1 << 8));
+  } else {
+    float mult = ts;
+    if constexpr (SC == MGQ_MX32_E8M0) {
+      const int e = mx_exponent(amax_bits, FmtInfo<DT>::emax, a.rceil != 0);
+      mult = mx_multiplier(e);
+      a.col_scales[tiled_scale_offset(crow, rg / 32, a.M / 128)] = (uint8_t)mx_scale_code(e);
+    }
+    uint32_t cw[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-    cw[i] = cvt_fp8x4<DT>(__fmul_rn(v[4 * i], mult), __fmul_rn(v[4 * i + 1], mult), __fmul_rn(v[4 * i + 2], mult),
-                          __fmul_rn(v[4 * i + 3], mult));
-  uint4* dst = reinterpret_cast<uint4*>(a.col_codes + crow * a.M + rg);
-  dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-  dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+    for (int i = 0; i < 8; ++i)
+      cw[i] = cvt_fp8x4<DT>(__fmul_rn(v[4 * i], mult), __fmul_rn(v[4 * i + 1], mult), __fmul_rn(v[4 * i + 2], mult),
+                            __fmul_rn(v[4 * i + 3], mult));
+    uint4* dst = reinterpret_cast<uint4*>(a.col_codes + crow * a.M + rg);
+    dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+    dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+  }
 }
 
 // Row-wise codes of a bf16 tile [P][TR][LD]: the P*TR (part, row) pairs, 8 per
@@ -208,8 +233,31 @@ __device__ __forceinline__ void row_phase(const uint16_t* tile, int64_t r0, int6
       const uint4 w = src[q ^ sw];
       ww[4 * q] = w.x; ww[4 * q + 1] = w.y; ww[4 * q + 2] = w.z; ww[4 * q + 3] = w.w;
     }
+    if constexpr (SC == MGQ_NV16_UE4M3) {
+      // two 16-column blocks: ww[0..7] hold block sw / 2 of the lane's 32
+      // columns, ww[8..15] the other; ts is s_g
+      uint32_t sc2 = 0;
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        uint32_t acc = 0;
+        float y[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          acc = absmax_acc_bf16x2(acc, ww[8 * hb + i]);
+          y[2 * i] = bf16_lo(ww[8 * hb + i]);
+          y[2 * i + 1] = bf16_hi(ww[8 * hb + i]);
+        }
+        uint2 c;
+        const uint32_t code = nv_block16(y, __uint_as_float(fold_bf16x2(absmax_bf16x2_final(acc))), ts, c);
+        const int blk = (sw >> 1) ^ hb;
+        if (r < nrows) *reinterpret_cast<uint2*>(a.row_codes + r * (a.C / 2) + (cb + 16 * blk) / 2) = c;
+        sc2 |= code << (8 * blk);
+      }
+      if (r < nrows)
+        *reinterpret_cast<uint16_t*>(a.row_scales + tiled_scale_offset(r, cb / 16, a.C / 64)) = (uint16_t)sc2;
+    } else {
     float mult = ts;
-    if (SC == MGQ_MX32_E8M0) {
+    if constexpr (SC == MGQ_MX32_E8M0) {
       uint32_t acc = 0;
 #pragma unroll
       for (int i = 0; i < 16; ++i) acc = absmax_acc_bf16x2(acc, ww[i]);
@@ -226,6 +274,7 @@ __device__ __forceinline__ void row_phase(const uint16_t* tile, int64_t r0, int6
       uint8_t* dst = a.row_codes + r * a.C + cb;
       *reinterpret_cast<uint4*>(dst + 8 * sw) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
       *reinterpret_cast<uint4*>(dst + (16 - 8 * sw)) = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+    }
     }
   }
 }
@@ -260,7 +309,7 @@ __device__ __forceinline__ void col_phase(const uint16_t* tile, const float* fac
 #pragma unroll
       for (int i = 0; i < 32; ++i) w[i] = *reinterpret_cast<const uint32_t*>(&tile[(p * TR + 32 * rb + i) * LD + cc]);
       uint32_t amh[2] = {0, 0};
-      if (SC == MGQ_MX32_E8M0 || a.amax_out) {
+      if (SC == MGQ_MX32_E8M0 || (SC == MGQ_TENSOR_F32 && a.amax_out)) {
         uint32_t acc = 0;
 #pragma unroll
         for (int i = 0; i < 32; ++i) acc = absmax_acc_bf16x2(acc, w[i]);
@@ -278,6 +327,15 @@ __device__ __forceinline__ void col_phase(const uint16_t* tile, const float* fac
       }
     }
   }
+}
+
+// the scale a tile's codes are made with: per-tensor s of the group, NVFP4 s_g
+// of the group from its amax (pre-pass), else unused
+template <int SC>
+__device__ __forceinline__ float tile_scale(const RowColArgs& a, int64_t g) {
+  if (SC == MGQ_TENSOR_F32) return a.tensor_scale[g];
+  if (SC == MGQ_NV16_UE4M3) return nv_global_scale(a.amax_out[g]);
+  return 1.0f;
 }
 
 // per-tensor amax of group g: CTA reduction, one atomic
@@ -310,7 +368,8 @@ __global__ void __launch_bounds__(256, Src::kParts == 2 ? 3 : 4)
   for (int rt = blockIdx.y; rt < n_rt; rt += gridDim.y) {
     const int64_t r0 = (int64_t)rt * TR;
     const int64_t g = (int)r0 / (int)a.M;
-    const float ts = (SC == MGQ_TENSOR_F32) ? a.tensor_scale[g] : 1.0f;
+    const float ts = tile_scale<SC>(a, g);
+    if (SC == MGQ_NV16_UE4M3 && blockIdx.x == 0 && r0 == g * a.M && tid == 0) a.s_out[g] = ts;
     // ---- load: TR rows x 16 chunks of 8 columns, 8 chunks per thread
     uint32_t am2 = 0;
     if constexpr (!Src::kComputed) {
@@ -429,7 +488,7 @@ __global__ void __launch_bounds__(256, 3) quant_rowcol_stream_kernel(const Src s
   __syncthreads();
   issue(rt, ct, 0);
   int64_t g = (int)((int64_t)rt * TR) / (int)a.M;
-  float ts = (SC == MGQ_TENSOR_F32) ? a.tensor_scale[g] : 1.0f;
+  float ts = tile_scale<SC>(a, g);
   uint32_t am = 0;
 #pragma unroll 1
   for (int64_t item = i0; item < i1; ++item) {
@@ -452,6 +511,7 @@ __global__ void __launch_bounds__(256, 3) quant_rowcol_stream_kernel(const Src s
     __syncthreads();
     const int64_t r0 = (int64_t)rt * TR, c0 = (int64_t)ct * TC;
     const uint16_t* t = tiles + buf * TR * LD;
+    if (SC == MGQ_NV16_UE4M3 && ct == 0 && r0 == g * a.M && tid == 0) a.s_out[g] = ts;
     if (!Src::kColumnsOnly && a.row_codes) row_phase<1, SC, DT>(t, r0, nrows, c0, ts, a, warp, lane);
     col_phase<1, SC, DT, Src::kFactor>(t, s_fac[rt & 1], g, r0, c0, ts, a, tid, am);
     __syncthreads();   // the buffer is refilled two items on
@@ -459,7 +519,7 @@ __global__ void __launch_bounds__(256, 3) quant_rowcol_stream_kernel(const Src s
       if (SC == MGQ_TENSOR_F32 && a.amax_out) flush_amax(am, a.amax_out, g, s_amax, tid);
       am = 0;
       g = (int)((int64_t)rt_n * TR) / (int)a.M;
-      if (SC == MGQ_TENSOR_F32 && item + 1 < i1) ts = a.tensor_scale[g];
+      if (item + 1 < i1) ts = tile_scale<SC>(a, g);
     }
     rt = rt_n;
     ct = ct_n;
@@ -506,6 +566,16 @@ int launch_rowcol(const Src& src, const mgq_qdesc* q, RowColArgs a, cudaStream_t
   if (a.rows_cap >= (1ll << 31) || a.M >= (1ll << 31)) return MGQ_ERR_UNSUPPORTED;
   if (Src::kStream && !a.col_codes) return MGQ_ERR_UNSUPPORTED;   // a row + column pass
   const int sc = q->scaling, dt = q->dtype;
+  // NVFP4 (s_g from the amax pre-pass in amax_out): streamed and plain sources
+  constexpr bool kComputedSrc = std::is_same<Src, SrcSwiglu>::value || std::is_same<Src, SrcDswiglu>::value;
+  if (sc == MGQ_NV16_UE4M3) {
+    if constexpr (kComputedSrc) {
+      return MGQ_ERR_UNSUPPORTED;
+    } else {
+      if (dt != MGQ_E2M1 || !a.amax_out || !a.s_out) return MGQ_ERR_INVALID_ARG;
+      return launch_rowcol_t<Src, MGQ_NV16_UE4M3, MGQ_E2M1>(src, a, s);
+    }
+  }
   if (sc == MGQ_MX32_E8M0 && dt == MGQ_E4M3) return launch_rowcol_t<Src, MGQ_MX32_E8M0, MGQ_E4M3>(src, a, s);
   if (sc == MGQ_MX32_E8M0 && dt == MGQ_E5M2) return launch_rowcol_t<Src, MGQ_MX32_E8M0, MGQ_E5M2>(src, a, s);
   // per-tensor column copies of gathered rows are transposed casts of the row codes
@@ -532,6 +602,7 @@ RowColArgs make_args(const mgq_qdesc* q, int64_t rows_cap, const int32_t* rows_u
   a.col_scales = static_cast<uint8_t*>(q->col.scale);
   a.tensor_scale = q->tensor_scale;
   a.amax_out = q->amax_out;
+  a.s_out = q->tensor_scale;
   a.rceil = q->e8m0_mode == MGQ_E8M0_RCEIL;
   return a;
 }
@@ -637,6 +708,11 @@ __global__ void __launch_bounds__(256) quant_nv2d_kernel(const uint16_t* x, int6
 
 int rowcol_plain(const uint16_t* x, int64_t G, int64_t M, int64_t K, const mgq_qdesc* q, cudaStream_t s) {
   return launch_rowcol(SrcPlain{x, K}, q, make_args(q, G * M, nullptr, K, M), s);
+}
+
+int rowcol_rows(const uint16_t* x, int64_t rows_cap, const int32_t* rows_used, int64_t C, const mgq_qdesc* q,
+                cudaStream_t s) {
+  return launch_rowcol(SrcPlain{x, C}, q, make_args(q, rows_cap, rows_used, C, rows_cap), s);
 }
 
 int rowcol_swiglu(const uint16_t* gu, int64_t R_cap, int64_t F, const int32_t* rows_used, uint16_t* h_out,

@@ -459,7 +459,8 @@ int check_permute_q(const mgq_qdesc* q, int align) {
   MGQ_CHECK_ARG(q->row.data && aligned16(q->row.data));
   if (q->scaling == MGQ_NV16_UE4M3) {
     MGQ_CHECK_ARG(q->dtype == MGQ_E2M1 && q->row.scale && aligned16(q->row.scale) && q->amax_out &&
-                  q->tensor_scale && !q->col.data);
+                  q->tensor_scale);
+    if (q->col.data) MGQ_CHECK_ARG(aligned16(q->col.data) && q->col.scale && aligned16(q->col.scale) && align % 32 == 0);
     return MGQ_OK;
   }
   MGQ_CHECK_ARG(q->dtype == MGQ_E4M3 || q->dtype == MGQ_E5M2);
@@ -511,7 +512,7 @@ int route_impl(const int32_t* topk_idx, int T, int k, int E, int align, int32_t*
 // MX with a column-wise copy and no bf16 copy: one tile pass over the
 // permuted rows writes both copies (needs the final src_row)
 bool permute_fused_rowcol(const mgq_qdesc* q, const void* out_bf16) {
-  return q->scaling == MGQ_MX32_E8M0 && q->col.data && !out_bf16;
+  return (q->scaling == MGQ_MX32_E8M0 || q->scaling == MGQ_NV16_UE4M3) && q->col.data && !out_bf16;
 }
 
 // permute + quantise of the token rows to their routed rows (row_id_map final,
@@ -519,8 +520,13 @@ bool permute_fused_rowcol(const mgq_qdesc* q, const void* out_bf16) {
 int permute_impl(const void* x_bf16, int T, int H, int k, int E, const mgq_qdesc* q, void* out_bf16, int64_t R_cap,
                  int32_t* row_id_map, int32_t* src_row, const int32_t* offsets, const int32_t* counts,
                  const int32_t* idx, const int32_t* cnt, bool resolve, int* err, cudaStream_t s) {
-  if (!resolve && permute_fused_rowcol(q, out_bf16))
+  if (!resolve && permute_fused_rowcol(q, out_bf16)) {
+    if (q->scaling == MGQ_NV16_UE4M3) {   // s_g needs the amax of X first
+      const int rc = launch_amax_groups(static_cast<const uint16_t*>(x_bf16), (int64_t)T * H, 1, q->amax_out, s);
+      if (rc != MGQ_OK) return rc;
+    }
     return gather_x_rowcol(static_cast<const uint16_t*>(x_bf16), src_row, k, H, R_cap, offsets + E, true, q, s);
+  }
   PermuteArgs a;
   a.x = static_cast<const uint16_t*>(x_bf16);
   a.T = T; a.H = H; a.k = k; a.E = E;
@@ -548,6 +554,8 @@ int permute_impl(const void* x_bf16, int T, int H, int k, int E, const mgq_qdesc
     if (rc != MGQ_OK) return rc;
     permute_quant_nv_kernel<<<grid, 256, 0, s>>>(a);
     MGQ_LAUNCH_CHECK();
+    // column-wise copy (16-row blocks along the permuted rows) from the gathered rows
+    if (q->col.data) return gather_x_rowcol(a.x, src_row, k, H, R_cap, offsets + E, false, q, s);
     return MGQ_OK;
   }
 #define MGQ_PERMUTE_LAUNCH(SC, DT) permute_quant_kernel<SC, DT><<<grid, 256, 0, s>>>(a)

@@ -54,7 +54,7 @@ PERMUTE_CASES = [
 
 @pytest.mark.parametrize("case", PERMUTE_CASES, ids=lambda c: f"T{c[0]}E{c[1]}k{c[2]}H{c[3]}a{c[4]}")
 @pytest.mark.parametrize("mode", ["mx_e4m3", "mx_e5m2", "mx_col_e4m3", "mx_col_e5m2", "tensor_e4m3", "blk_e4m3",
-                                  "nvfp4"])
+                                  "nvfp4", "nvfp4_col"])
 def test_permute_quantize(mgq, case, mode):
     T, E, k, H, align, empty = case
     rng = np.random.default_rng(T * 7 + E)
@@ -70,15 +70,21 @@ def test_permute_quantize(mgq, case, mode):
     off = torch.empty(E + 1, dtype=torch.int32, device=dev)
     cnt = torch.empty(E, dtype=torch.int32, device=dev)
     ws = torch.empty(mgq.permute_workspace_size(T, k, E), dtype=torch.uint8, device=dev)
-    codes = torch.full((R, H // 2 if mode == "nvfp4" else H), 0xAB, dtype=torch.uint8, device=dev)
+    nv = mode.startswith("nvfp4")
+    codes = torch.full((R, H // 2 if nv else H), 0xAB, dtype=torch.uint8, device=dev)
     fmt = "e5m2" if "e5m2" in mode else "e4m3"
     dt = mgq.E5M2 if fmt == "e5m2" else mgq.E4M3
     xf = bf16_np(x)
-    if mode == "nvfp4":
+    if nv:
         sc = torch.full((mgq.nv_scale_bytes(R, H),), 0xCD, dtype=torch.uint8, device=dev)
         amax = torch.full((1,), 7.0, dtype=torch.float32, device=dev)     # overwritten by the call
         sg = torch.zeros(1, dtype=torch.float32, device=dev)
-        q = mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, codes, sc, tensor_scale=sg, amax_out=amax)
+        col = csc = None
+        if mode == "nvfp4_col":
+            # column-wise copy: 16-row blocks along the permuted rows, packed along them
+            col = torch.full((H, R // 2), 0xAB, dtype=torch.uint8, device=dev)
+            csc = torch.full((mgq.nv_scale_bytes(H, R),), 0xCD, dtype=torch.uint8, device=dev)
+        q = mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, codes, sc, col, csc, tensor_scale=sg, amax_out=amax)
     elif mode.startswith("mx_col"):
         # row-wise and column-wise (blocks of 32 along the permuted rows) copies
         sc = torch.full((mgq.mx_scale_bytes(R, H),), 0xCD, dtype=torch.uint8, device=dev)
@@ -105,13 +111,18 @@ def test_permute_quantize(mgq, case, mode):
     assert np.array_equal(cnt.cpu().numpy(), w_cnt)
     assert np.array_equal(rim.cpu().numpy(), w_rim)
     assert np.array_equal(src.cpu().numpy()[:Rp], w_src)
-    if mode == "nvfp4":
+    if nv:
         am = float(np.max(np.abs(xf)))
         s_g = OQ.nvfp4_global_scale(am)
         assert float(amax.item()) == am and float(sg.item()) == float(s_g)
         c, s = OQ.quantize_nvfp4(xf, s_g)
         assert np.array_equal(u8_np(codes)[:Rp], OR.permute_rows(c, w_rim, Rp))
         assert np.array_equal(untile_mx_scales(u8_np(sc), R, H, 16)[:Rp], OR.permute_rows(s, w_rim, Rp))
+        if mode == "nvfp4_col":
+            xp = OR.permute_rows(xf, w_rim, Rp, fill=0.0)
+            cc, cs = OQ.quantize_nvfp4(xp.T, s_g)
+            assert np.array_equal(u8_np(col)[:, :Rp // 2], cc)
+            assert np.array_equal(untile_mx_scales(u8_np(csc), H, R, 16)[:, :Rp // 16], cs)
     elif mode.startswith("mx"):
         c, s = OQ.quantize_mx(xf, fmt)
         assert np.array_equal(u8_np(codes)[:Rp], OR.permute_rows(c, w_rim, Rp))
@@ -648,7 +659,7 @@ def _layout(rng, T, E, k, dev, align=128):
     return idx, rim, src, off, cnt
 
 
-@pytest.mark.parametrize("mode", ["mx", "tensor", "mx_col"])
+@pytest.mark.parametrize("mode", ["mx", "tensor", "mx_col", "nvfp4_col"])
 @pytest.mark.parametrize("F", [512, 768, 1536])
 def test_swiglu_quantize(mgq, mode, F):
     rng = np.random.default_rng(F)
@@ -658,9 +669,15 @@ def test_swiglu_quantize(mgq, mode, F):
     gu = _bf16(rng, (R, 2 * F), 2.0)
     gu[off[-1]:] = 0
     offd = torch.from_numpy(off).to(dev)
-    codes = torch.empty(R, F, dtype=torch.uint8, device=dev)
+    codes = torch.empty(R, F // 2 if mode.startswith("nvfp4") else F, dtype=torch.uint8, device=dev)
     h = torch.empty(R, F, dtype=torch.bfloat16, device=dev)
-    if mode == "mx":
+    if mode == "nvfp4_col":
+        sc = torch.empty(mgq.nv_scale_bytes(R, F), dtype=torch.uint8, device=dev)
+        col = torch.full((F, R // 2), 0xAB, dtype=torch.uint8, device=dev)
+        csc = torch.full((mgq.nv_scale_bytes(F, R),), 0xCD, dtype=torch.uint8, device=dev)
+        amax, sg = torch.full((1,), 7.0, device=dev), torch.zeros(1, device=dev)
+        q = mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, codes, sc, col, csc, tensor_scale=sg, amax_out=amax)
+    elif mode == "mx":
         sc = torch.empty(mgq.mx_scale_bytes(R, F), dtype=torch.uint8, device=dev)
         q = mgq.qdesc(mgq.E4M3, mgq.MX32_E8M0, codes, sc)
     elif mode == "mx_col":
@@ -678,7 +695,17 @@ def test_swiglu_quantize(mgq, mode, F):
     n = int(off[-1])
     hg = bf16_np(h)[:n]
     check_elementwise(OL.swiglu(bf16_np(gu)[:n], F), hg, "swiglu")
-    if mode in ("mx", "mx_col"):
+    if mode == "nvfp4_col":
+        am = float(np.max(np.abs(hg)))
+        s_g = OQ.nvfp4_global_scale(am)
+        assert float(amax.item()) == am and float(sg.item()) == float(s_g)
+        c, s_ = OQ.quantize_nvfp4(hg, s_g)
+        assert np.array_equal(u8_np(codes)[:n], c)
+        assert np.array_equal(untile_mx_scales(u8_np(sc), R, F, 16)[:n], s_)
+        cc, cs = OQ.quantize_nvfp4(hg.T, s_g)
+        assert np.array_equal(u8_np(col)[:, :n // 2], cc)
+        assert np.array_equal(untile_mx_scales(u8_np(csc), F, R, 16)[:, :n // 16], cs)
+    elif mode in ("mx", "mx_col"):
         c, s_ = OQ.quantize_mx(hg)
         assert np.array_equal(u8_np(codes)[:n], c)
         assert np.array_equal(untile_mx_scales(u8_np(sc), R, F)[:n], s_)
@@ -694,7 +721,7 @@ def test_swiglu_quantize(mgq, mode, F):
         assert float(amax.item()) == am
 
 
-@pytest.mark.parametrize("mode", ["tensor", "mx_col"])
+@pytest.mark.parametrize("mode", ["tensor", "mx_col", "nvfp4", "nvfp4_col"])
 def test_dswiglu_quantize(mgq, mode):
     rng = np.random.default_rng(5)
     dev = torch.device(DEV)
@@ -702,12 +729,19 @@ def test_dswiglu_quantize(mgq, mode):
     off = np.array([0, 256, 384], dtype=np.int32)
     gu = _bf16(rng, (R, 2 * F), 2.0)
     dh = _bf16(rng, (R, F), 1e-3)
-    codes = torch.empty(R, 2 * F, dtype=torch.uint8, device=dev)
-    col = torch.empty(2 * F, R, dtype=torch.uint8, device=dev)
+    nv = mode.startswith("nvfp4")
+    codes = torch.empty(R, F if nv else 2 * F, dtype=torch.uint8, device=dev)
+    col = torch.empty(2 * F, R // 2 if nv else R, dtype=torch.uint8, device=dev)
     dgu = torch.empty(R, 2 * F, dtype=torch.bfloat16, device=dev)
     s = torch.tensor([20000.0], device=dev)
     amax = torch.zeros(1, device=dev)
-    if mode == "tensor":
+    if nv:
+        sc = torch.empty(mgq.nv_scale_bytes(R, 2 * F), dtype=torch.uint8, device=dev)
+        csc = torch.empty(mgq.nv_scale_bytes(2 * F, R), dtype=torch.uint8, device=dev)
+        sg = torch.zeros(1, device=dev)
+        q = mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, codes, sc, col if mode == "nvfp4_col" else None,
+                      csc if mode == "nvfp4_col" else None, tensor_scale=sg, amax_out=amax)
+    elif mode == "tensor":
         q = mgq.qdesc(mgq.E5M2, mgq.TENSOR_F32, codes, None, col, None, s, amax)
     else:
         sc = torch.empty(mgq.mx_scale_bytes(R, 2 * F), dtype=torch.uint8, device=dev)
@@ -717,7 +751,20 @@ def test_dswiglu_quantize(mgq, mode):
     torch.cuda.synchronize()
     g = bf16_np(dgu)
     check_elementwise(OL.dswiglu(bf16_np(dh), bf16_np(gu), F), g, "dswiglu")
-    if mode == "tensor":
+    if nv:
+        n = int(off[-1])
+        gn = g[:n]
+        am = float(np.max(np.abs(gn)))
+        s_g = OQ.nvfp4_global_scale(am)
+        assert float(amax.item()) == am and float(sg.item()) == float(s_g)
+        c, s_ = OQ.quantize_nvfp4(gn, s_g)
+        assert np.array_equal(u8_np(codes)[:n], c)
+        assert np.array_equal(untile_mx_scales(u8_np(sc), R, 2 * F, 16)[:n], s_)
+        if mode == "nvfp4_col":
+            cc, cs = OQ.quantize_nvfp4(gn.T, s_g)
+            assert np.array_equal(u8_np(col)[:, :n // 2], cc)
+            assert np.array_equal(untile_mx_scales(u8_np(csc), 2 * F, R, 16)[:, :n // 16], cs)
+    elif mode == "tensor":
         c, am = OQ.quantize_tensor(g, np.float32(20000.0), "e5m2")
         assert np.array_equal(u8_np(codes), c)
         assert np.array_equal(u8_np(col), c.T)
@@ -749,7 +796,7 @@ def test_unpermute_and_permute_bwd(mgq, T, E, k, H):
     check_elementwise(OR.permute_bwd(bf16_np(y), rim), bf16_np(dx), "permute_bwd")
 
 
-@pytest.mark.parametrize("mode", ["tensor", "mx", "mx_col"])
+@pytest.mark.parametrize("mode", ["tensor", "mx", "mx_col", "nvfp4", "nvfp4_col"])
 def test_unpermute_bwd_quantize(mgq, mode):
     rng = np.random.default_rng(9)
     dev = torch.device(DEV)
@@ -760,9 +807,19 @@ def test_unpermute_bwd_quantize(mgq, mode):
     dout = _bf16(rng, (T, H), 1e-3)
     y = _bf16(rng, (R, H))
     probs = rng.random((T, k)).astype(np.float32)
-    codes = torch.full((R, H), 0xAB, dtype=torch.uint8, device=dev)
+    nv = mode.startswith("nvfp4")
+    codes = torch.full((R, H // 2 if nv else H), 0xAB, dtype=torch.uint8, device=dev)
     dprobs = torch.empty(T, k, dtype=torch.float32, device=dev)
-    if mode == "tensor":
+    if nv:
+        sc = torch.full((mgq.nv_scale_bytes(R, H),), 0xCD, dtype=torch.uint8, device=dev)
+        amax = torch.full((1,), 7.0, device=dev)
+        sg = torch.zeros(1, device=dev)
+        col = csc = None
+        if mode == "nvfp4_col":
+            col = torch.full((H, R // 2), 0xAB, dtype=torch.uint8, device=dev)
+            csc = torch.full((mgq.nv_scale_bytes(H, R),), 0xCD, dtype=torch.uint8, device=dev)
+        q = mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, codes, sc, col, csc, tensor_scale=sg, amax_out=amax)
+    elif mode == "tensor":
         col = torch.empty(H, R, dtype=torch.uint8, device=dev)
         s = torch.tensor([30000.0], device=dev)
         amax = torch.zeros(1, device=dev)
@@ -780,7 +837,18 @@ def test_unpermute_bwd_quantize(mgq, mode):
     torch.cuda.synchronize()
     dy32, dp = OR.unpermute_bwd(bf16_np(dout), bf16_np(y), rim, probs, Rp)
     assert rel_fro(dp, dprobs.cpu().numpy()) <= 1e-5
-    if mode == "tensor":
+    if nv:
+        am = float(np.max(np.abs(dy32)))
+        s_g = OQ.nvfp4_global_scale(am)
+        assert float(amax.item()) == am and float(sg.item()) == float(s_g)
+        c, s_ = OQ.quantize_nvfp4(dy32.astype(np.float64), s_g)
+        assert np.array_equal(u8_np(codes)[:Rp], c)
+        assert np.array_equal(untile_mx_scales(u8_np(sc), R, H, 16)[:Rp], s_)
+        if mode == "nvfp4_col":
+            cc, cs = OQ.quantize_nvfp4(dy32.astype(np.float64).T, s_g)
+            assert np.array_equal(u8_np(col)[:, :Rp // 2], cc)
+            assert np.array_equal(untile_mx_scales(u8_np(csc), H, R, 16)[:, :Rp // 16], cs)
+    elif mode == "tensor":
         c, am = OQ.quantize_tensor(dy32.astype(np.float64), np.float32(30000.0), "e5m2")
         assert np.array_equal(u8_np(codes)[:Rp], c)
         assert np.array_equal(u8_np(col)[:, :Rp], c.T)
@@ -835,7 +903,7 @@ def test_block_quantize_mx_special_values(mgq, fmt, e8m0):
     assert s_[0, 0] == 255 and s_[40, 0] == 255                 # the NaN and inf blocks
 
 
-@pytest.mark.parametrize("mode", ["mx", "tensor", "blk128", "nvfp4", "mx_col"])
+@pytest.mark.parametrize("mode", ["mx", "tensor", "blk128", "nvfp4", "mx_col", "nvfp4_col"])
 def test_block_quantize_weights(mgq, mode):
     rng = np.random.default_rng(13)
     dev = torch.device(DEV)
@@ -858,6 +926,32 @@ def test_block_quantize_weights(mgq, mode):
         cs_all = untile_mx_scales(u8_np(csc), G * K, M).reshape(G, K, M // 32)
         for g in range(G):
             cc, cs = OQ.quantize_mx(wf[g].T)
+            assert np.array_equal(u8_np(col)[g], cc)
+            assert np.array_equal(cs_all[g], cs)
+        return
+    if mode == "nvfp4_col":
+        # 1x16 blocks along K (rows) and along each group's M rows (columns)
+        w[2, 100, 9] = -0.75
+        wf = bf16_np(w)
+        cnv = torch.empty(G, M, K // 2, dtype=torch.uint8, device=dev)
+        sc = torch.empty(mgq.nv_scale_bytes(G * M, K), dtype=torch.uint8, device=dev)
+        col = torch.full((G, K, M // 2), 0xAB, dtype=torch.uint8, device=dev)
+        csc = torch.full((mgq.nv_scale_bytes(G * K, M),), 0xCD, dtype=torch.uint8, device=dev)
+        amax = torch.empty(G, dtype=torch.float32, device=dev)
+        sg = torch.empty(G, dtype=torch.float32, device=dev)
+        mgq.block_quantize(w.to(dev), mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, cnv, sc, col, csc, tensor_scale=sg,
+                                                amax_out=amax))
+        torch.cuda.synchronize()
+        s_all = untile_mx_scales(u8_np(sc), G * M, K, 16).reshape(G, M, K // 16)
+        cs_all = untile_mx_scales(u8_np(csc), G * K, M, 16).reshape(G, K, M // 16)
+        for g in range(G):
+            am = float(np.max(np.abs(wf[g])))
+            s_g = OQ.nvfp4_global_scale(am)
+            assert float(amax[g].item()) == am and float(sg[g].item()) == float(s_g)
+            c, s_ = OQ.quantize_nvfp4(wf[g], s_g)
+            assert np.array_equal(u8_np(cnv)[g], c)
+            assert np.array_equal(s_all[g], s_)
+            cc, cs = OQ.quantize_nvfp4(wf[g].T, s_g)
             assert np.array_equal(u8_np(col)[g], cc)
             assert np.array_equal(cs_all[g], cs)
         return
