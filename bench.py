@@ -164,14 +164,22 @@ def algorithmic_bytes(w, R_pad, cols):
 
 def algorithmic_bytes_nvfp4(w):
     """NVFP4: codes are 0.5 byte per element plus one scale byte per 16; the
-    tensor amax passes re-read their input once."""
+    tensor amax passes re-read their input once, and the two-pass casts
+    (SwiGLU, dSwiGLU) write their bf16 result and read it back. Training adds
+    the column-wise copies."""
     T, k, H, F, E = w.T, w.k, w.H, w.F, w.E
     R = T * k
     q = 0.5 + 1.0 / 16
-    return {"permute_quant": T * H * 2 * 2 + R * H * q,
-            "swiglu_quant": R * 2 * F * 2 + R * F * 2 * 2 + R * F * q,
-            "unpermute": R * H * 2 + T * H * 2,
-            "weight_quant": E * 3 * F * H * 2 * 2 + E * 3 * F * H * q}
+    c = 1 if w.backward else 0
+    b = {"permute_quant": T * H * 2 * 2 + (1 + c) * R * H * q,
+         "swiglu_quant": R * 2 * F * 2 + R * F * 2 * 2 + (1 + c) * R * F * q,
+         "unpermute": R * H * 2 + T * H * 2,
+         "weight_quant": E * 3 * F * H * 2 * 2 + (1 + c) * E * 3 * F * H * q}
+    if w.backward:
+        b["unpermute_bwd_quant"] = T * H * 2 * 2 + R * H * 2 + (1 + c) * R * H * q
+        b["dswiglu_quant"] = R * F * 2 + R * 2 * F * 2 + R * 2 * F * 2 * 2 + (1 + c) * R * 2 * F * q
+        b["permute_bwd"] = R * H * 2 + T * H * 2
+    return b
 
 
 def algorithmic_bytes_fp8(w, R_pad, cols):
@@ -224,7 +232,14 @@ def oracle_sample(w, rows=512, f_slice=1024):
     rim, src, o2, cnt = OR.permute_indices(idx, 1, 128)
     s = np.float32(1.0)
 
+    def q_nv(a):
+        s_g = OQ.nvfp4_global_scale(float(np.max(np.abs(a))))
+        c, sc = OQ.quantize_nvfp4(a, s_g)
+        return OQ.dequantize_nvfp4(c, sc, s_g, a.shape[1])
+
     def q_act(a):
+        if w.recipe == "nvfp4":
+            return q_nv(a)
         if w.recipe == "mxfp8":
             c, sc = OQ.quantize_mx(a)
             return OQ.dequantize_mx(c, sc)
@@ -238,6 +253,10 @@ def oracle_sample(w, rows=512, f_slice=1024):
         if w.recipe == "blockwise":
             c, sc = OQ.quantize_block_128x128(b)
             return OQ.dequantize_block_128x128(c, sc)
+        if w.recipe == "nvfp4" and w.backward:        # 16x16 weight blocks
+            s_g = OQ.nvfp4_global_scale(float(np.max(np.abs(b))))
+            rc, rs, _, _ = OQ.quantize_nvfp4_2d(b, s_g)
+            return OQ.dequantize_nvfp4(rc, rs, s_g, b.shape[1])
         return q_act(b)
 
     xd, w1d, w2d = q_act(x), q_w(w1[0])[None], q_w(w2[0])[None]
@@ -249,6 +268,8 @@ def oracle_sample(w, rows=512, f_slice=1024):
     flops = 2.0 * rows * H * 2 * Fs + 2.0 * rows * Fs * H
     if w.backward:
         def q_grad(a):
+            if w.recipe == "nvfp4":          # row-wise copy for dgrad, column-wise for wgrad
+                return q_nv(a), q_nv(np.ascontiguousarray(a.T)).T
             if w.recipe == "mxfp8":          # row-wise copy for dgrad, column-wise for wgrad
                 c, sc = OQ.quantize_mx(a, "e5m2")
                 ct, st = OQ.quantize_mx(a.T, "e5m2")
@@ -353,6 +374,9 @@ DTYPE = {"mxfp8": "e4m3 fwd / e5m2 grads (MXFP8: E8M0 per 32, f32 accumulate)", 
 def dtype_of(w):
     if w.recipe == "mxfp8" and not w.backward:
         return "e4m3 (MXFP8: E8M0 per 32, f32 accumulate)"
+    if w.recipe == "nvfp4" and w.backward:
+        return ("e2m1 fwd and grads (NVFP4: 16-element ue4m3 scales + float32 global scale, weights in 16x16 "
+                "blocks, f32 accumulate)")
     return DTYPE[w.recipe]
 
 

@@ -1323,11 +1323,13 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
     const int64_t F = N / 2;
     if (mode != kModeRows || kind == kKindBlock || b_mn) return MGQ_ERR_UNSUPPORTED;
     MGQ_CHECK_ARG(qh && qh->row.data && aligned16(qh->row.data) && N % 256 == 0 && aligned16(sw->h_bf16));
-    if (qh->scaling != scaling || qh->col.data) return MGQ_ERR_UNSUPPORTED;
+    // a column-wise copy of h only with NVFP4 (written by the second pass)
+    if (qh->scaling != scaling || (qh->col.data && !nv)) return MGQ_ERR_UNSUPPORTED;
     if (nv) {
       // h in bf16 and its amax from the epilogue, then the NVFP4 cast
       if (qh->dtype != MGQ_E2M1) return MGQ_ERR_UNSUPPORTED;
       MGQ_CHECK_ARG(qh->row.scale && aligned16(qh->row.scale) && qh->amax_out && qh->tensor_scale && sw->h_bf16);
+      if (qh->col.data) MGQ_CHECK_ARG(aligned16(qh->col.data) && qh->col.scale && aligned16(qh->col.scale));
     } else {
       if (qh->dtype != MGQ_E4M3 && qh->dtype != MGQ_E5M2) return MGQ_ERR_UNSUPPORTED;
       if (mx) MGQ_CHECK_ARG(qh->row.scale && aligned16(qh->row.scale));
@@ -1442,6 +1444,8 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
       if (sw && cudaMemsetAsync(sw->qh->amax_out, 0, sizeof(float), s) != cudaSuccess) return MGQ_ERR_CUDA;
       rc = launch_gemm<kModeRows, kKindNV>(ta, tb, to, th, p, s);
       if (rc != MGQ_OK || !sw) return rc;
+      if (sw->qh->col.data)   // row-wise and column-wise copies in one tile pass
+        return rowcol_rows(static_cast<const uint16_t*>(sw->h_bf16), R_cap, offsets + E, N / 2, sw->qh, s);
       return launch_quant_rows_nv(static_cast<const uint16_t*>(sw->h_bf16), R_cap, offsets + E, N / 2,
                                   static_cast<uint8_t*>(sw->qh->row.data), static_cast<uint8_t*>(sw->qh->row.scale),
                                   sw->qh->amax_out, sw->qh->tensor_scale, s);

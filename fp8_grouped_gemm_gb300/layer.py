@@ -34,6 +34,7 @@ from . import mgq
 from .workloads import Workload
 
 ALIGN = 128       # group padding: the grouped GEMM tiles rows by 128
+ALIGN_NV_TRAIN = 256   # NVFP4 wgrad: a 128-byte stage holds 256 rows of a group
 
 
 class ExpertLayer:
@@ -54,14 +55,19 @@ class ExpertLayer:
         # epilogue writes h and its amax, cast by a second pass), and no
         # column-wise copy of h wanted (MX training needs one; the blockwise
         # 1x128 block spans both epilogue halves)
-        self.fused_swiglu = fuse_swiglu and ((self.recipe in ("mxfp8", "nvfp4") and not self.train) or self.mn)
-        if self.train and self.recipe not in ("delayed", "mxfp8"):
+        # NVFP4 training: the epilogue's second pass writes both copies of h
+        self.fused_swiglu = fuse_swiglu and ((self.recipe in ("mxfp8", "nvfp4") and not self.train) or self.mn
+                                             or (self.recipe == "nvfp4" and self.train))
+        if self.train and self.recipe not in ("delayed", "mxfp8", "nvfp4"):
             raise NotImplementedError(f"backward with {self.recipe}")
         self.scaling = {"mxfp8": mgq.MX32_E8M0, "delayed": mgq.TENSOR_F32,
                         "blockwise": mgq.BLK_1x128_F32, "nvfp4": mgq.NV16_UE4M3}[self.recipe]
         self.nv = self.recipe == "nvfp4"
+        self.align = ALIGN_NV_TRAIN if (self.nv and self.train) else ALIGN
         E, k, T, H, F = w.E, w.k, w.T, w.H, w.F
-        self.R_cap = mgq.r_cap(T, k, E, ALIGN)
+        self.R_cap = mgq.r_cap(T, k, E, self.align)
+        if self.align == ALIGN_NV_TRAIN:          # the NVFP4 wgrad reads whole 256-row stages
+            self.R_cap = (self.R_cap + 255) // 256 * 256
         R = self.R_cap
         d = self.dev
         u8 = dict(dtype=torch.uint8, device=d)
@@ -158,8 +164,31 @@ class ExpertLayer:
         self.w1s = torch.empty(mgq.nv_scale_bytes(E * 2 * F, H), **u8)
         self.w2q = torch.empty(E, H, F // 2, **u8)
         self.w2s = torch.empty(mgq.nv_scale_bytes(E * H, F), **u8)
-        self.nv_amax = torch.zeros(2 + 2 * E, dtype=torch.float32, device=d)
-        self.nv_sg = torch.ones(2 + 2 * E, dtype=torch.float32, device=d)
+        # amax and s_g: [x, h, w1 x E, w2 x E, dy2, dy1]
+        self.nv_amax = torch.zeros(4 + 2 * E, dtype=torch.float32, device=d)
+        self.nv_sg = torch.ones(4 + 2 * E, dtype=torch.float32, device=d)
+        if not self.train:
+            return
+        ns = mgq.nv_scale_bytes
+        # column-wise copies (16x1 blocks along the tokens; weights: the same
+        # 16x16 block scales as their row-wise copies), e2m1 packed along them
+        self.xcol, self.xcs = torch.empty(H, R // 2, **u8), torch.empty(ns(H, R), **u8)
+        self.hcol, self.hcs = torch.empty(F, R // 2, **u8), torch.empty(ns(F, R), **u8)
+        self.w1col, self.w1cs = torch.empty(E, H, F, **u8), torch.empty(ns(E * H, 2 * F), **u8)
+        self.w2col, self.w2cs = torch.empty(E, F, H // 2, **u8), torch.empty(ns(E * F, H), **u8)
+        self.dy2q, self.dy2s = torch.empty(R, H // 2, **u8), torch.empty(ns(R, H), **u8)
+        self.dy2col, self.dy2cs = torch.empty(H, R // 2, **u8), torch.empty(ns(H, R), **u8)
+        self.dy1q, self.dy1s = torch.empty(R, F, **u8), torch.empty(ns(R, 2 * F), **u8)
+        self.dy1col, self.dy1cs = torch.empty(2 * F, R // 2, **u8), torch.empty(ns(2 * F, R), **u8)
+        bf = dict(dtype=torch.bfloat16, device=d)
+        f32 = dict(dtype=torch.float32, device=d)
+        self.dprobs = torch.empty(T, w.k, **f32)
+        self.dh = torch.empty(R, F, **bf)
+        self.dgu_bf16 = torch.empty(R, 2 * F, **bf)      # materialised: its amax precedes the cast
+        self.dw1 = torch.empty(E, 2 * F, H, **f32)
+        self.dw2 = torch.empty(E, H, F, **f32)
+        self.dxp = torch.empty(R, H, **bf)
+        self.dx = torch.empty(T, H, **bf)
 
     # ---- scale views (delayed recipe) ------------------------------------------
     def _fs(self, i, n=1):
@@ -177,8 +206,18 @@ class ExpertLayer:
         E, Q = self.w.E, mgq.block_quantize
         if self.nv:
             a, g = self.nv_amax, self.nv_sg
-            q1 = mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, self.w1q, self.w1s, tensor_scale=g[2:2 + E], amax_out=a[2:2 + E])
-            q2 = mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, self.w2q, self.w2s, tensor_scale=g[2 + E:], amax_out=a[2 + E:])
+            if self.train:
+                # 16x16 blocks: one pass writes the row-wise and column-wise copies
+                sc2d = mgq.NV16x16_UE4M3
+                q1 = mgq.qdesc(mgq.E2M1, sc2d, self.w1q, self.w1s, self.w1col, self.w1cs, tensor_scale=g[2:2 + E],
+                               amax_out=a[2:2 + E])
+                q2 = mgq.qdesc(mgq.E2M1, sc2d, self.w2q, self.w2s, self.w2col, self.w2cs,
+                               tensor_scale=g[2 + E:2 + 2 * E], amax_out=a[2 + E:2 + 2 * E])
+            else:
+                q1 = mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, self.w1q, self.w1s, tensor_scale=g[2:2 + E],
+                               amax_out=a[2:2 + E])
+                q2 = mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, self.w2q, self.w2s, tensor_scale=g[2 + E:2 + 2 * E],
+                               amax_out=a[2 + E:2 + 2 * E])
         elif self.scaling == mgq.MX32_E8M0:
             c1 = (self.w1col, self.w1cs) if self.train else (None, None)
             c2 = (self.w2col, self.w2cs) if self.train else (None, None)
@@ -199,8 +238,10 @@ class ExpertLayer:
         if self.nv:
             a, g = self.nv_amax, self.nv_sg
             dt = mgq.E2M1
-            qx = mgq.qdesc(dt, sc, self.xq, self.xs, tensor_scale=g[0:1], amax_out=a[0:1])
-            qh = mgq.qdesc(dt, sc, self.hq, self.hs, tensor_scale=g[1:2], amax_out=a[1:2])
+            cx = (self.xcol, self.xcs) if self.train else (None, None)
+            ch = (self.hcol, self.hcs) if self.train else (None, None)
+            qx = mgq.qdesc(dt, sc, self.xq, self.xs, *cx, tensor_scale=g[0:1], amax_out=a[0:1])
+            qh = mgq.qdesc(dt, sc, self.hq, self.hs, *ch, tensor_scale=g[1:2], amax_out=a[1:2])
             A1, B1 = (mgq.operand(self.xq, self.xs, H, dt, g[0:1]),
                       mgq.operand(self.w1q, self.w1s, H, dt, g[2:2 + E]))
             A2, B2 = (mgq.operand(self.hq, self.hs, F, dt, g[1:2]),
@@ -220,7 +261,7 @@ class ExpertLayer:
             A1, B1 = mgq.operand(self.xq, sa, H, dt), mgq.operand(self.w1q, sw1, H, dt)
             A2, B2 = mgq.operand(self.hq, sh, F, dt), mgq.operand(self.w2q, sw2, F, dt)
         # routing (index work) and the permute + quantise (HBM-bound) as two ops
-        permute = [("route", lambda: mgq.moe_route(topk_idx, E, ALIGN, R, self.row_id_map, self.src_row,
+        permute = [("route", lambda: mgq.moe_route(topk_idx, E, self.align, R, self.row_id_map, self.src_row,
                                                    self.offsets, self.counts, self.ws, stream)),
                    ("permute_quant", lambda: mgq.moe_permute_routed(x, self.w.k, E, qx, R, self.row_id_map,
                                                                     self.src_row, self.offsets, self.counts, None,
@@ -246,6 +287,8 @@ class ExpertLayer:
     def bwd_ops(self, dout, probs, stream=None):
         assert self.train
         E, H, F, R = self.w.E, self.w.H, self.w.F, self.R_cap
+        if self.nv:
+            return self._bwd_ops_nvfp4(dout, probs, stream)
         if self.delayed:
             sc = mgq.TENSOR_F32
             sdy2, sdy1 = self.bwd_scale[0:1], self.bwd_scale[1:2]
@@ -302,6 +345,41 @@ class ExpertLayer:
             ("permute_bwd", lambda: mgq.moe_permute_bwd(self.dxp, self.row_id_map, self.dx, stream)),
         ]
 
+    def _bwd_ops_nvfp4(self, dout, probs, stream=None):
+        """NVFP4 backward: dY2 and dY1 = [dG | dU] quantised row-wise (dgrad)
+        and column-wise (wgrad) with their own s_g; weights' column-wise
+        copies share the 16x16 block scales of the row-wise ones."""
+        E, H, F, R = self.w.E, self.w.H, self.w.F, self.R_cap
+        sc, dt, O = mgq.NV16_UE4M3, mgq.E2M1, mgq.operand
+        a, g = self.nv_amax, self.nv_sg
+        i2, i1 = 2 + 2 * E, 3 + 2 * E
+        q2 = mgq.qdesc(dt, sc, self.dy2q, self.dy2s, self.dy2col, self.dy2cs, tensor_scale=g[i2:i2 + 1],
+                       amax_out=a[i2:i2 + 1])
+        q1 = mgq.qdesc(dt, sc, self.dy1q, self.dy1s, self.dy1col, self.dy1cs, tensor_scale=g[i1:i1 + 1],
+                       amax_out=a[i1:i1 + 1])
+        gw1, gw2 = g[2:2 + E], g[2 + E:2 + 2 * E]
+        # down projection: dh = dY2 W2 ; dW2 = dY2^T h
+        d2 = (O(self.dy2q, self.dy2s, H, dt, g[i2:i2 + 1]), O(self.w2col, self.w2cs, H, dt, gw2))
+        w2 = (O(self.dy2col, self.dy2cs, R, dt, g[i2:i2 + 1]), O(self.hcol, self.hcs, R, dt, g[1:2]))
+        # gate/up projection: dXp = dY1 W1 ; dW1 = dY1^T X
+        d1 = (O(self.dy1q, self.dy1s, 2 * F, dt, g[i1:i1 + 1]), O(self.w1col, self.w1cs, 2 * F, dt, gw1))
+        w1 = (O(self.dy1col, self.dy1cs, R, dt, g[i1:i1 + 1]), O(self.xcol, self.xcs, R, dt, g[0:1]))
+        return [
+            ("unpermute_bwd_quant", lambda: mgq.moe_unpermute_bwd(dout, self.y, self.row_id_map, self.src_row, probs,
+                                                                  R, self.offsets, E, q2, self.dprobs, stream)),
+            ("gemm_dgrad_down", lambda: mgq.grouped_gemm_dgrad(*d2, sc, self.offsets, E, R, H, F, self.dh,
+                                                               mgq.OUT_BF16, stream)),
+            ("gemm_wgrad_down", lambda: mgq.grouped_gemm_wgrad(*w2, sc, self.offsets, E, R, H, F, self.dw2, 0.0,
+                                                               mgq.OUT_F32, stream)),
+            ("dswiglu_quant", lambda: mgq.dswiglu_quantize(self.dh, self.gu, R, F, self.offsets, E, q1,
+                                                           self.dgu_bf16, stream)),
+            ("gemm_dgrad_gateup", lambda: mgq.grouped_gemm_dgrad(*d1, sc, self.offsets, E, R, 2 * F, H, self.dxp,
+                                                                 mgq.OUT_BF16, stream)),
+            ("gemm_wgrad_gateup", lambda: mgq.grouped_gemm_wgrad(*w1, sc, self.offsets, E, R, 2 * F, H, self.dw1,
+                                                                 0.0, mgq.OUT_F32, stream)),
+            ("permute_bwd", lambda: mgq.moe_permute_bwd(self.dxp, self.row_id_map, self.dx, stream)),
+        ]
+
     def update_ops(self, stream=None):
         return [("scaling_update", lambda: self.update_scaling(stream))] if self.delayed else []
 
@@ -344,6 +422,13 @@ class ExpertLayer:
         fwd = n_route + 1 + 1 + 1 + 1 + 1               # route, permute-quant, gemm1, swiglu, gemm2, unpermute
         if self.fused_swiglu:
             fwd -= 1                                    # SwiGLU in the gate/up GEMM epilogue
+        if self.nv and self.train:
+            # permute: x amax + one row/column tile pass; the gate/up GEMM's
+            # second pass writes both copies of h; weights: 2 x (amax + 16x16
+            # pass); backward: dY amax + token rows + column gather, dgrad,
+            # wgrad, dSwiGLU (dGU + amax, then rows and columns), dgrad, wgrad,
+            # permute_bwd
+            return fwd + 2 + 4 + (3 + 1 + 1 + 2 + 1 + 1 + 1)
         if self.nv:
             return fwd + 2 + 4                          # + amax passes (x, h); weights: 2 x (amax + rows)
         if not self.train:

@@ -17,6 +17,7 @@ scout_fwd               16  1  16384  5120  8192   Zipf(1.2)  blockwise
 finegrained_fwd         128 8  32768  2048  768    uniform    NVFP4
 mixtral_fwdbwd          8   2  16384  4096  14336  top-k      delayed
 mixtral_fwdbwd_mx       8   2  16384  4096  14336  top-k      MXFP8 (train)
+mixtral_fwdbwd_nvfp4    8   2  16384  4096  14336  top-k      NVFP4 (train)
 ======================  ==  =  =====  ====  =====  =========  ===========
 
 Draws: activations bf16(N(0,1)) (Mixtral shapes: 0.1% of the hidden channels,
@@ -88,6 +89,11 @@ WORKLOADS = {
     # forward, e5m2 gradients; column-wise 32x1 requantisation for wgrad)
     "mixtral_fwdbwd_mx": Workload("mixtral_fwdbwd_mx", 5, 8, 2, 16384, 4096, 14336, "topk",
                                   "mxfp8", backward=True, outlier_frac=0.001),
+    # and with NVFP4 in both passes (e2m1 with 16-element ue4m3 scales and a
+    # float32 global scale per tensor; weights with 16x16 blocks, one
+    # quantisation giving both copies; column-wise 16x1 blocks along tokens)
+    "mixtral_fwdbwd_nvfp4": Workload("mixtral_fwdbwd_nvfp4", 5, 8, 2, 16384, 4096, 14336, "topk",
+                                     "nvfp4", backward=True, outlier_frac=0.001),
 }
 
 

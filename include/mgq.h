@@ -164,7 +164,9 @@ int mgq_get_error(void* stream, int* device_status);
  *  topk_idx    device [T, k] int32, distinct experts per token in [0, E)
  *              (out of range: the entry is skipped, MGQ_ERR_DEVICE_INDEX set)
  *  q           quantisation of the permuted rows (row: [R_cap, H]; col:
- *              [H, R_cap]); NULL = no quantised output
+ *              [H, R_cap], MX / NVFP4 blocks along the rows, per-tensor the
+ *              transposed row codes; e2m1: [R_cap, H/2] and [H, R_cap/2]
+ *              bytes, s_g from an amax pre-pass); NULL = no quantised output
  *  out_bf16    device [R_cap, H] bf16 permuted copy, or NULL
  *  row_id_map  device [T, k] int32: destination row of (t, j)
  *  src_row     device [R_cap] int32: t*k + j of the row, -1 for padding
@@ -254,7 +256,15 @@ int mgq_block_quantize(const void* x_bf16, int64_t G, int64_t M, int64_t K,
  *        dgrad, MGQ_BLK_1x128_F32: A with 1x128 float32 scale_inv
  *        [K/128][R_cap], W with 128x128 float32 scale_inv [E][N/128][K/128]
  *        ([BLOCK]'s DeepSeek-style recipe; each 128-deep partial product is
- *        scaled and summed in float32).
+ *        scaled and summed in float32), or MGQ_NV16_UE4M3 (fwd, dgrad and
+ *        wgrad): e2m1 codes packed two per byte along the contraction (ld and
+ *        the contraction length in elements, multiples of 256), 16-element
+ *        ue4m3 block scales, and each operand's global_scale s_g (A / dY /
+ *        the column-wise copies: one per tensor; W, Wcol: one per expert);
+ *        the product is multiplied by 1/(s_g,a s_g,b). NVFP4 wgrad contracts
+ *        in 256-row stages: offsets[e] multiples of 256 (otherwise
+ *        MGQ_ERR_INVALID_ARG in the device error word, nothing written) and
+ *        R_cap a multiple of 256.
  * Operand layout (MGQ_TENSOR_F32 only): with per-tensor scales the
  *        column-wise copy holds the same codes as the row-wise one,
  *        transposed, so dgrad accepts the forward weight W [E, N, K] (ld >= K)
@@ -284,7 +294,10 @@ int mgq_grouped_gemm_wgrad(const mgq_operand* dYcol, const mgq_operand* Acol, in
  * it (same codes, scales and amax). The tiles pair gate rows f.. with the up
  * rows F + f.., so each tile holds both halves of 128 ffn columns.
  *  scaling  MGQ_MX32_E8M0 or MGQ_TENSOR_F32 (qh->scaling must match; qh->col
- *           must be NULL: no column-wise copy from the epilogue)
+ *           must be NULL: no column-wise copy from the epilogue), or
+ *           MGQ_NV16_UE4M3: the epilogue writes h (h_bf16 required) and its
+ *           amax, and a second pass casts h as mgq_swiglu_quantize does, rows
+ *           and (qh->col set) columns
  *  gu_bf16  [R_cap, 2F] receives g | u when not NULL (the backward's
  *           dSwiGLU input); h_bf16 [R_cap, F] receives h when not NULL
  * Requirements as mgq_grouped_gemm_fwd with N = 2F, F a multiple of 128.
@@ -314,7 +327,11 @@ int mgq_grouped_gemm_dgrad_dswiglu(const mgq_operand* dY, const mgq_operand* W2,
  * h = silu(g) * u, g = gu[:, :F], u = gu[:, F:2F] (float32, rounded to bf16,
  * then quantised). dG = dh u s (1 + g (1 - s)), dU = dh silu(g), s = sigmoid(g),
  * rounded to bf16 then quantised ([dG | dU] is one [R_cap, 2F] matrix).
- * Rows [0, offsets[E]) are processed. */
+ * Rows [0, offsets[E]) are processed. q->col (when set) receives the
+ * column-wise copy [C, R_cap] with blocks along the rows.
+ * NVFP4 (q->scaling MGQ_NV16_UE4M3): two passes, the bf16 result (h_bf16 /
+ * dgu_bf16 required) with its amax in q->amax_out, then the cast with s_g =
+ * 6*448/amax written to q->tensor_scale. */
 int mgq_swiglu_quantize(const void* gu_bf16, int64_t R_cap, int F, const int32_t* offsets,
                         int E, const mgq_qdesc* q, void* h_bf16, void* stream);
 int mgq_dswiglu_quantize(const void* dh_bf16, const void* gu_bf16, int64_t R_cap, int F,
@@ -328,7 +345,9 @@ int mgq_moe_unpermute(const void* y_bf16, const int32_t* row_id_map, const float
 
 /* ---- a8: unpermute backward, fused with quantisation of dY -----------------
  * dY[row(t, j)] = float32(probs[t, j] * dout[t]) quantised into q (row and
- * col), filler rows zero; dprobs[t, j] = <dout[t], Y[row(t, j)]> (float32). */
+ * col), filler rows zero; dprobs[t, j] = <dout[t], Y[row(t, j)]> (float32).
+ * NVFP4: an amax pre-pass over dY (max |fl(p d)| over a row is
+ * fl(|p| max |d|)) into q->amax_out, s_g into q->tensor_scale. */
 int mgq_moe_unpermute_bwd(const void* dout_bf16, const void* y_bf16,
                           const int32_t* row_id_map, const int32_t* src_row,
                           const float* probs, int T, int k, int H, int64_t R_cap,

@@ -160,7 +160,7 @@ def run_fwd_and_check(w, device, recipe: str = "mxfp8") -> dict:
         assert np.array_equal(untile_mx_scales(u8_np(lay.w2s), E * H, F, 16), np.concatenate([q[1] for q in q2]))
         sgs = [OQ.nvfp4_global_scale(np.max(np.abs(w1f[e]))) for e in range(E)] + \
               [OQ.nvfp4_global_scale(np.max(np.abs(w2f[e]))) for e in range(E)]
-        assert np.array_equal(lay.nv_sg.cpu().numpy()[2:], np.array(sgs, dtype=np.float32))
+        assert np.array_equal(lay.nv_sg.cpu().numpy()[2:2 + 2 * E], np.array(sgs, dtype=np.float32))
     else:
         q1 = [_q_weight(w1f[e], recipe) for e in range(E)]
         q2 = [_q_weight(w2f[e], recipe) for e in range(E)]

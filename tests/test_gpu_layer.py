@@ -233,3 +233,92 @@ def test_mxfp8_training_step_scaled_down():
     check_elementwise(OR.permute_bwd(dxp, rim), bf16_np(lay.dx), "permute_bwd")
     # quantised-vs-bf16 SQNR of the e4m3 forward GEMM
     assert OG.sqnr_db(OG.grouped_gemm_fwd(xp, w1f, off), gu) >= 28.0
+
+
+def test_nvfp4_training_step_scaled_down():
+    """NVFP4 in both passes: activations and gradients e2m1 with 16-element
+    ue4m3 scales and one s_g per tensor (row-wise for fwd/dgrad, 16x1 blocks
+    along each expert's tokens for wgrad), weights with 16x16 blocks (one pass,
+    both copies), groups padded to 256 rows for the NVFP4 wgrad."""
+    from fp8_grouped_gemm_gb300 import layer as L
+    from fp8_grouped_gemm_gb300 import mgq
+    from fp8_grouped_gemm_gb300 import workloads as W
+    from tests.layer_check import untile_mx_scales
+    w = W.WORKLOADS["mixtral_fwdbwd_nvfp4"].scaled(T=700, H=512, F=768, E=4)
+    E, k, T, H, F = w.E, w.k, w.T, w.H, w.F
+    x = W.make_activations(w)
+    w1, w2 = W.make_weights(w)
+    idx, probs = W.make_routing(w)
+    dout = W.make_dout(w)
+    lay = L.ExpertLayer(w, DEV, keep_bf16=True)
+    assert lay.train and lay.nv and lay.align == 256 and lay.fused_swiglu
+    lay.quantize_weights(w1.to(DEV), w2.to(DEV))
+    lay.forward(x.to(DEV), torch.from_numpy(idx).to(DEV), torch.from_numpy(probs).to(DEV))
+    lay.backward(dout.to(DEV), torch.from_numpy(probs).to(DEV))
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    R = lay.R_cap
+    rim, src, off, cnt = OR.permute_indices(idx, E, lay.align)
+    Rp = int(off[-1])
+    amax, sg = lay.nv_amax.cpu().numpy(), lay.nv_sg.cpu().numpy()
+    sc = lambda t, rows, ld: untile_mx_scales(u8_np(t), rows, ld, 16)
+
+    def row_col(m, i, rq, rs, cq, cs):
+        """m [Rp, C] with its own s_g (slot i): both NVFP4 copies; returns them dequantised [Rp, C]."""
+        am = float(np.max(np.abs(m)))
+        s_g = OQ.nvfp4_global_scale(am)
+        assert amax[i] == np.float32(am) and sg[i] == s_g
+        C = m.shape[1]
+        c, s = OQ.quantize_nvfp4(m, s_g)
+        assert np.array_equal(u8_np(rq)[:Rp], c)
+        assert np.array_equal(sc(rs, R, C)[:Rp], s)
+        ct, st = OQ.quantize_nvfp4(m.T, s_g)
+        assert np.array_equal(u8_np(cq)[:, :Rp // 2], ct)
+        assert np.array_equal(sc(cs, C, R)[:, :Rp // 16], st)
+        return OQ.dequantize_nvfp4(c, s, s_g, C), OQ.dequantize_nvfp4(ct, st, s_g, Rp).T
+
+    xp = OR.permute_rows(bf16_np(x), rim, Rp)
+    x_r, x_c = row_col(xp, 0, lay.xq, lay.xs, lay.xcol, lay.xcs)
+    w1f, w2f = bf16_np(w1), bf16_np(w2)
+
+    def weight(wf, q, s, col, cs, base, N, Kd):
+        """16x16-block copies of each expert [N, Kd]; returns the dequantised weight [E, N, Kd]."""
+        rs_all = sc(s, E * N, Kd).reshape(E, N, Kd // 16)
+        cs_all = sc(cs, E * Kd, N).reshape(E, Kd, N // 16)
+        out = []
+        for e in range(E):
+            am = float(np.max(np.abs(wf[e])))
+            s_g = OQ.nvfp4_global_scale(am)
+            assert amax[base + e] == np.float32(am) and sg[base + e] == s_g
+            rc, rs, cc, css = OQ.quantize_nvfp4_2d(wf[e], s_g)
+            assert np.array_equal(u8_np(q)[e], rc) and np.array_equal(rs_all[e], rs)
+            assert np.array_equal(u8_np(col)[e], cc) and np.array_equal(cs_all[e], css)
+            out.append(OQ.dequantize_nvfp4(rc, rs, s_g, Kd))
+        return np.stack(out)
+
+    w1_d = weight(w1f, lay.w1q, lay.w1s, lay.w1col, lay.w1cs, 2, 2 * F, H)
+    w2_d = weight(w2f, lay.w2q, lay.w2s, lay.w2col, lay.w2cs, 2 + E, H, F)
+    gu = bf16_np(lay.gu)[:Rp]
+    assert rel_fro(OF.round_to_bf16(OG.grouped_gemm_fwd(x_r, w1_d, off)), gu) <= GEMM_TOL_BF16
+    hg = bf16_np(lay.h_bf16)[:Rp]
+    check_elementwise(OL.swiglu(gu, F), hg, "swiglu")
+    h_r, h_c = row_col(hg, 1, lay.hq, lay.hs, lay.hcol, lay.hcs)
+    y = bf16_np(lay.y)[:Rp]
+    assert rel_fro(OF.round_to_bf16(OG.grouped_gemm_fwd(h_r, w2_d, off)), y) <= GEMM_TOL_BF16
+    # backward
+    i2, i1 = 2 + 2 * E, 3 + 2 * E
+    dy32, dp = OR.unpermute_bwd(bf16_np(dout), y, rim, probs, Rp)
+    assert rel_fro(dp, lay.dprobs.cpu().numpy()) <= 1e-5
+    dy2_r, dy2_c = row_col(dy32.astype(np.float64), i2, lay.dy2q, lay.dy2s, lay.dy2col, lay.dy2cs)
+    dh = bf16_np(lay.dh)[:Rp]
+    assert rel_fro(OF.round_to_bf16(OG.grouped_gemm_dgrad(dy2_r, w2_d, off)), dh) <= GEMM_TOL_BF16
+    assert rel_fro(OG.grouped_gemm_wgrad(dy2_c, h_c, off, E), lay.dw2.cpu().numpy()) <= GEMM_TOL_F32
+    dgu = bf16_np(lay.dgu_bf16)[:Rp]
+    check_elementwise(OL.dswiglu(dh, gu, F), dgu, "dswiglu")
+    dy1_r, dy1_c = row_col(dgu, i1, lay.dy1q, lay.dy1s, lay.dy1col, lay.dy1cs)
+    dxp = bf16_np(lay.dxp)[:Rp]
+    assert rel_fro(OF.round_to_bf16(OG.grouped_gemm_dgrad(dy1_r, w1_d, off)), dxp) <= GEMM_TOL_BF16
+    assert rel_fro(OG.grouped_gemm_wgrad(dy1_c, x_c, off, E), lay.dw1.cpu().numpy()) <= GEMM_TOL_F32
+    check_elementwise(OR.permute_bwd(dxp, rim), bf16_np(lay.dx), "permute_bwd")
+    # quantised-vs-bf16 SQNR of the NVFP4 forward GEMM (the NVFP4 bar)
+    assert OG.sqnr_db(OG.grouped_gemm_fwd(xp, w1f, off), gu) >= 15.0
