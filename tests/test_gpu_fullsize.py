@@ -182,3 +182,108 @@ def test_mixtral_training_step_full_size_sampled():
         ref = OQ.dequantize_tensor(dyc, bs[1], "e5m2") @ OQ.dequantize_tensor(xc, fs[0]).T
         got = dw1[e][torch.from_numpy(ns).to(DEV)][:, torch.from_numpy(ks).to(DEV)].cpu().numpy()
         assert rel_fro(ref, got) <= 1e-5, e
+
+
+@pytest.mark.parametrize("recipe", ["mxfp8", "nvfp4"])
+def test_block_scaled_training_step_full_size_sampled(recipe):
+    """The MXFP8 and NVFP4 training steps at the full Mixtral size: routing in
+    full; the row-wise dY2 codes and scales of sampled rows (NVFP4: with s_g
+    from the dY amax, max |fl(p d)| = fl(|p| max |d|)); dh at sampled rows and
+    columns against the oracle's GEMM of the dequantised dY2 rows and the weight
+    copy requantised here; sampled gate/up wgrad elements from the column-wise
+    copies."""
+    from fp8_grouped_gemm_gb300 import layer as L
+    from fp8_grouped_gemm_gb300 import mgq
+    from fp8_grouped_gemm_gb300 import workloads as W
+    w = W.WORKLOADS["mixtral_fwdbwd_mx" if recipe == "mxfp8" else "mixtral_fwdbwd_nvfp4"]
+    E, H, F, k = w.E, w.H, w.F, w.k
+    nv = recipe == "nvfp4"
+    rng = np.random.default_rng(2)
+    x = W.make_activations(w)
+    idx, probs = W.make_routing(w)
+    dout = W.make_dout(w)
+    w1, w2 = _weights_on_device(w)
+    lay = L.ExpertLayer(w, DEV)
+    assert lay.train
+    lay.quantize_weights(w1, w2)
+    lay.forward(x.to(DEV), torch.from_numpy(idx).to(DEV), torch.from_numpy(probs).to(DEV))
+    lay.backward(dout.to(DEV), torch.from_numpy(probs).to(DEV))
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    rim, src, off, cnt = OR.permute_indices(idx, E, lay.align)
+    Rp = int(off[-1])
+    R = lay.R_cap
+    assert np.array_equal(lay.offsets.cpu().numpy(), off)
+    assert np.array_equal(lay.row_id_map.cpu().numpy(), rim)
+    assert np.array_equal(lay.src_row.cpu().numpy()[:Rp], src)
+    rows = _sample_rows(off, cnt, rng)
+    rr = np.array([r for _, r in rows])
+    ee = np.array([e for e, _ in rows])
+    toks, slots = src[rr] // k, src[rr] % k
+    df = bf16_np(dout).astype(np.float32)
+    dy32 = probs[toks, slots][:, None].astype(np.float32) * df[toks]
+    rrd = torch.from_numpy(rr).to(DEV)
+    if nv:
+        i2, i1 = 2 + 2 * E, 3 + 2 * E
+        am = float(np.max(np.abs(probs).astype(np.float32) * np.max(np.abs(df), axis=1)[:, None]))
+        s_g = OQ.nvfp4_global_scale(am)
+        assert float(lay.nv_amax[i2].item()) == am and float(lay.nv_sg[i2].item()) == float(s_g)
+        c2, s2 = OQ.quantize_nvfp4(dy32.astype(np.float64), s_g)
+        got_s = untile_mx_scales(u8_np(lay.dy2s), R, H, 16)[rr]
+        dy2_deq = OQ.dequantize_nvfp4(c2, s2, s_g, H)
+    else:
+        c2, s2 = OQ.quantize_mx(dy32.astype(np.float64), "e5m2")
+        got_s = untile_mx_scales(u8_np(lay.dy2s), R, H)[rr]
+        dy2_deq = OQ.dequantize_mx(c2, s2, "e5m2")
+    assert np.array_equal(u8_np(lay.dy2q[rrd]), c2)
+    assert np.array_equal(got_s, s2)
+    # dh = dY2 W2_e at sampled columns; the dgrad reads W2's column-wise copy
+    # (blocks along H), requantised here from the bf16 weight
+    fcols = np.sort(rng.choice(F, 24, replace=False))
+    dh_gpu = bf16_np(lay.dh[rrd])
+    refs, gots = [], []
+    for e in range(E):
+        sel = ee == e
+        if not sel.any():
+            continue
+        if nv:
+            w2e = w2[e].float().cpu().numpy()                          # [H, F]
+            sg_w = OQ.nvfp4_global_scale(float(np.max(np.abs(w2e))))
+            cols = []
+            for f in fcols:
+                fb = f // 16
+                _, _, cc, cs = OQ.quantize_nvfp4_2d(w2e[:, 16 * fb:16 * fb + 16], sg_w)
+                cols.append(OQ.dequantize_nvfp4(cc, cs, sg_w, H)[f - 16 * fb])
+            wcol = np.stack(cols)                                      # [24, H]
+        else:
+            w2c = bf16_np(w2[e][:, torch.from_numpy(fcols).to(DEV)])   # [H, 24]
+            cc, cs = OQ.quantize_mx(np.ascontiguousarray(w2c.T))
+            wcol = OQ.dequantize_mx(cc, cs)
+        refs.append(dy2_deq[sel] @ wcol.T)
+        gots.append(dh_gpu[sel][:, fcols])
+    assert rel_fro(OF.round_to_bf16(np.concatenate(refs)), np.concatenate(gots)) <= GEMM_TOL_BF16
+    # gate/up wgrad at sampled (n, k): sum over the expert's rows of the
+    # column-wise dY1 and X copies, dequantised
+    ns = np.sort(rng.choice(2 * F, 6, replace=False))
+    ks = np.sort(rng.choice(H, 6, replace=False))
+    nsd, ksd = torch.from_numpy(ns).to(DEV), torch.from_numpy(ks).to(DEV)
+    blk = 16 if nv else 32
+    dyc_s = untile_mx_scales(u8_np(lay.dy1cs), 2 * F, R, blk)[ns]
+    xc_s = untile_mx_scales(u8_np(lay.xcs), H, R, blk)[ks]
+    dyc_all, xc_all = u8_np(lay.dy1col[nsd]), u8_np(lay.xcol[ksd])
+    for e in range(E):
+        lo, hi = int(off[e]), int(off[e + 1])
+        if hi == lo:
+            continue
+        # (the columns past the rows in use are never written: dequantise [0, Rp) only)
+        if nv:
+            dq = OQ.dequantize_nvfp4(dyc_all[:, :Rp // 2], dyc_s[:, :Rp // 16], float(lay.nv_sg[i1].item()),
+                                     Rp)[:, lo:hi]
+            xq = OQ.dequantize_nvfp4(xc_all[:, :Rp // 2], xc_s[:, :Rp // 16], float(lay.nv_sg[0].item()),
+                                     Rp)[:, lo:hi]
+        else:
+            dq = OQ.dequantize_mx(dyc_all[:, :Rp], dyc_s[:, :Rp // 32], "e5m2")[:, lo:hi]
+            xq = OQ.dequantize_mx(xc_all[:, :Rp], xc_s[:, :Rp // 32])[:, lo:hi]
+        ref = dq @ xq.T
+        got = lay.dw1[e][nsd][:, ksd].cpu().numpy()
+        assert rel_fro(ref, got) <= 1e-5, e
