@@ -817,15 +817,24 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
 //     into both CTAs' tensor memory with pair scale copies. Tensor memory then
 //     has no room for a second accumulator: the epilogue moves it to registers
 //     and releases it before storing.
-constexpr int PSTAGES = 6;
+constexpr int PSTAGES = 6;                                     // per-tensor and MX; NVFP4 5
+__host__ __device__ constexpr int pstages_of(int kind) { return kind == kKindNV ? 5 : PSTAGES; }
 constexpr uint32_t kPairTile = 128 * 128;                      // bytes of one A or B half tile
-constexpr uint32_t kPairSfa = 512, kPairSfb = 1024;            // MX scale bytes per stage
-__host__ __device__ constexpr uint32_t pair_sf_bytes(int kind) { return kind == kKindMX ? kPairSfa + kPairSfb : 0u; }
-__host__ __device__ constexpr size_t pair_smem(int kind) {
-  return 1024 + PSTAGES * (2 * kPairTile + pair_sf_bytes(kind)) + 8 * kStageOut + 256 + (2 * kMaxE + 16) * 4;
+// block-scale bytes per stage for this CTA's A rows (B: twice, both halves):
+// MX one 512-byte chunk per 128 rows, NVFP4 four (the 4 MMAs of a 256-element stage)
+__host__ __device__ constexpr uint32_t pair_sfa_bytes(int kind) {
+  return kind == kKindMX ? 512u : (kind == kKindNV ? 2048u : 0u);
 }
-// tensor-memory columns: accumulator(s), then the MX scale slots of every stage
-constexpr uint32_t kPairSfaCol = 256, kPairSfbCol = kPairSfaCol + PSTAGES * 4;
+__host__ __device__ constexpr uint32_t pair_sf_bytes(int kind) { return 3 * pair_sfa_bytes(kind); }
+__host__ __device__ constexpr size_t pair_smem(int kind) {
+  return 1024 + pstages_of(kind) * (2 * kPairTile + pair_sf_bytes(kind)) + 8 * kStageOut + 256 + (2 * kMaxE + 16) * 4;
+}
+// tensor-memory columns: accumulator(s), then the scale slots of every stage
+// (4 columns per chunk of A, 8 per chunk pair of B; NVFP4: 496 columns in all)
+constexpr uint32_t kPairSfaCol = 256;
+__host__ __device__ constexpr uint32_t pair_sfb_col(int kind) {
+  return kPairSfaCol + pstages_of(kind) * 4 * (pair_sfa_bytes(kind) / 512);
+}
 
 template <int MODE>
 __device__ __forceinline__ bool get_pair_tile(const int32_t* s_off, const int32_t* s_cum, int E, const GemmParams& p,
@@ -856,10 +865,10 @@ __device__ __forceinline__ bool get_pair_tile(const int32_t* s_off, const int32_
     const int64_t local = t % tpe;
     const int64_t m = local / nK, n = local % nK;
     tl.e = e;
-    tl.nst = (s_off[e + 1] - s_off[e]) / BK;
+    tl.nst = (s_off[e + 1] - s_off[e]) / (BK * p.kdiv);     // (e2m1: 2 BK rows a stage)
     tl.row_a = 256 * m;
     tl.row_b = BN * n;
-    tl.kx0 = s_off[e];
+    tl.kx0 = s_off[e] / p.kdiv;
     tl.out_row = (int64_t)e * p.N + 256 * m;
     tl.out_col = BN * n;
   }
@@ -873,21 +882,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                              const __grid_constant__ CUtensorMap tmSFB, const __grid_constant__ CUtensorMap tmH,
                              const GemmParams p) {
   constexpr bool MX = KIND == kKindMX;
-  constexpr int kAccBufs = MX ? 1 : 2;             // MX: scale slots leave room for one accumulator
+  constexpr bool NV = KIND == kKindNV;
+  constexpr bool BS = MX || NV;                    // block scales through tensor memory
+  constexpr int PST = pstages_of(KIND);
+  constexpr uint32_t kSfa = pair_sfa_bytes(KIND), kSfb = 2 * kSfa, kCh = kSfa / 512;   // chunks per 128 rows
+  constexpr uint32_t kSfbCol = pair_sfb_col(KIND);
+  constexpr int kAccBufs = BS ? 1 : 2;             // block scales: their slots leave room for one accumulator
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   uint8_t* sA = smem;
-  uint8_t* sB = sA + PSTAGES * kPairTile;
-  uint8_t* sOut = sB + PSTAGES * kPairTile;        // [8 warps][32 rows][64 bytes] epilogue staging
-  uint8_t* sSFA = sOut + 8 * kStageOut;            // MX: [stage] 512-byte chunk of this CTA's A rows
-  uint8_t* sSFB = sSFA + PSTAGES * kPairSfa;       // MX: [stage] two chunks of all B rows
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + 8 * kStageOut + PSTAGES * pair_sf_bytes(KIND));
+  uint8_t* sB = sA + PST * kPairTile;
+  uint8_t* sOut = sB + PST * kPairTile;            // [8 warps][32 rows][64 bytes] epilogue staging
+  uint8_t* sSFA = sOut + 8 * kStageOut;            // block scales: [stage] chunks of this CTA's A rows
+  uint8_t* sSFB = sSFA + PST * kSfa;               // block scales: [stage] chunks of both B halves
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + 8 * kStageOut + PST * pair_sf_bytes(KIND));
   uint64_t* full = bars;
-  uint64_t* empty = bars + PSTAGES;
-  uint64_t* tmem_full = bars + 2 * PSTAGES;        // [2]
-  uint64_t* tmem_empty = bars + 2 * PSTAGES + 2;   // [2]
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * PSTAGES + 4);
+  uint64_t* empty = bars + PST;
+  uint64_t* tmem_full = bars + 2 * PST;            // [2]
+  uint64_t* tmem_empty = bars + 2 * PST + 2;       // [2]
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * PST + 4);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   int* s_bad = reinterpret_cast<int*>(s_tmem + 2);
   int32_t* s_off = reinterpret_cast<int32_t*>(bars + 32);
@@ -902,7 +916,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   for (int i = threadIdx.x; i <= E; i += kThreads) s_off[i] = p.offsets[i];
   if (threadIdx.x == 0) {
-    for (int s = 0; s < PSTAGES; ++s) {
+    for (int s = 0; s < PST; ++s) {
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
     }
@@ -917,7 +931,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB);
-    if (MX) {
+    if (BS) {
       ptx::prefetch_tmap(&tmSFA);
       ptx::prefetch_tmap(&tmSFB);
     }
@@ -931,7 +945,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool bad = s_off[0] != 0;
     int cum = 0;
     for (int e = 0; e < E; ++e) {
-      bad |= (s_off[e + 1] < s_off[e]) || (s_off[e + 1] % BM) != 0;
+      // (contract mode over e2m1: whole 256-row stages)
+      bad |= (s_off[e + 1] < s_off[e]) || (s_off[e + 1] % (MODE == kModeContract ? BM * p.kdiv : BM)) != 0;
       s_cum[e] = cum;
       cum += (s_off[e + 1] - s_off[e] + 255) / 256;
     }
@@ -955,14 +970,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     Tile tl;
     for (int64_t t = pair; get_pair_tile<MODE>(s_off, s_cum, E, p, t, ecur, tl); t += npairs) {
       for (int s = 0; s < tl.nst; ++s, ++it) {
-        const uint32_t st = it % PSTAGES, ph = (it / PSTAGES) & 1;
+        const uint32_t st = it % PST, ph = (it / PST) & 1;
         if (*s_abort) break;
         if (!ptx::mbar_wait(&empty[st], ph ^ 1, p.wait_ns)) {
           report(p.err, MGQ_ERR_TIMEOUT);
           *s_abort = 1;
           break;
         }
-        // both CTAs' A and B halves (and MX scale chunks)
+        // both CTAs' A and B halves (and the scale chunks)
         if (leader) ptx::mbar_arrive_expect_tx(&full[st], 4 * kPairTile + 2 * pair_sf_bytes(KIND));
         const uint32_t bar0 = ptx::mapa_shared(ptx::smem_u32(&full[st]), 0);
         const int32_t kx = (int32_t)(tl.kx0 + (int64_t)s * BK);
@@ -976,14 +991,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 (int32_t)((MODE == kModeRows ? (int64_t)tl.e * p.K : 0) + kx));
         else
           ptx::tma_load_2d_pair(sB + st * kPairTile, &tmB, bar0, kx, (int32_t)(tl.row_b + p.b_half2 * rank));
-        if (MX) {
-          // scale chunk (row tile, k tile) is row tile * kb4 + kx / 128 of the
-          // [chunks][128 words] view of the scales
-          const int32_t kt = kx / BK;
-          ptx::tma_load_2d_pair(sSFA + st * kPairSfa, &tmSFA, bar0, 0,
+        if (BS) {
+          // the stage's chunks (row tile, chunk) start at row tile * kb4 + kt in
+          // the [chunks][128 words] view of the scales (boxes of kCh chunks):
+          // MX one chunk per 128-element k tile, NVFP4 four per 256-element stage
+          const int32_t kt = (kx / BK) * (int32_t)kCh;
+          ptx::tma_load_2d_pair(sSFA + st * kSfa, &tmSFA, bar0, 0,
                                 (int32_t)(((tl.row_a + 128 * rank) / 128) * p.sfa_kb4 + kt));
-          ptx::tma_load_2d_pair(sSFB + st * kPairSfb, &tmSFB, bar0, 0, (int32_t)((tl.row_b / 128) * p.sfb_kb4 + kt));
-          ptx::tma_load_2d_pair(sSFB + st * kPairSfb + 512, &tmSFB, bar0, 0,
+          ptx::tma_load_2d_pair(sSFB + st * kSfb, &tmSFB, bar0, 0, (int32_t)((tl.row_b / 128) * p.sfb_kb4 + kt));
+          ptx::tma_load_2d_pair(sSFB + st * kSfb + kSfa, &tmSFB, bar0, 0,
                                 (int32_t)(((tl.row_b + p.b_half2) / 128) * p.sfb_kb4 + kt));
         }
       }
@@ -1008,7 +1024,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       bool ok = true;
       for (int s = 0; s < tl.nst; ++s, ++it) {
-        const uint32_t st = it % PSTAGES, ph = (it / PSTAGES) & 1;
+        const uint32_t st = it % PST, ph = (it / PST) & 1;
         if (*s_abort || !ptx::mbar_wait(&full[st], ph, p.wait_ns)) {
           report(p.err, MGQ_ERR_TIMEOUT);
           *s_abort = 1;
@@ -1023,20 +1039,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint64_t bd = p.b_mn ? ptx::sdesc_mnmajor_sw128(sB0 + st * kPairTile)
                                    : ptx::sdesc_kmajor_sw128(sB0 + st * kPairTile);
         const uint64_t astep = p.a_mn ? 256 : 2, bstep = p.b_mn ? 256 : 2;
-        if (MX) {
+        if constexpr (BS) {
           // this stage's scales into both CTAs' tensor memory (ordered before
-          // the MMAs below, which read them)
-          {
-            const uint32_t fa = tmem + kPairSfaCol + st * 4, fb = tmem + kPairSfbCol + st * 8;
-            ptx::tmem_cp_32x128b_x4_pair(fa, ptx::sdesc_sf(sSFA0 + st * kPairSfa));
-            ptx::tmem_cp_32x128b_x4_pair(fb, ptx::sdesc_sf(sSFB0 + st * kPairSfb));
-            ptx::tmem_cp_32x128b_x4_pair(fb + 4, ptx::sdesc_sf(sSFB0 + st * kPairSfb + 512));
-          }
-          const uint32_t sfa_t = tmem + kPairSfaCol + st * 4, sfb_t = tmem + kPairSfbCol + st * 8;
+          // the MMAs below, which read them): chunk ch of A at 4 ch columns,
+          // of the two B halves at 8 ch and 8 ch + 4
+          const uint32_t sfa_t = tmem + kPairSfaCol + st * 4 * kCh, sfb_t = tmem + kSfbCol + st * 8 * kCh;
 #pragma unroll
-          for (int kk = 0; kk < BK / 32; ++kk)
-            ptx::mma_mxf8f6f4_pair(tmem + a * BN, ad + kk * astep, bd + kk * bstep,
-                                   p.idesc | ptx::idesc_sf_ids(kk, kk), sfa_t, sfb_t, (s > 0 || kk > 0) ? 1u : 0u);
+          for (uint32_t ch = 0; ch < kCh; ++ch) {
+            ptx::tmem_cp_32x128b_x4_pair(sfa_t + ch * 4, ptx::sdesc_sf(sSFA0 + st * kSfa + ch * 512));
+            ptx::tmem_cp_32x128b_x4_pair(sfb_t + ch * 8, ptx::sdesc_sf(sSFB0 + st * kSfb + ch * 512));
+            ptx::tmem_cp_32x128b_x4_pair(sfb_t + ch * 8 + 4, ptx::sdesc_sf(sSFB0 + st * kSfb + kSfa + ch * 512));
+          }
+#pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk) {
+            // a 32-byte step: K=32 of e4m3/e5m2 or K=64 of e2m1 (one chunk each)
+            if constexpr (NV)
+              ptx::mma_mxf4nvf4_pair(tmem + a * BN, ad + kk * astep, bd + kk * bstep, p.idesc, sfa_t + kk * 4,
+                                     sfb_t + kk * 8, (s > 0 || kk > 0) ? 1u : 0u);
+            else
+              ptx::mma_mxf8f6f4_pair(tmem + a * BN, ad + kk * astep, bd + kk * bstep,
+                                     p.idesc | ptx::idesc_sf_ids(kk, kk), sfa_t, sfb_t, (s > 0 || kk > 0) ? 1u : 0u);
+          }
         } else {
 #pragma unroll
           for (int kk = 0; kk < BK / 32; ++kk)
@@ -1200,6 +1223,16 @@ bool mx_pair_selected() {
   }();
   return f;
 }
+// NVFP4 on the 2-CTA kernel when MGQ_GEMM_NV_PAIR=1: correct, but measured
+// slower than the 1-CTA kernel (the pair form of the four scale copies a stage
+// costs more than the copies it saves), so not the default
+bool nv_pair_selected() {
+  static const bool f = [] {
+    const char* e = getenv("MGQ_GEMM_NV_PAIR");
+    return e && e[0] == '1';
+  }();
+  return f;
+}
 
 int check_operand(const mgq_operand* o) {
   if (!o || !o->data || !aligned16(o->data)) return MGQ_ERR_INVALID_ARG;
@@ -1221,6 +1254,17 @@ struct DswigluOut {
   const mgq_qdesc* q;
   void* dgu_bf16;
 };
+
+// NVFP4 SwiGLU: the epilogue wrote h (bf16) and its amax; cast h with s_g,
+// row-wise (and column-wise when qh->col is set) (N = 2F)
+int nv_swiglu_second_pass(const SwigluOut* sw, int64_t R_cap, const int32_t* offsets, int E, int64_t N,
+                          cudaStream_t s) {
+  if (sw->qh->col.data)   // row-wise and column-wise copies in one tile pass
+    return rowcol_rows(static_cast<const uint16_t*>(sw->h_bf16), R_cap, offsets + E, N / 2, sw->qh, s);
+  return launch_quant_rows_nv(static_cast<const uint16_t*>(sw->h_bf16), R_cap, offsets + E, N / 2,
+                              static_cast<uint8_t*>(sw->qh->row.data), static_cast<uint8_t*>(sw->qh->row.scale),
+                              sw->qh->amax_out, sw->qh->tensor_scale, s);
+}
 
 int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scaling, const int32_t* offsets, int E,
                 int64_t R_cap, int64_t N, int64_t K, float beta, void* out, int out_dtype, void* stream,
@@ -1376,7 +1420,8 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
                  : ptx::idesc_f8f6f4(A->dtype, B->dtype, BM, BN);
   p.err = err;
   cudaStream_t s = as_stream(stream);
-  if ((kind == kKindTensor || (kind == kKindMX && mx_pair_selected())) && use_pair_kernel(mode, N)) {
+  if ((kind == kKindTensor || (kind == kKindMX && mx_pair_selected()) || (nv && nv_pair_selected())) &&
+      use_pair_kernel(mode, N)) {
     // the pair kernel loads 128-row halves of B (K-major) or 128-column
     // halves (MN-major); MN-major operands are stored with the contraction
     // index down the rows:
@@ -1396,21 +1441,27 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
       MGQ_CHECK_ARG(B->ld >= K);
       ok = encode_tmap_u8_2d(&tb2, B->data, (uint64_t)K, (uint64_t)R_cap, (uint64_t)B->ld, 128, 128);
     } else {
+      // (e2m1: the contraction extent and pitch in bytes)
       ok = mode == kModeRows
-               ? encode_tmap_u8_2d(&tb2, B->data, (uint64_t)K, (uint64_t)E * N, (uint64_t)B->ld, 128, 128)
-               : encode_tmap_u8_2d(&tb2, B->data, (uint64_t)R_cap, (uint64_t)K, (uint64_t)B->ld, 128, 128);
+               ? encode_tmap_u8_2d(&tb2, B->data, (uint64_t)(K / ebytes_den), (uint64_t)E * N,
+                                   (uint64_t)(B->ld / ebytes_den), 128, 128)
+               : encode_tmap_u8_2d(&tb2, B->data, (uint64_t)(R_cap / ebytes_den), (uint64_t)K,
+                                   (uint64_t)(B->ld / ebytes_den), 128, 128);
     }
     if (!ok) return MGQ_ERR_CUDA;
     p.a_mn = a_mn;
     p.b_mn = b_mn;
-    p.idesc = mx ? ptx::idesc_mxf8f6f4(A->dtype, B->dtype, 256, BN)
-                 : ptx::idesc_f8f6f4(A->dtype, B->dtype, 256, BN) | ptx::idesc_mn_major(a_mn, b_mn);
-    // MX scales as [chunks][128 words]: chunk (row tile, k tile) = row tile * kb4 + k tile
+    p.idesc = nv   ? ptx::idesc_mxf4nvf4_ue4m3(256, BN)
+              : mx ? ptx::idesc_mxf8f6f4(A->dtype, B->dtype, 256, BN)
+                   : ptx::idesc_f8f6f4(A->dtype, B->dtype, 256, BN) | ptx::idesc_mn_major(a_mn, b_mn);
+    // block scales as [chunks][128 words]: chunk (row tile, k chunk) = row tile * kb4 + k chunk;
+    // a stage's box holds its chunks (MX 1, NVFP4 4)
     CUtensorMap tsfa = ta, tsfb = ta;
-    if (mx) {
+    if (mx || nv) {
       const int64_t rows_a = mode == kModeRows ? R_cap : N, rows_b = mode == kModeRows ? (int64_t)E * N : K;
-      if (!encode_tmap_2d(&tsfa, A->scale, 4, 128, (uint64_t)(rows_a / 128 * p.sfa_kb4), 512, 128, 1) ||
-          !encode_tmap_2d(&tsfb, B->scale, 4, 128, (uint64_t)(rows_b / 128 * p.sfb_kb4), 512, 128, 1))
+      const uint32_t box = nv ? 4 : 1;
+      if (!encode_tmap_2d(&tsfa, A->scale, 4, 128, (uint64_t)(rows_a / 128 * p.sfa_kb4), 512, 128, box) ||
+          !encode_tmap_2d(&tsfb, B->scale, 4, 128, (uint64_t)(rows_b / 128 * p.sfb_kb4), 512, 128, box))
         return MGQ_ERR_CUDA;
     }
     // output map: [rows, ldo] elements, boxes of 64 bytes x 32 rows
@@ -1423,6 +1474,12 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
     if (mx)
       return mode == kModeRows ? launch_gemm_pair<kModeRows, kKindMX>(ta, tb2, to, tsfa, tsfb, th, p, s)
                                : launch_gemm_pair<kModeContract, kKindMX>(ta, tb2, to, tsfa, tsfb, th, p, s);
+    if (nv) {
+      if (mode == kModeContract) return launch_gemm_pair<kModeContract, kKindNV>(ta, tb2, to, tsfa, tsfb, th, p, s);
+      if (sw && cudaMemsetAsync(sw->qh->amax_out, 0, sizeof(float), s) != cudaSuccess) return MGQ_ERR_CUDA;
+      rc = launch_gemm_pair<kModeRows, kKindNV>(ta, tb2, to, tsfa, tsfb, th, p, s);
+      return (rc != MGQ_OK || !sw) ? rc : nv_swiglu_second_pass(sw, R_cap, offsets, E, N, s);
+    }
     if (p.dswiglu) return launch_gemm_pair<kModeRows, kKindTensor, true>(ta, tb2, to, tsfa, tsfb, th, p, s);
     return mode == kModeRows ? launch_gemm_pair<kModeRows, kKindTensor>(ta, tb2, to, tsfa, tsfb, th, p, s)
                              : launch_gemm_pair<kModeContract, kKindTensor>(ta, tb2, to, tsfa, tsfb, th, p, s);
@@ -1444,11 +1501,7 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
       if (sw && cudaMemsetAsync(sw->qh->amax_out, 0, sizeof(float), s) != cudaSuccess) return MGQ_ERR_CUDA;
       rc = launch_gemm<kModeRows, kKindNV>(ta, tb, to, th, p, s);
       if (rc != MGQ_OK || !sw) return rc;
-      if (sw->qh->col.data)   // row-wise and column-wise copies in one tile pass
-        return rowcol_rows(static_cast<const uint16_t*>(sw->h_bf16), R_cap, offsets + E, N / 2, sw->qh, s);
-      return launch_quant_rows_nv(static_cast<const uint16_t*>(sw->h_bf16), R_cap, offsets + E, N / 2,
-                                  static_cast<uint8_t*>(sw->qh->row.data), static_cast<uint8_t*>(sw->qh->row.scale),
-                                  sw->qh->amax_out, sw->qh->tensor_scale, s);
+      return nv_swiglu_second_pass(sw, R_cap, offsets, E, N, s);
     }
     return launch_gemm<kModeRows, kKindBlock>(ta, tb, to, th, p, s);
   }
