@@ -754,8 +754,8 @@ int mgq_moe_unpermute_bwd(const void* dout_bf16, const void* y_bf16, const int32
                           const int32_t* offsets, int E, const mgq_qdesc* q, float* dprobs, void* stream) {
   int rc = check_q(q);
   if (rc != MGQ_OK) return rc;
-  MGQ_CHECK_ARG(T >= 0 && k >= 1 && k <= 8 && H > 0 && H % 128 == 0 && E >= 1 && offsets && dprobs && src_row);
-  MGQ_CHECK_ARG(T == 0 || (dout_bf16 && y_bf16 && row_id_map && probs));
+  MGQ_CHECK_ARG(T >= 0 && k >= 1 && k <= 8 && H > 0 && H % 128 == 0 && E >= 1 && offsets && src_row);
+  MGQ_CHECK_ARG(T == 0 || (dout_bf16 && y_bf16 && row_id_map && probs && dprobs));   // no entries: may be null
   MGQ_CHECK_ARG(aligned16(dout_bf16) && aligned16(y_bf16) && R_cap > 0 && R_cap % 128 == 0);
   cudaStream_t s = as_stream(stream);
   const bool nv = q->scaling == MGQ_NV16_UE4M3;

@@ -232,7 +232,9 @@ int mgq_moe_permute_noalloc(const void* x_bf16, int T, int H, const int32_t* top
  *  NVFP4 (MGQ_NV16_UE4M3, row-wise only; MGQ_NV16x16_UE4M3, row-wise and
  *    optionally column-wise, dtype MGQ_E2M1): an amax pre-pass writes each
  *    group's amax to q->amax_out [G] and s_g = 6*448/amax to
- *    q->tensor_scale [G]; codes [G, M, K/2] / [G, K, M/2] bytes.
+ *    q->tensor_scale [G]; codes [G, M, K/2] / [G, K, M/2] bytes. (Every
+ *    NVFP4 call writes s_g with the first row it quantises: with no rows in
+ *    use it writes the amax, 0, and leaves q->tensor_scale as it was.)
  * Requires M and K multiples of 128. */
 int mgq_block_quantize(const void* x_bf16, int64_t G, int64_t M, int64_t K,
                        const mgq_qdesc* q, void* stream);

@@ -1203,6 +1203,108 @@ def test_route_then_permute_routed_equals_permute(mgq, mode):
     assert np.array_equal(two["src"].cpu().numpy()[:Rp], src)
 
 
+@pytest.mark.parametrize("mode", ["mx_col", "nvfp4", "nvfp4_col"])
+def test_empty_batch_block_scaled_paths(mgq, mode):
+    """T = 0 through the block-scaled permute (routed), unpermute backward and
+    (NVFP4) SwiGLU / dSwiGLU quantisers: no error, no code written, the NVFP4
+    amax set to 0."""
+    dev = torch.device(DEV)
+    E, k, H, F = 4, 2, 256, 256
+    T = 0
+    nv = mode.startswith("nvfp4")
+    align = 256 if nv else 128
+    R_cap = max(256, mgq.r_cap(T, k, E, align))
+    idx = torch.empty(0, k, dtype=torch.int32, device=dev)
+    rim = torch.empty(0, k, dtype=torch.int32, device=dev)
+    src = torch.full((R_cap,), -9, dtype=torch.int32, device=dev)
+    off = torch.full((E + 1,), -9, dtype=torch.int32, device=dev)
+    cnt = torch.full((E,), -9, dtype=torch.int32, device=dev)
+    ws = torch.empty(max(16, mgq.permute_workspace_size(T, k, E)), dtype=torch.uint8, device=dev)
+    mgq.moe_route(idx, E, align, R_cap, rim, src, off, cnt, ws)
+
+    def qd(C):
+        cb = C // 2 if nv else C
+        codes = torch.full((R_cap, cb), 0xAB, dtype=torch.uint8, device=dev)
+        sc = torch.full(((mgq.nv_scale_bytes if nv else mgq.mx_scale_bytes)(R_cap, C),), 0xCD, dtype=torch.uint8,
+                        device=dev)
+        col = csc = None
+        if mode.endswith("col"):
+            col = torch.full((C, R_cap // 2 if nv else R_cap), 0xAB, dtype=torch.uint8, device=dev)
+            csc = torch.full(((mgq.nv_scale_bytes if nv else mgq.mx_scale_bytes)(C, R_cap),), 0xCD,
+                             dtype=torch.uint8, device=dev)
+        if nv:
+            am, sg = torch.full((1,), 7.0, device=dev), torch.full((1,), 9.0, device=dev)
+            q = mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, codes, sc, col, csc, tensor_scale=sg, amax_out=am)
+        else:
+            am = sg = None
+            q = mgq.qdesc(mgq.E4M3, mgq.MX32_E8M0, codes, sc, col, csc)
+        return q, [codes, sc] + ([col, csc] if col is not None else []), am
+
+    x = torch.empty(0, H, dtype=torch.bfloat16, device=dev)
+    qx, bx, amx = qd(H)
+    mgq.moe_permute_routed(x, k, E, qx, R_cap, rim, src, off, cnt)
+    qy, by, amy = qd(H)
+    dprobs = torch.empty(0, k, device=dev)
+    mgq.moe_unpermute_bwd(torch.empty(0, H, dtype=torch.bfloat16, device=dev),
+                          torch.zeros(R_cap, H, dtype=torch.bfloat16, device=dev), rim, src,
+                          torch.empty(0, k, device=dev), R_cap, off, E, qy, dprobs)
+    bufs, ams = bx + by, [amx, amy]
+    if nv:
+        gu = torch.zeros(R_cap, 2 * F, dtype=torch.bfloat16, device=dev)
+        h = torch.full((R_cap, F), 3.0, dtype=torch.bfloat16, device=dev)
+        qh, bh, amh = qd(F)
+        mgq.swiglu_quantize(gu, R_cap, F, off, E, qh, h)
+        dgu = torch.full((R_cap, 2 * F), 3.0, dtype=torch.bfloat16, device=dev)
+        qg, bg, amg = qd(2 * F)
+        mgq.dswiglu_quantize(torch.zeros(R_cap, F, dtype=torch.bfloat16, device=dev), gu, R_cap, F, off, E, qg, dgu)
+        bufs, ams = bufs + bh + bg, ams + [amh, amg]
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    assert torch.all(off == 0) and torch.all(cnt == 0)
+    for b in bufs:
+        assert torch.all((b == 0xAB) | (b == 0xCD)).item()      # nothing written
+    if nv:
+        assert all(float(a.item()) == 0.0 for a in ams)
+        assert torch.all(h == 3.0).item() and torch.all(dgu == 3.0).item()
+
+
+def test_tile_pass_beyond_the_grid_row_limit(mgq):
+    """An MX row-wise + column-wise pass over 66560 row tiles (more than a
+    grid dimension holds): the CTAs stride over the row tiles; the first, a
+    middle, the 65536th and the last tiles equal the oracle's."""
+    dev = torch.device(DEV)
+    K = 128
+    M = 66560 * 128
+    g = torch.Generator(device=dev)
+    g.manual_seed(77)
+    x = torch.randn(M, K, generator=g, device=dev).to(torch.bfloat16)
+    codes = torch.empty(M, K, dtype=torch.uint8, device=dev)
+    sc = torch.empty(mgq.mx_scale_bytes(M, K), dtype=torch.uint8, device=dev)
+    col = torch.empty(K, M, dtype=torch.uint8, device=dev)
+    csc = torch.empty(mgq.mx_scale_bytes(K, M), dtype=torch.uint8, device=dev)
+    mgq.block_quantize(x, mgq.qdesc(mgq.E4M3, mgq.MX32_E8M0, codes, sc, col, csc))
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    s_nat = untile_mx_scales(u8_np(sc), M, K)
+    for t in (0, 12345, 65535, 66559):
+        r0 = t * 128
+        xt = bf16_np(x[r0:r0 + 128])
+        c, s_ = OQ.quantize_mx(xt)
+        assert np.array_equal(u8_np(codes[r0:r0 + 128]), c), t
+        assert np.array_equal(s_nat[r0:r0 + 128], s_), t
+        cc, cs = OQ.quantize_mx(xt.T)
+        assert np.array_equal(u8_np(col[:, r0:r0 + 128]), cc), t
+    # the column-wise scales of the last tile (natural [K, M/32] view, computed
+    # from the tiled layout directly for its 4 blocks)
+    kb4 = M // 128
+    ks = np.arange(K)[:, None]
+    bs = (66559 * 128) // 32 + np.arange(4)[None, :]
+    offs = ((ks // 128) * kb4 + bs // 4) * 512 + (ks % 32) * 16 + ((ks // 32) % 4) * 4 + bs % 4
+    got = u8_np(csc)[offs]
+    _, cs_last = OQ.quantize_mx(bf16_np(x[66559 * 128:]).T)
+    assert np.array_equal(got, cs_last)
+
+
 def test_empty_batch_through_every_call(mgq):
     """T = 0 tokens: routing gives empty groups (offsets all zero), the
     permute writes nothing, the GEMMs compute nothing (wgrad writes zeros for
