@@ -8,13 +8,18 @@
 // work on TE", TransformerEngine issue #2393: 128x1 backward blocks with the
 // transpose done in shared memory, transpose(colwise(x)) = rowwise(x^T)).
 //
-// A CTA reads its tile once from its source functor (a plain bf16 matrix,
-// SwiGLU of the gate/up output, or dSwiGLU), keeps the float values in shared
-// memory, and writes
-//   row-wise codes [rows, C] (blocks of 32 along C for MX), and
-//   column-wise codes [C, M] per group of M rows (blocks of 32 along the rows),
-// with per-tensor scales (the column copy is then the transposed cast) or
-// E8M0 block scales in the 128x4-tiled layout.
+// A tile is read once from its source (a plain bf16 matrix, SwiGLU of the
+// gate/up output, dSwiGLU, or rows gathered through the routing), held as bf16
+// in shared memory, and written as
+//   row-wise codes [rows, C] (MX blocks of 32 along C, NVFP4 blocks of 16), and
+//   column-wise codes [C, M] per group of M rows (blocks along the rows),
+// with per-tensor scales (the column copy is then the transposed cast), E8M0
+// block scales, or NVFP4 ue4m3 block scales with s_g from an amax pre-pass,
+// all in the 128x4-tiled scale layout.
+// Kernels: quant_rowcol_kernel (one tile per CTA: plain and computed sources),
+// quant_rowcol_stream_kernel (gathered rows: a CTA walks a range of tiles and
+// stages the next with cp.async), quant_nv2d_kernel (NVFP4 weights with 16x16
+// blocks: both copies share the block scales).
 #include "mgq_internal.h"
 #include "rowquant.cuh"
 
