@@ -560,6 +560,35 @@ __global__ void __launch_bounds__(256) dswiglu_dgu_kernel(const uint16_t* __rest
   if (lane == 0) atomic_max_nonneg(amax, __uint_as_float(tam));
 }
 
+// max |x| over the rows [0, *rows_used) of a bf16 [rows, C] matrix: one warp
+// per row (strided), one atomic per CTA (amax zeroed by the caller)
+__global__ void __launch_bounds__(256) amax_rows_kernel(const uint16_t* __restrict__ x, const int32_t* rows_used,
+                                                        int64_t C, float* amax) {
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31;
+  const int64_t n = *rows_used;
+  uint32_t tam = 0;
+  for (int64_t r = (int64_t)blockIdx.x * kWarps + warp; r < n; r += (int64_t)gridDim.x * kWarps) {
+    uint32_t acc = 0;
+    for (int64_t c = 8 * lane; c < C; c += 256) {
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(x + r * C + c));
+      acc = absmax_acc_bf16x2(absmax_acc_bf16x2(absmax_acc_bf16x2(absmax_acc_bf16x2(acc, w.x), w.y), w.z), w.w);
+    }
+    tam = max(tam, warp_max_u32(fold_bf16x2(absmax_bf16x2_final(acc))));
+  }
+  cta_amax_atomic(tam, amax);
+}
+
+// a group layout whose starts are not multiples of `blk` rows (or that is not
+// monotone, or runs past R_cap) is reported in the error word
+__global__ void group_layout_check_kernel(const int32_t* off, int E, int64_t R_cap, int blk, int* err) {
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    const int64_t o = off[e];
+    const bool bad = (o % blk) != 0 || o > R_cap || (e == 0 && o != 0) || (e > 0 && off[e - 1] > o);
+    if (bad) report(err, MGQ_ERR_INVALID_ARG);
+  }
+}
+
 // ---- delayed scaling ------------------------------------------------------------
 // One warp per role: the lanes read the ring coalesced (entry h already
 // replaced by this step's amax) and reduce the max with shuffles; fmaxf drops
@@ -865,6 +894,32 @@ int mgq_block_quantize(const void* x_bf16, int64_t G, int64_t M, int64_t K, cons
   const unsigned grid = (unsigned)((G * M + kWarps - 1) / kWarps);
   MGQ_DISPATCH_Q(q, quant_rows_kernel, grid, a);
   return MGQ_OK;
+}
+
+int mgq_grouped_quantize(const void* x_bf16, int64_t R_cap, int64_t C, const int32_t* offsets, int E,
+                         const mgq_qdesc* q, void* stream) {
+  int rc = check_q(q);
+  if (rc != MGQ_OK) return rc;
+  MGQ_CHECK_ARG(x_bf16 && aligned16(x_bf16) && offsets && E >= 1 && E <= 1024);
+  MGQ_CHECK_ARG(C > 0 && C % 128 == 0 && R_cap > 0 && R_cap % 128 == 0 && R_cap < (1ll << 31));
+  const int sc = q->scaling;
+  if (sc != MGQ_MX32_E8M0 && sc != MGQ_TENSOR_F32 && sc != MGQ_NV16_UE4M3) return MGQ_ERR_UNSUPPORTED;
+  int* err = error_word();
+  if (!err) return MGQ_ERR_CUDA;
+  cudaStream_t s = as_stream(stream);
+  // column blocks run inside the groups: group starts on block boundaries
+  const int blk = sc == MGQ_MX32_E8M0 ? 32 : (sc == MGQ_NV16_UE4M3 ? 16 : 1);
+  group_layout_check_kernel<<<1, 256, 0, s>>>(offsets, E, R_cap, blk, err);
+  MGQ_LAUNCH_CHECK();
+  if (sc == MGQ_NV16_UE4M3) {   // s_g needs the amax of the rows in use first
+    if (cudaMemsetAsync(q->amax_out, 0, sizeof(float), s) != cudaSuccess) return MGQ_ERR_CUDA;
+    const int blocks = (int)std::min<int64_t>((R_cap + kWarps - 1) / kWarps, (int64_t)num_sms() * 4);
+    amax_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint16_t*>(x_bf16), offsets + E, C, q->amax_out);
+    MGQ_LAUNCH_CHECK();
+  }
+  // one tile pass over the rows in use: the groups are whole column blocks, so
+  // treating the matrix as one group gives every group's own column blocks
+  return rowcol_rows(static_cast<const uint16_t*>(x_bf16), R_cap, offsets + E, C, q, s);
 }
 
 int mgq_amax_history_update(float* history, int32_t* head, float* amax, float* scale, int n, int L, float fmax,

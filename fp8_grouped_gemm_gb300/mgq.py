@@ -30,7 +30,7 @@ FMAX = {E4M3: 448.0, E5M2: 57344.0}
 # every symbol include/mgq.h declares
 EXPORTS = (
     "mgq_status_string", "mgq_version", "mgq_get_error", "mgq_permute_workspace_size",
-    "mgq_moe_permute", "mgq_moe_route", "mgq_moe_permute_routed", "mgq_moe_permute_noalloc", "mgq_block_quantize", "mgq_grouped_gemm_fwd", "mgq_grouped_gemm_dgrad",
+    "mgq_moe_permute", "mgq_moe_route", "mgq_moe_permute_routed", "mgq_moe_permute_noalloc", "mgq_block_quantize", "mgq_grouped_quantize", "mgq_grouped_gemm_fwd", "mgq_grouped_gemm_dgrad",
     "mgq_grouped_gemm_wgrad", "mgq_grouped_gemm_fwd_swiglu",
     "mgq_grouped_gemm_dgrad_dswiglu", "mgq_swiglu_quantize", "mgq_dswiglu_quantize", "mgq_moe_unpermute",
     "mgq_moe_unpermute_bwd", "mgq_moe_permute_bwd", "mgq_amax_history_update",
@@ -82,6 +82,7 @@ def load() -> ctypes.CDLL:
         lib.mgq_moe_permute_noalloc.argtypes = [vp, i32, i32, vp, i32, i32, i32, P(QDesc), vp, i64,
                                                 vp, vp, vp, vp, vp]
         lib.mgq_block_quantize.argtypes = [vp, i64, i64, i64, P(QDesc), vp]
+        lib.mgq_grouped_quantize.argtypes = [vp, i64, i64, vp, i32, P(QDesc), vp]
         gemm = [P(Operand), P(Operand), i32, vp, i32, i64, i64, i64]
         lib.mgq_grouped_gemm_fwd.argtypes = gemm + [vp, i32, vp]
         lib.mgq_grouped_gemm_dgrad.argtypes = gemm + [vp, i32, vp]
@@ -210,6 +211,13 @@ def block_quantize(x, q: QDesc, stream=None):
     shp = tuple(x.shape)
     G, M, K = shp if len(shp) == 3 else (1,) + shp
     _check(load().mgq_block_quantize(_p(x), G, M, K, ctypes.byref(q), _s(stream)), "mgq_block_quantize")
+
+
+def grouped_quantize(x, offsets, E, q: QDesc, stream=None):
+    """x: [R_cap, C] bf16; rows [0, offsets[E]) in ragged groups."""
+    R_cap, C = x.shape
+    _check(load().mgq_grouped_quantize(_p(x), R_cap, C, _p(offsets), E, ctypes.byref(q), _s(stream)),
+           "mgq_grouped_quantize")
 
 
 def grouped_gemm_fwd(A: Operand, W: Operand, scaling, offsets, E, R_cap, N, K, Y, out_dtype=OUT_BF16,

@@ -239,6 +239,24 @@ int mgq_moe_permute_noalloc(const void* x_bf16, int T, int H, const int32_t* top
 int mgq_block_quantize(const void* x_bf16, int64_t G, int64_t M, int64_t K,
                        const mgq_qdesc* q, void* stream);
 
+/* Row-wise and column-wise quantisation of a bf16 matrix over ragged groups
+ * ([GROUPED]'s grouped tensor with row-wise and column-wise data; [BLOCK]'s
+ * 128x1 backward blocks inside each group): x_bf16 device [R_cap, C]; rows
+ * [0, offsets[E]) are in use, group e = rows [offsets[e], offsets[e+1]).
+ *  q->row  [R_cap, C] codes (+ scales over [R_cap, C]) for the rows in use
+ *  q->col  [C, R_cap] codes (+ scales over [C, R_cap]) or NULL; column blocks
+ *          (MX 32, NVFP4 16 rows) run inside each group
+ * scaling: MGQ_TENSOR_F32 (q->tensor_scale[0]; the column copy is the
+ * transposed cast; q->amax_out optional), MGQ_MX32_E8M0, or MGQ_NV16_UE4M3
+ * (an amax pre-pass over the rows in use into q->amax_out[0], s_g into
+ * q->tensor_scale[0]; e2m1 codes [R_cap, C/2] / [C, R_cap/2] bytes).
+ * Group starts must be multiples of the column block (MX 32, NVFP4 16): a
+ * layout that is not (or not monotone, or past R_cap) is reported as
+ * MGQ_ERR_INVALID_ARG in the device error word, and the codes are then
+ * unspecified. Requires C and R_cap multiples of 128, E <= 1024. */
+int mgq_grouped_quantize(const void* x_bf16, int64_t R_cap, int64_t C, const int32_t* offsets,
+                         int E, const mgq_qdesc* q, void* stream);
+
 /* ---- a5/a9/a11: grouped GEMMs ------------------------------------------------
  * [MOE-FP8] one grouped GEMM for all experts; [AO-MOE] scaled grouped mm;
  * [GROUPED] single grouped weight [E, N, K], gradient accumulation fusion.

@@ -83,6 +83,11 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.mgq_block_quantize(16, 1, 128, 100, ctypes.byref(q), None) == INV
     q2 = mgq.qdesc(mgq.E4M3, 9, 16, 16)
     assert lib.mgq_block_quantize(16, 1, 128, 128, ctypes.byref(q2), None) == mgq.ERR_UNSUPPORTED
+    # ragged-group quantiser: C not a multiple of 128, missing offsets, blockwise scaling
+    assert lib.mgq_grouped_quantize(16, 256, 100, 16, 4, ctypes.byref(q), None) == INV
+    assert lib.mgq_grouped_quantize(16, 256, 128, None, 4, ctypes.byref(q), None) == INV
+    q3 = mgq.qdesc(mgq.E4M3, mgq.BLK_1x128_F32, 16, 16)
+    assert lib.mgq_grouped_quantize(16, 256, 128, 16, 4, ctypes.byref(q3), None) == mgq.ERR_UNSUPPORTED
     assert lib.mgq_amax_history_update(None, None, None, None, 1, 1, ctypes.c_float(448.0), None) == INV
     assert lib.mgq_get_error(None, None) == INV
 

@@ -1305,6 +1305,81 @@ def test_tile_pass_beyond_the_grid_row_limit(mgq):
     assert np.array_equal(got, cs_last)
 
 
+@pytest.mark.parametrize("mode", ["mx", "nvfp4", "tensor"])
+def test_grouped_quantize_ragged_groups(mgq, mode):
+    """Row-wise and column-wise codes of a bf16 matrix over ragged groups (an
+    empty group, a 32-row group, unpadded rows past the last group): equal to
+    the oracle's, column blocks inside each group; a group start off the block
+    boundary is reported."""
+    rng = np.random.default_rng(81)
+    dev = torch.device(DEV)
+    C, R_cap = 384, 768
+    sizes = [160, 0, 32, 320, 64]                 # multiples of 32 (MX) and 16 (NVFP4)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    E, Rp = len(sizes), int(off[-1])
+    x = _bf16(rng, (R_cap, C), 2.0)
+    x[Rp:] = 1e4                                  # rows past the groups: never read
+    xf = bf16_np(x)[:Rp]
+    nv = mode == "nvfp4"
+    cb = C // 2 if nv else C
+    codes = torch.full((R_cap, cb), 0xAB, dtype=torch.uint8, device=dev)
+    col = torch.full((C, R_cap // 2 if nv else R_cap), 0xAB, dtype=torch.uint8, device=dev)
+    if nv:
+        sc = torch.full((mgq.nv_scale_bytes(R_cap, C),), 0xCD, dtype=torch.uint8, device=dev)
+        csc = torch.full((mgq.nv_scale_bytes(C, R_cap),), 0xCD, dtype=torch.uint8, device=dev)
+        am, sg = torch.full((1,), 7.0, device=dev), torch.zeros(1, device=dev)
+        q = mgq.qdesc(mgq.E2M1, mgq.NV16_UE4M3, codes, sc, col, csc, tensor_scale=sg, amax_out=am)
+    elif mode == "mx":
+        sc = torch.full((mgq.mx_scale_bytes(R_cap, C),), 0xCD, dtype=torch.uint8, device=dev)
+        csc = torch.full((mgq.mx_scale_bytes(C, R_cap),), 0xCD, dtype=torch.uint8, device=dev)
+        q = mgq.qdesc(mgq.E4M3, mgq.MX32_E8M0, codes, sc, col, csc)
+    else:
+        s = torch.tensor([3.0], device=dev)
+        am = torch.zeros(1, device=dev)
+        q = mgq.qdesc(mgq.E4M3, mgq.TENSOR_F32, codes, None, col, None, s, am)
+    offd = torch.from_numpy(off).to(dev)
+    mgq.grouped_quantize(x.to(dev), offd, E, q)
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    if nv:
+        amv = float(np.max(np.abs(xf)))
+        s_g = OQ.nvfp4_global_scale(amv)
+        assert float(am.item()) == amv and float(sg.item()) == float(s_g)
+        c, s_ = OQ.quantize_nvfp4(xf, s_g)
+        assert np.array_equal(u8_np(codes)[:Rp], c)
+        assert np.array_equal(untile_mx_scales(u8_np(sc), R_cap, C, 16)[:Rp], s_)
+        for e in range(E):
+            lo, hi = int(off[e]), int(off[e + 1])
+            if hi == lo:
+                continue
+            cc, cs = OQ.quantize_nvfp4(xf[lo:hi].T, s_g)
+            assert np.array_equal(u8_np(col)[:, lo // 2:hi // 2], cc), e
+            assert np.array_equal(untile_mx_scales(u8_np(csc), C, R_cap, 16)[:, lo // 16:hi // 16], cs), e
+    elif mode == "mx":
+        c, s_ = OQ.quantize_mx(xf)
+        assert np.array_equal(u8_np(codes)[:Rp], c)
+        assert np.array_equal(untile_mx_scales(u8_np(sc), R_cap, C)[:Rp], s_)
+        for e in range(E):
+            lo, hi = int(off[e]), int(off[e + 1])
+            if hi == lo:
+                continue
+            cc, cs = OQ.quantize_mx(xf[lo:hi].T)
+            assert np.array_equal(u8_np(col)[:, lo:hi], cc), e
+            assert np.array_equal(untile_mx_scales(u8_np(csc), C, R_cap)[:, lo // 32:hi // 32], cs), e
+    else:
+        c, amv = OQ.quantize_tensor(xf, np.float32(3.0))
+        assert np.array_equal(u8_np(codes)[:Rp], c)
+        assert np.array_equal(u8_np(col)[:, :Rp], c.T)
+        assert float(am.item()) == amv
+    assert torch.all(codes[Rp:] == 0xAB).item()     # rows past the groups untouched
+    if mode != "tensor":
+        # a group start off the column-block boundary is reported
+        bad = torch.from_numpy(np.array([0, 48, Rp], dtype=np.int32)).to(dev)
+        mgq.grouped_quantize(x.to(dev), bad, 2, q)
+        torch.cuda.synchronize()
+        assert mgq.get_error() == (mgq.ERR_INVALID_ARG if mode == "mx" else mgq.OK)   # 48: an NVFP4 block start
+
+
 def test_empty_batch_through_every_call(mgq):
     """T = 0 tokens: routing gives empty groups (offsets all zero), the
     permute writes nothing, the GEMMs compute nothing (wgrad writes zeros for
