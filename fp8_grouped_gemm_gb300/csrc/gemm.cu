@@ -113,6 +113,12 @@ struct GemmParams {
   // [R_cap, 2F] with h_scale; dh itself only when `out` is set
   int dswiglu;
   const uint16_t* gu_in;   // [R_cap, 2F]
+  // MX column-wise copy of h (SwiGLU) or of [dG | dU] (dSwiGLU), written by
+  // the epilogue: codes [C, c_ld] (C = F or 2F, c_ld = R_cap) with E8M0 scales
+  // per 32 rows (the 32 rows of one epilogue warp), tiled; null = none
+  uint8_t* c_codes;
+  uint8_t* c_scales;
+  int64_t c_ld;
   int debug_stall;    // failure-detection test: the producer issues no loads, so
                       // every consumer wait runs out and reports MGQ_ERR_TIMEOUT
   uint64_t wait_ns;   // limit of every mbarrier wait
@@ -278,13 +284,87 @@ __device__ __forceinline__ uint32_t acc_col(int swiglu, uint32_t half, int c) {
   return swiglu ? (c < 2 ? half * 64 + 32 * c : 128 + half * 64 + 32 * (c - 2)) : half * 128 + 32 * c;
 }
 
+// 32 x 32 transpose of 16-bit values across a warp. On entry lane l holds
+// row l as 16 words (word j: columns 2j and 2j + 1, the first in the low
+// half); on exit lane l holds column l (word j: rows 2j and 2j + 1). Round k
+// exchanges, with lane l ^ 2^k, the elements whose row and column indices
+// differ in bit k (whole words for k >= 1, half words for k = 0); after the
+// five rounds element (r, c) has moved to lane c, position r.
+__device__ __forceinline__ void warp_transpose32_b16(uint32_t (&w)[16], uint32_t lane) {
+#pragma unroll
+  for (int k = 4; k >= 1; --k) {
+    const int m = 1 << (k - 1);               // the word-index bit of column bit k
+    const bool up = (lane >> k) & 1u;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (j & m) continue;
+      const uint32_t send = up ? w[j] : w[j | m];
+      const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, send, 1 << k);
+      if (up) w[j] = recv;
+      else w[j | m] = recv;
+    }
+  }
+  // round 0: an even lane trades its odd columns (high halves) for the odd
+  // lane's even columns (low halves), two words per exchange
+  const bool odd = lane & 1u;
+#pragma unroll
+  for (int j = 0; j < 16; j += 2) {
+    const uint32_t send = odd ? __byte_perm(w[j], w[j + 1], 0x5410) : __byte_perm(w[j], w[j + 1], 0x7632);
+    const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, send, 1);
+    if (odd) {
+      w[j] = __byte_perm(w[j], recv, 0x3254);
+      w[j + 1] = __byte_perm(w[j + 1], recv, 0x3276);
+    } else {
+      w[j] = __byte_perm(w[j], recv, 0x5410);
+      w[j + 1] = __byte_perm(w[j + 1], recv, 0x7610);
+    }
+  }
+}
+
+// E8M0 block quantisation of 32 bf16 values held as pairs: the block's
+// exponent from max |x| (NaN and infinity give the NaN marker), the codes
+// cast(x * 2^-e) as eight words (element 0 in the low byte of word 0)
+__device__ __forceinline__ uint32_t mx_block32(const uint32_t (&w)[16], bool e5, bool rceil, uint32_t (&cw)[8]) {
+  uint32_t acc = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc = absmax_acc_bf16x2(acc, w[i]);
+  const int e = mx_exponent(fold_bf16x2(absmax_bf16x2_final(acc)),
+                            e5 ? FmtInfo<MGQ_E5M2>::emax : FmtInfo<MGQ_E4M3>::emax, rceil);
+  const float mult = mx_multiplier(e);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float a0 = __fmul_rn(bf16_lo(w[2 * i]), mult), a1 = __fmul_rn(bf16_hi(w[2 * i]), mult);
+    const float a2 = __fmul_rn(bf16_lo(w[2 * i + 1]), mult), a3 = __fmul_rn(bf16_hi(w[2 * i + 1]), mult);
+    cw[i] = e5 ? cvt_fp8x4<MGQ_E5M2>(a0, a1, a2, a3) : cvt_fp8x4<MGQ_E4M3>(a0, a1, a2, a3);
+  }
+  return mx_scale_code(e);
+}
+
+// Column-wise MX copy of a warp's 32 rows (row0..row0+31, one per lane) and 32
+// columns (col..col+31, one 32-bit pair of each per word of `w`, the lane's own
+// row): after the warp transpose lane l holds column col + l, one E8M0 block of
+// 32 rows, whose codes (32 bytes) go to c_codes[col + l][row0..] and whose
+// scale to the tiled scales of [C, c_ld]. `w` is clobbered. Warp-collective.
+__device__ __forceinline__ void col_copy_mx32(const GemmParams& p, uint32_t (&w)[16], int64_t col, int64_t row0,
+                                              uint32_t lane) {
+  warp_transpose32_b16(w, lane);
+  uint32_t cw[8];
+  const uint32_t code = mx_block32(w, p.h_dtype == MGQ_E5M2, p.h_rceil != 0, cw);
+  const int64_t c = col + lane;
+  p.c_scales[tiled_scale_offset(c, row0 / 32, p.c_ld / 128)] = (uint8_t)code;
+  uint4* dst = reinterpret_cast<uint4*>(p.c_codes + c * p.c_ld + row0);
+  dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+  dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+}
+
 // SwiGLU epilogue of the gate/up GEMM for one thread's row `orow` and ffn
 // columns f0..f0+63: g, u = bf16(acc * alpha) (the values the plain GEMM would
 // write), h = bf16(silu(g) u), quantised with the GEMM's scaling kind (MX:
 // E8M0 per 32 columns; per-tensor: *p.h_scale, max |h| into tam). The codes,
 // and (p.out set) g and u, go out through TMA stores from the warp's staging
-// buffer; MX scales and the optional bf16 h by plain stores.
-template <int KIND>
+// buffer; MX scales and the optional bf16 h by plain stores. MX with
+// p.c_codes: also the column-wise copy of h (blocks of the warp's 32 rows).
+template <int KIND, bool COL = true>
 __device__ __forceinline__ void epilogue_swiglu(const GemmParams& p, const uint32_t (&r)[4][32], float alpha,
                                                 int64_t orow, int64_t f0, Stager& sg, const CUtensorMap* tmO,
                                                 const CUtensorMap* tmH, int32_t y0, uint32_t lane, uint32_t& tam) {
@@ -346,6 +426,8 @@ __device__ __forceinline__ void epilogue_swiglu(const GemmParams& p, const uint3
         const float a2 = __fmul_rn(bf16_lo(hp[2 * w + 1]), mult), a3 = __fmul_rn(bf16_hi(hp[2 * w + 1]), mult);
         hw[8 * c + w] = e5 ? cvt_fp8x4<MGQ_E5M2>(a0, a1, a2, a3) : cvt_fp8x4<MGQ_E4M3>(a0, a1, a2, a3);
       }
+      // MX column-wise copy of these 32 columns over the warp's 32 rows
+      if (COL && KIND == kKindMX && p.c_codes) col_copy_mx32(p, hp, f0 + 32 * c, y0, lane);
     }
   }
   if (KIND != kKindNV) {
@@ -456,6 +538,89 @@ __device__ __forceinline__ void epilogue_dswiglu(const GemmParams& p, uint32_t t
                                         F + col0 + 16 * (c - 3));
     }
 
+  }
+}
+
+// dSwiGLU epilogue of the down-projection dgrad with MX scaling, for one
+// thread's row `orow` and dh columns col0..col0+127. dhp holds dh = bf16(acc)
+// as pairs (consumed), read from tensor memory before the accumulator was released (so
+// this work overlaps the next tile's MMAs). Per 32-column chunk: g and u of
+// the forward's gu (the next chunk's requested before this one is worked
+// on), [dG | dU] = dswiglu_bf16, the row-wise E8M0 blocks (codes [R_cap, 2F]
+// through `tmR`, tiled scales into h_scales), with p.c_codes the column-wise
+// blocks of the warp's 32 rows from row0 (codes [2F, R_cap] through `tmC`,
+// tiled scales into c_scales), and the optional bf16 dh (p.out) and dG | dU
+// (p.h_bf16), all by plain stores (32 bytes of a row per lane).
+// Warp-collective.
+__device__ __forceinline__ void epilogue_dswiglu_mx(const GemmParams& p, uint32_t (&dhp)[64], int64_t orow,
+                                                    int64_t col0, int64_t row0, uint32_t lane) {
+  const int64_t F = p.F;
+  const bool e5 = p.h_dtype == MGQ_E5M2, rceil = p.h_rceil != 0;
+  const uint16_t* grow = p.gu_in + orow * 2 * F + col0;
+  uint4 gq[4], uq[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    gq[q] = __ldg(reinterpret_cast<const uint4*>(grow) + q);
+    uq[q] = __ldg(reinterpret_cast<const uint4*>(grow + F) + q);
+  }
+  // a rolled loop keeps the code small: chunk c works on dhp[0..15], then the
+  // words of the later chunks move down (static register indices throughout)
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t dg[16], du[16];   // bf16 pairs (exact)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t gw[4] = {gq[q].x, gq[q].y, gq[q].z, gq[q].w};
+      const uint32_t uw[4] = {uq[q].x, uq[q].y, uq[q].z, uq[q].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t d = dhp[4 * q + i];
+        float g0, g1, u0, u1;
+        dswiglu_bf16(bf16_lo(d), bf16_lo(gw[i]), bf16_lo(uw[i]), g0, u0);
+        dswiglu_bf16(bf16_hi(d), bf16_hi(gw[i]), bf16_hi(uw[i]), g1, u1);
+        dg[4 * q + i] = pack_bf16x2(g0, g1);
+        du[4 * q + i] = pack_bf16x2(u0, u1);
+      }
+    }
+    if (c < 3) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        gq[q] = __ldg(reinterpret_cast<const uint4*>(grow + 32 * (c + 1)) + q);
+        uq[q] = __ldg(reinterpret_cast<const uint4*>(grow + F + 32 * (c + 1)) + q);
+      }
+    }
+    const int64_t col = col0 + 32 * c;
+    if (p.out) {
+      uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow * p.ldo + col);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) o[q] = make_uint4(dhp[4 * q], dhp[4 * q + 1], dhp[4 * q + 2], dhp[4 * q + 3]);
+    }
+#pragma unroll
+    for (int i = 0; i < 48; ++i) dhp[i] = dhp[i + 16];
+    if (p.h_bf16) {
+      uint4* og = reinterpret_cast<uint4*>(p.h_bf16 + orow * 2 * F + col);
+      uint4* ou = reinterpret_cast<uint4*>(p.h_bf16 + orow * 2 * F + F + col);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        og[q] = make_uint4(dg[4 * q], dg[4 * q + 1], dg[4 * q + 2], dg[4 * q + 3]);
+        ou[q] = make_uint4(du[4 * q], du[4 * q + 1], du[4 * q + 2], du[4 * q + 3]);
+      }
+    }
+    uint32_t cw[8];
+    const uint32_t sg = mx_block32(dg, e5, rceil, cw);
+    uint4* dst = reinterpret_cast<uint4*>(p.h_codes + orow * 2 * F + col);
+    dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+    dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+    const uint32_t su = mx_block32(du, e5, rceil, cw);
+    dst = reinterpret_cast<uint4*>(p.h_codes + orow * 2 * F + F + col);
+    dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+    dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+    p.h_scales[tiled_scale_offset(orow, col / 32, 2 * F / 128)] = (uint8_t)sg;
+    p.h_scales[tiled_scale_offset(orow, (F + col) / 32, 2 * F / 128)] = (uint8_t)su;
+    if (p.c_codes) {
+      col_copy_mx32(p, dg, col, row0, lane);
+      col_copy_mx32(p, du, F + col, row0, lane);
+    }
   }
 }
 
@@ -729,7 +894,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         const uint32_t a = tc % kAcc, aph = (tc / kAcc) & 1;
         uint4 gq[2], uq[2];    // dSwiGLU: the first g / u chunk, requested before the accumulator is ready
-        if (DSW) dswiglu_load_gu(p, orow, col0, 0, gq, uq);
+        if (DSW && KIND == kKindTensor) dswiglu_load_gu(p, orow, col0, 0, gq, uq);
         // the whole warp agrees before the .sync.aligned tensor-memory loads
         if (__any_sync(0xFFFFFFFFu, *s_abort != 0)) break;
         const bool got = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&tmem_full[a], aph, p.wait_ns));
@@ -740,7 +905,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tc_fence_after();
         const uint32_t tbase = tmem + a * BN + ((q * 32) << 16);
-        if (DSW) {
+        if (DSW && KIND == kKindTensor) {
           epilogue_dswiglu(p, tbase + half * (BN / 2), 1.0f / (p.sa[0] * p.sb[tl.e]), orow, col0,
                            sg, &tmO, &tmH, (int32_t)(tl.out_row + q * 32), lane, h_tam,
                            gq, uq);
@@ -755,6 +920,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_before();
         ptx::mbar_arrive(&tmem_empty[a]);       // accumulator free for the next tile
         ++tc;
+        if (DSW && KIND == kKindMX) {
+          // MX dSwiGLU: dh = bf16(acc) packed, then the epilogue from registers
+          uint32_t dhp[64];
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              dhp[16 * c + i] = pack_bf16x2(__uint_as_float(r[c][2 * i]), __uint_as_float(r[c][2 * i + 1]));
+          epilogue_dswiglu_mx(p, dhp, orow, col0, tl.out_row + q * 32, lane);
+          continue;
+        }
       }
       float alpha = 1.0f;
       if (KIND == kKindTensor || NV) alpha = 1.0f / (p.sa[0] * p.sb[MODE == kModeRows ? tl.e : 0]);
@@ -1137,7 +1313,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!store) continue;    // the warp's 32 rows lie wholly inside or past the group
       const float alpha = MX ? 1.0f : 1.0f / (p.sa[0] * p.sb[MODE == kModeRows ? tl.e : 0]);
       if (MODE == kModeRows && p.swiglu)
-        epilogue_swiglu<KIND>(p, r, alpha, orow, tl.out_col + half * 64, sg, &tmO, &tmH,
+        epilogue_swiglu<KIND, false>(p, r, alpha, orow, tl.out_col + half * 64, sg, &tmO, &tmH,
                               (int32_t)(tl.out_row + 128 * rank + q * 32), lane, h_tam);
       else
         epilogue_store(p, r, alpha, orow, col0, p.tma_store != 0, sg, &tmO,
@@ -1359,6 +1535,9 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
   p.h_rceil = 1;
   p.dswiglu = 0;
   p.gu_in = nullptr;
+  p.c_codes = nullptr;
+  p.c_scales = nullptr;
+  p.c_ld = R_cap;
   CUtensorMap th = ta;    // SwiGLU / dSwiGLU codes map (unused otherwise)
   if (sw) {
     // gate/up tiles: gate rows 128 n.. and up rows F + 128 n..; h quantised
@@ -1367,8 +1546,9 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
     const int64_t F = N / 2;
     if (mode != kModeRows || kind == kKindBlock || b_mn) return MGQ_ERR_UNSUPPORTED;
     MGQ_CHECK_ARG(qh && qh->row.data && aligned16(qh->row.data) && N % 256 == 0 && aligned16(sw->h_bf16));
-    // a column-wise copy of h only with NVFP4 (written by the second pass)
-    if (qh->scaling != scaling || (qh->col.data && !nv)) return MGQ_ERR_UNSUPPORTED;
+    // a column-wise copy of h with NVFP4 (written by the second pass) or MX
+    // (written by the epilogue); not per tensor
+    if (qh->scaling != scaling || (qh->col.data && !nv && !mx)) return MGQ_ERR_UNSUPPORTED;
     if (nv) {
       // h in bf16 and its amax from the epilogue, then the NVFP4 cast
       if (qh->dtype != MGQ_E2M1) return MGQ_ERR_UNSUPPORTED;
@@ -1378,6 +1558,11 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
       if (qh->dtype != MGQ_E4M3 && qh->dtype != MGQ_E5M2) return MGQ_ERR_UNSUPPORTED;
       if (mx) MGQ_CHECK_ARG(qh->row.scale && aligned16(qh->row.scale));
       else MGQ_CHECK_ARG(qh->tensor_scale != nullptr);
+      if (mx && qh->col.data) {
+        MGQ_CHECK_ARG(aligned16(qh->col.data) && qh->col.scale && aligned16(qh->col.scale));
+        p.c_codes = static_cast<uint8_t*>(qh->col.data);
+        p.c_scales = static_cast<uint8_t*>(qh->col.scale);
+      }
     }
     MGQ_CHECK_ARG(out_dtype == MGQ_OUT_BF16);
     p.swiglu = 1;
@@ -1396,21 +1581,36 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
   }
   if (dsw) {
     // down-projection dgrad (N = F output columns): [dG | dU] quantised
-    // row-wise per tensor into dsw->q ([R_cap, 2F] codes)
+    // row-wise into dsw->q ([R_cap, 2F] codes): per tensor, or MX (E8M0
+    // blocks of 32 columns, and optionally the column-wise copy [2F, R_cap]
+    // with blocks of 32 rows)
     const mgq_qdesc* q = dsw->q;
-    if (mode != kModeRows || kind != kKindTensor || q->scaling != MGQ_TENSOR_F32 || q->col.data)
-      return MGQ_ERR_UNSUPPORTED;
+    const bool dsw_mx = kind == kKindMX && q->scaling == MGQ_MX32_E8M0;
+    const bool dsw_pt = kind == kKindTensor && q->scaling == MGQ_TENSOR_F32 && !q->col.data;
+    if (mode != kModeRows || !(dsw_mx || dsw_pt)) return MGQ_ERR_UNSUPPORTED;
     if (q->dtype != MGQ_E4M3 && q->dtype != MGQ_E5M2) return MGQ_ERR_UNSUPPORTED;
-    MGQ_CHECK_ARG(q->row.data && aligned16(q->row.data) && q->tensor_scale && dsw->gu && aligned16(dsw->gu) &&
+    MGQ_CHECK_ARG(q->row.data && aligned16(q->row.data) && dsw->gu && aligned16(dsw->gu) &&
                   aligned16(dsw->dgu_bf16) && N % 128 == 0 && out_dtype == MGQ_OUT_BF16);
+    if (dsw_mx) {
+      MGQ_CHECK_ARG(q->row.scale && aligned16(q->row.scale));
+      if (q->col.data) {
+        MGQ_CHECK_ARG(aligned16(q->col.data) && q->col.scale && aligned16(q->col.scale));
+        p.c_codes = static_cast<uint8_t*>(q->col.data);
+        p.c_scales = static_cast<uint8_t*>(q->col.scale);
+      }
+    } else {
+      MGQ_CHECK_ARG(q->tensor_scale != nullptr);
+    }
     p.dswiglu = 1;
     p.F = N;
     p.gu_in = static_cast<const uint16_t*>(dsw->gu);
     p.h_codes = static_cast<uint8_t*>(q->row.data);
+    p.h_scales = static_cast<uint8_t*>(q->row.scale);
     p.h_scale = q->tensor_scale;
     p.h_amax = q->amax_out;
     p.h_bf16 = static_cast<uint16_t*>(dsw->dgu_bf16);
     p.h_dtype = q->dtype;
+    p.h_rceil = q->e8m0_mode == MGQ_E8M0_RCEIL;
     if (!encode_tmap_2d(&th, q->row.data, 1, (uint64_t)(2 * N), (uint64_t)R_cap, (uint64_t)(2 * N), 64, 32))
       return MGQ_ERR_CUDA;
   }
@@ -1420,8 +1620,9 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
                  : ptx::idesc_f8f6f4(A->dtype, B->dtype, BM, BN);
   p.err = err;
   cudaStream_t s = as_stream(stream);
-  if ((kind == kKindTensor || (kind == kKindMX && mx_pair_selected()) || (nv && nv_pair_selected())) &&
-      use_pair_kernel(mode, N)) {
+  // (the epilogue's MX column-wise copies and MX dSwiGLU run on the 1-CTA kernel)
+  const bool mx_pair = kind == kKindMX && mx_pair_selected() && !p.c_codes && !p.dswiglu;
+  if ((kind == kKindTensor || mx_pair || (nv && nv_pair_selected())) && use_pair_kernel(mode, N)) {
     // the pair kernel loads 128-row halves of B (K-major) or 128-column
     // halves (MN-major); MN-major operands are stored with the contraction
     // index down the rows:
@@ -1493,7 +1694,9 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
     p.tma_store = (beta == 0.0f && !direct_store_forced()) ? 1 : 0;
   }
   if (mode == kModeRows) {
-    if (kind == kKindMX) return launch_gemm<kModeRows, kKindMX>(ta, tb, to, th, p, s);
+    if (kind == kKindMX)
+      return p.dswiglu ? launch_gemm<kModeRows, kKindMX, true>(ta, tb, to, th, p, s)
+                       : launch_gemm<kModeRows, kKindMX>(ta, tb, to, th, p, s);
     if (kind == kKindTensor)
       return p.dswiglu ? launch_gemm<kModeRows, kKindTensor, true>(ta, tb, to, th, p, s)
                        : launch_gemm<kModeRows, kKindTensor>(ta, tb, to, th, p, s);

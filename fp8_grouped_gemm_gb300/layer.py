@@ -6,10 +6,12 @@ per-tensor recipe, of the backward step:
 
 forward:  moe_permute (+ quantise) -> grouped_gemm_fwd (gate/up) ->
           swiglu_quantize -> grouped_gemm_fwd (down) -> moe_unpermute
-          (MXFP8 inference and the delayed recipe fuse the gate/up GEMM and
-          SwiGLU + quantise into grouped_gemm_fwd_swiglu; the delayed recipe
-          also fuses the down dgrad and dSwiGLU + quantise into
-          grouped_gemm_dgrad_dswiglu)
+          (MXFP8, NVFP4 and the delayed recipe fuse the gate/up GEMM and
+          SwiGLU + quantise into grouped_gemm_fwd_swiglu, MXFP8 training with
+          the column-wise copy of h; delayed training also fuses the down
+          dgrad and dSwiGLU + quantise into grouped_gemm_dgrad_dswiglu, whose
+          MX form, with its column-wise copy, runs no faster than the two
+          separate steps on the Mixtral shapes, so MXFP8 training keeps those)
 backward: moe_unpermute_bwd (+ quantise dY, dprobs) -> grouped_gemm_dgrad and
           grouped_gemm_wgrad (down) -> dswiglu_quantize -> grouped_gemm_dgrad
           and grouped_gemm_wgrad (gate/up) -> moe_permute_bwd
@@ -51,13 +53,12 @@ class ExpertLayer:
         # per-tensor backward GEMMs read the row-wise codes MN-major
         self.mn = self.delayed and not col_copies
         self.keep_bf16 = keep_bf16
-        # SwiGLU in the gate/up GEMM epilogue: MX, per-tensor or NVFP4 (whose
-        # epilogue writes h and its amax, cast by a second pass), and no
-        # column-wise copy of h wanted (MX training needs one; the blockwise
-        # 1x128 block spans both epilogue halves)
-        # NVFP4 training: the epilogue's second pass writes both copies of h
-        self.fused_swiglu = fuse_swiglu and ((self.recipe in ("mxfp8", "nvfp4") and not self.train) or self.mn
-                                             or (self.recipe == "nvfp4" and self.train))
+        # SwiGLU in the gate/up GEMM epilogue: MX (training: the epilogue also
+        # writes the column-wise copy of h), NVFP4 (the epilogue writes h and
+        # its amax; a second pass casts both copies) or per-tensor without a
+        # column-wise copy (the blockwise 1x128 block spans both epilogue
+        # halves); dSwiGLU in the down dgrad epilogue for per-tensor training
+        self.fused_swiglu = fuse_swiglu and (self.recipe in ("mxfp8", "nvfp4") or self.mn)
         if self.train and self.recipe not in ("delayed", "mxfp8", "nvfp4"):
             raise NotImplementedError(f"backward with {self.recipe}")
         self.scaling = {"mxfp8": mgq.MX32_E8M0, "delayed": mgq.TENSOR_F32,

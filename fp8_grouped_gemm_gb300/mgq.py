@@ -243,7 +243,8 @@ def grouped_gemm_wgrad(dYcol: Operand, Acol: Operand, scaling, offsets, E, R_cap
 def grouped_gemm_fwd_swiglu(A: Operand, W1: Operand, scaling, offsets, E, R_cap, F, K, qh: QDesc, gu=None, h=None,
                             stream=None):
     """Gate/up GEMM with SwiGLU + row-wise quantisation of h in its epilogue
-    (gu [R_cap, 2F] and h [R_cap, F] bf16 written only when given)."""
+    (MX: also the column-wise copy when qh has one; gu [R_cap, 2F] and h
+    [R_cap, F] bf16 written only when given)."""
     _check(load().mgq_grouped_gemm_fwd_swiglu(ctypes.byref(A), ctypes.byref(W1), scaling, _p(offsets), E, R_cap,
                                               F, K, ctypes.byref(qh), _p(gu), _p(h), _s(stream)),
            "mgq_grouped_gemm_fwd_swiglu")
@@ -252,7 +253,8 @@ def grouped_gemm_fwd_swiglu(A: Operand, W1: Operand, scaling, offsets, E, R_cap,
 def grouped_gemm_dgrad_dswiglu(dY: Operand, W2: Operand, scaling, offsets, E, R_cap, H, F, gu, q: QDesc, dh=None,
                                dgu=None, stream=None):
     """Down-projection dgrad with dSwiGLU + row-wise quantisation of [dG | dU]
-    in its epilogue (dh [R_cap, F] and dgu [R_cap, 2F] bf16 only when given)."""
+    in its epilogue, per tensor or MX (MX: also the column-wise copy when q has
+    one; dh [R_cap, F] and dgu [R_cap, 2F] bf16 only when given)."""
     _check(load().mgq_grouped_gemm_dgrad_dswiglu(ctypes.byref(dY), ctypes.byref(W2), scaling, _p(offsets), E,
                                                  R_cap, H, F, _p(gu), ctypes.byref(q), _p(dh), _p(dgu), _s(stream)),
            "mgq_grouped_gemm_dgrad_dswiglu")

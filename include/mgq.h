@@ -313,11 +313,15 @@ int mgq_grouped_gemm_wgrad(const mgq_operand* dYcol, const mgq_operand* Acol, in
  * is quantised row-wise into qh exactly as mgq_swiglu_quantize would quantise
  * it (same codes, scales and amax). The tiles pair gate rows f.. with the up
  * rows F + f.., so each tile holds both halves of 128 ffn columns.
- *  scaling  MGQ_MX32_E8M0 or MGQ_TENSOR_F32 (qh->scaling must match; qh->col
- *           must be NULL: no column-wise copy from the epilogue), or
+ *  scaling  MGQ_MX32_E8M0 or MGQ_TENSOR_F32 (qh->scaling must match), or
  *           MGQ_NV16_UE4M3: the epilogue writes h (h_bf16 required) and its
  *           amax, and a second pass casts h as mgq_swiglu_quantize does, rows
- *           and (qh->col set) columns
+ *           and (qh->col set) columns.
+ *           qh->col: MX only (NULL for MGQ_TENSOR_F32): the epilogue also
+ *           writes the column-wise copy of h exactly as mgq_swiglu_quantize
+ *           would: codes [F, R_cap] (row f holds column f of h, one E8M0
+ *           block per 32 rows of a group) and their tiled scales
+ *           (mgq_mx_scale_bytes(F, R_cap) bytes)
  *  gu_bf16  [R_cap, 2F] receives g | u when not NULL (the backward's
  *           dSwiGLU input); h_bf16 [R_cap, F] receives h when not NULL
  * Requirements as mgq_grouped_gemm_fwd with N = 2F, F a multiple of 128.
@@ -333,8 +337,12 @@ int mgq_grouped_gemm_fwd_swiglu(const mgq_operand* A, const mgq_operand* W1, int
  * forward weight [E, H, F] with MGQ_LAYOUT_MN) whose epilogue rounds dh to
  * bf16 and applies the SwiGLU derivative with the forward's gu_bf16 [R_cap, 2F]
  * (g | u), then quantises [dG | dU] row-wise into q exactly as
- * mgq_dswiglu_quantize would (same codes and amax).
- *  scaling  MGQ_TENSOR_F32 only (q->scaling too; q->col must be NULL)
+ * mgq_dswiglu_quantize would (same codes, scales and amax).
+ *  scaling  MGQ_TENSOR_F32 (q->scaling too; q->col must be NULL) or
+ *           MGQ_MX32_E8M0 (q->scaling too; q->row.scale required): E8M0
+ *           blocks of 32 along the 2F columns, and with q->col set the
+ *           column-wise copy [2F, R_cap] with blocks of 32 rows of a group
+ *           and tiled scales, as mgq_dswiglu_quantize writes it
  *  dh_bf16  [R_cap, F] receives dh when not NULL; dgu_bf16 [R_cap, 2F]
  *           receives dG | dU when not NULL
  * MGQ_ERR_UNSUPPORTED for other scalings. */

@@ -1025,12 +1025,15 @@ def test_amax_history_update(mgq):
         assert torch.count_nonzero(amax).item() == 0
 
 
-@pytest.mark.parametrize("scaling", ["tensor", "mx", "nvfp4"])
+@pytest.mark.parametrize("scaling", ["tensor", "mx", "mx_col", "nvfp4"])
 def test_gemm_fwd_swiglu_equals_separate_steps(mgq, scaling):
     """The gate/up GEMM with SwiGLU + quantisation in its epilogue writes the
     same bytes as grouped_gemm_fwd followed by swiglu_quantize: g | u, h, the
-    h codes and scales, and the per-tensor amax (groups of 128 and 384 rows,
-    an empty group, pair tiles reaching past a group)."""
+    h codes and scales, the per-tensor amax and (mx_col) the MX column-wise
+    copy of h (groups of 128 and 384 rows, an empty group, pair tiles reaching
+    past a group)."""
+    col = scaling == "mx_col"
+    scaling = "mx" if col else scaling
     rng = np.random.default_rng(31)
     dev = torch.device(DEV)
     offs = np.array([0, 128, 128, 512, 640], dtype=np.int32)
@@ -1074,8 +1077,10 @@ def test_gemm_fwd_swiglu_equals_separate_steps(mgq, scaling):
                  hs=torch.full(((mgq.nv_scale_bytes if nv else mgq.mx_scale_bytes)(R_cap, F),), 0xCD,
                                dtype=torch.uint8, device=dev),
                  ts=torch.tensor([2.5], device=dev), am=torch.full((1,), 7.0, device=dev))
+        o["c"] = torch.full((F, R_cap), 0xAB, dtype=torch.uint8, device=dev)
+        o["cs"] = torch.full((mgq.mx_scale_bytes(F, R_cap),), 0xCD, dtype=torch.uint8, device=dev)
         if sc == mgq.MX32_E8M0:
-            o["q"] = mgq.qdesc(mgq.E4M3, sc, o["hq"], o["hs"])
+            o["q"] = mgq.qdesc(mgq.E4M3, sc, o["hq"], o["hs"], *((o["c"], o["cs"]) if col else (None, None)))
         elif nv:   # s_g is written to ts, the amax (zeroed by the call) to am
             o["q"] = mgq.qdesc(mgq.E2M1, sc, o["hq"], o["hs"], tensor_scale=o["ts"], amax_out=o["am"])
         else:
@@ -1093,22 +1098,32 @@ def test_gemm_fwd_swiglu_equals_separate_steps(mgq, scaling):
                                 h=bare["h"] if sc == mgq.NV16_UE4M3 else None)
     torch.cuda.synchronize()
     assert mgq.get_error() == mgq.OK
-    for key in ("gu", "h", "hq", "hs", "am", "ts"):
+    for key in ("gu", "h", "hq", "hs", "am", "ts", "c", "cs"):
         assert torch.equal(sep[key], fus[key]), key
     assert torch.equal(sep["hq"], bare["hq"]) and torch.equal(sep["am"], bare["am"])
+    assert torch.equal(sep["c"], bare["c"]) and torch.equal(sep["cs"], bare["cs"])
     assert torch.all(bare["gu"] == 3.0)
     assert torch.all(fus["hq"][Rp:] == 0xAB)          # rows past the groups untouched
     # and h against the oracle's SwiGLU of the GEMM output
     gu = bf16_np(sep["gu"])[:Rp]
-    check_elementwise(OL.swiglu(gu, F), bf16_np(fus["h"])[:Rp], "swiglu")
+    hf = bf16_np(fus["h"])[:Rp]
+    check_elementwise(OL.swiglu(gu, F), hf, "swiglu")
+    if col:   # the column-wise copy against the oracle: 32-row blocks inside the groups
+        assert torch.all(fus["c"][:, Rp:] == 0xAB)
+        ct, st = OQ.quantize_mx(hf.T, "e4m3")
+        assert np.array_equal(u8_np(fus["c"])[:, :Rp], ct)
+        assert np.array_equal(untile_mx_scales(u8_np(fus["cs"]), F, R_cap)[:, :Rp // 32], st)
 
 
-@pytest.mark.parametrize("w_layout", ["mn_major", "k_major"])
+@pytest.mark.parametrize("w_layout", ["mn_major", "k_major", "mx", "mx_col"])
 def test_gemm_dgrad_dswiglu_equals_separate_steps(mgq, w_layout):
     """The down-projection dgrad with dSwiGLU + quantisation in its epilogue
     writes the same bytes as grouped_gemm_dgrad followed by dswiglu_quantize
-    (W2 read MN-major or as its column-wise copy, per-tensor e5m2 gradients,
-    an empty group, pair tiles reaching past a group)."""
+    (per-tensor e5m2 gradients with W2 read MN-major or as its column-wise
+    copy; MX e5m2 gradients, rows only or with the column-wise copy; an empty
+    group, pair tiles reaching past a group)."""
+    mx = w_layout.startswith("mx")
+    col = w_layout == "mx_col"
     rng = np.random.default_rng(37)
     dev = torch.device(DEV)
     offs = np.array([0, 128, 128, 512, 640], dtype=np.int32)
@@ -1121,7 +1136,12 @@ def test_gemm_dgrad_dswiglu_equals_separate_steps(mgq, w_layout):
     wc = (rng.choice(f4.pos_codes[:-1], size=(E, H, F)) | (rng.integers(0, 2, (E, H, F)) * 0x80)).astype(np.uint8)
     dY = _op(mgq, dyc, np.array([2048.0], dtype=np.float32), H, mgq.E5M2, dev)
     s_w = np.array([40.0, 16.0, 8.0, 30.0], dtype=np.float32)
-    if w_layout == "mn_major":
+    if mx:
+        dyc, dys = _mx_operand(rng, R_cap, H, fmt="e5m2", sc_lo=110, sc_hi=116)
+        dY = _op(mgq, dyc, tile_mx_scales(dys), H, mgq.E5M2, dev)
+        wc2, ws2 = _mx_operand(rng, E * F, H, sc_lo=118, sc_hi=124)          # W2col [E, F, H]
+        W2 = _op(mgq, wc2, tile_mx_scales(ws2), H, mgq.E4M3, dev)
+    elif w_layout == "mn_major":
         W2 = _op(mgq, wc, s_w, F, mgq.E4M3, dev)
         W2.layout = mgq.LAYOUT_MN
     else:
@@ -1132,25 +1152,47 @@ def test_gemm_dgrad_dswiglu_equals_separate_steps(mgq, w_layout):
         o = dict(dh=torch.full((R_cap, F), 3.0, dtype=torch.bfloat16, device=dev),
                  dgu=torch.full((R_cap, 2 * F), 3.0, dtype=torch.bfloat16, device=dev),
                  q=torch.full((R_cap, 2 * F), 0xAB, dtype=torch.uint8, device=dev),
+                 s=torch.full((mgq.mx_scale_bytes(R_cap, 2 * F),), 0xCD, dtype=torch.uint8, device=dev),
+                 c=torch.full((2 * F, R_cap), 0xAB, dtype=torch.uint8, device=dev),
+                 cs=torch.full((mgq.mx_scale_bytes(2 * F, R_cap),), 0xCD, dtype=torch.uint8, device=dev),
                  ts=torch.tensor([5000.0], device=dev), am=torch.zeros(1, device=dev))
-        o["qd"] = mgq.qdesc(mgq.E5M2, mgq.TENSOR_F32, o["q"], None, None, None, o["ts"], o["am"])
+        if mx:
+            o["qd"] = mgq.qdesc(mgq.E5M2, mgq.MX32_E8M0, o["q"], o["s"],
+                                *((o["c"], o["cs"]) if col else (None, None)))
+        else:
+            o["qd"] = mgq.qdesc(mgq.E5M2, mgq.TENSOR_F32, o["q"], None, None, None, o["ts"], o["am"])
         return o
 
     sep, fus, bare = outputs(), outputs(), outputs()
-    sc = mgq.TENSOR_F32
+    sc = mgq.MX32_E8M0 if mx else mgq.TENSOR_F32
     mgq.grouped_gemm_dgrad(dY, W2, sc, offd, E, R_cap, H, F, sep["dh"])
     mgq.dswiglu_quantize(sep["dh"], gu, R_cap, F, offd, E, sep["qd"], sep["dgu"])
     mgq.grouped_gemm_dgrad_dswiglu(dY, W2, sc, offd, E, R_cap, H, F, gu, fus["qd"], fus["dh"], fus["dgu"])
     mgq.grouped_gemm_dgrad_dswiglu(dY, W2, sc, offd, E, R_cap, H, F, gu, bare["qd"])
     torch.cuda.synchronize()
     assert mgq.get_error() == mgq.OK
-    for key in ("dh", "dgu", "q", "am"):
-        assert torch.equal(sep[key][:Rp] if key != "am" else sep[key], fus[key][:Rp] if key != "am" else fus[key]), key
-    assert torch.equal(sep["q"][:Rp], bare["q"][:Rp]) and torch.equal(sep["am"], bare["am"])
+    for key in ("dh", "dgu", "q"):
+        assert torch.equal(sep[key][:Rp], fus[key][:Rp]), key
+    for key in ("am", "s", "c", "cs"):      # (untouched alike outside the groups)
+        assert torch.equal(sep[key], fus[key]), key
+    for key in ("q", "s", "c", "cs"):
+        assert torch.equal(sep[key][:Rp] if key == "q" else sep[key], bare[key][:Rp] if key == "q" else bare[key])
+    assert torch.equal(sep["am"], bare["am"])
     assert torch.all(bare["dh"] == 3.0)
     assert torch.all(fus["q"][Rp:] == 0xAB)
     # and dSwiGLU against the oracle
-    check_elementwise(OL.dswiglu(bf16_np(sep["dh"])[:Rp], bf16_np(gu)[:Rp], F), bf16_np(fus["dgu"])[:Rp], "dswiglu")
+    dgu = bf16_np(fus["dgu"])[:Rp]
+    check_elementwise(OL.dswiglu(bf16_np(sep["dh"])[:Rp], bf16_np(gu)[:Rp], F), dgu, "dswiglu")
+    if mx:    # the codes against the oracle's MX blocks (columns: 32 rows inside the groups)
+        c, s_ = OQ.quantize_mx(dgu, "e5m2")
+        assert np.array_equal(u8_np(fus["q"])[:Rp], c)
+        assert np.array_equal(untile_mx_scales(u8_np(fus["s"]), R_cap, 2 * F)[:Rp], s_)
+        if col:
+            ct, st = OQ.quantize_mx(dgu.T, "e5m2")
+            assert np.array_equal(u8_np(fus["c"])[:, :Rp], ct)
+            assert np.array_equal(untile_mx_scales(u8_np(fus["cs"]), 2 * F, R_cap)[:, :Rp // 32], st)
+        else:
+            assert torch.all(fus["c"] == 0xAB)
 
 
 @pytest.mark.parametrize("mode", ["mx", "mx_col", "tensor", "nvfp4"])
