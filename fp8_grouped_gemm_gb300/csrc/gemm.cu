@@ -393,9 +393,9 @@ __device__ __forceinline__ void epilogue_swiglu(const GemmParams& p, const uint3
     uint32_t am2 = 0;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const float h0 = swiglu_bf16(bf(r[c][2 * i]), bf(r[2 + c][2 * i]));
-      const float h1 = swiglu_bf16(bf(r[c][2 * i + 1]), bf(r[2 + c][2 * i + 1]));
-      hp[i] = pack_bf16x2(h0, h1);
+      // (the pair conversion rounds each value to bf16 once)
+      hp[i] = pack_bf16x2(swiglu_f32(bf(r[c][2 * i]), bf(r[2 + c][2 * i])),
+                          swiglu_f32(bf(r[c][2 * i + 1]), bf(r[2 + c][2 * i + 1])));
       am2 = absmax_bf16x2(am2, hp[i]);
     }
     if (KIND == kKindNV) {
@@ -503,8 +503,8 @@ __device__ __forceinline__ void epilogue_dswiglu(const GemmParams& p, uint32_t t
       for (int i = 0; i < 4; ++i) {
         const int k = 8 * q + 2 * i;
         float g0, g1, u0, u1;
-        dswiglu_bf16(d[k], bf16_lo(gw[i]), bf16_lo(uw[i]), g0, u0);
-        dswiglu_bf16(d[k + 1], bf16_hi(gw[i]), bf16_hi(uw[i]), g1, u1);
+        dswiglu_f32(d[k], bf16_lo(gw[i]), bf16_lo(uw[i]), g0, u0);
+        dswiglu_f32(d[k + 1], bf16_hi(gw[i]), bf16_hi(uw[i]), g1, u1);
         dgp[4 * q + i] = pack_bf16x2(g0, g1);
         dup[4 * q + i] = pack_bf16x2(u0, u1);
         am2 = absmax_bf16x2(absmax_bf16x2(am2, dgp[4 * q + i]), dup[4 * q + i]);
@@ -576,8 +576,8 @@ __device__ __forceinline__ void epilogue_dswiglu_mx(const GemmParams& p, uint32_
       for (int i = 0; i < 4; ++i) {
         const uint32_t d = dhp[4 * q + i];
         float g0, g1, u0, u1;
-        dswiglu_bf16(bf16_lo(d), bf16_lo(gw[i]), bf16_lo(uw[i]), g0, u0);
-        dswiglu_bf16(bf16_hi(d), bf16_hi(gw[i]), bf16_hi(uw[i]), g1, u1);
+        dswiglu_f32(bf16_lo(d), bf16_lo(gw[i]), bf16_lo(uw[i]), g0, u0);
+        dswiglu_f32(bf16_hi(d), bf16_hi(gw[i]), bf16_hi(uw[i]), g1, u1);
         dg[4 * q + i] = pack_bf16x2(g0, g1);
         du[4 * q + i] = pack_bf16x2(u0, u1);
       }
