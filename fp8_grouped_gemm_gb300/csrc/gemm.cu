@@ -449,11 +449,41 @@ __device__ __forceinline__ void dswiglu_load_gu(const GemmParams& p, int64_t oro
   }
 }
 
+// g / u staging of the per-tensor dSwiGLU epilogue (2-CTA kernel): a warp's
+// 4 KB slot holds, for its 32 rows and 32 columns, g (bytes 0..63 of a row's
+// 128) and u (64..127) in 16-byte units, unit j of row r at r * 128 + 16 (j ^
+// (r & 7)). Each copy instruction moves four whole row segments (8 lines, 64
+// bytes each) where a lane-per-row load would touch 32 lines for 16 bytes each;
+// the swizzle keeps both the copies and the lanes' row reads free of bank
+// conflicts.
+constexpr uint32_t kGuSlot = 4096;
+__device__ __forceinline__ void gu_stage_issue(const GemmParams& p, uint32_t slot, int64_t row0, int64_t col,
+                                               uint32_t lane) {
+  const uint32_t j = lane & 7;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t r = 4 * i + (lane >> 3);
+    const uint16_t* src = p.gu_in + (row0 + r) * 2 * p.F + col + (j >> 2) * p.F + (j & 3) * 8;
+    ptx::cp_async16(slot + r * 128 + 16 * (j ^ (r & 7)), src);
+  }
+  ptx::cp_async_commit();
+}
+// the lane's row of a landed slot: g and u of columns 0..15 and 16..31
+__device__ __forceinline__ void gu_stage_read(const uint8_t* slot, uint32_t lane, uint4 (&g0)[2], uint4 (&u0)[2],
+                                              uint4 (&g1)[2], uint4 (&u1)[2]) {
+  const uint8_t* row = slot + lane * 128;
+  auto unit = [&](uint32_t jj) { return *reinterpret_cast<const uint4*>(row + 16 * (jj ^ (lane & 7))); };
+  g0[0] = unit(0); g0[1] = unit(1); g1[0] = unit(2); g1[1] = unit(3);
+  u0[0] = unit(4); u0[1] = unit(5); u1[0] = unit(6); u1[1] = unit(7);
+}
+
 // dSwiGLU epilogue of the down-projection dgrad (per-tensor) for one thread's
 // row `orow` and columns col0..col0+127, in 8 chunks of 16: each reads its
 // accumulator columns from tensor memory (`tcol` = the first) and the matching
 // g and u of the forward's gu (chunk 0 already in gq / uq, requested by the
-// caller before the accumulator was ready; further chunks in pairs, 32 columns per request);
+// caller before the accumulator was ready; further chunks in pairs, 32 columns
+// per request), or with `gslot` (a warp's staging slot, shared-memory address;
+// its first 32 columns already requested by the caller) through the slot;
 // dh = bf16(acc * alpha), [dG | dU] = dswiglu_bf16, quantised with *p.h_scale
 // (max |.| into tam). Codes and (p.out set) dh go out through TMA stores from
 // the warp's staging buffer; the optional bf16 dG | dU by plain stores.
@@ -461,7 +491,7 @@ __device__ __forceinline__ void dswiglu_load_gu(const GemmParams& p, int64_t oro
 __device__ __forceinline__ void epilogue_dswiglu(const GemmParams& p, uint32_t tcol, float alpha, int64_t orow,
                                                  int64_t col0, Stager& sg, const CUtensorMap* tmO,
                                                  const CUtensorMap* tmH, int32_t y0, uint32_t lane, uint32_t& tam,
-                                                 uint4 (&gq)[2], uint4 (&uq)[2]) {
+                                                 uint4 (&gq)[2], uint4 (&uq)[2], uint8_t* gslot = nullptr) {
   auto stage = [&](int j, uint4 v, const CUtensorMap* m, int64_t x) { sg.put(lane, j, v, m, x, y0, 64); };
   const int64_t F = p.F;
   const float ts = *p.h_scale;
@@ -471,8 +501,19 @@ __device__ __forceinline__ void epilogue_dswiglu(const GemmParams& p, uint32_t t
   uint4 g2[2], u2[2];          // the odd chunk of a pair, requested with the even one
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
-    if (c > 0 && (c & 1) == 0) dswiglu_load_gu(p, orow, col0, c, gq, uq);
-    if ((c & 1) == 0) dswiglu_load_gu(p, orow, col0, c + 1, g2, u2);
+    if (gslot) {
+      if ((c & 1) == 0) {
+        // this pair of chunks from the slot, then the next pair into it
+        ptx::cp_async_wait_all();
+        __syncwarp();
+        gu_stage_read(gslot, lane, gq, uq, g2, u2);
+        __syncwarp();
+        if (c < 6) gu_stage_issue(p, ptx::smem_u32(gslot), orow - lane, col0 + 16 * (c + 2), lane);
+      }
+    } else {
+      if (c > 0 && (c & 1) == 0) dswiglu_load_gu(p, orow, col0, c, gq, uq);
+      if ((c & 1) == 0) dswiglu_load_gu(p, orow, col0, c + 1, g2, u2);
+    }
     if (c & 1) {
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
@@ -994,7 +1035,10 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
 //     has no room for a second accumulator: the epilogue moves it to registers
 //     and releases it before storing.
 constexpr int PSTAGES = 6;                                     // per-tensor and MX; NVFP4 5
-__host__ __device__ constexpr int pstages_of(int kind) { return kind == kKindNV ? 5 : PSTAGES; }
+// (the per-tensor dSwiGLU instantiation gives one stage to its g / u staging slots)
+__host__ __device__ constexpr int pstages_of(int kind, bool dsw = false) {
+  return (kind == kKindNV || dsw) ? 5 : PSTAGES;
+}
 constexpr uint32_t kPairTile = 128 * 128;                      // bytes of one A or B half tile
 // block-scale bytes per stage for this CTA's A rows (B: twice, both halves):
 // MX one 512-byte chunk per 128 rows, NVFP4 four (the 4 MMAs of a 256-element stage)
@@ -1002,8 +1046,9 @@ __host__ __device__ constexpr uint32_t pair_sfa_bytes(int kind) {
   return kind == kKindMX ? 512u : (kind == kKindNV ? 2048u : 0u);
 }
 __host__ __device__ constexpr uint32_t pair_sf_bytes(int kind) { return 3 * pair_sfa_bytes(kind); }
-__host__ __device__ constexpr size_t pair_smem(int kind) {
-  return 1024 + pstages_of(kind) * (2 * kPairTile + pair_sf_bytes(kind)) + 8 * kStageOut + 256 + (2 * kMaxE + 16) * 4;
+__host__ __device__ constexpr size_t pair_smem(int kind, bool dsw = false) {
+  return 1024 + pstages_of(kind, dsw) * (2 * kPairTile + pair_sf_bytes(kind)) + 8 * kStageOut +
+         (dsw ? 8 * kGuSlot : 0) + 256 + (2 * kMaxE + 16) * 4;
 }
 // tensor-memory columns: accumulator(s), then the scale slots of every stage
 // (4 columns per chunk of A, 8 per chunk pair of B; NVFP4: 496 columns in all)
@@ -1060,7 +1105,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   constexpr bool MX = KIND == kKindMX;
   constexpr bool NV = KIND == kKindNV;
   constexpr bool BS = MX || NV;                    // block scales through tensor memory
-  constexpr int PST = pstages_of(KIND);
+  constexpr int PST = pstages_of(KIND, DSW);
   constexpr uint32_t kSfa = pair_sfa_bytes(KIND), kSfb = 2 * kSfa, kCh = kSfa / 512;   // chunks per 128 rows
   constexpr uint32_t kSfbCol = pair_sfb_col(KIND);
   constexpr int kAccBufs = BS ? 1 : 2;             // block scales: their slots leave room for one accumulator
@@ -1072,7 +1117,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* sOut = sB + PST * kPairTile;            // [8 warps][32 rows][64 bytes] epilogue staging
   uint8_t* sSFA = sOut + 8 * kStageOut;            // block scales: [stage] chunks of this CTA's A rows
   uint8_t* sSFB = sSFA + PST * kSfa;               // block scales: [stage] chunks of both B halves
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + 8 * kStageOut + PST * pair_sf_bytes(KIND));
+  uint8_t* sGU = sOut + 8 * kStageOut + PST * pair_sf_bytes(KIND);   // dSwiGLU: [8 warps] g / u slots
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sGU + (DSW ? 8 * kGuSlot : 0));
   uint64_t* full = bars;
   uint64_t* empty = bars + PST;
   uint64_t* tmem_full = bars + 2 * PST;            // [2]
@@ -1279,7 +1325,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       const uint32_t a = tc % kAccBufs, aph = (tc / kAccBufs) & 1;
       uint4 gq[2], uq[2];    // dSwiGLU: the first g / u chunk, requested before the accumulator is ready
-      if (DSW && store) dswiglu_load_gu(p, orow, col0, 0, gq, uq);
+      uint8_t* gslot = sGU + (warp - 2) * kGuSlot;
+      if (DSW && store) gu_stage_issue(p, ptx::smem_u32(gslot), orow - lane, col0, lane);
       if (__any_sync(0xFFFFFFFFu, *s_abort != 0)) break;
       const bool got = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&tmem_full[a], aph, p.wait_ns));
       if (!got) {
@@ -1295,7 +1342,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (store)
           epilogue_dswiglu(p, tbase + half * (BN / 2), 1.0f / (p.sa[0] * p.sb[tl.e]), orow, col0,
                            sg, &tmO, &tmH, (int32_t)(tl.out_row + 128 * rank + q * 32),
-                           lane, h_tam, gq, uq);
+                           lane, h_tam, gq, uq, gslot);
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive_cluster(a ? empty_remote1 : empty_remote0);
@@ -1324,6 +1371,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int o = 16; o > 0; o >>= 1) h_tam = max(h_tam, __shfl_xor_sync(0xFFFFFFFFu, h_tam, o));
       if (lane == 0) atomic_max_nonneg(p.h_amax, __uint_as_float(h_tam));
     }
+    if (DSW) ptx::cp_async_wait_all();   // (a timeout can leave a g / u copy in flight)
   }
   if (warp >= 2 && lane == 0) ptx::bulk_wait0();   // this warp's TMA stores are complete
   __syncthreads();
@@ -1340,7 +1388,7 @@ template <int MODE, int KIND, bool DSW = false>
 int launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const CUtensorMap& tsfa,
                      const CUtensorMap& tsfb, const CUtensorMap& th, const GemmParams& p, cudaStream_t s) {
   auto kern = grouped_gemm_pair_kernel<MODE, KIND, DSW>;
-  constexpr size_t kSmem = pair_smem(KIND);
+  constexpr size_t kSmem = pair_smem(KIND, DSW);
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
