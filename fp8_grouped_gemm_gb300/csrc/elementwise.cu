@@ -514,9 +514,9 @@ __global__ void __launch_bounds__(256) swiglu_h_kernel(const uint16_t* __restric
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
   const int64_t r = (int64_t)blockIdx.x * kWarps + warp;
-  if (r >= *rows_used) return;
+  const bool live = r < *rows_used;      // (all warps stay for the CTA's amax reduction)
   uint32_t tam = 0;
-  for (int c0 = 0; c0 < F; c0 += 1024) {
+  for (int c0 = 0; live && c0 < F; c0 += 1024) {
     const int c = c0 + 32 * lane;
     if (c < F) {
       float g[32], u[32], hv[32];
@@ -528,8 +528,7 @@ __global__ void __launch_bounds__(256) swiglu_h_kernel(const uint16_t* __restric
       store_bf16x32(h + r * F + c, hv);
     }
   }
-  tam = warp_max_u32(tam);
-  if (lane == 0) atomic_max_nonneg(amax, __uint_as_float(tam));
+  cta_amax_atomic(tam, amax);
 }
 
 // [dG | dU] = dSwiGLU(dh, g, u) (bf16, as the quantising kernels round them)
@@ -540,9 +539,9 @@ __global__ void __launch_bounds__(256) dswiglu_dgu_kernel(const uint16_t* __rest
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
   const int64_t r = (int64_t)blockIdx.x * kWarps + warp;
-  if (r >= *rows_used) return;
+  const bool live = r < *rows_used;      // (all warps stay for the CTA's amax reduction)
   uint32_t tam = 0;
-  for (int c0 = 0; c0 < F; c0 += 1024) {
+  for (int c0 = 0; live && c0 < F; c0 += 1024) {
     const int c = c0 + 32 * lane;
     if (c < F) {
       float d[32], g[32], u[32], dg[32], du[32];
@@ -556,8 +555,7 @@ __global__ void __launch_bounds__(256) dswiglu_dgu_kernel(const uint16_t* __rest
       store_bf16x32(dgu + r * 2 * F + F + c, du);
     }
   }
-  tam = warp_max_u32(tam);
-  if (lane == 0) atomic_max_nonneg(amax, __uint_as_float(tam));
+  cta_amax_atomic(tam, amax);
 }
 
 // max |x| over the rows [0, *rows_used) of a bf16 [rows, C] matrix: one warp

@@ -344,9 +344,17 @@ __global__ void __launch_bounds__(256, 4) permute_quant_kernel(PermuteArgs a) {
   }
   }
   if (SC == MGQ_TENSOR_F32 && a.amax_out) {
+    // one atomic per CTA (every warp of a token CTA gets here): thousands of
+    // same-address atomics would queue at one L2 slice
+    __shared__ uint32_t s_am[8];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) tamax = max(tamax, __shfl_xor_sync(0xFFFFFFFFu, tamax, o));
-    if (lane == 0) atomic_max_nonneg(a.amax_out, __uint_as_float(tamax));
+    if (lane == 0) s_am[warp] = tamax;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int w = 1; w < 8; ++w) tamax = max(tamax, s_am[w]);
+      atomic_max_nonneg(a.amax_out, __uint_as_float(tamax));
+    }
   }
 }
 

@@ -1025,14 +1025,15 @@ def test_amax_history_update(mgq):
         assert torch.count_nonzero(amax).item() == 0
 
 
-@pytest.mark.parametrize("scaling", ["tensor", "mx", "mx_col", "nvfp4"])
+@pytest.mark.parametrize("scaling", ["tensor", "mx", "mx_col", "mx_col_e5m2_floor", "nvfp4"])
 def test_gemm_fwd_swiglu_equals_separate_steps(mgq, scaling):
     """The gate/up GEMM with SwiGLU + quantisation in its epilogue writes the
     same bytes as grouped_gemm_fwd followed by swiglu_quantize: g | u, h, the
     h codes and scales, the per-tensor amax and (mx_col) the MX column-wise
-    copy of h (groups of 128 and 384 rows, an empty group, pair tiles reaching
-    past a group)."""
-    col = scaling == "mx_col"
+    copy of h, also with e5m2 codes and the OCP floor exponent (groups of 128
+    and 384 rows, an empty group, pair tiles reaching past a group)."""
+    col = scaling.startswith("mx_col")
+    hfmt, hmode = ("e5m2", "floor") if scaling.endswith("floor") else ("e4m3", "rceil")
     scaling = "mx" if col else scaling
     rng = np.random.default_rng(31)
     dev = torch.device(DEV)
@@ -1080,7 +1081,9 @@ def test_gemm_fwd_swiglu_equals_separate_steps(mgq, scaling):
         o["c"] = torch.full((F, R_cap), 0xAB, dtype=torch.uint8, device=dev)
         o["cs"] = torch.full((mgq.mx_scale_bytes(F, R_cap),), 0xCD, dtype=torch.uint8, device=dev)
         if sc == mgq.MX32_E8M0:
-            o["q"] = mgq.qdesc(mgq.E4M3, sc, o["hq"], o["hs"], *((o["c"], o["cs"]) if col else (None, None)))
+            o["q"] = mgq.qdesc(mgq.E5M2 if hfmt == "e5m2" else mgq.E4M3, sc, o["hq"], o["hs"],
+                               *((o["c"], o["cs"]) if col else (None, None)),
+                               e8m0_mode=mgq.FLOOR if hmode == "floor" else mgq.RCEIL)
         elif nv:   # s_g is written to ts, the amax (zeroed by the call) to am
             o["q"] = mgq.qdesc(mgq.E2M1, sc, o["hq"], o["hs"], tensor_scale=o["ts"], amax_out=o["am"])
         else:
@@ -1108,14 +1111,17 @@ def test_gemm_fwd_swiglu_equals_separate_steps(mgq, scaling):
     gu = bf16_np(sep["gu"])[:Rp]
     hf = bf16_np(fus["h"])[:Rp]
     check_elementwise(OL.swiglu(gu, F), hf, "swiglu")
-    if col:   # the column-wise copy against the oracle: 32-row blocks inside the groups
+    if col:   # both copies against the oracle (the columns: 32-row blocks inside the groups)
+        c_, s_ = OQ.quantize_mx(hf, hfmt, hmode)
+        assert np.array_equal(u8_np(fus["hq"])[:Rp], c_)
+        assert np.array_equal(untile_mx_scales(u8_np(fus["hs"]), R_cap, F)[:Rp], s_)
         assert torch.all(fus["c"][:, Rp:] == 0xAB)
-        ct, st = OQ.quantize_mx(hf.T, "e4m3")
+        ct, st = OQ.quantize_mx(hf.T, hfmt, hmode)
         assert np.array_equal(u8_np(fus["c"])[:, :Rp], ct)
         assert np.array_equal(untile_mx_scales(u8_np(fus["cs"]), F, R_cap)[:, :Rp // 32], st)
 
 
-@pytest.mark.parametrize("w_layout", ["mn_major", "k_major", "mx", "mx_col"])
+@pytest.mark.parametrize("w_layout", ["mn_major", "k_major", "mx", "mx_col", "mx_col_floor"])
 def test_gemm_dgrad_dswiglu_equals_separate_steps(mgq, w_layout):
     """The down-projection dgrad with dSwiGLU + quantisation in its epilogue
     writes the same bytes as grouped_gemm_dgrad followed by dswiglu_quantize
@@ -1123,7 +1129,8 @@ def test_gemm_dgrad_dswiglu_equals_separate_steps(mgq, w_layout):
     copy; MX e5m2 gradients, rows only or with the column-wise copy; an empty
     group, pair tiles reaching past a group)."""
     mx = w_layout.startswith("mx")
-    col = w_layout == "mx_col"
+    col = w_layout.startswith("mx_col")
+    mode = "floor" if w_layout.endswith("floor") else "rceil"
     rng = np.random.default_rng(37)
     dev = torch.device(DEV)
     offs = np.array([0, 128, 128, 512, 640], dtype=np.int32)
@@ -1158,7 +1165,8 @@ def test_gemm_dgrad_dswiglu_equals_separate_steps(mgq, w_layout):
                  ts=torch.tensor([5000.0], device=dev), am=torch.zeros(1, device=dev))
         if mx:
             o["qd"] = mgq.qdesc(mgq.E5M2, mgq.MX32_E8M0, o["q"], o["s"],
-                                *((o["c"], o["cs"]) if col else (None, None)))
+                                *((o["c"], o["cs"]) if col else (None, None)),
+                                e8m0_mode=mgq.FLOOR if mode == "floor" else mgq.RCEIL)
         else:
             o["qd"] = mgq.qdesc(mgq.E5M2, mgq.TENSOR_F32, o["q"], None, None, None, o["ts"], o["am"])
         return o
@@ -1184,11 +1192,11 @@ def test_gemm_dgrad_dswiglu_equals_separate_steps(mgq, w_layout):
     dgu = bf16_np(fus["dgu"])[:Rp]
     check_elementwise(OL.dswiglu(bf16_np(sep["dh"])[:Rp], bf16_np(gu)[:Rp], F), dgu, "dswiglu")
     if mx:    # the codes against the oracle's MX blocks (columns: 32 rows inside the groups)
-        c, s_ = OQ.quantize_mx(dgu, "e5m2")
+        c, s_ = OQ.quantize_mx(dgu, "e5m2", mode)
         assert np.array_equal(u8_np(fus["q"])[:Rp], c)
         assert np.array_equal(untile_mx_scales(u8_np(fus["s"]), R_cap, 2 * F)[:Rp], s_)
         if col:
-            ct, st = OQ.quantize_mx(dgu.T, "e5m2")
+            ct, st = OQ.quantize_mx(dgu.T, "e5m2", mode)
             assert np.array_equal(u8_np(fus["c"])[:, :Rp], ct)
             assert np.array_equal(untile_mx_scales(u8_np(fus["cs"]), 2 * F, R_cap)[:, :Rp // 32], st)
         else:
