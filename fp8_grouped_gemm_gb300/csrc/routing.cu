@@ -171,10 +171,11 @@ __device__ __forceinline__ int resolve_row(const int32_t* __restrict__ idx, int3
 }
 
 // ---- fused permute + quantise ---------------------------------------------------
-// One warp per token row; lane l handles elements [32 l, 32 l + 32) of each
-// 1024-element slice, i.e. exactly one 32-element MX block. The row is read
-// once (16-byte loads) and its codes and scales are written to the k
-// destination rows.
+// One warp per token row, in 1024-element chunks: per tensor, lane l takes
+// 8-element runs 256 apart (fully coalesced loads); with block scales, lane l
+// takes the 32-element block [32 l, 32 l + 32) (one MX block, a quarter of a
+// 1x128 block). The row is read once and its codes and scales are written to
+// the k destination rows.
 
 struct PermuteArgs {
   const uint16_t* x;
@@ -217,15 +218,6 @@ __device__ __forceinline__ void token_rows(const PermuteArgs& a, int t, uint32_t
   for (int j = 0; j < 8; ++j) dest[j] = __shfl_sync(0xFFFFFFFFu, mine, j);
 }
 
-__device__ __forceinline__ void load_block32(const uint16_t* src, uint32_t (&w)[16]) {
-  const uint4* p = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 v = __ldg(p + q);
-    w[4 * q + 0] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
-  }
-}
-
 template <int SC, int DT>
 __global__ void __launch_bounds__(256, 4) permute_quant_kernel(PermuteArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -254,15 +246,26 @@ __global__ void __launch_bounds__(256, 4) permute_quant_kernel(PermuteArgs a) {
   }
   // token CTAs stride over the tokens (a few waves' worth of CTAs, no tail
   // wave); a warp keeps the next 1024-element chunk in flight, across token
-  // boundaries too
+  // boundaries too. Lane l holds the runs of G elements at 32 G q + G l
+  // (q < 32 / G). G = 8 (per tensor): each 16-byte load of the warp covers 512
+  // contiguous bytes. G = 32 (block scales): a lane holds one whole 32-block,
+  // so a chunk needs one scale computation per lane (a 1x128 block: 4 lanes).
+  constexpr int G = SC == MGQ_TENSOR_F32 ? 8 : 32;
+  constexpr int NQ = 32 / G;          // runs per lane and chunk
+  constexpr int WQ = G / 2;           // bf16-pair words per run
   const int tstride = a.token_blocks * 8;
   auto load_chunk = [&](int tt, int c0, uint32_t (&w)[16]) {
-    const int c = c0 + lane * 32;
-    if (c < H) {
-      load_block32(a.x + (int64_t)tt * H + c, w);
-    } else {
+    const uint16_t* row = a.x + (int64_t)tt * H + c0 + lane * G;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) w[i] = 0;
+    for (int q = 0; q < NQ; ++q) {
+      const bool in = c0 + 32 * G * q + (int)lane * G < H;
+#pragma unroll
+      for (int u = 0; u < G / 8; ++u) {
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (in) v = __ldg(reinterpret_cast<const uint4*>(row + 32 * G * q + 8 * u));
+        uint32_t* d = &w[WQ * q + 4 * u];
+        d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
+      }
     }
   };
   const float ts = (SC == MGQ_TENSOR_F32) ? a.tensor_scale[0] : 1.0f;
@@ -274,71 +277,80 @@ __global__ void __launch_bounds__(256, 4) permute_quant_kernel(PermuteArgs a) {
   int dest[8];
   token_rows(a, t, lane, dest);
   for (int c0 = 0; c0 < H; c0 += 1024) {
-    const int c = c0 + lane * 32;
-    const bool active = c < H;       // every lane stays in the loop (shuffles below)
     uint32_t w[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) w[i] = wnext[i];
     if (c0 + 1024 < H) load_chunk(t, c0 + 1024, wnext);
     else if (t + tstride < a.T) load_chunk(t + tstride, 0, wnext);
-    uint32_t am2 = 0;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) am2 = absmax_bf16x2(am2, w[i]);
-    uint32_t amax_bits = fold_bf16x2(am2);
-    float mult;
-    uint32_t scode = 0;
-    float sinv = 0.0f;
-    if (SC == MGQ_MX32_E8M0) {
-      int e = mx_exponent(amax_bits, FmtInfo<DT>::emax, a.e8m0_rceil != 0);
-      mult = mx_multiplier(e);
-      scode = mx_scale_code(e);
-    } else if (SC == MGQ_BLK_1x128_F32) {
-      // amax over 128 elements = 4 lanes
-      uint32_t m = amax_bits;
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-      float am = __uint_as_float(m);
-      float s = (m == 0) ? 1.0f : __fdiv_rn(FmtInfo<DT>::fmax, am);
-      if (isinf(s)) s = 3.40282347e38f;
-      mult = s;
-      sinv = __fdiv_rn(1.0f, s);
-    } else {  // MGQ_TENSOR_F32
-      mult = ts;
-      tamax = max(tamax, amax_bits);
-    }
-    uint32_t cw[8];
+    for (int q = 0; q < NQ; ++q) {
+      const int c = c0 + 32 * G * q + lane * G;
+      const bool active = c < H;     // every lane stays in the loop (shuffles below)
+      const uint32_t* wq = &w[WQ * q];
+      uint32_t am2 = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float v0 = __fmul_rn(bf16_lo(w[2 * i]), mult), v1 = __fmul_rn(bf16_hi(w[2 * i]), mult);
-      float v2 = __fmul_rn(bf16_lo(w[2 * i + 1]), mult), v3 = __fmul_rn(bf16_hi(w[2 * i + 1]), mult);
-      cw[i] = cvt_fp8x4<DT>(v0, v1, v2, v3);
-    }
-    // gather the 4 scale bytes of lanes 4j..4j+3 into lane 4j
-    uint32_t s4 = 0;
-    if (SC == MGQ_MX32_E8M0) {
-      uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, scode, 1);
-      uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, scode, 2);
-      uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, scode, 3);
-      s4 = scode | (b1 << 8) | (b2 << 16) | (b3 << 24);
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (j >= a.k || !active) break;
-      int r = dest[j];
-      if (r < 0) continue;
-      uint4* dst = reinterpret_cast<uint4*>(a.codes + (int64_t)r * H + c);
-      dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-      dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-      if (a.out_bf16) {
-        uint4* ob = reinterpret_cast<uint4*>(a.out_bf16 + (int64_t)r * H + c);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) ob[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-      }
+      for (int i = 0; i < WQ; ++i) am2 = absmax_bf16x2(am2, wq[i]);
+      uint32_t amax_bits = fold_bf16x2(am2);
+      float mult;
+      uint32_t scode = 0;
+      float sinv = 0.0f;
       if (SC == MGQ_MX32_E8M0) {
-        if ((lane & 3) == 0)
-          *reinterpret_cast<uint32_t*>(a.scales + tiled_scale_offset(r, c / 32, H / 128)) = s4;
+        const int e = mx_exponent(amax_bits, FmtInfo<DT>::emax, a.e8m0_rceil != 0);
+        mult = mx_multiplier(e);
+        scode = mx_scale_code(e);
       } else if (SC == MGQ_BLK_1x128_F32) {
-        if ((lane & 3) == 0) reinterpret_cast<float*>(a.scales)[(int64_t)(c / 128) * a.R_cap + r] = sinv;
+        // amax over 128 elements = 4 lanes
+        uint32_t m = amax_bits;
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+        const float am = __uint_as_float(m);
+        float sc = (m == 0) ? 1.0f : __fdiv_rn(FmtInfo<DT>::fmax, am);
+        if (isinf(sc)) sc = 3.40282347e38f;
+        mult = sc;
+        sinv = __fdiv_rn(1.0f, sc);
+      } else {  // MGQ_TENSOR_F32
+        mult = ts;
+        tamax = max(tamax, amax_bits);
+      }
+      uint32_t cw[G / 4];
+#pragma unroll
+      for (int i = 0; i < G / 4; ++i) {
+        const float v0 = __fmul_rn(bf16_lo(wq[2 * i]), mult), v1 = __fmul_rn(bf16_hi(wq[2 * i]), mult);
+        const float v2 = __fmul_rn(bf16_lo(wq[2 * i + 1]), mult), v3 = __fmul_rn(bf16_hi(wq[2 * i + 1]), mult);
+        cw[i] = cvt_fp8x4<DT>(v0, v1, v2, v3);
+      }
+      // MX: the 4 scale bytes of lanes 4j..4j+3 into lane 4j
+      uint32_t s4 = 0;
+      if (SC == MGQ_MX32_E8M0) {
+        const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, scode, 1);
+        const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, scode, 2);
+        const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, scode, 3);
+        s4 = scode | (b1 << 8) | (b2 << 16) | (b3 << 24);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j >= a.k || !active) break;
+        const int r = dest[j];
+        if (r < 0) continue;
+        uint8_t* dst = a.codes + (int64_t)r * H + c;
+        if (G == 8) {
+          *reinterpret_cast<uint2*>(dst) = make_uint2(cw[0], cw[1]);
+        } else {
+#pragma unroll
+          for (int u = 0; u < G / 16; ++u)
+            reinterpret_cast<uint4*>(dst)[u] = make_uint4(cw[4 * u], cw[4 * u + 1], cw[4 * u + 2], cw[4 * u + 3]);
+        }
+        if (a.out_bf16) {
+          uint4* ob = reinterpret_cast<uint4*>(a.out_bf16 + (int64_t)r * H + c);
+#pragma unroll
+          for (int u = 0; u < G / 8; ++u) ob[u] = make_uint4(wq[4 * u], wq[4 * u + 1], wq[4 * u + 2], wq[4 * u + 3]);
+        }
+        if (SC == MGQ_MX32_E8M0) {
+          if ((lane & 3) == 0)
+            *reinterpret_cast<uint32_t*>(a.scales + tiled_scale_offset(r, c / 32, H / 128)) = s4;
+        } else if (SC == MGQ_BLK_1x128_F32) {
+          if ((lane & 3) == 0) reinterpret_cast<float*>(a.scales)[(int64_t)(c / 128) * a.R_cap + r] = sinv;
+        }
       }
     }
   }
