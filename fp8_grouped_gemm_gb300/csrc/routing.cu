@@ -172,10 +172,10 @@ __device__ __forceinline__ int resolve_row(const int32_t* __restrict__ idx, int3
 
 // ---- fused permute + quantise ---------------------------------------------------
 // One warp per token row, in 1024-element chunks: per tensor, lane l takes
-// 8-element runs 256 apart (fully coalesced loads); with block scales, lane l
-// takes the 32-element block [32 l, 32 l + 32) (one MX block, a quarter of a
-// 1x128 block). The row is read once and its codes and scales are written to
-// the k destination rows.
+// 8-element runs 256 apart (fully coalesced loads); with block scales,
+// 16-element runs 512 apart (half an MX block, an eighth of a 1x128 block).
+// The row is read once and its codes and scales are written to the k
+// destination rows.
 
 struct PermuteArgs {
   const uint16_t* x;
@@ -248,11 +248,13 @@ __global__ void __launch_bounds__(256, 4) permute_quant_kernel(PermuteArgs a) {
   // wave); a warp keeps the next 1024-element chunk in flight, across token
   // boundaries too. Lane l holds the runs of G elements at 32 G q + G l
   // (q < 32 / G). G = 8 (per tensor): each 16-byte load of the warp covers 512
-  // contiguous bytes. G = 32 (block scales): a lane holds one whole 32-block,
-  // so a chunk needs one scale computation per lane (a 1x128 block: 4 lanes).
-  constexpr int G = SC == MGQ_TENSOR_F32 ? 8 : 32;
+  // contiguous bytes. G = 16 (block scales): a 32-block spans 2 lanes (a 1x128
+  // block 8), so a chunk needs two scale computations per lane, against four
+  // with G = 8; the warp's loads cover 1 KB (8 lines) each.
+  constexpr int G = SC == MGQ_TENSOR_F32 ? 8 : 16;
   constexpr int NQ = 32 / G;          // runs per lane and chunk
   constexpr int WQ = G / 2;           // bf16-pair words per run
+  constexpr int LB = 32 / G;          // lanes per 32-element block
   const int tstride = a.token_blocks * 8;
   auto load_chunk = [&](int tt, int c0, uint32_t (&w)[16]) {
     const uint16_t* row = a.x + (int64_t)tt * H + c0 + lane * G;
@@ -295,14 +297,16 @@ __global__ void __launch_bounds__(256, 4) permute_quant_kernel(PermuteArgs a) {
       uint32_t scode = 0;
       float sinv = 0.0f;
       if (SC == MGQ_MX32_E8M0) {
+#pragma unroll
+        for (int o = 1; o < LB; o <<= 1) amax_bits = max(amax_bits, __shfl_xor_sync(0xFFFFFFFFu, amax_bits, o));
         const int e = mx_exponent(amax_bits, FmtInfo<DT>::emax, a.e8m0_rceil != 0);
         mult = mx_multiplier(e);
         scode = mx_scale_code(e);
       } else if (SC == MGQ_BLK_1x128_F32) {
-        // amax over 128 elements = 4 lanes
+        // amax over 128 elements = 4 LB lanes
         uint32_t m = amax_bits;
-        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+#pragma unroll
+        for (int o = 1; o < 4 * LB; o <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
         const float am = __uint_as_float(m);
         float sc = (m == 0) ? 1.0f : __fdiv_rn(FmtInfo<DT>::fmax, am);
         if (isinf(sc)) sc = 3.40282347e38f;
@@ -319,12 +323,12 @@ __global__ void __launch_bounds__(256, 4) permute_quant_kernel(PermuteArgs a) {
         const float v2 = __fmul_rn(bf16_lo(wq[2 * i + 1]), mult), v3 = __fmul_rn(bf16_hi(wq[2 * i + 1]), mult);
         cw[i] = cvt_fp8x4<DT>(v0, v1, v2, v3);
       }
-      // MX: the 4 scale bytes of lanes 4j..4j+3 into lane 4j
+      // MX: the 4 scale bytes of 4 consecutive blocks (lanes 4 LB j, + LB, ..) into lane 4 LB j
       uint32_t s4 = 0;
       if (SC == MGQ_MX32_E8M0) {
-        const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, scode, 1);
-        const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, scode, 2);
-        const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, scode, 3);
+        const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, scode, LB);
+        const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, scode, 2 * LB);
+        const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, scode, 3 * LB);
         s4 = scode | (b1 << 8) | (b2 << 16) | (b3 << 24);
       }
 #pragma unroll
@@ -346,10 +350,10 @@ __global__ void __launch_bounds__(256, 4) permute_quant_kernel(PermuteArgs a) {
           for (int u = 0; u < G / 8; ++u) ob[u] = make_uint4(wq[4 * u], wq[4 * u + 1], wq[4 * u + 2], wq[4 * u + 3]);
         }
         if (SC == MGQ_MX32_E8M0) {
-          if ((lane & 3) == 0)
+          if ((lane & (4 * LB - 1)) == 0)
             *reinterpret_cast<uint32_t*>(a.scales + tiled_scale_offset(r, c / 32, H / 128)) = s4;
         } else if (SC == MGQ_BLK_1x128_F32) {
-          if ((lane & 3) == 0) reinterpret_cast<float*>(a.scales)[(int64_t)(c / 128) * a.R_cap + r] = sinv;
+          if ((lane & (4 * LB - 1)) == 0) reinterpret_cast<float*>(a.scales)[(int64_t)(c / 128) * a.R_cap + r] = sinv;
         }
       }
     }
