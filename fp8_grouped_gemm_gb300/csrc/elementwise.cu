@@ -302,9 +302,23 @@ __global__ void __launch_bounds__(256, SC == MGQ_TENSOR_F32 ? 3 : 2) unpermute_b
     const uint16_t* drow = a.dout + (g / a.k) * H;
     const uint16_t* yrow = a.y + (int64_t)r * H;
     float dp = 0.0f;
+    // per tensor (codes element by element), lane l takes the 8-element runs
+    // 256 q + 8 l of a 1024-element chunk, so each 16-byte load of the warp
+    // covers 512 contiguous bytes; with block scales it takes its own block(s)
+    constexpr bool kRuns = SC == MGQ_TENSOR_F32;
     auto load = [&](int c0, uint4 (&d)[4], uint4 (&y)[4]) {
       const int c = c0 + 32 * (int)lane;
-      if (c < H) {
+      if (kRuns) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int cq = c0 + 256 * q + 8 * (int)lane;
+          d[q] = y[q] = make_uint4(0, 0, 0, 0);
+          if (cq < H) {
+            d[q] = __ldg(reinterpret_cast<const uint4*>(drow + cq));
+            y[q] = __ldg(reinterpret_cast<const uint4*>(yrow + cq));
+          }
+        }
+      } else if (c < H) {
         const uint4* pd = reinterpret_cast<const uint4*>(drow + c);
         const uint4* py = reinterpret_cast<const uint4*>(yrow + c);
 #pragma unroll
@@ -344,7 +358,15 @@ __global__ void __launch_bounds__(256, SC == MGQ_TENSOR_F32 ? 3 : 2) unpermute_b
         tam = max(tam, am);
         Block32 o;
         quantize32<SC, DT>(v, am, ts, a.rceil != 0, o);
-        if (c < H) store32<SC>(o, a.codes, a.scales, r, c, H, a.R_cap, lane);
+        if (kRuns) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int cq = c0 + 256 * q + 8 * (int)lane;
+            if (cq < H) *reinterpret_cast<uint2*>(a.codes + (int64_t)r * H + cq) = make_uint2(o.cw[2 * q], o.cw[2 * q + 1]);
+          }
+        } else if (c < H) {
+          store32<SC>(o, a.codes, a.scales, r, c, H, a.R_cap, lane);
+        }
       }
     };
     uint4 d0[4], y0[4], d1[4], y1[4];
