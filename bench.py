@@ -386,7 +386,7 @@ def sample_desc(rows, f_slice):
 
 
 REF_SAMPLE = (512, 1024)        # per --impl reference step (about a second on 16 cores)
-BASELINE_SAMPLE = (2048, 2048)  # the cpu_baseline of our own line (about 10 s)
+CPU_BASELINE_SAMPLE = (2048, 2048)  # the cpu_baseline of our own line (about 10 s)
 
 
 def config_of(w, args):
@@ -522,9 +522,9 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        dt, f = oracle_sample(w, *BASELINE_SAMPLE)
+        dt, f = oracle_sample(w, *CPU_BASELINE_SAMPLE)
         cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
-               "sample": sample_desc(*BASELINE_SAMPLE), "seconds": dt}
+               "sample": sample_desc(*CPU_BASELINE_SAMPLE), "seconds": dt}
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
