@@ -796,11 +796,12 @@ def test_unpermute_and_permute_bwd(mgq, T, E, k, H):
     check_elementwise(OR.permute_bwd(bf16_np(y), rim), bf16_np(dx), "permute_bwd")
 
 
+@pytest.mark.parametrize("H", [1024, 384])      # (384: a partial 1024-element chunk per row)
 @pytest.mark.parametrize("mode", ["tensor", "mx", "mx_col", "nvfp4", "nvfp4_col"])
-def test_unpermute_bwd_quantize(mgq, mode):
+def test_unpermute_bwd_quantize(mgq, mode, H):
     rng = np.random.default_rng(9)
     dev = torch.device(DEV)
-    T, E, k, H = 700, 8, 2, 1024
+    T, E, k = 700, 8, 2
     idx, rim, src, off, cnt = _layout(rng, T, E, k, dev)
     Rp = int(off[-1])
     R = Rp + 128
