@@ -1,8 +1,9 @@
 """Host-side wiring of ExpertLayer (no GPU): which steps each recipe fuses,
 the order of the calls of a step, and the kernel launches per step that
 bench.py reports (the training counts are those of the ncu launch lists of
-the three Mixtral-shaped training steps). The layer is built over CPU tensors;
-building the op list issues no call."""
+the three Mixtral-shaped training steps); and the binding's buffer-size
+helpers. The layer is built over CPU tensors; building the op list issues no
+call."""
 import pytest
 import torch
 
@@ -71,3 +72,22 @@ def test_unfused_mx_training_has_the_separate_swiglu_pass():
 def test_nvfp4_training_pads_groups_to_256_rows():
     lay, _ = _layer_and_ops("mixtral_fwdbwd_nvfp4")
     assert lay.align == L.ALIGN_NV_TRAIN == 256 and lay.R_cap % 256 == 0
+
+
+def test_buffer_sizes_bound_the_layouts():
+    """The binding's size helpers: r_cap holds the oracle's padded group layout
+    in the worst case, and the tiled-scale byte counts equal the length of the
+    128x4 tiling of [rows, ld / block] scales."""
+    import numpy as np
+    from fp8_grouped_gemm_gb300 import mgq
+    from oracle import routing as OR
+    from tests.layer_check import tile_mx_scales
+    rng = np.random.default_rng(5)
+    for T, E, k, align in [(1000, 8, 2, 128), (37, 16, 1, 32), (4096, 128, 8, 128), (5, 4, 4, 256)]:
+        idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+        _, _, off, _ = OR.permute_indices(idx, E, align)
+        rc = mgq.r_cap(T, k, E, align)
+        assert int(off[-1]) <= rc and rc % 128 == 0 and rc - (T * k + E * (align - 1)) < 128
+    for rows, ld in [(128, 128), (300, 512), (4096, 4096)]:
+        assert mgq.mx_scale_bytes(rows, ld) == tile_mx_scales(np.zeros((rows, ld // 32), np.uint8)).size
+        assert mgq.nv_scale_bytes(rows, ld) == tile_mx_scales(np.zeros((rows, ld // 16), np.uint8)).size
