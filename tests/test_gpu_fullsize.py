@@ -115,6 +115,133 @@ def test_mixtral_forward_full_size_sampled():
     check_elementwise(ref, bf16_np(lay.out[torch.from_numpy(tsel).to(DEV)]), "unpermute")
 
 
+@pytest.mark.parametrize("name", ["scout_fwd", "finegrained_fwd"])
+def test_blockwise_and_nvfp4_forward_full_size_sampled(name):
+    """The Scout-shaped blockwise FP8 forward (1x128 activations, 128x128
+    weights, Zipf loads with empty experts) and the fine-grained NVFP4 forward
+    (128 experts, top-8) at full size: routing in full; sampled rows of the X
+    and h codes and scales, every s_g (NVFP4); gate/up and down outputs at
+    sampled rows and columns against the oracle's GEMM on the identical
+    quantised inputs (blockwise weights requantised by the 128x128 slabs that
+    hold the sampled columns); SwiGLU from the GPU's own gate/up rows; the
+    combine of sampled tokens."""
+    from fp8_grouped_gemm_gb300 import layer as L
+    from fp8_grouped_gemm_gb300 import mgq
+    from fp8_grouped_gemm_gb300 import workloads as W
+    from tests.layer_check import _gpu_row_scales, _q_rows
+    w = W.WORKLOADS[name]
+    recipe = w.recipe
+    nv = recipe == "nvfp4"
+    E, H, F, k = w.E, w.H, w.F, w.k
+    rng = np.random.default_rng(3)
+    x = W.make_activations(w)
+    idx, probs = W.make_routing(w)
+    w1, w2 = _weights_on_device(w)
+    lay = L.ExpertLayer(w, DEV, keep_bf16=True)
+    assert not lay.train and lay.recipe == recipe
+    lay.quantize_weights(w1, w2)
+    lay.forward(x.to(DEV), torch.from_numpy(idx).to(DEV), torch.from_numpy(probs).to(DEV))
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    rim, src, off, cnt = OR.permute_indices(idx, E, lay.align)
+    Rp = int(off[-1])
+    assert np.array_equal(lay.offsets.cpu().numpy(), off)
+    assert np.array_equal(lay.counts.cpu().numpy(), cnt)
+    assert np.array_equal(lay.row_id_map.cpu().numpy(), rim)
+    assert np.array_equal(lay.src_row.cpu().numpy()[:Rp], src)
+    rows = _sample_rows(off, cnt, rng, n_random=2 if nv else 4)
+    rr = np.array([r for _, r in rows])
+    ee = np.array([e for e, _ in rows])
+    rrd = torch.from_numpy(rr).to(DEV)
+    toks = src[rr] // k
+    xf = bf16_np(x)
+    # X: the tensor's s_g (NVFP4) and the sampled rows' codes and scales
+    if nv:
+        sg_x = OQ.nvfp4_global_scale(np.max(np.abs(xf)))
+        assert float(lay.nv_sg[0].item()) == float(sg_x)
+        cx, sx = OQ.quantize_nvfp4(xf[toks], sg_x)
+        x_deq = OQ.dequantize_nvfp4(cx, sx, sg_x, H)
+    else:
+        cx, sx, x_deq = _q_rows(xf[toks], recipe)
+    assert np.array_equal(u8_np(lay.xq[rrd]), cx)
+    assert np.array_equal(_gpu_row_scales(lay, lay.xs, lay.R_cap, H, recipe)[rr], sx)
+
+    def weight_rows(wt, wscales, e, sel_rows, slot):
+        """Codes and dequantised values of rows `sel_rows` of expert e's weight
+        [N, K] (bf16 on the device), quantised here: NVFP4 with the s_g of the
+        whole expert (checked against the GPU's), blockwise through the
+        128x128 slabs holding the rows (their scales checked against the
+        GPU's)."""
+        we = wt[e]
+        if nv:
+            sg = OQ.nvfp4_global_scale(np.max(np.abs(bf16_np(we))))
+            assert float(lay.nv_sg[slot + e].item()) == float(sg)
+            c, sc = OQ.quantize_nvfp4(bf16_np(we[torch.from_numpy(sel_rows).to(DEV)]), sg)
+            return c, OQ.dequantize_nvfp4(c, sc, sg, we.shape[1])
+        gpu_si = wscales[e].cpu().numpy()                               # [N/128, K/128]
+        slabs = {}
+        for b in np.unique(sel_rows // 128):
+            c, si = OQ.quantize_block_128x128(bf16_np(we[128 * b:128 * b + 128]), "e4m3")
+            assert np.array_equal(gpu_si[b], si[0])
+            slabs[b] = (c, OQ.dequantize_block_128x128(c, si))
+        return (np.stack([slabs[n // 128][0][n % 128] for n in sel_rows]),
+                np.stack([slabs[n // 128][1][n % 128] for n in sel_rows]))
+
+    def sample_cols(n_total, n_blocks=3, per_block=8):
+        blocks = rng.choice(n_total // 128, n_blocks, replace=False)
+        return np.sort(np.concatenate([128 * b + rng.choice(128, per_block, replace=False) for b in blocks]))
+
+    # gate/up at sampled gate columns and the matching up columns
+    cols = sample_cols(F)
+    cols2 = np.concatenate([cols, cols + F])
+    gu_gpu = bf16_np(lay.gu[rrd])                                   # [S, 2F]
+    w1q_s = u8_np(lay.w1q[:, torch.from_numpy(cols2).to(DEV)])
+    refs, gots = [], []
+    for e in range(E):
+        sel = ee == e
+        if not sel.any():
+            continue
+        c, d = weight_rows(w1, lay.w1s, e, cols2, 2)
+        assert np.array_equal(w1q_s[e], c)
+        refs.append(x_deq[sel] @ d.T)
+        gots.append(gu_gpu[sel][:, cols2])
+    assert rel_fro(OF.round_to_bf16(np.concatenate(refs)), np.concatenate(gots)) <= GEMM_TOL_BF16
+    # SwiGLU of the GPU's gate/up rows; h codes from the GPU's h
+    h_gpu = bf16_np(lay.h_bf16[rrd])
+    check_elementwise(OL.swiglu(gu_gpu, F), h_gpu, "swiglu")
+    if nv:
+        # s_g of h from the GPU's whole h (the quantiser's input), reduced here in row chunks
+        h_all = max(float(np.max(np.abs(bf16_np(lay.h_bf16[r0:min(r0 + 32768, Rp)]))))
+                    for r0 in range(0, Rp, 32768))
+        sg_h = OQ.nvfp4_global_scale(h_all)
+        assert float(lay.nv_sg[1].item()) == float(sg_h)
+        ch, sh = OQ.quantize_nvfp4(h_gpu, sg_h)
+        h_deq = OQ.dequantize_nvfp4(ch, sh, sg_h, F)
+    else:
+        ch, sh, h_deq = _q_rows(h_gpu, recipe)
+    assert np.array_equal(u8_np(lay.hq[rrd]), ch)
+    assert np.array_equal(_gpu_row_scales(lay, lay.hs, lay.R_cap, F, recipe)[rr], sh)
+    # down projection at sampled columns
+    ocols = sample_cols(H)
+    y_gpu = bf16_np(lay.y[rrd])
+    w2q_s = u8_np(lay.w2q[:, torch.from_numpy(ocols).to(DEV)])
+    refs, gots = [], []
+    for e in range(E):
+        sel = ee == e
+        if not sel.any():
+            continue
+        c, d = weight_rows(w2, lay.w2s, e, ocols, 2 + E)
+        assert np.array_equal(w2q_s[e], c)
+        refs.append(h_deq[sel] @ d.T)
+        gots.append(y_gpu[sel][:, ocols])
+    assert rel_fro(OF.round_to_bf16(np.concatenate(refs)), np.concatenate(gots)) <= GEMM_TOL_BF16
+    # combine of sampled tokens from the GPU's expert outputs
+    tsel = np.unique(toks)[:64]
+    y_rows = bf16_np(lay.y[torch.from_numpy(rim[tsel].reshape(-1)).to(DEV)]).reshape(len(tsel), k, H)
+    ref = np.einsum("tk,tkh->th", probs[tsel].astype(np.float64), y_rows)
+    check_elementwise(ref, bf16_np(lay.out[torch.from_numpy(tsel).to(DEV)]), "unpermute")
+
+
 def test_mixtral_training_step_full_size_sampled():
     """The fwd+bwd step of the bench workload (hybrid e4m3/e5m2, delayed
     scaling), after two warm-up steps so the scales are non-trivial; sampled
