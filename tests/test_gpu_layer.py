@@ -222,8 +222,17 @@ def test_mxfp8_training_step_scaled_down():
     assert rel_fro(dp, lay.dprobs.cpu().numpy()) <= 1e-5
     dy2_r, dy2_c = row_col(dy32.astype(np.float64), "e5m2", lay.dy2q, lay.dy2s, lay.dy2col, lay.dy2cs)
     dh = bf16_np(lay.dh)[:Rp]
-    assert rel_fro(OF.round_to_bf16(OG.grouped_gemm_dgrad(dy2_r, w2_c, off)), dh) <= GEMM_TOL_BF16
-    assert rel_fro(OG.grouped_gemm_wgrad(dy2_c, h_c, off, E), lay.dw2.cpu().numpy()) <= GEMM_TOL_F32
+    dh_q = OG.grouped_gemm_dgrad(dy2_r, w2_c, off)
+    assert rel_fro(OF.round_to_bf16(dh_q), dh) <= GEMM_TOL_BF16
+    dw2_q = OG.grouped_gemm_wgrad(dy2_c, h_c, off, E)
+    assert rel_fro(dw2_q, lay.dw2.cpu().numpy()) <= GEMM_TOL_F32
+    # GEMMs with an e5m2 operand against the unquantised operands: at least
+    # 23 dB, and within 0.5 dB of the oracle's own quantised GEMM
+    for ref, q_oracle, got in [(OG.grouped_gemm_dgrad(dy32.astype(np.float64), w2f, off), dh_q, dh),
+                               (OG.grouped_gemm_wgrad(dy32.astype(np.float64), hg, off, E), dw2_q,
+                                lay.dw2.cpu().numpy().astype(np.float64))]:
+        s_gpu, s_orc = OG.sqnr_db(ref, got), OG.sqnr_db(ref, q_oracle)
+        assert s_gpu >= 23.0 and abs(s_gpu - s_orc) <= 0.5, (s_gpu, s_orc)
     dgu = bf16_np(lay.dgu_bf16)[:Rp]
     check_elementwise(OL.dswiglu(dh, gu, F), dgu, "dswiglu")
     dy1_r, dy1_c = row_col(dgu, "e5m2", lay.dy1q, lay.dy1s, lay.dy1col, lay.dy1cs)
