@@ -22,7 +22,7 @@ from __future__ import annotations
 import numpy as np
 
 
-def grouped_gemm_fwd(a, w, offsets, rows=None):
+def grouped_gemm_fwd(a, w, offsets):
     a = np.asarray(a, dtype=np.float64)
     w = np.asarray(w, dtype=np.float64)
     E, N, K = w.shape
@@ -60,15 +60,6 @@ def grouped_gemm_wgrad(dy, a, offsets, E, beta=0.0, dw_in=None):
     return out
 
 
-def grouped_gemm_fwd_rows(a_rows, w, expert_of_row):
-    """Forward for a sample of rows: a_rows [S, K], their experts [S]."""
-    a_rows = np.asarray(a_rows, dtype=np.float64)
-    out = np.empty((a_rows.shape[0], w.shape[1]), dtype=np.float64)
-    for i, e in enumerate(expert_of_row):
-        out[i] = np.asarray(w[e], dtype=np.float64) @ a_rows[i]
-    return out
-
-
 def sqnr_db(ref, q):
     """10 log10(|ref|^2 / |ref - q|^2): the quantised-vs-bf16 comparison of
     pytorch/ao PR #2275 (testing)."""
@@ -80,6 +71,8 @@ def sqnr_db(ref, q):
 
 
 def rel_frobenius(ref, got):
+    """|ref - got|_F / |ref|_F (Frobenius norms over every element): the
+    relative error behind the GEMM tolerances."""
     ref = np.asarray(ref, dtype=np.float64)
     got = np.asarray(got, dtype=np.float64)
     n = np.linalg.norm(ref)

@@ -173,12 +173,14 @@ def quantize_block_128x128(w, fmt="e4m3", block=128):
 
 
 def dequantize_block_1x128(codes, scale_inv, fmt="e4m3", block=128):
+    """value = decode(code) * scale_inv of the code's 1 x block block."""
     fmt = _fmt(fmt)
     M, K = codes.shape
     return decode(codes, fmt) * np.repeat(scale_inv.astype(np.float64), block, axis=1)[:, :K]
 
 
 def dequantize_block_128x128(codes, scale_inv, fmt="e4m3", block=128):
+    """value = decode(code) * scale_inv of the code's block x block tile."""
     fmt = _fmt(fmt)
     N, K = codes.shape
     s = np.repeat(np.repeat(scale_inv.astype(np.float64), block, axis=0), block, axis=1)
@@ -199,6 +201,8 @@ def quantize_tensor(x, scale, fmt="e4m3"):
 
 
 def dequantize_tensor(codes, scale, fmt="e4m3"):
+    """value = decode(code) / s, with s the float32 scale the codes were cast
+    with (float64 division)."""
     return decode(codes, _fmt(fmt)) / np.float64(np.float32(scale))
 
 

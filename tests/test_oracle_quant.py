@@ -269,3 +269,69 @@ def test_nvfp4_2d_dequantised_error_bound():
     assert np.all(np.abs(deq - w) <= bound + 1e-30)
     assert np.max(y) > 6.0                      # the case the excess term covers occurs here
     np.testing.assert_array_equal(Q.dequantize_nvfp4(cc, cs, s_g, 64), deq.T)
+
+
+def test_tensor_dequantise_divides_by_the_float32_scale():
+    """Per-tensor dequantisation (delayed scaling, Megatron-LM issue #1152):
+    the value of a code is decode(code) / s with s the float32 scale. Checked
+    against exact rational arithmetic for a scale that is not a power of two
+    (so float64(448 / 3) and float32(448 / 3) give different values), and by
+    the round trip x -> codes -> values staying within e4m3's half step."""
+    from fractions import Fraction
+    s32 = np.float32(448.0) / np.float32(3.0)
+    assert float(s32) != 448.0 / 3.0
+    codes = np.array([[0x7E, 0x38, 0x01, 0xFE, 0x00, 0x80]], dtype=np.uint8)
+    got = Q.dequantize_tensor(codes, s32)
+    for c, v in zip(codes[0], got[0]):
+        want = Fraction(float(F.decode(np.uint8(c), F.E4M3))) / Fraction(float(s32))
+        assert v == float(want), (c, v, float(want))
+    assert abs(got[0, 0] - 3.0) < 1e-6                  # 448 / (448 / 3)
+    # a scale handed in as a float64 is the float32 the codes were cast with
+    np.testing.assert_array_equal(Q.dequantize_tensor(codes, 448.0 / 3.0), got)
+    rng = np.random.default_rng(9)
+    x = F.round_to_bf16(rng.standard_normal((16, 64)) * 0.7)
+    s = np.float32(448.0) / np.float32(np.max(np.abs(x)))
+    c, _ = Q.quantize_tensor(x, s)
+    back = Q.dequantize_tensor(c, s)
+    big = np.abs(x) >= 2.0 ** -6 / float(s)             # normal range of e4m3 after scaling
+    assert np.all(np.abs(back - x)[big] <= 2.0 ** -4 * np.abs(x)[big] + 1e-12)
+
+
+def test_blockwise_1x128_dequantise_roundtrip():
+    """1x128 blocks (TransformerEngine issue #2393): with power-of-two block
+    scales the round trip codes -> values -> codes -> values is exact, and
+    each 128-element block of each row carries its own scale (four rows times
+    two blocks, all different)."""
+    rng = np.random.default_rng(10)
+    f = F.E4M3
+    codes = (rng.choice(f.pos_codes[:-1], size=(4, 256)) | (rng.integers(0, 2, (4, 256)) * 0x80)).astype(np.uint8)
+    codes[:, 3] = 0x7E
+    codes[:, 131] = 0xFE
+    k = np.arange(8).reshape(4, 2) - 3                   # eight different exponents
+    x = F.decode(codes, f) * np.repeat(np.exp2(-k.astype(np.float64)), 128, axis=1)
+    c, si = Q.quantize_block_1x128(x)
+    np.testing.assert_array_equal(c, codes)
+    np.testing.assert_array_equal(Q.dequantize_block_1x128(c, si), x)
+    # the block of element (r, j) is (r, j // 128): a wrong axis would mix rows
+    assert Q.dequantize_block_1x128(c, si)[1, 200] == F.decode(codes[1, 200], f) * 2.0 ** -k[1, 1]
+
+
+def test_blockwise_128x128_dequantise_roundtrip():
+    """128x128 weight tiles (TransformerEngine issue #2393): a 256x384 weight
+    whose six tiles have six different power-of-two scales comes back
+    exactly, so the scale of element (n, k) is tile (n // 128, k // 128) and
+    not its transpose."""
+    rng = np.random.default_rng(11)
+    f = F.E4M3
+    N, K = 256, 384
+    codes = (rng.choice(f.pos_codes[:-1], size=(N, K)) | (rng.integers(0, 2, (N, K)) * 0x80)).astype(np.uint8)
+    for bn in range(2):
+        for bk in range(3):
+            codes[bn * 128 + 5, bk * 128 + 7] = 0x7E     # each tile reaches the largest code
+    k = np.array([[0, 2, 5], [-3, 1, 4]])
+    scale = np.repeat(np.repeat(np.exp2(-k.astype(np.float64)), 128, axis=0), 128, axis=1)
+    x = F.decode(codes, f) * scale
+    c, si = Q.quantize_block_128x128(x)
+    np.testing.assert_array_equal(c, codes)
+    np.testing.assert_array_equal(si, np.exp2(-k).astype(np.float32))
+    np.testing.assert_array_equal(Q.dequantize_block_128x128(c, si), x)

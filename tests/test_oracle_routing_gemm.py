@@ -217,3 +217,26 @@ def test_zipf_counts_of_scout_workload():
     idx, probs = make_routing(w)
     cnt = np.bincount(idx[:, 0], minlength=16)
     assert np.sum(cnt == 0) == 2 and cnt.sum() == 2048 and np.all(probs == 1)
+
+
+def test_rel_frobenius_closed_forms():
+    """Relative Frobenius error |ref - got|_F / |ref|_F on hand-computed
+    cases: a vector (0.3 / 2 = 0.15; without the square roots it would read
+    0.0225) and a matrix whose spectral and Frobenius norms differ
+    (0.5 / 5 = 0.1; the spectral norm would give 0.125)."""
+    assert G.rel_frobenius(np.ones(4), np.ones(4) + np.array([0.3, 0, 0, 0])) == pytest.approx(0.15, rel=1e-15)
+    ref = np.array([[3.0, 0.0], [0.0, 4.0]])
+    got = ref + np.array([[0.0, 0.0], [0.0, 0.5]])
+    assert G.rel_frobenius(ref, got) == pytest.approx(0.1, rel=1e-15)
+    assert G.rel_frobenius(ref, ref) == 0.0
+    assert G.rel_frobenius(np.zeros(3), np.zeros(3)) == 0.0
+
+
+def test_sqnr_closed_forms():
+    """SQNR = 10 log10(|ref|^2 / |ref - q|^2) (pytorch/ao PR #2275, testing):
+    a uniform 10% error is 20 dB (a 20 log10 slip would give 40 dB), a 1%
+    error 40 dB, and an exact result is infinite."""
+    ref = np.linspace(-3.0, 5.0, 100)
+    assert G.sqnr_db(ref, 1.1 * ref) == pytest.approx(20.0, abs=1e-12)
+    assert G.sqnr_db(ref, 0.99 * ref) == pytest.approx(40.0, abs=1e-12)
+    assert G.sqnr_db(ref, ref) == float("inf")
