@@ -186,17 +186,20 @@ def algorithmic_bytes_fp8(w, R_pad, cols):
     """Compulsory HBM bytes of the memory-bound steps: each input read once,
     each output written once (a row quantised once per token is written k
     times). A quantised output is one byte per element plus, with MX scaling,
-    one E8M0 byte per 32; `cols` adds the column-wise copies (MX training;
+    one E8M0 byte per 32 (blockwise: a float32 per 128); `cols` adds the column-wise copies (MX training;
     per-tensor scaling reads the row-wise codes MN-major and writes none)."""
     T, k, H, F, E = w.T, w.k, w.H, w.F, w.E
     R = T * k
-    q = 1 + 1 / 32 if w.recipe == "mxfp8" else 1
+    # MX: one E8M0 byte per 32; blockwise: one float32 per 128 (activations)
+    # or per 128x128 tile (weights)
+    q = 1 + 1 / 32 if w.recipe in ("mxfp8", "blockwise") else 1
+    qw = 1 + 4 / (128 * 128) if w.recipe == "blockwise" else q
     c = 1 if cols else 0
     b = {}
     b["permute_quant"] = T * H * 2 + (1 + c) * R * H * q
     b["swiglu_quant"] = R * 2 * F * 2 + (1 + c) * R * F * q
     b["unpermute"] = R * H * 2 + T * H * 2
-    b["weight_quant"] = E * 3 * F * H * 2 + (1 + c) * E * 3 * F * H * q
+    b["weight_quant"] = E * 3 * F * H * 2 + (1 + c) * E * 3 * F * H * qw
     if w.backward:
         b["unpermute_bwd_quant"] = T * H * 2 + R * H * 2 + (1 + c) * R * H * q
         b["dswiglu_quant"] = R * F * 2 + R * 2 * F * 2 + (1 + c) * R * 2 * F * q
@@ -323,7 +326,9 @@ def measured_gemm_traffic(workload: str):
     if rec.get("sources_sha256") != h.hexdigest():
         return None
     return {"bytes_per_launch": int(rec["bytes_per_launch"]),
-            "algorithmic_bytes_per_launch": int(rec["algorithmic_bytes_per_launch"])}
+            "algorithmic_bytes_per_launch": int(rec["algorithmic_bytes_per_launch"]),
+            "source": f"stored ncu capture (profiles/{os.path.basename(path)}; {rec.get('case', 'see file')}), "
+                      "valid for the current GEMM sources; not measured in this run"}
 
 
 def max_over_ranks(x: float, device=None) -> float:
@@ -397,6 +402,223 @@ def config_of(w, args):
             "l2": "inputs larger than L2 (bf16 weights 2.8 GB resident, re-quantised every step)"}
 
 
+def gemm_roofline(w, gemm_ms, pk, pk_src):
+    """Algorithmic GEMM FLOP/s of the step's grouped-GEMM launches against the
+    burst tensor peak (the kernels run in a loop well under a second long),
+    with the sustained fraction beside it."""
+    flops = w.gemm_flops()
+    achieved = flops / (gemm_ms * 1e-3) / 1e12
+    ratio = FP4_OVER_BF16 if w.recipe == "nvfp4" else FP8_OVER_BF16
+    kind = "fp4" if w.recipe == "nvfp4" else "fp8"
+    peak = pk["bf16_tflops"] * ratio
+    peak_sus = pk["bf16_tflops_sustained"] * ratio
+    return {"bound": "tensor", "kernel": "grouped GEMM (all grouped GEMM launches of the step)",
+            "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "frac_of_sustained": achieved / peak_sus,
+            "peak_source": f"{pk_src}: bf16 burst {pk['bf16_tflops']} TFLOP/s x {ratio:g} ({kind}/bf16 nominal); "
+                           f"frac_of_sustained uses bf16 sustained {pk['bf16_tflops_sustained']} x {ratio:g}",
+            "gemm_ms_per_step": gemm_ms}
+
+
+def hbm_table(w, per, lay, pk):
+    R_pad = int(lay.offsets[-1].item())
+    ab = algorithmic_bytes(w, R_pad, cols=lay.train and not lay.mn)
+    return {k: {"ms": per[k], "GB/s": ab[k] / (per[k] * 1e-3) / 1e9,
+                "frac": ab[k] / (per[k] * 1e-3) / 1e9 / pk["hbm_gbs"], "bytes": ab[k]} for k in ab if k in per}
+
+
+def kernel_times(step, steps):
+    """ms per step of every named op, from CUDA events around each launch
+    group (on the launching stream) over `steps` further steps."""
+    kstep = Step.__new__(Step)
+    kstep.__dict__.update(step.__dict__)
+    kstep.time_kernels = True
+    kstep.events = []
+    for _ in range(steps):
+        kstep()
+    torch.cuda.synchronize()
+    per = {}
+    for ev in kstep.events:
+        for name, pairs in ev.items():
+            per.setdefault(name, 0.0)
+            per[name] += sum(a.elapsed_time(b) for a, b in pairs)
+    return {k: v / steps for k, v in per.items()}
+
+
+def e2e_run(step, flops, world, steps, barrier):
+    """End to end through host buffers: every step copies its inputs from
+    pinned host memory and reads its results back: the forward output, and
+    for training also dX and dprobs (the weight gradients stay on the device,
+    where an optimizer would consume them). The copies run on a second
+    stream, pipelined with the compute: step i computes on input set i % 2
+    while the copy stream reads back step i - 1's results and fills the other
+    set for step i + 1. A step starts once its inputs have landed; the first
+    op that rewrites a result (the unpermute) waits until the previous results
+    have been read out. All copies of the timed steps lie inside the timed
+    region (the first starts after its opening event, and the closing event
+    waits for the last read-back)."""
+    lay = step.lay
+    hx = step.x.cpu().pin_memory()
+    hidx = step.idx.cpu().pin_memory()
+    hp = step.probs.cpu().pin_memory()
+    hd = step.dout.cpu().pin_memory() if step.train else None
+    res_dev = [lay.out] + ([lay.dx, lay.dprobs] if step.train else [])
+    hres = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in res_dev]
+    h2d = hx.numel() * 2 + hidx.numel() * 4 + hp.numel() * 4 + (hd.numel() * 2 if hd is not None else 0)
+    d2h = sum(r.numel() * r.element_size() for r in hres)
+    sets = [(step.x, step.idx, step.probs, step.dout),
+            tuple(None if t is None else torch.empty_like(t) for t in (step.x, step.idx, step.probs, step.dout))]
+    ops = [step.ops, step.lay.step_ops(step.w1, step.w2, *sets[1])]
+    wr = [n for n, _ in ops[0]].index("unpermute")
+    cur, cs = torch.cuda.current_stream(), torch.cuda.Stream()
+    landed = [torch.cuda.Event(), torch.cuda.Event()]
+    done = [torch.cuda.Event(), torch.cuda.Event()]
+    read_out = torch.cuda.Event()
+
+    def h2d_into(si):                       # on the copy stream
+        x_, i_, p_, d_ = sets[si]
+        x_.copy_(hx, non_blocking=True)
+        i_.copy_(hidx, non_blocking=True)
+        p_.copy_(hp, non_blocking=True)
+        if d_ is not None:
+            d_.copy_(hd, non_blocking=True)
+        landed[si].record(cs)
+
+    def run(n):
+        """n pipelined steps on `cur` (the copy stream starts after `cur`'s current point)."""
+        start = torch.cuda.Event()
+        start.record(cur)
+        cs.wait_event(start)
+        with torch.cuda.stream(cs):
+            h2d_into(0)
+            if n > 1:
+                h2d_into(1)
+        for i in range(n):
+            si = i % 2
+            cur.wait_event(landed[si])
+            for j, (_, op) in enumerate(ops[si]):
+                if j == wr and i > 0:
+                    cur.wait_event(read_out)
+                op()
+            done[si].record(cur)
+            cs.wait_event(done[si])
+            with torch.cuda.stream(cs):
+                for h, r in zip(hres, res_dev):
+                    h.copy_(r, non_blocking=True)
+                read_out.record(cs)
+                if i + 2 < n:
+                    h2d_into(si)
+        cur.wait_event(read_out)
+
+    run(2)
+    barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    run(steps)
+    b.record()
+    barrier()
+    ems = a.elapsed_time(b) / steps
+    return {"value": flops * world / (ems * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ems, "copies": "pipelined on a second stream",
+            "read_back": "out" + (", dX, dprobs (dW stays on the device)" if step.train else "")}
+
+
+def measure(w, dev, world, steps, warmup, barrier, local, with_e2e=False):
+    """One workload: `warmup` untimed steps, then `steps` timed steps between
+    barriers, clocks sampled meanwhile; then the per-kernel event timing and,
+    if asked, the end-to-end run. Returns the record and the Step."""
+    from fp8_grouped_gemm_gb300 import mgq
+    step = Step(w, dev)
+    for _ in range(max(3, warmup)):
+        step()
+    torch.cuda.synchronize()
+    if mgq.get_error() != mgq.OK:
+        raise RuntimeError(f"{w.name}: device error in the warm-up steps")
+    clocks = ClockSampler(local)
+    barrier()
+    clocks.start()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        step()
+    t1.record()
+    barrier()
+    clk = clocks.stop()
+    ms = max_over_ranks(t0.elapsed_time(t1), dev if world > 1 else None)
+    ms_step = ms / steps
+    flops = w.gemm_flops()
+    per = kernel_times(step, steps)
+    pk, pk_src = peaks()
+    gemm_ms = sum(v for k, v in per.items() if k.startswith("gemm"))
+    rec = {"ms_per_step": ms_step, "value": job_value(flops, world, ms_step), "unit": "TFLOP/s",
+           "steps": steps, "warmup": max(3, warmup), "dtype": dtype_of(w), "config": None,
+           "roofline": gemm_roofline(w, gemm_ms, pk, pk_src), "hbm_kernels": hbm_table(w, per, step.lay, pk),
+           "hbm_peak": {"GB/s": pk["hbm_gbs"], "source": pk_src}, "kernel_ms_per_step": per,
+           "gpu_launches": step.lay.gpu_launches_per_step() * steps, "clocks": clk}
+    if with_e2e:
+        rec["e2e"] = e2e_run(step, flops, world, steps, barrier)
+    if mgq.get_error() != mgq.OK:
+        raise RuntimeError(f"{w.name}: device error in the timed steps")
+    return rec, step
+
+
+# the other configurations, each measured briefly in the same run beside the
+# headline (same timing rules; no end-to-end or CPU legs)
+OTHER_WORKLOADS = ("tiny", "mixtral_fwd", "scout_fwd", "finegrained_fwd", "mixtral_fwdbwd_mx",
+                   "mixtral_fwdbwd_nvfp4")
+OTHER_STEPS = 20
+
+
+def oracle_memory_steps(w):
+    """The oracle's memory-bound steps timed on a bounded sample (2048 tokens
+    of the workload's hidden size for permute + quantise and the unpermute;
+    a 1024-row slice of one expert's W1 for the weight quantisation), as
+    algorithmic GB/s by the byte counts the GPU kernels are measured with."""
+    from oracle import quant as OQ
+    from oracle import routing as OR
+    from oracle.formats import round_to_bf16
+    rng = np.random.default_rng(w.seed)
+    Ts, H, k, E = 2048, w.H, w.k, w.E
+    x = round_to_bf16(rng.standard_normal((Ts, H)))
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(Ts)]).astype(np.int32)
+    probs = np.full((Ts, k), 1.0 / k, dtype=np.float32)
+    wslice = round_to_bf16(rng.standard_normal((1024, H)) * 0.02)
+
+    def quant(a):
+        if w.recipe == "mxfp8":
+            return OQ.quantize_mx(a)
+        if w.recipe == "blockwise":
+            return OQ.quantize_block_1x128(a)
+        if w.recipe == "nvfp4":
+            return OQ.quantize_nvfp4(a, OQ.nvfp4_global_scale(float(np.max(np.abs(a)))))
+        return OQ.quantize_tensor(a, np.float32(1.0))
+
+    q = 1.0 if w.recipe in ("delayed",) else (0.5 + 1 / 16 if w.recipe == "nvfp4" else 1 + 1 / 32)
+    out = {}
+    t = time.perf_counter()
+    rim, src, off, cnt = OR.permute_indices(idx, E, 128)
+    codes = quant(x)[0]
+    OR.permute_rows(codes, rim, int(off[-1]))
+    dt = time.perf_counter() - t
+    out["permute_quant"] = {"GB/s": (Ts * H * 2 + Ts * k * H * q) / dt / 1e9, "seconds": dt,
+                            "sample": f"{Ts} tokens x {H}, top-{k} of {E}"}
+    y = round_to_bf16(rng.standard_normal((int(off[-1]), H)))
+    t = time.perf_counter()
+    OR.unpermute(y, rim, probs)
+    dt = time.perf_counter() - t
+    out["unpermute"] = {"GB/s": (Ts * k * H * 2 + Ts * H * 2) / dt / 1e9, "seconds": dt,
+                        "sample": f"{Ts} tokens x {H}, top-{k}"}
+    t = time.perf_counter()
+    if w.recipe == "blockwise":
+        OQ.quantize_block_128x128(wslice)
+    else:
+        quant(wslice)
+    dt = time.perf_counter() - t
+    out["weight_quant"] = {"GB/s": 1024 * H * (2 + q) / dt / 1e9, "seconds": dt,
+                           "sample": f"1024 x {H} rows of one expert's W1"}
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -406,13 +628,22 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the token count (small cases for profiler captures)")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="override the expert count (small cases for profiler captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-others", action="store_true",
+                    help="measure only the named workload (no `workloads` entries)")
     args = ap.parse_args()
     from fp8_grouped_gemm_gb300.workloads import WORKLOADS
     w = WORKLOADS[args.workload]
+    small = {}
     if args.tokens:
-        w = w.scaled(T=args.tokens)
+        small["T"] = args.tokens
+    if args.experts:
+        small["E"] = args.experts
+    if small:
+        w = w.scaled(**small)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -427,154 +658,54 @@ def main():
     torch.cuda.set_device(dev)
     from fp8_grouped_gemm_gb300 import mgq
     mgq.load()
-    step = Step(w, dev)
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
-    assert mgq.get_error() == mgq.OK
 
     def barrier():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
 
-    clocks = ClockSampler(local)
-    barrier()
-    clocks.start()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for _ in range(args.steps):
-        step()
-    t1.record()
-    barrier()
-    clk = clocks.stop()
-    ms = max_over_ranks(t0.elapsed_time(t1), dev if world > 1 else None)
-    ms_step = ms / args.steps
-    flops = w.gemm_flops()
-    value = job_value(flops, world, ms_step)
-    launches = step.lay.gpu_launches_per_step() * args.steps
+    rec, step = measure(w, dev, world, args.steps, args.warmup, barrier, local, with_e2e=not args.no_e2e)
+    roofline = rec["roofline"]
+    tr = measured_gemm_traffic(w.name) if not small else None
+    roofline["traffic"] = tr["bytes_per_launch"] if tr else None
+    if tr:
+        roofline["algorithmic_bytes_per_launch"] = tr["algorithmic_bytes_per_launch"]
+        roofline["traffic_source"] = tr["source"]
+    del step
+    torch.cuda.empty_cache()
 
-    # per-kernel timing: the same steps with events around every launch
-    kstep = Step.__new__(Step)
-    kstep.__dict__.update(step.__dict__)
-    kstep.time_kernels = True
-    kstep.events = []
-    for _ in range(args.steps):
-        kstep()
-    torch.cuda.synchronize()
-    per = {}
-    for ev in kstep.events:
-        for name, pairs in ev.items():
-            per.setdefault(name, 0.0)
-            per[name] += sum(a.elapsed_time(b) for a, b in pairs)
-    per = {k: v / args.steps for k, v in per.items()}          # ms per step
-    pk, pk_src = peaks()
-    gemm_ms = sum(v for k, v in per.items() if k.startswith("gemm"))
-    achieved = flops / (gemm_ms * 1e-3) / 1e12
-    ratio = FP4_OVER_BF16 if w.recipe == "nvfp4" else FP8_OVER_BF16
-    peak_fp8 = pk["bf16_tflops_sustained"] * ratio
-    R_pad = int(step.lay.offsets[-1].item())
-    ab = algorithmic_bytes(w, R_pad, cols=step.lay.train and not step.lay.mn)
-    hbm = {k: {"ms": per[k], "GB/s": ab[k] / (per[k] * 1e-3) / 1e9,
-               "frac": ab[k] / (per[k] * 1e-3) / 1e9 / pk["hbm_gbs"]} for k in ab if k in per}
-    tr = measured_gemm_traffic(w.name) if not args.tokens else None
-    roofline = {"bound": "tensor", "kernel": "grouped GEMM (all grouped GEMM launches of the step)",
-                "achieved": achieved, "peak": peak_fp8, "unit": "TFLOP/s", "frac": achieved / peak_fp8,
-                "traffic": tr["bytes_per_launch"] if tr else None,
-                "algorithmic_bytes_per_launch": tr["algorithmic_bytes_per_launch"] if tr else None,
-                "peak_source": f"{pk_src}: bf16 sustained {pk['bf16_tflops_sustained']} TFLOP/s x {ratio:g} "
-                               f"({'fp4' if w.recipe == 'nvfp4' else 'fp8'}/bf16 nominal)",
-                "gemm_ms_per_step": gemm_ms}
-
-    # end to end through host buffers: every step copies its inputs from pinned
-    # host memory and reads its result (dX, or the output) back. The copies run
-    # on a second stream, pipelined with the compute: step i computes on input
-    # set i % 2 while the copy stream reads back step i - 1's result and fills
-    # the other set for step i + 1. A step starts once its inputs have landed;
-    # the op that rewrites the result waits until the previous result has been
-    # read out. All copies of the timed steps lie inside the timed
-    # region (the first start after its opening event, and the closing event
-    # waits for the last read-back).
-    e2e = None
-    if not args.no_e2e:
-        lay = step.lay
-        hx = step.x.cpu().pin_memory()
-        hidx = step.idx.cpu().pin_memory()
-        hp = step.probs.cpu().pin_memory()
-        hd = step.dout.cpu().pin_memory() if step.train else None
-        res_dev = lay.dx if step.train else lay.out
-        hres = torch.empty(res_dev.shape, dtype=res_dev.dtype, pin_memory=True)
-        h2d = hx.numel() * 2 + hidx.numel() * 4 + hp.numel() * 4 + (hd.numel() * 2 if hd is not None else 0)
-        d2h = hres.numel() * 2
-        sets = [(step.x, step.idx, step.probs, step.dout),
-                tuple(None if t is None else torch.empty_like(t) for t in (step.x, step.idx, step.probs, step.dout))]
-        ops = [step.ops, lay.step_ops(step.w1, step.w2, *sets[1])]
-        # the op that writes the result: it waits until the previous result has been read out
-        wr = [n for n, _ in ops[0]].index("permute_bwd" if step.train else "unpermute")
-        cur, cs = torch.cuda.current_stream(), torch.cuda.Stream()
-        landed = [torch.cuda.Event(), torch.cuda.Event()]
-        done = [torch.cuda.Event(), torch.cuda.Event()]
-        read_out = torch.cuda.Event()
-
-        def h2d_into(si):                       # on the copy stream
-            x_, i_, p_, d_ = sets[si]
-            x_.copy_(hx, non_blocking=True)
-            i_.copy_(hidx, non_blocking=True)
-            p_.copy_(hp, non_blocking=True)
-            if d_ is not None:
-                d_.copy_(hd, non_blocking=True)
-            landed[si].record(cs)
-
-        def run(n):
-            """n pipelined steps on `cur` (the copy stream starts after `cur`'s current point)."""
-            start = torch.cuda.Event()
-            start.record(cur)
-            cs.wait_event(start)
-            with torch.cuda.stream(cs):
-                h2d_into(0)
-                if n > 1:
-                    h2d_into(1)
-            for i in range(n):
-                si = i % 2
-                cur.wait_event(landed[si])
-                for j, (_, op) in enumerate(ops[si]):
-                    if j == wr and i > 0:
-                        cur.wait_event(read_out)
-                    op()
-                done[si].record(cur)
-                cs.wait_event(done[si])
-                with torch.cuda.stream(cs):
-                    hres.copy_(res_dev, non_blocking=True)
-                    read_out.record(cs)
-                    if i + 2 < n:
-                        h2d_into(si)
-            cur.wait_event(read_out)
-
-        run(2)
-        barrier()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        run(args.steps)
-        b.record()
-        barrier()
-        ems = a.elapsed_time(b) / args.steps
-        e2e = {"value": flops * world / (ems * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": ems, "copies": "pipelined on a second stream"}
-    assert mgq.get_error() == mgq.OK
+    others = {}
+    if not args.no_others and not small:
+        for name in OTHER_WORKLOADS:
+            if name == w.name:
+                continue
+            ow = WORKLOADS[name]
+            orec, ostep = measure(ow, dev, world, min(args.steps, OTHER_STEPS), args.warmup, barrier, local)
+            orec["config"] = config_of(ow, args)
+            orec["metric"] = ("grouped GEMM TFLOP/s of the step (" + ("fwd+bwd" if ow.backward else "fwd")
+                              + ", algorithmic FLOPs of the unpadded rows)")
+            others[name] = orec
+            del ostep
+            torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         dt, f = oracle_sample(w, *CPU_BASELINE_SAMPLE)
         cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
-               "sample": sample_desc(*CPU_BASELINE_SAMPLE), "seconds": dt}
+               "sample": sample_desc(*CPU_BASELINE_SAMPLE), "seconds": dt,
+               "memory_steps": oracle_memory_steps(w)}
+        for k_, v in cpu["memory_steps"].items():
+            if k_ in rec["hbm_kernels"]:
+                v["gpu_GB/s"] = rec["hbm_kernels"][k_]["GB/s"]
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": dtype_of(w), "data": "synthetic (seeded; shapes of the workload)",
-            "config": config_of(w, args), "roofline": roofline, "hbm_kernels": hbm,
-            "kernel_ms_per_step": per, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-            "clocks": clk,
+            "metric": METRIC, "value": rec["value"], "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": rec["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": dtype_of(w),
+            "data": "synthetic (seeded; shapes of the workload)",
+            "config": config_of(w, args), "roofline": roofline, "hbm_kernels": rec["hbm_kernels"],
+            "kernel_ms_per_step": rec["kernel_ms_per_step"], "cpu_baseline": cpu, "e2e": rec.get("e2e"),
+            "gpu_launches": rec["gpu_launches"], "clocks": rec["clocks"], "workloads": others,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -24,6 +24,7 @@
 // The dSwiGLU instantiations leave the plain epilogue after their `continue`
 // unreachable by design.
 #pragma nv_diag_suppress 128
+#include <atomic>
 #include <cstdlib>
 
 #include "device_common.cuh"
@@ -1402,61 +1403,42 @@ int launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtenso
   return MGQ_OK;
 }
 
-// The 2-CTA kernel serves per-tensor FP8 (wgrad needs output rows in
-// multiples of 256); MGQ_GEMM_1CTA=1 in the environment selects the 1-CTA
-// kernel for every call (both compute the same values). MX goes to the 1-CTA
-// kernel unless MGQ_GEMM_MX_PAIR=1: measured on the Mixtral gate/up and down
-// shapes, the pair scale copies (three 32x128b.warpx4 copies per 128-deep
-// stage, executed in order with the MMAs) cost the pair kernel about a fifth
-// of its MMA rate, which leaves it behind the 1-CTA kernel.
-// Failure-detection knobs (read at every launch): MGQ_DEBUG_GEMM_STALL=1 makes
-// the producer issue no loads, so the pipeline waits run out and the kernel
-// reports MGQ_ERR_TIMEOUT and exits cleanly; MGQ_DEBUG_WAIT_MS sets the wait
-// limit (default 2000 ms).
+// Process-wide GEMM options (mgq_set_gemm_option): which kernel serves a call,
+// how the pair kernel stores, and the failure-detection test hooks. Each launch
+// reads them with relaxed atomic loads; nothing is taken from the environment.
+//  - The 2-CTA kernel serves per-tensor FP8 (wgrad needs output rows in
+//    multiples of 256); MGQ_GEMM_OPT_FORCE_1CTA puts every call on the 1-CTA
+//    kernel (both compute the same values).
+//  - MX goes to the 1-CTA kernel unless MGQ_GEMM_OPT_MX_PAIR is set: measured
+//    on the Mixtral gate/up and down shapes, the pair scale copies (three
+//    32x128b.warpx4 copies per 128-deep stage, executed in order with the
+//    MMAs) cost the pair kernel about a fifth of its MMA rate, which leaves it
+//    behind the 1-CTA kernel.
+//  - NVFP4 on the 2-CTA kernel with MGQ_GEMM_OPT_NV_PAIR: correct, but
+//    measured slower than the 1-CTA kernel (the pair form of the four scale
+//    copies a stage costs more than the copies it saves), so not the default.
+//  - MGQ_GEMM_OPT_DEBUG_STALL makes the producer issue no loads, so the
+//    pipeline waits run out and the kernel reports MGQ_ERR_TIMEOUT and exits
+//    cleanly; MGQ_GEMM_OPT_WAIT_MS sets the wait limit (0: 2000 ms).
+std::atomic<int64_t> g_gemm_opt[MGQ_GEMM_OPT_COUNT];
+
+int64_t gemm_opt(int o) { return g_gemm_opt[o].load(std::memory_order_relaxed); }
+
 void debug_knobs(int* stall, uint64_t* wait_ns) {
-  const char* e = getenv("MGQ_DEBUG_GEMM_STALL");
-  *stall = (e && e[0] == '1') ? 1 : 0;
-  const char* w = getenv("MGQ_DEBUG_WAIT_MS");
-  const long ms = w ? atol(w) : 0;
+  *stall = gemm_opt(MGQ_GEMM_OPT_DEBUG_STALL) ? 1 : 0;
+  const int64_t ms = gemm_opt(MGQ_GEMM_OPT_WAIT_MS);
   *wait_ns = ms > 0 ? (uint64_t)ms * 1000000ull : kWaitNs;
 }
 
-// MGQ_GEMM_DIRECT_STORE=1 makes the pair kernel store from registers
-// instead of through TMA (same values).
-bool direct_store_forced() {
-  static const bool f = [] {
-    const char* e = getenv("MGQ_GEMM_DIRECT_STORE");
-    return e && e[0] == '1';
-  }();
-  return f;
-}
+bool direct_store_forced() { return gemm_opt(MGQ_GEMM_OPT_DIRECT_STORE) != 0; }
 
 bool use_pair_kernel(int mode, int64_t N) {
-  static const bool force_1cta = [] {
-    const char* e = getenv("MGQ_GEMM_1CTA");
-    return e && e[0] == '1';
-  }();
-  if (force_1cta) return false;
+  if (gemm_opt(MGQ_GEMM_OPT_FORCE_1CTA)) return false;
   return mode == kModeRows || N % 256 == 0;
 }
 
-bool mx_pair_selected() {
-  static const bool f = [] {
-    const char* e = getenv("MGQ_GEMM_MX_PAIR");
-    return e && e[0] == '1';
-  }();
-  return f;
-}
-// NVFP4 on the 2-CTA kernel when MGQ_GEMM_NV_PAIR=1: correct, but measured
-// slower than the 1-CTA kernel (the pair form of the four scale copies a stage
-// costs more than the copies it saves), so not the default
-bool nv_pair_selected() {
-  static const bool f = [] {
-    const char* e = getenv("MGQ_GEMM_NV_PAIR");
-    return e && e[0] == '1';
-  }();
-  return f;
-}
+bool mx_pair_selected() { return gemm_opt(MGQ_GEMM_OPT_MX_PAIR) != 0; }
+bool nv_pair_selected() { return gemm_opt(MGQ_GEMM_OPT_NV_PAIR) != 0; }
 
 int check_operand(const mgq_operand* o) {
   if (!o || !o->data || !aligned16(o->data)) return MGQ_ERR_INVALID_ARG;
@@ -1803,6 +1785,21 @@ int mgq_grouped_gemm_fwd_swiglu(const mgq_operand* A, const mgq_operand* W1, int
   const SwigluOut sw{qh, h_bf16};
   return run_grouped(kModeRows, A, W1, scaling, offsets, E, R_cap, 2 * F, K, 0.0f, gu_bf16, MGQ_OUT_BF16, stream,
                      &sw);
+}
+
+int mgq_set_gemm_option(int option, int64_t value) {
+  if (option < 0 || option >= MGQ_GEMM_OPT_COUNT) return MGQ_ERR_INVALID_ARG;
+  if (value < 0 || (option != MGQ_GEMM_OPT_WAIT_MS && value > 1) ||
+      (option == MGQ_GEMM_OPT_WAIT_MS && value > 600000))
+    return MGQ_ERR_INVALID_ARG;
+  g_gemm_opt[option].store(value, std::memory_order_relaxed);
+  return MGQ_OK;
+}
+
+int mgq_get_gemm_option(int option, int64_t* value) {
+  if (option < 0 || option >= MGQ_GEMM_OPT_COUNT || !value) return MGQ_ERR_INVALID_ARG;
+  *value = g_gemm_opt[option].load(std::memory_order_relaxed);
+  return MGQ_OK;
 }
 
 }  // extern "C"

@@ -24,6 +24,8 @@ MX32_E8M0, NV16_UE4M3, BLK_1x128_F32, BLK_128x128_F32, TENSOR_F32, NV16x16_UE4M3
 RCEIL, FLOOR = 0, 1
 OUT_BF16, OUT_F32 = 0, 1
 LAYOUT_K, LAYOUT_MN = 0, 1
+(GEMM_OPT_FORCE_1CTA, GEMM_OPT_MX_PAIR, GEMM_OPT_NV_PAIR, GEMM_OPT_DIRECT_STORE, GEMM_OPT_DEBUG_STALL,
+ GEMM_OPT_WAIT_MS) = range(6)
 
 FMAX = {E4M3: 448.0, E5M2: 57344.0}
 
@@ -33,7 +35,8 @@ EXPORTS = (
     "mgq_moe_permute", "mgq_moe_route", "mgq_moe_permute_routed", "mgq_moe_permute_noalloc", "mgq_block_quantize", "mgq_grouped_quantize", "mgq_grouped_gemm_fwd", "mgq_grouped_gemm_dgrad",
     "mgq_grouped_gemm_wgrad", "mgq_grouped_gemm_fwd_swiglu",
     "mgq_grouped_gemm_dgrad_dswiglu", "mgq_swiglu_quantize", "mgq_dswiglu_quantize", "mgq_moe_unpermute",
-    "mgq_moe_unpermute_bwd", "mgq_moe_permute_bwd", "mgq_amax_history_update",
+    "mgq_moe_unpermute_bwd", "mgq_moe_permute_bwd", "mgq_amax_history_update", "mgq_set_gemm_option",
+    "mgq_get_gemm_option",
 )
 
 
@@ -96,6 +99,8 @@ def load() -> ctypes.CDLL:
                                               P(QDesc), vp, vp]
         lib.mgq_moe_permute_bwd.argtypes = [vp, vp, i32, i32, i32, vp, vp]
         lib.mgq_amax_history_update.argtypes = [vp, vp, vp, vp, i32, i32, ctypes.c_float, vp]
+        lib.mgq_set_gemm_option.argtypes = [i32, i64]
+        lib.mgq_get_gemm_option.argtypes = [i32, P(i64)]
         for name in EXPORTS:
             if name not in ("mgq_status_string", "mgq_permute_workspace_size"):
                 getattr(lib, name).restype = i32
@@ -164,6 +169,16 @@ def get_error(stream=None) -> int:
     st = ctypes.c_int(0)
     _check(load().mgq_get_error(_s(stream), ctypes.byref(st)), "mgq_get_error")
     return st.value
+
+
+def set_gemm_option(option: int, value: int) -> None:
+    _check(load().mgq_set_gemm_option(int(option), int(value)), "mgq_set_gemm_option")
+
+
+def get_gemm_option(option: int) -> int:
+    v = ctypes.c_int64(0)
+    _check(load().mgq_get_gemm_option(int(option), ctypes.byref(v)), "mgq_get_gemm_option")
+    return v.value
 
 
 def moe_permute(x, topk_idx, E, align, q: QDesc | None, R_cap, row_id_map, src_row, offsets,

@@ -10,7 +10,10 @@
  * argument errors are detected on the host before anything is launched;
  * errors found by a kernel (an expert id out of range, a pipeline wait that
  * timed out) are recorded in the device error word and reported by
- * mgq_get_error. No call traps, aborts or throws.
+ * mgq_get_error. No call traps, aborts or throws. The error word's device
+ * address is looked up once per device and kept for the life of the process,
+ * so using the library after cudaDeviceReset in the same process is not
+ * supported.
  *
  * What the operations compute comes from four pages on low-precision MoE
  * training:
@@ -217,7 +220,9 @@ int mgq_moe_permute_routed(const void* x_bf16, int T, int H, int k, int E, const
  *    GPU (different streams or host threads) race and must be serialised by
  *    the caller. Every scratch entry is written before it is read, so the
  *    previous call's contents need no clearing.
- *  - Every GPU that loads the library holds the array until the process exits. */
+ *  - Every GPU that loads the library holds the array until the process exits.
+ *  - The looked-up address is kept for the life of the process: calling this
+ *    entry point after cudaDeviceReset in the same process is not supported. */
 int mgq_moe_permute_noalloc(const void* x_bf16, int T, int H, const int32_t* topk_idx, int k,
                             int E, int align, const mgq_qdesc* q, void* out_bf16, int64_t R_cap,
                             int32_t* row_id_map, int32_t* src_row, int32_t* offsets,
@@ -304,6 +309,38 @@ int mgq_grouped_gemm_dgrad(const mgq_operand* dY, const mgq_operand* Wcol, int s
 int mgq_grouped_gemm_wgrad(const mgq_operand* dYcol, const mgq_operand* Acol, int scaling,
                            const int32_t* offsets, int E, int64_t R_cap, int64_t N,
                            int64_t K, float beta, void* dW, int out_dtype, void* stream);
+
+/* Process-wide options of the grouped GEMMs (every entry point above and
+ * below). They change which kernel runs or how it stores, never the values it
+ * computes, except the two test hooks. They start at 0 (the defaults), apply
+ * to calls made after they are set, and are never read from the environment.
+ *  MGQ_GEMM_OPT_FORCE_1CTA    1: every call on the one-SM kernel (per-tensor
+ *                             calls otherwise run on the 2-SM pair kernel)
+ *  MGQ_GEMM_OPT_MX_PAIR       1: MX calls on the pair kernel (slower on the
+ *                             Mixtral shapes; the default is the one-SM kernel)
+ *  MGQ_GEMM_OPT_NV_PAIR       1: NVFP4 calls on the pair kernel (likewise)
+ *  MGQ_GEMM_OPT_DIRECT_STORE  1: the pair kernel stores from registers
+ *                             instead of through TMA
+ *  MGQ_GEMM_OPT_DEBUG_STALL   failure-detection test hook: 1 makes the
+ *                             producer issue no loads, so the pipeline waits
+ *                             run out and the call reports MGQ_ERR_TIMEOUT
+ *                             through mgq_get_error with nothing stored
+ *  MGQ_GEMM_OPT_WAIT_MS       limit of every pipeline wait in ms (0: 2000;
+ *                             at most 600000)
+ * Values outside {0, 1} (WAIT_MS: outside [0, 600000]) or an unknown option
+ * give MGQ_ERR_INVALID_ARG. Setting an option while another host thread
+ * launches a GEMM is safe; which setting that launch sees is unspecified. */
+typedef enum {
+  MGQ_GEMM_OPT_FORCE_1CTA = 0,
+  MGQ_GEMM_OPT_MX_PAIR = 1,
+  MGQ_GEMM_OPT_NV_PAIR = 2,
+  MGQ_GEMM_OPT_DIRECT_STORE = 3,
+  MGQ_GEMM_OPT_DEBUG_STALL = 4,
+  MGQ_GEMM_OPT_WAIT_MS = 5,
+  MGQ_GEMM_OPT_COUNT = 6
+} mgq_gemm_option;
+int mgq_set_gemm_option(int option, int64_t value);
+int mgq_get_gemm_option(int option, int64_t* value);
 
 /* ---- f1: gate/up GEMM with SwiGLU + quantisation in its epilogue ------------
  * The forward gate/up GEMM of mgq_grouped_gemm_fwd (A [R_cap, K], W1 [E, 2F, K]

@@ -133,3 +133,24 @@ def test_struct_layouts_match_the_header(tmp_path):
     O, Q = mgq.Operand, mgq.QDesc
     assert got == [ctypes.sizeof(O), O.ld.offset, O.dtype.offset, O.global_scale.offset, O.layout.offset,
                    ctypes.sizeof(Q), Q.amax_out.offset]
+
+
+def test_gemm_options_round_trip_and_validation(lib):
+    """The GEMM options are host state only: set, read back, reset; values
+    outside their range and unknown options are refused."""
+    from fp8_grouped_gemm_gb300 import mgq
+    for opt in (mgq.GEMM_OPT_FORCE_1CTA, mgq.GEMM_OPT_MX_PAIR, mgq.GEMM_OPT_NV_PAIR, mgq.GEMM_OPT_DIRECT_STORE,
+                mgq.GEMM_OPT_DEBUG_STALL):
+        assert mgq.get_gemm_option(opt) == 0
+        mgq.set_gemm_option(opt, 1)
+        assert mgq.get_gemm_option(opt) == 1
+        mgq.set_gemm_option(opt, 0)
+        assert lib.mgq_set_gemm_option(opt, 2) == mgq.ERR_INVALID_ARG
+        assert lib.mgq_set_gemm_option(opt, -1) == mgq.ERR_INVALID_ARG
+    mgq.set_gemm_option(mgq.GEMM_OPT_WAIT_MS, 50)
+    assert mgq.get_gemm_option(mgq.GEMM_OPT_WAIT_MS) == 50
+    mgq.set_gemm_option(mgq.GEMM_OPT_WAIT_MS, 0)
+    assert lib.mgq_set_gemm_option(mgq.GEMM_OPT_WAIT_MS, 600001) == mgq.ERR_INVALID_ARG
+    assert lib.mgq_set_gemm_option(6, 0) == mgq.ERR_INVALID_ARG
+    assert lib.mgq_set_gemm_option(-1, 0) == mgq.ERR_INVALID_ARG
+    assert lib.mgq_get_gemm_option(0, None) == mgq.ERR_INVALID_ARG

@@ -1,8 +1,9 @@
 """Failure detection without a GPU fault: a grouped GEMM whose pipeline never
 receives data (the producer is told to issue no loads) must come back with
 MGQ_ERR_TIMEOUT after its bounded waits, leave the output untouched, and leave
-the CUDA context usable for the next call. Runs in a subprocess because the
-test knobs are process environment variables."""
+the CUDA context usable for the next call. The stall and the short wait limit
+are the library's test hooks (mgq_set_gemm_option); the test runs in a
+subprocess so that its options cannot leak into other tests."""
 import os
 import subprocess
 import sys
@@ -36,8 +37,8 @@ SCRIPT = textwrap.dedent("""
         A = mgq.operand(ad, asc, K, mgq.E4M3)
         W = mgq.operand(wd, wsc, K, mgq.E4M3)
         y = torch.full((R, N), 7.0, dtype=torch.bfloat16, device=dev)
-        os.environ["MGQ_DEBUG_GEMM_STALL"] = "1"
-        os.environ["MGQ_DEBUG_WAIT_MS"] = "50"
+        mgq.set_gemm_option(mgq.GEMM_OPT_DEBUG_STALL, 1)
+        mgq.set_gemm_option(mgq.GEMM_OPT_WAIT_MS, 50)
         t0 = time.time()
         mgq.grouped_gemm_fwd(A, W, sc, offs, E, R, N, K, y)
         torch.cuda.synchronize()
@@ -46,8 +47,8 @@ SCRIPT = textwrap.dedent("""
         assert st == mgq.ERR_TIMEOUT, (name, st)
         assert bool(torch.all(y == 7.0)), name            # nothing stored
         assert dt < 10.0, (name, dt)
-        del os.environ["MGQ_DEBUG_GEMM_STALL"]
-        del os.environ["MGQ_DEBUG_WAIT_MS"]
+        mgq.set_gemm_option(mgq.GEMM_OPT_DEBUG_STALL, 0)
+        mgq.set_gemm_option(mgq.GEMM_OPT_WAIT_MS, 0)
         # the context is still usable: the same call without the stall is correct
         mgq.grouped_gemm_fwd(A, W, sc, offs, E, R, N, K, y)
         torch.cuda.synchronize()

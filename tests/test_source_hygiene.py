@@ -24,3 +24,11 @@ def test_no_batched_memcpy_calls():
 def test_build_targets_sm103a_only():
     from fp8_grouped_gemm_gb300 import _build
     assert _build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_library_reads_no_environment():
+    """Kernel choice and test hooks are explicit calls (mgq_set_gemm_option):
+    no stray environment variable can change what the library runs."""
+    for p in glob.glob(os.path.join(ROOT, "fp8_grouped_gemm_gb300", "csrc", "*")):
+        text = open(p, errors="replace").read()
+        assert "getenv" not in text, os.path.relpath(p, ROOT)
