@@ -379,6 +379,9 @@ DTYPE = {"mxfp8": "e4m3 fwd / e5m2 grads (MXFP8: E8M0 per 32, f32 accumulate)", 
 def dtype_of(w):
     if w.recipe == "mxfp8" and not w.backward:
         return "e4m3 (MXFP8: E8M0 per 32, f32 accumulate)"
+    if w.recipe == "blockwise" and w.backward:
+        return ("e4m3 fwd / e5m2 grads (blockwise float32 scales: 1x128 rows, 128x1 columns, 128x128 weight "
+                "tiles; f32 accumulate)")
     if w.recipe == "nvfp4" and w.backward:
         return ("e2m1 fwd and grads (NVFP4: 16-element ue4m3 scales + float32 global scale, weights in 16x16 "
                 "blocks, f32 accumulate)")
@@ -565,7 +568,7 @@ def measure(w, dev, world, steps, warmup, barrier, local, with_e2e=False):
 # the other configurations, each measured briefly in the same run beside the
 # headline (same timing rules; no end-to-end or CPU legs)
 OTHER_WORKLOADS = ("tiny", "mixtral_fwd", "scout_fwd", "finegrained_fwd", "mixtral_fwdbwd_mx",
-                   "mixtral_fwdbwd_nvfp4")
+                   "mixtral_fwdbwd_nvfp4", "scout_fwdbwd")
 OTHER_STEPS = 20
 
 

@@ -286,6 +286,8 @@ __global__ void __launch_bounds__(256, SC == MGQ_TENSOR_F32 ? 3 : 2) unpermute_b
       if (SC == MGQ_MX32_E8M0 || SC == MGQ_NV16_UE4M3)
         for (int b4 = lane; b4 < H / (4 * kBlk); b4 += 32)
           *reinterpret_cast<uint32_t*>(a.scales + tiled_scale_offset(r, (int64_t)b4 * 4, H / (4 * kBlk))) = 0u;
+      else if (SC == MGQ_BLK_1x128_F32)
+        for (int b = lane; b < H / 128; b += 32) reinterpret_cast<float*>(a.scales)[(int64_t)b * a.R_cap + r] = 0.0f;
     }
     return;
   }
@@ -655,9 +657,9 @@ int check_q(const mgq_qdesc* q) {
     return MGQ_ERR_UNSUPPORTED;
   }
   if (q->col.data && !aligned16(q->col.data)) return MGQ_ERR_INVALID_ARG;
-  if (q->col.data && q->scaling == MGQ_MX32_E8M0 && (!q->col.scale || !aligned16(q->col.scale)))
+  if (q->col.data && (q->scaling == MGQ_MX32_E8M0 || q->scaling == MGQ_BLK_1x128_F32) &&
+      (!q->col.scale || !aligned16(q->col.scale)))
     return MGQ_ERR_INVALID_ARG;
-  if (q->col.data && q->scaling == MGQ_BLK_1x128_F32) return MGQ_ERR_UNSUPPORTED;
   return MGQ_OK;
 }
 
@@ -839,7 +841,9 @@ int mgq_moe_unpermute_bwd(const void* dout_bf16, const void* y_bf16, const int32
   a.token_blocks = (int)std::min<int64_t>(((int64_t)T * k + kWarps - 1) / kWarps,
                                           (int64_t)num_sms() * (q->scaling == MGQ_TENSOR_F32 ? 3 : 2));
   const unsigned grid = (unsigned)(a.token_blocks + E);
-  if (q->col.data && q->scaling != MGQ_TENSOR_F32 && q->scaling != MGQ_MX32_E8M0 && !nv) return MGQ_ERR_UNSUPPORTED;
+  if (q->col.data && q->scaling != MGQ_TENSOR_F32 && q->scaling != MGQ_MX32_E8M0 &&
+      q->scaling != MGQ_BLK_1x128_F32 && !nv)
+    return MGQ_ERR_UNSUPPORTED;
   if (nv) {
     unpermute_bwd_kernel<MGQ_NV16_UE4M3, MGQ_E2M1><<<grid, 256, 0, s>>>(a);
     MGQ_LAUNCH_CHECK();
@@ -887,7 +891,13 @@ int mgq_block_quantize(const void* x_bf16, int64_t G, int64_t M, int64_t K, cons
   if (q && q->scaling == MGQ_BLK_128x128_F32) {
     MGQ_CHECK_ARG(q->row.data && q->row.scale && aligned16(q->row.data) && x_bf16 && aligned16(x_bf16));
     MGQ_CHECK_ARG(G >= 1 && M > 0 && K > 0 && M % 128 == 0 && K % 128 == 0);
-    if (q->col.data) return MGQ_ERR_UNSUPPORTED;
+    if (q->col.data) {
+      // both copies in one tile pass: the column-wise copy holds the
+      // transposed codes and the transposed tile scales
+      MGQ_CHECK_ARG(aligned16(q->col.data) && q->col.scale);
+      if (q->dtype != MGQ_E4M3 && q->dtype != MGQ_E5M2) return MGQ_ERR_UNSUPPORTED;
+      return rowcol_plain(static_cast<const uint16_t*>(x_bf16), G, M, K, q, as_stream(stream));
+    }
     const unsigned grid = (unsigned)(G * (M / 128) * (K / 128));
     cudaStream_t s = as_stream(stream);
     if (q->dtype == MGQ_E4M3)
@@ -923,12 +933,13 @@ int mgq_grouped_quantize(const void* x_bf16, int64_t R_cap, int64_t C, const int
   MGQ_CHECK_ARG(x_bf16 && aligned16(x_bf16) && offsets && E >= 1 && E <= 1024);
   MGQ_CHECK_ARG(C > 0 && C % 128 == 0 && R_cap > 0 && R_cap % 128 == 0 && R_cap < (1ll << 31));
   const int sc = q->scaling;
-  if (sc != MGQ_MX32_E8M0 && sc != MGQ_TENSOR_F32 && sc != MGQ_NV16_UE4M3) return MGQ_ERR_UNSUPPORTED;
+  if (sc != MGQ_MX32_E8M0 && sc != MGQ_TENSOR_F32 && sc != MGQ_NV16_UE4M3 && sc != MGQ_BLK_1x128_F32)
+    return MGQ_ERR_UNSUPPORTED;
   int* err = error_word();
   if (!err) return MGQ_ERR_CUDA;
   cudaStream_t s = as_stream(stream);
   // column blocks run inside the groups: group starts on block boundaries
-  const int blk = sc == MGQ_MX32_E8M0 ? 32 : (sc == MGQ_NV16_UE4M3 ? 16 : 1);
+  const int blk = sc == MGQ_MX32_E8M0 ? 32 : (sc == MGQ_NV16_UE4M3 ? 16 : (sc == MGQ_BLK_1x128_F32 ? 128 : 1));
   group_layout_check_kernel<<<1, 256, 0, s>>>(offsets, E, R_cap, blk, err);
   MGQ_LAUNCH_CHECK();
   if (sc == MGQ_NV16_UE4M3) {   // s_g needs the amax of the rows in use first

@@ -86,8 +86,11 @@ struct GemmParams {
   const uint8_t* sfb;
   int64_t sfb_kb4;
   const float* sa;    // tensor: s_a; block: scale_inv_a [K/128][sa_ld]; NVFP4: s_g of A
-  const float* sb;    // tensor: s_b per expert; block: scale_inv_b [E][N/128][K/128]; NVFP4: s_g per expert
+  const float* sb;    // tensor: s_b per expert; block rows mode: scale_inv_b [E][N/128][K/128], block
+                      // contract mode: scale_inv_b [R_cap/128][sb_ld] (one per column and 128 rows);
+                      // NVFP4: s_g per expert
   int64_t sa_ld;
+  int64_t sb_ld;
   void* out;
   int64_t ldo;
   int out_f32;
@@ -889,23 +892,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       uint32_t r[4][32];
       if (BLOCK) {
-        // promotion: acc += partial(stage) * s_a[row, kb] * s_b[n block, kb]
+        // promotion: acc += partial(stage) * s_a[row, kb] * s_b[n block, kb];
+        // contract mode (wgrad, 128x1 blocks of both operands along the
+        // group's rows): acc += partial(stage) * s_a[row, kb] * s_b[column, kb]
         const float* sa_row = p.sa + (tl.row_a + row_in_tile);
-        const float* sb_blk = p.sb + ((int64_t)tl.e * (p.N / 128) + (col0 / 128)) * (p.K / 128);
+        const float* sb_blk = MODE == kModeRows
+                                  ? p.sb + ((int64_t)tl.e * (p.N / 128) + (col0 / 128)) * (p.K / 128)
+                                  : p.sb + col0;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i) r[c][i] = 0u;   // +0.0f
         // both scales are loaded one stage ahead of their partial product
         float sa_next = sa_row[(tl.kx0 / 128) * p.sa_ld];
-        float sb_next = sb_blk[tl.kx0 / 128];
+        float sb_next = MODE == kModeRows ? sb_blk[tl.kx0 / 128] : 1.0f;
         bool alive = true;
         for (int s = 0; s < tl.nst; ++s) {
           const uint32_t a = tc % kAcc, aph = (tc / kAcc) & 1;
           const float f = sa_next * sb_next;
+          // contract mode: this stage's 128 column scales of B (this half's columns)
+          const float* sb_cols = sb_blk + (tl.kx0 / 128 + s) * p.sb_ld;
           if (s + 1 < tl.nst) {
             sa_next = sa_row[(tl.kx0 / 128 + s + 1) * p.sa_ld];
-            sb_next = sb_blk[tl.kx0 / 128 + s + 1];
+            if (MODE == kModeRows) sb_next = sb_blk[tl.kx0 / 128 + s + 1];
           }
           if (__any_sync(0xFFFFFFFFu, *s_abort != 0)) { alive = false; break; }
           const bool got = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&tmem_full[a], aph, p.wait_ns));
@@ -924,9 +933,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_ld_32x32b_x16(taddr + c * 16, v);
             ptx::tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              r[c / 2][(c & 1) * 16 + i] =
-                  __float_as_uint(fmaf(__uint_as_float(v[i]), f, __uint_as_float(r[c / 2][(c & 1) * 16 + i])));
+            for (int j = 0; j < 4; ++j) {
+              // contract mode: 4 column scales at a time (the same for every
+              // lane: broadcast loads)
+              float4 fq = make_float4(f, f, f, f);
+              if (MODE == kModeContract) {
+                const float4 q4 = __ldg(reinterpret_cast<const float4*>(sb_cols + c * 16) + j);
+                fq = make_float4(f * q4.x, f * q4.y, f * q4.z, f * q4.w);
+              }
+              const float fj[4] = {fq.x, fq.y, fq.z, fq.w};
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                const int i = 4 * j + t;
+                r[c / 2][(c & 1) * 16 + i] =
+                    __float_as_uint(fmaf(__uint_as_float(v[i]), fj[t], __uint_as_float(r[c / 2][(c & 1) * 16 + i])));
+              }
+            }
           }
           ptx::tc_fence_before();
           ptx::mbar_arrive(&tmem_empty[a]);
@@ -1485,7 +1507,7 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
   int kind;
   if (scaling == MGQ_MX32_E8M0) kind = kKindMX;
   else if (scaling == MGQ_TENSOR_F32) kind = kKindTensor;
-  else if (scaling == MGQ_BLK_1x128_F32 && mode == kModeRows) kind = kKindBlock;
+  else if (scaling == MGQ_BLK_1x128_F32) kind = kKindBlock;
   else if (scaling == MGQ_NV16_UE4M3) kind = kKindNV;
   else return MGQ_ERR_UNSUPPORTED;
   const bool mx = kind == kKindMX;
@@ -1499,7 +1521,7 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
     return MGQ_ERR_UNSUPPORTED;
   if (nv != (A->dtype == MGQ_E2M1) || nv != (B->dtype == MGQ_E2M1)) return MGQ_ERR_UNSUPPORTED;
   MGQ_CHECK_ARG(A->scale && B->scale);
-  if (mx || nv) MGQ_CHECK_ARG(aligned16(A->scale) && aligned16(B->scale));
+  if (mx || nv || kind == kKindBlock) MGQ_CHECK_ARG(aligned16(A->scale) && aligned16(B->scale));
   if (nv) MGQ_CHECK_ARG(A->global_scale && B->global_scale && K % 256 == 0 && A->ld % 256 == 0 && B->ld % 256 == 0);
   // operand bytes per element: e2m1 codes are packed two per byte
   const int64_t ebytes_den = nv ? 2 : 1;
@@ -1544,7 +1566,10 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
   p.sfb = static_cast<const uint8_t*>(B->scale);
   p.sa = nv ? A->global_scale : static_cast<const float*>(A->scale);
   p.sb = nv ? B->global_scale : static_cast<const float*>(B->scale);
-  p.sa_ld = R_cap;
+  // block scales: A's scale_inv [k block][rows of A]; contract mode B's
+  // [k block][rows of B = output columns]
+  p.sa_ld = mode == kModeRows ? R_cap : N;
+  p.sb_ld = mode == kModeRows ? 0 : K;
   p.out = out;
   p.ldo = (mode == kModeRows) ? N : K;
   p.out_f32 = out_dtype == MGQ_OUT_F32;
@@ -1740,6 +1765,7 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
   }
   if (kind == kKindMX) return launch_gemm<kModeContract, kKindMX>(ta, tb, to, th, p, s);
   if (kind == kKindNV) return launch_gemm<kModeContract, kKindNV>(ta, tb, to, th, p, s);
+  if (kind == kKindBlock) return launch_gemm<kModeContract, kKindBlock>(ta, tb, to, th, p, s);
   return launch_gemm<kModeContract, kKindTensor>(ta, tb, to, th, p, s);
 }
 

@@ -11,11 +11,17 @@
 // A tile is read once from its source (a plain bf16 matrix, SwiGLU of the
 // gate/up output, dSwiGLU, or rows gathered through the routing), held as bf16
 // in shared memory, and written as
-//   row-wise codes [rows, C] (MX blocks of 32 along C, NVFP4 blocks of 16), and
-//   column-wise codes [C, M] per group of M rows (blocks along the rows),
+//   row-wise codes [rows, C] (MX blocks of 32 along C, NVFP4 blocks of 16,
+//   blockwise 1x128 blocks), and
+//   column-wise codes [C, M] per group of M rows (blocks along the rows: MX 32,
+//   NVFP4 16, blockwise 128x1),
 // with per-tensor scales (the column copy is then the transposed cast), E8M0
-// block scales, or NVFP4 ue4m3 block scales with s_g from an amax pre-pass,
-// all in the 128x4-tiled scale layout.
+// block scales or NVFP4 ue4m3 block scales with s_g from an amax pre-pass (both
+// in the 128x4-tiled scale layout), or blockwise float32 scale_inv stored
+// block-major: row-wise [C/128][rows], column-wise [M/128][G*C]. Weights with
+// 128x128 tiles (one scale per tile) get both copies from one pass, the
+// column-wise copy the transposed codes with the transposed tile scales
+// ([G][M/128][C/128] and [G][C/128][M/128]).
 // Kernels: quant_rowcol_kernel (one tile per CTA: plain and computed sources),
 // quant_rowcol_stream_kernel (gathered rows: a CTA walks a range of tiles and
 // stages the next with cp.async), quant_nv2d_kernel (NVFP4 weights with 16x16
@@ -220,9 +226,13 @@ __device__ __forceinline__ void col_block_out(float* v, uint32_t amax_bits, floa
 // warp at a time; 4 lanes per row, lane takes one 32-column block. The lane
 // reads its four 16-byte chunks in the order q ^ sw (sw = 0 for blocks 0, 1 and
 // 2 for blocks 2, 3), so the 8 lanes of a quarter warp hit 8 different bank groups.
+// srow (gathered sources): the tile rows' source offsets, negative for filler
+// rows, whose blockwise scale_inv is written as 0 like their codes (zero
+// codes and zero scales for padding)
 template <int P, int SC, int DT>
 __device__ __forceinline__ void row_phase(const uint16_t* tile, int64_t r0, int64_t nrows, int64_t c0, float ts,
-                                          const RowColArgs& a, int warp, uint32_t lane) {
+                                          const RowColArgs& a, int warp, uint32_t lane,
+                                          const int64_t* srow = nullptr) {
   const int seg = lane & 3;
   const int sw = (seg >> 1) * 2;
 #pragma unroll 1
@@ -269,6 +279,18 @@ __device__ __forceinline__ void row_phase(const uint16_t* tile, int64_t r0, int6
       const int e = mx_exponent(fold_bf16x2(absmax_bf16x2_final(acc)), FmtInfo<DT>::emax, a.rceil != 0);
       mult = mx_multiplier(e);
       if (r < nrows) a.row_scales[tiled_scale_offset(r, cb / 32, a.C / 128)] = (uint8_t)mx_scale_code(e);
+    } else if constexpr (SC == MGQ_BLK_1x128_F32) {
+      // the row's 128 tile columns are one block: the 4 lanes of the row agree on its amax
+      uint32_t acc = 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc = absmax_acc_bf16x2(acc, ww[i]);
+      uint32_t m = fold_bf16x2(absmax_bf16x2_final(acc));
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+      mult = blk_scale<DT>(m);
+      if (seg == 0 && r < nrows)
+        reinterpret_cast<float*>(a.row_scales)[((c0 + p * a.part_off) / 128) * a.rows_cap + r] =
+            (srow && srow[rr] < 0) ? 0.0f : __fdiv_rn(1.0f, mult);
     }
     uint32_t cw[8];        // codes in the order held (chunk q ^ sw in cw[2q], cw[2q + 1])
 #pragma unroll
@@ -288,16 +310,58 @@ __device__ __forceinline__ void row_phase(const uint16_t* tile, int64_t r0, int6
 // columns of one 32-row block (one MX block each); its 32 output bytes per
 // column are contiguous. FAC: values are fac[row] * tile (float32 products).
 // am: running |v| maximum (float bits) for the per-tensor amax.
+// Blockwise (128x1 blocks: the tile's 128 rows): the four 32-row partial
+// maxima of each column meet in s_cm [4][TC]; every thread of the CTA calls.
+template <int DT>
+__device__ __forceinline__ float col_blk_scale(uint32_t* s_cm, int rb, int col, uint32_t part_max,
+                                               const RowColArgs& a, int64_t crow, int64_t rtile) {
+  s_cm[rb * TC + col] = part_max;
+  __syncthreads();
+  const uint32_t m = max(max(s_cm[col], s_cm[TC + col]), max(s_cm[2 * TC + col], s_cm[3 * TC + col]));
+  const float s = blk_scale<DT>(m);
+  if (rb == 0) reinterpret_cast<float*>(a.col_scales)[rtile * ((a.rows_cap / a.M) * a.C) + crow] = __fdiv_rn(1.0f, s);
+  return s;
+}
+
 template <int P, int SC, int DT, bool FAC>
 __device__ __forceinline__ void col_phase(const uint16_t* tile, const float* fac, int64_t g, int64_t r0, int64_t c0,
-                                          float ts, const RowColArgs& a, int tid, uint32_t& am) {
+                                          float ts, const RowColArgs& a, int tid, uint32_t& am, uint32_t* s_cm) {
   const int cp = tid & 63, rb = (tid >> 6) & 3;
   const int cc = 2 * cp;
   const int64_t rg = r0 - g * a.M + 32 * rb;                 // row inside the group
 #pragma unroll 1
   for (int p = 0; p < P; ++p) {
     const int64_t crow = g * a.C + c0 + p * a.part_off + cc;  // row of the column-wise output
-    if constexpr (FAC) {
+    if constexpr (SC == MGQ_BLK_1x128_F32) {
+      // 128x1 blocks: per column the amax of the tile's 128 rows, then the
+      // column's codes with its scale (two columns per thread)
+      const int64_t rtile = (r0 - g * a.M) / TR;
+      auto val = [&](int i, int h) {
+        const float x = __uint_as_float((uint32_t)tile[(p * TR + 32 * rb + i) * LD + cc + h] << 16);
+        if constexpr (FAC) return __fmul_rn(fac[32 * rb + i], x);
+        else return x;
+      };
+      uint32_t m2[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t m = 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) m = max(m, __float_as_uint(val(i, h)) & 0x7FFFFFFFu);
+        m2[h] = m;
+      }
+      float sc[2];
+      sc[0] = col_blk_scale<DT>(s_cm, rb, cc, m2[0], a, crow, rtile);
+      __syncthreads();
+      sc[1] = col_blk_scale<DT>(s_cm, rb, cc + 1, m2[1], a, crow + 1, rtile);
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = val(i, h);
+        col_block_out<MGQ_TENSOR_F32, DT>(v, 0u, sc[h], a, crow + h, rg);
+      }
+      __syncthreads();     // s_cm is reused by the next part / tile
+    } else if constexpr (FAC) {
       // one column at a time (32 products live)
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
@@ -361,9 +425,14 @@ template <class Src, int SC, int DT>
 __global__ void __launch_bounds__(256, Src::kParts == 2 ? 3 : 4)
     quant_rowcol_kernel(const Src src, const RowColArgs a) {
   constexpr int P = Src::kParts;
+  // 128x128 weight tiles: one scale per tile, then both copies cast like a
+  // per-tensor scale (the column-wise copy is the transposed cast)
+  constexpr bool T128 = SC == MGQ_BLK_128x128_F32;
+  constexpr int SCC = T128 ? MGQ_TENSOR_F32 : SC;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint16_t* tile = reinterpret_cast<uint16_t*>(smem_raw);   // [P][TR][LD]
   __shared__ uint32_t s_amax[8];
+  __shared__ uint32_t s_cm[SC == MGQ_BLK_1x128_F32 ? 4 * TC : 1];
   const int tid = threadIdx.x, warp = tid >> 5;
   const uint32_t lane = tid & 31;
   const int64_t nrows = a.rows_used ? (int64_t)*a.rows_used : a.rows_cap;
@@ -391,7 +460,7 @@ __global__ void __launch_bounds__(256, Src::kParts == 2 ? 3 : 4)
       for (int i = 0; i < 8; ++i) {
         const int chunk = tid + 256 * i;
         const int rr = chunk >> 4, cc = (chunk & 15) * 8;
-        if (SC == MGQ_TENSOR_F32)
+        if (SC == MGQ_TENSOR_F32 || T128)
           am2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(am2, w[i].x), w[i].y), w[i].z), w[i].w);
         *reinterpret_cast<uint4*>(&tile[rr * LD + cc]) = w[i];
       }
@@ -428,9 +497,27 @@ __global__ void __launch_bounds__(256, Src::kParts == 2 ? 3 : 4)
     }
     }
     __syncthreads();
-    if (a.row_codes) row_phase<P, SC, DT>(tile, r0, nrows, c0, ts, a, warp, lane);
+    float tsc = ts;
+    if constexpr (T128) {
+      // the tile's amax (CTA reduction) sets its scale; scale_inv of both copies
+      uint32_t m = warp_max_u32(fold_bf16x2(am2));
+      if (lane == 0) s_amax[warp] = m;
+      __syncthreads();
+      m = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m = max(m, s_amax[i]);
+      tsc = blk_scale<DT>(m);
+      if (tid == 0) {
+        const float sinv = __fdiv_rn(1.0f, tsc);
+        const int64_t mt = (r0 - g * a.M) / TR, ct = c0 / TC;
+        reinterpret_cast<float*>(a.row_scales)[(r0 / TR) * (a.C / TC) + ct] = sinv;
+        if (a.col_codes) reinterpret_cast<float*>(a.col_scales)[(g * (a.C / TC) + ct) * (a.M / TR) + mt] = sinv;
+      }
+      __syncthreads();   // s_amax is reused by the next row tile
+    }
+    if (a.row_codes) row_phase<P, SCC, DT>(tile, r0, nrows, c0, tsc, a, warp, lane);
     uint32_t am_unused = 0;
-    if (a.col_codes) col_phase<P, SC, DT, false>(tile, nullptr, g, r0, c0, ts, a, tid, am_unused);
+    if (a.col_codes) col_phase<P, SCC, DT, false>(tile, nullptr, g, r0, c0, tsc, a, tid, am_unused, s_cm);
     if (SC == MGQ_TENSOR_F32 && a.amax_out) flush_amax(fold_bf16x2(am2), a.amax_out, g, s_amax, tid);
     __syncthreads();   // the tile is reused by the next row tile
   }
@@ -459,6 +546,7 @@ __global__ void __launch_bounds__(256, 3) quant_rowcol_stream_kernel(const Src s
   __shared__ int64_t s_off[2][TR];
   __shared__ float s_fac[2][TR];
   __shared__ uint32_t s_amax[8];
+  __shared__ uint32_t s_cm[SC == MGQ_BLK_1x128_F32 ? 4 * TC : 1];
   const int tid = threadIdx.x, warp = tid >> 5;
   const uint32_t lane = tid & 31;
   const int64_t nrows = a.rows_used ? (int64_t)*a.rows_used : a.rows_cap;
@@ -517,8 +605,8 @@ __global__ void __launch_bounds__(256, 3) quant_rowcol_stream_kernel(const Src s
     const int64_t r0 = (int64_t)rt * TR, c0 = (int64_t)ct * TC;
     const uint16_t* t = tiles + buf * TR * LD;
     if (SC == MGQ_NV16_UE4M3 && ct == 0 && r0 == g * a.M && tid == 0) a.s_out[g] = ts;
-    if (!Src::kColumnsOnly && a.row_codes) row_phase<1, SC, DT>(t, r0, nrows, c0, ts, a, warp, lane);
-    col_phase<1, SC, DT, Src::kFactor>(t, s_fac[rt & 1], g, r0, c0, ts, a, tid, am);
+    if (!Src::kColumnsOnly && a.row_codes) row_phase<1, SC, DT>(t, r0, nrows, c0, ts, a, warp, lane, s_off[rt & 1]);
+    col_phase<1, SC, DT, Src::kFactor>(t, s_fac[rt & 1], g, r0, c0, ts, a, tid, am, s_cm);
     __syncthreads();   // the buffer is refilled two items on
     if (rt_n != rt || item + 1 == i1) {
       if (SC == MGQ_TENSOR_F32 && a.amax_out) flush_amax(am, a.amax_out, g, s_amax, tid);
@@ -583,6 +671,19 @@ int launch_rowcol(const Src& src, const mgq_qdesc* q, RowColArgs a, cudaStream_t
   }
   if (sc == MGQ_MX32_E8M0 && dt == MGQ_E4M3) return launch_rowcol_t<Src, MGQ_MX32_E8M0, MGQ_E4M3>(src, a, s);
   if (sc == MGQ_MX32_E8M0 && dt == MGQ_E5M2) return launch_rowcol_t<Src, MGQ_MX32_E8M0, MGQ_E5M2>(src, a, s);
+  // blockwise: 1x128 rows / 128x1 columns inside 128-row groups; 128x128
+  // tiles for plain matrices (weights)
+  if (sc == MGQ_BLK_1x128_F32 || sc == MGQ_BLK_128x128_F32) {
+    // (the gathered dY source writes column-wise codes only)
+    if (a.M % TR != 0 || (a.row_codes && !a.row_scales) || (a.col_codes && !a.col_scales)) return MGQ_ERR_INVALID_ARG;
+    if (sc == MGQ_BLK_1x128_F32 && dt == MGQ_E4M3) return launch_rowcol_t<Src, MGQ_BLK_1x128_F32, MGQ_E4M3>(src, a, s);
+    if (sc == MGQ_BLK_1x128_F32 && dt == MGQ_E5M2) return launch_rowcol_t<Src, MGQ_BLK_1x128_F32, MGQ_E5M2>(src, a, s);
+    if constexpr (std::is_same<Src, SrcPlain>::value) {
+      if (dt == MGQ_E4M3) return launch_rowcol_t<Src, MGQ_BLK_128x128_F32, MGQ_E4M3>(src, a, s);
+      if (dt == MGQ_E5M2) return launch_rowcol_t<Src, MGQ_BLK_128x128_F32, MGQ_E5M2>(src, a, s);
+    }
+    return MGQ_ERR_UNSUPPORTED;
+  }
   // per-tensor column copies of gathered rows are transposed casts of the row codes
   if constexpr (std::is_same<Src, SrcGatherX>::value || std::is_same<Src, SrcGatherDy>::value) {
     return MGQ_ERR_UNSUPPORTED;

@@ -495,9 +495,9 @@ int check_permute_q(const mgq_qdesc* q, int align) {
   else
     return MGQ_ERR_UNSUPPORTED;
   if (q->col.data) {
-    if (q->scaling != MGQ_TENSOR_F32 && q->scaling != MGQ_MX32_E8M0) return MGQ_ERR_UNSUPPORTED;
-    MGQ_CHECK_ARG(aligned16(q->col.data) && align % 32 == 0);
-    if (q->scaling == MGQ_MX32_E8M0) MGQ_CHECK_ARG(q->col.scale && aligned16(q->col.scale));
+    // column blocks run inside the groups: groups padded to the block (MX 32, blockwise 128)
+    MGQ_CHECK_ARG(aligned16(q->col.data) && align % (q->scaling == MGQ_BLK_1x128_F32 ? 128 : 32) == 0);
+    if (q->scaling != MGQ_TENSOR_F32) MGQ_CHECK_ARG(q->col.scale && aligned16(q->col.scale));
   }
   return MGQ_OK;
 }
@@ -533,10 +533,12 @@ int route_impl(const int32_t* topk_idx, int T, int k, int E, int align, int32_t*
   return MGQ_OK;
 }
 
-// MX with a column-wise copy and no bf16 copy: one tile pass over the
-// permuted rows writes both copies (needs the final src_row)
+// block scales (MX, NVFP4, blockwise) with a column-wise copy and no bf16
+// copy: one tile pass over the permuted rows writes both copies (needs the
+// final src_row)
 bool permute_fused_rowcol(const mgq_qdesc* q, const void* out_bf16) {
-  return (q->scaling == MGQ_MX32_E8M0 || q->scaling == MGQ_NV16_UE4M3) && q->col.data && !out_bf16;
+  return (q->scaling == MGQ_MX32_E8M0 || q->scaling == MGQ_NV16_UE4M3 || q->scaling == MGQ_BLK_1x128_F32) &&
+         q->col.data && !out_bf16;
 }
 
 // permute + quantise of the token rows to their routed rows (row_id_map final,
@@ -649,7 +651,8 @@ int mgq_moe_permute_routed(const void* x_bf16, int T, int H, int k, int E, const
   int rc = check_route_args(T, k, E, 1, R_cap, row_id_map, src_row, offsets, counts);
   if (rc != MGQ_OK) return rc;
   MGQ_CHECK_ARG(H > 0 && H % 128 == 0 && (T == 0 || x_bf16) && aligned16(x_bf16) && aligned16(out_bf16));
-  if ((rc = check_permute_q(q, 32)) != MGQ_OK) return rc;
+  // (the group alignment a column copy needs is the routing's, stated by the caller)
+  if ((rc = check_permute_q(q, 128)) != MGQ_OK) return rc;
   int* err = error_word();
   if (!err) return MGQ_ERR_CUDA;
   // the kernels only read row_id_map and src_row when the rows are final

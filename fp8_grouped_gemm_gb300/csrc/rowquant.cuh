@@ -19,6 +19,15 @@ __device__ __forceinline__ uint32_t absmax_bits_f32(const float* v, int n) {
   return m;
 }
 
+// Blockwise (1x128, 128x1, 128x128) scale of a block from the float bits of its
+// amax: s = max_finite / amax (IEEE division), 1 for an all-zero block, the
+// largest float32 when the quotient overflows. The stored scale_inv is 1 / s.
+template <int DT>
+__device__ __forceinline__ float blk_scale(uint32_t amax_bits) {
+  const float s = (amax_bits == 0) ? 1.0f : __fdiv_rn(FmtInfo<DT>::fmax, __uint_as_float(amax_bits));
+  return isinf(s) ? 3.40282347e38f : s;
+}
+
 // v: the lane's 32 values; amax_bits: float bits of max |v| of this lane's
 // 32 values; ts: per-tensor scale (MGQ_TENSOR_F32)
 template <int SC, int DT>

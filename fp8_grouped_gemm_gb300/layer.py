@@ -18,9 +18,10 @@ backward: moe_unpermute_bwd (+ quantise dY, dprobs) -> grouped_gemm_dgrad and
 then:     amax_history_update (delayed scaling)
 
 The backward GEMMs contract over the other dimension of their operands (dgrad
-over the weight's rows, wgrad over the tokens). With block scales (MXFP8) each
-of those operands is requantised column-wise with blocks along the new
-contraction. With per-tensor scales the column-wise copy would hold the same
+over the weight's rows, wgrad over the tokens). With block scales (MXFP8,
+NVFP4, blockwise 1x128 / 128x128) each of those operands is requantised
+column-wise with blocks along the new contraction (blockwise: 128x1 blocks
+along each expert's tokens; weights' 128x128 tiles are simply transposed). With per-tensor scales the column-wise copy would hold the same
 codes transposed, so by default the delayed recipe writes none and hands the
 row-wise codes to the GEMMs as MN-major operands (``col_copies=True`` keeps
 the explicit copies).
@@ -59,7 +60,7 @@ class ExpertLayer:
         # column-wise copy (the blockwise 1x128 block spans both epilogue
         # halves); dSwiGLU in the down dgrad epilogue for per-tensor training
         self.fused_swiglu = fuse_swiglu and (self.recipe in ("mxfp8", "nvfp4") or self.mn)
-        if self.train and self.recipe not in ("delayed", "mxfp8", "nvfp4"):
+        if self.train and self.recipe not in ("delayed", "mxfp8", "nvfp4", "blockwise"):
             raise NotImplementedError(f"backward with {self.recipe}")
         self.scaling = {"mxfp8": mgq.MX32_E8M0, "delayed": mgq.TENSOR_F32,
                         "blockwise": mgq.BLK_1x128_F32, "nvfp4": mgq.NV16_UE4M3}[self.recipe]
@@ -135,6 +136,19 @@ class ExpertLayer:
             self.dw2 = torch.empty(E, H, F, **f32)
             self.dxp = torch.empty(R, H, **bf)
             self.dx = torch.empty(T, H, **bf)
+            if blk:
+                # float32 scale_inv: row-wise [C/128][R_cap], column-wise
+                # [R_cap/128][C] (128x1 blocks along each expert's tokens);
+                # weights' column-wise copies carry the transposed 128x128
+                # tile scales [E][K/128][N/128]
+                self.xcs = torch.empty(R // 128, H, **f32)
+                self.hcs = torch.empty(R // 128, F, **f32)
+                self.w1cs = torch.empty(E, H // 128, 2 * F // 128, **f32)
+                self.w2cs = torch.empty(E, F // 128, H // 128, **f32)
+                self.dy2s = torch.empty(H // 128, R, **f32)
+                self.dy2cs = torch.empty(R // 128, H, **f32)
+                self.dy1s = torch.empty(2 * F // 128, R, **f32)
+                self.dy1cs = torch.empty(R // 128, 2 * F, **f32)
             if mx:
                 ms = mgq.mx_scale_bytes
                 self.xcs = torch.empty(ms(H, R), **u8)
@@ -225,8 +239,12 @@ class ExpertLayer:
             q1 = mgq.qdesc(mgq.E4M3, self.scaling, self.w1q, self.w1s, *c1)
             q2 = mgq.qdesc(mgq.E4M3, self.scaling, self.w2q, self.w2s, *c2)
         elif self.scaling == mgq.BLK_1x128_F32:
-            q1 = mgq.qdesc(mgq.E4M3, mgq.BLK_128x128_F32, self.w1q, self.w1s)
-            q2 = mgq.qdesc(mgq.E4M3, mgq.BLK_128x128_F32, self.w2q, self.w2s)
+            # 128x128 tiles; training: the column-wise copy (transposed codes
+            # and tile scales) from the same pass
+            c1 = (self.w1col, self.w1cs) if self.train else (None, None)
+            c2 = (self.w2col, self.w2cs) if self.train else (None, None)
+            q1 = mgq.qdesc(mgq.E4M3, mgq.BLK_128x128_F32, self.w1q, self.w1s, *c1)
+            q2 = mgq.qdesc(mgq.E4M3, mgq.BLK_128x128_F32, self.w2q, self.w2s, *c2)
         else:
             q1 = mgq.qdesc(mgq.E4M3, self.scaling, self.w1q, None, self.w1col, None, self._fs(2, E), self._fa(2, E))
             q2 = mgq.qdesc(mgq.E4M3, self.scaling, self.w2q, None, self.w2col, None, self._fs(2 + E, E),
@@ -301,7 +319,9 @@ class ExpertLayer:
             s_w2c, s_w1c = self._fs(2 + E, E), self._fs(2, E)
             s_hc, s_xc = self._fs(1), self._fs(0)
         else:
-            sc = mgq.MX32_E8M0
+            # block scales (MX E8M0 per 32, or blockwise float32 1x128 / 128x1):
+            # row-wise and column-wise copies of each gradient
+            sc = self.scaling
             q2 = mgq.qdesc(mgq.E5M2, sc, self.dy2q, self.dy2s, self.dy2col, self.dy2cs)
             q1 = mgq.qdesc(mgq.E5M2, sc, self.dy1q, self.dy1s, self.dy1col, self.dy1cs)
             s_dy2r, s_dy2c, s_dy1r, s_dy1c = self.dy2s, self.dy2cs, self.dy1s, self.dy1cs

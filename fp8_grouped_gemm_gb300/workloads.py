@@ -94,6 +94,11 @@ WORKLOADS = {
     # quantisation giving both copies; column-wise 16x1 blocks along tokens)
     "mixtral_fwdbwd_nvfp4": Workload("mixtral_fwdbwd_nvfp4", 5, 8, 2, 16384, 4096, 14336, "topk",
                                      "nvfp4", backward=True, outlier_frac=0.001),
+    # the Scout-shaped experts trained with blockwise FP8 (e4m3 forward, e5m2
+    # gradients; 1x128 row-wise and 128x1 column-wise activation / gradient
+    # blocks, 128x128 weight tiles)
+    "scout_fwdbwd": Workload("scout_fwdbwd", 3, 16, 1, 16384, 5120, 8192, "zipf", "blockwise",
+                             backward=True, n_empty=2),
 }
 
 

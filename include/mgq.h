@@ -167,9 +167,11 @@ int mgq_get_error(void* stream, int* device_status);
  *  topk_idx    device [T, k] int32, distinct experts per token in [0, E)
  *              (out of range: the entry is skipped, MGQ_ERR_DEVICE_INDEX set)
  *  q           quantisation of the permuted rows (row: [R_cap, H]; col:
- *              [H, R_cap], MX / NVFP4 blocks along the rows, per-tensor the
- *              transposed row codes; e2m1: [R_cap, H/2] and [H, R_cap/2]
- *              bytes, s_g from an amax pre-pass); NULL = no quantised output
+ *              [H, R_cap], MX / NVFP4 / blockwise 128x1 blocks along the rows
+ *              of each group (blockwise: align a multiple of 128, scale_inv
+ *              [R_cap/128][H]), per-tensor the transposed row codes; e2m1:
+ *              [R_cap, H/2] and [H, R_cap/2] bytes, s_g from an amax
+ *              pre-pass); NULL = no quantised output
  *  out_bf16    device [R_cap, H] bf16 permuted copy, or NULL
  *  row_id_map  device [T, k] int32: destination row of (t, j)
  *  src_row     device [R_cap] int32: t*k + j of the row, -1 for padding
@@ -192,7 +194,8 @@ int mgq_moe_permute(const void* x_bf16, int T, int H, const int32_t* topk_idx, i
  * routing arrays (read only): the codes and scales equal those of
  * mgq_moe_permute with the same routing. It requires the arrays from
  * mgq_moe_route (or mgq_moe_permute) for this T, k, E, and, for a column-wise
- * copy, an `align` that was a multiple of 32.
+ * copy, an `align` that was a multiple of the column block (MX and NVFP4 32,
+ * blockwise 128).
  * Splitting lets a caller route once and permute several tensors, or run the
  * routing (index work, latency-bound) beside other work. */
 int mgq_moe_route(const int32_t* topk_idx, int T, int k, int E, int align, int64_t R_cap,
@@ -234,6 +237,12 @@ int mgq_moe_permute_noalloc(const void* x_bf16, int T, int H, const int32_t* top
  *  x_bf16  device [G, M, K] bf16 (G groups, e.g. experts)
  *  q->row  [G, M, K] codes (+ scales); q->col [G, K, M] codes (+ scales)
  *  per-tensor mode reads one scale per group from q->tensor_scale.
+ *  blockwise: MGQ_BLK_1x128_F32 row-wise scale_inv [K/128][G*M] and, with
+ *    q->col, 128x1 column blocks (the transpose identity: the 1x128
+ *    quantisation of each group's transpose) with scale_inv [M/128][G*K];
+ *    MGQ_BLK_128x128_F32 (weights) one scale per 128x128 tile, row-wise
+ *    scale_inv [G][M/128][K/128] and, with q->col, the transposed codes with
+ *    the transposed tile scales [G][K/128][M/128] from the same pass.
  *  NVFP4 (MGQ_NV16_UE4M3, row-wise only; MGQ_NV16x16_UE4M3, row-wise and
  *    optionally column-wise, dtype MGQ_E2M1): an amax pre-pass writes each
  *    group's amax to q->amax_out [G] and s_g = 6*448/amax to
@@ -250,12 +259,14 @@ int mgq_block_quantize(const void* x_bf16, int64_t G, int64_t M, int64_t K,
  * [0, offsets[E]) are in use, group e = rows [offsets[e], offsets[e+1]).
  *  q->row  [R_cap, C] codes (+ scales over [R_cap, C]) for the rows in use
  *  q->col  [C, R_cap] codes (+ scales over [C, R_cap]) or NULL; column blocks
- *          (MX 32, NVFP4 16 rows) run inside each group
+ *          (MX 32, NVFP4 16, blockwise 128 rows) run inside each group
  * scaling: MGQ_TENSOR_F32 (q->tensor_scale[0]; the column copy is the
- * transposed cast; q->amax_out optional), MGQ_MX32_E8M0, or MGQ_NV16_UE4M3
- * (an amax pre-pass over the rows in use into q->amax_out[0], s_g into
- * q->tensor_scale[0]; e2m1 codes [R_cap, C/2] / [C, R_cap/2] bytes).
- * Group starts must be multiples of the column block (MX 32, NVFP4 16): a
+ * transposed cast; q->amax_out optional), MGQ_MX32_E8M0, MGQ_BLK_1x128_F32
+ * (row-wise scale_inv [C/128][R_cap], column-wise [R_cap/128][C]), or
+ * MGQ_NV16_UE4M3 (an amax pre-pass over the rows in use into q->amax_out[0],
+ * s_g into q->tensor_scale[0]; e2m1 codes [R_cap, C/2] / [C, R_cap/2] bytes).
+ * Group starts must be multiples of the column block (MX 32, NVFP4 16,
+ * blockwise 128): a
  * layout that is not (or not monotone, or past R_cap) is reported as
  * MGQ_ERR_INVALID_ARG in the device error word, and the codes are then
  * unspecified. Requires C and R_cap multiples of 128, E <= 1024. */
@@ -393,7 +404,9 @@ int mgq_grouped_gemm_dgrad_dswiglu(const mgq_operand* dY, const mgq_operand* W2,
  * then quantised). dG = dh u s (1 + g (1 - s)), dU = dh silu(g), s = sigmoid(g),
  * rounded to bf16 then quantised ([dG | dU] is one [R_cap, 2F] matrix).
  * Rows [0, offsets[E]) are processed. q->col (when set) receives the
- * column-wise copy [C, R_cap] with blocks along the rows.
+ * column-wise copy [C, R_cap] with blocks along the rows of each group (MX
+ * 32, blockwise 128 with scale_inv [R_cap/128][C]; blockwise row-wise
+ * scale_inv [C/128][R_cap]).
  * NVFP4 (q->scaling MGQ_NV16_UE4M3): two passes, the bf16 result (h_bf16 /
  * dgu_bf16 required) with its amax in q->amax_out, then the cast with s_g =
  * 6*448/amax written to q->tensor_scale. */
@@ -410,7 +423,9 @@ int mgq_moe_unpermute(const void* y_bf16, const int32_t* row_id_map, const float
 
 /* ---- a8: unpermute backward, fused with quantisation of dY -----------------
  * dY[row(t, j)] = float32(probs[t, j] * dout[t]) quantised into q (row and
- * col), filler rows zero; dprobs[t, j] = <dout[t], Y[row(t, j)]> (float32).
+ * col; the column-wise copy [H, R_cap] with blocks along each group's rows:
+ * MX 32, NVFP4 16, blockwise 128), filler rows zero;
+ * dprobs[t, j] = <dout[t], Y[row(t, j)]> (float32).
  * NVFP4: an amax pre-pass over dY (max |fl(p d)| over a row is
  * fl(|p| max |d|)) into q->amax_out, s_g into q->tensor_scale. */
 int mgq_moe_unpermute_bwd(const void* dout_bf16, const void* y_bf16,

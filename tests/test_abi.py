@@ -86,8 +86,17 @@ def test_host_validation_rejects_bad_arguments(lib):
     # ragged-group quantiser: C not a multiple of 128, missing offsets, blockwise scaling
     assert lib.mgq_grouped_quantize(16, 256, 100, 16, 4, ctypes.byref(q), None) == INV
     assert lib.mgq_grouped_quantize(16, 256, 128, None, 4, ctypes.byref(q), None) == INV
-    q3 = mgq.qdesc(mgq.E4M3, mgq.BLK_1x128_F32, 16, 16)
+    # 128x128 tiles are a weight layout, not one over ragged groups
+    q3 = mgq.qdesc(mgq.E4M3, mgq.BLK_128x128_F32, 16, 16)
     assert lib.mgq_grouped_quantize(16, 256, 128, 16, 4, ctypes.byref(q3), None) == mgq.ERR_UNSUPPORTED
+    # blockwise column copies need their scale_inv buffer, and the permute's
+    # groups padded to the 128-row column block
+    q4 = mgq.qdesc(mgq.E4M3, mgq.BLK_1x128_F32, 16, 16, 32, None)
+    assert lib.mgq_grouped_quantize(16, 256, 128, 16, 4, ctypes.byref(q4), None) == mgq.ERR_INVALID_ARG
+    assert lib.mgq_block_quantize(16, 1, 128, 128, ctypes.byref(q4), None) == mgq.ERR_INVALID_ARG
+    q5 = mgq.qdesc(mgq.E4M3, mgq.BLK_1x128_F32, 16, 16, 32, 48)
+    assert lib.mgq_moe_permute(16, 4, 128, 16, 2, 8, 32, ctypes.byref(q5), None, 1024, 16, 16, 16, 16, 16,
+                               1 << 20, None) == mgq.ERR_INVALID_ARG
     assert lib.mgq_amax_history_update(None, None, None, None, 1, 1, ctypes.c_float(448.0), None) == INV
     assert lib.mgq_get_error(None, None) == INV
 

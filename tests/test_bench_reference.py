@@ -38,3 +38,18 @@ def test_reference_other_ranks_exit_quietly():
     r = _run({"WORLD_SIZE": "2", "RANK": "1", "LOCAL_RANK": "1"})
     assert r.returncode == 0, r.stderr[-2000:]
     assert not [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+
+
+def test_bench_compiles_and_names_every_configuration():
+    """bench.py parses, and its extra workloads are configurations that exist."""
+    import ast
+    import importlib.util
+    src = open(os.path.join(ROOT, "bench.py")).read()
+    ast.parse(src)
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    from fp8_grouped_gemm_gb300.workloads import WORKLOADS
+    assert set(mod.OTHER_WORKLOADS) <= set(WORKLOADS)
+    for name in WORKLOADS:
+        assert mod.dtype_of(WORKLOADS[name])

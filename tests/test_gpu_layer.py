@@ -331,3 +331,102 @@ def test_nvfp4_training_step_scaled_down():
     check_elementwise(OR.permute_bwd(dxp, rim), bf16_np(lay.dx), "permute_bwd")
     # quantised-vs-bf16 SQNR of the NVFP4 forward GEMM (the NVFP4 bar)
     assert OG.sqnr_db(OG.grouped_gemm_fwd(xp, w1f, off), gu) >= 15.0
+
+
+def test_blockwise_training_step_scaled_down():
+    """Blockwise FP8 in both passes (TransformerEngine issue #2393: 1x128
+    forward blocks, 128x1 backward blocks, 128x128 weight tiles; e4m3
+    forward, e5m2 gradients) on the Scout-shaped experts scaled down (Zipf
+    loads with two empty experts, top-1): every code and scale_inv of both
+    copies of X, h, dY2, dY1 and the weights equal the oracle's, and every
+    GEMM is within tolerance of the oracle's GEMM on the same quantised
+    operands."""
+    from fp8_grouped_gemm_gb300 import layer as L
+    from fp8_grouped_gemm_gb300 import mgq
+    from fp8_grouped_gemm_gb300 import workloads as W
+    w = W.WORKLOADS["scout_fwdbwd"].scaled(T=900, H=512, F=768, E=6)
+    E, k, T, H, F = w.E, w.k, w.T, w.H, w.F
+    x = W.make_activations(w)
+    w1, w2 = W.make_weights(w)
+    idx, probs = W.make_routing(w)
+    dout = W.make_dout(w)
+    lay = L.ExpertLayer(w, DEV, keep_bf16=True)
+    assert lay.train and lay.recipe == "blockwise" and not lay.fused_swiglu
+    lay.quantize_weights(w1.to(DEV), w2.to(DEV))
+    lay.forward(x.to(DEV), torch.from_numpy(idx).to(DEV), torch.from_numpy(probs).to(DEV))
+    lay.backward(dout.to(DEV), torch.from_numpy(probs).to(DEV))
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    rim, src, off, cnt = OR.permute_indices(idx, E, L.ALIGN)
+    assert np.sum(cnt == 0) >= 1
+    Rp = int(off[-1])
+    filler = src < 0
+
+    def row_col(m, fmt, rq, rs, cq, cs, zero_filler):
+        """m [Rp, C]: the row-wise (1x128) and column-wise (128x1 inside each
+        group) copies; returns both dequantised ([Rp, C])."""
+        c, si = OQ.quantize_block_1x128(m, fmt)
+        r_deq = OQ.dequantize_block_1x128(c, si, fmt)
+        if zero_filler:
+            si = si.copy()
+            si[filler] = 0.0                 # padding rows: zero codes and zero scales
+        assert np.array_equal(u8_np(rq)[:Rp], c)
+        assert np.array_equal(rs.cpu().numpy().T[:Rp], si)
+        c_deq = np.zeros_like(m)
+        for e in range(E):
+            lo, hi = int(off[e]), int(off[e + 1])
+            if hi == lo:
+                continue
+            ct, st = OQ.quantize_block_1x128(np.ascontiguousarray(m[lo:hi].T), fmt)
+            assert np.array_equal(u8_np(cq)[:, lo:hi], ct), e
+            assert np.array_equal(cs.cpu().numpy()[lo // 128:hi // 128].T, st), e
+            c_deq[lo:hi] = OQ.dequantize_block_1x128(ct, st, fmt).T
+        return r_deq, c_deq
+
+    xp = OR.permute_rows(bf16_np(x), rim, Rp)
+    x_r, x_c = row_col(xp, "e4m3", lay.xq, lay.xs, lay.xcol, lay.xcs, True)
+    w1f, w2f = bf16_np(w1), bf16_np(w2)
+    w1_r, w2_r, w1_c, w2_c = [], [], [], []
+    for e in range(E):
+        for wf, q, s, qc, sc_, rl, cl in ((w1f, lay.w1q, lay.w1s, lay.w1col, lay.w1cs, w1_r, w1_c),
+                                          (w2f, lay.w2q, lay.w2s, lay.w2col, lay.w2cs, w2_r, w2_c)):
+            c, si = OQ.quantize_block_128x128(wf[e])
+            ct, sit = OQ.quantize_block_128x128(np.ascontiguousarray(wf[e].T))
+            assert np.array_equal(u8_np(q[e]), c) and np.array_equal(s[e].cpu().numpy(), si), e
+            assert np.array_equal(u8_np(qc[e]), ct) and np.array_equal(sc_[e].cpu().numpy(), sit), e
+            rl.append(OQ.dequantize_block_128x128(c, si))
+            cl.append(OQ.dequantize_block_128x128(ct, sit))
+    w1_r, w2_r, w1_c, w2_c = map(np.stack, (w1_r, w2_r, w1_c, w2_c))
+    gu = bf16_np(lay.gu)[:Rp]
+    assert rel_fro(OF.round_to_bf16(OG.grouped_gemm_fwd(x_r, w1_r, off)), gu) <= GEMM_TOL_BF16
+    hg = bf16_np(lay.h_bf16)[:Rp]
+    check_elementwise(OL.swiglu(gu, F), hg, "swiglu")
+    h_r, h_c = row_col(hg, "e4m3", lay.hq, lay.hs, lay.hcol, lay.hcs, False)
+    y = bf16_np(lay.y)[:Rp]
+    assert rel_fro(OF.round_to_bf16(OG.grouped_gemm_fwd(h_r, w2_r, off)), y) <= GEMM_TOL_BF16
+    # backward
+    dy32, dp = OR.unpermute_bwd(bf16_np(dout), y, rim, probs, Rp)
+    assert rel_fro(dp, lay.dprobs.cpu().numpy()) <= 1e-5
+    dy2_r, dy2_c = row_col(dy32.astype(np.float64), "e5m2", lay.dy2q, lay.dy2s, lay.dy2col, lay.dy2cs, True)
+    dh = bf16_np(lay.dh)[:Rp]
+    # dgrad through the column-wise weight copy: dY2 (W2col)^T = dY2 W2
+    dh_q = OG.grouped_gemm_fwd(dy2_r, w2_c, off)
+    assert rel_fro(OF.round_to_bf16(dh_q), dh) <= GEMM_TOL_BF16
+    dw2_q = OG.grouped_gemm_wgrad(dy2_c, h_c, off, E)
+    assert rel_fro(dw2_q, lay.dw2.cpu().numpy()) <= GEMM_TOL_F32
+    for ref, q_oracle, got in [(OG.grouped_gemm_dgrad(dy32.astype(np.float64), w2f, off), dh_q, dh),
+                               (OG.grouped_gemm_wgrad(dy32.astype(np.float64), hg, off, E), dw2_q,
+                                lay.dw2.cpu().numpy().astype(np.float64))]:
+        s_gpu, s_orc = OG.sqnr_db(ref, got), OG.sqnr_db(ref, q_oracle)
+        assert s_gpu >= 23.0 and abs(s_gpu - s_orc) <= 0.5, (s_gpu, s_orc)
+    dgu = bf16_np(lay.dgu_bf16)[:Rp]
+    check_elementwise(OL.dswiglu(dh, gu, F), dgu, "dswiglu")
+    dy1_r, dy1_c = row_col(dgu, "e5m2", lay.dy1q, lay.dy1s, lay.dy1col, lay.dy1cs, False)
+    dxp = bf16_np(lay.dxp)[:Rp]
+    assert rel_fro(OF.round_to_bf16(OG.grouped_gemm_fwd(dy1_r, w1_c, off)), dxp) <= GEMM_TOL_BF16
+    assert rel_fro(OG.grouped_gemm_wgrad(dy1_c, x_c, off, E), lay.dw1.cpu().numpy()) <= GEMM_TOL_F32
+    dw = lay.dw1.cpu().numpy()
+    for e in np.flatnonzero(cnt == 0):
+        assert np.all(dw[e] == 0.0)         # empty experts: zero weight gradients
+    check_elementwise(OR.permute_bwd(dxp, rim), bf16_np(lay.dx), "permute_bwd")
+    assert OG.sqnr_db(OG.grouped_gemm_fwd(xp, w1f, off), gu) >= 28.0

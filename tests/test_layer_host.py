@@ -26,6 +26,10 @@ CASES = {
                              ["gemm_fwd_gateup_swiglu", "gemm_fwd_down", "unpermute", "unpermute_bwd_quant",
                               "gemm_dgrad_down", "gemm_wgrad_down", "dswiglu_quant", "gemm_dgrad_gateup",
                               "gemm_wgrad_gateup", "permute_bwd"], 23),
+    "scout_fwdbwd": ("blockwise", True,
+                     ["gemm_fwd_gateup", "swiglu_quant", "gemm_fwd_down", "unpermute", "unpermute_bwd_quant",
+                      "gemm_dgrad_down", "gemm_wgrad_down", "dswiglu_quant", "gemm_dgrad_gateup",
+                      "gemm_wgrad_gateup", "permute_bwd"], 18),
     "mixtral_fwd": ("mxfp8", False, ["gemm_fwd_gateup_swiglu", "gemm_fwd_down", "unpermute"], 9),
     "scout_fwd": ("blockwise", False, ["gemm_fwd_gateup", "swiglu_quant", "gemm_fwd_down", "unpermute"], 10),
     "finegrained_fwd": ("nvfp4", False, ["gemm_fwd_gateup_swiglu", "gemm_fwd_down", "unpermute"], 13),

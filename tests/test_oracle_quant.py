@@ -335,3 +335,21 @@ def test_blockwise_128x128_dequantise_roundtrip():
     np.testing.assert_array_equal(c, codes)
     np.testing.assert_array_equal(si, np.exp2(-k).astype(np.float32))
     np.testing.assert_array_equal(Q.dequantize_block_128x128(c, si), x)
+
+
+def test_tile_128x128_transpose_identity():
+    """The column-wise copy of a 128x128-tile weight (TransformerEngine issue
+    #2393: 128x128 weight blocks, transpose identity): quantising W^T gives
+    the transposed codes and the transposed tile scales, because a tile's
+    amax does not depend on its orientation. Tiles with different scales and
+    an all-zero tile."""
+    rng = np.random.default_rng(12)
+    w = F.round_to_bf16(rng.standard_normal((256, 384)) * 0.02)
+    w[:128, 128:256] *= 1000.0
+    w[128:, :128] = 0.0
+    for fmt in ("e4m3", "e5m2"):
+        c, si = Q.quantize_block_128x128(w, fmt)
+        ct, sit = Q.quantize_block_128x128(np.ascontiguousarray(w.T), fmt)
+        np.testing.assert_array_equal(ct, c.T)
+        np.testing.assert_array_equal(sit, si.T)
+        assert si[1, 0] == 1.0 and np.all(c[128:, :128] == 0)
