@@ -910,8 +910,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < tl.nst; ++s) {
           const uint32_t a = tc % kAcc, aph = (tc / kAcc) & 1;
           const float f = sa_next * sb_next;
-          // contract mode: this stage's 128 column scales of B (this half's columns)
-          const float* sb_cols = sb_blk + (tl.kx0 / 128 + s) * p.sb_ld;
+          // contract mode: this stage's 128 column scales of B (this half's
+          // columns), four per lane, loaded before the partial product is ready
+          float4 sb4 = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+          if (MODE == kModeContract)
+            sb4 = __ldg(reinterpret_cast<const float4*>(sb_blk + (tl.kx0 / 128 + s) * p.sb_ld) + lane);
           if (s + 1 < tl.nst) {
             sa_next = sa_row[(tl.kx0 / 128 + s + 1) * p.sa_ld];
             if (MODE == kModeRows) sb_next = sb_blk[tl.kx0 / 128 + s + 1];
@@ -934,12 +937,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              // contract mode: 4 column scales at a time (the same for every
-              // lane: broadcast loads)
+              // contract mode: columns 16 c + 4 j .. + 3 are lane 4 c + j's four scales
               float4 fq = make_float4(f, f, f, f);
               if (MODE == kModeContract) {
-                const float4 q4 = __ldg(reinterpret_cast<const float4*>(sb_cols + c * 16) + j);
-                fq = make_float4(f * q4.x, f * q4.y, f * q4.z, f * q4.w);
+                const int src = 4 * c + j;
+                fq = make_float4(f * __shfl_sync(0xFFFFFFFFu, sb4.x, src), f * __shfl_sync(0xFFFFFFFFu, sb4.y, src),
+                                 f * __shfl_sync(0xFFFFFFFFu, sb4.z, src), f * __shfl_sync(0xFFFFFFFFu, sb4.w, src));
               }
               const float fj[4] = {fq.x, fq.y, fq.z, fq.w};
 #pragma unroll
