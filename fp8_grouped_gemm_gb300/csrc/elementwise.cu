@@ -436,34 +436,49 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantRowsArgs a) {
 // FLT_MAX on overflow); codes = cast(x * s); scale_inv = 1 / s at
 // [(g * N/128 + n/128) * K/128 + k/128].
 template <int DT>
-__global__ void __launch_bounds__(256) quant_tile128_kernel(const uint16_t* __restrict__ x, int64_t N, int64_t K,
-                                                            uint8_t* __restrict__ codes, float* __restrict__ sinv) {
+__global__ void __launch_bounds__(256, 4) quant_tile128_kernel(const uint16_t* __restrict__ x, int64_t N, int64_t K,
+                                                               uint8_t* __restrict__ codes, float* __restrict__ sinv) {
+  // one tile per CTA; a thread's 64 values stay packed bf16 pairs (32
+  // registers), so four CTAs fit an SM
   __shared__ uint32_t s_max[8];
   const int64_t nb = N / 128, kb = K / 128;
   const int64_t tile = blockIdx.x;
   const int64_t g = tile / (nb * kb), rem = tile % (nb * kb);
-  const int64_t n0 = (rem / kb) * 128, k0 = (rem % kb) * 128;
   const int row = threadIdx.x >> 1, cofs = (threadIdx.x & 1) * 64;
-  const uint16_t* src = x + (g * N + n0 + row) * K + k0 + cofs;
-  float v[64];
-  load_bf16x32(src, v);
-  load_bf16x32(src + 32, v + 32);
-  uint32_t m = warp_max_u32(absmax_bits_f32(v, 64));
+  const int64_t off = (g * N + (rem / kb) * 128 + row) * K + (rem % kb) * 128 + cofs;
+  uint4 w[8];
+  const uint4* src = reinterpret_cast<const uint4*>(x + off);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) w[q] = __ldg(src + q);
+  uint32_t acc = 0;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    acc = absmax_acc_bf16x2(acc, w[q].x);
+    acc = absmax_acc_bf16x2(acc, w[q].y);
+    acc = absmax_acc_bf16x2(acc, w[q].z);
+    acc = absmax_acc_bf16x2(acc, w[q].w);
+  }
+  uint32_t m = warp_max_u32(fold_bf16x2(absmax_bf16x2_final(acc)));
   if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = m;
   __syncthreads();
   m = 0;
 #pragma unroll
   for (int i = 0; i < 8; ++i) m = max(m, s_max[i]);
-  float sc = (m == 0) ? 1.0f : __fdiv_rn(FmtInfo<DT>::fmax, __uint_as_float(m));
-  if (isinf(sc)) sc = 3.40282347e38f;
-  uint32_t cw[16];
+  const float sc = blk_scale<DT>(m);
+  uint4* dst = reinterpret_cast<uint4*>(codes + off);
 #pragma unroll
-  for (int i = 0; i < 16; ++i)
-    cw[i] = cvt_fp8x4<DT>(__fmul_rn(v[4 * i], sc), __fmul_rn(v[4 * i + 1], sc), __fmul_rn(v[4 * i + 2], sc),
-                          __fmul_rn(v[4 * i + 3], sc));
-  uint4* dst = reinterpret_cast<uint4*>(codes + (g * N + n0 + row) * K + k0 + cofs);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) dst[q] = make_uint4(cw[4 * q], cw[4 * q + 1], cw[4 * q + 2], cw[4 * q + 3]);
+  for (int q = 0; q < 4; ++q) {
+    const uint4 a = w[2 * q], b = w[2 * q + 1];
+    dst[q] = make_uint4(
+        cvt_fp8x4<DT>(__fmul_rn(bf16_lo(a.x), sc), __fmul_rn(bf16_hi(a.x), sc), __fmul_rn(bf16_lo(a.y), sc),
+                      __fmul_rn(bf16_hi(a.y), sc)),
+        cvt_fp8x4<DT>(__fmul_rn(bf16_lo(a.z), sc), __fmul_rn(bf16_hi(a.z), sc), __fmul_rn(bf16_lo(a.w), sc),
+                      __fmul_rn(bf16_hi(a.w), sc)),
+        cvt_fp8x4<DT>(__fmul_rn(bf16_lo(b.x), sc), __fmul_rn(bf16_hi(b.x), sc), __fmul_rn(bf16_lo(b.y), sc),
+                      __fmul_rn(bf16_hi(b.y), sc)),
+        cvt_fp8x4<DT>(__fmul_rn(bf16_lo(b.z), sc), __fmul_rn(bf16_hi(b.z), sc), __fmul_rn(bf16_lo(b.w), sc),
+                      __fmul_rn(bf16_hi(b.w), sc)));
+  }
   if (threadIdx.x == 0) sinv[tile] = __fdiv_rn(1.0f, sc);
 }
 

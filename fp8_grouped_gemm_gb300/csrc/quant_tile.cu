@@ -24,12 +24,15 @@
 // ([G][M/128][C/128] and [G][C/128][M/128]).
 // Kernels: quant_rowcol_kernel (one tile per CTA: plain and computed sources),
 // quant_rowcol_stream_kernel (gathered rows: a CTA walks a range of tiles and
-// stages the next with cp.async), quant_nv2d_kernel (NVFP4 weights with 16x16
+// stages the next with cp.async; FP8 column codes go out through a staged
+// tile and one TMA store per item), quant_nv2d_kernel (NVFP4 weights with 16x16
 // blocks: both copies share the block scales).
 #include "mgq_internal.h"
+#include "ptx_sm100.cuh"
 #include "rowquant.cuh"
 
 #include <algorithm>
+#include <cstring>
 #include <type_traits>
 
 namespace mgq {
@@ -37,6 +40,27 @@ namespace {
 
 constexpr int TR = 128, TC = 128;  // tile rows x columns (per part)
 constexpr int LD = TC + 8;          // bf16 tile row pitch in elements (rows stay 16-byte aligned)
+constexpr int kStgBytes = TC * TR;  // one part's staged column codes (FP8): 128 rows of 128 bytes
+
+// Staged column-wise codes (FP8 kinds, gathered sources): the CTA's writes to the staging tiles
+// become visible to the TMA unit, then one thread stores each part's tile
+// ([128 output rows][128 bytes] at output row y0 + p * part_off, byte x0).
+template <int P>
+__device__ __forceinline__ void store_col_tiles(const CUtensorMap* tm, const uint8_t* stg, int32_t x0, int32_t y0,
+                                                int64_t part_off, int tid) {
+  ptx::fence_proxy_async_smem();
+  __syncthreads();
+  if (tid == 0) {
+#pragma unroll
+    for (int p = 0; p < P; ++p) ptx::tma_store_2d(tm, stg + p * kStgBytes, x0, y0 + (int32_t)(p * part_off));
+    ptx::bulk_commit();
+  }
+}
+// before the staging tiles are written again: the previous stores have read them
+__device__ __forceinline__ void wait_col_tiles(int tid) {
+  if (tid == 0) ptx::bulk_wait_read0();
+  __syncthreads();
+}
 
 // Sources. Every value a source produces is a bf16 value, or (kFactor) a bf16
 // value times a per-row float32 factor, so tiles hold bf16 in shared memory.
@@ -125,6 +149,7 @@ struct SrcDswiglu {
 // (t = e / k), zeros for filler rows
 struct SrcGatherX {
   static constexpr bool kStream = true;
+  static constexpr int kParts = 1;
   static constexpr bool kFactor = false;
   static constexpr bool kColumnsOnly = false;
   const uint16_t* x;
@@ -143,6 +168,7 @@ struct SrcGatherX {
 // (the row-wise codes come from the token-major kernel)
 struct SrcGatherDy {
   static constexpr bool kStream = true;
+  static constexpr int kParts = 1;
   static constexpr bool kFactor = true;
   static constexpr bool kColumnsOnly = true;
   const uint16_t* dout;
@@ -173,6 +199,7 @@ struct RowColArgs {
   float* amax_out;           // per group: TENSOR optional output; NVFP4 the pre-pass amax (input)
   float* s_out;              // NVFP4: s_g per group (output)
   int rceil;
+  int col_tma;               // FP8 column copies: staged in shared memory, one TMA store per tile and part
 };
 
 // ---- the quantisation of one tile (shared by both kernels) -----------------
@@ -193,9 +220,14 @@ __device__ __forceinline__ uint32_t nv_block16(float* v, float amax_b, float s_g
 
 // one column-wise block: the 32 values of output row crow, rows rg..rg+31 of
 // its group (amax_bits: float bits of their |v| maximum, MX)
+// stg (FP8, when staging): this part's staging tile [128 tile columns][128
+// tile rows] of code bytes in the 128-byte-swizzled layout a TMA store reads
+// (16-byte chunk k of row c at chunk k ^ (c & 7)); cl: the tile column, rl:
+// the block's first tile row
 template <int SC, int DT>
 __device__ __forceinline__ void col_block_out(float* v, uint32_t amax_bits, float ts, const RowColArgs& a,
-                                              int64_t crow, int64_t rg) {
+                                              int64_t crow, int64_t rg, uint8_t* stg = nullptr, int cl = 0,
+                                              int rl = 0) {
   if constexpr (SC == MGQ_NV16_UE4M3) {
     // two 16-row blocks, e2m1 packed along the rows; ts is s_g
     uint2 c0, c1;
@@ -216,9 +248,16 @@ __device__ __forceinline__ void col_block_out(float* v, uint32_t amax_bits, floa
     for (int i = 0; i < 8; ++i)
       cw[i] = cvt_fp8x4<DT>(__fmul_rn(v[4 * i], mult), __fmul_rn(v[4 * i + 1], mult), __fmul_rn(v[4 * i + 2], mult),
                             __fmul_rn(v[4 * i + 3], mult));
-    uint4* dst = reinterpret_cast<uint4*>(a.col_codes + crow * a.M + rg);
-    dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-    dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+    if (stg) {
+      uint4* row = reinterpret_cast<uint4*>(stg + cl * 128);
+      const int k0 = rl / 16;
+      row[k0 ^ (cl & 7)] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+      row[(k0 + 1) ^ (cl & 7)] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+    } else {
+      uint4* dst = reinterpret_cast<uint4*>(a.col_codes + crow * a.M + rg);
+      dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+      dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+    }
   }
 }
 
@@ -325,13 +364,15 @@ __device__ __forceinline__ float col_blk_scale(uint32_t* s_cm, int rb, int col, 
 
 template <int P, int SC, int DT, bool FAC>
 __device__ __forceinline__ void col_phase(const uint16_t* tile, const float* fac, int64_t g, int64_t r0, int64_t c0,
-                                          float ts, const RowColArgs& a, int tid, uint32_t& am, uint32_t* s_cm) {
+                                          float ts, const RowColArgs& a, int tid, uint32_t& am, uint32_t* s_cm,
+                                          uint8_t* stg0 = nullptr) {
   const int cp = tid & 63, rb = (tid >> 6) & 3;
   const int cc = 2 * cp;
   const int64_t rg = r0 - g * a.M + 32 * rb;                 // row inside the group
 #pragma unroll 1
   for (int p = 0; p < P; ++p) {
     const int64_t crow = g * a.C + c0 + p * a.part_off + cc;  // row of the column-wise output
+    uint8_t* stg = stg0 ? stg0 + p * kStgBytes : nullptr;     // this part's staging tile
     if constexpr (SC == MGQ_BLK_1x128_F32) {
       // 128x1 blocks: per column the amax of the tile's 128 rows, then the
       // column's codes with its scale (two columns per thread)
@@ -358,7 +399,7 @@ __device__ __forceinline__ void col_phase(const uint16_t* tile, const float* fac
         float v[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = val(i, h);
-        col_block_out<MGQ_TENSOR_F32, DT>(v, 0u, sc[h], a, crow + h, rg);
+        col_block_out<MGQ_TENSOR_F32, DT>(v, 0u, sc[h], a, crow + h, rg, stg, cc + h, 32 * rb);
       }
       __syncthreads();     // s_cm is reused by the next part / tile
     } else if constexpr (FAC) {
@@ -371,7 +412,7 @@ __device__ __forceinline__ void col_phase(const uint16_t* tile, const float* fac
           v[i] = __fmul_rn(fac[32 * rb + i], __uint_as_float((uint32_t)tile[(p * TR + 32 * rb + i) * LD + cc + h] << 16));
         const uint32_t m = absmax_bits_f32(v, 32);
         am = max(am, m);
-        col_block_out<SC, DT>(v, m, ts, a, crow + h, rg);
+        col_block_out<SC, DT>(v, m, ts, a, crow + h, rg, stg, cc + h, 32 * rb);
       }
     } else {
       uint32_t w[32];      // the two columns' 32 values as bf16 pairs
@@ -392,7 +433,7 @@ __device__ __forceinline__ void col_phase(const uint16_t* tile, const float* fac
         float v[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = h ? bf16_hi(w[i]) : bf16_lo(w[i]);
-        col_block_out<SC, DT>(v, amh[h], ts, a, crow + h, rg);
+        col_block_out<SC, DT>(v, amh[h], ts, a, crow + h, rg, stg, cc + h, 32 * rb);
       }
     }
   }
@@ -423,7 +464,7 @@ __device__ __forceinline__ void flush_amax(uint32_t am, float* amax_out, int64_t
 
 template <class Src, int SC, int DT>
 __global__ void __launch_bounds__(256, Src::kParts == 2 ? 3 : 4)
-    quant_rowcol_kernel(const Src src, const RowColArgs a) {
+    quant_rowcol_kernel(const Src src, const RowColArgs a, const __grid_constant__ CUtensorMap tmc) {
   constexpr int P = Src::kParts;
   // 128x128 weight tiles: one scale per tile, then both copies cast like a
   // per-tensor scale (the column-wise copy is the transposed cast)
@@ -431,6 +472,12 @@ __global__ void __launch_bounds__(256, Src::kParts == 2 ? 3 : 4)
   constexpr int SCC = T128 ? MGQ_TENSOR_F32 : SC;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint16_t* tile = reinterpret_cast<uint16_t*>(smem_raw);   // [P][TR][LD]
+  // staged column codes [P][128][128] (1024-byte aligned for the swizzled TMA store)
+  uint8_t* stg = nullptr;
+  if (a.col_tma) {
+    const uint32_t raw = ptx::smem_u32(smem_raw) + P * TR * LD * 2;
+    stg = smem_raw + P * TR * LD * 2 + (((raw + 1023u) & ~1023u) - raw);
+  }
   __shared__ uint32_t s_amax[8];
   __shared__ uint32_t s_cm[SC == MGQ_BLK_1x128_F32 ? 4 * TC : 1];
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -517,10 +564,17 @@ __global__ void __launch_bounds__(256, Src::kParts == 2 ? 3 : 4)
     }
     if (a.row_codes) row_phase<P, SCC, DT>(tile, r0, nrows, c0, tsc, a, warp, lane);
     uint32_t am_unused = 0;
-    if (a.col_codes) col_phase<P, SCC, DT, false>(tile, nullptr, g, r0, c0, tsc, a, tid, am_unused, s_cm);
+    if (a.col_codes) {
+      if (stg) wait_col_tiles(tid);
+      col_phase<P, SCC, DT, false>(tile, nullptr, g, r0, c0, tsc, a, tid, am_unused, s_cm, stg);
+      if (stg) store_col_tiles<P>(&tmc, stg, (int32_t)(r0 - g * a.M), (int32_t)(g * a.C + c0), a.part_off, tid);
+    }
     if (SC == MGQ_TENSOR_F32 && a.amax_out) flush_amax(fold_bf16x2(am2), a.amax_out, g, s_amax, tid);
     __syncthreads();   // the tile is reused by the next row tile
   }
+  // the staged stores have read shared memory before the CTA exits (their
+  // global writes complete with the grid)
+  if (stg && tid == 0) ptx::bulk_wait_read0();
 }
 
 // ---- streamed sources: pipelined over the CTA's items -----------------------
@@ -540,9 +594,15 @@ template <int N> __device__ __forceinline__ void cp_async_wait() {
 // next item's tile with cp.async (zero fill for zero rows) while it quantises
 // the current one: two tile buffers, two offset slots.
 template <class Src, int SC, int DT>
-__global__ void __launch_bounds__(256, 3) quant_rowcol_stream_kernel(const Src src, const RowColArgs a) {
+__global__ void __launch_bounds__(256, 3)
+    quant_rowcol_stream_kernel(const Src src, const RowColArgs a, const __grid_constant__ CUtensorMap tmc) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint16_t* tiles = reinterpret_cast<uint16_t*>(smem_raw);   // [2][TR][LD]
+  uint8_t* stg = nullptr;                                     // staged column codes [128][128]
+  if (a.col_tma) {
+    const uint32_t raw = ptx::smem_u32(smem_raw) + 2 * TR * LD * 2;
+    stg = smem_raw + 2 * TR * LD * 2 + (((raw + 1023u) & ~1023u) - raw);
+  }
   __shared__ int64_t s_off[2][TR];
   __shared__ float s_fac[2][TR];
   __shared__ uint32_t s_amax[8];
@@ -606,7 +666,9 @@ __global__ void __launch_bounds__(256, 3) quant_rowcol_stream_kernel(const Src s
     const uint16_t* t = tiles + buf * TR * LD;
     if (SC == MGQ_NV16_UE4M3 && ct == 0 && r0 == g * a.M && tid == 0) a.s_out[g] = ts;
     if (!Src::kColumnsOnly && a.row_codes) row_phase<1, SC, DT>(t, r0, nrows, c0, ts, a, warp, lane, s_off[rt & 1]);
-    col_phase<1, SC, DT, Src::kFactor>(t, s_fac[rt & 1], g, r0, c0, ts, a, tid, am, s_cm);
+    if (stg) wait_col_tiles(tid);
+    col_phase<1, SC, DT, Src::kFactor>(t, s_fac[rt & 1], g, r0, c0, ts, a, tid, am, s_cm, stg);
+    if (stg) store_col_tiles<1>(&tmc, stg, (int32_t)(r0 - g * a.M), (int32_t)(g * a.C + c0), 0, tid);
     __syncthreads();   // the buffer is refilled two items on
     if (rt_n != rt || item + 1 == i1) {
       if (SC == MGQ_TENSOR_F32 && a.amax_out) flush_amax(am, a.amax_out, g, s_amax, tid);
@@ -617,6 +679,9 @@ __global__ void __launch_bounds__(256, 3) quant_rowcol_stream_kernel(const Src s
     rt = rt_n;
     ct = ct_n;
   }
+  // the staged stores have read shared memory before the CTA exits (their
+  // global writes complete with the grid)
+  if (stg && tid == 0) ptx::bulk_wait_read0();
 }
 
 // the dynamic shared memory limit of one kernel, set once per device
@@ -634,21 +699,39 @@ int set_smem(Kern kern, size_t smem, bool* attr_set) {
 }
 
 template <class Src, int SC, int DT>
-int launch_rowcol_t(const Src& src, const RowColArgs& a, cudaStream_t s) {
+int launch_rowcol_t(const Src& src, RowColArgs a, cudaStream_t s) {
   static bool attr_set[64] = {false};   // one per instantiation
+  // FP8 column copies go out through staged TMA stores: a map of the column
+  // output [G * C rows, M bytes], 128 x 128-byte boxes
+  CUtensorMap tmc;
+  memset(&tmc, 0, sizeof(tmc));
+  a.col_tma = 0;
+  // (measured: the gathered-row passes gain from the staging; the one-tile
+  // CTAs of plain and computed sources do not, and two-part tiles would fit
+  // only two CTAs an SM)
+  if (SC != MGQ_NV16_UE4M3 && Src::kStream && a.col_codes) {
+    if (!encode_tmap_u8_2d(&tmc, a.col_codes, (uint64_t)a.M, (uint64_t)((a.rows_cap / a.M) * a.C), (uint64_t)a.M,
+                           128, 128))
+      return MGQ_ERR_CUDA;
+    a.col_tma = 1;
+  }
+  constexpr int P = Src::kParts;
+  constexpr size_t stg_max = (SC == MGQ_NV16_UE4M3 || !Src::kStream) ? 0 : 1024 + (size_t)kStgBytes;
+  const size_t stg = a.col_tma ? stg_max : 0;
   if constexpr (!Src::kStream) {
-    constexpr size_t smem = (size_t)Src::kParts * TR * LD * sizeof(uint16_t);
+    constexpr size_t tiles = (size_t)P * TR * LD * sizeof(uint16_t);
     auto kern = quant_rowcol_kernel<Src, SC, DT>;
-    if (set_smem(kern, smem, attr_set) != MGQ_OK) return MGQ_ERR_CUDA;
-    const dim3 grid((unsigned)(a.C / Src::kParts / TC), (unsigned)std::min<int64_t>((a.rows_cap + TR - 1) / TR, 65535));
-    kern<<<grid, 256, smem, s>>>(src, a);
+    if (set_smem(kern, tiles + stg_max, attr_set) != MGQ_OK) return MGQ_ERR_CUDA;
+    const dim3 grid((unsigned)(a.C / P / TC), (unsigned)std::min<int64_t>((a.rows_cap + TR - 1) / TR, 65535));
+    kern<<<grid, 256, tiles + stg, s>>>(src, a, tmc);
   } else {
-    constexpr size_t smem = 2 * TR * LD * sizeof(uint16_t);
+    constexpr size_t tiles = 2 * TR * LD * sizeof(uint16_t);
     auto kern = quant_rowcol_stream_kernel<Src, SC, DT>;
-    if (set_smem(kern, smem, attr_set) != MGQ_OK) return MGQ_ERR_CUDA;
+    if (set_smem(kern, tiles + stg_max, attr_set) != MGQ_OK) return MGQ_ERR_CUDA;
     const int64_t items = (a.rows_cap + TR - 1) / TR * (a.C / TC);
-    const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>(items, (int64_t)num_sms() * 3));
-    kern<<<(unsigned)ctas, 256, smem, s>>>(src, a);
+    // resident CTAs per SM: 3 with the tile buffers alone, 2 with the staging
+    const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>(items, (int64_t)num_sms() * (stg ? 2 : 3)));
+    kern<<<(unsigned)ctas, 256, tiles + stg, s>>>(src, a, tmc);
   }
   MGQ_LAUNCH_CHECK();
   return MGQ_OK;
@@ -710,6 +793,7 @@ RowColArgs make_args(const mgq_qdesc* q, int64_t rows_cap, const int32_t* rows_u
   a.amax_out = q->amax_out;
   a.s_out = q->tensor_scale;
   a.rceil = q->e8m0_mode == MGQ_E8M0_RCEIL;
+  a.col_tma = 0;
   return a;
 }
 
