@@ -572,20 +572,17 @@ OTHER_WORKLOADS = ("tiny", "mixtral_fwd", "scout_fwd", "finegrained_fwd", "mixtr
 OTHER_STEPS = 20
 
 
-def oracle_memory_steps(w):
-    """The oracle's memory-bound steps timed on a bounded sample (2048 tokens
-    of the workload's hidden size for permute + quantise and the unpermute;
-    a 1024-row slice of one expert's W1 for the weight quantisation), as
-    algorithmic GB/s by the byte counts the GPU kernels are measured with."""
+def oracle_memory_steps(w, x, idx, probs):
+    """The oracle's memory-bound steps timed on the host cores, as algorithmic
+    GB/s by the byte counts the GPU kernels are measured with: permute +
+    quantise and the unpermute at the workload's full token count (its own X
+    and routing), the weight quantisation on 2048 rows of one expert's W1."""
     from oracle import quant as OQ
     from oracle import routing as OR
     from oracle.formats import round_to_bf16
-    rng = np.random.default_rng(w.seed)
-    Ts, H, k, E = 2048, w.H, w.k, w.E
-    x = round_to_bf16(rng.standard_normal((Ts, H)))
-    idx = np.stack([rng.permutation(E)[:k] for _ in range(Ts)]).astype(np.int32)
-    probs = np.full((Ts, k), 1.0 / k, dtype=np.float32)
-    wslice = round_to_bf16(rng.standard_normal((1024, H)) * 0.02)
+    x64 = x.float().numpy().astype(np.float64)
+    T, H = x64.shape
+    k, E = w.k, w.E
 
     def quant(a):
         if w.recipe == "mxfp8":
@@ -596,29 +593,32 @@ def oracle_memory_steps(w):
             return OQ.quantize_nvfp4(a, OQ.nvfp4_global_scale(float(np.max(np.abs(a)))))
         return OQ.quantize_tensor(a, np.float32(1.0))
 
-    q = 1.0 if w.recipe in ("delayed",) else (0.5 + 1 / 16 if w.recipe == "nvfp4" else 1 + 1 / 32)
+    q = 1.0 if w.recipe == "delayed" else (0.5 + 1 / 16 if w.recipe == "nvfp4" else 1 + 1 / 32)
     out = {}
     t = time.perf_counter()
     rim, src, off, cnt = OR.permute_indices(idx, E, 128)
-    codes = quant(x)[0]
-    OR.permute_rows(codes, rim, int(off[-1]))
+    Rp = int(off[-1])
+    codes = quant(x64)[0]
+    OR.permute_rows(codes, rim, Rp)
     dt = time.perf_counter() - t
-    out["permute_quant"] = {"GB/s": (Ts * H * 2 + Ts * k * H * q) / dt / 1e9, "seconds": dt,
-                            "sample": f"{Ts} tokens x {H}, top-{k} of {E}"}
-    y = round_to_bf16(rng.standard_normal((int(off[-1]), H)))
+    out["permute_quant"] = {"GB/s": (T * H * 2 + T * k * H * q) / dt / 1e9, "seconds": dt,
+                            "sample": f"full size: {T} tokens x {H}, top-{k} of {E}"}
+    y = OR.permute_rows(x64, rim, Rp)
     t = time.perf_counter()
     OR.unpermute(y, rim, probs)
     dt = time.perf_counter() - t
-    out["unpermute"] = {"GB/s": (Ts * k * H * 2 + Ts * H * 2) / dt / 1e9, "seconds": dt,
-                        "sample": f"{Ts} tokens x {H}, top-{k}"}
+    out["unpermute"] = {"GB/s": (T * k * H * 2 + T * H * 2) / dt / 1e9, "seconds": dt,
+                        "sample": f"full size: {T} tokens x {H}, top-{k}"}
+    rng = np.random.default_rng(w.seed)
+    wslice = round_to_bf16(rng.standard_normal((2048, H)) * 0.02)
     t = time.perf_counter()
     if w.recipe == "blockwise":
         OQ.quantize_block_128x128(wslice)
     else:
         quant(wslice)
     dt = time.perf_counter() - t
-    out["weight_quant"] = {"GB/s": 1024 * H * (2 + q) / dt / 1e9, "seconds": dt,
-                           "sample": f"1024 x {H} rows of one expert's W1"}
+    out["weight_quant"] = {"GB/s": 2048 * H * (2 + q) / dt / 1e9, "seconds": dt,
+                           "sample": f"2048 x {H} rows of one expert's W1"}
     return out
 
 
@@ -668,6 +668,10 @@ def main():
         torch.cuda.synchronize()
 
     rec, step = measure(w, dev, world, args.steps, args.warmup, barrier, local, with_e2e=not args.no_e2e)
+    # the headline's own inputs, for the oracle's memory steps (CPU leg below)
+    oracle_inputs = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        oracle_inputs = (step.x.cpu(), step.idx.cpu().numpy(), step.probs.cpu().numpy())
     roofline = rec["roofline"]
     tr = measured_gemm_traffic(w.name) if not small else None
     roofline["traffic"] = tr["bytes_per_launch"] if tr else None
@@ -696,7 +700,9 @@ def main():
         dt, f = oracle_sample(w, *CPU_BASELINE_SAMPLE)
         cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
                "sample": sample_desc(*CPU_BASELINE_SAMPLE), "seconds": dt,
-               "memory_steps": oracle_memory_steps(w)}
+               # the whole step's GEMMs at the sample's rate: extrapolated, not run
+               "gemm_full_step_seconds_extrapolated": w.gemm_flops() / (f / dt),
+               "memory_steps": oracle_memory_steps(w, *oracle_inputs)}
         for k_, v in cpu["memory_steps"].items():
             if k_ in rec["hbm_kernels"]:
                 v["gpu_GB/s"] = rec["hbm_kernels"][k_]["GB/s"]
