@@ -135,9 +135,24 @@ struct Tile {
   int64_t row_a, row_b, kx0, out_row, out_col;
 };
 
-// Tile t of the sequence. kModeRows: tiles ordered expert, N tile, M tile
-// (M fastest, so a wave shares the B tiles of one expert); kModeContract
-// (wgrad): expert, output-row tile, output-column tile (columns fastest).
+// Order of an expert's (N tile, M tile) pairs in rows mode: bands of kBandN N
+// tiles; inside a band the N tiles run fastest, then the M tiles. A wave of
+// consecutive tiles then covers a block about kBandN wide and a few M tiles
+// high, and the waves of one band reuse its B tiles from L2, so A is read
+// once per band instead of once per wave (the operand that re-streamed when
+// the M tiles ran fastest over a whole expert: the down forward's h and the
+// gate/up dgrad's dY, larger than L2 per expert).
+constexpr int64_t kBandN = 8;
+__device__ __forceinline__ void band_order(int64_t local, int64_t mt, int64_t nN, int64_t& n, int64_t& m) {
+  const int64_t band = local / (kBandN * mt), r = local - band * (kBandN * mt);
+  const int64_t gn = min(kBandN, nN - band * kBandN);    // the last band may be narrower
+  m = r / gn;
+  n = band * kBandN + (r - m * gn);
+}
+
+// Tile t of the sequence. kModeRows: tiles ordered expert, then N bands
+// (band_order); kModeContract (wgrad): expert, output-row tile, output-column
+// tile (columns fastest).
 template <int MODE>
 __device__ __forceinline__ bool get_tile(const int32_t* s_off, int E, const GemmParams& p, int64_t t, int& ecur,
                                          Tile& tl) {
@@ -149,7 +164,8 @@ __device__ __forceinline__ bool get_tile(const int32_t* s_off, int E, const Gemm
     const int e = ecur;
     const int64_t mt = (s_off[e + 1] - s_off[e]) / BM;
     const int64_t local = t - (int64_t)(s_off[e] / BM) * nN;
-    const int64_t n = local / mt, m = local % mt;
+    int64_t n, m;
+    band_order(local, mt, nN, n, m);
     tl.e = e;
     tl.nst = (int)(p.K / BK);
     tl.row_a = s_off[e] + BM * m;
@@ -1096,7 +1112,8 @@ __device__ __forceinline__ bool get_pair_tile(const int32_t* s_off, const int32_
     const int e = ecur;
     const int64_t mt = s_cum[e + 1] - s_cum[e];
     const int64_t local = t - (int64_t)s_cum[e] * nN;
-    const int64_t n = local / mt, m = local % mt;
+    int64_t n, m;
+    band_order(local, mt, nN, n, m);
     tl.e = e;
     tl.nst = (int)(p.K / BK);
     tl.row_a = s_off[e] + 256 * m;
