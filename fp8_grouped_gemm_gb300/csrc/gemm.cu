@@ -61,10 +61,19 @@ __host__ __device__ constexpr uint32_t staging_bytes(int kind) { return 8 * kSta
 // pipeline depth: NVFP4's larger scale chunks leave room for 3 stages next to
 // the staging buffers (its 128-byte stages hold 256 elements of K)
 __host__ __device__ constexpr int stages_of(int kind) { return kind == 3 ? 3 : STAGES; }
+// float32 block scales (kind 2): a ring of kBlkSlots slots, one per contraction
+// stage, each with the stage's 128 A row scales and (contract mode) the 256
+// B column scales of the tile, bulk-copied by the producer and read by the
+// epilogue warps from shared memory. The ring is deeper than the operand ring
+// plus the two tensor-memory buffers, so its slots are always free in time.
+constexpr uint32_t kBlkSlots = 8, kBlkSlotFloats = 128 + BN;
+__host__ __device__ constexpr uint32_t blk_ring_bytes(int kind) { return kind == 2 ? kBlkSlots * kBlkSlotFloats * 4 : 0u; }
 __host__ __device__ constexpr size_t smem_bytes(int kind) {
   return 1024 /*align slack*/ + stages_of(kind) * (size_t)(kABytes + kBBytes + sf_stage_bytes(kind)) +
-         staging_bytes(kind) + 256 /*barriers*/ + (kMaxE + 8) * 4;
+         staging_bytes(kind) + blk_ring_bytes(kind) + 256 /*barriers*/ + (kMaxE + 8) * 4;
 }
+static_assert(smem_bytes(2) <= 232448, "blockwise kernel exceeds the shared memory of a block");
+static_assert(kBlkSlots >= STAGES + 2, "the scale ring must cover the operand ring and both partial buffers");
 
 enum { kModeRows = 0, kModeContract = 1 };
 // operand scaling handled by the kernel: E8M0 block scales in the MMA, one
@@ -703,7 +712,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sSFA = sB + STG * kBBytes;
   uint8_t* sSFB = sSFA + STG * kSfaBytes;
   uint8_t* sOut = sSFA + STG * sf_stage_bytes(KIND);       // epilogue staging (TMA stores)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + staging_bytes(KIND));
+  float* sRing = reinterpret_cast<float*>(sOut + staging_bytes(KIND));   // block scales
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + staging_bytes(KIND) + blk_ring_bytes(KIND));
   uint64_t* full = bars;
   uint64_t* empty = bars + STG;
   uint64_t* tmem_full = bars + 2 * STG;        // [2]
@@ -711,6 +721,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * STG + 4);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   int* s_bad = reinterpret_cast<int*>(s_tmem + 2);
+  uint64_t* s_full = bars + 14;                // [kBlkSlots] block-scale slot loaded
+  uint64_t* s_empty = bars + 14 + kBlkSlots;   // [kBlkSlots] block-scale slot read by the epilogue
+  static_assert(2 * STG + 4 + 2 <= 14 && 14 + 2 * kBlkSlots <= 32, "barrier region");
   int32_t* s_off = reinterpret_cast<int32_t*>(bars + 32);
 
   const int warp = threadIdx.x >> 5;
@@ -733,6 +746,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&tmem_full[a], 1);
       ptx::mbar_init(&tmem_empty[a], 8 * 32);
+    }
+    if (KIND == kKindBlock) {
+      for (uint32_t i = 0; i < kBlkSlots; ++i) {
+        ptx::mbar_init(&s_full[i], 1);
+        ptx::mbar_init(&s_empty[i], 8 * 32);
+      }
     }
     *s_abort = 0;
     *s_bad = 0;
@@ -778,6 +797,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           report(p.err, MGQ_ERR_TIMEOUT);
           *s_abort = 1;
           break;
+        }
+        if (BLOCK) {
+          // this stage's float32 scales into ring slot it % kBlkSlots (free once
+          // the epilogue has promoted stage it - kBlkSlots)
+          const uint32_t sl = it % kBlkSlots;
+          if (!ptx::mbar_wait(&s_empty[sl], ((it / kBlkSlots) & 1) ^ 1, p.wait_ns)) {
+            report(p.err, MGQ_ERR_TIMEOUT);
+            *s_abort = 1;
+            break;
+          }
+          const int64_t kb = tl.kx0 / BK + s;
+          float* dst = sRing + sl * kBlkSlotFloats;
+          ptx::mbar_arrive_expect_tx(&s_full[sl], MODE == kModeContract ? kBlkSlotFloats * 4 : 128 * 4);
+          ptx::bulk_load(dst, p.sa + kb * p.sa_ld + tl.row_a, 128 * 4, &s_full[sl]);
+          if (MODE == kModeContract) ptx::bulk_load(dst + 128, p.sb + kb * p.sb_ld + tl.out_col, BN * 4, &s_full[sl]);
         }
         const uint32_t bytes = kABytes + kBBytes + (MX ? kSfaBytes + kSfbBytes : 0);
         ptx::mbar_arrive_expect_tx(&full[st], bytes);
@@ -889,6 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t h_tam = 0;    // per-tensor SwiGLU: this thread's max |h| (float bits)
     int ecur = 0;
     uint32_t tc = 0;
+    uint32_t it_e = 0;     // block scales: stage count, as the producer's `it`
     Tile tl;
     for (int64_t t = blockIdx.x; run && get_tile<MODE>(s_off, E, p, t, ecur, tl); t += gridDim.x) {
       const int64_t orow = tl.out_row + row_in_tile;
@@ -910,33 +945,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (BLOCK) {
         // promotion: acc += partial(stage) * s_a[row, kb] * s_b[n block, kb];
         // contract mode (wgrad, 128x1 blocks of both operands along the
-        // group's rows): acc += partial(stage) * s_a[row, kb] * s_b[column, kb]
-        const float* sa_row = p.sa + (tl.row_a + row_in_tile);
+        // group's rows): acc += partial(stage) * s_a[row, kb] * s_b[column, kb].
+        // The stage's row (and column) scales come from the shared ring slot
+        // the producer filled; rows mode's B tile scale is one float per
+        // stage and 128-column half, loaded one stage ahead.
         const float* sb_blk = MODE == kModeRows
                                   ? p.sb + ((int64_t)tl.e * (p.N / 128) + (col0 / 128)) * (p.K / 128)
-                                  : p.sb + col0;
+                                  : nullptr;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i) r[c][i] = 0u;   // +0.0f
-        // both scales are loaded one stage ahead of their partial product
-        float sa_next = sa_row[(tl.kx0 / 128) * p.sa_ld];
-        float sb_next = MODE == kModeRows ? sb_blk[tl.kx0 / 128] : 1.0f;
+        float sb_next = MODE == kModeRows ? __ldg(sb_blk + tl.kx0 / 128) : 1.0f;
         bool alive = true;
-        for (int s = 0; s < tl.nst; ++s) {
+        for (int s = 0; s < tl.nst; ++s, ++it_e) {
           const uint32_t a = tc % kAcc, aph = (tc / kAcc) & 1;
-          const float f = sa_next * sb_next;
-          // contract mode: this stage's 128 column scales of B (this half's
-          // columns), four per lane, loaded before the partial product is ready
-          float4 sb4 = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
-          if (MODE == kModeContract)
-            sb4 = __ldg(reinterpret_cast<const float4*>(sb_blk + (tl.kx0 / 128 + s) * p.sb_ld) + lane);
-          if (s + 1 < tl.nst) {
-            sa_next = sa_row[(tl.kx0 / 128 + s + 1) * p.sa_ld];
-            if (MODE == kModeRows) sb_next = sb_blk[tl.kx0 / 128 + s + 1];
-          }
+          const uint32_t sl = it_e % kBlkSlots;
+          const float sb_cur = sb_next;
+          if (MODE == kModeRows && s + 1 < tl.nst) sb_next = __ldg(sb_blk + tl.kx0 / 128 + s + 1);
           if (__any_sync(0xFFFFFFFFu, *s_abort != 0)) { alive = false; break; }
-          const bool got = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&tmem_full[a], aph, p.wait_ns));
+          const bool got = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&s_full[sl], (it_e / kBlkSlots) & 1, p.wait_ns) &&
+                                                       ptx::mbar_wait(&tmem_full[a], aph, p.wait_ns));
           if (!got) {
             report(p.err, MGQ_ERR_TIMEOUT);
             *s_abort = 1;
@@ -944,6 +973,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           ptx::tc_fence_after();
+          const float* slot = sRing + sl * kBlkSlotFloats;
+          const float f = slot[row_in_tile] * sb_cur;     // rows: s_a * s_b; contract: s_a
+          const float4* sbc = reinterpret_cast<const float4*>(slot + 128 + half * (BN / 2));
           const uint32_t taddr = tmem + a * BN + ((q * 32) << 16) + half * (BN / 2);
           // 16 columns per load keep the partial and the accumulator in registers
 #pragma unroll
@@ -953,24 +985,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              // contract mode: columns 16 c + 4 j .. + 3 are lane 4 c + j's four scales
-              float4 fq = make_float4(f, f, f, f);
+              uint32_t* acc = &r[c / 2][(c & 1) * 16 + 4 * j];
               if (MODE == kModeContract) {
-                const int src = 4 * c + j;
-                fq = make_float4(f * __shfl_sync(0xFFFFFFFFu, sb4.x, src), f * __shfl_sync(0xFFFFFFFFu, sb4.y, src),
-                                 f * __shfl_sync(0xFFFFFFFFu, sb4.z, src), f * __shfl_sync(0xFFFFFFFFu, sb4.w, src));
-              }
-              const float fj[4] = {fq.x, fq.y, fq.z, fq.w};
-#pragma unroll
-              for (int t = 0; t < 4; ++t) {
-                const int i = 4 * j + t;
-                r[c / 2][(c & 1) * 16 + i] =
-                    __float_as_uint(fmaf(__uint_as_float(v[i]), fj[t], __uint_as_float(r[c / 2][(c & 1) * 16 + i])));
+                // columns 16 c + 4 j .. + 3: their scales (the same for every
+                // lane: one broadcast read) times this row's s_a
+                const float4 cs = sbc[4 * c + j];
+                uint32_t f0, f1, f2, f3;
+                ptx::fmul2(f0, f1, __float_as_uint(cs.x), __float_as_uint(cs.y), __float_as_uint(f), __float_as_uint(f));
+                ptx::fmul2(f2, f3, __float_as_uint(cs.z), __float_as_uint(cs.w), __float_as_uint(f), __float_as_uint(f));
+                ptx::ffma2(acc[0], acc[1], v[4 * j], v[4 * j + 1], f0, f1);
+                ptx::ffma2(acc[2], acc[3], v[4 * j + 2], v[4 * j + 3], f2, f3);
+              } else {
+                ptx::ffma2(acc[0], acc[1], v[4 * j], v[4 * j + 1], __float_as_uint(f), __float_as_uint(f));
+                ptx::ffma2(acc[2], acc[3], v[4 * j + 2], v[4 * j + 3], __float_as_uint(f), __float_as_uint(f));
               }
             }
           }
           ptx::tc_fence_before();
           ptx::mbar_arrive(&tmem_empty[a]);
+          ptx::mbar_arrive(&s_empty[sl]);     // this thread's reads of the slot are done
           ++tc;
         }
         if (!alive) break;

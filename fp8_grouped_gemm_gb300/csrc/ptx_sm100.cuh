@@ -360,5 +360,23 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask
       : "memory");
 }
 
+// ---- packed float32 pairs (two independent IEEE round-to-nearest operations)
+// (d0, d1) = (a0 * b0 + d0, a1 * b1 + d1)
+__device__ __forceinline__ void ffma2(uint32_t& d0, uint32_t& d1, uint32_t a0, uint32_t a1, uint32_t b0, uint32_t b1) {
+  asm("{\n\t.reg .b64 d, a, b;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 d, {%0, %1};\n\t"
+      "fma.rn.f32x2 d, a, b, d;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "+r"(d0), "+r"(d1)
+      : "r"(a0), "r"(a1), "r"(b0), "r"(b1));
+}
+// (d0, d1) = (a0 * b0, a1 * b1)
+__device__ __forceinline__ void fmul2(uint32_t& d0, uint32_t& d1, uint32_t a0, uint32_t a1, uint32_t b0, uint32_t b1) {
+  asm("{\n\t.reg .b64 d, a, b;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=r"(d0), "=r"(d1)
+      : "r"(a0), "r"(a1), "r"(b0), "r"(b1));
+}
+
 }  // namespace ptx
 }  // namespace mgq

@@ -76,7 +76,8 @@ def weight_job(job):
     memory), quantised by the oracle with `job["recipe"]`:
       "mx"      MXFP8 e4m3 row-wise (and, with "col", the column-wise copy
                 quantize_mx(W^T) with blocks along N; n0, n1 multiples of 32)
-      "blk"     128x128 float32 tiles (n0, n1 multiples of 128)
+      "blk"     128x128 float32 tiles (n0, n1 multiples of 128; with "col",
+                the column-wise copy quantize_block_128x128(W^T))
       "nv"      NVFP4 1x16 with the expert's s_g
       "nv2d"    NVFP4 16x16 with the expert's s_g (row and column copies)
       "tensor"  per-tensor e4m3 with the expert's scale
@@ -121,6 +122,11 @@ def weight_job(job):
             cmp("codes", (e, slice(n0, n1)), c)
             cmp("scales", (e, slice(n0 // 128, n1 // 128)), si)
             deq = OQ.dequantize_block_128x128(c, si)
+            if job.get("col"):
+                cc, cs = OQ.quantize_block_128x128(np.ascontiguousarray(w.T))   # [K, n]
+                cmp("col_codes", (e, slice(None), slice(n0, n1)), cc)
+                cmp("col_scales", (e, slice(None), slice(n0 // 128, n1 // 128)), cs)
+                col_deq = OQ.dequantize_block_128x128(cc, cs)
         elif rec == "nv":
             sg = np.float32(job["s_g"])
             c, s = OQ.quantize_nvfp4(w, sg)
@@ -157,7 +163,7 @@ def weight_job(job):
 def rows_job(job):
     """Rows r0:r1 of an activation [M, C] in shared memory (bf16 bits, or
     float32 values), quantised row-wise by the oracle with `job["recipe"]`
-    ("mx", "mx_e5m2", "blk", "nv" with s_g, "tensor" / "tensor_e5m2" with a
+    ("mx", "mx_e5m2", "blk", "blk_e5m2", "nv" with s_g, "tensor" / "tensor_e5m2" with a
     scale). Returns (codes, scales or None)."""
     from oracle import quant as OQ
     s, v = _attach(job["x"])
@@ -166,8 +172,8 @@ def rows_job(job):
         rec = job["recipe"]
         if rec in ("mx", "mx_e5m2"):
             return OQ.quantize_mx(x, "e5m2" if rec == "mx_e5m2" else "e4m3")
-        if rec == "blk":
-            return OQ.quantize_block_1x128(x)
+        if rec in ("blk", "blk_e5m2"):
+            return OQ.quantize_block_1x128(x, "e5m2" if rec == "blk_e5m2" else "e4m3")
         if rec == "nv":
             return OQ.quantize_nvfp4(x, np.float32(job["s_g"]))
         if rec in ("tensor", "tensor_e5m2"):

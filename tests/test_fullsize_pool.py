@@ -36,9 +36,11 @@ def test_weight_sweep_equals_direct_oracle(recipe):
             gpu.setdefault("col_scales", []).append(cs)
         elif recipe == "blk":
             c, si = OQ.quantize_block_128x128(w[e])
+            cc, cs = OQ.quantize_block_128x128(np.ascontiguousarray(w[e].T))
             deq.append(OQ.dequantize_block_128x128(c, si))
-            gpu.setdefault("codes", []).append(c)
-            gpu.setdefault("scales", []).append(si)
+            deq_col.append(OQ.dequantize_block_128x128(cc, cs))
+            for key, v in (("codes", c), ("scales", si), ("col_codes", cc), ("col_scales", cs)):
+                gpu.setdefault(key, []).append(v)
         elif recipe in ("nv", "nv2d"):
             sg = OQ.nvfp4_global_scale(float(np.max(np.abs(w[e]))))
             per.setdefault("s_g", []).append(float(sg))
@@ -63,7 +65,7 @@ def test_weight_sweep_equals_direct_oracle(recipe):
     # plant one wrong byte in the GPU codes of expert 1
     gpu["codes"][1, 3, 5] ^= 1
     tot, fwd, dgrad = FP.weight_sweep(wb, recipe, gpu=gpu, a_rows=a, dy_rows=dy, chunk=128,
-                                      col=(recipe == "mx"), per_expert={k: np.array(v) for k, v in per.items()})
+                                      col=(recipe in ("mx", "blk")), per_expert={k: np.array(v) for k, v in per.items()})
     assert tot["codes"] == 1
     assert all(v == 0 for k, v in tot.items() if k != "codes")
     for e in range(E):
@@ -72,7 +74,7 @@ def test_weight_sweep_equals_direct_oracle(recipe):
         np.testing.assert_allclose(dgrad[e], dy[e] @ wcol.T, rtol=1e-12, atol=1e-12)
 
 
-@pytest.mark.parametrize("recipe", ["mx", "mx_e5m2", "blk", "nv", "tensor_e5m2"])
+@pytest.mark.parametrize("recipe", ["mx", "mx_e5m2", "blk", "blk_e5m2", "nv", "tensor_e5m2"])
 def test_quantize_rows_equals_direct_oracle(recipe):
     rng = np.random.default_rng(1)
     x = rng.standard_normal((300, 256))
@@ -82,8 +84,8 @@ def test_quantize_rows_equals_direct_oracle(recipe):
     c, s = FP.quantize_rows(xb, recipe, chunk=64, **kw)
     if recipe in ("mx", "mx_e5m2"):
         wc, ws = OQ.quantize_mx(xf, "e5m2" if recipe == "mx_e5m2" else "e4m3")
-    elif recipe == "blk":
-        wc, ws = OQ.quantize_block_1x128(xf)
+    elif recipe in ("blk", "blk_e5m2"):
+        wc, ws = OQ.quantize_block_1x128(xf, "e5m2" if recipe == "blk_e5m2" else "e4m3")
     elif recipe == "nv":
         wc, ws = OQ.quantize_nvfp4(xf, np.float32(100.0))
     else:

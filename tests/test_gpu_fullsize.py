@@ -16,6 +16,8 @@ What is compared, for every workload:
 * unpermute, permute-backward and the unpermute-backward's dY codes and
   dprobs: every token;
 * wgrads: 16 x 16 sampled (n, k) elements of every expert.
+Training runs for the per-tensor (delayed) headline, MXFP8, NVFP4 and
+blockwise recipes.
 """
 import numpy as np
 import pytest
@@ -512,3 +514,126 @@ def test_block_scaled_training_step_full_size(recipe):
             continue
         _wgrad_samples(lay.dw2, e, ns2, ks2, dy2c[:, lo:hi].T, hc[:, lo:hi].T)
         _wgrad_samples(lay.dw1, e, ns1, ks1, dc[:, lo:hi].T, xc[:, lo:hi].T)
+
+
+def test_blockwise_training_step_full_size():
+    """The Scout-shaped experts trained with blockwise FP8 at full size (1x128
+    row blocks and 128x1 column blocks of activations and gradients, 128x128
+    weight tiles; e4m3 forward, e5m2 gradients; Zipf loads with two empty
+    experts, top-1). Both copies of X and dY2 in full, both copies of every
+    weight in full, the forward GEMMs and the dgrads at the sampled rows
+    against all columns, h's and dY1's codes on the sampled rows and their
+    column copies on sampled columns, and sampled wgrad elements of every
+    expert from the column-wise copies."""
+    w, lay, x, idx, probs, dout, w1, w2, _, _ = _train_layer("scout_fwdbwd", 0)
+    E, H, F, k = w.E, w.H, w.F, w.k
+    rng = np.random.default_rng(13)
+    rim, src, off, cnt, Rp = _routing(lay, idx, E)
+    assert np.sum(cnt == 0) >= 1
+    filler = src < 0
+
+    def rows_si(buf):                      # row-wise scale_inv [C/128][R_cap] -> [R_cap, C/128]
+        return buf.cpu().numpy().T
+
+    def cols_si(buf, cols=None):           # column-wise [R_cap/128][C] -> [C, Rp/128]
+        a = buf.cpu().numpy()[:Rp // 128]
+        return (a if cols is None else a[:, cols]).T
+
+    # X: every routed row; the column-wise copy ([H, R_cap], 128x1 blocks along
+    # each group's tokens) in full
+    xb = _bits(x)
+    cx, sx = FP.quantize_rows(xb, "blk")
+    _check_permuted(u8_np(lay.xq), rows_si(lay.xs), cx, sx, rim, Rp, "X")
+    xperm_t = np.ascontiguousarray(OR.permute_rows(xb, rim, Rp).T)      # bf16 bits [H, Rp], filler rows 0
+    ccx, csx = FP.quantize_rows(xperm_t, "blk")
+    del xperm_t
+    assert np.array_equal(u8_np(lay.xcol)[:, :Rp], ccx)
+    assert np.array_equal(cols_si(lay.xcs), csx)
+    ee, rr = _sample_rows(off, cnt, rng)
+    toks = src[rr] // k
+    x_deq = OQ.dequantize_block_1x128(cx[toks], sx[toks])
+
+    # dY2 = float32(probs * dout): both copies in full; dprobs
+    dy32, dprobs_ref = OR.unpermute_bwd(bf16_np(dout), bf16_np(lay.y[:Rp]), rim, probs, Rp)
+    assert rel_fro(dprobs_ref, lay.dprobs.cpu().numpy()) <= 1e-5
+    c2, s2 = FP.quantize_rows(dy32, "blk_e5m2")
+    assert np.array_equal(u8_np(lay.dy2q[:Rp]), c2)
+    s2z = s2.copy()
+    s2z[filler] = 0.0
+    assert np.array_equal(rows_si(lay.dy2s)[:Rp], s2z)
+    cc2, cs2 = FP.quantize_rows(np.ascontiguousarray(dy32.T), "blk_e5m2")
+    assert np.array_equal(u8_np(lay.dy2col)[:, :Rp], cc2)
+    assert np.array_equal(cols_si(lay.dy2cs), cs2)
+    dy2_deq = OQ.dequantize_block_1x128(c2[rr], s2[rr], "e5m2")
+    del dy32
+
+    def weight_gpu(q, s, qc, scs):
+        return {"codes": u8_np(q), "scales": s.cpu().numpy(), "col_codes": u8_np(qc), "col_scales": scs.cpu().numpy()}
+
+    # forward: gate/up rows, SwiGLU, h's row codes on the sampled rows
+    gu_gpu = bf16_np(_gather(lay.gu, rr))
+    h_gpu = bf16_np(_gather(lay.h_bf16, rr))
+    check_elementwise(OL.swiglu(gu_gpu, F), h_gpu, "swiglu")
+    ch, sh = OQ.quantize_block_1x128(h_gpu)
+    assert np.array_equal(u8_np(_gather(lay.hq, rr)), ch)
+    assert np.array_equal(rows_si(lay.hs)[rr], sh)
+    h_deq = OQ.dequantize_block_1x128(ch, sh)
+
+    # W2 in full (both copies): down forward (all H columns) and down dgrad
+    # through the column copy (all F columns) at the sampled rows
+    w2b = _bits(w2)
+    tot, fwd2, dgr2 = FP.weight_sweep(w2b, "blk", gpu=weight_gpu(lay.w2q, lay.w2s, lay.w2col, lay.w2cs),
+                                      a_rows=_by_expert(ee, h_deq), dy_rows=_by_expert(ee, dy2_deq), col=True)
+    del w2b
+    assert all(v == 0 for v in tot.values()) and len(tot) == 4, tot
+    _gemm_check(fwd2, bf16_np(_gather(lay.y, rr)), ee, "down fwd")
+    dh_gpu = bf16_np(_gather(lay.dh, rr))
+    _gemm_check(dgr2, dh_gpu, ee, "down dgrad")
+
+    # dSwiGLU and dY1's row codes on the sampled rows
+    dgu_gpu = bf16_np(_gather(lay.dgu_bf16, rr))
+    check_elementwise(OL.dswiglu(dh_gpu, gu_gpu, F), dgu_gpu, "dswiglu")
+    c1, s1 = OQ.quantize_block_1x128(dgu_gpu, "e5m2")
+    assert np.array_equal(u8_np(_gather(lay.dy1q, rr)), c1)
+    assert np.array_equal(rows_si(lay.dy1s)[rr], s1)
+    dy1_deq = OQ.dequantize_block_1x128(c1, s1, "e5m2")
+
+    # W1 in full (both copies): gate/up forward and gate/up dgrad
+    w1b = _bits(w1)
+    tot, fwd1, dgr1 = FP.weight_sweep(w1b, "blk", gpu=weight_gpu(lay.w1q, lay.w1s, lay.w1col, lay.w1cs),
+                                      a_rows=_by_expert(ee, x_deq), dy_rows=_by_expert(ee, dy1_deq), col=True)
+    del w1b
+    assert all(v == 0 for v in tot.values()) and len(tot) == 4, tot
+    _gemm_check(fwd1, gu_gpu, ee, "gate/up fwd")
+    _gemm_check(dgr1, bf16_np(_gather(lay.dxp, rr)), ee, "gate/up dgrad")
+
+    check_elementwise(OR.unpermute(bf16_np(lay.y[:Rp]), rim, probs), bf16_np(lay.out), "unpermute")
+    check_elementwise(OR.permute_bwd(bf16_np(lay.dxp[:Rp]), rim), bf16_np(lay.dx), "permute_bwd")
+
+    # wgrads at 16 x 16 sampled (n, k) of every expert from the column-wise
+    # copies: dY2's and X's checked in full above; h's and dY1's requantised
+    # here from the GPU's bf16 columns and compared first
+    ns2, ks2 = np.sort(rng.choice(H, 16, replace=False)), np.sort(rng.choice(F, 16, replace=False))
+    ns1, ks1 = np.sort(rng.choice(2 * F, 16, replace=False)), np.sort(rng.choice(H, 16, replace=False))
+    sel = lambda t, idx_: t[torch.from_numpy(idx_).to(DEV)]                     # noqa: E731
+    dy2c = OQ.dequantize_block_1x128(cc2[ns2], cs2[ns2], "e5m2")
+    xc = OQ.dequantize_block_1x128(ccx[ks1], csx[ks1])
+    h_cols = OF.bf16_bits_to_f64(np.ascontiguousarray(_bits(lay.h_bf16[:Rp][:, torch.from_numpy(ks2).to(DEV)]).T))
+    d_cols = OF.bf16_bits_to_f64(np.ascontiguousarray(_bits(lay.dgu_bf16[:Rp][:, torch.from_numpy(ns1).to(DEV)]).T))
+    hc_c, hc_s = OQ.quantize_block_1x128(h_cols)
+    dc_c, dc_s = OQ.quantize_block_1x128(d_cols, "e5m2")
+    assert np.array_equal(u8_np(sel(lay.hcol, ks2))[:, :Rp], hc_c)
+    assert np.array_equal(u8_np(sel(lay.dy1col, ns1))[:, :Rp], dc_c)
+    assert np.array_equal(cols_si(lay.hcs, ks2), hc_s)
+    assert np.array_equal(cols_si(lay.dy1cs, ns1), dc_s)
+    hc = OQ.dequantize_block_1x128(hc_c, hc_s)
+    dc = OQ.dequantize_block_1x128(dc_c, dc_s, "e5m2")
+    dw1, dw2 = lay.dw1, lay.dw2
+    for e in range(E):
+        lo, hi = int(off[e]), int(off[e + 1])
+        if hi == lo:
+            # empty expert: zero weight gradients
+            assert float(dw1[e].abs().max()) == 0.0 and float(dw2[e].abs().max()) == 0.0
+            continue
+        _wgrad_samples(dw2, e, ns2, ks2, dy2c[:, lo:hi].T, hc[:, lo:hi].T)
+        _wgrad_samples(dw1, e, ns1, ks1, dc[:, lo:hi].T, xc[:, lo:hi].T)
