@@ -37,6 +37,17 @@ namespace {
 constexpr int BM = 128, BN = 256, BK = 128;     // BK: bytes = fp8 elements
 constexpr int STAGES = 4;
 constexpr int kThreads = 320;     // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
+// The 1-CTA kernel with float32 block scales (kind 2) runs 384 threads: warp 0
+// TMA, warp 1 MMA, warps 2-3 idle, warps 4-11 epilogue. After the prologue the
+// first warpgroup gives up registers (setmaxnreg) to the two epilogue
+// warpgroups, whose promotion keeps a 128-column float32 accumulator plus two
+// tensor-memory loads in flight. The split needs kBlkRegLaunch registers a
+// thread at launch (128 x kBlkRegLow + 256 x kBlkRegHigh <= 384 x that); the
+// launch checks the compiled kernel's count first.
+__host__ __device__ constexpr int threads_of(int kind) { return kind == 2 ? 384 : kThreads; }
+__host__ __device__ constexpr int epi_warp0(int kind) { return kind == 2 ? 4 : 2; }
+constexpr int kBlkRegLow = 40, kBlkRegHigh = 208, kBlkRegLaunch = 152;
+static_assert(128 * kBlkRegLow + 256 * kBlkRegHigh <= 384 * kBlkRegLaunch, "register split");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfaCol = 256;
 // scale bytes and tensor-memory scale columns per stage (MX: one chunk per
@@ -697,7 +708,7 @@ __device__ __forceinline__ void epilogue_dswiglu_mx(const GemmParams& p, uint32_
 // DSW: the down-projection dgrad with the dSwiGLU epilogue (a separate
 // instantiation, so the other epilogues keep their registers)
 template <int MODE, int KIND, bool DSW = false>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_of(KIND), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmH,
                         const GemmParams p) {
@@ -737,7 +748,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // In block mode the two buffers hold per-stage partial products.
   constexpr uint32_t kAcc = MX ? 1 : 2;
 
-  for (int i = threadIdx.x; i <= E; i += kThreads) s_off[i] = p.offsets[i];
+  constexpr int NT = threads_of(KIND), EW0 = epi_warp0(KIND);
+  for (int i = threadIdx.x; i <= E; i += NT) s_off[i] = p.offsets[i];
   if (threadIdx.x == 0) {
     for (int s = 0; s < STG; ++s) {
       ptx::mbar_init(&full[s], 1);
@@ -784,6 +796,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *s_tmem;
   const bool run = (*s_bad == 0);
 
+  if (warp < EW0) {
+  // (the register budget changes inside each role's branch: code after a
+  // setmaxnreg is compiled for that budget only where no other path joins it)
+  if (KIND == kKindBlock) ptx::setmaxnreg_dec<kBlkRegLow>();   // to the epilogue warpgroups
   if (run && warp == 0 && lane == 0 && !p.debug_stall) {
     // ------------------------------------------------------------ producer
     int ecur = 0;
@@ -910,16 +926,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++tc;
       }
     }
-  } else if (warp >= 2) {
+  }
+  } else {
+    if (KIND == kKindBlock) ptx::setmaxnreg_inc<kBlkRegHigh>();
     // ------------------------------------------------------------ epilogue
     // 8 warps: warp w reads tensor-memory lane quadrant w % 4 (the hardware
-    // rule) and the column half (w - 2) / 4 of the 256-column accumulator. The
+    // rule) and the column half (w - EW0) / 4 of the 256-column accumulator. The
     // whole accumulator is moved to registers first and released to the MMA
     // issuer; the scaling, conversion and stores overlap the next tile.
     const uint32_t q = warp & 3;
-    const uint32_t half = (uint32_t)(warp - 2) >> 2;
+    const uint32_t half = (uint32_t)(warp - EW0) >> 2;
     const int64_t row_in_tile = q * 32 + lane;
-    Stager sg{sOut + (warp - 2) * kStageOut * staging_slots(KIND), staging_slots(KIND), 0u};
+    Stager sg{sOut + (warp - EW0) * kStageOut * staging_slots(KIND), staging_slots(KIND), 0u};
     uint32_t h_tam = 0;    // per-tensor SwiGLU: this thread's max |h| (float bits)
     int ecur = 0;
     uint32_t tc = 0;
@@ -977,12 +995,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float f = slot[row_in_tile] * sb_cur;     // rows: s_a * s_b; contract: s_a
           const float4* sbc = reinterpret_cast<const float4*>(slot + 128 + half * (BN / 2));
           const uint32_t taddr = tmem + a * BN + ((q * 32) << 16) + half * (BN / 2);
-          // 16 columns per load keep the partial and the accumulator in registers
+          // 16 columns per load, two loads in flight: chunk c + 1 is read
+          // while chunk c is scaled and added
+          uint32_t vb[2][16];
+          ptx::tmem_ld_32x32b_x16(taddr, vb[0]);
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            uint32_t v[16];
-            ptx::tmem_ld_32x32b_x16(taddr + c * 16, v);
-            ptx::tmem_ld_wait();
+            uint32_t (&v)[16] = vb[c & 1];
+            ptx::tmem_ld_wait_regs(v);
+            if (c + 1 < 8) ptx::tmem_ld_32x32b_x16(taddr + (c + 1) * 16, vb[(c + 1) & 1]);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               uint32_t* acc = &r[c / 2][(c & 1) * 16 + 4 * j];
@@ -1064,7 +1085,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) atomic_max_nonneg(p.h_amax, __uint_as_float(h_tam));
     }
   }
-  if (warp >= 2 && lane == 0) ptx::bulk_wait0();   // this warp's TMA stores are complete
+  if (warp >= EW0 && lane == 0) ptx::bulk_wait0();   // this warp's TMA stores are complete
   __syncthreads();
   if (warp == 1) {
     __syncwarp();
@@ -1084,9 +1105,15 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
   if (dev < 64 && !attr_set[dev]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
       return MGQ_ERR_CUDA;
+    if (KIND == kKindBlock) {
+      // the register split must fit in what the block is launched with, or
+      // setmaxnreg.inc would never return: never launch such a build
+      cudaFuncAttributes fa;
+      if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.numRegs < kBlkRegLaunch) return MGQ_ERR_CUDA;
+    }
     attr_set[dev] = true;
   }
-  kern<<<num_sms(), kThreads, kSmemBytes, s>>>(ta, tb, to, th, p);
+  kern<<<num_sms(), threads_of(KIND), kSmemBytes, s>>>(ta, tb, to, th, p);
   MGQ_LAUNCH_CHECK();
   return MGQ_OK;
 }
