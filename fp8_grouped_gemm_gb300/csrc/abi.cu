@@ -74,7 +74,7 @@ bool encode_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint6
 }
 
 bool encode_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner, uint64_t outer,
-                    uint64_t pitch, uint32_t box_inner, uint32_t box_outer) {
+                    uint64_t pitch, uint32_t box_inner, uint32_t box_outer, bool sw128) {
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!load_encode()) return false;
@@ -87,7 +87,8 @@ bool encode_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t
                                  : elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
                                                    : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        sw128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 

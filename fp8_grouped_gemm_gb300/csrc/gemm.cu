@@ -68,10 +68,23 @@ __host__ __device__ constexpr uint32_t sf_stage_bytes(int kind) {
 // store's read-out behind; the other kinds have no shared memory to spare)
 constexpr uint32_t kStageOut = 32 * 64;
 __host__ __device__ constexpr uint32_t staging_slots(int kind) { return kind == 3 ? 2u : 1u; }
-__host__ __device__ constexpr uint32_t staging_bytes(int kind) { return 8 * kStageOut * staging_slots(kind); }
+// float32 block scales (kind 2) in contract mode (wgrad): the accumulator
+// lives in the epilogue's registers, so the MMA can run only two stages ahead
+// while a tile's 128 KB of float32 output is stored; each warp stages half its
+// tile slice at once in 8 KB, swizzled, and moves on while the TMA stores
+// drain it. That takes the shared memory of one pipeline stage; in rows mode
+// (bf16 output, long contractions) the fourth stage is worth more.
+constexpr uint32_t kStageWide = 32 * 256;
+__host__ __device__ constexpr bool wide_staging(int kind, int mode) { return kind == 2 && mode == 1; }
+__host__ __device__ constexpr uint32_t staging_bytes(int kind, int mode) {
+  return wide_staging(kind, mode) ? 8 * kStageWide : 8 * kStageOut * staging_slots(kind);
+}
 // pipeline depth: NVFP4's larger scale chunks leave room for 3 stages next to
-// the staging buffers (its 128-byte stages hold 256 elements of K)
-__host__ __device__ constexpr int stages_of(int kind) { return kind == 3 ? 3 : STAGES; }
+// the staging buffers (its 128-byte stages hold 256 elements of K); so do the
+// wide staging buffers
+__host__ __device__ constexpr int stages_of(int kind, int mode) {
+  return kind == 3 || wide_staging(kind, mode) ? 3 : STAGES;
+}
 // float32 block scales (kind 2): a ring of kBlkSlots slots, one per contraction
 // stage, each with the stage's 128 A row scales and (contract mode) the 256
 // B column scales of the tile, bulk-copied by the producer and read by the
@@ -79,11 +92,11 @@ __host__ __device__ constexpr int stages_of(int kind) { return kind == 3 ? 3 : S
 // plus the two tensor-memory buffers, so its slots are always free in time.
 constexpr uint32_t kBlkSlots = 8, kBlkSlotFloats = 128 + BN;
 __host__ __device__ constexpr uint32_t blk_ring_bytes(int kind) { return kind == 2 ? kBlkSlots * kBlkSlotFloats * 4 : 0u; }
-__host__ __device__ constexpr size_t smem_bytes(int kind) {
-  return 1024 /*align slack*/ + stages_of(kind) * (size_t)(kABytes + kBBytes + sf_stage_bytes(kind)) +
-         staging_bytes(kind) + blk_ring_bytes(kind) + 256 /*barriers*/ + (kMaxE + 8) * 4;
+__host__ __device__ constexpr size_t smem_bytes(int kind, int mode) {
+  return 1024 /*align slack*/ + stages_of(kind, mode) * (size_t)(kABytes + kBBytes + sf_stage_bytes(kind)) +
+         staging_bytes(kind, mode) + blk_ring_bytes(kind) + 256 /*barriers*/ + (kMaxE + 8) * 4;
 }
-static_assert(smem_bytes(2) <= 232448, "blockwise kernel exceeds the shared memory of a block");
+static_assert(smem_bytes(2, 0) <= 232448 && smem_bytes(2, 1) <= 232448, "blockwise kernel exceeds the shared memory");
 static_assert(kBlkSlots >= STAGES + 2, "the scale ring must cover the operand ring and both partial buffers");
 
 enum { kModeRows = 0, kModeContract = 1 };
@@ -314,6 +327,60 @@ __device__ __forceinline__ void epilogue_store(const GemmParams& p, const uint32
         *reinterpret_cast<uint4*>(o + c * 32 + i) = v;
       }
     }
+  }
+}
+
+// Stores one warp's 32 rows x 128 accumulator columns (kind 2: alpha is 1)
+// through its 8 KB staging buffer `stg` and TMA stores of 32 rows x 128 bytes
+// with the 128-byte swizzle (16-byte chunk j of row l at chunk j ^ (l % 8):
+// the eight lanes of each shared-memory phase hit distinct banks). bf16 goes
+// out in one round of two boxes, float32 in two; a round first waits until
+// the stores that last read the buffer have read it.
+__device__ __forceinline__ void epilogue_store_wide(const GemmParams& p, const uint32_t (&r)[4][32], uint8_t* stg,
+                                                    const CUtensorMap* tmO, int64_t col0, int32_t y0, uint32_t lane) {
+  auto chunk = [&](int b, int j) -> uint4* {
+    return reinterpret_cast<uint4*>(stg + b * 4096 + lane * 128 + ((j ^ (lane & 7)) << 4));
+  };
+  auto issue = [&](int x0, int ncols) {
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      ptx::tma_store_2d(tmO, stg, (int32_t)(col0 + x0), y0);
+      ptx::tma_store_2d(tmO, stg + 4096, (int32_t)(col0 + x0 + ncols), y0);
+      ptx::bulk_commit();
+    }
+  };
+  auto wait_buffer = [&]() {
+    if (lane == 0) ptx::bulk_wait_read0();
+    __syncwarp();
+  };
+  if (p.out_f32) {
+#pragma unroll
+    for (int rd = 0; rd < 2; ++rd) {
+      wait_buffer();
+#pragma unroll
+      for (int b = 0; b < 2; ++b)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int c = 2 * rd + b;      // columns 32 c .. 32 c + 31
+          *chunk(b, j) = make_uint4(r[c][4 * j], r[c][4 * j + 1], r[c][4 * j + 2], r[c][4 * j + 3]);
+        }
+      issue(64 * rd, 32);
+    }
+  } else {
+    wait_buffer();
+#pragma unroll
+    for (int b = 0; b < 2; ++b)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int c = 2 * b + j / 4, i = (j % 4) * 8;     // columns 64 b + 8 j ..
+        *chunk(b, j) = make_uint4(
+            pack_bf16x2(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])),
+            pack_bf16x2(__uint_as_float(r[c][i + 2]), __uint_as_float(r[c][i + 3])),
+            pack_bf16x2(__uint_as_float(r[c][i + 4]), __uint_as_float(r[c][i + 5])),
+            pack_bf16x2(__uint_as_float(r[c][i + 6]), __uint_as_float(r[c][i + 7])));
+      }
+    issue(0, 64);
   }
 }
 
@@ -712,7 +779,7 @@ __global__ void __launch_bounds__(threads_of(KIND), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmH,
                         const GemmParams p) {
-  constexpr int STG = stages_of(KIND);
+  constexpr int STG = stages_of(KIND, MODE);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -723,8 +790,8 @@ __global__ void __launch_bounds__(threads_of(KIND), 1)
   uint8_t* sSFA = sB + STG * kBBytes;
   uint8_t* sSFB = sSFA + STG * kSfaBytes;
   uint8_t* sOut = sSFA + STG * sf_stage_bytes(KIND);       // epilogue staging (TMA stores)
-  float* sRing = reinterpret_cast<float*>(sOut + staging_bytes(KIND));   // block scales
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + staging_bytes(KIND) + blk_ring_bytes(KIND));
+  float* sRing = reinterpret_cast<float*>(sOut + staging_bytes(KIND, MODE));   // block scales
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + staging_bytes(KIND, MODE) + blk_ring_bytes(KIND));
   uint64_t* full = bars;
   uint64_t* empty = bars + STG;
   uint64_t* tmem_full = bars + 2 * STG;        // [2]
@@ -1071,7 +1138,10 @@ __global__ void __launch_bounds__(threads_of(KIND), 1)
       }
       float alpha = 1.0f;
       if (KIND == kKindTensor || NV) alpha = 1.0f / (p.sa[0] * p.sb[MODE == kModeRows ? tl.e : 0]);
-      if (MODE == kModeRows && KIND != kKindBlock && p.swiglu)
+      if (wide_staging(KIND, MODE) && p.tma_store)
+        epilogue_store_wide(p, r, sOut + (warp - EW0) * kStageWide, &tmO, col0, (int32_t)(tl.out_row + q * 32),
+                            lane);
+      else if (MODE == kModeRows && KIND != kKindBlock && p.swiglu)
         epilogue_swiglu<KIND == kKindBlock ? kKindTensor : KIND>(p, r, alpha, orow, tl.out_col + half * 64,
                                                                  sg, &tmO, &tmH,
                                                                  (int32_t)(tl.out_row + q * 32), lane, h_tam);
@@ -1098,7 +1168,7 @@ template <int MODE, int KIND, bool DSW = false>
 int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const CUtensorMap& th,
                 const GemmParams& p, cudaStream_t s) {
   auto kern = grouped_gemm_kernel<MODE, KIND, DSW>;
-  constexpr size_t kSmemBytes = smem_bytes(KIND);
+  constexpr size_t kSmemBytes = smem_bytes(KIND, MODE);
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1824,7 +1894,10 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
   {
     const int eb = p.out_f32 ? 4 : 2;
     const uint64_t orows = mode == kModeRows ? (uint64_t)R_cap : (uint64_t)E * N;
-    if (out && !encode_tmap_2d(&to, out, eb, (uint64_t)p.ldo, orows, (uint64_t)p.ldo * eb, 64 / eb, 32))
+    // float32 block scales in contract mode: 128-byte swizzled boxes (the wide staging)
+    const bool wide = wide_staging(kind, mode);
+    if (out && !encode_tmap_2d(&to, out, eb, (uint64_t)p.ldo, orows, (uint64_t)p.ldo * eb, (wide ? 128 : 64) / eb,
+                               32, wide))
       return MGQ_ERR_CUDA;
     p.tma_store = (beta == 0.0f && !direct_store_forced()) ? 1 : 0;
   }

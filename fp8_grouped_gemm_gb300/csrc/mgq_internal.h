@@ -18,10 +18,11 @@ int* error_word();
 bool encode_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch,
                        uint32_t box_inner, uint32_t box_outer);
 
-// 2D row-major tensor map of 8-, 16- or 32-bit elements (elem_bytes 1, 2 or 4),
-// no swizzle: `inner` elements per row, `outer` rows, pitch bytes.
+// 2D row-major tensor map of 8-, 16- or 32-bit elements (elem_bytes 1, 2 or 4):
+// `inner` elements per row, `outer` rows, pitch bytes; no swizzle, or with
+// sw128 the 128-byte swizzle (box_inner * elem_bytes == 128).
 bool encode_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner, uint64_t outer,
-                    uint64_t pitch, uint32_t box_inner, uint32_t box_outer);
+                    uint64_t pitch, uint32_t box_inner, uint32_t box_outer, bool sw128 = false);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
