@@ -197,6 +197,7 @@ struct PermuteArgs {
   int32_t* rim;            // row_id_map: rank inside the chunk in, final row out
   int32_t* src_row;
   int resolve;             // 0: rim already holds the final rows
+  int nv_rowmajor;         // NVFP4: write the scales row-major ([R_cap][H/16]) for retile_nv_scales
 };
 
 // ---- routing pass 3 (standalone routing only): final rows and src_row -------
@@ -387,7 +388,8 @@ __global__ void __launch_bounds__(256) permute_quant_nv_kernel(PermuteArgs a) {
       for (int c = lane * 32; c < H; c += 32 * 32)
         *reinterpret_cast<uint4*>(a.codes + r * (H / 2) + c / 2) = make_uint4(0, 0, 0, 0);
       for (int b4 = lane; b4 < H / 64; b4 += 32)
-        *reinterpret_cast<uint32_t*>(a.scales + tiled_scale_offset(r, (int64_t)b4 * 4, H / 64)) = 0u;
+        *reinterpret_cast<uint32_t*>(a.scales + (a.nv_rowmajor ? r * (H / 16) + b4 * 4
+                                                                : tiled_scale_offset(r, (int64_t)b4 * 4, H / 64))) = 0u;
     }
     return;
   }
@@ -412,9 +414,47 @@ __global__ void __launch_bounds__(256) permute_quant_nv_kernel(PermuteArgs a) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       if (j >= a.k || !act) break;
-      if (dest[j] >= 0) store32_nv(o, a.codes, a.scales, dest[j], c, H, lane);
+      const int r = dest[j];
+      if (r < 0) continue;
+      if (a.nv_rowmajor) {
+        // codes as usual; the lane pair's 4 scale bytes at their row-major place
+        *reinterpret_cast<uint4*>(a.codes + (int64_t)r * (H / 2) + c / 2) = make_uint4(o.cw[0], o.cw[1], o.cw[2], o.cw[3]);
+        if ((lane & 1) == 0) *reinterpret_cast<uint32_t*>(a.scales + (int64_t)r * (H / 16) + c / 16) = o.s4;
+      } else {
+        store32_nv(o, a.codes, a.scales, r, c, H, lane);
+      }
     }
   }
+  }
+}
+
+// ---- NVFP4 scales: row-major -> 128x4-tiled, in place ------------------------
+// A token row's scales go to k scattered destination rows; in the tiled
+// layout each row owns only 4 contiguous bytes of every 512-byte tile, so the
+// permute writes them row-major (64 contiguous bytes per warp and destination)
+// and this pass re-tiles them. The 128 rows of a row group occupy the same
+// 128 x H/16 bytes in both layouts, so each CTA loads its group's block into
+// shared memory (row stride kb4 + 1 words: conflict-free column reads) and
+// writes it back tiled. Groups past the used rows (offsets[E]) are left alone.
+__global__ void __launch_bounds__(256) retile_nv_scales_kernel(uint8_t* scales, int kb4, const int32_t* rows_used) {
+  extern __shared__ uint32_t rt_words[];          // [128][kb4 + 1]
+  const int64_t g = blockIdx.x;
+  if (g * 128 >= (int64_t)*rows_used) return;
+  uint8_t* blk = scales + g * (int64_t)kb4 * 512;
+  const int ld = kb4 + 1;
+  const int nvec = 128 * kb4 / 4;                 // 16-byte pieces of the block
+  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+    const uint4 x = reinterpret_cast<const uint4*>(blk)[v];
+    const int w = 4 * v, row = w / kb4, jj = w - row * kb4;   // kb4 is a multiple of 4 (H % 256 == 0)
+    uint32_t* d = rt_words + row * ld + jj;
+    d[0] = x.x; d[1] = x.y; d[2] = x.z; d[3] = x.w;
+  }
+  __syncthreads();
+  // tile j, line l (16 bytes): word j of rows l, l + 32, l + 64, l + 96
+  for (int line = threadIdx.x; line < kb4 * 32; line += blockDim.x) {
+    const int jj = line >> 5, l = line & 31;
+    reinterpret_cast<uint4*>(blk)[line] = make_uint4(rt_words[l * ld + jj], rt_words[(l + 32) * ld + jj],
+                                                     rt_words[(l + 64) * ld + jj], rt_words[(l + 96) * ld + jj]);
   }
 }
 
@@ -567,6 +607,7 @@ int permute_impl(const void* x_bf16, int T, int H, int k, int E, const mgq_qdesc
   a.s_out = q->tensor_scale;
   a.R_cap = R_cap;
   a.e8m0_rceil = q->e8m0_mode == MGQ_E8M0_RCEIL;
+  a.nv_rowmajor = 0;
   // token CTAs: FP8 kernels stride over the tokens from at most four resident
   // waves (keeping the next chunk in flight across tokens); the NVFP4 kernel,
   // whose tokens fan out to many destinations, runs one token per warp
@@ -578,8 +619,23 @@ int permute_impl(const void* x_bf16, int T, int H, int k, int E, const mgq_qdesc
   if (sc == MGQ_NV16_UE4M3) {
     int rc = launch_amax_groups(a.x, (int64_t)T * H, 1, q->amax_out, s);
     if (rc != MGQ_OK) return rc;
+    // row-major scales and a re-tiling pass, when a row group's scales fit a
+    // CTA's shared memory
+    const int kb4 = H / 64;
+    const size_t rt_smem = (size_t)128 * (kb4 + 1) * 4;
+    a.nv_rowmajor = (H % 256 == 0 && rt_smem <= 200 * 1024) ? 1 : 0;
+    if (a.nv_rowmajor && rt_smem > 48 * 1024) {
+      if (cudaFuncSetAttribute(retile_nv_scales_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rt_smem) !=
+          cudaSuccess)
+        return MGQ_ERR_CUDA;
+    }
     permute_quant_nv_kernel<<<grid, 256, 0, s>>>(a);
     MGQ_LAUNCH_CHECK();
+    if (a.nv_rowmajor) {
+      retile_nv_scales_kernel<<<(unsigned)(R_cap / 128), 256, rt_smem, s>>>(static_cast<uint8_t*>(q->row.scale), kb4,
+                                                                          offsets + E);
+      MGQ_LAUNCH_CHECK();
+    }
     // column-wise copy (16-row blocks along the permuted rows) from the gathered rows
     if (q->col.data) return gather_x_rowcol(a.x, src_row, k, H, R_cap, offsets + E, false, q, s);
     return MGQ_OK;
