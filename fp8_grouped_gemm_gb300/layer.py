@@ -451,7 +451,12 @@ class ExpertLayer:
             # permute_bwd
             return fwd + 2 + 4 + (3 + 1 + 1 + 2 + 1 + 1 + 1)
         if self.nv:
-            return fwd + 2 + 4                          # + amax passes (x, h); weights: 2 x (amax + rows)
+            # + amax passes (x, h); weights: 2 x (amax + rows); the permute's
+            # row-major scales re-tiled in a second pass when a 128-row group's
+            # scales fit a CTA's shared memory
+            H = self.w.H
+            retile = 1 if H % 256 == 0 and 128 * (H // 64 + 1) * 4 <= 200 * 1024 else 0
+            return fwd + 2 + 4 + retile
         if not self.train:
             return fwd + 2                              # weight quantisation (row)
         wq = 2                                          # weights: rows (+ columns) in one pass each

@@ -32,7 +32,7 @@ CASES = {
                       "gemm_wgrad_gateup", "permute_bwd"], 18),
     "mixtral_fwd": ("mxfp8", False, ["gemm_fwd_gateup_swiglu", "gemm_fwd_down", "unpermute"], 9),
     "scout_fwd": ("blockwise", False, ["gemm_fwd_gateup", "swiglu_quant", "gemm_fwd_down", "unpermute"], 10),
-    "finegrained_fwd": ("nvfp4", False, ["gemm_fwd_gateup_swiglu", "gemm_fwd_down", "unpermute"], 13),
+    "finegrained_fwd": ("nvfp4", False, ["gemm_fwd_gateup_swiglu", "gemm_fwd_down", "unpermute"], 14),
 }
 
 
