@@ -288,11 +288,17 @@ int mgq_grouped_quantize(const void* x_bf16, int64_t R_cap, int64_t C, const int
  *        leaves dW_e unchanged (beta 1).
  * scaling: MGQ_MX32_E8M0 (e4m3/e5m2 codes with blocked E8M0 scales),
  *        MGQ_TENSOR_F32 (scale = device float s: one for A / dY, E for the
- *        weight; the product is multiplied by 1/(s_a s_b)), or, for fwd and
- *        dgrad, MGQ_BLK_1x128_F32: A with 1x128 float32 scale_inv
- *        [K/128][R_cap], W with 128x128 float32 scale_inv [E][N/128][K/128]
- *        ([BLOCK]'s DeepSeek-style recipe; each 128-deep partial product is
- *        scaled and summed in float32), or MGQ_NV16_UE4M3 (fwd, dgrad and
+ *        weight; the product is multiplied by 1/(s_a s_b)), or
+ *        MGQ_BLK_1x128_F32 ([BLOCK]'s DeepSeek-style recipe; each 128-deep
+ *        partial product is scaled and summed in float32): for fwd and dgrad
+ *        A (dY) with 1x128 float32 scale_inv [K/128][R_cap] and W (Wcol)
+ *        with 128x128 float32 scale_inv [E][N/128][K/128]; for wgrad the
+ *        column-wise copies with 128x1 blocks along each group's rows,
+ *        scale_inv [R_cap/128][N] for dYcol and [R_cap/128][K] for Acol
+ *        (one per column and 128 rows). The blockwise kernel needs at
+ *        least 152 registers a thread in its compiled form (its register
+ *        split); a build below that returns MGQ_ERR_CUDA instead of
+ *        launching. Or MGQ_NV16_UE4M3 (fwd, dgrad and
  *        wgrad): e2m1 codes packed two per byte along the contraction (ld and
  *        the contraction length in elements, multiples of 256), 16-element
  *        ue4m3 block scales, and each operand's global_scale s_g (A / dY /
