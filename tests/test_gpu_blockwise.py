@@ -349,3 +349,12 @@ def test_gemm_dgrad_and_wgrad_blockwise(mgq, fmts):
     assert np.all(got2[1] == 0.0)
     for e in (0, 2):
         assert rel_fro(2.0 * ref[e], got2[e]) <= GEMM_TOL_F32, e
+    # bf16 dW (beta 0): the same products, rounded once
+    dWb = torch.full((E, N, K), 3.0, dtype=torch.bfloat16, device=DEV)
+    mgq.grouped_gemm_wgrad(A_, B_, mgq.BLK_1x128_F32, offd, E, R_cap, N, K, dWb, 0.0, mgq.OUT_BF16)
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    gotb = bf16_np(dWb)
+    assert np.all(gotb[1] == 0.0)
+    for e in (0, 2):
+        assert rel_fro(OF.round_to_bf16(ref[e]), gotb[e]) <= GEMM_TOL_BF16, e
