@@ -439,17 +439,20 @@ template <int DT>
 __global__ void __launch_bounds__(256, 4) quant_tile128_kernel(const uint16_t* __restrict__ x, int64_t N, int64_t K,
                                                                uint8_t* __restrict__ codes, float* __restrict__ sinv) {
   // one tile per CTA; a thread's 64 values stay packed bf16 pairs (32
-  // registers), so four CTAs fit an SM
+  // registers), so four CTAs fit an SM. Each load instruction of a warp
+  // covers two whole 256-byte tile rows, so every sector it requests is used
+  // in full (16-byte lanes at a wider stride leave each request's sectors
+  // half used)
   __shared__ uint32_t s_max[8];
   const int64_t nb = N / 128, kb = K / 128;
   const int64_t tile = blockIdx.x;
   const int64_t g = tile / (nb * kb), rem = tile % (nb * kb);
-  const int row = threadIdx.x >> 1, cofs = (threadIdx.x & 1) * 64;
-  const int64_t off = (g * N + (rem / kb) * 128 + row) * K + (rem % kb) * 128 + cofs;
+  // chunk q of this thread: tile row 16 q + t / 16, 16-byte column chunk t % 16
+  // (a warp's load covers two whole 256-byte rows)
+  const int64_t base = (g * N + (rem / kb) * 128 + threadIdx.x / 16) * K + (rem % kb) * 128 + (threadIdx.x % 16) * 8;
   uint4 w[8];
-  const uint4* src = reinterpret_cast<const uint4*>(x + off);
 #pragma unroll
-  for (int q = 0; q < 8; ++q) w[q] = __ldg(src + q);
+  for (int q = 0; q < 8; ++q) w[q] = __ldg(reinterpret_cast<const uint4*>(x + base + (int64_t)q * 16 * K));
   uint32_t acc = 0;
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
@@ -465,19 +468,14 @@ __global__ void __launch_bounds__(256, 4) quant_tile128_kernel(const uint16_t* _
 #pragma unroll
   for (int i = 0; i < 8; ++i) m = max(m, s_max[i]);
   const float sc = blk_scale<DT>(m);
-  uint4* dst = reinterpret_cast<uint4*>(codes + off);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint4 a = w[2 * q], b = w[2 * q + 1];
-    dst[q] = make_uint4(
+  for (int q = 0; q < 8; ++q) {
+    const uint4 a = w[q];
+    *reinterpret_cast<uint2*>(codes + base + (int64_t)q * 16 * K) = make_uint2(
         cvt_fp8x4<DT>(__fmul_rn(bf16_lo(a.x), sc), __fmul_rn(bf16_hi(a.x), sc), __fmul_rn(bf16_lo(a.y), sc),
                       __fmul_rn(bf16_hi(a.y), sc)),
         cvt_fp8x4<DT>(__fmul_rn(bf16_lo(a.z), sc), __fmul_rn(bf16_hi(a.z), sc), __fmul_rn(bf16_lo(a.w), sc),
-                      __fmul_rn(bf16_hi(a.w), sc)),
-        cvt_fp8x4<DT>(__fmul_rn(bf16_lo(b.x), sc), __fmul_rn(bf16_hi(b.x), sc), __fmul_rn(bf16_lo(b.y), sc),
-                      __fmul_rn(bf16_hi(b.y), sc)),
-        cvt_fp8x4<DT>(__fmul_rn(bf16_lo(b.z), sc), __fmul_rn(bf16_hi(b.z), sc), __fmul_rn(bf16_lo(b.w), sc),
-                      __fmul_rn(bf16_hi(b.w), sc)));
+                      __fmul_rn(bf16_hi(a.w), sc)));
   }
   if (threadIdx.x == 0) sinv[tile] = __fdiv_rn(1.0f, sc);
 }
