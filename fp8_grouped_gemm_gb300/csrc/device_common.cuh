@@ -76,6 +76,60 @@ __device__ __forceinline__ uint32_t cvt_fp8x4(float a, float b, float c, float d
   if (DT == MGQ_E4M3) return cvt_e4m3x2(a, b) | (cvt_e4m3x2(c, d) << 16);
   return cvt_e5m2x2(a, b) | (cvt_e5m2x2(c, d) << 16);
 }
+// four values times m -> four codes in one word, element 0 in the low byte.
+// The products are float32 round-to-nearest (packed f32x2 multiplies, the
+// same IEEE rounding as four __fmul_rn), then cast like cvt_fp8x4.
+template <int DT>
+__device__ __forceinline__ uint32_t cvt_fp8x4_mul(float a, float b, float c, float d, float m) {
+  uint32_t r;
+  if (DT == MGQ_E4M3)
+    asm("{\n\t.reg .b64 p, q, s;\n\t.reg .b32 a, b, c, d;\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b64 s, {%5, %5};\n\t"
+        "mov.b64 p, {%1, %2};\n\tmul.rn.f32x2 p, p, s;\n\tmov.b64 {a, b}, p;\n\t"
+        "mov.b64 q, {%3, %4};\n\tmul.rn.f32x2 q, q, s;\n\tmov.b64 {c, d}, q;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 lo, b, a;\n\tcvt.rn.satfinite.e4m3x2.f32 hi, d, c;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(r)
+        : "r"(__float_as_uint(a)), "r"(__float_as_uint(b)), "r"(__float_as_uint(c)), "r"(__float_as_uint(d)),
+          "r"(__float_as_uint(m)));
+  else
+    asm("{\n\t.reg .b64 p, q, s;\n\t.reg .b32 a, b, c, d;\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b64 s, {%5, %5};\n\t"
+        "mov.b64 p, {%1, %2};\n\tmul.rn.f32x2 p, p, s;\n\tmov.b64 {a, b}, p;\n\t"
+        "mov.b64 q, {%3, %4};\n\tmul.rn.f32x2 q, q, s;\n\tmov.b64 {c, d}, q;\n\t"
+        "cvt.rn.satfinite.e5m2x2.f32 lo, b, a;\n\tcvt.rn.satfinite.e5m2x2.f32 hi, d, c;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(r)
+        : "r"(__float_as_uint(a)), "r"(__float_as_uint(b)), "r"(__float_as_uint(c)), "r"(__float_as_uint(d)),
+          "r"(__float_as_uint(m)));
+  return r;
+}
+// four bf16 values (two packed pairs, element 0 in the low half of w0) times m
+template <int DT>
+__device__ __forceinline__ uint32_t cvt_fp8x4_bf16_mul(uint32_t w0, uint32_t w1, float m) {
+  return cvt_fp8x4_mul<DT>(bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1), m);
+}
+// eight values times m -> one word of e2m1 codes, element 2i in the low nibble
+// of byte i (float32 round-to-nearest products, packed f32x2 multiplies)
+__device__ __forceinline__ uint32_t cvt_e2m1x8_mul(const float* v, float m) {
+  uint32_t r;
+  asm("{\n\t.reg .b64 p0, p1, p2, p3, s;\n\t.reg .b32 a<8>;\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b64 s, {%9, %9};\n\t"
+      "mov.b64 p0, {%1, %2};\n\tmul.rn.f32x2 p0, p0, s;\n\tmov.b64 {a0, a1}, p0;\n\t"
+      "mov.b64 p1, {%3, %4};\n\tmul.rn.f32x2 p1, p1, s;\n\tmov.b64 {a2, a3}, p1;\n\t"
+      "mov.b64 p2, {%5, %6};\n\tmul.rn.f32x2 p2, p2, s;\n\tmov.b64 {a4, a5}, p2;\n\t"
+      "mov.b64 p3, {%7, %8};\n\tmul.rn.f32x2 p3, p3, s;\n\tmov.b64 {a6, a7}, p3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, a1, a0;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, a3, a2;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, a5, a4;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, a7, a6;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(m)));
+  return r;
+}
 // eight e2m1 values -> one word, element 2i in the low nibble of byte i
 __device__ __forceinline__ uint32_t cvt_e2m1x8(const float* v) {
   uint32_t r;

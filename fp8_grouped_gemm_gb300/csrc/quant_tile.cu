@@ -42,6 +42,19 @@ constexpr int TR = 128, TC = 128;  // tile rows x columns (per part)
 constexpr int LD = TC + 8;          // bf16 tile row pitch in elements (rows stay 16-byte aligned)
 constexpr int kStgBytes = TC * TR;  // one part's staged column codes (FP8): 128 rows of 128 bytes
 
+// Tile layout: element (row, col) of a bf16 tile [rows][LD] sits in 16-byte
+// unit (col / 8) ^ sw(row) of its row, sw(row) = 2 * ((row / 32) % 4). With
+// the padded pitch alone, lanes reading one column in the four 32-row blocks
+// hit the same bank; the swizzle moves the blocks 0, 32, 64 and 96 bytes apart,
+// so the column reads are conflict-free whichever lanes share an instruction.
+// Row reads and the 16-byte tile writes stay conflict-free (a row's units are
+// only permuted).
+__device__ __forceinline__ int tile_sw(int row) { return (row >> 4) & 6; }
+// element offset of (row, col); col a multiple of 8 for a 16-byte unit
+__device__ __forceinline__ int tix(int row, int col) {
+  return row * LD + ((((col >> 3) ^ tile_sw(row))) << 3) + (col & 7);
+}
+
 // Staged column-wise codes (FP8 kinds, gathered sources): the CTA's writes to the staging tiles
 // become visible to the TMA unit, then one thread stores each part's tile
 // ([128 output rows][128 bytes] at output row y0 + p * part_off, byte x0).
@@ -204,7 +217,7 @@ struct RowColArgs {
 
 // ---- the quantisation of one tile (shared by both kernels) -----------------
 
-// One NVFP4 block of 16 values (scaled in place): scale code =
+// One NVFP4 block of 16 values: scale code =
 // ue4m3(float32(amax_b / 6) * s_g); with sc its value, r = s_g / sc (0 when sc
 // is 0) and each element is e2m1(v * r). Returns the scale code.
 __device__ __forceinline__ uint32_t nv_block16(float* v, float amax_b, float s_g, uint2& codes) {
@@ -212,9 +225,7 @@ __device__ __forceinline__ uint32_t nv_block16(float* v, float amax_b, float s_g
   const uint32_t code = cvt_ue4m3(t);
   const float sc = ue4m3_value(code);
   const float r = (sc == 0.0f) ? 0.0f : __fdiv_rn(s_g, sc);
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], r);
-  codes = make_uint2(cvt_e2m1x8(v), cvt_e2m1x8(v + 8));
+  codes = make_uint2(cvt_e2m1x8_mul(v, r), cvt_e2m1x8_mul(v + 8, r));
   return code;
 }
 
@@ -245,9 +256,7 @@ __device__ __forceinline__ void col_block_out(float* v, uint32_t amax_bits, floa
     }
     uint32_t cw[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      cw[i] = cvt_fp8x4<DT>(__fmul_rn(v[4 * i], mult), __fmul_rn(v[4 * i + 1], mult), __fmul_rn(v[4 * i + 2], mult),
-                            __fmul_rn(v[4 * i + 3], mult));
+    for (int i = 0; i < 8; ++i) cw[i] = cvt_fp8x4_mul<DT>(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3], mult);
     if (stg) {
       uint4* row = reinterpret_cast<uint4*>(stg + cl * 128);
       const int k0 = rl / 16;
@@ -280,11 +289,12 @@ __device__ __forceinline__ void row_phase(const uint16_t* tile, int64_t r0, int6
     const int p = pr / TR, rr = pr % TR;
     const int64_t r = r0 + rr;
     const int64_t cb = c0 + p * a.part_off + 32 * seg;   // first output column of the block
-    const uint4* src = reinterpret_cast<const uint4*>(&tile[(p * TR + rr) * LD + 32 * seg]);
+    const uint4* src = reinterpret_cast<const uint4*>(&tile[(p * TR + rr) * LD]);
+    const int usw = tile_sw(rr);
     uint32_t ww[16];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const uint4 w = src[q ^ sw];
+      const uint4 w = src[(4 * seg + (q ^ sw)) ^ usw];
       ww[4 * q] = w.x; ww[4 * q + 1] = w.y; ww[4 * q + 2] = w.z; ww[4 * q + 3] = w.w;
     }
     if constexpr (SC == MGQ_NV16_UE4M3) {
@@ -333,9 +343,7 @@ __device__ __forceinline__ void row_phase(const uint16_t* tile, int64_t r0, int6
     }
     uint32_t cw[8];        // codes in the order held (chunk q ^ sw in cw[2q], cw[2q + 1])
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      cw[i] = cvt_fp8x4<DT>(__fmul_rn(bf16_lo(ww[2 * i]), mult), __fmul_rn(bf16_hi(ww[2 * i]), mult),
-                            __fmul_rn(bf16_lo(ww[2 * i + 1]), mult), __fmul_rn(bf16_hi(ww[2 * i + 1]), mult));
+    for (int i = 0; i < 8; ++i) cw[i] = cvt_fp8x4_bf16_mul<DT>(ww[2 * i], ww[2 * i + 1], mult);
     if (r < nrows) {
       uint8_t* dst = a.row_codes + r * a.C + cb;
       *reinterpret_cast<uint4*>(dst + 8 * sw) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
@@ -378,6 +386,8 @@ __device__ __forceinline__ void col_phase(const uint16_t* tile, const float* fac
   const bool by_rows = stg0 == nullptr && (SC == MGQ_MX32_E8M0 || SC == MGQ_TENSOR_F32);
   const int cp = by_rows ? (tid >> 2) : (tid & 63), rb = by_rows ? (tid & 3) : ((tid >> 6) & 3);
   const int cc = 2 * cp;
+  // the thread's column pair inside a swizzled tile row of its row block
+  const int cx = (((cc >> 3) ^ (2 * rb)) << 3) + (cc & 7);
   const int64_t rg = r0 - g * a.M + 32 * rb;                 // row inside the group
 #pragma unroll 1
   for (int p = 0; p < P; ++p) {
@@ -388,7 +398,7 @@ __device__ __forceinline__ void col_phase(const uint16_t* tile, const float* fac
       // column's codes with its scale (two columns per thread)
       const int64_t rtile = (r0 - g * a.M) / TR;
       auto val = [&](int i, int h) {
-        const float x = __uint_as_float((uint32_t)tile[(p * TR + 32 * rb + i) * LD + cc + h] << 16);
+        const float x = __uint_as_float((uint32_t)tile[(p * TR + 32 * rb + i) * LD + cx + h] << 16);
         if constexpr (FAC) return __fmul_rn(fac[32 * rb + i], x);
         else return x;
       };
@@ -419,7 +429,7 @@ __device__ __forceinline__ void col_phase(const uint16_t* tile, const float* fac
         float v[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-          v[i] = __fmul_rn(fac[32 * rb + i], __uint_as_float((uint32_t)tile[(p * TR + 32 * rb + i) * LD + cc + h] << 16));
+          v[i] = __fmul_rn(fac[32 * rb + i], __uint_as_float((uint32_t)tile[(p * TR + 32 * rb + i) * LD + cx + h] << 16));
         const uint32_t m = absmax_bits_f32(v, 32);
         am = max(am, m);
         col_block_out<SC, DT>(v, m, ts, a, crow + h, rg, stg, cc + h, 32 * rb);
@@ -427,7 +437,7 @@ __device__ __forceinline__ void col_phase(const uint16_t* tile, const float* fac
     } else {
       uint32_t w[32];      // the two columns' 32 values as bf16 pairs
 #pragma unroll
-      for (int i = 0; i < 32; ++i) w[i] = *reinterpret_cast<const uint32_t*>(&tile[(p * TR + 32 * rb + i) * LD + cc]);
+      for (int i = 0; i < 32; ++i) w[i] = *reinterpret_cast<const uint32_t*>(&tile[(p * TR + 32 * rb + i) * LD + cx]);
       uint32_t amh[2] = {0, 0};
       if (SC == MGQ_MX32_E8M0 || (SC == MGQ_TENSOR_F32 && a.amax_out)) {
         uint32_t acc = 0;
@@ -519,7 +529,7 @@ __global__ void __launch_bounds__(256, Src::kParts == 2 ? 3 : 4)
         const int rr = chunk >> 4, cc = (chunk & 15) * 8;
         if (SC == MGQ_TENSOR_F32 || T128)
           am2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(am2, w[i].x), w[i].y), w[i].z), w[i].w);
-        *reinterpret_cast<uint4*>(&tile[rr * LD + cc]) = w[i];
+        *reinterpret_cast<uint4*>(&tile[tix(rr, cc)]) = w[i];
       }
     } else {
     // the operands of kBatch chunks loaded together
@@ -548,7 +558,7 @@ __global__ void __launch_bounds__(256, Src::kParts == 2 ? 3 : 4)
         for (int p = 0; p < P; ++p) {
           if (SC == MGQ_TENSOR_F32)
             am2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(am2, o[p].x), o[p].y), o[p].z), o[p].w);
-          *reinterpret_cast<uint4*>(&tile[(p * TR + rr) * LD + cc]) = o[p];
+          *reinterpret_cast<uint4*>(&tile[p * TR * LD + tix(rr, cc)]) = o[p];
         }
       }
     }
@@ -641,7 +651,7 @@ __global__ void __launch_bounds__(256, 3)
       const int chunk = tid + 256 * j;
       const int rr = chunk >> 4, cc = (chunk & 15) * 8;
       const int64_t off = s_off[rt & 1][rr];
-      cp_async16(&t[rr * LD + cc], src.base() + (off >= 0 ? off + c0 + cc : 0), off >= 0);
+      cp_async16(&t[tix(rr, cc)], src.base() + (off >= 0 ? off + c0 + cc : 0), off >= 0);
     }
     cp_async_commit();
   };
@@ -809,18 +819,22 @@ RowColArgs make_args(const mgq_qdesc* q, int64_t rows_cap, const int32_t* rows_u
 
 // ---- NVFP4 weights with 16x16 blocks ------------------------------------------
 // One 128x128 tile of a group's [M, K] weight per CTA, staged in shared
-// memory: the 64 block amaxes (4 threads per 16x16 block), then the ue4m3
-// scale code and multiplier r = s_g / sc of each block by the 1x16 rule, then
-// the row-wise copy ([G*M, K/2], one 1x16 block per thread step) and the
-// column-wise copy ([G*K, M/2], a thread takes 64 rows of one column). Both
-// copies' 1x16 blocks carry the scale of their 16x16 block.
+// memory (swizzled like the row/column tiles): the 64 block amaxes (4 threads
+// per 16x16 block), then the ue4m3 scale code and multiplier r = s_g / sc of
+// each block by the 1x16 rule, then the row-wise copy ([G*M, K/2], one 1x16
+// block per thread step) and the column-wise copy ([G*K, M/2]). Both copies'
+// 1x16 blocks carry the scale of their 16x16 block. In the column-wise copy a
+// thread takes two adjacent columns of one 32-row quarter, and the four
+// quarters of a column are adjacent lanes, so one store instruction writes
+// the whole 64-byte piece of 8 output rows.
 __global__ void __launch_bounds__(256) quant_nv2d_kernel(const uint16_t* x, int64_t M, int64_t K, uint8_t* row_codes,
                                                          uint8_t* row_scales, uint8_t* col_codes, uint8_t* col_scales,
                                                          const float* amax, float* s_out) {
   __shared__ __align__(16) uint16_t tile[TR * LD];
-  __shared__ uint8_t s_code[64];
+  __shared__ __align__(16) uint8_t s_code[64];
   __shared__ float s_r[64];
   const int tid = threadIdx.x;
+  const uint32_t lane = tid & 31;
   const int64_t c0 = (int64_t)blockIdx.x * TC, r0 = (int64_t)blockIdx.y * TR;
   const int64_t g = r0 / M, m0 = r0 - g * M;    // group, first row inside it
   const float s_g = nv_global_scale(amax[g]);
@@ -835,7 +849,7 @@ __global__ void __launch_bounds__(256) quant_nv2d_kernel(const uint16_t* x, int6
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int chunk = tid + 256 * i;
-      *reinterpret_cast<uint4*>(&tile[(chunk >> 4) * LD + (chunk & 15) * 8]) = w[i];
+      *reinterpret_cast<uint4*>(&tile[tix(chunk >> 4, (chunk & 15) * 8)]) = w[i];
     }
   }
   __syncthreads();
@@ -845,8 +859,9 @@ __global__ void __launch_bounds__(256) quant_nv2d_kernel(const uint16_t* x, int6
     uint32_t acc = 0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const uint4* p = reinterpret_cast<const uint4*>(&tile[(16 * br + 4 * q + j) * LD + 16 * bc]);
-      const uint4 w0 = p[0], w1 = p[1];
+      const int row = 16 * br + 4 * q + j;
+      const uint4 w0 = *reinterpret_cast<const uint4*>(&tile[tix(row, 16 * bc)]);
+      const uint4 w1 = *reinterpret_cast<const uint4*>(&tile[tix(row, 16 * bc + 8)]);
       acc = absmax_acc_bf16x2(absmax_acc_bf16x2(absmax_acc_bf16x2(absmax_acc_bf16x2(acc, w0.x), w0.y), w0.z), w0.w);
       acc = absmax_acc_bf16x2(absmax_acc_bf16x2(absmax_acc_bf16x2(absmax_acc_bf16x2(acc, w1.x), w1.y), w1.z), w1.w);
     }
@@ -862,45 +877,54 @@ __global__ void __launch_bounds__(256) quant_nv2d_kernel(const uint16_t* x, int6
     }
   }
   __syncthreads();
-  // row-wise copy: items (row, 16-column block), 4 per thread
+  // row-wise copy: items (row, 16-column block), 4 per thread; the lane of
+  // blocks 0 and 4 of a row stores the row's four scale codes of its half
 #pragma unroll 1
   for (int j = 0; j < 4; ++j) {
     const int item = tid + 256 * j, row = item >> 3, blk = item & 7;
     const int b = (row >> 4) * 8 + blk;
     const float r = s_r[b];
-    const uint4* p = reinterpret_cast<const uint4*>(&tile[row * LD + 16 * blk]);
-    const uint4 w0 = p[0], w1 = p[1];
-    const uint32_t ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    const uint4 w0 = *reinterpret_cast<const uint4*>(&tile[tix(row, 16 * blk)]);
+    const uint4 w1 = *reinterpret_cast<const uint4*>(&tile[tix(row, 16 * blk + 8)]);
     float y[16];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      y[2 * i] = __fmul_rn(bf16_lo(ww[i]), r);
-      y[2 * i + 1] = __fmul_rn(bf16_hi(ww[i]), r);
-    }
+    unpack8_bf16(w0, y);
+    unpack8_bf16(w1, y + 8);
     const int64_t grow = r0 + row, c = c0 + 16 * blk;
-    *reinterpret_cast<uint2*>(row_codes + grow * (K / 2) + c / 2) = make_uint2(cvt_e2m1x8(y), cvt_e2m1x8(y + 8));
-    row_scales[tiled_scale_offset(grow, c / 16, K / 64)] = s_code[b];
+    *reinterpret_cast<uint2*>(row_codes + grow * (K / 2) + c / 2) = make_uint2(cvt_e2m1x8_mul(y, r),
+                                                                                cvt_e2m1x8_mul(y + 8, r));
+    if ((blk & 3) == 0)
+      *reinterpret_cast<uint32_t*>(row_scales + tiled_scale_offset(grow, c / 16, K / 64)) =
+          *reinterpret_cast<const uint32_t*>(&s_code[b]);
   }
   if (!col_codes) return;
-  // column-wise copy: column col, row blocks 4 hb .. 4 hb + 3 (64 rows, 32 bytes)
+  // column-wise copy: columns 2 cp, 2 cp + 1, rows 32 qr .. 32 qr + 31 (the
+  // 16x16 blocks 2 qr and 2 qr + 1 of the columns' block column)
   {
-    const int col = tid & 127, hb = tid >> 7;
-    const int64_t crow = g * K + c0 + col;        // row of the column-wise copy
-    uint32_t out[8];
+    const int qr = lane & 3, cp = (tid >> 5) * 8 + (int)(lane >> 2);
+    const int cc = 2 * cp;
+    const int cx = (((cc >> 3) ^ (2 * qr)) << 3) + (cc & 7);   // swizzled column offset (tile_sw of rows 32 qr..)
+    uint32_t w[32];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int rb = 4 * hb + k, b = rb * 8 + (col >> 4);
-      const float r = s_r[b];
-      float y[16];
+    for (int i = 0; i < 32; ++i) w[i] = *reinterpret_cast<const uint32_t*>(&tile[(32 * qr + i) * LD + cx]);
+    const int b0 = (2 * qr) * 8 + (cc >> 4), b1 = b0 + 8;
+    const float rk[2] = {s_r[b0], s_r[b1]};
+    const uint16_t sc2 = (uint16_t)(s_code[b0] | (s_code[b1] << 8));
 #pragma unroll
-      for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(__uint_as_float((uint32_t)tile[(16 * rb + i) * LD + col] << 16), r);
-      out[2 * k] = cvt_e2m1x8(y);
-      out[2 * k + 1] = cvt_e2m1x8(y + 8);
-      col_scales[tiled_scale_offset(crow, (m0 + 16 * rb) / 16, M / 64)] = s_code[b];
+    for (int h = 0; h < 2; ++h) {
+      uint32_t out[4];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        float y[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) y[i] = h ? bf16_hi(w[16 * k + i]) : bf16_lo(w[16 * k + i]);
+        out[2 * k] = cvt_e2m1x8_mul(y, rk[k]);
+        out[2 * k + 1] = cvt_e2m1x8_mul(y + 8, rk[k]);
+      }
+      const int64_t crow = g * K + c0 + cc + h;                  // row of the column-wise copy
+      *reinterpret_cast<uint4*>(col_codes + crow * (M / 2) + (m0 + 32 * qr) / 2) =
+          make_uint4(out[0], out[1], out[2], out[3]);
+      *reinterpret_cast<uint16_t*>(col_scales + tiled_scale_offset(crow, (m0 + 32 * qr) / 16, M / 64)) = sc2;
     }
-    uint4* dst = reinterpret_cast<uint4*>(col_codes + crow * (M / 2) + (m0 + 64 * hb) / 2);
-    dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
-    dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
   }
 }
 

@@ -319,11 +319,7 @@ __global__ void __launch_bounds__(256, 4) permute_quant_kernel(PermuteArgs a) {
       }
       uint32_t cw[G / 4];
 #pragma unroll
-      for (int i = 0; i < G / 4; ++i) {
-        const float v0 = __fmul_rn(bf16_lo(wq[2 * i]), mult), v1 = __fmul_rn(bf16_hi(wq[2 * i]), mult);
-        const float v2 = __fmul_rn(bf16_lo(wq[2 * i + 1]), mult), v3 = __fmul_rn(bf16_hi(wq[2 * i + 1]), mult);
-        cw[i] = cvt_fp8x4<DT>(v0, v1, v2, v3);
-      }
+      for (int i = 0; i < G / 4; ++i) cw[i] = cvt_fp8x4_bf16_mul<DT>(wq[2 * i], wq[2 * i + 1], mult);
       // MX: the 4 scale bytes of 4 consecutive blocks (lanes 4 LB j, + LB, ..) into lane 4 LB j
       uint32_t s4 = 0;
       if (SC == MGQ_MX32_E8M0) {

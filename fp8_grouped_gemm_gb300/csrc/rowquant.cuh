@@ -53,9 +53,7 @@ __device__ __forceinline__ void quantize32(const float* v, uint32_t amax_bits, f
     o.sinv = __fdiv_rn(1.0f, s);
   }
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-    o.cw[i] = cvt_fp8x4<DT>(__fmul_rn(v[4 * i], mult), __fmul_rn(v[4 * i + 1], mult),
-                            __fmul_rn(v[4 * i + 2], mult), __fmul_rn(v[4 * i + 3], mult));
+  for (int i = 0; i < 8; ++i) o.cw[i] = cvt_fp8x4_mul<DT>(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3], mult);
 }
 
 // Stores the lane's block of row r, columns [c, c + 32), of a matrix with row
@@ -131,11 +129,8 @@ __device__ __forceinline__ void quantize32_nv(const float* v, float s_g, Block32
     const uint32_t code = cvt_ue4m3(t);
     const float sc = ue4m3_value(code);
     const float r = (sc == 0.0f) ? 0.0f : __fdiv_rn(s_g, sc);
-    float y[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(vb[i], r);
-    o.cw[2 * blk] = cvt_e2m1x8(y);
-    o.cw[2 * blk + 1] = cvt_e2m1x8(y + 8);
+    o.cw[2 * blk] = cvt_e2m1x8_mul(vb, r);
+    o.cw[2 * blk + 1] = cvt_e2m1x8_mul(vb + 8, r);
     sc2 |= code << (8 * blk);
   }
   const uint32_t nb = __shfl_down_sync(0xFFFFFFFFu, sc2, 1);
