@@ -24,9 +24,9 @@
 // ([G][M/128][C/128] and [G][C/128][M/128]).
 // Kernels: quant_rowcol_kernel (one tile per CTA: plain and computed sources),
 // quant_rowcol_stream_kernel (gathered rows: a CTA walks a range of tiles and
-// stages the next with cp.async; FP8 column codes go out through a staged
-// tile and one TMA store per item), quant_nv2d_kernel (NVFP4 weights with 16x16
-// blocks: both copies share the block scales).
+// stages the next with cp.async; the FP8 column codes of dY = probs * dout go
+// out through a staged tile and one TMA store per item), quant_nv2d_kernel
+// (NVFP4 weights with 16x16 blocks: both copies share the block scales).
 #include "mgq_internal.h"
 #include "ptx_sm100.cuh"
 #include "rowquant.cuh"
@@ -85,6 +85,7 @@ __device__ __forceinline__ void wait_col_tiles(int tid) {
 //    bf16 operands (fetch, then make), loads of several chunks in flight
 struct SrcPlain {
   static constexpr bool kComputed = false;
+  static constexpr bool kFactor = false;
   static constexpr bool kStream = false;      // one tile per CTA (4 CTAs per SM) is faster for dense rows
   static constexpr int kParts = 1;
   const uint16_t* x;
@@ -99,6 +100,7 @@ __device__ __forceinline__ void unpack8_bf16(const uint4 w, float* v) {
 // h = bf16(silu(g) * u), g = gu[:, :F], u = gu[:, F:]; h optionally written out
 struct SrcSwiglu {
   static constexpr bool kComputed = true;
+  static constexpr bool kFactor = false;
   static constexpr bool kStream = false;
   static constexpr int kParts = 1;
   static constexpr int kLoads = 2;
@@ -127,6 +129,7 @@ struct SrcSwiglu {
 // (columns f and F + f) when requested. One read of dh, g, u serves both.
 struct SrcDswiglu {
   static constexpr bool kComputed = true;
+  static constexpr bool kFactor = false;
   static constexpr bool kStream = false;
   static constexpr int kParts = 2;
   static constexpr int kLoads = 3;
@@ -374,16 +377,15 @@ template <int P, int SC, int DT, bool FAC>
 __device__ __forceinline__ void col_phase(const uint16_t* tile, const float* fac, int64_t g, int64_t r0, int64_t c0,
                                           float ts, const RowColArgs& a, int tid, uint32_t& am, uint32_t* s_cm,
                                           uint8_t* stg0 = nullptr) {
-  // thread -> (column pair cp, 32-row block rb). With direct FP8 stores of
-  // MX or per-tensor codes a warp takes 8 column pairs x the 4 row blocks, so
-  // each store instruction covers whole 128-byte output rows (8 of them)
-  // instead of 32-byte pieces of 32 rows, at the price of 4-way bank
-  // conflicts on the column reads (measured: MX weights 0.71 -> 0.80 of the
-  // copy bandwidth, 128x128 tiles 0.79 -> 0.90, MX dSwiGLU 0.59 -> 0.63).
-  // Otherwise a warp takes 32 column pairs of one row block (conflict-free
-  // reads): staged stores, NVFP4, and blockwise 128x1, which measured slower
-  // with the other mapping.
-  const bool by_rows = stg0 == nullptr && (SC == MGQ_MX32_E8M0 || SC == MGQ_TENSOR_F32);
+  // thread -> (column pair cp, 32-row block rb). A warp takes 8 column pairs
+  // x the 4 row blocks, so each direct store instruction covers whole output
+  // rows of the tile (128 FP8 bytes or 64 NVFP4 bytes, 8 of them) instead of
+  // pieces of 32 rows; the tile swizzle keeps its column reads conflict-free.
+  // The factor pass (dY = probs * dout) is the exception: there a warp takes
+  // 32 column pairs of one row block, which measured faster for it (with the
+  // FP8 column codes staged for one TMA store), while the whole-row mapping
+  // measured faster for every other source and format.
+  const bool by_rows = stg0 == nullptr && !FAC;
   const int cp = by_rows ? (tid >> 2) : (tid & 63), rb = by_rows ? (tid & 3) : ((tid >> 6) & 3);
   const int cc = 2 * cp;
   // the thread's column pair inside a swizzled tile row of its row block
@@ -721,22 +723,22 @@ int set_smem(Kern kern, size_t smem, bool* attr_set) {
 template <class Src, int SC, int DT>
 int launch_rowcol_t(const Src& src, RowColArgs a, cudaStream_t s) {
   static bool attr_set[64] = {false};   // one per instantiation
-  // FP8 column copies go out through staged TMA stores: a map of the column
-  // output [G * C rows, M bytes], 128 x 128-byte boxes
+  // FP8 column copies of the factor pass go out through staged TMA stores: a
+  // map of the column output [G * C rows, M bytes], 128 x 128-byte boxes
   CUtensorMap tmc;
   memset(&tmc, 0, sizeof(tmc));
   a.col_tma = 0;
-  // (measured: the gathered-row passes gain from the staging; the one-tile
-  // CTAs of plain and computed sources do not, and two-part tiles would fit
-  // only two CTAs an SM)
-  if (SC != MGQ_NV16_UE4M3 && Src::kStream && a.col_codes) {
+  // (measured: the factor pass gains from the staging; the gathered X with
+  // whole-row column stores and three CTAs an SM, and the one-tile CTAs of
+  // plain and computed sources, do not)
+  if (SC != MGQ_NV16_UE4M3 && Src::kStream && Src::kFactor && a.col_codes) {
     if (!encode_tmap_u8_2d(&tmc, a.col_codes, (uint64_t)a.M, (uint64_t)((a.rows_cap / a.M) * a.C), (uint64_t)a.M,
                            128, 128))
       return MGQ_ERR_CUDA;
     a.col_tma = 1;
   }
   constexpr int P = Src::kParts;
-  constexpr size_t stg_max = (SC == MGQ_NV16_UE4M3 || !Src::kStream) ? 0 : 1024 + (size_t)kStgBytes;
+  constexpr size_t stg_max = (SC == MGQ_NV16_UE4M3 || !Src::kStream || !Src::kFactor) ? 0 : 1024 + (size_t)kStgBytes;
   const size_t stg = a.col_tma ? stg_max : 0;
   if constexpr (!Src::kStream) {
     constexpr size_t tiles = (size_t)P * TR * LD * sizeof(uint16_t);
