@@ -50,10 +50,66 @@ __device__ __forceinline__ void dswiglu_f32(float d, float g, float u, float& dg
   dg = __fmul_rn(__fmul_rn(__fmul_rn(d, u), s), t);
   du = __fmul_rn(__fmul_rn(d, g), s);
 }
+// Packed float32 pairs (sm_100 f32x2 forms): each lane is one IEEE operation
+// with round-to-nearest, the same result as the scalar __fadd_rn / __fsub_rn /
+// __fmul_rn / __fmaf_rn.
+struct f32x2 {
+  float x, y;
+};
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("{\n\t.reg .b64 p, q, d;\n\tmov.b64 p, {%2, %3};\n\tmov.b64 q, {%4, %5};\n\t"
+      "mul.rn.f32x2 d, p, q;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("{\n\t.reg .b64 p, q, d;\n\tmov.b64 p, {%2, %3};\n\tmov.b64 q, {%4, %5};\n\t"
+      "add.rn.f32x2 d, p, q;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("{\n\t.reg .b64 p, q, d;\n\tmov.b64 p, {%2, %3};\n\tmov.b64 q, {%4, %5};\n\t"
+      "sub.rn.f32x2 d, p, q;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 r;
+  asm("{\n\t.reg .b64 p, q, s, d;\n\tmov.b64 p, {%2, %3};\n\tmov.b64 q, {%4, %5};\n\t"
+      "mov.b64 s, {%6, %7};\n\tfma.rn.f32x2 d, p, q, s;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return r;
+}
+// dswiglu_f32 of two elements: the same operations in the same order, paired
+__device__ __forceinline__ void dswiglu_f32x2(f32x2 d, f32x2 g, f32x2 u, f32x2& dg, f32x2& du) {
+  const f32x2 one{1.0f, 1.0f};
+  const f32x2 den = add2(one, f32x2{__expf(-g.x), __expf(-g.y)});
+  const f32x2 s{__fdividef(1.0f, den.x), __fdividef(1.0f, den.y)};
+  const f32x2 t = fma2(g, sub2(one, s), one);
+  dg = mul2(mul2(mul2(d, u), s), t);
+  du = mul2(mul2(d, g), s);
+}
 __device__ __forceinline__ void dswiglu_bf16(float d, float g, float u, float& dg, float& du) {
   dswiglu_f32(d, g, u, dg, du);
   dg = round_bf16(dg);
   du = round_bf16(du);
+}
+// dswiglu_bf16 of elements i, i + 1 of d, g, u (paired)
+__device__ __forceinline__ void dswiglu_bf16x2(const float* d, const float* g, const float* u, float* dg, float* du) {
+  f32x2 a, b;
+  dswiglu_f32x2(f32x2{d[0], d[1]}, f32x2{g[0], g[1]}, f32x2{u[0], u[1]}, a, b);
+  dg[0] = round_bf16(a.x);
+  dg[1] = round_bf16(a.y);
+  du[0] = round_bf16(b.x);
+  du[1] = round_bf16(b.y);
 }
 
 // ---------------------------------------------------------------------------

@@ -121,9 +121,7 @@ __global__ void __launch_bounds__(256) dswiglu_quant_kernel(DswigluArgs a) {
       load_bf16x32(a.gu + r * 2 * F + c, g);
       load_bf16x32(a.gu + r * 2 * F + F + c, u);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        dswiglu_bf16(d[i], g[i], u[i], dg[i], du[i]);
-      }
+      for (int i = 0; i < 32; i += 2) dswiglu_bf16x2(d + i, g + i, u + i, dg + i, du + i);
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i) dg[i] = du[i] = 0.0f;
@@ -586,7 +584,7 @@ __global__ void __launch_bounds__(256) dswiglu_dgu_kernel(const uint16_t* __rest
       load_bf16x32(gu + r * 2 * F + c, g);
       load_bf16x32(gu + r * 2 * F + F + c, u);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) dswiglu_bf16(d[i], g[i], u[i], dg[i], du[i]);
+      for (int i = 0; i < 32; i += 2) dswiglu_bf16x2(d + i, g + i, u + i, dg + i, du + i);
       tam = max(tam, max(absmax_bits_f32(dg, 32), absmax_bits_f32(du, 32)));
       store_bf16x32(dgu + r * 2 * F + c, dg);
       store_bf16x32(dgu + r * 2 * F + F + c, du);

@@ -631,11 +631,15 @@ __device__ __forceinline__ void epilogue_dswiglu(const GemmParams& p, uint32_t t
     uint32_t v[16];
     ptx::tmem_ld_32x32b_x16(tcol + 16 * c, v);
     ptx::tmem_ld_wait();
-    float d[16];
+    float d[16];   // dh = bf16(acc * alpha), as float
 #pragma unroll
-    for (int i = 0; i < 16; ++i) d[i] = round_bf16(__uint_as_float(v[i]) * alpha);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) dhw[8 * (c & 1) + i] = pack_bf16x2(d[2 * i], d[2 * i + 1]);
+    for (int i = 0; i < 8; ++i) {
+      const f32x2 pr = mul2(f32x2{__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])}, f32x2{alpha, alpha});
+      const uint32_t w = pack_bf16x2(pr.x, pr.y);
+      dhw[8 * (c & 1) + i] = w;
+      d[2 * i] = bf16_lo(w);
+      d[2 * i + 1] = bf16_hi(w);
+    }
     if (p.out && (c & 1)) {   // dh: 32 columns at col0 + 16 (c - 1)
 #pragma unroll
       for (int j = 0; j < 4; ++j) stage(j, make_uint4(dhw[4 * j], dhw[4 * j + 1], dhw[4 * j + 2], dhw[4 * j + 3]),
@@ -650,11 +654,11 @@ __device__ __forceinline__ void epilogue_dswiglu(const GemmParams& p, uint32_t t
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int k = 8 * q + 2 * i;
-        float g0, g1, u0, u1;
-        dswiglu_f32(d[k], bf16_lo(gw[i]), bf16_lo(uw[i]), g0, u0);
-        dswiglu_f32(d[k + 1], bf16_hi(gw[i]), bf16_hi(uw[i]), g1, u1);
-        dgp[4 * q + i] = pack_bf16x2(g0, g1);
-        dup[4 * q + i] = pack_bf16x2(u0, u1);
+        f32x2 dg, du;
+        dswiglu_f32x2(f32x2{d[k], d[k + 1]}, f32x2{bf16_lo(gw[i]), bf16_hi(gw[i])},
+                      f32x2{bf16_lo(uw[i]), bf16_hi(uw[i])}, dg, du);
+        dgp[4 * q + i] = pack_bf16x2(dg.x, dg.y);
+        dup[4 * q + i] = pack_bf16x2(du.x, du.y);
         am2 = absmax_bf16x2(absmax_bf16x2(am2, dgp[4 * q + i]), dup[4 * q + i]);
       }
     }
@@ -670,12 +674,10 @@ __device__ __forceinline__ void epilogue_dswiglu(const GemmParams& p, uint32_t t
     }
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-      const float a0 = __fmul_rn(bf16_lo(dgp[2 * w]), ts), a1 = __fmul_rn(bf16_hi(dgp[2 * w]), ts);
-      const float a2 = __fmul_rn(bf16_lo(dgp[2 * w + 1]), ts), a3 = __fmul_rn(bf16_hi(dgp[2 * w + 1]), ts);
-      const float b0 = __fmul_rn(bf16_lo(dup[2 * w]), ts), b1 = __fmul_rn(bf16_hi(dup[2 * w]), ts);
-      const float b2 = __fmul_rn(bf16_lo(dup[2 * w + 1]), ts), b3 = __fmul_rn(bf16_hi(dup[2 * w + 1]), ts);
-      cg[4 * (c & 3) + w] = e5 ? cvt_fp8x4<MGQ_E5M2>(a0, a1, a2, a3) : cvt_fp8x4<MGQ_E4M3>(a0, a1, a2, a3);
-      cu[4 * (c & 3) + w] = e5 ? cvt_fp8x4<MGQ_E5M2>(b0, b1, b2, b3) : cvt_fp8x4<MGQ_E4M3>(b0, b1, b2, b3);
+      cg[4 * (c & 3) + w] = e5 ? cvt_fp8x4_bf16_mul<MGQ_E5M2>(dgp[2 * w], dgp[2 * w + 1], ts)
+                               : cvt_fp8x4_bf16_mul<MGQ_E4M3>(dgp[2 * w], dgp[2 * w + 1], ts);
+      cu[4 * (c & 3) + w] = e5 ? cvt_fp8x4_bf16_mul<MGQ_E5M2>(dup[2 * w], dup[2 * w + 1], ts)
+                               : cvt_fp8x4_bf16_mul<MGQ_E4M3>(dup[2 * w], dup[2 * w + 1], ts);
     }
     if ((c & 3) == 3) {   // 64 columns of codes: dG at col0 + 16 (c - 3), dU F further
 #pragma unroll

@@ -149,7 +149,14 @@ struct SrcDswiglu {
     unpack8_bf16(w[1], g);
     unpack8_bf16(w[2], u);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) dswiglu_f32(d[i], g[i], u[i], dg[i], du[i]);
+    for (int i = 0; i < 8; i += 2) {
+      f32x2 a, b;
+      dswiglu_f32x2(f32x2{d[i], d[i + 1]}, f32x2{g[i], g[i + 1]}, f32x2{u[i], u[i + 1]}, a, b);
+      dg[i] = a.x;
+      dg[i + 1] = a.y;
+      du[i] = b.x;
+      du[i + 1] = b.y;
+    }
     o[0] = make_uint4(pack_bf16x2(dg[0], dg[1]), pack_bf16x2(dg[2], dg[3]), pack_bf16x2(dg[4], dg[5]),
                       pack_bf16x2(dg[6], dg[7]));
     o[1] = make_uint4(pack_bf16x2(du[0], du[1]), pack_bf16x2(du[2], du[3]), pack_bf16x2(du[4], du[5]),
