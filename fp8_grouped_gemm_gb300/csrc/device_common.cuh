@@ -56,6 +56,8 @@ __device__ __forceinline__ void dswiglu_f32(float d, float g, float u, float& dg
 struct f32x2 {
   float x, y;
 };
+// a pair rounded to bf16 and packed (.x in the low half)
+__device__ __forceinline__ uint32_t pack_bf16x2x2(f32x2 v) { return pack_bf16x2(v.x, v.y); }
 __device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
   f32x2 r;
   asm("{\n\t.reg .b64 p, q, d;\n\tmov.b64 p, {%2, %3};\n\tmov.b64 q, {%4, %5};\n\t"
@@ -87,6 +89,11 @@ __device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
       : "=f"(r.x), "=f"(r.y)
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
   return r;
+}
+// swiglu_f32 of two elements: the same operations in the same order, paired
+__device__ __forceinline__ f32x2 swiglu_f32x2(f32x2 g, f32x2 u) {
+  const f32x2 den = add2(f32x2{1.0f, 1.0f}, f32x2{__expf(-g.x), __expf(-g.y)});
+  return mul2(f32x2{__fdividef(g.x, den.x), __fdividef(g.y, den.y)}, u);
 }
 // dswiglu_f32 of two elements: the same operations in the same order, paired
 __device__ __forceinline__ void dswiglu_f32x2(f32x2 d, f32x2 g, f32x2 u, f32x2& dg, f32x2& du) {

@@ -116,10 +116,11 @@ struct SrcSwiglu {
     float g[8], u[8];
     unpack8_bf16(w[0], g);
     unpack8_bf16(w[1], u);
-    out[0] = make_uint4(pack_bf16x2(swiglu_f32(g[0], u[0]), swiglu_f32(g[1], u[1])),
-                        pack_bf16x2(swiglu_f32(g[2], u[2]), swiglu_f32(g[3], u[3])),
-                        pack_bf16x2(swiglu_f32(g[4], u[4]), swiglu_f32(g[5], u[5])),
-                        pack_bf16x2(swiglu_f32(g[6], u[6]), swiglu_f32(g[7], u[7])));
+    uint32_t hw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      hw[i] = pack_bf16x2x2(swiglu_f32x2(f32x2{g[2 * i], g[2 * i + 1]}, f32x2{u[2 * i], u[2 * i + 1]}));
+    out[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
     if (h_out && valid) *reinterpret_cast<uint4*>(h_out + r * F + c) = out[0];
   }
 };
