@@ -59,15 +59,28 @@ constexpr uint64_t kWaitNs = 2000000000ull;     // default wait limit, 2 s: far 
 constexpr int kMaxE = 1024;
 
 constexpr uint32_t kABytes = BM * BK, kBBytes = BN * BK;
-// per stage: A + B tiles and the scale chunks (MX 512 + 1024 bytes, NVFP4 2048 + 4096)
+// B scale bytes per stage: MX the two 512-byte chunks of the 256 B rows;
+// NVFP4 room for the stage's slice of a scale image (its 8 chunks, two row
+// blocks x the stage's 4 MMAs, each four times over: mgq_nv_scale_image),
+// of which the compact chunks use the first 4 KB; none for the other kinds
+__host__ __device__ constexpr uint32_t sfb_bytes(int kind) {
+  return kind == 3 ? 2 * 4 * 4 * 512u : kind == 0 ? 2 * 512u : 0u;
+}
+// per stage: A + B tiles and the scale chunks (MX 512 + 1024 bytes, NVFP4 2048 + 16384)
 __host__ __device__ constexpr uint32_t sf_stage_bytes(int kind) {
-  return kind == 0 ? 3 * 512u : kind == 3 ? 3 * 2048u : 0u;
+  return kind == 0 || kind == 3 ? sfa_bytes(kind) + sfb_bytes(kind) : 0u;
 }
 // epilogue staging for TMA stores: per warp 32 rows x 64 bytes, in two slots
-// for NVFP4 (whose short contractions leave little mainloop to hide each
-// store's read-out behind; the other kinds have no shared memory to spare)
+// for NVFP4 read with compact B scales (whose short contractions leave little
+// mainloop to hide each store's read-out behind); one slot otherwise (NVFP4
+// with a B scale image gives the room to the image's 16 KB a stage; the other
+// kinds have no shared memory to spare)
 constexpr uint32_t kStageOut = 32 * 64;
-__host__ __device__ constexpr uint32_t staging_slots(int kind) { return kind == 3 ? 2u : 1u; }
+__host__ __device__ constexpr uint32_t staging_slots(int kind, bool img = true) {
+  return kind == 3 && !img ? 2u : 1u;
+}
+// NVFP4 B scale bytes a stage actually used: the image slice or the compact chunks
+__host__ __device__ constexpr uint32_t nv_sfb_stage(bool img) { return img ? 8 * 4 * 512u : 8 * 512u; }
 // float32 block scales (kind 2) in contract mode (wgrad): the accumulator
 // lives in the epilogue's registers, so the MMA can run only two stages ahead
 // while a tile's 128 KB of float32 output is stored; each warp stages half its
@@ -96,7 +109,19 @@ __host__ __device__ constexpr size_t smem_bytes(int kind, int mode) {
   return 1024 /*align slack*/ + stages_of(kind, mode) * (size_t)(kABytes + kBBytes + sf_stage_bytes(kind)) +
          staging_bytes(kind, mode) + blk_ring_bytes(kind) + 256 /*barriers*/ + (kMaxE + 8) * 4;
 }
+// NVFP4 with compact B scales: 4 KB of B scales a stage and two staging slots
+__host__ __device__ constexpr size_t smem_bytes_nv_compact(int mode) {
+  return 1024 + stages_of(3, mode) * (size_t)(kABytes + kBBytes + sfa_bytes(3) + nv_sfb_stage(false)) +
+         8 * kStageOut * staging_slots(3, false) + 256 + (kMaxE + 8) * 4;
+}
 static_assert(smem_bytes(2, 0) <= 232448 && smem_bytes(2, 1) <= 232448, "blockwise kernel exceeds the shared memory");
+static_assert(smem_bytes(3, 0) <= 232448 && smem_bytes(3, 1) <= 232448, "NVFP4 kernel exceeds the shared memory");
+static_assert(smem_bytes_nv_compact(0) <= smem_bytes(3, 0) && smem_bytes_nv_compact(1) <= smem_bytes(3, 1),
+              "the compact NVFP4 layout fits the launch's shared-memory limit");
+static_assert((3 * nv_sfb_stage(false)) % 1024 == 0, "the compact B scale stages keep the tiles aligned");
+static_assert(smem_bytes(0, 0) <= 232448 && smem_bytes(0, 1) <= 232448, "MX kernel exceeds the shared memory");
+static_assert((STAGES * sfb_bytes(0)) % 1024 == 0 && (3 * sfb_bytes(3)) % 1024 == 0,
+              "the B scale stages keep the operand tiles 1024-byte aligned");
 static_assert(kBlkSlots >= STAGES + 2, "the scale ring must cover the operand ring and both partial buffers");
 
 enum { kModeRows = 0, kModeContract = 1 };
@@ -118,6 +143,7 @@ struct GemmParams {
   int64_t sfa_kb4;    // 512-byte scale chunks per 128-row tile of A
   const uint8_t* sfb;
   int64_t sfb_kb4;
+  const uint8_t* sfb_img;  // NVFP4: B's scale image (mgq_nv_scale_image), or null
   const float* sa;    // tensor: s_a; block: scale_inv_a [K/128][sa_ld]; NVFP4: s_g of A
   const float* sb;    // tensor: s_b per expert; block rows mode: scale_inv_b [E][N/128][K/128], block
                       // contract mode: scale_inv_b [R_cap/128][sb_ld] (one per column and 128 rows);
@@ -776,7 +802,7 @@ __device__ __forceinline__ void epilogue_dswiglu_mx(const GemmParams& p, uint32_
 
 // DSW: the down-projection dgrad with the dSwiGLU epilogue (a separate
 // instantiation, so the other epilogues keep their registers)
-template <int MODE, int KIND, bool DSW = false>
+template <int MODE, int KIND, bool DSW = false, bool IMG = false>
 __global__ void __launch_bounds__(threads_of(KIND), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmH,
@@ -785,15 +811,24 @@ __global__ void __launch_bounds__(threads_of(KIND), 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  uint8_t* sA = smem;
-  uint8_t* sB = sA + STG * kABytes;
-  constexpr uint32_t kSfaBytes = sfa_bytes(KIND), kSfbBytes = 2 * sfa_bytes(KIND);
+  constexpr uint32_t kSfaBytes = sfa_bytes(KIND), kSfbBytes = sfb_bytes(KIND);
   constexpr uint32_t kSfbCol = sfb_col0(KIND);
+  // [B scale stages][A stages][B stages][A scale stages][staging]...: the B
+  // scale stages (multiples of 1024 bytes) come first, so the operand tiles
+  // stay 1024-byte aligned
+  // NVFP4: B scales a stage and staging slots follow the kind of B scales
+  // (IMG: B's scale image, p.sfb_img; else the compact chunks)
+  constexpr bool img = KIND == kKindNV && IMG;
+  constexpr uint32_t sfb_stage = KIND == kKindNV ? nv_sfb_stage(img) : kSfbBytes;
+  constexpr uint32_t nslots = staging_slots(KIND, img);
+  constexpr uint32_t stage_out_bytes = wide_staging(KIND, MODE) ? staging_bytes(KIND, MODE) : 8 * kStageOut * nslots;
+  uint8_t* sSFB = smem;
+  uint8_t* sA = sSFB + STG * sfb_stage;
+  uint8_t* sB = sA + STG * kABytes;
   uint8_t* sSFA = sB + STG * kBBytes;
-  uint8_t* sSFB = sSFA + STG * kSfaBytes;
-  uint8_t* sOut = sSFA + STG * sf_stage_bytes(KIND);       // epilogue staging (TMA stores)
-  float* sRing = reinterpret_cast<float*>(sOut + staging_bytes(KIND, MODE));   // block scales
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + staging_bytes(KIND, MODE) + blk_ring_bytes(KIND));
+  uint8_t* sOut = sSFA + STG * (sf_stage_bytes(KIND) - kSfbBytes);   // epilogue staging (TMA stores)
+  float* sRing = reinterpret_cast<float*>(sOut + stage_out_bytes);   // block scales
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + stage_out_bytes + blk_ring_bytes(KIND));
   uint64_t* full = bars;
   uint64_t* empty = bars + STG;
   uint64_t* tmem_full = bars + 2 * STG;        // [2]
@@ -898,7 +933,8 @@ __global__ void __launch_bounds__(threads_of(KIND), 1)
           ptx::bulk_load(dst, p.sa + kb * p.sa_ld + tl.row_a, 128 * 4, &s_full[sl]);
           if (MODE == kModeContract) ptx::bulk_load(dst + 128, p.sb + kb * p.sb_ld + tl.out_col, BN * 4, &s_full[sl]);
         }
-        const uint32_t bytes = kABytes + kBBytes + (MX ? kSfaBytes + kSfbBytes : 0);
+        // (NVFP4 B scales: the image slice, 16 KB, or the compact chunks, 4 KB)
+        const uint32_t bytes = kABytes + kBBytes + (MX ? kSfaBytes + sfb_stage : 0);
         ptx::mbar_arrive_expect_tx(&full[st], bytes);
         const int32_t kx = (int32_t)(tl.kx0 + (int64_t)s * BK);
         ptx::tma_load_2d(sA + st * kABytes, &tmA, &full[st], kx, (int32_t)tl.row_a);
@@ -913,8 +949,16 @@ __global__ void __launch_bounds__(threads_of(KIND), 1)
           const uint8_t* fb = p.sfb + ((tl.row_b / BM) * p.sfb_kb4 + kt) * 512;
           const uint8_t* fb2 = p.sfb + (((tl.row_b + p.b_half2) / BM) * p.sfb_kb4 + kt) * 512;
           ptx::bulk_load(sSFA + st * kSfaBytes, fa, kSfaBytes, &full[st]);
-          ptx::bulk_load(sSFB + st * kSfbBytes, fb, kSfaBytes, &full[st]);
-          ptx::bulk_load(sSFB + st * kSfbBytes + kSfaBytes, fb2, kSfaBytes, &full[st]);
+          if (img) {
+            // the stage's 8 KB slice of the image for each B row block
+            const int64_t ks = kt / 4, nks = p.sfb_kb4 / 4;
+            ptx::bulk_load(sSFB + st * sfb_stage, p.sfb_img + ((tl.row_b / BM) * nks + ks) * 8192, 8192, &full[st]);
+            ptx::bulk_load(sSFB + st * sfb_stage + 8192,
+                           p.sfb_img + (((tl.row_b + p.b_half2) / BM) * nks + ks) * 8192, 8192, &full[st]);
+          } else {
+            ptx::bulk_load(sSFB + st * sfb_stage, fb, kSfaBytes, &full[st]);
+            ptx::bulk_load(sSFB + st * sfb_stage + kSfaBytes, fb2, kSfaBytes, &full[st]);
+          }
         }
       }
       if (*s_abort) break;
@@ -965,8 +1009,16 @@ __global__ void __launch_bounds__(threads_of(KIND), 1)
 #pragma unroll
           for (uint32_t ch = 0; ch < kSfaBytes / 512; ++ch) {
             ptx::tmem_cp_32x128b_x4(sfa_t + ch * 4, ptx::sdesc_sf(sSFA0 + st * kSfaBytes + ch * 512));
-            ptx::tmem_cp_32x128b_x4(sfb_t + ch * 8, ptx::sdesc_sf(sSFB0 + st * kSfbBytes + ch * 512));
-            ptx::tmem_cp_32x128b_x4(sfb_t + ch * 8 + 4, ptx::sdesc_sf(sSFB0 + st * kSfbBytes + kSfaBytes + ch * 512));
+            if (img) {
+              // both B row blocks of MMA ch in one copy: 128 rows of 2 x 16
+              // bytes, the second 16 bytes 8192 bytes on (the other row block)
+              ptx::tmem_cp_128x256b(sfb_t + ch * 8, ptx::sdesc(sSFB0 + st * sfb_stage + ch * 2048, 8192, 128,
+                                                                ptx::kSwizzleNone));
+            } else {
+              ptx::tmem_cp_32x128b_x4(sfb_t + ch * 8, ptx::sdesc_sf(sSFB0 + st * sfb_stage + ch * 512));
+              ptx::tmem_cp_32x128b_x4(sfb_t + ch * 8 + 4,
+                                      ptx::sdesc_sf(sSFB0 + st * sfb_stage + kSfaBytes + ch * 512));
+            }
           }
         }
         const uint64_t ad = ptx::sdesc_kmajor_sw128(sA0 + st * kABytes);
@@ -1006,7 +1058,7 @@ __global__ void __launch_bounds__(threads_of(KIND), 1)
     const uint32_t q = warp & 3;
     const uint32_t half = (uint32_t)(warp - EW0) >> 2;
     const int64_t row_in_tile = q * 32 + lane;
-    Stager sg{sOut + (warp - EW0) * kStageOut * staging_slots(KIND), staging_slots(KIND), 0u};
+    Stager sg{sOut + (warp - EW0) * kStageOut * nslots, nslots, 0u};
     uint32_t h_tam = 0;    // per-tensor SwiGLU: this thread's max |h| (float bits)
     int ecur = 0;
     uint32_t tc = 0;
@@ -1166,11 +1218,12 @@ __global__ void __launch_bounds__(threads_of(KIND), 1)
   }
 }
 
-template <int MODE, int KIND, bool DSW = false>
-int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const CUtensorMap& th,
+template <int MODE, int KIND, bool DSW = false, bool IMG = false>
+int launch_gemm_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const CUtensorMap& th,
                 const GemmParams& p, cudaStream_t s) {
-  auto kern = grouped_gemm_kernel<MODE, KIND, DSW>;
-  constexpr size_t kSmemBytes = smem_bytes(KIND, MODE);
+  auto kern = grouped_gemm_kernel<MODE, KIND, DSW, IMG>;
+  // (NVFP4 with compact B scales: the smaller layout)
+  constexpr size_t kSmemBytes = KIND == kKindNV && !IMG ? smem_bytes_nv_compact(MODE) : smem_bytes(KIND, MODE);
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1188,6 +1241,16 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
   kern<<<num_sms(), threads_of(KIND), kSmemBytes, s>>>(ta, tb, to, th, p);
   MGQ_LAUNCH_CHECK();
   return MGQ_OK;
+}
+
+// NVFP4 calls with a B scale image run the IMG instantiation
+template <int MODE, int KIND, bool DSW = false>
+int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const CUtensorMap& th,
+                const GemmParams& p, cudaStream_t s) {
+  if constexpr (KIND == kKindNV && !DSW) {
+    if (p.sfb_img) return launch_gemm_t<MODE, KIND, DSW, true>(ta, tb, to, th, p, s);
+  }
+  return launch_gemm_t<MODE, KIND, DSW, false>(ta, tb, to, th, p, s);
 }
 
 
@@ -1716,6 +1779,8 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
   p.R_cap = R_cap;
   p.sfa = static_cast<const uint8_t*>(A->scale);
   p.sfb = static_cast<const uint8_t*>(B->scale);
+  p.sfb_img = nv ? static_cast<const uint8_t*>(B->scale_image) : nullptr;
+  if (p.sfb_img) MGQ_CHECK_ARG(aligned16(p.sfb_img));
   p.sa = nv ? A->global_scale : static_cast<const float*>(A->scale);
   p.sb = nv ? B->global_scale : static_cast<const float*>(B->scale);
   // block scales: A's scale_inv [k block][rows of A]; contract mode B's
@@ -1929,6 +1994,23 @@ int run_grouped(int mode, const mgq_operand* A, const mgq_operand* B, int scalin
 
 using namespace mgq;
 
+namespace mgq {
+namespace {
+// The scale image of an NVFP4 operand: its 512-byte chunks in order, each
+// written four times (chunk c at image chunks 4c .. 4c + 3). One thread per
+// 16 bytes of the source; a warp moves one chunk.
+__global__ void __launch_bounds__(256) nv_scale_image_kernel(const uint4* __restrict__ src, int64_t units,
+                                                             uint4* __restrict__ dst) {
+  const int64_t t = (int64_t)blockIdx.x * 256 + threadIdx.x;
+  if (t >= units) return;
+  const uint4 v = __ldg(src + t);
+  uint4* d = dst + (t >> 5) * 128 + (t & 31);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) d[32 * q] = v;
+}
+}  // namespace
+}  // namespace mgq
+
 extern "C" {
 
 int mgq_grouped_gemm_fwd(const mgq_operand* A, const mgq_operand* W, int scaling, const int32_t* offsets, int E,
@@ -1980,6 +2062,18 @@ int mgq_set_gemm_option(int option, int64_t value) {
 int mgq_get_gemm_option(int option, int64_t* value) {
   if (option < 0 || option >= MGQ_GEMM_OPT_COUNT || !value) return MGQ_ERR_INVALID_ARG;
   *value = g_gemm_opt[option].load(std::memory_order_relaxed);
+  return MGQ_OK;
+}
+
+int mgq_nv_scale_image(const void* scale, int64_t rows, int64_t ld, void* image, void* stream) {
+  using namespace mgq;
+  MGQ_CHECK_ARG(scale && image && aligned16(scale) && aligned16(image));
+  MGQ_CHECK_ARG(rows > 0 && rows % 128 == 0 && ld > 0 && ld % 256 == 0);
+  const int64_t units = rows / 128 * (ld / 64) * 32;   // 16-byte units of the scales
+  MGQ_CHECK_ARG((units + 255) / 256 < (1ll << 31));
+  nv_scale_image_kernel<<<(unsigned)((units + 255) / 256), 256, 0, as_stream(stream)>>>(
+      static_cast<const uint4*>(scale), units, static_cast<uint4*>(image));
+  MGQ_LAUNCH_CHECK();
   return MGQ_OK;
 }
 

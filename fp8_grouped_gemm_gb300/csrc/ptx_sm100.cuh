@@ -151,6 +151,12 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 }
 // copy 32 rows x 128 bits from shared memory to tensor memory, replicated to
 // the four 32-lane quadrants
+// 128 rows x 256 bits (no multicast): tensor-memory lane r, 8 columns, from
+// source row r (core matrices of 8 rows x 16 bytes: stride byte offset between
+// row groups, leading byte offset between the two 16-byte halves)
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
 __device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }

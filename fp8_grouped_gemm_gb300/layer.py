@@ -38,12 +38,18 @@ from .workloads import Workload
 
 ALIGN = 128       # group padding: the grouped GEMM tiles rows by 128
 ALIGN_NV_TRAIN = 256   # NVFP4 wgrad: a 128-byte stage holds 256 rows of a group
+# NVFP4 GEMMs read the scale image of their second operand
+# (mgq_nv_scale_image) when the contraction is at least this long: measured on
+# the Mixtral shapes (contractions of 4096 and more) every GEMM gained 4-9%,
+# more than the image costs; the fine-grained forward's short contractions
+# (768, 2048) gained less than the images cost
+NV_IMAGE_MIN_K = 4096
 
 
 class ExpertLayer:
     def __init__(self, w: Workload, device, recipe: str | None = None, keep_bf16: bool = False,
                  history: int = 1024, train: bool | None = None, col_copies: bool = False,
-                 fuse_swiglu: bool = True):
+                 fuse_swiglu: bool = True, nv_image_min_k: int = NV_IMAGE_MIN_K):
         self.w = w
         self.dev = torch.device(device)
         self.recipe = recipe or w.recipe
@@ -54,6 +60,7 @@ class ExpertLayer:
         # per-tensor backward GEMMs read the row-wise codes MN-major
         self.mn = self.delayed and not col_copies
         self.keep_bf16 = keep_bf16
+        self.nv_image_min_k = nv_image_min_k
         # SwiGLU in the gate/up GEMM epilogue: MX (training: the epilogue also
         # writes the column-wise copy of h), NVFP4 (the epilogue writes h and
         # its amax; a second pass casts both copies) or per-tensor without a
@@ -182,8 +189,15 @@ class ExpertLayer:
         # amax and s_g: [x, h, w1 x E, w2 x E, dy2, dy1]
         self.nv_amax = torch.zeros(4 + 2 * E, dtype=torch.float32, device=d)
         self.nv_sg = torch.ones(4 + 2 * E, dtype=torch.float32, device=d)
+        # scale images of the GEMMs' second operands (mgq_nv_scale_image), for
+        # the GEMMs whose contraction (ld, the operand's row pitch) is long enough
+        img = lambda rows, ld: (torch.empty(mgq.nv_scale_image_bytes(rows, ld), **u8)
+                                if ld >= self.nv_image_min_k else None)
+        self.w1img, self.w2img = img(E * 2 * F, H), img(E * H, F)
         if not self.train:
             return
+        self.w1cimg, self.w2cimg = img(E * H, 2 * F), img(E * F, H)
+        self.xcimg, self.hcimg = img(H, R), img(F, R)
         ns = mgq.nv_scale_bytes
         # column-wise copies (16x1 blocks along the tokens; weights: the same
         # 16x16 block scales as their row-wise copies), e2m1 packed along them
@@ -249,7 +263,20 @@ class ExpertLayer:
             q1 = mgq.qdesc(mgq.E4M3, self.scaling, self.w1q, None, self.w1col, None, self._fs(2, E), self._fa(2, E))
             q2 = mgq.qdesc(mgq.E4M3, self.scaling, self.w2q, None, self.w2col, None, self._fs(2 + E, E),
                            self._fa(2 + E, E))
-        return [("weight_quant", lambda: Q(w1, q1, stream)), ("weight_quant", lambda: Q(w2, q2, stream))]
+        ops = [("weight_quant", lambda: Q(w1, q1, stream)), ("weight_quant", lambda: Q(w2, q2, stream))]
+        if self.nv:
+            H, F = self.w.H, self.w.F
+            ops += self._image_ops([(self.w1s, E * 2 * F, H, self.w1img), (self.w2s, E * H, F, self.w2img)], stream)
+            if self.train:
+                ops += self._image_ops([(self.w1cs, E * H, 2 * F, self.w1cimg), (self.w2cs, E * F, H, self.w2cimg)],
+                                       stream)
+        return ops
+
+    @staticmethod
+    def _image_ops(items, stream):
+        """One scale-image op per (scales, rows, ld, image) with an image."""
+        return [("scale_image", (lambda s=s, r=r, ld=ld, im=im: mgq.nv_scale_image(s, r, ld, im, stream)))
+                for s, r, ld, im in items if im is not None]
 
     def fwd_ops(self, x, topk_idx, probs, stream=None):
         E, H, F, R = self.w.E, self.w.H, self.w.F, self.R_cap
@@ -262,9 +289,9 @@ class ExpertLayer:
             qx = mgq.qdesc(dt, sc, self.xq, self.xs, *cx, tensor_scale=g[0:1], amax_out=a[0:1])
             qh = mgq.qdesc(dt, sc, self.hq, self.hs, *ch, tensor_scale=g[1:2], amax_out=a[1:2])
             A1, B1 = (mgq.operand(self.xq, self.xs, H, dt, g[0:1]),
-                      mgq.operand(self.w1q, self.w1s, H, dt, g[2:2 + E]))
+                      mgq.operand(self.w1q, self.w1s, H, dt, g[2:2 + E], scale_image=self.w1img))
             A2, B2 = (mgq.operand(self.hq, self.hs, F, dt, g[1:2]),
-                      mgq.operand(self.w2q, self.w2s, F, dt, g[2 + E:2 + 2 * E]))
+                      mgq.operand(self.w2q, self.w2s, F, dt, g[2 + E:2 + 2 * E], scale_image=self.w2img))
         else:
             dt = mgq.E4M3
             if sc in (mgq.MX32_E8M0, mgq.BLK_1x128_F32):       # block scales beside the codes
@@ -297,6 +324,10 @@ class ExpertLayer:
                                                                  mgq.OUT_BF16, stream)),
                 ("swiglu_quant", lambda: mgq.swiglu_quantize(self.gu, R, F, self.offsets, E, qh, self.h_bf16,
                                                              stream))]
+        if self.nv and self.train:
+            # scale images of the column-wise copies of x and h (the wgrads' second operands)
+            permute += self._image_ops([(self.xcs, H, R, self.xcimg)], stream)
+            gateup += self._image_ops([(self.hcs, F, R, self.hcimg)], stream)
         return permute + gateup + [
             ("gemm_fwd_down", lambda: mgq.grouped_gemm_fwd(A2, B2, sc, self.offsets, E, R, H, F, self.y,
                                                            mgq.OUT_BF16, stream)),
@@ -380,11 +411,15 @@ class ExpertLayer:
                        amax_out=a[i1:i1 + 1])
         gw1, gw2 = g[2:2 + E], g[2 + E:2 + 2 * E]
         # down projection: dh = dY2 W2 ; dW2 = dY2^T h
-        d2 = (O(self.dy2q, self.dy2s, H, dt, g[i2:i2 + 1]), O(self.w2col, self.w2cs, H, dt, gw2))
-        w2 = (O(self.dy2col, self.dy2cs, R, dt, g[i2:i2 + 1]), O(self.hcol, self.hcs, R, dt, g[1:2]))
+        d2 = (O(self.dy2q, self.dy2s, H, dt, g[i2:i2 + 1]),
+              O(self.w2col, self.w2cs, H, dt, gw2, scale_image=self.w2cimg))
+        w2 = (O(self.dy2col, self.dy2cs, R, dt, g[i2:i2 + 1]),
+              O(self.hcol, self.hcs, R, dt, g[1:2], scale_image=self.hcimg))
         # gate/up projection: dXp = dY1 W1 ; dW1 = dY1^T X
-        d1 = (O(self.dy1q, self.dy1s, 2 * F, dt, g[i1:i1 + 1]), O(self.w1col, self.w1cs, 2 * F, dt, gw1))
-        w1 = (O(self.dy1col, self.dy1cs, R, dt, g[i1:i1 + 1]), O(self.xcol, self.xcs, R, dt, g[0:1]))
+        d1 = (O(self.dy1q, self.dy1s, 2 * F, dt, g[i1:i1 + 1]),
+              O(self.w1col, self.w1cs, 2 * F, dt, gw1, scale_image=self.w1cimg))
+        w1 = (O(self.dy1col, self.dy1cs, R, dt, g[i1:i1 + 1]),
+              O(self.xcol, self.xcs, R, dt, g[0:1], scale_image=self.xcimg))
         return [
             ("unpermute_bwd_quant", lambda: mgq.moe_unpermute_bwd(dout, self.y, self.row_id_map, self.src_row, probs,
                                                                   R, self.offsets, E, q2, self.dprobs, stream)),
@@ -436,6 +471,10 @@ class ExpertLayer:
         mgq.amax_history_update(self.bwd_hist, self.heads[1:2], self.bwd_amax, self.bwd_scale,
                                 mgq.FMAX[mgq.E5M2], stream)
 
+    def _n_images(self) -> int:
+        names = ("w1img", "w2img", "w1cimg", "w2cimg", "xcimg", "hcimg")
+        return sum(getattr(self, n, None) is not None for n in names)
+
     def gpu_launches_per_step(self) -> int:
         """Kernels this object launches per forward (+ backward) step."""
         E = self.w.E
@@ -448,15 +487,16 @@ class ExpertLayer:
             # second pass writes both copies of h; weights: 2 x (amax + 16x16
             # pass); backward: dY amax + token rows + column gather, dgrad,
             # wgrad, dSwiGLU (dGU + amax, then rows and columns), dgrad, wgrad,
-            # permute_bwd
-            return fwd + 2 + 4 + (3 + 1 + 1 + 2 + 1 + 1 + 1)
+            # permute_bwd; the scale images (both weights, both weight column
+            # copies, the column copies of x and h) where they are used
+            return fwd + 2 + 4 + (3 + 1 + 1 + 2 + 1 + 1 + 1) + self._n_images()
         if self.nv:
             # + amax passes (x, h); weights: 2 x (amax + rows); the permute's
             # row-major scales re-tiled in a second pass when a 128-row group's
             # scales fit a CTA's shared memory
             H = self.w.H
             retile = 1 if H % 256 == 0 and 128 * (H // 64 + 1) * 4 <= 200 * 1024 else 0
-            return fwd + 2 + 4 + retile
+            return fwd + 2 + 4 + retile + self._n_images()   # + the weights' scale images
         if not self.train:
             return fwd + 2                              # weight quantisation (row)
         wq = 2                                          # weights: rows (+ columns) in one pass each

@@ -36,7 +36,7 @@ EXPORTS = (
     "mgq_grouped_gemm_wgrad", "mgq_grouped_gemm_fwd_swiglu",
     "mgq_grouped_gemm_dgrad_dswiglu", "mgq_swiglu_quantize", "mgq_dswiglu_quantize", "mgq_moe_unpermute",
     "mgq_moe_unpermute_bwd", "mgq_moe_permute_bwd", "mgq_amax_history_update", "mgq_set_gemm_option",
-    "mgq_get_gemm_option",
+    "mgq_get_gemm_option", "mgq_nv_scale_image",
 )
 
 
@@ -58,7 +58,8 @@ class QDesc(ctypes.Structure):
 
 class Operand(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("ld", ctypes.c_int64),
-                ("dtype", ctypes.c_int), ("global_scale", ctypes.c_void_p), ("layout", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("global_scale", ctypes.c_void_p), ("layout", ctypes.c_int),
+                ("scale_image", ctypes.c_void_p)]
 
 
 _lib = None
@@ -90,6 +91,7 @@ def load() -> ctypes.CDLL:
         lib.mgq_grouped_gemm_fwd.argtypes = gemm + [vp, i32, vp]
         lib.mgq_grouped_gemm_dgrad.argtypes = gemm + [vp, i32, vp]
         lib.mgq_grouped_gemm_wgrad.argtypes = gemm + [ctypes.c_float, vp, i32, vp]
+        lib.mgq_nv_scale_image.argtypes = [vp, i64, i64, vp, vp]
         lib.mgq_grouped_gemm_fwd_swiglu.argtypes = gemm + [P(QDesc), vp, vp, vp]
         lib.mgq_grouped_gemm_dgrad_dswiglu.argtypes = gemm + [vp, P(QDesc), vp, vp, vp]
         lib.mgq_swiglu_quantize.argtypes = [vp, i64, i32, vp, i32, P(QDesc), vp, vp]
@@ -137,8 +139,8 @@ def qdesc(dtype, scaling, row_data, row_scale=None, col_data=None, col_scale=Non
                  QBuf(_p(col_data), _p(col_scale)), _p(tensor_scale), _p(amax_out))
 
 
-def operand(data, scale, ld, dtype, global_scale=None, layout=0) -> Operand:
-    return Operand(_p(data), _p(scale), int(ld), int(dtype), _p(global_scale), int(layout))
+def operand(data, scale, ld, dtype, global_scale=None, layout=0, scale_image=None) -> Operand:
+    return Operand(_p(data), _p(scale), int(ld), int(dtype), _p(global_scale), int(layout), _p(scale_image))
 
 
 # ---- sizes of the caller-owned buffers (host arithmetic only) ----------------
@@ -253,6 +255,15 @@ def grouped_gemm_wgrad(dYcol: Operand, Acol: Operand, scaling, offsets, E, R_cap
     _check(load().mgq_grouped_gemm_wgrad(ctypes.byref(dYcol), ctypes.byref(Acol), scaling, _p(offsets), E,
                                          R_cap, N, K, ctypes.c_float(beta), _p(dW), out_dtype, _s(stream)),
            "mgq_grouped_gemm_wgrad")
+
+
+def nv_scale_image(scale, rows, ld, image, stream=None):
+    """The GEMM scale image of an NVFP4 operand's scales (rows * ld / 4 bytes)."""
+    _check(load().mgq_nv_scale_image(_p(scale), rows, ld, _p(image), _s(stream)), "mgq_nv_scale_image")
+
+
+def nv_scale_image_bytes(rows, ld):
+    return rows * ld // 4
 
 
 def grouped_gemm_fwd_swiglu(A: Operand, W1: Operand, scaling, offsets, E, R_cap, F, K, qh: QDesc, gu=None, h=None,

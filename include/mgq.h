@@ -142,6 +142,9 @@ typedef struct {
   int dtype;                 /* mgq_dtype                                       */
   const float* global_scale; /* NVFP4: device s_g per tensor (A) / per expert (W); else NULL */
   int layout;                /* mgq_layout; 0 (MGQ_LAYOUT_K) unless stated      */
+  const void* scale_image;   /* NVFP4 second operand (W, Wcol, Acol) only: the
+                                image of `scale` from mgq_nv_scale_image, or
+                                NULL (the GEMM then reads `scale` alone)       */
 } mgq_operand;
 
 /* ---- status --------------------------------------------------------------- */
@@ -306,7 +309,10 @@ int mgq_grouped_quantize(const void* x_bf16, int64_t R_cap, int64_t C, const int
  *        the product is multiplied by 1/(s_g,a s_g,b). NVFP4 wgrad contracts
  *        in 256-row stages: offsets[e] multiples of 256 (otherwise
  *        MGQ_ERR_INVALID_ARG in the device error word, nothing written) and
- *        R_cap a multiple of 256.
+ *        R_cap a multiple of 256. The second operand may carry scale_image
+ *        (built by mgq_nv_scale_image from its scales, 16-byte aligned): the
+ *        same values, one tensor-memory copy per MMA instead of two; the
+ *        results are identical. scale_image is ignored for other scalings.
  * Operand layout (MGQ_TENSOR_F32 only): with per-tensor scales the
  *        column-wise copy holds the same codes as the row-wise one,
  *        transposed, so dgrad accepts the forward weight W [E, N, K] (ld >= K)
@@ -326,6 +332,21 @@ int mgq_grouped_gemm_dgrad(const mgq_operand* dY, const mgq_operand* Wcol, int s
 int mgq_grouped_gemm_wgrad(const mgq_operand* dYcol, const mgq_operand* Acol, int scaling,
                            const int32_t* offsets, int E, int64_t R_cap, int64_t N,
                            int64_t K, float beta, void* dW, int out_dtype, void* stream);
+
+/* Scale image of an NVFP4 GEMM operand for the grouped GEMMs above ([GROUPED]:
+ * NVFP4 e2m1 elements with ue4m3 scales per 16 along the contraction). The
+ * same scale bytes, rearranged: for each 128-row block rb and each 256-element
+ * stage s of the contraction, its four 512-byte chunks c = 4 s + i (the 128x4
+ * tiled layout: 128 rows x 4 blocks of 16), each written four times,
+ *   image[(((rb * (ld / 256) + s) * 4 + i) * 4 + q) * 512 + b]
+ *       = scale[(rb * (ld / 64) + 4 s + i) * 512 + b],   q = 0..3,
+ * one copy per tensor-memory lane quadrant.
+ * scale: device, the operand's scales (rows x ld / 16 bytes); rows: the
+ * operand's rows (a multiple of 128); ld: its row pitch in elements (a
+ * multiple of 256); image: device, caller-owned, rows * ld / 4 bytes, 16-byte
+ * aligned. Enqueued on `stream`; MGQ_ERR_INVALID_ARG for bad sizes or
+ * pointers. */
+int mgq_nv_scale_image(const void* scale, int64_t rows, int64_t ld, void* image, void* stream);
 
 /* Process-wide options of the grouped GEMMs (every entry point above and
  * below). They change which kernel runs or how it stores, never the values it

@@ -110,7 +110,7 @@ def _gpu_row_scales(lay, buf, rows_cap, ld, recipe):
     return buf.detach().cpu().numpy().T          # [K/128][R_cap] -> [R_cap, K/128]
 
 
-def run_fwd_and_check(w, device, recipe: str = "mxfp8") -> dict:
+def run_fwd_and_check(w, device, recipe: str = "mxfp8", **layer_kw) -> dict:
     """One forward of workload ``w`` through ExpertLayer (MXFP8 or blockwise
     FP8), every step compared with the oracle. Returns the measured errors."""
     from fp8_grouped_gemm_gb300 import layer as L
@@ -120,7 +120,7 @@ def run_fwd_and_check(w, device, recipe: str = "mxfp8") -> dict:
     x = W.make_activations(w)
     w1, w2 = W.make_weights(w)
     idx, probs = W.make_routing(w)
-    lay = L.ExpertLayer(w, device, recipe=recipe, keep_bf16=True)
+    lay = L.ExpertLayer(w, device, recipe=recipe, keep_bf16=True, **layer_kw)
     xd, w1d, w2d = x.to(device), w1.to(device), w2.to(device)
     idxd = torch.from_numpy(idx).to(device)
     pd = torch.from_numpy(probs).to(device)

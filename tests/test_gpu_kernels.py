@@ -588,6 +588,70 @@ def test_gemm_wgrad_nvfp4(mgq):
     assert rel_fro(ref + prev.cpu().numpy(), got2) <= GEMM_TOL_F32
 
 
+def test_nv_scale_image_gemms_identical(mgq):
+    """The scale image of an NVFP4 operand holds each 512-byte scale chunk four
+    times in order; the grouped GEMMs fed the image (fwd and dgrad in rows mode,
+    wgrad in contract mode) give the same bits as those fed the scales alone."""
+    rng = np.random.default_rng(75)
+    dev = torch.device(DEV)
+    offs = np.array([0, 256, 256, 768], dtype=np.int32)
+    E, N, K = 3, 512, 768
+    Rp = int(offs[-1])
+    R_cap = Rp + 256
+    offd = torch.from_numpy(offs).to(dev)
+
+    def nv_op(rows, cols, g):
+        c, s = _nv_operand(rng, rows, cols)
+        st = tile_mx_scales(s)
+        op = _op(mgq, c, st, cols, mgq.E2M1, dev)
+        op.global_scale = g.data_ptr()
+        img = torch.full((mgq.nv_scale_image_bytes(rows, cols),), 0xEE, dtype=torch.uint8, device=dev)
+        mgq.nv_scale_image(op.scale, rows, cols, img)
+        torch.cuda.synchronize()
+        assert mgq.get_error() == mgq.OK
+        assert np.array_equal(u8_np(img), np.repeat(st.reshape(-1, 512), 4, axis=0).reshape(-1))
+        return op, img
+
+    ga = _to_dev(np.array([2.5], dtype=np.float32), dev)
+    gw = _to_dev(np.exp2(rng.uniform(-3, 3, size=E)).astype(np.float32), dev)
+    # forward: A [R_cap, K], W [E * N, K]
+    A, _ = nv_op(R_cap, K, ga)
+    W, w_img = nv_op(E * N, K, gw)
+    outs = []
+    for img in (None, w_img):
+        W.scale_image = 0 if img is None else img.data_ptr()
+        Y = torch.full((R_cap, N), float("nan"), dtype=torch.bfloat16, device=dev)
+        mgq.grouped_gemm_fwd(A, W, mgq.NV16_UE4M3, offd, E, R_cap, N, K, Y)
+        torch.cuda.synchronize()
+        assert mgq.get_error() == mgq.OK
+        outs.append(bf16_np(Y)[:Rp])
+    assert np.array_equal(outs[0], outs[1])
+    # dgrad: dY [R_cap, N], Wcol [E * K, N]
+    dY, _ = nv_op(R_cap, N, ga)
+    Wc, wc_img = nv_op(E * K, N, gw)
+    outs = []
+    for img in (None, wc_img):
+        Wc.scale_image = 0 if img is None else img.data_ptr()
+        dA = torch.full((R_cap, K), float("nan"), dtype=torch.bfloat16, device=dev)
+        mgq.grouped_gemm_dgrad(dY, Wc, mgq.NV16_UE4M3, offd, E, R_cap, N, K, dA)
+        torch.cuda.synchronize()
+        assert mgq.get_error() == mgq.OK
+        outs.append(bf16_np(dA)[:Rp])
+    assert np.array_equal(outs[0], outs[1])
+    # wgrad: dYcol [N, R_cap], Acol [K, R_cap]
+    dYc, _ = nv_op(N, R_cap, ga)
+    Ac, ac_img = nv_op(K, R_cap, ga)
+    outs = []
+    for img in (None, ac_img):
+        Ac.scale_image = 0 if img is None else img.data_ptr()
+        dW = torch.full((E, N, K), 5.0, dtype=torch.float32, device=dev)
+        mgq.grouped_gemm_wgrad(dYc, Ac, mgq.NV16_UE4M3, offd, E, R_cap, N, K, dW, 0.0)
+        torch.cuda.synchronize()
+        assert mgq.get_error() == mgq.OK
+        outs.append(dW.cpu().numpy())
+    assert np.array_equal(outs[0], outs[1])
+
+
 def test_gemm_wgrad_nvfp4_needs_256_row_groups(mgq):
     """A group boundary inside a 256-row e2m1 stage is reported by the kernel
     (MGQ_ERR_INVALID_ARG through the error word) and nothing is written."""

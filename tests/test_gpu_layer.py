@@ -43,13 +43,16 @@ def test_scout_forward_blockwise_scaled_down():
     assert res["gemm1_sqnr_vs_bf16"] >= 28.0, res
 
 
-def test_finegrained_forward_nvfp4_scaled_down():
+@pytest.mark.parametrize("image_min_k", [None, 0], ids=["scales", "scale_image"])
+def test_finegrained_forward_nvfp4_scaled_down(image_min_k):
     """Fine-grained MoE proportions (uniform top-8 routing) in NVFP4 (e2m1,
     16-element ue4m3 scales, float32 global scales) at a size checked in full;
-    SQNR bar 15 dB against bf16."""
+    SQNR bar 15 dB against bf16. Both with the weights' scales read as they
+    are and through their GEMM scale images."""
     from fp8_grouped_gemm_gb300.workloads import WORKLOADS
     w = WORKLOADS["finegrained_fwd"].scaled(T=1024, E=32, H=512, F=768)
-    res = run_fwd_and_check(w, DEV, recipe="nvfp4")
+    kw = {} if image_min_k is None else {"nv_image_min_k": image_min_k}
+    res = run_fwd_and_check(w, DEV, recipe="nvfp4", **kw)
     assert res["gemm1_sqnr_vs_bf16"] >= 15.0, res
 
 
@@ -244,11 +247,13 @@ def test_mxfp8_training_step_scaled_down():
     assert OG.sqnr_db(OG.grouped_gemm_fwd(xp, w1f, off), gu) >= 28.0
 
 
-def test_nvfp4_training_step_scaled_down():
+@pytest.mark.parametrize("image_min_k", [None, 0], ids=["scales", "scale_image"])
+def test_nvfp4_training_step_scaled_down(image_min_k):
     """NVFP4 in both passes: activations and gradients e2m1 with 16-element
     ue4m3 scales and one s_g per tensor (row-wise for fwd/dgrad, 16x1 blocks
     along each expert's tokens for wgrad), weights with 16x16 blocks (one pass,
-    both copies), groups padded to 256 rows for the NVFP4 wgrad."""
+    both copies), groups padded to 256 rows for the NVFP4 wgrad. Both with the
+    second operands' scales read as they are and through their scale images."""
     from fp8_grouped_gemm_gb300 import layer as L
     from fp8_grouped_gemm_gb300 import mgq
     from fp8_grouped_gemm_gb300 import workloads as W
@@ -259,8 +264,10 @@ def test_nvfp4_training_step_scaled_down():
     w1, w2 = W.make_weights(w)
     idx, probs = W.make_routing(w)
     dout = W.make_dout(w)
-    lay = L.ExpertLayer(w, DEV, keep_bf16=True)
+    kw = {} if image_min_k is None else {"nv_image_min_k": image_min_k}
+    lay = L.ExpertLayer(w, DEV, keep_bf16=True, **kw)
     assert lay.train and lay.nv and lay.align == 256 and lay.fused_swiglu
+    assert (lay.xcimg is not None) == (image_min_k == 0)
     lay.quantize_weights(w1.to(DEV), w2.to(DEV))
     lay.forward(x.to(DEV), torch.from_numpy(idx).to(DEV), torch.from_numpy(probs).to(DEV))
     lay.backward(dout.to(DEV), torch.from_numpy(probs).to(DEV))

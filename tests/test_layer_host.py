@@ -73,6 +73,24 @@ def test_unfused_mx_training_has_the_separate_swiglu_pass():
     assert lay.gpu_launches_per_step() == 18
 
 
+@pytest.mark.parametrize("name", ["mixtral_fwdbwd_nvfp4", "finegrained_fwd"])
+def test_nvfp4_scale_images_follow_their_quantisers(name):
+    """NVFP4 GEMMs whose contraction reaches the threshold read the scale image
+    of their second operand; its op follows the quantiser that writes the
+    scales: the weights (training: also their column-wise copies), the column
+    copy of x after the permute and that of h after the gate/up GEMM. (The
+    scaled-down shapes above stay below the default threshold.)"""
+    recipe, train, rest, launches = CASES[name]
+    lay, names = _layer_and_ops(name, nv_image_min_k=0)
+    n_img = 6 if train else 2
+    head = ["weight_quant", "weight_quant"] + ["scale_image"] * (4 if train else 2) + ["route", "permute_quant"]
+    if train:
+        head += ["scale_image"]
+        rest = rest[:1] + ["scale_image"] + rest[1:]
+    assert names == head + rest
+    assert lay.gpu_launches_per_step() == launches + n_img
+
+
 def test_nvfp4_training_pads_groups_to_256_rows():
     lay, _ = _layer_and_ops("mixtral_fwdbwd_nvfp4")
     assert lay.align == L.ALIGN_NV_TRAIN == 256 and lay.R_cap % 256 == 0
