@@ -99,6 +99,11 @@ def test_host_validation_rejects_bad_arguments(lib):
                                1 << 20, None) == mgq.ERR_INVALID_ARG
     assert lib.mgq_amax_history_update(None, None, None, None, 1, 1, ctypes.c_float(448.0), None) == INV
     assert lib.mgq_get_error(None, None) == INV
+    # NVFP4 scale image: rows a multiple of 128, ld of 256, aligned pointers
+    assert lib.mgq_nv_scale_image(16, 100, 256, 16, None) == INV
+    assert lib.mgq_nv_scale_image(16, 128, 200, 16, None) == INV
+    assert lib.mgq_nv_scale_image(16, 128, 256, 8, None) == INV
+    assert lib.mgq_nv_scale_image(None, 128, 256, 16, None) == INV
 
 
 def test_operand_layout_validation(lib):
@@ -134,14 +139,15 @@ def test_struct_layouts_match_the_header(tmp_path):
         "#include <stdio.h>\n#include <stddef.h>\n#include \"mgq.h\"\n"
         "int main(void){printf(\"%zu %zu %zu %zu %zu %zu %zu\\n\", sizeof(mgq_operand),"
         " offsetof(mgq_operand, ld), offsetof(mgq_operand, dtype), offsetof(mgq_operand, global_scale),"
-        " offsetof(mgq_operand, layout), sizeof(mgq_qdesc), offsetof(mgq_qdesc, amax_out));return 0;}\n")
+        " offsetof(mgq_operand, layout), sizeof(mgq_qdesc), offsetof(mgq_qdesc, amax_out));"
+        "printf(\"%zu\\n\", offsetof(mgq_operand, scale_image));return 0;}\n")
     exe = tmp_path / "probe"
     subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
     got = [int(v) for v in subprocess.run([str(exe)], check=True, capture_output=True,
                                           text=True).stdout.split()]
     O, Q = mgq.Operand, mgq.QDesc
     assert got == [ctypes.sizeof(O), O.ld.offset, O.dtype.offset, O.global_scale.offset, O.layout.offset,
-                   ctypes.sizeof(Q), Q.amax_out.offset]
+                   ctypes.sizeof(Q), Q.amax_out.offset, O.scale_image.offset]
 
 
 def test_gemm_options_round_trip_and_validation(lib):
