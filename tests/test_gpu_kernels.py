@@ -842,6 +842,51 @@ def test_dswiglu_quantize(mgq, mode):
         assert np.array_equal(untile_mx_scales(u8_np(csc), 2 * F, R), cs)
 
 
+@pytest.mark.parametrize("mode", ["tensor", "mx_col"])
+def test_dswiglu_quantize_partial_tile(mgq, mode):
+    """Rows in use end inside a 128-row tile (320 of R_cap = 512) and the
+    buffers hold NaN past them: the row-wise codes and dG | dU cover the rows
+    in use, and the column-wise copy treats the rest of the last tile as zeros
+    (zero codes and scales), as the oracle's blocks of the zero-filled tile."""
+    rng = np.random.default_rng(9)
+    dev = torch.device(DEV)
+    F, R, n = 768, 512, 320
+    off = np.array([0, 256, n], dtype=np.int32)
+    gu = _bf16(rng, (R, 2 * F), 2.0)
+    dh = _bf16(rng, (R, F), 1e-3)
+    gu[n:] = float("nan")
+    dh[n:] = float("nan")
+    codes = torch.full((R, 2 * F), 0xAB, dtype=torch.uint8, device=dev)
+    col = torch.full((2 * F, R), 0xAB, dtype=torch.uint8, device=dev)
+    dgu = torch.zeros(R, 2 * F, dtype=torch.bfloat16, device=dev)
+    amax = torch.zeros(1, device=dev)
+    if mode == "tensor":
+        q = mgq.qdesc(mgq.E5M2, mgq.TENSOR_F32, codes, None, col, None, torch.tensor([20000.0], device=dev), amax)
+    else:
+        sc = torch.full((mgq.mx_scale_bytes(R, 2 * F),), 0xAB, dtype=torch.uint8, device=dev)
+        csc = torch.full((mgq.mx_scale_bytes(2 * F, R),), 0xAB, dtype=torch.uint8, device=dev)
+        q = mgq.qdesc(mgq.E5M2, mgq.MX32_E8M0, codes, sc, col, csc)
+    mgq.dswiglu_quantize(dh.to(dev), gu.to(dev), R, F, torch.from_numpy(off).to(dev), 2, q, dgu)
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    g = bf16_np(dgu)[:n]
+    check_elementwise(OL.dswiglu(bf16_np(dh)[:n], bf16_np(gu)[:n], F), g, "dswiglu")
+    gz = np.zeros((384, 2 * F), dtype=g.dtype)          # the three tiles in use, zero past n
+    gz[:n] = g
+    if mode == "tensor":
+        c, am = OQ.quantize_tensor(gz, np.float32(20000.0), "e5m2")
+        assert np.array_equal(u8_np(codes)[:n], c[:n])
+        assert np.array_equal(u8_np(col)[:, :384], c.T)
+        assert float(amax.item()) == am
+    else:
+        c, s_ = OQ.quantize_mx(gz, "e5m2")
+        assert np.array_equal(u8_np(codes)[:n], c[:n])
+        assert np.array_equal(untile_mx_scales(u8_np(sc), R, 2 * F)[:n], s_[:n])
+        cc, cs = OQ.quantize_mx(gz.T, "e5m2")
+        assert np.array_equal(u8_np(col)[:, :384], cc)
+        assert np.array_equal(untile_mx_scales(u8_np(csc), 2 * F, R)[:, :384 // 32], cs)
+
+
 @pytest.mark.parametrize("T,E,k,H", [(1000, 8, 2, 512), (333, 16, 8, 256), (64, 4, 1, 5120)])
 def test_unpermute_and_permute_bwd(mgq, T, E, k, H):
     rng = np.random.default_rng(T)
