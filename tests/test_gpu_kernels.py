@@ -860,8 +860,9 @@ def test_dswiglu_quantize_partial_tile(mgq, mode):
     col = torch.full((2 * F, R), 0xAB, dtype=torch.uint8, device=dev)
     dgu = torch.zeros(R, 2 * F, dtype=torch.bfloat16, device=dev)
     amax = torch.zeros(1, device=dev)
+    s = torch.tensor([20000.0], device=dev)              # (kept alive: the descriptor holds its address)
     if mode == "tensor":
-        q = mgq.qdesc(mgq.E5M2, mgq.TENSOR_F32, codes, None, col, None, torch.tensor([20000.0], device=dev), amax)
+        q = mgq.qdesc(mgq.E5M2, mgq.TENSOR_F32, codes, None, col, None, s, amax)
     else:
         sc = torch.full((mgq.mx_scale_bytes(R, 2 * F),), 0xAB, dtype=torch.uint8, device=dev)
         csc = torch.full((mgq.mx_scale_bytes(2 * F, R),), 0xAB, dtype=torch.uint8, device=dev)
