@@ -1569,12 +1569,15 @@ def test_empty_batch_through_every_call(mgq):
     # GEMMs over all-empty groups
     w = torch.zeros(E * N, H, dtype=torch.uint8, device=dev)
     A = mgq.operand(codes, s, H, mgq.E4M3)
-    W = mgq.operand(w, torch.ones(E, device=dev), H, mgq.E4M3)
+    sw = torch.ones(E, device=dev)              # (tensors kept alive: operands hold addresses)
+    W = mgq.operand(w, sw, H, mgq.E4M3)
     Y = torch.full((R_cap, N), 3.0, dtype=torch.bfloat16, device=dev)
     mgq.grouped_gemm_fwd(A, W, mgq.TENSOR_F32, off, E, R_cap, N, H, Y)
     dW = torch.full((E, N, H), 5.0, dtype=torch.float32, device=dev)
-    dYc = mgq.operand(torch.zeros(N, R_cap, dtype=torch.uint8, device=dev), s, R_cap, mgq.E5M2)
-    Ac = mgq.operand(torch.zeros(H, R_cap, dtype=torch.uint8, device=dev), s, R_cap, mgq.E4M3)
+    dyc_codes = torch.zeros(N, R_cap, dtype=torch.uint8, device=dev)
+    ac_codes = torch.zeros(H, R_cap, dtype=torch.uint8, device=dev)
+    dYc = mgq.operand(dyc_codes, s, R_cap, mgq.E5M2)
+    Ac = mgq.operand(ac_codes, s, R_cap, mgq.E4M3)
     mgq.grouped_gemm_wgrad(dYc, Ac, mgq.TENSOR_F32, off, E, R_cap, N, H, dW, 0.0)
     dW1 = torch.full((E, N, H), 5.0, dtype=torch.float32, device=dev)
     mgq.grouped_gemm_wgrad(dYc, Ac, mgq.TENSOR_F32, off, E, R_cap, N, H, dW1, 1.0)
