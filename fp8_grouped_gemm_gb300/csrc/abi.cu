@@ -108,7 +108,7 @@ const char* mgq_status_string(int s) {
   }
 }
 
-int mgq_version(void) { return 1; }
+int mgq_version(void) { return MGQ_VERSION; }
 
 int mgq_get_error(void* stream, int* device_status) {
   if (!device_status) return MGQ_ERR_INVALID_ARG;

@@ -30,6 +30,8 @@ LAYOUT_K, LAYOUT_MN = 0, 1
 FMAX = {E4M3: 448.0, E5M2: 57344.0}
 
 # every symbol include/mgq.h declares
+INTERFACE_VERSION = 2   # mgq_version() of the library these struct mirrors match
+
 EXPORTS = (
     "mgq_status_string", "mgq_version", "mgq_get_error", "mgq_permute_workspace_size",
     "mgq_moe_permute", "mgq_moe_route", "mgq_moe_permute_routed", "mgq_moe_permute_noalloc", "mgq_block_quantize", "mgq_grouped_quantize", "mgq_grouped_gemm_fwd", "mgq_grouped_gemm_dgrad",
@@ -106,6 +108,8 @@ def load() -> ctypes.CDLL:
         for name in EXPORTS:
             if name not in ("mgq_status_string", "mgq_permute_workspace_size"):
                 getattr(lib, name).restype = i32
+        if lib.mgq_version() != INTERFACE_VERSION:   # the struct layouts below are this version's
+            raise RuntimeError(f"{LIB_PATH}: interface version {lib.mgq_version()}, expected {INTERFACE_VERSION}")
         _lib = lib
     return _lib
 

@@ -150,6 +150,9 @@ typedef struct {
 /* ---- status --------------------------------------------------------------- */
 
 const char* mgq_status_string(int status);
+/* The interface version: 2 since mgq_operand gained scale_image (callers
+ * built against version 1 pass the shorter struct and must be rebuilt). */
+#define MGQ_VERSION 2
 int mgq_version(void);
 
 /* Reads and clears the device error word of the current device after

@@ -39,7 +39,7 @@ def test_status_strings(lib):
     from fp8_grouped_gemm_gb300 import mgq
     assert mgq.status_string(mgq.OK) == "ok"
     assert "invalid" in mgq.status_string(mgq.ERR_INVALID_ARG)
-    assert lib.mgq_version() >= 1
+    assert lib.mgq_version() == 2          # the operand struct with scale_image
 
 
 def test_workspace_size(lib):
