@@ -22,11 +22,14 @@
 // 128x128 tiles (one scale per tile) get both copies from one pass, the
 // column-wise copy the transposed codes with the transposed tile scales
 // ([G][M/128][C/128] and [G][C/128][M/128]).
-// Kernels: quant_rowcol_kernel (one tile per CTA: plain and computed sources),
-// quant_rowcol_stream_kernel (gathered rows: a CTA walks a range of tiles and
-// stages the next with cp.async; the FP8 column codes of dY = probs * dout go
-// out through a staged tile and one TMA store per item), quant_nv2d_kernel
-// (NVFP4 weights with 16x16 blocks: both copies share the block scales).
+// Kernels: quant_rowcol_kernel (one tile per CTA: plain sources, SwiGLU, and
+// dSwiGLU with blockwise 128x1 blocks), quant_rowcol_pipe_kernel (dSwiGLU with
+// MX or per-tensor scaling: a persistent CTA whose operands arrive by TMA in
+// half tiles while it quantises the previous tile), quant_rowcol_stream_kernel
+// (gathered rows: a CTA walks a range of tiles and stages the next with
+// cp.async; the FP8 column codes of dY = probs * dout go out through a staged
+// tile and one TMA store per item), quant_nv2d_kernel (NVFP4 weights with 16x16
+// blocks: both copies share the block scales). Tiles are XOR-swizzled (tix).
 #include "mgq_internal.h"
 #include "ptx_sm100.cuh"
 #include "rowquant.cuh"
