@@ -329,6 +329,67 @@ def test_gemm_dgrad_and_wgrad(mgq, scaling):
     assert rel_fro(ref_w + prev.cpu().numpy(), got2) <= GEMM_TOL_F32
 
 
+@pytest.mark.parametrize("scaling", ["tensor", "mx"])
+def test_gemm_largest_expert_count(mgq, scaling):
+    """The largest expert count the library takes (1024 groups), most of them
+    empty and the rest one or two 128-row tiles: forward over the groups'
+    rows (rows past them untouched) and wgrad (empty groups written as
+    zeros), against the oracle."""
+    rng = np.random.default_rng(1024 + (scaling == "mx"))
+    dev = torch.device(DEV)
+    E, N, K = 1024, 256, 256
+    sizes = rng.choice([0, 128, 256], size=E, p=[0.7, 0.25, 0.05])
+    offs = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    Rp = int(offs[-1])
+    R_cap = Rp + 256
+    offd = torch.from_numpy(offs).to(dev)
+    if scaling == "tensor":
+        f4 = OF.E4M3
+        ac = (rng.choice(f4.pos_codes[:-1], size=(R_cap, K)) | (rng.integers(0, 2, (R_cap, K)) * 0x80)).astype(np.uint8)
+        wc = (rng.choice(f4.pos_codes[:-1], size=(E * N, K)) | (rng.integers(0, 2, (E * N, K)) * 0x80)).astype(np.uint8)
+        dyt = (rng.choice(f4.pos_codes[:-1], size=(N, Rp)) | (rng.integers(0, 2, (N, Rp)) * 0x80)).astype(np.uint8)
+        s_a = np.array([2.5], dtype=np.float32)
+        s_w = rng.uniform(0.25, 8.0, size=E).astype(np.float32)
+        s_dy = np.array([300.0], dtype=np.float32)
+        A = _op(mgq, ac, s_a, K, mgq.E4M3, dev)
+        Wo = _op(mgq, wc, s_w, K, mgq.E4M3, dev)
+        wg_A = _op(mgq, dyt, s_dy, Rp, mgq.E4M3, dev)
+        wg_B = _op(mgq, np.ascontiguousarray(ac[:Rp].T), s_a, Rp, mgq.E4M3, dev)
+        a_deq = OQ.dequantize_tensor(ac[:Rp], s_a[0])
+        w_deq = np.stack([OQ.dequantize_tensor(wc[e * N:(e + 1) * N], s_w[e]) for e in range(E)])
+        dy_deq = OQ.dequantize_tensor(dyt, s_dy[0]).T
+        wa_deq = a_deq
+        sc = mgq.TENSOR_F32
+    else:
+        ac, asc = _mx_operand(rng, R_cap, K)
+        wc, wsc = _mx_operand(rng, E * N, K)
+        dyt, dyts = _mx_operand(rng, N, Rp)
+        at, ats = _mx_operand(rng, K, Rp)
+        A = _op(mgq, ac, tile_mx_scales(asc), K, mgq.E4M3, dev)
+        Wo = _op(mgq, wc, tile_mx_scales(wsc), K, mgq.E4M3, dev)
+        wg_A = _op(mgq, dyt, tile_mx_scales(dyts), Rp, mgq.E4M3, dev)
+        wg_B = _op(mgq, at, tile_mx_scales(ats), Rp, mgq.E4M3, dev)
+        a_deq = OQ.dequantize_mx(ac, asc)[:Rp]
+        w_deq = OQ.dequantize_mx(wc, wsc).reshape(E, N, K)
+        dy_deq = OQ.dequantize_mx(dyt, dyts).T
+        wa_deq = OQ.dequantize_mx(at, ats).T
+        sc = mgq.MX32_E8M0
+    Y = torch.full((R_cap, N), float("nan"), dtype=torch.bfloat16, device=dev)
+    mgq.grouped_gemm_fwd(A, Wo, sc, offd, E, R_cap, N, K, Y)
+    dW = torch.full((E, N, K), 5.0, dtype=torch.float32, device=dev)
+    mgq.grouped_gemm_wgrad(wg_A, wg_B, sc, offd, E, Rp, N, K, dW, 0.0)
+    torch.cuda.synchronize()
+    assert mgq.get_error() == mgq.OK
+    got = bf16_np(Y)
+    assert np.all(np.isnan(got[Rp:]))
+    ref = OG.grouped_gemm_fwd(a_deq, w_deq, offs)
+    assert rel_fro(OF.round_to_bf16(ref), got[:Rp]) <= GEMM_TOL_BF16
+    got_w = dW.cpu().numpy().astype(np.float64)
+    assert np.all(got_w[sizes == 0] == 0.0)
+    ref_w = OG.grouped_gemm_wgrad(dy_deq, wa_deq, offs, E)
+    assert rel_fro(ref_w, got_w) <= GEMM_TOL_F32
+
+
 @pytest.mark.parametrize("exact", [True, False], ids=["exact", "random"])
 def test_gemm_mn_major_operands(mgq, exact):
     """Per-tensor dgrad and wgrad reading the row-wise codes transposed
