@@ -459,14 +459,20 @@ def test_gemm_mn_major_operands(mgq, exact):
         assert rel_fro(dW_k.cpu().numpy(), got_w) <= 1e-4
 
 
-@pytest.mark.parametrize("offs", [[0, 128, 128, 512], [0, 384]], ids=["E3", "E1"])
+def _many_groups(seed, E=1024):
+    """Offsets of E groups, most of them empty, the rest one or two 128-row tiles."""
+    sizes = np.random.default_rng(seed).choice([0, 128, 256], size=E, p=[0.7, 0.25, 0.05])
+    return [0] + np.cumsum(sizes).tolist()
+
+
+@pytest.mark.parametrize("offs", [[0, 128, 128, 512], [0, 384], _many_groups(41)], ids=["E3", "E1", "E1024"])
 def test_gemm_fwd_blockwise(mgq, offs):
     """1x128 activation x 128x128 weight float32 block scales (promotion of
     every 128-deep partial product)."""
     rng = np.random.default_rng(41)
     dev = torch.device(DEV)
     E = len(offs) - 1
-    N, K = 512, 640
+    N, K = (512, 640) if E < 1024 else (256, 256)
     Rp = offs[-1]
     R_cap = Rp + 128
     f = OF.E4M3
@@ -489,14 +495,14 @@ def test_gemm_fwd_blockwise(mgq, offs):
     assert rel_fro(OF.round_to_bf16(ref), got[:Rp]) <= GEMM_TOL_BF16
 
 
-@pytest.mark.parametrize("offs", [[0, 128, 128, 512], [0, 256]], ids=["E3", "E1"])
+@pytest.mark.parametrize("offs", [[0, 128, 128, 512], [0, 256], _many_groups(51)], ids=["E3", "E1", "E1024"])
 def test_gemm_fwd_nvfp4(mgq, offs):
     """e2m1 x e2m1 with 16-element ue4m3 block scales (kind::mxf4nvf4,
     scale_vec::4X) and a float32 global scale per tensor / per expert."""
     rng = np.random.default_rng(51)
     dev = torch.device(DEV)
     E = len(offs) - 1
-    N, K = 512, 768
+    N, K = (512, 768) if E < 1024 else (256, 256)
     Rp = offs[-1]
     R_cap = Rp + 128
     qa = rng.integers(0, 16, size=(R_cap, K)).astype(np.uint8)
@@ -517,8 +523,10 @@ def test_gemm_fwd_nvfp4(mgq, offs):
     torch.cuda.synchronize()
     assert mgq.get_error() == mgq.OK
     a_deq = OQ.dequantize_nvfp4(pack(qa)[:Rp], sca[:Rp], sga[0], K)
-    w_deq = np.stack([OQ.dequantize_nvfp4(pack(qw)[e * N:(e + 1) * N], scw[e * N:(e + 1) * N], sgw[e], K)
-                      for e in range(E)])
+    # all experts in one call with s_g = 1, then each expert's 1 / s_g (the same
+    # float64 values as one call per expert: v * sc / 1 is exact)
+    w_deq = (OQ.dequantize_nvfp4(pack(qw), scw, 1.0, K).reshape(E, N, K)
+             / sgw.astype(np.float64)[:, None, None])
     ref = OG.grouped_gemm_fwd(a_deq, w_deq, np.array(offs))
     got = bf16_np(Y)
     assert np.all(np.isnan(got[Rp:]))
