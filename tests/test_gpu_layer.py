@@ -43,6 +43,17 @@ def test_scout_forward_blockwise_scaled_down():
     assert res["gemm1_sqnr_vs_bf16"] >= 28.0, res
 
 
+@pytest.mark.parametrize("recipe", ["mxfp8", "nvfp4"])
+def test_skewed_routing_forward_scaled_down(recipe):
+    """The degenerate load: top-1 Zipf(3) routing over two of eight experts
+    (about 89% of the tokens in one group, six groups empty), checked in full."""
+    from fp8_grouped_gemm_gb300.workloads import WORKLOADS
+    w = WORKLOADS["mixtral_fwd"].scaled(T=1500, H=512, F=768, k=1, routing="zipf", zipf_s=3.0, n_empty=6,
+                                        recipe=recipe)
+    res = run_fwd_and_check(w, DEV, recipe=recipe)
+    assert res["gemm1_sqnr_vs_bf16"] >= (28.0 if recipe == "mxfp8" else 15.0), res
+
+
 @pytest.mark.parametrize("image_min_k", [None, 0], ids=["scales", "scale_image"])
 def test_finegrained_forward_nvfp4_scaled_down(image_min_k):
     """Fine-grained MoE proportions (uniform top-8 routing) in NVFP4 (e2m1,
