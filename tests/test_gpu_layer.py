@@ -71,16 +71,21 @@ def _tensor_deq(codes, s, fmt="e4m3"):
     return OQ.dequantize_tensor(codes, np.float32(s), fmt)
 
 
-@pytest.mark.parametrize("col_copies", [False, True], ids=["mn_major", "col_copies"])
-def test_delayed_training_steps(col_copies):
+@pytest.mark.parametrize("col_copies,skewed", [(False, False), (True, False), (False, True)],
+                         ids=["mn_major", "col_copies", "skewed"])
+def test_delayed_training_steps(col_copies, skewed):
     """Three delayed-scaling training steps: every code bit-exact, GEMMs within
     tolerance, amaxes and next scales exact. By default the backward GEMMs read
     the row-wise codes MN-major; col_copies=True writes and uses the explicit
-    column-wise copies (which must be the transposed row-wise codes)."""
+    column-wise copies (which must be the transposed row-wise codes). skewed:
+    top-1 Zipf(3) routing over two of the four experts (two groups empty, one
+    holding most of the tokens)."""
     from fp8_grouped_gemm_gb300 import layer as L
     from fp8_grouped_gemm_gb300 import mgq
     from fp8_grouped_gemm_gb300 import workloads as W
     w = W.WORKLOADS["mixtral_fwdbwd"].scaled(T=700, H=512, F=768, E=4)
+    if skewed:
+        w = w.scaled(k=1, routing="zipf", zipf_s=3.0, n_empty=2)
     E, k, T, H, F = w.E, w.k, w.T, w.H, w.F
     x = W.make_activations(w)
     w1, w2 = W.make_weights(w)
