@@ -41,9 +41,9 @@ ALIGN_NV_TRAIN = 256   # NVFP4 wgrad: a 128-byte stage holds 256 rows of a group
 # NVFP4 GEMMs read the scale image of their second operand
 # (mgq_nv_scale_image) when the contraction is at least this long: measured on
 # the Mixtral shapes (contractions of 4096 and more) every GEMM gained 4-9%,
-# more than the image costs; the fine-grained forward's short contractions
-# (768, 2048) gained less than the images cost
-NV_IMAGE_MIN_K = 4096
+# more than the image costs; in the fine-grained forward the gate/up GEMM
+# (contraction 2048) gains 6%, the down GEMM (768) less than its image costs
+NV_IMAGE_MIN_K = 2048
 
 
 class ExpertLayer:

@@ -54,7 +54,7 @@ def test_skewed_routing_forward_scaled_down(recipe):
     assert res["gemm1_sqnr_vs_bf16"] >= (28.0 if recipe == "mxfp8" else 15.0), res
 
 
-@pytest.mark.parametrize("image_min_k", [None, 0], ids=["scales", "scale_image"])
+@pytest.mark.parametrize("image_min_k", [1 << 30, 0], ids=["scales", "scale_image"])
 def test_finegrained_forward_nvfp4_scaled_down(image_min_k):
     """Fine-grained MoE proportions (uniform top-8 routing) in NVFP4 (e2m1,
     16-element ue4m3 scales, float32 global scales) at a size checked in full;
@@ -62,7 +62,7 @@ def test_finegrained_forward_nvfp4_scaled_down(image_min_k):
     are and through their GEMM scale images."""
     from fp8_grouped_gemm_gb300.workloads import WORKLOADS
     w = WORKLOADS["finegrained_fwd"].scaled(T=1024, E=32, H=512, F=768)
-    kw = {} if image_min_k is None else {"nv_image_min_k": image_min_k}
+    kw = {"nv_image_min_k": image_min_k}
     res = run_fwd_and_check(w, DEV, recipe="nvfp4", **kw)
     assert res["gemm1_sqnr_vs_bf16"] >= 15.0, res
 
@@ -263,7 +263,7 @@ def test_mxfp8_training_step_scaled_down():
     assert OG.sqnr_db(OG.grouped_gemm_fwd(xp, w1f, off), gu) >= 28.0
 
 
-@pytest.mark.parametrize("image_min_k", [None, 0], ids=["scales", "scale_image"])
+@pytest.mark.parametrize("image_min_k", [1 << 30, 0], ids=["scales", "scale_image"])
 def test_nvfp4_training_step_scaled_down(image_min_k):
     """NVFP4 in both passes: activations and gradients e2m1 with 16-element
     ue4m3 scales and one s_g per tensor (row-wise for fwd/dgrad, 16x1 blocks
@@ -280,7 +280,7 @@ def test_nvfp4_training_step_scaled_down(image_min_k):
     w1, w2 = W.make_weights(w)
     idx, probs = W.make_routing(w)
     dout = W.make_dout(w)
-    kw = {} if image_min_k is None else {"nv_image_min_k": image_min_k}
+    kw = {"nv_image_min_k": image_min_k}
     lay = L.ExpertLayer(w, DEV, keep_bf16=True, **kw)
     assert lay.train and lay.nv and lay.align == 256 and lay.fused_swiglu
     assert (lay.xcimg is not None) == (image_min_k == 0)
